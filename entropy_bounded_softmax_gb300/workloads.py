@@ -1,0 +1,157 @@
+"""Seeded synthetic inputs for the constrained-softmax workloads.
+
+This module only draws random numbers; it holds none of the method's
+arithmetic.  Both the CUDA path's tests/benchmark and the CPU oracle take
+their inputs from here, so the two always see the same logits.
+
+Recipe (numpy ``Generator(PCG64)``): rows are drawn in blocks of
+``BLOCK_ROWS``; block ``k`` of a workload with seed ``s`` uses
+``Generator(PCG64([s, k]))``, so any subset of rows can be regenerated
+without drawing the whole matrix.  Within a block the draws are, in order:
+the block's normals (``standard_normal`` in fp32, times sigma), then the
+workload-specific extras described on each workload.
+
+The workloads are the shapes the page quotes or the ones a user of the op
+meets: a small case, the page's latency case (batch 32 x 50000 classes,
+"BURT-IMMA CUDA Kernel API Reference", section 2.1 Performance Notes and
+section 7.1), a mixture-of-experts router (64 experts; the Parameters table
+names "number of experts" as a use of num_classes), rows too long for one
+CTA's shared memory, and a throughput sweep over the bound and the iteration
+count.  The page measures on no dataset; every input is synthetic.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field, replace
+
+import numpy as np
+
+BLOCK_ROWS = 64
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    batch: int
+    num_classes: int
+    kind: str                 # "normal" | "router" | "long_mixed"
+    sigma: float = 1.0
+    seed: int = 1000
+    entropy_bound: float = 0.20
+    t_min: float = 0.01
+    t_max: float = 10.0
+    max_iter: int = 20
+    note: str = ""
+    extra: dict = field(default_factory=dict)
+
+    def with_(self, **kw) -> "Workload":
+        return replace(self, **kw)
+
+    @property
+    def elements(self) -> int:
+        return self.batch * self.num_classes
+
+
+# The five workloads (sizes and distributions as stated on each line).
+SMALL = Workload("small_4x1000", 4, 1000, "normal", 1.0, 1001,
+                 note="batch 4, 1000 classes, N(0,1)")
+LATENCY = Workload("latency_32x50000", 32, 50000, "normal", 2.0, 1002,
+                   note="batch 32, 50000 classes, N(0,2^2); one CTA per row")
+ROUTER = Workload("moe_router_65536x64", 65536, 64, "router", 1.0, 1003,
+                  note="65536 tokens, 64 experts, N(0,1) plus one expert per "
+                       "row boosted by U(0,3)")
+LONG = Workload("long_rows_256x131072", 256, 131072, "long_mixed", 1.0, 1004,
+                note="256 rows of 131072 classes: 13 constant rows, the rest "
+                     "alternate N(0,1) and N(0,1) with one index +15",
+                extra={"constant_frac": 0.05, "spike": 15.0})
+SWEEP = Workload("sweep_4096x32000", 4096, 32000, "normal", 3.0, 1005,
+                 note="batch 4096, 32000 classes, N(0,3^2); bound in "
+                      "{0.05,0.2,1.0} x max_iter in {20,40}")
+
+WORKLOADS = {w.name: w for w in (SMALL, LATENCY, ROUTER, LONG, SWEEP)}
+SWEEP_POINTS = [(b, it) for b in (0.05, 0.20, 1.0) for it in (20, 40)]
+
+
+def sweep_workloads() -> list[Workload]:
+    return [SWEEP.with_(name=f"{SWEEP.name}_b{b}_it{it}", entropy_bound=b,
+                        max_iter=it) for b, it in SWEEP_POINTS]
+
+
+def _block_rng(seed: int, block: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64([seed, block]))
+
+
+def _constant_rows(w: Workload) -> np.ndarray:
+    """Indices of the constant rows of a long_mixed workload (seeded)."""
+    n_const = int(round(w.extra.get("constant_frac", 0.05) * w.batch))
+    rng = np.random.Generator(np.random.PCG64([w.seed, 1 << 30]))
+    return np.sort(rng.choice(w.batch, size=n_const, replace=False))
+
+
+def row_kinds(w: Workload) -> np.ndarray:
+    """Per-row label for long_mixed: 0 normal, 1 spiked, 2 constant."""
+    kinds = np.zeros(w.batch, dtype=np.int8)
+    if w.kind != "long_mixed":
+        return kinds
+    const = np.zeros(w.batch, dtype=bool)
+    const[_constant_rows(w)] = True
+    rest = np.flatnonzero(~const)
+    kinds[rest[1::2]] = 1
+    kinds[const] = 2
+    return kinds
+
+
+def _gen_block(w: Workload, block: int, kinds: np.ndarray) -> np.ndarray:
+    r0 = block * BLOCK_ROWS
+    r1 = min(w.batch, r0 + BLOCK_ROWS)
+    n = r1 - r0
+    C = w.num_classes
+    rng = _block_rng(w.seed, block)
+    x = rng.standard_normal((n, C), dtype=np.float32)
+    x *= np.float32(w.sigma)
+    if w.kind == "router":
+        idx = rng.integers(0, C, size=n)
+        boost = rng.uniform(0.0, 3.0, size=n).astype(np.float32)
+        x[np.arange(n), idx] += boost
+    elif w.kind == "long_mixed":
+        idx = rng.integers(0, C, size=n)
+        const_val = rng.standard_normal(n, dtype=np.float32)
+        spike = np.float32(w.extra.get("spike", 15.0))
+        k = kinds[r0:r1]
+        for j in range(n):
+            if k[j] == 1:
+                x[j, idx[j]] += spike
+            elif k[j] == 2:
+                x[j, :] = const_val[j]
+    elif w.kind != "normal":
+        raise ValueError(f"unknown workload kind {w.kind!r}")
+    return x
+
+
+def generate(w: Workload, rows=None) -> np.ndarray:
+    """The workload's fp32 logits, or only ``rows`` (indices) of them."""
+    kinds = row_kinds(w)
+    if rows is None:
+        rows_arr = np.arange(w.batch)
+    else:
+        rows_arr = np.asarray(rows, dtype=np.int64).reshape(-1)
+        if rows_arr.size and (rows_arr.min() < 0 or rows_arr.max() >= w.batch):
+            raise IndexError("row index out of range")
+    out = np.empty((rows_arr.size, w.num_classes), dtype=np.float32)
+    if rows_arr.size == 0:
+        return out
+    blocks = np.unique(rows_arr // BLOCK_ROWS)
+    for blk in blocks:
+        xb = _gen_block(w, int(blk), kinds)
+        sel = np.flatnonzero(rows_arr // BLOCK_ROWS == blk)
+        out[sel] = xb[rows_arr[sel] - blk * BLOCK_ROWS]
+    return out
+
+
+def sample_rows(w: Workload, n: int, seed: int = 7) -> np.ndarray:
+    """A seeded, sorted sample of n distinct row indices (always includes
+    the first and last row)."""
+    n = min(n, w.batch)
+    rng = np.random.Generator(np.random.PCG64([w.seed, seed, 99]))
+    picks = set(rng.choice(w.batch, size=n, replace=False).tolist())
+    picks.update({0, w.batch - 1})
+    return np.array(sorted(picks), dtype=np.int64)

@@ -1,0 +1,184 @@
+/*
+ * Oracle for the entropy-bounded softmax ("constrained_softmax").
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the slow, plain, obviously correct
+ * CPU statement of what the method computes.  Only the test suite, the smoke
+ * check and the CPU-baseline leg of the benchmark load it.  The CUDA library
+ * shares no code, header, table or helper with it, and neither side calls the
+ * other.
+ *
+ * Source of the method: "BURT-IMMA CUDA Kernel API Reference", section 2.1
+ * `constrained_softmax` (Parameters table, Description steps 1-4, Performance
+ * Notes) and section 5 (5.1 Error Codes, 5.3 NaN/Inf Propagation Policy,
+ * 5.4 Graceful Degradation).
+ *
+ * Arithmetic: IEEE double throughout, libm exp() and log().  The fp32
+ * parameters are promoted exactly to double, so both sides of any comparison
+ * see the same bound (0.2f is 0.20000000298... here as on the GPU).
+ *
+ * Readings of the page where it is silent or loose (all stated again in the
+ * design notes):
+ *  - Description step 1 divides by T before any T exists: the first softmax
+ *    is the standard one, T = 1.
+ *  - The search (step 3) runs only when H(1) > entropy_bound.  Entropy is
+ *    nondecreasing in T (step 4 says lower T concentrates the distribution),
+ *    so temperatures above 1 can never help; the search interval is
+ *    [temperature_min, min(1, temperature_max)].
+ *  - Step 3 aims at "H = entropy_bound" while the section heading asks for
+ *    H(p) <= entropy_bound: the search keeps the feasible end `lo` (ties go
+ *    to lo) and the output is softmax(l / lo).
+ *  - "Number of binary search iterations": exactly max_iterations halvings,
+ *    no early exit.  When temperature_min >= min(1, temperature_max) there is
+ *    no interval to halve and T = temperature_min.
+ *  - 5.3: a NaN or an Inf anywhere in a row affects every p_i of that row, so
+ *    the whole row is zeroed, T is reported as NaN and the row's flag is
+ *    NAN_INPUT (1) or INF_INPUT (2); NaN wins when both occur.
+ *  - 5.4: an unsatisfiable bound returns the lowest achievable entropy, which
+ *    is softmax at T = temperature_min, with flag ENTROPY_OVERFLOW (3).
+ */
+#include <math.h>
+#include <stdint.h>
+
+/* Flag values: section 5.1, enum BurtError. */
+#define ORACLE_FLAG_NONE 0
+#define ORACLE_FLAG_NAN_INPUT 1
+#define ORACLE_FLAG_INF_INPUT 2
+#define ORACLE_FLAG_ENTROPY_OVERFLOW 3
+
+/* Largest logit of the row (the max-subtraction that keeps exp() finite;
+ * softmax is unchanged by subtracting a constant from every logit). */
+static double row_max(const float* l, int64_t C)
+{
+    double m = (double)l[0];
+    for (int64_t i = 1; i < C; ++i) {
+        if ((double)l[i] > m) m = (double)l[i];
+    }
+    return m;
+}
+
+/* p = softmax(l / T): Description step 1, p_i = exp(l_i/T) / sum_j exp(l_j/T). */
+static void softmax_at(const float* l, int64_t C, double T, double* p)
+{
+    double m = row_max(l, C);
+    double S = 0.0;
+    for (int64_t i = 0; i < C; ++i) {
+        S += exp(((double)l[i] - m) / T);
+    }
+    for (int64_t i = 0; i < C; ++i) {
+        p[i] = exp(((double)l[i] - m) / T) / S;
+    }
+}
+
+/* H(T) = -sum_i p_i ln p_i with p = softmax(l / T), in nats (Description
+ * step 2; the Parameters table gives the bound in nats).  A term with
+ * p_i = 0 contributes 0 (the limit of p ln p). */
+static double entropy_at(const float* l, int64_t C, double T)
+{
+    double m = row_max(l, C);
+    double S = 0.0;
+    for (int64_t i = 0; i < C; ++i) {
+        S += exp(((double)l[i] - m) / T);
+    }
+    double H = 0.0;
+    for (int64_t i = 0; i < C; ++i) {
+        double p = exp(((double)l[i] - m) / T) / S;
+        if (p > 0.0) H -= p * log(p);
+    }
+    return H;
+}
+
+/* Public: H(T) of one row, for pinning the oracle against closed forms. */
+double oracle_entropy(const float* l, int64_t C, double T)
+{
+    return entropy_at(l, C, T);
+}
+
+/* Public: softmax(l / T) of one row. */
+void oracle_softmax(const float* l, int64_t C, double T, double* p)
+{
+    softmax_at(l, C, T, p);
+}
+
+/*
+ * One row of constrained_softmax.  Writes C probabilities to p and returns
+ * the flag; *T_out gets the temperature used, *iters_out the number of
+ * bisection steps taken (each step evaluates H once).  If path_mid/path_H are
+ * non-NULL they receive the midpoint and H(midpoint) of every step.
+ */
+static int one_row(const float* l, int64_t C, double bound, double t_min,
+                   double t_max, int32_t max_iter, double* p, double* T_out,
+                   int32_t* iters_out, double* path_mid, double* path_H)
+{
+    int has_nan = 0, has_inf = 0;
+    for (int64_t i = 0; i < C; ++i) {
+        if (isnan(l[i])) has_nan = 1;
+        else if (isinf(l[i])) has_inf = 1;
+    }
+    *iters_out = 0;
+    if (has_nan || has_inf) {
+        for (int64_t i = 0; i < C; ++i) p[i] = 0.0;
+        *T_out = NAN;
+        return has_nan ? ORACLE_FLAG_NAN_INPUT : ORACLE_FLAG_INF_INPUT;
+    }
+
+    /* Steps 1-2: standard softmax and its entropy. */
+    if (entropy_at(l, C, 1.0) <= bound) {
+        softmax_at(l, C, 1.0, p);
+        *T_out = 1.0;
+        return ORACLE_FLAG_NONE;
+    }
+
+    /* Step 3: bisection on T over [t_min, min(1, t_max)]. */
+    double lo = t_min;
+    double hi = t_max < 1.0 ? t_max : 1.0;
+    if (lo < hi) {
+        for (int32_t k = 0; k < max_iter; ++k) {
+            double mid = (lo + hi) / 2.0;
+            double Hmid = entropy_at(l, C, mid);
+            if (path_mid) path_mid[k] = mid;
+            if (path_H) path_H[k] = Hmid;
+            if (Hmid > bound) {
+                hi = mid;
+            } else {
+                lo = mid;
+            }
+        }
+        *iters_out = max_iter;
+    }
+
+    softmax_at(l, C, lo, p);
+    *T_out = lo;
+    /* 5.4: only lo = t_min can still violate the bound. */
+    if (entropy_at(l, C, lo) > bound) return ORACLE_FLAG_ENTROPY_OVERFLOW;
+    return ORACLE_FLAG_NONE;
+}
+
+/*
+ * Rows [row_begin, row_end) of a row-major [batch, C] fp32 logit matrix.
+ * out is [batch, C] double; T_out, flags_out and iters_out are [batch].
+ * Rows are independent, so callers may split a batch over threads.
+ */
+void oracle_constrained_softmax_rows(const float* logits, double* out,
+                                     int64_t row_begin, int64_t row_end,
+                                     int64_t C, float entropy_bound,
+                                     float t_min, float t_max,
+                                     int32_t max_iter, double* T_out,
+                                     int32_t* flags_out, int32_t* iters_out)
+{
+    for (int64_t b = row_begin; b < row_end; ++b) {
+        flags_out[b] = one_row(logits + b * C, C, (double)entropy_bound,
+                               (double)t_min, (double)t_max, max_iter,
+                               out + b * C, &T_out[b], &iters_out[b], 0, 0);
+    }
+}
+
+/* One row with its bisection path recorded (max_iter entries each). */
+int32_t oracle_constrained_softmax_path(const float* l, double* p, int64_t C,
+                                        float entropy_bound, float t_min,
+                                        float t_max, int32_t max_iter,
+                                        double* T_out, int32_t* iters_out,
+                                        double* path_mid, double* path_H)
+{
+    return one_row(l, C, (double)entropy_bound, (double)t_min, (double)t_max,
+                   max_iter, p, T_out, iters_out, path_mid, path_H);
+}

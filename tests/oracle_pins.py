@@ -1,0 +1,367 @@
+"""Pins for the CPU oracle: facts fixed by the mathematics, not by the oracle.
+
+Each ``check_*`` function takes a loaded oracle library and raises
+AssertionError when the oracle disagrees with:
+  * closed forms of H(T) and of the optimal temperature for 2-class rows and
+    for "spike" rows (C-1 equal logits, one larger),
+  * a library softmax (scipy) in the case where no search is needed,
+  * a brute-force scan of a dense temperature grid on tiny rows, using
+    scipy's softmax and entropy routines,
+  * invariants (probabilities sum to 1, argmax kept, constant rows uniform,
+    shift invariance, H monotone along the search path, C = 1),
+  * the NaN/Inf and unsatisfiable-bound policy of "BURT-IMMA CUDA Kernel API
+    Reference", sections 5.1, 5.3 and 5.4.
+
+The same checks run against deliberately broken copies of the oracle in
+``test_oracle_mutants.py``: every plausible mistake must fail at least one.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import scipy.optimize
+import scipy.special
+import scipy.stats
+
+import oracle
+
+T_MIN, T_MAX, ITERS, BOUND = 0.01, 10.0, 20, 0.20
+
+
+# ---------------------------------------------------------------- closed forms
+def h_two_class(delta: float, T: float) -> float:
+    """Entropy (nats) of softmax([0, delta] / T): the binary entropy of
+    q = sigmoid(delta / T), written with log1p so that it stays accurate when
+    q is close to 1."""
+    z = abs(delta) / T
+    ez = math.exp(-z)
+    q = 1.0 / (1.0 + ez)
+    one_minus_q = ez / (1.0 + ez)
+    lp = math.log1p(ez)              # -ln q
+    return q * lp + one_minus_q * (z + lp)
+
+
+def h_spike(C: int, delta: float, T: float) -> float:
+    """Entropy of softmax(l / T) where C-1 logits are equal and one is larger
+    by delta > 0: p_top = 1 / (1 + (C-1) e^{-z}), every other p = e^{-z} p_top,
+    z = delta / T."""
+    z = delta / T
+    a = (C - 1) * math.exp(-z)
+    p_top = 1.0 / (1.0 + a)
+    r = math.exp(-z) / (1.0 + a)
+    lp = math.log1p(a)               # -ln p_top
+    return p_top * lp + (C - 1) * r * (z + lp)
+
+
+def t_star(h_of_T, bound: float, lo: float, hi: float) -> float | None:
+    """Temperature where the (increasing) closed-form H crosses the bound,
+    or None if it does not cross inside (lo, hi)."""
+    f = lambda T: h_of_T(T) - bound
+    if f(lo) > 0 or f(hi) <= 0:
+        return None
+    return scipy.optimize.brentq(f, lo, hi, xtol=1e-16, rtol=1e-15,
+                                 maxiter=500)
+
+
+def _f32(x) -> float:
+    return float(np.float32(x))
+
+
+# --------------------------------------------------------------------- checks
+def check_two_class_entropy(lib) -> None:
+    for delta in (0.125, 0.5, 1.5, 3.0, 7.25):
+        for T in (0.01, 0.05, 0.1, 0.37, 1.0, 2.0):
+            row = np.array([0.25, 0.25 + delta], dtype=np.float32)
+            d = float(row[1]) - float(row[0])
+            got = oracle.entropy(row, T, lib=lib)
+            want = h_two_class(d, T)
+            assert abs(got - want) <= 1e-13 + 1e-12 * want, (delta, T, got, want)
+
+
+def check_spike_entropy(lib) -> None:
+    for C in (3, 10, 1000):
+        for delta in (0.5, 2.0, 9.0):
+            for T in (0.02, 0.2, 1.0):
+                row = np.full(C, -1.5, dtype=np.float32)
+                row[C // 3] += np.float32(delta)
+                d = float(row[C // 3]) - float(row[0])
+                got = oracle.entropy(row, T, lib=lib)
+                want = h_spike(C, d, T)
+                assert abs(got - want) <= 1e-12 * max(1.0, want), \
+                    (C, delta, T, got, want)
+
+
+def check_large_logits(lib) -> None:
+    """Rows of large logits: exp() of them overflows unless the row maximum
+    is subtracted first, so this fixes that subtraction."""
+    row = np.array([1000.0, 1001.5], dtype=np.float32)
+    for T in (0.05, 1.0):
+        got = oracle.entropy(row, T, lib=lib)
+        assert math.isfinite(got)
+        assert abs(got - h_two_class(1.5, T)) < 1e-13
+    p = oracle.softmax(row, 1.0, lib=lib)
+    assert np.all(np.isfinite(p))
+    q = 1.0 / (1.0 + math.exp(-1.5))
+    assert abs(p[1] - q) < 1e-15 and abs(p[0] - (1 - q)) < 1e-15
+    # A gap of 40 at T = 0.05 puts exp(800) in reach of a wrong shift.
+    row = np.array([1000.0, 1040.0], dtype=np.float32)
+    for T in (0.05, 1.0):
+        got = oracle.entropy(row, T, lib=lib)
+        assert math.isfinite(got) and abs(got - h_two_class(40.0, T)) < 1e-13
+        p = oracle.softmax(row, T, lib=lib)
+        assert np.all(np.isfinite(p)) and abs(p.sum() - 1.0) < 1e-15
+
+
+def _check_T_against(res_T, Tstar, w, flag, row_desc):
+    # The search keeps lo feasible and hi infeasible, so lo lies in
+    # (T* - w, T*]; allow relative 1e-11 for fp64 rounding of H near T*.
+    slack = 1e-11 * Tstar
+    assert flag == 0, row_desc
+    assert Tstar - w - slack <= res_T <= Tstar + slack, \
+        (row_desc, res_T, Tstar, w)
+
+
+def check_two_class_temperature(lib) -> None:
+    for max_iter in (20, 40, 7):
+        w = oracle.final_interval(T_MIN, T_MAX, max_iter)
+        lo0, hi0 = oracle.search_interval(T_MIN, T_MAX)
+        for delta in (0.05, 0.1, 0.3, 0.9, 2.7):
+            row = np.array([0.0, delta], dtype=np.float32)
+            d = float(row[1])
+            Ts = t_star(lambda T: h_two_class(d, T), _f32(BOUND), lo0, hi0)
+            assert Ts is not None
+            r = oracle.constrained_softmax(row[None, :], BOUND, T_MIN, T_MAX,
+                                           max_iter, threads=1, lib=lib)
+            _check_T_against(r.T[0], Ts, w, r.flags[0], (delta, max_iter))
+            assert r.iters[0] == max_iter
+            q = 1.0 / (1.0 + math.exp(-d / r.T[0]))
+            assert abs(r.p[0, 1] - q) < 1e-14 and abs(r.p[0, 0] - (1 - q)) < 1e-14
+    # delta = 0.02: even T = t_min leaves H above 0.2 (z = 2 gives
+    # h_b(sigmoid(2)) = 0.36), so the bound is unsatisfiable.
+    row = np.array([[0.0, 0.02]], dtype=np.float32)
+    assert h_two_class(float(row[0, 1]), _f32(T_MIN)) > _f32(BOUND)
+    r = oracle.constrained_softmax(row, BOUND, T_MIN, T_MAX, ITERS, threads=1,
+                                   lib=lib)
+    assert r.flags[0] == oracle.FLAG_ENTROPY_OVERFLOW and r.T[0] == _f32(T_MIN)
+
+
+def check_spike_temperature(lib) -> None:
+    w = oracle.final_interval(T_MIN, T_MAX, ITERS)
+    lo0, hi0 = oracle.search_interval(T_MIN, T_MAX)
+    for C, delta, bound in ((5, 1.0, 0.2), (64, 3.0, 0.2), (1000, 4.0, 0.5),
+                            (50000, 6.0, 0.2), (7, 0.7, 1.0)):
+        row = np.zeros(C, dtype=np.float32)
+        row[C - 2] = delta
+        d = float(row[C - 2])
+        Ts = t_star(lambda T: h_spike(C, d, T), _f32(bound), lo0, hi0)
+        assert Ts is not None, (C, delta, bound)
+        r = oracle.constrained_softmax(row[None, :], bound, T_MIN, T_MAX,
+                                       ITERS, threads=1, lib=lib)
+        _check_T_against(r.T[0], Ts, w, r.flags[0], (C, delta, bound))
+
+
+def check_softmax_special_case(lib) -> None:
+    """A bound at or above H(1) needs no search: the output is the plain
+    softmax, which scipy computes independently."""
+    rng = np.random.default_rng(11)
+    for C in (1, 2, 17, 1000):
+        x = rng.normal(0.0, 2.0, size=(3, C)).astype(np.float32)
+        for bound in (math.log(C) + 0.5, 1e30):
+            r = oracle.constrained_softmax(x, bound, T_MIN, T_MAX, ITERS,
+                                           threads=1, lib=lib)
+            ref = scipy.special.softmax(x.astype(np.float64), axis=1)
+            assert np.all(r.T == 1.0) and np.all(r.flags == 0)
+            assert np.all(r.iters == 0)
+            assert np.max(np.abs(r.p - ref)) < 1e-15
+    # Bounds a hair above and below H(1) of a 2-class row: the first must
+    # give T = 1 exactly, the second must search (T < 1).
+    for delta in (1.0, 3.0, 5.0):
+        row = np.array([[0.0, delta]], dtype=np.float32)
+        H1 = h_two_class(delta, 1.0)
+        above = np.nextafter(np.float32(H1), np.float32(1.0))
+        below = np.nextafter(np.float32(H1), np.float32(0.0))
+        if float(above) < H1:
+            above = np.nextafter(above, np.float32(1.0))
+        if float(below) >= H1:
+            below = np.nextafter(below, np.float32(0.0))
+        r = oracle.constrained_softmax(row, float(above), T_MIN, T_MAX, ITERS,
+                                       threads=1, lib=lib)
+        assert r.T[0] == 1.0 and r.iters[0] == 0
+        r = oracle.constrained_softmax(row, float(below), T_MIN, T_MAX, ITERS,
+                                       threads=1, lib=lib)
+        assert r.T[0] < 1.0 and r.iters[0] == ITERS
+
+
+def _grid_largest_feasible(row: np.ndarray, bound: float, lo: float,
+                           hi: float, n: int):
+    T = np.linspace(lo, hi, n)
+    p = scipy.special.softmax(row.astype(np.float64)[None, :] / T[:, None],
+                              axis=1)
+    H = scipy.stats.entropy(p, axis=1)
+    ok = np.flatnonzero(H <= bound)
+    return (T[ok[-1]] if ok.size else None), T[1] - T[0]
+
+
+def check_brute_force(lib) -> None:
+    rng = np.random.default_rng(5)
+    lo0, hi0 = oracle.search_interval(T_MIN, T_MAX)
+    w = oracle.final_interval(T_MIN, T_MAX, ITERS)
+    n = 1_000_000
+    seen_search = seen_overflow = 0
+    for trial in range(8):
+        C = int(rng.integers(2, 9))
+        row = rng.normal(0.0, 0.4 + 0.3 * trial, size=C).astype(np.float32)
+        bound = _f32([0.2, 0.35, 0.6, 0.1][trial % 4])
+        r = oracle.constrained_softmax(row[None, :], bound, T_MIN, T_MAX,
+                                       ITERS, threads=1, lib=lib)
+        H1 = scipy.stats.entropy(scipy.special.softmax(row.astype(np.float64)))
+        if H1 <= bound:
+            assert r.T[0] == 1.0 and r.flags[0] == 0
+            continue
+        Tg, dT = _grid_largest_feasible(row, bound, lo0, hi0, n)
+        if Tg is None:
+            seen_overflow += 1
+            assert r.flags[0] == oracle.FLAG_ENTROPY_OVERFLOW
+            assert r.T[0] == lo0
+        else:
+            seen_search += 1
+            assert r.flags[0] == 0
+            assert abs(r.T[0] - Tg) <= dT + w + 1e-12, (trial, r.T[0], Tg)
+    assert seen_search >= 4
+
+
+def check_invariants(lib) -> None:
+    rng = np.random.default_rng(3)
+    x = rng.normal(0.0, 2.0, size=(16, 300)).astype(np.float32)
+    r = oracle.constrained_softmax(x, BOUND, T_MIN, T_MAX, ITERS, threads=1,
+                                   lib=lib)
+    assert np.max(np.abs(r.p.sum(axis=1) - 1.0)) < 1e-12
+    assert np.all(np.argmax(r.p, axis=1) == np.argmax(x, axis=1))
+    for b in range(x.shape[0]):
+        Hout = scipy.stats.entropy(r.p[b])
+        H_tmin = oracle.entropy(x[b], _f32(T_MIN), lib=lib)
+        if H_tmin <= _f32(BOUND):
+            assert r.flags[b] == 0
+            assert Hout <= _f32(BOUND) + 1e-9
+        else:
+            assert r.flags[b] == oracle.FLAG_ENTROPY_OVERFLOW
+            assert r.T[b] == _f32(T_MIN)
+
+    # Shift invariance (the shift by 8 is exact in fp32 for these values).
+    xs = (np.round(x * 64) / 64).astype(np.float32)
+    r1 = oracle.constrained_softmax(xs, BOUND, T_MIN, T_MAX, ITERS, threads=1,
+                                    lib=lib)
+    r2 = oracle.constrained_softmax(xs + np.float32(8.0), BOUND, T_MIN, T_MAX,
+                                    ITERS, threads=1, lib=lib)
+    assert np.array_equal(r1.T, r2.T) and np.array_equal(r1.flags, r2.flags)
+    assert np.max(np.abs(r1.p - r2.p)) < 1e-12
+
+    # Constant rows: H = ln C at every T, so any bound below ln C is
+    # unsatisfiable and the output stays exactly uniform.
+    for C in (2, 5, 1000):
+        row = np.full((1, C), 0.7, dtype=np.float32)
+        r = oracle.constrained_softmax(row, BOUND, T_MIN, T_MAX, ITERS,
+                                       threads=1, lib=lib)
+        assert np.all(r.p == r.p[0, 0]) and abs(r.p[0, 0] * C - 1) < 1e-15
+        assert r.flags[0] == oracle.FLAG_ENTROPY_OVERFLOW
+        assert r.T[0] == _f32(T_MIN)
+        assert abs(oracle.entropy(row[0], 0.3, lib=lib) - math.log(C)) < 1e-12
+
+    # C = 1: the only probability is 1 and H = 0 <= bound.
+    r = oracle.constrained_softmax(np.array([[3.5]], np.float32), BOUND,
+                                   T_MIN, T_MAX, ITERS, threads=1, lib=lib)
+    assert r.p[0, 0] == 1.0 and r.T[0] == 1.0 and r.flags[0] == 0
+
+
+def check_search_path(lib) -> None:
+    """H is nondecreasing in T (section 2.1 step 4), each step keeps the
+    feasible half, and the bracket halves every step."""
+    rng = np.random.default_rng(9)
+    lo0, hi0 = oracle.search_interval(T_MIN, T_MAX)
+    for trial in range(6):
+        row = rng.normal(0.0, 1.0 + trial, size=200).astype(np.float32)
+        path = oracle.constrained_softmax_path(row, BOUND, T_MIN, T_MAX,
+                                               ITERS, lib=lib)
+        assert path.iters == ITERS
+        order = np.argsort(path.mids)
+        assert np.all(np.diff(path.H[order]) >= -1e-12)
+        lo, hi = lo0, hi0
+        for mid, H in zip(path.mids, path.H):
+            assert abs(mid - (lo + hi) / 2) <= 1e-15
+            assert abs(H - oracle.entropy(row, mid, lib=lib)) <= 1e-12
+            if H > _f32(BOUND):
+                hi = mid
+            else:
+                lo = mid
+        assert path.T == lo
+        assert abs((hi - lo) - (hi0 - lo0) / 2 ** ITERS) < 1e-15
+
+
+def check_fault_policy(lib) -> None:
+    """Section 5.3: a NaN/Inf in the input zeroes the row and sets its flag;
+    section 5.4: an unsatisfiable bound gives T = temperature_min and flag 3."""
+    x = np.random.default_rng(1).normal(size=(6, 40)).astype(np.float32)
+    x[1, 7] = np.nan
+    x[2, 0] = np.inf
+    x[3, 39] = -np.inf
+    x[4, 3] = np.nan
+    x[4, 5] = np.inf
+    r = oracle.constrained_softmax(x, BOUND, T_MIN, T_MAX, ITERS, threads=1,
+                                   lib=lib)
+    assert list(r.flags[1:5]) == [1, 2, 2, 1]
+    for b in (1, 2, 3, 4):
+        assert np.all(r.p[b] == 0.0) and math.isnan(r.T[b])
+        assert r.iters[b] == 0
+    clean = oracle.constrained_softmax(x[[0, 5]], BOUND, T_MIN, T_MAX, ITERS,
+                                       threads=1, lib=lib)
+    assert np.array_equal(clean.p, r.p[[0, 5]])
+
+    # Negative bound: no distribution has H < 0.
+    r = oracle.constrained_softmax(x[[0]], -0.5, T_MIN, T_MAX, ITERS,
+                                   threads=1, lib=lib)
+    assert r.flags[0] == 3 and r.T[0] == _f32(T_MIN)
+    np.testing.assert_allclose(r.p[0], oracle.softmax(x[0], _f32(T_MIN),
+                                                      lib=lib), rtol=0,
+                               atol=1e-15)
+
+
+def check_parameter_edges(lib) -> None:
+    rng = np.random.default_rng(21)
+    x = rng.normal(0.0, 3.0, size=(4, 50)).astype(np.float32)
+    # max_iter = 0: no halving, T = temperature_min.
+    r = oracle.constrained_softmax(x, BOUND, T_MIN, T_MAX, 0, threads=1,
+                                   lib=lib)
+    for b in range(4):
+        assert r.T[b] == _f32(T_MIN) and r.iters[b] == 0
+        H_tmin = oracle.entropy(x[b], _f32(T_MIN), lib=lib)
+        assert r.flags[b] == (3 if H_tmin > _f32(BOUND) else 0)
+    # temperature_max < 1: the search runs on [t_min, t_max].
+    row = np.array([0.0, 0.3], dtype=np.float32)
+    t_max = 0.2
+    Ts = t_star(lambda T: h_two_class(float(row[1]), T), _f32(0.6),
+                _f32(T_MIN), _f32(t_max))
+    assert Ts is None   # whole interval feasible: lo -> t_max
+    r = oracle.constrained_softmax(row[None], 0.6, T_MIN, t_max, ITERS,
+                                   threads=1, lib=lib)
+    w = oracle.final_interval(T_MIN, t_max, ITERS)
+    assert _f32(t_max) - w - 1e-15 <= r.T[0] < _f32(t_max)
+    # temperature_min >= 1: nothing to halve, T = temperature_min.
+    r = oracle.constrained_softmax(row[None], 0.01, 1.5, 10.0, ITERS,
+                                   threads=1, lib=lib)
+    assert r.T[0] == 1.5 and r.iters[0] == 0 and r.flags[0] == 3
+
+
+ALL_CHECKS = [
+    check_two_class_entropy,
+    check_spike_entropy,
+    check_large_logits,
+    check_two_class_temperature,
+    check_spike_temperature,
+    check_softmax_special_case,
+    check_brute_force,
+    check_invariants,
+    check_search_path,
+    check_fault_policy,
+    check_parameter_edges,
+]

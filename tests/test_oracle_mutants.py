@@ -1,0 +1,81 @@
+"""The pins are sharp enough: each plausible mistake, planted in a copy of the
+oracle's C source and compiled on the CPU, must fail at least one pin.
+
+The mutations are textual edits of a temporary copy; the oracle itself is
+never modified.  CPU only (gcc).
+"""
+import os
+import shutil
+import subprocess
+
+import pytest
+
+import oracle
+import oracle_pins
+
+# (name, text in the oracle source, replacement)
+MUTANTS = [
+    ("entropy_sign", "if (p > 0.0) H -= p * log(p);",
+     "if (p > 0.0) H += p * log(p);"),
+    ("entropy_log2", "if (p > 0.0) H -= p * log(p);",
+     "if (p > 0.0) H -= p * log2(p);"),
+    ("sum_skips_first_term",
+     "    double S = 0.0;\n    for (int64_t i = 0; i < C; ++i) {\n"
+     "        S += exp(((double)l[i] - m) / T);\n    }\n    double H = 0.0;",
+     "    double S = 0.0;\n    for (int64_t i = 1; i < C; ++i) {\n"
+     "        S += exp(((double)l[i] - m) / T);\n    }\n    double H = 0.0;"),
+    ("max_is_min", "if ((double)l[i] > m) m = (double)l[i];",
+     "if ((double)l[i] < m) m = (double)l[i];"),
+    ("softmax_ignores_T", "p[i] = exp(((double)l[i] - m) / T) / S;",
+     "p[i] = exp(((double)l[i] - m)) / S;"),
+    ("softmax_times_T", "p[i] = exp(((double)l[i] - m) / T) / S;",
+     "p[i] = exp(((double)l[i] - m) * T) / S;"),
+    ("branch_swapped", "if (Hmid > bound) {", "if (Hmid < bound) {"),
+    ("search_up_to_t_max", "double hi = t_max < 1.0 ? t_max : 1.0;",
+     "double hi = t_max;"),
+    ("output_at_hi", "softmax_at(l, C, lo, p);\n    *T_out = lo;",
+     "softmax_at(l, C, hi, p);\n    *T_out = hi;"),
+    ("one_step_short", "for (int32_t k = 0; k < max_iter; ++k) {",
+     "for (int32_t k = 1; k < max_iter; ++k) {"),
+    ("midpoint_wrong", "double mid = (lo + hi) / 2.0;",
+     "double mid = lo + hi / 2.0;"),
+    ("first_check_at_t_min", "if (entropy_at(l, C, 1.0) <= bound) {",
+     "if (entropy_at(l, C, t_min) <= bound) {"),
+    ("overflow_flag_at_hi",
+     "if (entropy_at(l, C, lo) > bound) return ORACLE_FLAG_ENTROPY_OVERFLOW;",
+     "if (entropy_at(l, C, hi) > bound) return ORACLE_FLAG_ENTROPY_OVERFLOW;"),
+    ("nan_inf_flags_swapped",
+     "return has_nan ? ORACLE_FLAG_NAN_INPUT : ORACLE_FLAG_INF_INPUT;",
+     "return has_nan ? ORACLE_FLAG_INF_INPUT : ORACLE_FLAG_NAN_INPUT;"),
+    ("inf_not_detected", "else if (isinf(l[i])) has_inf = 1;",
+     "else if (0) has_inf = 1;"),
+    ("bound_strict", "if (entropy_at(l, C, 1.0) <= bound) {",
+     "if (entropy_at(l, C, 1.0) < bound - 1e-3) {"),
+]
+
+
+@pytest.fixture(scope="module")
+def mutant_dir(tmp_path_factory):
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    return tmp_path_factory.mktemp("oracle_mutants")
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_fails_a_pin(name, old, new, mutant_dir):
+    src = open(oracle.SOURCE).read()
+    assert src.count(old) >= 1, f"mutation site for {name} not found"
+    mutated = src.replace(old, new, 1)
+    c_path = os.path.join(mutant_dir, f"{name}.c")
+    so_path = os.path.join(mutant_dir, f"lib{name}.so")
+    with open(c_path, "w") as f:
+        f.write(mutated)
+    subprocess.run(oracle.build_command(c_path, so_path), check=True)
+    lib = oracle.load(so_path)
+    failed = []
+    for check in oracle_pins.ALL_CHECKS:
+        try:
+            check(lib)
+        except (AssertionError, ValueError, FloatingPointError):
+            failed.append(check.__name__)
+    assert failed, f"mutant {name} passed every pin"
