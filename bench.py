@@ -1,0 +1,498 @@
+#!/usr/bin/env python3
+"""Benchmark of the entropy-bounded softmax (constrained_softmax) on GB300.
+
+One step = one constrained_softmax launch over the whole workload (every row:
+max, T = 1 pass, bisection, output), inputs resident in HBM.  The default
+workload is batch 32 x 50000 classes, the latency case quoted by "BURT-IMMA
+CUDA Kernel API Reference" (section 2.1 Performance Notes, section 7.1:
+0.8 ms on an RTX 3080).  Prints one JSON line:
+  value       rows/s over all GPUs (device-timed, CUDA events);
+  e2e         rows/s through the public API with pinned-host inputs, H2D
+              and D2H copies inside the timed region;
+  roofline    the kernel against the slower of HBM (8 bytes per class) and
+              the ex2 unit ((1 + bisection steps) ex2 per class per row),
+              both peaks measured on this GPU (HBM: the copy bandwidth
+              recorded for the machine, ex2: a probe kernel run here);
+  cpu_baseline  the CPU oracle on this host's cores on a bounded sample.
+
+--impl reference times the CPU oracle instead (the reference arm); under
+torchrun every rank runs an independent replica (rows are independent; no
+collective is on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from entropy_bounded_softmax_gb300 import workloads as wl  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+METRIC = "rows/s and effective HBM GB/s (% of roofline); latency at 32x50000"
+# The page's figure for this workload: 0.8 ms for batch 32 x 50000 classes
+# on an RTX 3080 (another machine: context, not a target).
+PAGE_LATENCY_MS = {"latency_32x50000": 0.8}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=wl.LATENCY.name,
+                    help="one of: " + ", ".join(
+                        list(wl.WORKLOADS) + [w.name for w in wl.sweep_workloads()]))
+    ap.add_argument("--variant", choices=["auto", "rowgroup", "cluster"],
+                    default="auto")
+    ap.add_argument("--param", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--soak-s", type=float, default=1.5,
+                    help="untimed load before the timed region, for the "
+                         "clock samples")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args(argv)
+
+
+def find_workload(name: str) -> wl.Workload:
+    if name in wl.WORKLOADS:
+        return wl.WORKLOADS[name]
+    for w in wl.sweep_workloads():
+        if w.name == name:
+            return w
+    raise SystemExit(f"unknown workload {name!r}")
+
+
+# ------------------------------------------------------------ distributed
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group(backend=backend)
+    return dist
+
+
+def reduce_max(dist, value: float, device=None) -> float:
+    """Max of a float over ranks (identity without a process group)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_rows_per_s(rows_per_rank: int, world: int,
+                         max_seconds: float) -> float:
+    """Whole-job throughput: all ranks' rows over the slowest rank's time."""
+    return rows_per_rank * world / max_seconds
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons (200 ms)."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        rows = [p for (t, p) in self.samples if t0 <= t <= t1]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for name, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        pw = [num(r[3]) for r in rows if num(r[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(pw) if pw else None}
+
+
+# ------------------------------------------------------------------ peaks
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
+
+
+def probe_ex2_peak(torch, cs, stream_ptr) -> float:
+    """ex2/s of the whole GPU from the probe kernel (best of 5)."""
+    n = cs.cs_probe_ex2_sink_floats()
+    sink = torch.empty(n, dtype=torch.float32, device="cuda")
+    iters = 256
+    best = 0.0
+    for _ in range(8):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record()
+        st, count = cs.cs_probe_ex2(sink.data_ptr(), iters, stream_ptr)
+        b.record()
+        b.synchronize()
+        if st != 0:
+            raise RuntimeError(f"probe failed: {st}")
+        ms = a.elapsed_time(b)
+        if ms < 20.0:
+            iters = int(iters * max(2.0, 40.0 / max(ms, 1e-3)))
+            continue
+        best = max(best, count / (ms * 1e-3))
+    return best
+
+
+# --------------------------------------------------------- algorithmic work
+def searched_rows(w: wl.Workload, x: np.ndarray) -> int:
+    """Rows whose entropy at T = 1 exceeds the bound (they run the full
+    bisection); a workload property computed in fp64 with scipy."""
+    import scipy.special
+    n = 0
+    step = 256
+    for r0 in range(0, x.shape[0], step):
+        blk = x[r0:r0 + step].astype(np.float64)
+        p = scipy.special.softmax(blk, axis=1)
+        H = scipy.special.entr(p).sum(axis=1)
+        n += int(np.sum(H > np.float32(w.entropy_bound)))
+    return n
+
+
+# ------------------------------------------------------------ reference arm
+def run_oracle_sample(w: wl.Workload, x: np.ndarray, seconds: float,
+                      threads: int) -> dict:
+    """The CPU oracle, as it stands, on whole rows of the workload until
+    `seconds` have passed (at least one batch of `threads` rows)."""
+    import oracle
+    oracle.load()
+    done = 0
+    t0 = time.perf_counter()
+    r = 0
+    while True:
+        rows = [(r + i) % x.shape[0] for i in range(threads)]
+        oracle.constrained_softmax(x[rows], w.entropy_bound, w.t_min,
+                                   w.t_max, w.max_iter, threads=threads)
+        done += len(rows)
+        r += threads
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"rows": done, "seconds": dt, "rows_per_s": done / dt}
+
+
+def reference_arm(args, w: wl.Workload) -> int:
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    threads = oracle.default_threads()
+    x = wl.generate(w)
+    oracle.load()
+    # Each step: the oracle on `threads` whole rows, one per core, so the
+    # whole --steps/--warmup run stays within a few minutes.
+    rows_per_step = threads
+    for i in range(args.warmup):
+        rows = [(i * rows_per_step + j) % w.batch for j in range(rows_per_step)]
+        oracle.constrained_softmax(x[rows], w.entropy_bound, w.t_min,
+                                   w.t_max, w.max_iter, threads=threads)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        rows = [(i * rows_per_step + j) % w.batch for j in range(rows_per_step)]
+        oracle.constrained_softmax(x[rows], w.entropy_bound, w.t_min,
+                                   w.t_max, w.max_iter, threads=threads)
+    dt = time.perf_counter() - t0
+    value = rows_per_step * args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value,
+        "unit": "rows/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w, "cpu"),
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": f"{rows_per_step} whole rows per step "
+                                   f"({args.steps} steps)"},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w: wl.Workload, l2: str) -> dict:
+    return {"workload": w.name, "batch": w.batch,
+            "num_classes": w.num_classes, "logits": w.note,
+            "entropy_bound": w.entropy_bound, "t_min": w.t_min,
+            "t_max": w.t_max, "max_iter": w.max_iter, "seed": w.seed,
+            "l2": l2}
+
+
+# ---------------------------------------------------------------- our arm
+def our_arm(args, w: wl.Workload) -> int:
+    import torch
+    import entropy_bounded_softmax_gb300 as cs
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+
+    x = wl.generate(w)
+    B, C = x.shape
+    elems = B * C
+    io_bytes = 8 * elems
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+    variant = cs.VARIANTS[args.variant]
+
+    # Inputs larger than L2 between timed launches: rotate through enough
+    # input/output pairs that one pass over them is >= 3x L2.
+    nbuf = max(1, math.ceil(3 * L2_BYTES / io_bytes)) if io_bytes < 3 * L2_BYTES else 1
+    xs = torch.from_numpy(x).to(dev)
+    ins = [xs] + [xs.clone() for _ in range(nbuf - 1)]
+    outs = [torch.empty_like(xs) for _ in range(nbuf)]
+    t_outs = [torch.empty(B, dtype=torch.float32, device=dev)
+              for _ in range(nbuf)]
+    l2_note = (f"rotating {nbuf} input/output pairs "
+               f"({nbuf * io_bytes / 2**20:.0f} MiB > L2)") if nbuf > 1 else \
+        f"inputs larger than L2 ({io_bytes / 2**20:.0f} MiB)"
+
+    def launch(i: int) -> None:
+        k = i % nbuf
+        st = cs.cs_constrained_softmax_variant(
+            ins[k].data_ptr(), outs[k].data_ptr(), B, C,
+            w.entropy_bound, w.t_min, w.t_max, w.max_iter,
+            t_outs[k].data_ptr(), variant, args.param, sptr)
+        if st != 0:
+            raise RuntimeError(f"cs_constrained_softmax failed: {st}")
+
+    cs.get_error()
+    for i in range(max(3, args.warmup)):
+        launch(i)
+    torch.cuda.synchronize()
+    plan = cs.plan(B, C, args.variant, args.param)
+
+    sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ
+                           else 0)
+    sampler.start()
+    t_soak = time.time()
+    i = 0
+    while time.time() - t_soak < args.soak_s:
+        for _ in range(50):
+            launch(i)
+            i += 1
+        torch.cuda.synchronize()
+
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for j in range(args.steps):
+        launch(j)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t_end = time.time()
+    if dist is not None:
+        dist.barrier()
+    sampler.stop()
+    local_ms = ev0.elapsed_time(ev1)
+    total_ms = reduce_max(dist, local_ms, dev)
+    ms_per_step = total_ms / args.steps
+    value = aggregate_rows_per_s(B, world, ms_per_step * 1e-3)
+    err = cs.get_error()
+
+    # End to end through the public API: pinned host input, H2D copy, the
+    # call, D2H of the probabilities and temperatures, all inside events.
+    h_in = torch.from_numpy(x).pin_memory()
+    h_out = torch.empty((B, C), dtype=torch.float32).pin_memory()
+    h_t = torch.empty(B, dtype=torch.float32).pin_memory()
+    d_in = torch.empty((B, C), dtype=torch.float32, device=dev)
+    e_steps = max(1, args.e2e_steps)
+    for _ in range(3):
+        d_in.copy_(h_in, non_blocking=True)
+        p, T = cs.constrained_softmax(d_in, w.entropy_bound, w.t_min, w.t_max,
+                                      w.max_iter, return_t=True,
+                                      variant=args.variant, param=args.param)
+        h_out.copy_(p, non_blocking=True)
+        h_t.copy_(T, non_blocking=True)
+    torch.cuda.synchronize()
+    out_e2e = torch.empty((B, C), dtype=torch.float32, device=dev)
+    t_e2e = torch.empty(B, dtype=torch.float32, device=dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        d_in.copy_(h_in, non_blocking=True)
+        cs.constrained_softmax(d_in, w.entropy_bound, w.t_min, w.t_max,
+                               w.max_iter, out=out_e2e, t_out=t_e2e,
+                               variant=args.variant, param=args.param)
+        h_out.copy_(out_e2e, non_blocking=True)
+        h_t.copy_(t_e2e, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(dist, e0.elapsed_time(e1), dev) / e_steps
+    e2e_value = aggregate_rows_per_s(B, world, e2e_ms * 1e-3)
+
+    line = None
+    if rank == 0:
+        peaks = measured_peaks()
+        ex2_peak = probe_ex2_peak(torch, cs, sptr)
+        n_search = searched_rows(w, x)
+        exps = (B + n_search * w.max_iter) * C
+        t_kernel = ms_per_step * 1e-3
+        ex2_rate = exps / t_kernel
+        hbm_rate = io_bytes / t_kernel / 1e9
+        t_hbm = io_bytes / (peaks["hbm_gbs"] * 1e9)
+        t_ex2 = exps / ex2_peak
+        if t_ex2 >= t_hbm:
+            roof = {"bound": "alu", "unit": "Gex2/s",
+                    "achieved": ex2_rate / 1e9, "peak": ex2_peak / 1e9,
+                    "frac": ex2_rate / ex2_peak,
+                    "peak_source": "measured ex2 probe (burst)"}
+        else:
+            roof = {"bound": "hbm", "unit": "GB/s", "achieved": hbm_rate,
+                    "peak": peaks["hbm_gbs"],
+                    "frac": hbm_rate / peaks["hbm_gbs"],
+                    "peak_source": f"{peaks['source']} copy bandwidth"}
+        roof.update({
+            "traffic": None,
+            "kernel": "cluster_kernel" if plan["variant"] == 2 else "rowgroup_kernel",
+            "algorithmic_bytes": io_bytes,
+            "algorithmic_ex2": exps,
+            "searched_rows": n_search,
+            "hbm_gbs": hbm_rate,
+            "hbm_frac": hbm_rate / peaks["hbm_gbs"],
+            "hbm_peak": peaks["hbm_gbs"],
+            "roofline_us": max(t_hbm, t_ex2) * 1e6,
+            "frac_of_roofline": max(t_hbm, t_ex2) / t_kernel,
+        })
+        cpu = None
+        if not args.no_cpu_baseline:
+            import oracle
+            threads = oracle.default_threads()
+            s = run_oracle_sample(w, x, args.cpu_seconds, threads)
+            cpu = {"value": s["rows_per_s"], "unit": "rows/s",
+                   "cores": threads, "kind": "oracle",
+                   "sample": f"{s['rows']} whole rows of the workload in "
+                             f"{s['seconds']:.1f} s, one row per thread"}
+        clocks = sampler.summary(t_soak, t_end)
+        page_ms = PAGE_LATENCY_MS.get(w.name)
+        line = {
+            "metric": METRIC, "value": value, "unit": "rows/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_per_step, "latency_ms": ms_per_step,
+            "hbm_gbs": hbm_rate, "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": (value / (B / (page_ms * 1e-3))) if page_ms else None,
+            "baseline_note": ("page figure 0.8 ms on an RTX 3080 for this "
+                              "shape (another machine)") if page_ms else None,
+            "dtype": "f32", "data": "synthetic",
+            "config": dict(workload_config(w, l2_note),
+                           parallelism=f"replicas x{world}",
+                           variant=args.variant, plan=plan),
+            "roofline": roof, "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "rows/s",
+                    "ms_per_step": e2e_ms,
+                    "h2d_bytes_per_step": 4 * elems,
+                    "d2h_bytes_per_step": 4 * elems + 4 * B},
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+            "device_errors": sorted(err),
+        }
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None) -> int:
+    args = parse_args(argv)
+    w = find_workload(args.workload)
+    if args.impl == "reference":
+        return reference_arm(args, w)
+    return our_arm(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,133 @@
+"""Entropy-bounded softmax (``constrained_softmax``) for GB300 (sm_103a).
+
+For each row of a [batch, num_classes] fp32 logit matrix: softmax and its
+entropy; if the entropy exceeds ``entropy_bound`` the temperature is bisected
+on [t_min, min(1, t_max)] for ``max_iter`` steps and softmax(l / T) is
+written ("BURT-IMMA CUDA Kernel API Reference", section 2.1).
+
+PyTorch supplies device memory and the current stream; the computation runs
+in the hand-written CUDA kernels of ``libcsoftmax.so`` behind a C ABI
+(``include/entropy_bounded_softmax.h``).  There is no CPU path: the calls
+raise if the library is missing or the tensors are not on a CUDA device.
+"""
+from __future__ import annotations
+
+from . import _lib
+from ._lib import (CONSTANTS, cs_check_args, cs_constrained_softmax,
+                   cs_constrained_softmax_variant, cs_get_error, cs_plan_host,
+                   cs_plan_launch, cs_probe_ex2, cs_probe_ex2_sink_floats,
+                   cs_status_string, cs_test_wait_timeout, cs_version)
+
+__all__ = [
+    "constrained_softmax", "get_error", "plan", "version", "CsError",
+    "ERROR_BITS", "VARIANTS", "cs_constrained_softmax",
+    "cs_constrained_softmax_variant", "cs_get_error", "cs_plan_launch",
+    "cs_plan_host", "cs_check_args", "cs_probe_ex2",
+    "cs_probe_ex2_sink_floats", "cs_test_wait_timeout", "cs_version",
+    "cs_status_string",
+]
+
+# Defaults of section 2.1's signature.
+DEFAULT_ENTROPY_BOUND = 0.20
+DEFAULT_T_MIN = 0.01
+DEFAULT_T_MAX = 10.0
+DEFAULT_MAX_ITER = 20
+
+VARIANTS = {"auto": CONSTANTS["CS_VARIANT_AUTO"],
+            "rowgroup": CONSTANTS["CS_VARIANT_ROWGROUP"],
+            "cluster": CONSTANTS["CS_VARIANT_CLUSTER"]}
+ERROR_BITS = {name: 1 << CONSTANTS[f"CS_ERR_{name}"]
+              for name in ("NAN_INPUT", "INF_INPUT", "ENTROPY_OVERFLOW",
+                           "TIMEOUT")}
+
+
+class CsError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: status {status} "
+                         f"({_lib.cs_status_string(status)})")
+
+
+def _stream_handle(device) -> int:
+    import torch
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def constrained_softmax(logits, entropy_bound: float = DEFAULT_ENTROPY_BOUND,
+                        t_min: float = DEFAULT_T_MIN,
+                        t_max: float = DEFAULT_T_MAX,
+                        max_iter: int = DEFAULT_MAX_ITER,
+                        return_t: bool = False, out=None, t_out=None,
+                        variant: str = "auto", param: int = 0):
+    """Entropy-bounded softmax of a CUDA fp32 [batch, num_classes] tensor.
+
+    Returns the probabilities (and the per-row temperature if ``return_t``).
+    ``out``/``t_out`` may be given to write into existing tensors.  The call
+    is asynchronous on the current stream; per-row conditions (NaN/Inf rows,
+    unsatisfiable bounds) are read with :func:`get_error`.
+    ``variant``/``param`` force a kernel variant (see
+    ``cs_constrained_softmax_variant``).
+    """
+    import torch
+    if not isinstance(logits, torch.Tensor):
+        raise TypeError("logits must be a torch.Tensor")
+    if logits.device.type != "cuda":
+        raise ValueError("logits must be on a CUDA device")
+    if logits.dtype != torch.float32:
+        raise TypeError("logits must be float32")
+    if logits.dim() != 2:
+        raise ValueError("logits must be 2-D [batch, num_classes]")
+    if not logits.is_contiguous():
+        raise ValueError("logits must be contiguous")
+    batch, num_classes = logits.shape
+    if out is None:
+        out = torch.empty_like(logits)
+    elif (out.shape != logits.shape or out.dtype != torch.float32
+          or out.device != logits.device or not out.is_contiguous()):
+        raise ValueError("out must be a contiguous float32 tensor shaped like "
+                         "logits on the same device")
+    t_ptr = None
+    if return_t or t_out is not None:
+        if t_out is None:
+            t_out = torch.empty(batch, dtype=torch.float32,
+                                device=logits.device)
+        elif (t_out.shape != (batch,) or t_out.dtype != torch.float32
+              or t_out.device != logits.device or not t_out.is_contiguous()):
+            raise ValueError("t_out must be a contiguous float32 [batch] "
+                             "tensor on the logits' device")
+        t_ptr = t_out.data_ptr()
+    with torch.cuda.device(logits.device):
+        st = cs_constrained_softmax_variant(
+            logits.data_ptr(), out.data_ptr(), batch, num_classes,
+            float(entropy_bound), float(t_min), float(t_max), int(max_iter),
+            t_ptr, VARIANTS[variant], int(param),
+            _stream_handle(logits.device))
+    if st != 0:
+        raise CsError(st, "cs_constrained_softmax")
+    return (out, t_out) if return_t else out
+
+
+def get_error(device=None) -> set[str]:
+    """Synchronise the current stream, read and clear the device error word;
+    returns the names of the conditions seen since the last call."""
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None \
+        else torch.device(device)
+    with torch.cuda.device(dev):
+        st, mask = cs_get_error(_stream_handle(dev))
+    if st != 0:
+        raise CsError(st, "cs_get_error")
+    return {name for name, bit in ERROR_BITS.items() if mask & bit}
+
+
+def plan(batch: int, num_classes: int, variant: str = "auto",
+         param: int = 0) -> dict:
+    """The launch plan for this shape on the current device."""
+    st, p = cs_plan_launch(batch, num_classes, VARIANTS[variant], param)
+    if st != 0:
+        raise CsError(st, "cs_plan_launch")
+    return p.as_dict()
+
+
+def version() -> str:
+    return cs_version()

@@ -1,0 +1,374 @@
+// C ABI of libcsoftmax: argument checks, launch planning, the device error
+// word, and dispatch to the kernels.  See include/entropy_bounded_softmax.h
+// for the contract of every function.
+#include <float.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "cs_internal.h"
+
+// The library's only device object: a bitmask of (1 << code) for the
+// asynchronous conditions of "BURT-IMMA CUDA Kernel API Reference",
+// section 5.1 (set with atomicOr, so no condition overwrites another).
+__device__ unsigned int g_cs_error_word;
+
+namespace cs {
+int probe_chains();
+}
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kProbeThreads = 512;
+constexpr int kProbeBlocksPerSm = 4;
+constexpr int kRowgroupThreads = 256;
+constexpr int kRowgroupMaxLanes = 32;
+constexpr int kRowgroupMaxE4 = 8;      // 32 classes per lane
+constexpr int kAutoRowgroupE4 = 4;     // 16 classes per lane
+constexpr int kAutoRowgroupMaxClasses = 512;
+constexpr int kMaxIter = 1024;
+constexpr int64_t kMaxGridX = 2147483647;
+
+struct DeviceInfo {
+    std::atomic<bool> ready{false};
+    int sm_count = 0;
+    int smem_optin = 0;
+    int smem_per_sm = 0;
+    int cc_major = 0;
+    int cc_minor = 0;
+    int max_cluster = 1;
+    unsigned int* err = nullptr;
+};
+
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+cs_status device_info(DeviceInfo** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return CS_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return CS_ERR_CUDA;
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready.load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lock(g_dev_mu);
+        if (!d.ready.load(std::memory_order_relaxed)) {
+            int v[5] = {0, 0, 0, 0, 0};
+            const cudaDeviceAttr attrs[5] = {
+                cudaDevAttrMultiProcessorCount,
+                cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                cudaDevAttrMaxSharedMemoryPerMultiprocessor,
+                cudaDevAttrComputeCapabilityMajor,
+                cudaDevAttrComputeCapabilityMinor};
+            for (int i = 0; i < 5; ++i) {
+                if (cudaDeviceGetAttribute(&v[i], attrs[i], dev) != cudaSuccess) {
+                    cudaGetLastError();
+                    return CS_ERR_CUDA;
+                }
+            }
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_cs_error_word) != cudaSuccess) {
+                cudaGetLastError();
+                return CS_ERR_CUDA;
+            }
+            d.sm_count = v[0];
+            d.smem_optin = v[1];
+            d.smem_per_sm = v[2];
+            d.cc_major = v[3];
+            d.cc_minor = v[4];
+            d.max_cluster = v[3] >= 9 ? cs::kMaxCluster : 1;
+            d.err = static_cast<unsigned int*>(p);
+            d.ready.store(true, std::memory_order_release);
+        }
+    }
+    *out = &d;
+    return CS_OK;
+}
+
+bool ranges_overlap(const void* a, int64_t a_bytes, const void* b,
+                    int64_t b_bytes) {
+    if (!a || !b || a_bytes <= 0 || b_bytes <= 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a);
+    const uintptr_t b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + static_cast<uintptr_t>(b_bytes) &&
+           b0 < a0 + static_cast<uintptr_t>(a_bytes);
+}
+
+int next_pow2(int64_t x) {
+    int p = 1;
+    while (p < x) p <<= 1;
+    return p;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+cs_status plan_rowgroup(int64_t batch, int32_t C, int32_t param,
+                        cs_plan* p) {
+    const int64_t q = ceil_div(C, 4);
+    int G = 0, e4 = 0;
+    if (param == 0) {
+        for (int g = 1; g <= kRowgroupMaxLanes; g <<= 1) {
+            if (ceil_div(q, g) <= kAutoRowgroupE4) {
+                G = g;
+                break;
+            }
+        }
+        if (G == 0) G = kRowgroupMaxLanes;
+    } else {
+        if (param < 1 || param > kRowgroupMaxLanes || (param & (param - 1)))
+            return CS_ERR_INVALID_ARG;
+        G = param;
+    }
+    e4 = next_pow2(ceil_div(q, G));
+    if (e4 > kRowgroupMaxE4) return CS_ERR_OOM;
+    p->variant = CS_VARIANT_ROWGROUP;
+    p->lanes_per_row = G;
+    p->elems_per_lane = 4 * e4;
+    p->cluster_size = 0;
+    p->slice_len = 0;
+    p->threads_per_cta = kRowgroupThreads;
+    p->smem_bytes = 0;
+    p->ctas_per_sm = 2048 / kRowgroupThreads;
+    int64_t blocks = ceil_div(batch * G, kRowgroupThreads);
+    if (blocks > kMaxGridX) blocks = kMaxGridX;
+    p->grid_ctas = blocks;
+    return CS_OK;
+}
+
+cs_status plan_cluster(int64_t batch, int32_t C, int32_t param, int sm_count,
+                       int smem_optin, int smem_per_sm, int max_cluster,
+                       cs_plan* p) {
+    (void)sm_count;
+    auto fits = [&](int n, int64_t* L, int* threads, int64_t* smem) {
+        *L = ceil_div(ceil_div(C, n), 4) * 4;
+        *threads = cs::cluster_threads_for(*L);
+        *smem = cs::cluster_smem_bytes(*L, *threads, n);
+        return *smem <= smem_optin;
+    };
+    int n = 0;
+    int64_t L = 0, smem = 0;
+    int threads = 0;
+    if (param == 0) {
+        for (int c = 1; c <= max_cluster; ++c) {
+            if (fits(c, &L, &threads, &smem)) {
+                n = c;
+                break;
+            }
+        }
+        if (n == 0) return CS_ERR_OOM;
+    } else {
+        if (param < 1 || param > cs::kMaxCluster) return CS_ERR_INVALID_ARG;
+        if (param > max_cluster) return CS_ERR_INVALID_ARG;
+        n = param;
+        if (!fits(n, &L, &threads, &smem)) return CS_ERR_OOM;
+    }
+    p->variant = CS_VARIANT_CLUSTER;
+    p->lanes_per_row = 0;
+    p->elems_per_lane = 0;
+    p->cluster_size = n;
+    p->slice_len = static_cast<int32_t>(L);
+    p->threads_per_cta = threads;
+    p->smem_bytes = static_cast<int32_t>(smem);
+    int by_smem = static_cast<int>(smem_per_sm / (smem + 1024));
+    int by_threads = 2048 / threads;
+    p->ctas_per_sm = by_smem < by_threads ? by_smem : by_threads;
+    int64_t rows = batch;
+    const int64_t max_rows = kMaxGridX / n;
+    if (rows > max_rows) rows = max_rows;
+    p->grid_ctas = rows * n;
+    return CS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+cs_status cs_check_args(const float* logits, const float* out, int64_t batch,
+                        int32_t num_classes, float entropy_bound, float t_min,
+                        float t_max, int32_t max_iter, const float* t_out) {
+    if (batch < 0 || num_classes < 1) return CS_ERR_DIM_MISMATCH;
+    if (num_classes > CS_MAX_NUM_CLASSES) return CS_ERR_OOM;
+    if (batch > INT64_MAX / 4 / num_classes) return CS_ERR_DIM_MISMATCH;
+    if (isnan(entropy_bound)) return CS_ERR_INVALID_ARG;
+    if (!(t_min >= FLT_MIN) || isinf(t_min)) return CS_ERR_INVALID_ARG;
+    if (isnan(t_max) || t_max < t_min) return CS_ERR_INVALID_ARG;
+    if (max_iter < 0 || max_iter > kMaxIter) return CS_ERR_INVALID_ARG;
+    if (batch == 0) return CS_OK;
+    if (!logits || !out) return CS_ERR_INVALID_ARG;
+    const int64_t bytes = batch * num_classes * 4;
+    if (ranges_overlap(logits, bytes, out, bytes)) return CS_ERR_INVALID_ARG;
+    if (t_out && (ranges_overlap(t_out, batch * 4, logits, bytes) ||
+                  ranges_overlap(t_out, batch * 4, out, bytes)))
+        return CS_ERR_INVALID_ARG;
+    return CS_OK;
+}
+
+cs_status cs_plan_host(int64_t batch, int32_t num_classes, int32_t variant,
+                       int32_t param, int32_t sm_count,
+                       int32_t smem_per_block_optin, int32_t smem_per_sm,
+                       int32_t max_cluster, cs_plan* plan) {
+    if (!plan) return CS_ERR_INVALID_ARG;
+    if (batch < 0 || num_classes < 1) return CS_ERR_DIM_MISMATCH;
+    if (num_classes > CS_MAX_NUM_CLASSES) return CS_ERR_OOM;
+    if (sm_count < 1 || smem_per_block_optin < 1 || smem_per_sm < 1 ||
+        max_cluster < 1)
+        return CS_ERR_INVALID_ARG;
+    if (max_cluster > cs::kMaxCluster) max_cluster = cs::kMaxCluster;
+    if (variant == CS_VARIANT_AUTO) {
+        if (param != 0) return CS_ERR_INVALID_ARG;
+        variant = num_classes <= kAutoRowgroupMaxClasses ? CS_VARIANT_ROWGROUP
+                                                         : CS_VARIANT_CLUSTER;
+    }
+    if (variant == CS_VARIANT_ROWGROUP)
+        return plan_rowgroup(batch, num_classes, param, plan);
+    if (variant == CS_VARIANT_CLUSTER)
+        return plan_cluster(batch, num_classes, param, sm_count,
+                            smem_per_block_optin, smem_per_sm, max_cluster,
+                            plan);
+    return CS_ERR_INVALID_ARG;
+}
+
+cs_status cs_plan_launch(int64_t batch, int32_t num_classes, int32_t variant,
+                         int32_t param, cs_plan* plan) {
+    DeviceInfo* d = nullptr;
+    const cs_status st = device_info(&d);
+    if (st != CS_OK) return st;
+    return cs_plan_host(batch, num_classes, variant, param, d->sm_count,
+                        d->smem_optin, d->smem_per_sm, d->max_cluster, plan);
+}
+
+cs_status cs_constrained_softmax_variant(const float* logits, float* out,
+                                         int64_t batch, int32_t num_classes,
+                                         float entropy_bound, float t_min,
+                                         float t_max, int32_t max_iter,
+                                         float* t_out, int32_t variant,
+                                         int32_t param, void* stream) {
+    cs_status st = cs_check_args(logits, out, batch, num_classes,
+                                 entropy_bound, t_min, t_max, max_iter, t_out);
+    if (st != CS_OK) return st;
+    if (batch == 0) return CS_OK;
+    DeviceInfo* d = nullptr;
+    st = device_info(&d);
+    if (st != CS_OK) return st;
+    cs_plan p;
+    st = cs_plan_host(batch, num_classes, variant, param, d->sm_count,
+                      d->smem_optin, d->smem_per_sm, d->max_cluster, &p);
+    if (st != CS_OK) return st;
+
+    cs::RowTask task;
+    task.logits = logits;
+    task.out = out;
+    task.t_out = t_out;
+    task.err = d->err;
+    task.batch = batch;
+    task.num_classes = num_classes;
+    task.max_iter = max_iter;
+    task.entropy_bound = entropy_bound;
+    task.t_min = t_min;
+    task.hi0 = t_max < 1.0f ? t_max : 1.0f;
+    task.wait_limit_ns = cs::kWaitLimitNs;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (p.variant == CS_VARIANT_ROWGROUP) {
+        e = cs::launch_rowgroup(task, p.lanes_per_row, p.elems_per_lane, s);
+    } else {
+        e = cs::launch_cluster(task, p.cluster_size, p.slice_len,
+                               p.threads_per_cta, p.smem_bytes, p.grid_ctas, s);
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return CS_ERR_CUDA;
+    }
+    return CS_OK;
+}
+
+cs_status cs_constrained_softmax(const float* logits, float* out,
+                                 int64_t batch, int32_t num_classes,
+                                 float entropy_bound, float t_min, float t_max,
+                                 int32_t max_iter, float* t_out, void* stream) {
+    return cs_constrained_softmax_variant(logits, out, batch, num_classes,
+                                          entropy_bound, t_min, t_max,
+                                          max_iter, t_out, CS_VARIANT_AUTO, 0,
+                                          stream);
+}
+
+cs_status cs_get_error(int32_t* code_mask, void* stream) {
+    if (!code_mask) return CS_ERR_INVALID_ARG;
+    DeviceInfo* d = nullptr;
+    const cs_status st = device_info(&d);
+    if (st != CS_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned int h = 0;
+    if (cudaMemcpyAsync(&h, d->err, sizeof(h), cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess ||
+        cudaMemsetAsync(d->err, 0, sizeof(h), s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return CS_ERR_CUDA;
+    }
+    *code_mask = static_cast<int32_t>(h);
+    return CS_OK;
+}
+
+int32_t cs_probe_ex2_sink_floats(void) {
+    DeviceInfo* d = nullptr;
+    if (device_info(&d) != CS_OK) return -1;
+    return d->sm_count * kProbeBlocksPerSm * kProbeThreads;
+}
+
+cs_status cs_probe_ex2(float* sink, int32_t iters, int64_t* ex2_count,
+                       void* stream) {
+    if (!sink || !ex2_count || iters < 1) return CS_ERR_INVALID_ARG;
+    DeviceInfo* d = nullptr;
+    const cs_status st = device_info(&d);
+    if (st != CS_OK) return st;
+    const int blocks = d->sm_count * kProbeBlocksPerSm;
+    const cudaError_t e = cs::launch_probe_ex2(
+        sink, iters, blocks, kProbeThreads, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return CS_ERR_CUDA;
+    }
+    *ex2_count = static_cast<int64_t>(blocks) * kProbeThreads * iters *
+                 cs::probe_chains();
+    return CS_OK;
+}
+
+cs_status cs_test_wait_timeout(int64_t limit_ns, void* stream) {
+    if (limit_ns < 1 || limit_ns > 10000000000ll) return CS_ERR_INVALID_ARG;
+    DeviceInfo* d = nullptr;
+    const cs_status st = device_info(&d);
+    if (st != CS_OK) return st;
+    const cudaError_t e = cs::launch_wait_timeout(
+        d->err, static_cast<uint64_t>(limit_ns),
+        static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return CS_ERR_CUDA;
+    }
+    return CS_OK;
+}
+
+const char* cs_version(void) { return "1.0.0 sm_103a"; }
+
+const char* cs_status_string(cs_status status) {
+    switch (status) {
+        case CS_OK: return "success";
+        case CS_ERR_NAN_INPUT: return "NaN in input";
+        case CS_ERR_INF_INPUT: return "Inf in input";
+        case CS_ERR_ENTROPY_OVERFLOW: return "entropy bound unsatisfiable";
+        case CS_ERR_DIM_MISMATCH: return "dimension mismatch";
+        case CS_ERR_OOM: return "row does not fit the shared-memory plan";
+        case CS_ERR_INVALID_ARG: return "invalid argument";
+        case CS_ERR_CUDA: return "CUDA error";
+        case CS_ERR_TIMEOUT: return "device wait timed out";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,74 @@
+// Internal interface between the C ABI (cs_api.cu) and the kernel
+// translation units.  Not installed; the public API is
+// include/entropy_bounded_softmax.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "entropy_bounded_softmax.h"
+
+namespace cs {
+
+// Bits of the device error word.
+constexpr unsigned int kBitNan = 1u << CS_ERR_NAN_INPUT;
+constexpr unsigned int kBitInf = 1u << CS_ERR_INF_INPUT;
+constexpr unsigned int kBitOverflow = 1u << CS_ERR_ENTROPY_OVERFLOW;
+constexpr unsigned int kBitTimeout = 1u << CS_ERR_TIMEOUT;
+
+// Default limit of every bounded device wait (2 s).
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// One launch's worth of work: every row of the matrix with the same
+// parameters (the arguments of section 2.1's signature plus t_out and the
+// error word).
+struct RowTask {
+    const float* logits;
+    float* out;
+    float* t_out;          // may be null
+    unsigned int* err;     // device error word
+    int64_t batch;
+    int32_t num_classes;
+    int32_t max_iter;
+    float entropy_bound;
+    float t_min;
+    float hi0;             // min(1, t_max): upper end of the search
+    uint64_t wait_limit_ns;
+};
+
+// Cluster kernel geometry.
+constexpr int kMaxCluster = 16;
+constexpr int kLoadChunks = 8;        // bulk copies per CTA slice
+constexpr int kClusterMaxThreads = 1024;
+
+// Dynamic shared memory of the cluster kernel for a slice of `slice_len`
+// classes, `threads` threads and cluster size `n`.
+inline int64_t cluster_smem_bytes(int64_t slice_len, int threads, int n) {
+    const int64_t warps = threads / 32;
+    const int64_t slots = 2 * warps * n * 8;            // exchange buffers
+    const int64_t bars = (2 + kLoadChunks) * 8;         // mbarriers
+    const int64_t head = ((slots + bars + 127) / 128) * 128;
+    const int64_t row = ((slice_len + 8 + 3) / 4) * 16;  // pad + tail room
+    return head + row;
+}
+
+inline int cluster_threads_for(int64_t slice_len) {
+    // About 16 classes per thread per pass, 128..1024 threads.
+    int64_t t = (slice_len + 15) / 16;
+    t = ((t + 31) / 32) * 32;
+    if (t < 128) t = 128;
+    if (t > kClusterMaxThreads) t = kClusterMaxThreads;
+    return static_cast<int>(t);
+}
+
+cudaError_t launch_rowgroup(const RowTask& task, int lanes_per_row,
+                            int elems_per_lane, cudaStream_t stream);
+cudaError_t launch_cluster(const RowTask& task, int cluster_size,
+                           int slice_len, int threads, int smem_bytes,
+                           int64_t grid_ctas, cudaStream_t stream);
+cudaError_t launch_probe_ex2(float* sink, int iters, int blocks, int threads,
+                             cudaStream_t stream);
+cudaError_t launch_wait_timeout(unsigned int* err, uint64_t limit_ns,
+                                cudaStream_t stream);
+
+}  // namespace cs

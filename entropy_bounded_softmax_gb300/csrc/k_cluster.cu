@@ -1,0 +1,422 @@
+// Cluster kernel: one thread-block cluster of n CTAs per row (n = 1: one CTA
+// per row).  Each CTA holds its slice of the row in shared memory for the
+// whole search, so the row is read from HBM once and written once.
+//
+// Method: "BURT-IMMA CUDA Kernel API Reference", section 2.1
+// `constrained_softmax`, Description steps 1-4, with the error policy of
+// sections 5.3 and 5.4.  Per row:
+//   stage   bulk copies (cp.async.bulk) of the slice into shared memory, in
+//           chunks, each on its own mbarrier, so the max pass starts on the
+//           first chunk while the rest are in flight;
+//   max     m = max_i l_i (T-independent, computed once) and a finiteness
+//           check, exchanged across the cluster;
+//   T = 1   one pass turns the slice into y_i = (l_i - m) log2(e) in place
+//           and sums S = sum 2^y_i and V = sum y_i 2^y_i;
+//   search  each bisection step is one pass over y at beta = 1/mid giving
+//           S(beta) = sum 2^(beta y_i) and V(beta) = sum y_i 2^(beta y_i);
+//           with p_i = 2^(beta y_i) / S the entropy in nats is
+//           H = ln 2 * (log2 S - beta V / S);
+//   output  p_i = 2^(beta_lo y_i) / S(lo), reusing S(lo) from the step that
+//           set lo, written with 128-bit streaming stores.
+//
+// Reductions: every warp reduces its (S, V) with shuffles and pushes the
+// pair into an exchange slot of every CTA of the cluster (st.async with an
+// mbarrier transaction count; a plain store + arrive when n = 1).  After the
+// mbarrier completes, every warp of every CTA sums the same slots in the
+// same order, so all of them take the same bisection decision without a
+// further barrier.  Two slot buffers alternate, which is safe because no
+// warp can reach exchange k+2 before every warp has left exchange k.
+//
+// Every wait is bounded (cs::kWaitLimitNs by default).  A thread whose wait
+// times out records CS_ERR_TIMEOUT and from then on neither waits, arrives,
+// pushes nor issues copies, but keeps the kernel's control flow so that all
+// threads still meet at every __syncthreads and cluster barrier.
+#include <math.h>
+
+#include "cs_device.cuh"
+
+namespace cs {
+namespace {
+
+using namespace csd;
+
+// Geometry of one CTA's slice in shared memory.  Element j of the slice
+// lives at row[pad + j], so 16-byte aligned global addresses land on
+// 16-byte aligned shared addresses.  Float4 q in [qb0, qb1) comes in by
+// bulk copy; the head (q = 0 when pad > 0) and tail float4s by plain loads.
+struct Slice {
+    int pad;
+    int len;
+    int q4;       // float4s of the slice in shared memory
+    int qb0, qb1; // bulk-copied body
+    int head_q;   // -1 if none
+    int tail_q;   // -1 if none
+};
+
+__device__ __forceinline__ Slice make_slice(const float* src, int len) {
+    Slice s;
+    s.pad = static_cast<int>((reinterpret_cast<uintptr_t>(src) >> 2) & 3);
+    s.len = len;
+    if (len <= 0) {
+        s.len = 0;
+        s.q4 = s.qb0 = s.qb1 = 0;
+        s.head_q = s.tail_q = -1;
+        return s;
+    }
+    const int end = s.pad + len;
+    s.q4 = (end + 3) >> 2;
+    s.qb0 = s.pad > 0 ? 1 : 0;
+    s.qb1 = end >> 2;
+    if (s.qb1 < s.qb0) s.qb1 = s.qb0;
+    s.head_q = s.pad > 0 ? 0 : -1;
+    s.tail_q = (end & 3) ? (end >> 2) : -1;
+    if (s.tail_q == s.head_q) s.tail_q = -1;
+    return s;
+}
+
+__device__ __forceinline__ int chunk_begin(const Slice& s, int nch, int c) {
+    const int body = s.qb1 - s.qb0;
+    return s.qb0 + static_cast<int>((static_cast<int64_t>(body) * c) / nch);
+}
+
+// One exchange across the warps of the CTA and the CTAs of the cluster.
+// `v` is this thread's partial; returns the cluster-wide sum (or max).
+template <bool CLUSTER, bool IS_MAX>
+__device__ __forceinline__ float2 exchange(float2 v, float2* xs,
+                                           uint64_t* xbar, uint32_t& xk,
+                                           int warps, int n, uint32_t rank,
+                                           uint64_t limit, bool& dead) {
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    v = IS_MAX ? warp_max2(v) : warp_sum2(v);
+    const uint32_t buf = xk & 1u;
+    const uint32_t parity = (xk >> 1) & 1u;
+    ++xk;
+    const int nslots = warps * n;
+    float2* slots = xs + buf * nslots;
+    if (!dead) {
+        if (CLUSTER) {
+            if (threadIdx.x == 0) mbar_arrive_expect_tx(&xbar[buf], nslots * 8);
+            if (lane < n) {
+                const uint32_t dst = map_to_rank(
+                    smem_addr(&slots[rank * warps + warp]), lane);
+                const uint32_t bar = map_to_rank(smem_addr(&xbar[buf]), lane);
+                push_pair(dst, v.x, v.y, bar);
+            }
+        } else if (lane == 0) {
+            slots[warp] = v;
+            mbar_arrive(&xbar[buf]);
+        }
+        if (!mbar_wait(&xbar[buf], parity, limit)) dead = true;
+    }
+    float2 acc = IS_MAX ? make_float2(-INFINITY, 0.0f) : make_float2(0.0f, 0.0f);
+    for (int j = lane; j < nslots; j += 32) {
+        const float2 s = slots[j];
+        if (IS_MAX) {
+            acc.x = fmaxf(acc.x, s.x);
+            acc.y = fmaxf(acc.y, s.y);
+        } else {
+            acc.x += s.x;
+            acc.y += s.y;
+        }
+    }
+    return IS_MAX ? warp_max2(acc) : warp_sum2(acc);
+}
+
+// One pass over this thread's float4s of the slice: returns the partial
+// (S, V) at inverse temperature beta.  With TRANSFORM the slice still holds
+// logits and is rewritten in place as y = max((l - m) log2 e, floor).
+template <bool TRANSFORM>
+__device__ __forceinline__ float2 pass_sv(float4* row4, int q4, float beta,
+                                          float m) {
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    float v0 = 0.f, v1 = 0.f, v2 = 0.f, v3 = 0.f;
+    for (int q = threadIdx.x; q < q4; q += blockDim.x) {
+        float4 y = row4[q];
+        if (TRANSFORM) {
+            y.x = fmaxf((y.x - m) * kLog2e, kYFloor);
+            y.y = fmaxf((y.y - m) * kLog2e, kYFloor);
+            y.z = fmaxf((y.z - m) * kLog2e, kYFloor);
+            y.w = fmaxf((y.w - m) * kLog2e, kYFloor);
+            row4[q] = y;
+        }
+        const float e0 = ex2(y.x * beta);
+        const float e1 = ex2(y.y * beta);
+        const float e2 = ex2(y.z * beta);
+        const float e3 = ex2(y.w * beta);
+        s0 += e0;
+        s1 += e1;
+        s2 += e2;
+        s3 += e3;
+        v0 = fmaf(e0, y.x, v0);
+        v1 = fmaf(e1, y.y, v1);
+        v2 = fmaf(e2, y.z, v2);
+        v3 = fmaf(e3, y.w, v3);
+    }
+    return make_float2((s0 + s1) + (s2 + s3), (v0 + v1) + (v2 + v3));
+}
+
+// Entropy in nats from the cluster-wide (S, V) at inverse temperature beta.
+__device__ __forceinline__ float entropy_nats(float2 sv, float beta) {
+    return kLn2 * (log2f(sv.x) - (beta * sv.y) / sv.x);
+}
+
+__device__ __forceinline__ void store_scalar_lanes(float* dst, int q, int pad,
+                                                   int len, float4 p) {
+    const int j0 = 4 * q - pad;
+    const float v[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int j = j0 + i;
+        if (j >= 0 && j < len) dst[j] = v[i];
+    }
+}
+
+// Output pass: p = 2^(beta y) * inv_s (or zeros) into dst[0, len).
+__device__ __forceinline__ void write_out(const float4* row4, const Slice& s,
+                                          float* dst, float beta, float inv_s,
+                                          bool zero) {
+    const int pad_o = static_cast<int>((reinterpret_cast<uintptr_t>(dst) >> 2) & 3);
+    const bool vec = pad_o == s.pad;
+    for (int q = threadIdx.x; q < s.q4; q += blockDim.x) {
+        float4 p = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (!zero) {
+            const float4 y = row4[q];
+            p.x = ex2(y.x * beta) * inv_s;
+            p.y = ex2(y.y * beta) * inv_s;
+            p.z = ex2(y.z * beta) * inv_s;
+            p.w = ex2(y.w * beta) * inv_s;
+        }
+        if (vec && q >= s.qb0 && q < s.qb1) {
+            __stcs(reinterpret_cast<float4*>(dst + (4 * q - s.pad)), p);
+        } else {
+            store_scalar_lanes(dst, q, s.pad, s.len, p);
+        }
+    }
+}
+
+template <bool CLUSTER>
+__global__ void __launch_bounds__(kClusterMaxThreads, 1)
+cluster_kernel(RowTask t, int n, int slice_len) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int nt = blockDim.x;
+    const int warps = nt >> 5;
+    const uint32_t rank = CLUSTER ? cluster_ctarank() : 0u;
+    const int64_t cid = blockIdx.x / n;
+    const int64_t ncl = gridDim.x / n;
+    const int nslots = warps * n;
+    float2* xs = reinterpret_cast<float2*>(smem);
+    uint64_t* xbar = reinterpret_cast<uint64_t*>(smem + 2 * nslots * 8);
+    uint64_t* lbar = xbar + 2;
+    const int head_bytes = ((2 * nslots * 8 + (2 + kLoadChunks) * 8 + 127) / 128) * 128;
+    float* row = reinterpret_cast<float*>(smem + head_bytes);
+    float4* row4 = reinterpret_cast<float4*>(row);
+
+    if (threadIdx.x == 0) {
+        mbar_init(&xbar[0], CLUSTER ? 1u : static_cast<uint32_t>(warps));
+        mbar_init(&xbar[1], CLUSTER ? 1u : static_cast<uint32_t>(warps));
+        for (int c = 0; c < kLoadChunks; ++c) mbar_init(&lbar[c], 1u);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (CLUSTER) cluster_sync();
+
+    const int64_t C = t.num_classes;
+    const int64_t s0 = static_cast<int64_t>(rank) * slice_len;
+    const int len = static_cast<int>(max(static_cast<int64_t>(0),
+                                         min(static_cast<int64_t>(slice_len), C - s0)));
+    const float bound = t.entropy_bound;
+    uint32_t xk = 0;           // exchanges so far (slot buffer, phase)
+    uint32_t lphase = 0;       // parity bit per load chunk
+    bool dead = false;         // this thread's waits timed out
+    bool reported = false;
+
+    for (int64_t r = cid; r < t.batch; r += ncl) {
+        const float* src = t.logits + r * C + s0;
+        const Slice s = make_slice(src, len);
+        const int body = s.qb1 - s.qb0;
+        const int nch = body > 0 ? min(kLoadChunks, body) : 0;
+
+        // Stage: thread 0 issues the bulk copies; threads 0-7 fetch the
+        // ragged head/tail float4s with plain loads.
+        if (threadIdx.x == 0 && !dead) {
+            fence_proxy_async_smem();
+            for (int c = 0; c < nch; ++c) {
+                const int qa = chunk_begin(s, nch, c);
+                const int qz = chunk_begin(s, nch, c + 1);
+                const uint32_t bytes = static_cast<uint32_t>(qz - qa) * 16u;
+                mbar_arrive_expect_tx(&lbar[c], bytes);
+                bulk_load(row4 + qa, src + (4 * qa - s.pad), bytes, &lbar[c]);
+            }
+        }
+        float m_loc = -INFINITY;
+        float bad = 0.0f;  // becomes NaN if any element is NaN or +-Inf
+        if (threadIdx.x < 8) {
+            const int q = threadIdx.x < 4 ? s.head_q : s.tail_q;
+            if (q >= 0) {
+                const int idx = 4 * q + (threadIdx.x & 3);
+                const int j = idx - s.pad;
+                float v = -INFINITY;
+                if (j >= 0 && j < s.len) {
+                    v = src[j];
+                    m_loc = v;
+                    bad = v * 0.0f;
+                }
+                row[idx] = v;
+            }
+        }
+        __syncthreads();
+
+        // Max pass, chunk by chunk as the copies land.
+        for (int c = 0; c < nch; ++c) {
+            if (!dead && !mbar_wait(&lbar[c], (lphase >> c) & 1u, t.wait_limit_ns))
+                dead = true;
+            lphase ^= 1u << c;
+            const int qa = chunk_begin(s, nch, c);
+            const int qz = chunk_begin(s, nch, c + 1);
+            for (int q = qa + threadIdx.x; q < qz; q += nt) {
+                const float4 v = row4[q];
+                m_loc = fmaxf(m_loc, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+                bad = fmaf(v.x, 0.0f, bad);
+                bad = fmaf(v.y, 0.0f, bad);
+                bad = fmaf(v.z, 0.0f, bad);
+                bad = fmaf(v.w, 0.0f, bad);
+            }
+        }
+        // Classify a non-finite row (rare): 2 = NaN seen, 1 = only Inf.
+        float code = 0.0f;
+        if (bad != bad) {
+            code = 1.0f;
+            for (int q = threadIdx.x; q < s.q4; q += nt) {
+                const float4 v = row4[q];
+                const int j0 = 4 * q - s.pad;
+                const float e[4] = {v.x, v.y, v.z, v.w};
+                for (int i = 0; i < 4; ++i) {
+                    const int j = j0 + i;
+                    if (j >= 0 && j < s.len && isnan(e[i])) code = 2.0f;
+                }
+            }
+        }
+        const float2 mc = exchange<CLUSTER, true>(
+            make_float2(m_loc, code), xs, xbar, xk, warps, n, rank,
+            t.wait_limit_ns, dead);
+        const float m = mc.x;
+        const int row_code = static_cast<int>(mc.y);
+
+        float* dst = t.out + r * C + s0;
+        unsigned int bits = 0;
+        float T_row = NAN;
+        if (row_code != 0) {
+            bits = row_code == 2 ? kBitNan : kBitInf;
+            write_out(row4, s, dst, 0.0f, 0.0f, true);
+        } else {
+            float2 sv = exchange<CLUSTER, false>(
+                pass_sv<true>(row4, s.q4, 1.0f, m), xs, xbar, xk, warps, n,
+                rank, t.wait_limit_ns, dead);
+            float H = entropy_nats(sv, 1.0f);
+            float beta_out, inv_s;
+            if (!(H > bound)) {
+                T_row = 1.0f;
+                beta_out = 1.0f;
+                inv_s = 1.0f / sv.x;
+            } else {
+                float lo = t.t_min, hi = t.hi0;
+                bool lo_eval = false;
+                bool hi_eval = hi == 1.0f;   // H(1) > bound is known
+                float s_lo = 0.0f;
+                if (lo < hi) {
+                    for (int k = 0; k < t.max_iter; ++k) {
+                        const float mid = 0.5f * (lo + hi);
+                        // Exact early exit: the fp32 midpoint has reached an
+                        // end whose side is already known, so every further
+                        // step repeats the same evaluation.
+                        if ((mid == lo && lo_eval) || (mid == hi && hi_eval)) break;
+                        const float b = 1.0f / mid;
+                        sv = exchange<CLUSTER, false>(
+                            pass_sv<false>(row4, s.q4, b, 0.0f), xs, xbar, xk,
+                            warps, n, rank, t.wait_limit_ns, dead);
+                        H = entropy_nats(sv, b);
+                        if (H > bound) {
+                            hi = mid;
+                            hi_eval = true;
+                        } else {
+                            lo = mid;
+                            lo_eval = true;
+                            s_lo = sv.x;
+                        }
+                    }
+                }
+                const float b_lo = 1.0f / lo;
+                if (!lo_eval) {
+                    // lo is still t_min: evaluate it (section 5.4 check).
+                    sv = exchange<CLUSTER, false>(
+                        pass_sv<false>(row4, s.q4, b_lo, 0.0f), xs, xbar, xk,
+                        warps, n, rank, t.wait_limit_ns, dead);
+                    H = entropy_nats(sv, b_lo);
+                    s_lo = sv.x;
+                    if (H > bound) bits |= kBitOverflow;
+                }
+                T_row = lo;
+                beta_out = b_lo;
+                inv_s = 1.0f / s_lo;
+            }
+            write_out(row4, s, dst, beta_out, inv_s, false);
+        }
+        if (rank == 0 && threadIdx.x == 0) {
+            if (t.t_out) t.t_out[r] = T_row;
+            raise_error(t.err, bits);
+        }
+        if (dead && !reported) {
+            raise_error(t.err, kBitTimeout);
+            reported = true;
+        }
+        // The slice buffer is rewritten by the next row's copies.
+        __syncthreads();
+    }
+    if (dead && threadIdx.x == 0) {
+        // Give copies still in flight a bounded chance to land before exit.
+        for (int c = 0; c < kLoadChunks; ++c)
+            mbar_wait(&lbar[c], ((lphase >> c) & 1u) ^ 1u, t.wait_limit_ns);
+    }
+    if (CLUSTER) cluster_sync();
+}
+
+}  // namespace
+
+cudaError_t launch_cluster(const RowTask& task, int cluster_size,
+                           int slice_len, int threads, int smem_bytes,
+                           int64_t grid_ctas, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid_ctas), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (cluster_size > 1) {
+        auto kern = cluster_kernel<true>;
+        cudaError_t e = cudaFuncSetAttribute(
+            kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+        if (e != cudaSuccess) return e;
+        if (cluster_size > 8) {
+            e = cudaFuncSetAttribute(
+                kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e != cudaSuccess) return e;
+        }
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(cluster_size);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kern, task, cluster_size, slice_len);
+    }
+    auto kern = cluster_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(
+        kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (e != cudaSuccess) return e;
+    cfg.attrs = nullptr;
+    cfg.numAttrs = 0;
+    return cudaLaunchKernelEx(&cfg, kern, task, 1, slice_len);
+}
+
+}  // namespace cs

@@ -1,0 +1,272 @@
+// Row-group kernel for narrow rows (mixture-of-experts router widths):
+// G lanes of a warp share one row and each lane keeps its 4*E4 classes in
+// registers for the whole search, so the row is read from HBM once (128-bit
+// streaming loads) and written once (128-bit streaming stores).
+//
+// Method: "BURT-IMMA CUDA Kernel API Reference", section 2.1
+// `constrained_softmax`, Description steps 1-4, with sections 5.3 and 5.4;
+// the steps are the same as in the cluster kernel: max once, y = (l - m)
+// log2 e, then one register pass per bisection step giving
+// S = sum 2^(beta y) and V = sum y 2^(beta y), H = ln 2 (log2 S - beta V/S).
+// The per-step reduction is a butterfly over the G lanes (all lanes end
+// with bit-identical sums, so they take the same decision); the decision
+// uses the MUFU lg2 and rcp units, the output normalisation an exact
+// reciprocal.
+#include <math.h>
+
+#include "cs_device.cuh"
+
+namespace cs {
+namespace {
+
+using namespace csd;
+
+template <int G>
+__device__ __forceinline__ float2 group_sum2(float2 v, unsigned mask) {
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) {
+        v.x += __shfl_xor_sync(mask, v.x, o);
+        v.y += __shfl_xor_sync(mask, v.y, o);
+    }
+    return v;
+}
+
+template <int G>
+__device__ __forceinline__ float2 group_max2(float2 v, unsigned mask) {
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) {
+        v.x = fmaxf(v.x, __shfl_xor_sync(mask, v.x, o));
+        v.y = fmaxf(v.y, __shfl_xor_sync(mask, v.y, o));
+    }
+    return v;
+}
+
+template <int E4>
+__device__ __forceinline__ float2 reg_pass(const float4 (&y)[E4], float beta) {
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    float v0 = 0.f, v1 = 0.f, v2 = 0.f, v3 = 0.f;
+#pragma unroll
+    for (int i = 0; i < E4; ++i) {
+        const float e0 = ex2(y[i].x * beta);
+        const float e1 = ex2(y[i].y * beta);
+        const float e2 = ex2(y[i].z * beta);
+        const float e3 = ex2(y[i].w * beta);
+        s0 += e0;
+        s1 += e1;
+        s2 += e2;
+        s3 += e3;
+        v0 = fmaf(e0, y[i].x, v0);
+        v1 = fmaf(e1, y[i].y, v1);
+        v2 = fmaf(e2, y[i].z, v2);
+        v3 = fmaf(e3, y[i].w, v3);
+    }
+    return make_float2((s0 + s1) + (s2 + s3), (v0 + v1) + (v2 + v3));
+}
+
+__device__ __forceinline__ float entropy_nats_fast(float2 sv, float beta) {
+    return kLn2 * (lg2_approx(sv.x) - beta * sv.y * rcp_approx(sv.x));
+}
+
+template <int G, int E4>
+__global__ void __launch_bounds__(256)
+rowgroup_kernel(RowTask t, int vec) {
+    const int lane = threadIdx.x & 31;
+    const int sub = lane & (G - 1);
+    const unsigned gmask =
+        G == 32 ? 0xffffffffu : (((1u << G) - 1u) << (lane & ~(G - 1)));
+    const int C = t.num_classes;
+    const int Q = (C + 3) >> 2;  // float4 slots per row
+    const float bound = t.entropy_bound;
+    const int64_t groups_per_grid =
+        (static_cast<int64_t>(gridDim.x) * blockDim.x) / G;
+
+    for (int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x +
+                        threadIdx.x) / G;
+         row < t.batch; row += groups_per_grid) {
+        const float* src = t.logits + row * C;
+        float* dst = t.out + row * C;
+        float4 y[E4];
+        float m = -INFINITY;
+        float bad = 0.0f;
+        if (vec) {
+            const float4* s4 = reinterpret_cast<const float4*>(src);
+#pragma unroll
+            for (int i = 0; i < E4; ++i) {
+                const int q = i * G + sub;
+                if (q < Q) {
+                    y[i] = __ldcs(s4 + q);
+                    m = fmaxf(m, fmaxf(fmaxf(y[i].x, y[i].y),
+                                       fmaxf(y[i].z, y[i].w)));
+                    bad = fmaf(y[i].x, 0.f, bad);
+                    bad = fmaf(y[i].y, 0.f, bad);
+                    bad = fmaf(y[i].z, 0.f, bad);
+                    bad = fmaf(y[i].w, 0.f, bad);
+                } else {
+                    y[i] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < E4; ++i) {
+                const int j0 = 4 * (i * G + sub);
+                float e[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int j = j0 + k;
+                    e[k] = -INFINITY;
+                    if (j < C) {
+                        e[k] = __ldcs(src + j);
+                        m = fmaxf(m, e[k]);
+                        bad = fmaf(e[k], 0.f, bad);
+                    }
+                }
+                y[i] = make_float4(e[0], e[1], e[2], e[3]);
+            }
+        }
+        float code = 0.0f;
+        if (bad != bad) {
+            code = 1.0f;
+#pragma unroll
+            for (int i = 0; i < E4; ++i) {
+                if (isnan(y[i].x) || isnan(y[i].y) || isnan(y[i].z) ||
+                    isnan(y[i].w))
+                    code = 2.0f;
+            }
+        }
+        const float2 mc = group_max2<G>(make_float2(m, code), gmask);
+        m = mc.x;
+        const int row_code = static_cast<int>(mc.y);
+
+        unsigned int bits = 0;
+        float T_row = NAN;
+        float beta_out = 0.0f, inv_s = 0.0f;
+        if (row_code != 0) {
+            bits = row_code == 2 ? kBitNan : kBitInf;
+        } else {
+#pragma unroll
+            for (int i = 0; i < E4; ++i) {
+                y[i].x = fmaxf((y[i].x - m) * kLog2e, kYFloor);
+                y[i].y = fmaxf((y[i].y - m) * kLog2e, kYFloor);
+                y[i].z = fmaxf((y[i].z - m) * kLog2e, kYFloor);
+                y[i].w = fmaxf((y[i].w - m) * kLog2e, kYFloor);
+            }
+            float2 sv = group_sum2<G>(reg_pass<E4>(y, 1.0f), gmask);
+            float H = entropy_nats_fast(sv, 1.0f);
+            if (!(H > bound)) {
+                T_row = 1.0f;
+                beta_out = 1.0f;
+                inv_s = 1.0f / sv.x;
+            } else {
+                float lo = t.t_min, hi = t.hi0;
+                bool lo_eval = false;
+                bool hi_eval = hi == 1.0f;
+                float s_lo = 0.0f;
+                if (lo < hi) {
+                    for (int k = 0; k < t.max_iter; ++k) {
+                        const float mid = 0.5f * (lo + hi);
+                        if ((mid == lo && lo_eval) || (mid == hi && hi_eval)) break;
+                        const float b = 1.0f / mid;
+                        sv = group_sum2<G>(reg_pass<E4>(y, b), gmask);
+                        H = entropy_nats_fast(sv, b);
+                        if (H > bound) {
+                            hi = mid;
+                            hi_eval = true;
+                        } else {
+                            lo = mid;
+                            lo_eval = true;
+                            s_lo = sv.x;
+                        }
+                    }
+                }
+                const float b_lo = 1.0f / lo;
+                if (!lo_eval) {
+                    sv = group_sum2<G>(reg_pass<E4>(y, b_lo), gmask);
+                    H = entropy_nats_fast(sv, b_lo);
+                    s_lo = sv.x;
+                    if (H > bound) bits |= kBitOverflow;
+                }
+                T_row = lo;
+                beta_out = b_lo;
+                inv_s = 1.0f / s_lo;
+            }
+        }
+        const bool zero = row_code != 0;
+        if (vec) {
+            float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+            for (int i = 0; i < E4; ++i) {
+                const int q = i * G + sub;
+                if (q < Q) {
+                    float4 p = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (!zero) {
+                        p.x = ex2(y[i].x * beta_out) * inv_s;
+                        p.y = ex2(y[i].y * beta_out) * inv_s;
+                        p.z = ex2(y[i].z * beta_out) * inv_s;
+                        p.w = ex2(y[i].w * beta_out) * inv_s;
+                    }
+                    __stcs(d4 + q, p);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < E4; ++i) {
+                const int j0 = 4 * (i * G + sub);
+                const float yy[4] = {y[i].x, y[i].y, y[i].z, y[i].w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int j = j0 + k;
+                    if (j < C)
+                        __stcs(dst + j, zero ? 0.0f : ex2(yy[k] * beta_out) * inv_s);
+                }
+            }
+        }
+        if (sub == 0) {
+            if (t.t_out) t.t_out[row] = T_row;
+            raise_error(t.err, bits);
+        }
+    }
+}
+
+template <int G>
+cudaError_t launch_g(const RowTask& t, int e4, int vec, dim3 grid, dim3 block,
+                     cudaStream_t s) {
+    switch (e4) {
+        case 1: rowgroup_kernel<G, 1><<<grid, block, 0, s>>>(t, vec); break;
+        case 2: rowgroup_kernel<G, 2><<<grid, block, 0, s>>>(t, vec); break;
+        case 4: rowgroup_kernel<G, 4><<<grid, block, 0, s>>>(t, vec); break;
+        case 8: rowgroup_kernel<G, 8><<<grid, block, 0, s>>>(t, vec); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+constexpr int kRowgroupThreads = 256;
+constexpr int64_t kMaxGridX = 2147483647;
+
+cudaError_t launch_rowgroup(const RowTask& t, int lanes_per_row,
+                            int elems_per_lane, cudaStream_t stream) {
+    const int e4 = elems_per_lane / 4;
+    const int C = t.num_classes;
+    const bool aligned =
+        (C % 4 == 0) && (reinterpret_cast<uintptr_t>(t.logits) % 16 == 0) &&
+        (reinterpret_cast<uintptr_t>(t.out) % 16 == 0);
+    const int64_t rows_per_block = kRowgroupThreads / lanes_per_row;
+    int64_t blocks = (t.batch + rows_per_block - 1) / rows_per_block;
+    if (blocks > kMaxGridX) blocks = kMaxGridX;
+    const dim3 grid(static_cast<unsigned>(blocks));
+    const dim3 block(kRowgroupThreads);
+    const int vec = aligned ? 1 : 0;
+    switch (lanes_per_row) {
+        case 1: return launch_g<1>(t, e4, vec, grid, block, stream);
+        case 2: return launch_g<2>(t, e4, vec, grid, block, stream);
+        case 4: return launch_g<4>(t, e4, vec, grid, block, stream);
+        case 8: return launch_g<8>(t, e4, vec, grid, block, stream);
+        case 16: return launch_g<16>(t, e4, vec, grid, block, stream);
+        case 32: return launch_g<32>(t, e4, vec, grid, block, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace cs

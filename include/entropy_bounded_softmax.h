@@ -1,0 +1,188 @@
+/*
+ * entropy_bounded_softmax.h -- C ABI of the GB300 (sm_103a) entropy-bounded
+ * softmax library, libcsoftmax.so.
+ *
+ * The operation is `constrained_softmax` as defined by "BURT-IMMA CUDA Kernel
+ * API Reference", section 2.1 (Signature, Parameters table, Description steps
+ * 1-4), with the error codes of section 5.1, the NaN/Inf policy of section 5.3
+ * and the degradation rule of section 5.4.  For each row l of a row-major
+ * [batch, num_classes] fp32 matrix:
+ *
+ *   1. p = softmax(l) (T = 1) and its entropy H = -sum p_i ln p_i (nats);
+ *   2. if H <= entropy_bound, write p and report T = 1;
+ *   3. otherwise bisect T on [t_min, min(1, t_max)] for exactly max_iter
+ *      steps: mid = (lo + hi) / 2; H(mid) > entropy_bound moves hi to mid,
+ *      otherwise lo moves to mid.  Temperatures above 1 are never searched
+ *      because H is nondecreasing in T (section 2.1 step 4);
+ *   4. write softmax(l / lo) and report T = lo.  If even lo = t_min violates
+ *      the bound, the row still gets softmax(l / t_min), the lowest entropy
+ *      reachable (section 5.4), and ENTROPY_OVERFLOW is raised.
+ *
+ * Arithmetic is fp32 with the exponential on the hardware ex2 unit; the
+ * bookkeeping of lo, hi and mid is fp32 as well.
+ *
+ * All functions are thread-safe.  No function allocates device memory per
+ * call; the library's only device object is one 32-bit error word per GPU.
+ */
+#ifndef ENTROPY_BOUNDED_SOFTMAX_H
+#define ENTROPY_BOUNDED_SOFTMAX_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes.  0-7 keep the numbering of section 5.1 (enum BurtError);
+ * 8-10 are new.  4 (spectral overflow) and 5 (capacity full) belong to other
+ * kernels of that page and are never returned here. */
+typedef int32_t cs_status;
+#define CS_OK 0
+#define CS_ERR_NAN_INPUT 1        /* a row held a NaN (asynchronous)        */
+#define CS_ERR_INF_INPUT 2        /* a row held +-Inf (asynchronous)        */
+#define CS_ERR_ENTROPY_OVERFLOW 3 /* bound unsatisfiable at t_min (async)   */
+#define CS_ERR_DIM_MISMATCH 6     /* batch < 0, num_classes < 1, overflow   */
+#define CS_ERR_OOM 7              /* row too long for the shared-memory plan */
+#define CS_ERR_INVALID_ARG 8      /* null/overlapping pointers, bad params  */
+#define CS_ERR_CUDA 9             /* a CUDA call failed (launch, attribute)  */
+#define CS_ERR_TIMEOUT 10         /* a bounded device wait gave up (async)  */
+
+/* Kernel variants (cs_plan.variant, and the `variant` argument of
+ * cs_constrained_softmax_variant). */
+#define CS_VARIANT_AUTO 0
+#define CS_VARIANT_ROWGROUP 1 /* 1-32 lanes per row, row in registers      */
+#define CS_VARIANT_CLUSTER 2  /* 1-16 CTAs per row, row in shared memory,
+                                 partial sums exchanged over DSMEM; one CTA
+                                 per row when the cluster size is 1        */
+
+/* Largest num_classes the library accepts: a 16-CTA cluster holding the row
+ * in shared memory. */
+#define CS_MAX_NUM_CLASSES 850000
+
+/* What a launch of the given shape uses.  Filled by cs_plan / cs_plan_host. */
+typedef struct cs_plan {
+    int32_t variant;         /* CS_VARIANT_ROWGROUP or CS_VARIANT_CLUSTER   */
+    int32_t lanes_per_row;   /* rowgroup: lanes that share one row          */
+    int32_t elems_per_lane;  /* rowgroup: fp32 registers of row per lane    */
+    int32_t cluster_size;    /* cluster: CTAs per row (1 = one CTA per row) */
+    int32_t slice_len;       /* cluster: classes held by one CTA            */
+    int32_t threads_per_cta;
+    int32_t smem_bytes;      /* dynamic shared memory per CTA               */
+    int32_t ctas_per_sm;     /* CTAs resident per SM by the plan's limits   */
+    int64_t grid_ctas;       /* CTAs in the launch                          */
+} cs_plan;
+
+/*
+ * cs_constrained_softmax -- section 2.1 `constrained_softmax`.
+ *
+ * logits   device pointer, [batch, num_classes] fp32, row-major, contiguous.
+ *          Read only.  Any 4-byte alignment is accepted; 16-byte aligned
+ *          rows (num_classes % 4 == 0 and an aligned base) take the bulk-copy
+ *          and 128-bit store path.
+ * out      device pointer, [batch, num_classes] fp32, written completely.
+ *          Must not overlap logits (the page declares both __restrict__).
+ * batch    rows; 0 is a no-op that returns CS_OK.
+ * num_classes  classes per row, 1..CS_MAX_NUM_CLASSES.
+ * entropy_bound  bound on H in nats (page default 0.20).  Any non-NaN value;
+ *          a negative bound is unsatisfiable, +inf disables the search.
+ * t_min, t_max  search interval (page defaults 0.01 and 10.0).  t_min must
+ *          be a finite normal float > 0 and t_max >= t_min (t_max may be +inf).
+ * max_iter bisection steps, 0..1024 (page default 20).
+ * t_out    optional device pointer, [batch] fp32: the temperature each row
+ *          used (1 when no search was needed, lo after a search, t_min when
+ *          the bound is unsatisfiable, NaN for a row with NaN/Inf input).
+ *          May be NULL; must not overlap logits or out.
+ * stream   a cudaStream_t (NULL = the legacy default stream).
+ *
+ * Ownership: the caller owns every buffer; nothing is allocated.
+ * Execution: asynchronous on `stream`; the call returns after the launch
+ * and never synchronises.
+ * Errors: argument problems return CS_ERR_DIM_MISMATCH / CS_ERR_INVALID_ARG /
+ * CS_ERR_OOM before anything is launched; a failed launch returns
+ * CS_ERR_CUDA.  Per-row conditions found on the device (NaN, Inf,
+ * unsatisfiable bound, wait timeout) do not fail the call: the rows get the
+ * section 5.3/5.4 treatment (NaN/Inf rows are all zeros) and the condition
+ * is OR-ed into the device error word, read with cs_get_error.
+ */
+cs_status cs_constrained_softmax(const float* logits, float* out,
+                                 int64_t batch, int32_t num_classes,
+                                 float entropy_bound, float t_min, float t_max,
+                                 int32_t max_iter, float* t_out, void* stream);
+
+/*
+ * Same operation with the kernel variant chosen by the caller (tests and
+ * benchmarks use it to run every variant on every shape).
+ * variant  CS_VARIANT_AUTO, CS_VARIANT_ROWGROUP or CS_VARIANT_CLUSTER.
+ * param    rowgroup: lanes per row (1, 2, 4, 8, 16 or 32; 0 = automatic).
+ *          cluster: CTAs per row (1..16; 0 = automatic).
+ * A variant that cannot hold the row returns CS_ERR_OOM (rowgroup: more than
+ * 32 classes per lane; cluster: slice larger than a CTA's shared memory).
+ */
+cs_status cs_constrained_softmax_variant(const float* logits, float* out,
+                                         int64_t batch, int32_t num_classes,
+                                         float entropy_bound, float t_min,
+                                         float t_max, int32_t max_iter,
+                                         float* t_out, int32_t variant,
+                                         int32_t param, void* stream);
+
+/*
+ * Reads and clears the calling thread's current device's error word after
+ * synchronising `stream`.  *code_mask receives a bitmask of (1 << code) for
+ * every asynchronous condition since the last call: CS_ERR_NAN_INPUT,
+ * CS_ERR_INF_INPUT, CS_ERR_ENTROPY_OVERFLOW, CS_ERR_TIMEOUT.  The word is
+ * shared by every launch on the device, so launches on other streams that
+ * run concurrently may be counted or cleared by this call.  This is the only
+ * function that synchronises.  Returns CS_ERR_INVALID_ARG for a NULL
+ * code_mask, CS_ERR_CUDA when a CUDA call fails.
+ */
+cs_status cs_get_error(int32_t* code_mask, void* stream);
+
+/* The plan cs_constrained_softmax_variant would launch on the current
+ * device (queries device attributes; no launch).  Same argument rules. */
+cs_status cs_plan_launch(int64_t batch, int32_t num_classes, int32_t variant,
+                         int32_t param, cs_plan* plan);
+
+/* The same planning on given device limits, host-only (no CUDA call):
+ * sm_count SMs, smem_per_block_optin bytes of dynamic shared memory per CTA,
+ * smem_per_sm bytes per SM, max_cluster CTAs per cluster. */
+cs_status cs_plan_host(int64_t batch, int32_t num_classes, int32_t variant,
+                       int32_t param, int32_t sm_count,
+                       int32_t smem_per_block_optin, int32_t smem_per_sm,
+                       int32_t max_cluster, cs_plan* plan);
+
+/* Host-only argument check of cs_constrained_softmax (no CUDA call). */
+cs_status cs_check_args(const float* logits, const float* out, int64_t batch,
+                        int32_t num_classes, float entropy_bound, float t_min,
+                        float t_max, int32_t max_iter, const float* t_out);
+
+/*
+ * Throughput probe of the ex2 unit, the unit this operation is bound by.
+ * Launches one kernel over all SMs in which every thread runs `iters`
+ * rounds of 8 independent ex2.approx.ftz.f32 chains; *ex2_count receives
+ * the number of ex2 the launch executes.  The caller times the launch (for
+ * example with CUDA events on `stream`).  sink: device pointer to at least
+ * cs_probe_ex2_sink_floats() floats, written so that the work is not dead.
+ */
+cs_status cs_probe_ex2(float* sink, int32_t iters, int64_t* ex2_count,
+                       void* stream);
+int32_t cs_probe_ex2_sink_floats(void);
+
+/*
+ * Exercises the bounded device wait that every kernel uses: launches one
+ * CTA that waits on a barrier nothing completes, for at most limit_ns
+ * nanoseconds (1..10^10), then gives up and records CS_ERR_TIMEOUT in the
+ * error word.  Used to test the timeout path without hanging anything.
+ */
+cs_status cs_test_wait_timeout(int64_t limit_ns, void* stream);
+
+/* Library version string, e.g. "1.0.0 sm_103a". */
+const char* cs_version(void);
+
+/* Short English name of a status code. */
+const char* cs_status_string(cs_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ENTROPY_BOUNDED_SOFTMAX_H */

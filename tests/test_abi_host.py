@@ -1,0 +1,168 @@
+"""The C ABI on the CPU: the library loads, exports every function the header
+declares, and its host-only logic (argument checks, launch planning, status
+strings) behaves as documented.  No CUDA call is made."""
+import os
+import re
+
+import pytest
+
+import entropy_bounded_softmax_gb300 as cs
+from entropy_bounded_softmax_gb300 import _lib
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include",
+                      "entropy_bounded_softmax.h")
+GB300 = dict(sm_count=152, smem_per_block_optin=232448, smem_per_sm=233472,
+             max_cluster=16)
+C = _lib.CONSTANTS
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(cs_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_function():
+    lib = _lib.load()
+    declared = header_functions()
+    assert "cs_constrained_softmax" in declared
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert sorted(_lib.exported_names()) == declared
+
+
+def test_status_codes_follow_the_page():
+    import json
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden",
+                                    "kernel_api_constants.json")))
+    codes = g["error_codes"]
+    assert C["CS_OK"] == codes["SUCCESS"]
+    for name in ("NAN_INPUT", "INF_INPUT", "ENTROPY_OVERFLOW",
+                 "DIM_MISMATCH", "OOM"):
+        assert C[f"CS_ERR_{name}"] == codes[name]
+    assert cs.cs_status_string(C["CS_ERR_INVALID_ARG"]) == "invalid argument"
+    assert cs.version().endswith("sm_103a")
+
+
+def test_binding_defaults_follow_the_page():
+    import inspect
+    import json
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden",
+                                    "kernel_api_constants.json")))["defaults"]
+    sig = inspect.signature(cs.constrained_softmax)
+    assert sig.parameters["entropy_bound"].default == g["entropy_bound"]
+    assert sig.parameters["t_min"].default == g["temperature_min"]
+    assert sig.parameters["t_max"].default == g["temperature_max"]
+    assert sig.parameters["max_iter"].default == g["max_iterations"]
+
+
+A, B = 1 << 20, 1 << 30   # two far-apart fake device addresses
+
+
+@pytest.mark.parametrize("args,status", [
+    ((A, B, 4, 10, 0.2, 0.01, 10.0, 20, None), 0),
+    ((A, B, 0, 10, 0.2, 0.01, 10.0, 20, None), 0),
+    ((None, None, 0, 10, 0.2, 0.01, 10.0, 20, None), 0),
+    ((A, B, -1, 10, 0.2, 0.01, 10.0, 20, None), 6),
+    ((A, B, 4, 0, 0.2, 0.01, 10.0, 20, None), 6),
+    ((A, B, 2**62, 1000, 0.2, 0.01, 10.0, 20, None), 6),
+    ((A, B, 4, 900000, 0.2, 0.01, 10.0, 20, None), 7),
+    ((None, B, 4, 10, 0.2, 0.01, 10.0, 20, None), 8),
+    ((A, None, 4, 10, 0.2, 0.01, 10.0, 20, None), 8),
+    ((A, A + 40, 4, 10, 0.2, 0.01, 10.0, 20, None), 8),     # overlap
+    ((A, A + 160, 4, 10, 0.2, 0.01, 10.0, 20, None), 0),    # adjacent
+    ((A, B, 4, 10, 0.2, 0.01, 10.0, 20, A + 8), 8),         # t_out overlap
+    ((A, B, 4, 10, float("nan"), 0.01, 10.0, 20, None), 8),
+    ((A, B, 4, 10, float("inf"), 0.01, 10.0, 20, None), 0),
+    ((A, B, 4, 10, -1.0, 0.01, 10.0, 20, None), 0),
+    ((A, B, 4, 10, 0.2, 0.0, 10.0, 20, None), 8),
+    ((A, B, 4, 10, 0.2, 1e-45, 10.0, 20, None), 8),         # subnormal
+    ((A, B, 4, 10, 0.2, float("inf"), float("inf"), 20, None), 8),
+    ((A, B, 4, 10, 0.2, 0.01, 0.001, 20, None), 8),
+    ((A, B, 4, 10, 0.2, 0.01, float("nan"), 20, None), 8),
+    ((A, B, 4, 10, 0.2, 0.01, float("inf"), 20, None), 0),
+    ((A, B, 4, 10, 0.2, 0.01, 10.0, -1, None), 8),
+    ((A, B, 4, 10, 0.2, 0.01, 10.0, 1025, None), 8),
+    ((A, B, 4, 10, 0.2, 0.01, 10.0, 0, None), 0),
+])
+def test_check_args(args, status):
+    assert cs.cs_check_args(*args) == status
+
+
+def plan(batch, classes, variant=0, param=0, **dev):
+    d = dict(GB300, **dev)
+    st, p = cs.cs_plan_host(batch, classes, variant, param, d["sm_count"],
+                            d["smem_per_block_optin"], d["smem_per_sm"],
+                            d["max_cluster"])
+    return st, p.as_dict()
+
+
+def test_auto_plans_for_the_workloads():
+    st, p = plan(65536, 64)
+    assert st == 0 and p["variant"] == C["CS_VARIANT_ROWGROUP"]
+    assert p["lanes_per_row"] * p["elems_per_lane"] >= 64
+    st, p = plan(32, 50000)
+    assert st == 0 and p["variant"] == C["CS_VARIANT_CLUSTER"]
+    assert p["smem_bytes"] <= GB300["smem_per_block_optin"]
+    st, p = plan(4096, 32000)
+    assert st == 0 and p["cluster_size"] >= 1
+    st, p = plan(256, 131072)
+    assert st == 0 and p["cluster_size"] >= 3
+    assert p["slice_len"] * p["cluster_size"] >= 131072
+    assert p["grid_ctas"] == 256 * p["cluster_size"]
+
+
+@pytest.mark.parametrize("classes", [1, 3, 17, 64, 511, 512, 513, 1000,
+                                     4099, 32000, 50001, 131072, 600000,
+                                     850000])
+def test_plans_hold_the_row(classes):
+    st, p = plan(8, classes)
+    assert st == 0
+    if p["variant"] == C["CS_VARIANT_ROWGROUP"]:
+        assert p["lanes_per_row"] * p["elems_per_lane"] >= classes
+        assert p["lanes_per_row"] in (1, 2, 4, 8, 16, 32)
+    else:
+        n = p["cluster_size"]
+        assert 1 <= n <= 16
+        assert p["slice_len"] % 4 == 0
+        assert n * p["slice_len"] >= classes
+        assert (n - 1) * p["slice_len"] < classes or n == 1 or classes < 4 * n
+        assert p["smem_bytes"] <= GB300["smem_per_block_optin"]
+        assert p["smem_bytes"] >= 4 * p["slice_len"]
+        assert p["threads_per_cta"] % 32 == 0 and p["threads_per_cta"] <= 1024
+
+
+def test_forced_variants_and_limits():
+    st, _ = plan(8, 64, C["CS_VARIANT_ROWGROUP"], 1)
+    assert st == C["CS_ERR_OOM"]          # 64 classes in one lane
+    st, p = plan(8, 32, C["CS_VARIANT_ROWGROUP"], 1)
+    assert st == 0 and p["elems_per_lane"] == 32
+    st, _ = plan(8, 4096, C["CS_VARIANT_ROWGROUP"], 32)
+    assert st == C["CS_ERR_OOM"]          # 128 classes per lane
+    st, _ = plan(8, 64, C["CS_VARIANT_ROWGROUP"], 3)
+    assert st == C["CS_ERR_INVALID_ARG"]
+    st, _ = plan(8, 64, C["CS_VARIANT_CLUSTER"], 17)
+    assert st == C["CS_ERR_INVALID_ARG"]
+    st, _ = plan(8, 131072, C["CS_VARIANT_CLUSTER"], 1)
+    assert st == C["CS_ERR_OOM"]
+    st, p = plan(8, 131072, C["CS_VARIANT_CLUSTER"], 16)
+    assert st == 0 and p["slice_len"] == 8192
+    st, _ = plan(8, 131072, C["CS_VARIANT_CLUSTER"], 8, max_cluster=4)
+    assert st == C["CS_ERR_INVALID_ARG"]
+    st, _ = plan(8, 64, C["CS_VARIANT_AUTO"], 4)
+    assert st == C["CS_ERR_INVALID_ARG"]
+    st, _ = plan(8, 64, 7, 0)
+    assert st == C["CS_ERR_INVALID_ARG"]
+    st, _ = plan(8, 850000, C["CS_VARIANT_CLUSTER"], 0, max_cluster=8)
+    assert st == C["CS_ERR_OOM"]
+
+
+def test_constrained_softmax_rejects_cpu_tensors():
+    import torch
+    with pytest.raises(ValueError):
+        cs.constrained_softmax(torch.zeros(2, 3))
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError, match="no fallback"):
+        _lib.load(str(tmp_path / "libcsoftmax.so"))

@@ -1,0 +1,111 @@
+"""GPU parity on the workload shapes: the CUDA path (through the C ABI)
+against the fp64 oracle, element by element on the same seeded inputs.
+
+Small shapes are compared in full; the full-size shapes are launched whole,
+in the configuration the benchmark times, and compared on sampled rows the
+oracle computes one by one."""
+import numpy as np
+import pytest
+
+import oracle
+from entropy_bounded_softmax_gb300 import workloads as wl
+from gpu_parity import compare, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def _params(w):
+    return dict(entropy_bound=w.entropy_bound, t_min=w.t_min, t_max=w.t_max,
+                max_iter=w.max_iter)
+
+
+def _oracle(x, w):
+    return oracle.constrained_softmax(x, **_params(w))
+
+
+@pytest.mark.parametrize("variant,param", [("auto", 0), ("cluster", 1),
+                                           ("cluster", 2), ("cluster", 4),
+                                           ("rowgroup", 32)])
+def test_small_4x1000(variant, param):
+    w = wl.SMALL
+    x = wl.generate(w)
+    p, T, mask = run_gpu(x, variant=variant, param=param, **_params(w))
+    compare(x, p, T, mask, _oracle(x, w), **_params(w))
+
+
+@pytest.mark.parametrize("variant,param", [("auto", 0), ("cluster", 2),
+                                           ("cluster", 4), ("cluster", 8)])
+def test_latency_32x50000(variant, param):
+    w = wl.LATENCY
+    x = wl.generate(w)
+    p, T, mask = run_gpu(x, variant=variant, param=param, **_params(w))
+    stats = compare(x, p, T, mask, _oracle(x, w), **_params(w))
+    assert stats["T_equal"] >= 28
+
+
+def test_moe_router_full():
+    w = wl.ROUTER
+    x = wl.generate(w)
+    p, T, mask = run_gpu(x, **_params(w))
+    stats = compare(x, p, T, mask, _oracle(x, w), **_params(w))
+    assert stats["T_equal"] >= 0.95 * w.batch
+
+
+@pytest.mark.parametrize("lanes", [1, 2, 4, 8, 16, 32])
+def test_moe_router_lanes(lanes):
+    w = wl.ROUTER
+    rows = np.arange(2048)
+    x = wl.generate(w, rows)
+    p, T, mask = run_gpu(x, variant="rowgroup", param=lanes, **_params(w))
+    compare(x, p, T, mask, _oracle(x, w), **_params(w))
+
+
+def test_moe_router_cluster_variant():
+    w = wl.ROUTER
+    x = wl.generate(w, np.arange(512))
+    p, T, mask = run_gpu(x, variant="cluster", param=1, **_params(w))
+    compare(x, p, T, mask, _oracle(x, w), **_params(w))
+
+
+@pytest.mark.parametrize("param", [0, 4, 8, 16])
+def test_long_rows_sampled(param):
+    """256 x 131072 launched whole; rows sampled for the oracle, always
+    including constant, spiked and normal rows."""
+    w = wl.LONG
+    x = wl.generate(w)
+    p, T, mask = run_gpu(x, variant="cluster" if param else "auto",
+                         param=param, **_params(w))
+    kinds = wl.row_kinds(w)
+    pick = sorted(set(wl.sample_rows(w, 10).tolist())
+                  | set(np.flatnonzero(kinds == 2)[:3].tolist())
+                  | set(np.flatnonzero(kinds == 1)[:3].tolist()))
+    ref = _oracle(x[pick], w)
+    compare(x[pick], p[pick], T[pick], mask, ref, check_mask=False,
+            **_params(w))
+    # Constant rows: exactly uniform, T = t_min, overflow flagged.
+    const = np.flatnonzero(kinds == 2)
+    assert np.all(p[const] == p[const][:, :1])
+    assert np.allclose(p[const], 1.0 / w.num_classes, rtol=1e-6, atol=0)
+    assert np.all(T[const] == np.float32(w.t_min))
+    assert mask & (1 << 3)
+
+
+def test_long_rows_no_search_branch():
+    """Rows spiked by +20 stay under the bound at T = 1 (no search)."""
+    w = wl.LONG.with_(extra={"constant_frac": 0.0, "spike": 20.0}, batch=16)
+    x = wl.generate(w)
+    p, T, mask = run_gpu(x, **_params(w))
+    ref = _oracle(x, w)
+    assert np.sum(ref.T == 1.0) >= 6
+    compare(x, p, T, mask, ref, **_params(w))
+
+
+@pytest.mark.parametrize("bound,iters", wl.SWEEP_POINTS)
+def test_sweep_sampled(bound, iters):
+    w = wl.SWEEP.with_(entropy_bound=bound, max_iter=iters)
+    x = wl.generate(w)
+    p, T, mask = run_gpu(x, **_params(w))
+    pick = wl.sample_rows(w, 24)
+    ref = _oracle(x[pick], w)
+    compare(x[pick], p[pick], T[pick], mask, ref, check_mask=False,
+            **_params(w))
