@@ -58,7 +58,13 @@ def parse_args(argv=None):
                         list(wl.WORKLOADS) + [w.name for w in wl.sweep_workloads()]))
     ap.add_argument("--variant", choices=["auto", "rowgroup", "cluster"],
                     default="auto")
-    ap.add_argument("--param", type=int, default=0)
+    ap.add_argument("--param", type=int, default=0,
+                    help="lanes per row (rowgroup) or CTAs per row (cluster)")
+    ap.add_argument("--threads", type=int, default=0,
+                    help="cluster variant: threads per CTA (0 = automatic)")
+    ap.add_argument("--full-scan", action="store_true",
+                    help="cluster variant: evaluate every class at every "
+                         "step (no active set)")
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--soak-s", type=float, default=1.5,
                     help="untimed load before the timed region, for the "
@@ -320,7 +326,8 @@ def our_arm(args, w: wl.Workload) -> int:
     io_bytes = 8 * elems
     stream = torch.cuda.current_stream(dev)
     sptr = stream.cuda_stream
-    variant = cs.VARIANTS[args.variant]
+    opts = cs.options(cs.VARIANTS[args.variant], args.param, args.threads,
+                      int(args.full_scan))
 
     # Inputs larger than L2 between timed launches: rotate through enough
     # input/output pairs that one pass over them is >= 3x L2.
@@ -336,10 +343,10 @@ def our_arm(args, w: wl.Workload) -> int:
 
     def launch(i: int) -> None:
         k = i % nbuf
-        st = cs.cs_constrained_softmax_variant(
+        st = cs.cs_constrained_softmax_ex(
             ins[k].data_ptr(), outs[k].data_ptr(), B, C,
             w.entropy_bound, w.t_min, w.t_max, w.max_iter,
-            t_outs[k].data_ptr(), variant, args.param, sptr)
+            t_outs[k].data_ptr(), opts, sptr)
         if st != 0:
             raise RuntimeError(f"cs_constrained_softmax failed: {st}")
 
@@ -347,7 +354,8 @@ def our_arm(args, w: wl.Workload) -> int:
     for i in range(max(3, args.warmup)):
         launch(i)
     torch.cuda.synchronize()
-    plan = cs.plan(B, C, args.variant, args.param)
+    plan = cs.plan(B, C, args.variant, args.param, args.threads,
+                   args.full_scan)
 
     sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ
                            else 0)
@@ -391,7 +399,9 @@ def our_arm(args, w: wl.Workload) -> int:
         d_in.copy_(h_in, non_blocking=True)
         p, T = cs.constrained_softmax(d_in, w.entropy_bound, w.t_min, w.t_max,
                                       w.max_iter, return_t=True,
-                                      variant=args.variant, param=args.param)
+                                      variant=args.variant, param=args.param,
+                                      threads=args.threads,
+                                      full_scan=args.full_scan)
         h_out.copy_(p, non_blocking=True)
         h_t.copy_(T, non_blocking=True)
     torch.cuda.synchronize()
@@ -404,7 +414,9 @@ def our_arm(args, w: wl.Workload) -> int:
         d_in.copy_(h_in, non_blocking=True)
         cs.constrained_softmax(d_in, w.entropy_bound, w.t_min, w.t_max,
                                w.max_iter, out=out_e2e, t_out=t_e2e,
-                               variant=args.variant, param=args.param)
+                               variant=args.variant, param=args.param,
+                               threads=args.threads,
+                               full_scan=args.full_scan)
         h_out.copy_(out_e2e, non_blocking=True)
         h_t.copy_(t_e2e, non_blocking=True)
     e1.record(stream)
@@ -468,7 +480,8 @@ def our_arm(args, w: wl.Workload) -> int:
             "dtype": "f32", "data": "synthetic",
             "config": dict(workload_config(w, l2_note),
                            parallelism=f"replicas x{world}",
-                           variant=args.variant, plan=plan),
+                           variant=args.variant, full_scan=args.full_scan,
+                           plan=plan),
             "roofline": roof, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "rows/s",
                     "ms_per_step": e2e_ms,

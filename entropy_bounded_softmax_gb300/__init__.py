@@ -14,14 +14,15 @@ from __future__ import annotations
 
 from . import _lib
 from ._lib import (CONSTANTS, cs_check_args, cs_constrained_softmax,
-                   cs_constrained_softmax_variant, cs_get_error, cs_plan_host,
+                   cs_constrained_softmax_ex, cs_get_error, cs_plan_host,
                    cs_plan_launch, cs_probe_ex2, cs_probe_ex2_sink_floats,
-                   cs_status_string, cs_test_wait_timeout, cs_version)
+                   cs_status_string, cs_test_wait_timeout, cs_version,
+                   options)
 
 __all__ = [
     "constrained_softmax", "get_error", "plan", "version", "CsError",
-    "ERROR_BITS", "VARIANTS", "cs_constrained_softmax",
-    "cs_constrained_softmax_variant", "cs_get_error", "cs_plan_launch",
+    "ERROR_BITS", "VARIANTS", "options", "cs_constrained_softmax",
+    "cs_constrained_softmax_ex", "cs_get_error", "cs_plan_launch",
     "cs_plan_host", "cs_check_args", "cs_probe_ex2",
     "cs_probe_ex2_sink_floats", "cs_test_wait_timeout", "cs_version",
     "cs_status_string",
@@ -58,15 +59,16 @@ def constrained_softmax(logits, entropy_bound: float = DEFAULT_ENTROPY_BOUND,
                         t_max: float = DEFAULT_T_MAX,
                         max_iter: int = DEFAULT_MAX_ITER,
                         return_t: bool = False, out=None, t_out=None,
-                        variant: str = "auto", param: int = 0):
+                        variant: str = "auto", param: int = 0,
+                        threads: int = 0, full_scan: bool = False):
     """Entropy-bounded softmax of a CUDA fp32 [batch, num_classes] tensor.
 
     Returns the probabilities (and the per-row temperature if ``return_t``).
     ``out``/``t_out`` may be given to write into existing tensors.  The call
     is asynchronous on the current stream; per-row conditions (NaN/Inf rows,
     unsatisfiable bounds) are read with :func:`get_error`.
-    ``variant``/``param`` force a kernel variant (see
-    ``cs_constrained_softmax_variant``).
+    ``variant``/``param``/``threads``/``full_scan`` are the launch options
+    of ``cs_constrained_softmax_ex`` (defaults: automatic).
     """
     import torch
     if not isinstance(logits, torch.Tensor):
@@ -97,10 +99,10 @@ def constrained_softmax(logits, entropy_bound: float = DEFAULT_ENTROPY_BOUND,
                              "tensor on the logits' device")
         t_ptr = t_out.data_ptr()
     with torch.cuda.device(logits.device):
-        st = cs_constrained_softmax_variant(
+        st = cs_constrained_softmax_ex(
             logits.data_ptr(), out.data_ptr(), batch, num_classes,
             float(entropy_bound), float(t_min), float(t_max), int(max_iter),
-            t_ptr, VARIANTS[variant], int(param),
+            t_ptr, options(VARIANTS[variant], param, threads, int(full_scan)),
             _stream_handle(logits.device))
     if st != 0:
         raise CsError(st, "cs_constrained_softmax")
@@ -121,9 +123,11 @@ def get_error(device=None) -> set[str]:
 
 
 def plan(batch: int, num_classes: int, variant: str = "auto",
-         param: int = 0) -> dict:
+         param: int = 0, threads: int = 0, full_scan: bool = False) -> dict:
     """The launch plan for this shape on the current device."""
-    st, p = cs_plan_launch(batch, num_classes, VARIANTS[variant], param)
+    st, p = cs_plan_launch(batch, num_classes,
+                           options(VARIANTS[variant], param, threads,
+                                   int(full_scan)))
     if st != 0:
         raise CsError(st, "cs_plan_launch")
     return p.as_dict()

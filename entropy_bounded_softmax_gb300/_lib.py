@@ -19,6 +19,15 @@ _lock = threading.Lock()
 _lib: ctypes.CDLL | None = None
 
 
+class cs_options(ctypes.Structure):
+    _fields_ = [
+        ("variant", ctypes.c_int32),
+        ("param", ctypes.c_int32),
+        ("threads", ctypes.c_int32),
+        ("full_scan", ctypes.c_int32),
+    ]
+
+
 class cs_plan(ctypes.Structure):
     _fields_ = [
         ("variant", ctypes.c_int32),
@@ -29,6 +38,8 @@ class cs_plan(ctypes.Structure):
         ("threads_per_cta", ctypes.c_int32),
         ("smem_bytes", ctypes.c_int32),
         ("ctas_per_sm", ctypes.c_int32),
+        ("warp_buffer", ctypes.c_int32),
+        ("prune_k", ctypes.c_float),
         ("grid_ctas", ctypes.c_int64),
     ]
 
@@ -58,14 +69,14 @@ _F32 = ctypes.c_float
 _SIGNATURES = {
     "cs_constrained_softmax": (_I32, [_VP, _VP, _I64, _I32, _F32, _F32, _F32,
                                       _I32, _VP, _VP]),
-    "cs_constrained_softmax_variant": (_I32, [_VP, _VP, _I64, _I32, _F32,
-                                              _F32, _F32, _I32, _VP, _I32,
-                                              _I32, _VP]),
+    "cs_constrained_softmax_ex": (_I32, [_VP, _VP, _I64, _I32, _F32, _F32,
+                                         _F32, _I32, _VP,
+                                         ctypes.POINTER(cs_options), _VP]),
     "cs_get_error": (_I32, [ctypes.POINTER(_I32), _VP]),
-    "cs_plan_launch": (_I32, [_I64, _I32, _I32, _I32,
+    "cs_plan_launch": (_I32, [_I64, _I32, ctypes.POINTER(cs_options),
                               ctypes.POINTER(cs_plan)]),
-    "cs_plan_host": (_I32, [_I64, _I32, _I32, _I32, _I32, _I32, _I32, _I32,
-                            ctypes.POINTER(cs_plan)]),
+    "cs_plan_host": (_I32, [_I64, _I32, ctypes.POINTER(cs_options), _I32,
+                            _I32, _I32, _I32, ctypes.POINTER(cs_plan)]),
     "cs_check_args": (_I32, [_VP, _VP, _I64, _I32, _F32, _F32, _F32, _I32,
                              _VP]),
     "cs_probe_ex2": (_I32, [_VP, _I32, ctypes.POINTER(_I64), _VP]),
@@ -110,12 +121,21 @@ def cs_constrained_softmax(logits, out, batch, num_classes, entropy_bound,
                                          max_iter, t_out, stream)
 
 
-def cs_constrained_softmax_variant(logits, out, batch, num_classes,
-                                   entropy_bound, t_min, t_max, max_iter,
-                                   t_out, variant, param, stream) -> int:
-    return load().cs_constrained_softmax_variant(
+def options(variant=0, param=0, threads=0, full_scan=0):
+    """A cs_options struct (all zero = automatic)."""
+    return cs_options(int(variant), int(param), int(threads), int(full_scan))
+
+
+def _opt_ref(opt):
+    return None if opt is None else ctypes.byref(opt)
+
+
+def cs_constrained_softmax_ex(logits, out, batch, num_classes, entropy_bound,
+                              t_min, t_max, max_iter, t_out, opt,
+                              stream) -> int:
+    return load().cs_constrained_softmax_ex(
         logits, out, batch, num_classes, entropy_bound, t_min, t_max,
-        max_iter, t_out, variant, param, stream)
+        max_iter, t_out, _opt_ref(opt), stream)
 
 
 def cs_get_error(stream) -> tuple[int, int]:
@@ -124,17 +144,17 @@ def cs_get_error(stream) -> tuple[int, int]:
     return st, mask.value
 
 
-def cs_plan_launch(batch, num_classes, variant=0, param=0):
+def cs_plan_launch(batch, num_classes, opt=None):
     p = cs_plan()
-    st = load().cs_plan_launch(batch, num_classes, variant, param,
+    st = load().cs_plan_launch(batch, num_classes, _opt_ref(opt),
                                ctypes.byref(p))
     return st, p
 
 
-def cs_plan_host(batch, num_classes, variant, param, sm_count,
-                 smem_per_block_optin, smem_per_sm, max_cluster):
+def cs_plan_host(batch, num_classes, opt, sm_count, smem_per_block_optin,
+                 smem_per_sm, max_cluster):
     p = cs_plan()
-    st = load().cs_plan_host(batch, num_classes, variant, param, sm_count,
+    st = load().cs_plan_host(batch, num_classes, _opt_ref(opt), sm_count,
                              smem_per_block_optin, smem_per_sm, max_cluster,
                              ctypes.byref(p))
     return st, p

@@ -125,13 +125,11 @@ cs_status plan_rowgroup(int64_t batch, int32_t C, int32_t param,
     }
     e4 = next_pow2(ceil_div(q, G));
     if (e4 > kRowgroupMaxE4) return CS_ERR_OOM;
+    *p = cs_plan{};
     p->variant = CS_VARIANT_ROWGROUP;
     p->lanes_per_row = G;
     p->elems_per_lane = 4 * e4;
-    p->cluster_size = 0;
-    p->slice_len = 0;
     p->threads_per_cta = kRowgroupThreads;
-    p->smem_bytes = 0;
     p->ctas_per_sm = 2048 / kRowgroupThreads;
     int64_t blocks = ceil_div(batch * G, kRowgroupThreads);
     if (blocks > kMaxGridX) blocks = kMaxGridX;
@@ -139,42 +137,56 @@ cs_status plan_rowgroup(int64_t batch, int32_t C, int32_t param,
     return CS_OK;
 }
 
-cs_status plan_cluster(int64_t batch, int32_t C, int32_t param, int sm_count,
-                       int smem_optin, int smem_per_sm, int max_cluster,
-                       cs_plan* p) {
-    (void)sm_count;
-    auto fits = [&](int n, int64_t* L, int* threads, int64_t* smem) {
-        *L = ceil_div(ceil_div(C, n), 4) * 4;
-        *threads = cs::cluster_threads_for(*L);
-        *smem = cs::cluster_smem_bytes(*L, *threads, n);
-        return *smem <= smem_optin;
-    };
-    int n = 0;
-    int64_t L = 0, smem = 0;
-    int threads = 0;
-    if (param == 0) {
-        for (int c = 1; c <= max_cluster; ++c) {
-            if (fits(c, &L, &threads, &smem)) {
-                n = c;
-                break;
-            }
-        }
-        if (n == 0) return CS_ERR_OOM;
-    } else {
-        if (param < 1 || param > cs::kMaxCluster) return CS_ERR_INVALID_ARG;
-        if (param > max_cluster) return CS_ERR_INVALID_ARG;
-        n = param;
-        if (!fits(n, &L, &threads, &smem)) return CS_ERR_OOM;
+// Cluster plan for n CTAs per row: slice, threads, active-set buffer and
+// shared memory.  Returns false if it does not fit smem_optin.
+bool cluster_geometry(int32_t C, int n, int threads_req, bool prune,
+                      int smem_optin, cs_plan* p) {
+    const int64_t L = ceil_div(ceil_div(C, n), 4) * 4;
+    const int threads = threads_req ? threads_req : cs::cluster_threads_for(L);
+    const int warps = threads / 32;
+    const int64_t base = cs::cluster_smem_bytes(L, threads, n, 0);
+    if (base > smem_optin) return false;
+    int cap = 0;
+    if (prune) {
+        int64_t room = (smem_optin - base) / (4 * warps);
+        room = (room / 32) * 32;
+        if (room > cs::kMaxWarpBuffer) room = cs::kMaxWarpBuffer;
+        if (room >= cs::kMinWarpBuffer) cap = static_cast<int>(room);
     }
-    p->variant = CS_VARIANT_CLUSTER;
-    p->lanes_per_row = 0;
-    p->elems_per_lane = 0;
     p->cluster_size = n;
     p->slice_len = static_cast<int32_t>(L);
     p->threads_per_cta = threads;
-    p->smem_bytes = static_cast<int32_t>(smem);
-    int by_smem = static_cast<int>(smem_per_sm / (smem + 1024));
-    int by_threads = 2048 / threads;
+    p->warp_buffer = cap;
+    p->prune_k = cap > 0 ? cs::prune_threshold(C) : 0.0f;
+    p->smem_bytes = static_cast<int32_t>(cs::cluster_smem_bytes(L, threads, n, cap));
+    return true;
+}
+
+cs_status plan_cluster(int64_t batch, int32_t C, const cs_options& o,
+                       int sm_count, int smem_optin, int smem_per_sm,
+                       int max_cluster, cs_plan* p) {
+    (void)sm_count;
+    if (o.threads != 0 &&
+        (o.threads < 64 || o.threads > cs::kClusterMaxThreads || o.threads % 32))
+        return CS_ERR_INVALID_ARG;
+    if (o.full_scan != 0 && o.full_scan != 1) return CS_ERR_INVALID_ARG;
+    const bool prune = o.full_scan == 0;
+    *p = cs_plan{};
+    p->variant = CS_VARIANT_CLUSTER;
+    if (o.param == 0) {
+        bool ok = false;
+        for (int c = 1; c <= max_cluster && !ok; ++c)
+            ok = cluster_geometry(C, c, o.threads, prune, smem_optin, p);
+        if (!ok) return CS_ERR_OOM;
+    } else {
+        if (o.param < 1 || o.param > cs::kMaxCluster) return CS_ERR_INVALID_ARG;
+        if (o.param > max_cluster) return CS_ERR_INVALID_ARG;
+        if (!cluster_geometry(C, o.param, o.threads, prune, smem_optin, p))
+            return CS_ERR_OOM;
+    }
+    const int n = p->cluster_size;
+    const int by_smem = static_cast<int>(smem_per_sm / (p->smem_bytes + 1024));
+    const int by_threads = 2048 / p->threads_per_cta;
     p->ctas_per_sm = by_smem < by_threads ? by_smem : by_threads;
     int64_t rows = batch;
     const int64_t max_rows = kMaxGridX / n;
@@ -207,8 +219,8 @@ cs_status cs_check_args(const float* logits, const float* out, int64_t batch,
     return CS_OK;
 }
 
-cs_status cs_plan_host(int64_t batch, int32_t num_classes, int32_t variant,
-                       int32_t param, int32_t sm_count,
+cs_status cs_plan_host(int64_t batch, int32_t num_classes,
+                       const cs_options* options, int32_t sm_count,
                        int32_t smem_per_block_optin, int32_t smem_per_sm,
                        int32_t max_cluster, cs_plan* plan) {
     if (!plan) return CS_ERR_INVALID_ARG;
@@ -218,35 +230,39 @@ cs_status cs_plan_host(int64_t batch, int32_t num_classes, int32_t variant,
         max_cluster < 1)
         return CS_ERR_INVALID_ARG;
     if (max_cluster > cs::kMaxCluster) max_cluster = cs::kMaxCluster;
-    if (variant == CS_VARIANT_AUTO) {
-        if (param != 0) return CS_ERR_INVALID_ARG;
-        variant = num_classes <= kAutoRowgroupMaxClasses ? CS_VARIANT_ROWGROUP
-                                                         : CS_VARIANT_CLUSTER;
+    cs_options o = options ? *options : cs_options{};
+    if (o.variant == CS_VARIANT_AUTO) {
+        if (o.param != 0) return CS_ERR_INVALID_ARG;
+        o.variant = num_classes <= kAutoRowgroupMaxClasses ? CS_VARIANT_ROWGROUP
+                                                           : CS_VARIANT_CLUSTER;
     }
-    if (variant == CS_VARIANT_ROWGROUP)
-        return plan_rowgroup(batch, num_classes, param, plan);
-    if (variant == CS_VARIANT_CLUSTER)
-        return plan_cluster(batch, num_classes, param, sm_count,
+    if (o.variant == CS_VARIANT_ROWGROUP) {
+        if (o.threads != 0 || (o.full_scan != 0 && o.full_scan != 1))
+            return CS_ERR_INVALID_ARG;
+        return plan_rowgroup(batch, num_classes, o.param, plan);
+    }
+    if (o.variant == CS_VARIANT_CLUSTER)
+        return plan_cluster(batch, num_classes, o, sm_count,
                             smem_per_block_optin, smem_per_sm, max_cluster,
                             plan);
     return CS_ERR_INVALID_ARG;
 }
 
-cs_status cs_plan_launch(int64_t batch, int32_t num_classes, int32_t variant,
-                         int32_t param, cs_plan* plan) {
+cs_status cs_plan_launch(int64_t batch, int32_t num_classes,
+                         const cs_options* options, cs_plan* plan) {
     DeviceInfo* d = nullptr;
     const cs_status st = device_info(&d);
     if (st != CS_OK) return st;
-    return cs_plan_host(batch, num_classes, variant, param, d->sm_count,
+    return cs_plan_host(batch, num_classes, options, d->sm_count,
                         d->smem_optin, d->smem_per_sm, d->max_cluster, plan);
 }
 
-cs_status cs_constrained_softmax_variant(const float* logits, float* out,
-                                         int64_t batch, int32_t num_classes,
-                                         float entropy_bound, float t_min,
-                                         float t_max, int32_t max_iter,
-                                         float* t_out, int32_t variant,
-                                         int32_t param, void* stream) {
+cs_status cs_constrained_softmax_ex(const float* logits, float* out,
+                                    int64_t batch, int32_t num_classes,
+                                    float entropy_bound, float t_min,
+                                    float t_max, int32_t max_iter,
+                                    float* t_out, const cs_options* options,
+                                    void* stream) {
     cs_status st = cs_check_args(logits, out, batch, num_classes,
                                  entropy_bound, t_min, t_max, max_iter, t_out);
     if (st != CS_OK) return st;
@@ -255,8 +271,8 @@ cs_status cs_constrained_softmax_variant(const float* logits, float* out,
     st = device_info(&d);
     if (st != CS_OK) return st;
     cs_plan p;
-    st = cs_plan_host(batch, num_classes, variant, param, d->sm_count,
-                      d->smem_optin, d->smem_per_sm, d->max_cluster, &p);
+    st = cs_plan_host(batch, num_classes, options, d->sm_count, d->smem_optin,
+                      d->smem_per_sm, d->max_cluster, &p);
     if (st != CS_OK) return st;
 
     cs::RowTask task;
@@ -270,6 +286,7 @@ cs_status cs_constrained_softmax_variant(const float* logits, float* out,
     task.entropy_bound = entropy_bound;
     task.t_min = t_min;
     task.hi0 = t_max < 1.0f ? t_max : 1.0f;
+    task.prune_k = p.prune_k;
     task.wait_limit_ns = cs::kWaitLimitNs;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -278,7 +295,8 @@ cs_status cs_constrained_softmax_variant(const float* logits, float* out,
         e = cs::launch_rowgroup(task, p.lanes_per_row, p.elems_per_lane, s);
     } else {
         e = cs::launch_cluster(task, p.cluster_size, p.slice_len,
-                               p.threads_per_cta, p.smem_bytes, p.grid_ctas, s);
+                               p.threads_per_cta, p.warp_buffer, p.smem_bytes,
+                               p.grid_ctas, s);
     }
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -291,10 +309,9 @@ cs_status cs_constrained_softmax(const float* logits, float* out,
                                  int64_t batch, int32_t num_classes,
                                  float entropy_bound, float t_min, float t_max,
                                  int32_t max_iter, float* t_out, void* stream) {
-    return cs_constrained_softmax_variant(logits, out, batch, num_classes,
-                                          entropy_bound, t_min, t_max,
-                                          max_iter, t_out, CS_VARIANT_AUTO, 0,
-                                          stream);
+    return cs_constrained_softmax_ex(logits, out, batch, num_classes,
+                                     entropy_bound, t_min, t_max, max_iter,
+                                     t_out, nullptr, stream);
 }
 
 cs_status cs_get_error(int32_t* code_mask, void* stream) {

@@ -40,6 +40,72 @@ __device__ __forceinline__ float rcp_approx(float x) {
     return y;
 }
 
+// Packed fp32x2 arithmetic (one instruction for two lanes of data).
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n"
+        " mov.b64 rb, {%4, %5};\n mul.rn.f32x2 rd, ra, rb;\n"
+        " mov.b64 {%0, %1}, rd;\n}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n"
+        " mov.b64 rb, {%4, %5};\n add.rn.f32x2 rd, ra, rb;\n"
+        " mov.b64 {%0, %1}, rd;\n}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n"
+        " mov.b64 rb, {%4, %5};\n mov.b64 rc, {%6, %7};\n"
+        " fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+// Accumulators of S = sum 2^(beta y) and V = sum y 2^(beta y), four lanes
+// each as two packed pairs.
+struct SV4 {
+    float2 s01, s23, v01, v23;
+    __device__ __forceinline__ void zero() {
+        s01 = s23 = v01 = v23 = make_float2(0.f, 0.f);
+    }
+    // Adds the four classes of y at inverse temperature beta (b2 = {beta,
+    // beta}).
+    __device__ __forceinline__ void add(float4 y, float2 b2) {
+        const float2 y01 = make_float2(y.x, y.y);
+        const float2 y23 = make_float2(y.z, y.w);
+        const float2 x01 = mul2(y01, b2);
+        const float2 x23 = mul2(y23, b2);
+        const float2 e01 = make_float2(ex2(x01.x), ex2(x01.y));
+        const float2 e23 = make_float2(ex2(x23.x), ex2(x23.y));
+        s01 = add2(s01, e01);
+        s23 = add2(s23, e23);
+        v01 = fma2(e01, y01, v01);
+        v23 = fma2(e23, y23, v23);
+    }
+    __device__ __forceinline__ float2 total() const {
+        const float2 s = add2(s01, s23);
+        const float2 v = add2(v01, v23);
+        return make_float2(s.x + s.y, v.x + v.y);
+    }
+};
+
+// Entropy test without a division: with H = ln 2 (log2 S - beta V / S) and
+// S > 0, H > bound  <=>  S (log2 S - bound log2 e) - beta V > 0.
+// bound_bits = bound * log2(e).
+__device__ __forceinline__ bool entropy_above(float2 sv, float beta,
+                                              float bound_bits) {
+    const float t = fmaf(sv.x, lg2_approx(sv.x) - bound_bits, -beta * sv.y);
+    return t > 0.0f;
+}
+
 // ------------------------------------------------------------ shared memory
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -79,13 +145,17 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
                  :: "r"(smem_addr(bar)) : "memory");
 }
 
+// One test of the phase; a thread whose phase is not complete may sleep in
+// hardware for up to kSuspendHintNs or until the phase completes.
+constexpr uint32_t kSuspendHintNs = 100000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n .reg .pred p;\n"
-        " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
         " selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+        : "=r"(ok) : "r"(bar), "r"(parity), "r"(kSuspendHintNs) : "memory");
     return ok != 0;
 }
 
@@ -98,7 +168,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
     const uint64_t t0 = global_timer_ns();
     for (uint32_t i = 1; i < (1u << 31); ++i) {
         if (mbar_try_wait(a, parity)) return true;
-        if ((i & 31u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
+        if ((i & 7u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
     }
     return false;
 }

@@ -33,6 +33,7 @@ struct RowTask {
     float entropy_bound;
     float t_min;
     float hi0;             // min(1, t_max): upper end of the search
+    float prune_k;         // active-set threshold K (0: no pruning)
     uint64_t wait_limit_ns;
 };
 
@@ -41,15 +42,23 @@ constexpr int kMaxCluster = 16;
 constexpr int kLoadChunks = 8;        // bulk copies per CTA slice
 constexpr int kClusterMaxThreads = 1024;
 
+// Per-warp active-set buffer of the cluster kernel: up to this many floats
+// (8 per lane); below kMinWarpBuffer pruning is off.
+constexpr int kMaxWarpBuffer = 256;
+constexpr int kMinWarpBuffer = 64;
+
 // Dynamic shared memory of the cluster kernel for a slice of `slice_len`
-// classes, `threads` threads and cluster size `n`.
-inline int64_t cluster_smem_bytes(int64_t slice_len, int threads, int n) {
+// classes, `threads` threads, cluster size `n` and `cap_w` floats of
+// active-set buffer per warp.
+inline int64_t cluster_smem_bytes(int64_t slice_len, int threads, int n,
+                                  int cap_w) {
     const int64_t warps = threads / 32;
     const int64_t slots = 2 * warps * n * 8;            // exchange buffers
     const int64_t bars = (2 + kLoadChunks) * 8;         // mbarriers
     const int64_t head = ((slots + bars + 127) / 128) * 128;
+    const int64_t wbuf = warps * cap_w * 4;
     const int64_t row = ((slice_len + 8 + 3) / 4) * 16;  // pad + tail room
-    return head + row;
+    return head + wbuf + row;
 }
 
 inline int cluster_threads_for(int64_t slice_len) {
@@ -61,11 +70,19 @@ inline int cluster_threads_for(int64_t slice_len) {
     return static_cast<int>(t);
 }
 
+// Active-set threshold K for rows of C classes: 36 + ceil(log2 C).
+inline float prune_threshold(int64_t C) {
+    int lg = 0;
+    while ((int64_t{1} << lg) < C) ++lg;
+    return static_cast<float>(36 + lg);
+}
+
 cudaError_t launch_rowgroup(const RowTask& task, int lanes_per_row,
                             int elems_per_lane, cudaStream_t stream);
 cudaError_t launch_cluster(const RowTask& task, int cluster_size,
-                           int slice_len, int threads, int smem_bytes,
-                           int64_t grid_ctas, cudaStream_t stream);
+                           int slice_len, int threads, int cap_w,
+                           int smem_bytes, int64_t grid_ctas,
+                           cudaStream_t stream);
 cudaError_t launch_probe_ex2(float* sink, int iters, int blocks, int threads,
                              cudaStream_t stream);
 cudaError_t launch_wait_timeout(unsigned int* err, uint64_t limit_ns,

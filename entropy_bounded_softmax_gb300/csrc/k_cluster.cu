@@ -12,12 +12,23 @@
 //           check, exchanged across the cluster;
 //   T = 1   one pass turns the slice into y_i = (l_i - m) log2(e) in place
 //           and sums S = sum 2^y_i and V = sum y_i 2^y_i;
-//   search  each bisection step is one pass over y at beta = 1/mid giving
+//   search  each bisection step is one pass at beta = 1/mid giving
 //           S(beta) = sum 2^(beta y_i) and V(beta) = sum y_i 2^(beta y_i);
 //           with p_i = 2^(beta y_i) / S the entropy in nats is
-//           H = ln 2 * (log2 S - beta V / S);
+//           H = ln 2 (log2 S - beta V / S), and H > bound is decided as
+//           S (log2 S - bound log2 e) - beta V > 0;
 //   output  p_i = 2^(beta_lo y_i) / S(lo), reusing S(lo) from the step that
 //           set lo, written with 128-bit streaming stores.
+//
+// Active set.  Every later step evaluates at beta = 1/mid >= 1/hi, so a class
+// with y_i < -K hi contributes less than 2^-K to S (which is >= 1: the
+// maximum contributes 1) at every remaining step.  With K = 36 + log2(C)
+// all such classes together change S and beta V by less than 2^-30 of
+// their values, far below fp32 resolution.  After hi drops, each warp
+// compacts its still-active classes (ballot + popc) into its own buffer in
+// shared memory and later steps read only that buffer; the full slice stays
+// in place for the output pass.  A warp whose active classes overflow its
+// buffer keeps scanning the slice and tries again after hi drops again.
 //
 // Reductions: every warp reduces its (S, V) with shuffles and pushes the
 // pair into an exchange slot of every CTA of the cluster (st.async with an
@@ -39,6 +50,10 @@ namespace cs {
 namespace {
 
 using namespace csd;
+
+__device__ __forceinline__ float4 floor4() {
+    return make_float4(kYFloor, kYFloor, kYFloor, kYFloor);
+}
 
 // Geometry of one CTA's slice in shared memory.  Element j of the slice
 // lives at row[pad + j], so 16-byte aligned global addresses land on
@@ -79,35 +94,45 @@ __device__ __forceinline__ int chunk_begin(const Slice& s, int nch, int c) {
     return s.qb0 + static_cast<int>((static_cast<int64_t>(body) * c) / nch);
 }
 
+// Exchange state of one CTA.
+struct Exch {
+    float2* xs;       // [2][warps * n] slots
+    uint64_t* xbar;   // [2] mbarriers
+    uint32_t xk;      // exchanges so far
+    int warps;
+    int n;
+    uint32_t rank;
+    uint64_t limit;
+    bool dead;
+};
+
 // One exchange across the warps of the CTA and the CTAs of the cluster.
-// `v` is this thread's partial; returns the cluster-wide sum (or max).
+// `v` is this thread's partial; returns the cluster-wide sum (or max),
+// bit-identical in every thread of the cluster.
 template <bool CLUSTER, bool IS_MAX>
-__device__ __forceinline__ float2 exchange(float2 v, float2* xs,
-                                           uint64_t* xbar, uint32_t& xk,
-                                           int warps, int n, uint32_t rank,
-                                           uint64_t limit, bool& dead) {
+__device__ __forceinline__ float2 exchange(float2 v, Exch& x) {
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     v = IS_MAX ? warp_max2(v) : warp_sum2(v);
-    const uint32_t buf = xk & 1u;
-    const uint32_t parity = (xk >> 1) & 1u;
-    ++xk;
-    const int nslots = warps * n;
-    float2* slots = xs + buf * nslots;
-    if (!dead) {
+    const uint32_t buf = x.xk & 1u;
+    const uint32_t parity = (x.xk >> 1) & 1u;
+    ++x.xk;
+    const int nslots = x.warps * x.n;
+    float2* slots = x.xs + buf * nslots;
+    if (!x.dead) {
         if (CLUSTER) {
-            if (threadIdx.x == 0) mbar_arrive_expect_tx(&xbar[buf], nslots * 8);
-            if (lane < n) {
+            if (threadIdx.x == 0) mbar_arrive_expect_tx(&x.xbar[buf], nslots * 8);
+            if (lane < x.n) {
                 const uint32_t dst = map_to_rank(
-                    smem_addr(&slots[rank * warps + warp]), lane);
-                const uint32_t bar = map_to_rank(smem_addr(&xbar[buf]), lane);
+                    smem_addr(&slots[x.rank * x.warps + warp]), lane);
+                const uint32_t bar = map_to_rank(smem_addr(&x.xbar[buf]), lane);
                 push_pair(dst, v.x, v.y, bar);
             }
         } else if (lane == 0) {
             slots[warp] = v;
-            mbar_arrive(&xbar[buf]);
+            mbar_arrive(&x.xbar[buf]);
         }
-        if (!mbar_wait(&xbar[buf], parity, limit)) dead = true;
+        if (!mbar_wait(&x.xbar[buf], parity, x.limit)) x.dead = true;
     }
     float2 acc = IS_MAX ? make_float2(-INFINITY, 0.0f) : make_float2(0.0f, 0.0f);
     for (int j = lane; j < nslots; j += 32) {
@@ -123,42 +148,99 @@ __device__ __forceinline__ float2 exchange(float2 v, float2* xs,
     return IS_MAX ? warp_max2(acc) : warp_sum2(acc);
 }
 
-// One pass over this thread's float4s of the slice: returns the partial
-// (S, V) at inverse temperature beta.  With TRANSFORM the slice still holds
-// logits and is rewritten in place as y = max((l - m) log2 e, floor).
-template <bool TRANSFORM>
-__device__ __forceinline__ float2 pass_sv(float4* row4, int q4, float beta,
-                                          float m) {
-    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-    float v0 = 0.f, v1 = 0.f, v2 = 0.f, v3 = 0.f;
+// T = 1 pass: rewrites this thread's float4s of the slice as
+// y = max((l - m) log2 e, floor) and returns the partial (S, V) at beta = 1.
+__device__ __forceinline__ float2 transform_pass(float4* row4, int q4,
+                                                 float m) {
+    SV4 acc;
+    acc.zero();
+    const float2 one = make_float2(1.0f, 1.0f);
     for (int q = threadIdx.x; q < q4; q += blockDim.x) {
         float4 y = row4[q];
-        if (TRANSFORM) {
-            y.x = fmaxf((y.x - m) * kLog2e, kYFloor);
-            y.y = fmaxf((y.y - m) * kLog2e, kYFloor);
-            y.z = fmaxf((y.z - m) * kLog2e, kYFloor);
-            y.w = fmaxf((y.w - m) * kLog2e, kYFloor);
-            row4[q] = y;
-        }
-        const float e0 = ex2(y.x * beta);
-        const float e1 = ex2(y.y * beta);
-        const float e2 = ex2(y.z * beta);
-        const float e3 = ex2(y.w * beta);
-        s0 += e0;
-        s1 += e1;
-        s2 += e2;
-        s3 += e3;
-        v0 = fmaf(e0, y.x, v0);
-        v1 = fmaf(e1, y.y, v1);
-        v2 = fmaf(e2, y.z, v2);
-        v3 = fmaf(e3, y.w, v3);
+        y.x = fmaxf((y.x - m) * kLog2e, kYFloor);
+        y.y = fmaxf((y.y - m) * kLog2e, kYFloor);
+        y.z = fmaxf((y.z - m) * kLog2e, kYFloor);
+        y.w = fmaxf((y.w - m) * kLog2e, kYFloor);
+        row4[q] = y;
+        acc.add(y, one);
     }
-    return make_float2((s0 + s1) + (s2 + s3), (v0 + v1) + (v2 + v3));
+    return acc.total();
 }
 
-// Entropy in nats from the cluster-wide (S, V) at inverse temperature beta.
-__device__ __forceinline__ float entropy_nats(float2 sv, float beta) {
-    return kLn2 * (log2f(sv.x) - (beta * sv.y) / sv.x);
+// Full pass over this thread's float4s of the slice at inverse temperature
+// beta.  Thread t owns float4s t, t + nt, ...; the loop runs a warp-uniform
+// number of times (two float4s per trip) so that GATHER can use warp votes.
+// GATHER: also appends every class with y >= thr to the warp's buffer wb
+// (capacity cap); *cnt returns the warp's count, > cap on overflow.
+template <bool GATHER>
+__device__ __forceinline__ float2 slice_pass(const float4* row4, int q4,
+                                             float beta, float thr, float* wb,
+                                             int cap, int* cnt) {
+    SV4 acc;
+    acc.zero();
+    const float2 b2 = make_float2(beta, beta);
+    const int nt = blockDim.x;
+    const int lane = threadIdx.x & 31;
+    const int warp_base = threadIdx.x & ~31;
+    const unsigned lt = (1u << lane) - 1u;
+    int cw = 0;
+    for (int qb = warp_base; qb < q4; qb += 2 * nt) {
+        const int qa = qb + lane;
+        const int qc = qa + nt;
+        const float4 ya = qa < q4 ? row4[qa] : floor4();
+        const float4 yc = qc < q4 ? row4[qc] : floor4();
+        acc.add(ya, b2);
+        acc.add(yc, b2);
+        if (GATHER && cw <= cap) {
+            const float v[8] = {ya.x, ya.y, ya.z, ya.w, yc.x, yc.y, yc.z, yc.w};
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const bool a = v[k] >= thr;
+                const unsigned msk = __ballot_sync(0xffffffffu, a);
+                const int pos = cw + __popc(msk & lt);
+                if (a && pos < cap) wb[pos] = v[k];
+                cw += __popc(msk);
+            }
+        }
+    }
+    if (GATHER) {
+        *cnt = cw;
+        __syncwarp();
+    }
+    return acc.total();
+}
+
+// Pass over the warp's buffer of active classes.  RECOMPACT: also drops the
+// classes below thr, compacting the buffer in place (entries only move to
+// lower positions, and every lane reads its entry of a round before any
+// lane writes).
+template <bool RECOMPACT>
+__device__ __forceinline__ float2 buffer_pass(float* wb, int* cnt, float beta,
+                                              float thr) {
+    const int lane = threadIdx.x & 31;
+    const unsigned lt = (1u << lane) - 1u;
+    const int c = *cnt;
+    float s = 0.0f, v = 0.0f;
+    int nc = 0;
+    for (int j0 = 0; j0 < c; j0 += 32) {
+        const int j = j0 + lane;
+        const float y = j < c ? wb[j] : kYFloor;
+        const float e = ex2(y * beta);
+        s += e;
+        v = fmaf(e, y, v);
+        if (RECOMPACT) {
+            const bool a = j < c && y >= thr;
+            const unsigned msk = __ballot_sync(0xffffffffu, a);
+            __syncwarp();
+            if (a) wb[nc + __popc(msk & lt)] = y;
+            nc += __popc(msk);
+        }
+    }
+    if (RECOMPACT) {
+        *cnt = nc;
+        __syncwarp();
+    }
+    return make_float2(s, v);
 }
 
 __device__ __forceinline__ void store_scalar_lanes(float* dst, int q, int pad,
@@ -178,14 +260,17 @@ __device__ __forceinline__ void write_out(const float4* row4, const Slice& s,
                                           bool zero) {
     const int pad_o = static_cast<int>((reinterpret_cast<uintptr_t>(dst) >> 2) & 3);
     const bool vec = pad_o == s.pad;
+    const float2 b2 = make_float2(beta, beta);
+    const float2 i2 = make_float2(inv_s, inv_s);
     for (int q = threadIdx.x; q < s.q4; q += blockDim.x) {
         float4 p = make_float4(0.f, 0.f, 0.f, 0.f);
         if (!zero) {
             const float4 y = row4[q];
-            p.x = ex2(y.x * beta) * inv_s;
-            p.y = ex2(y.y * beta) * inv_s;
-            p.z = ex2(y.z * beta) * inv_s;
-            p.w = ex2(y.w * beta) * inv_s;
+            const float2 x01 = mul2(make_float2(y.x, y.y), b2);
+            const float2 x23 = mul2(make_float2(y.z, y.w), b2);
+            const float2 p01 = mul2(make_float2(ex2(x01.x), ex2(x01.y)), i2);
+            const float2 p23 = mul2(make_float2(ex2(x23.x), ex2(x23.y)), i2);
+            p = make_float4(p01.x, p01.y, p23.x, p23.y);
         }
         if (vec && q >= s.qb0 && q < s.qb1) {
             __stcs(reinterpret_cast<float4*>(dst + (4 * q - s.pad)), p);
@@ -195,12 +280,49 @@ __device__ __forceinline__ void write_out(const float4* row4, const Slice& s,
     }
 }
 
+// Per-warp choice of what the next pass reads.
+struct ActiveSet {
+    float* wb;          // this warp's buffer
+    int cap;            // its capacity (0: pruning off)
+    int cnt;            // classes in the buffer
+    bool in_buffer;     // the warp reads its buffer instead of the slice
+    bool refilter;      // hi dropped since the buffer was last filtered
+    float thr;          // y >= thr is active (thr = -K hi)
+};
+
+template <bool CLUSTER>
+__device__ __forceinline__ float2 search_pass(const float4* row4, int q4,
+                                              float beta, ActiveSet& a,
+                                              Exch& x) {
+    float2 part;
+    if (a.in_buffer) {
+        if (a.refilter) {
+            part = buffer_pass<true>(a.wb, &a.cnt, beta, a.thr);
+            a.refilter = false;
+        } else {
+            part = buffer_pass<false>(a.wb, &a.cnt, beta, a.thr);
+        }
+    } else if (a.refilter) {
+        int c = 0;
+        part = slice_pass<true>(row4, q4, beta, a.thr, a.wb, a.cap, &c);
+        a.refilter = false;
+        if (c <= a.cap) {
+            a.in_buffer = true;
+            a.cnt = c;
+        }
+    } else {
+        part = slice_pass<false>(row4, q4, beta, 0.0f, nullptr, 0, nullptr);
+    }
+    return exchange<CLUSTER, false>(part, x);
+}
+
 template <bool CLUSTER>
 __global__ void __launch_bounds__(kClusterMaxThreads, 1)
-cluster_kernel(RowTask t, int n, int slice_len) {
+cluster_kernel(RowTask t, int n, int slice_len, int cap_w) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int nt = blockDim.x;
     const int warps = nt >> 5;
+    const int warp = threadIdx.x >> 5;
     const uint32_t rank = CLUSTER ? cluster_ctarank() : 0u;
     const int64_t cid = blockIdx.x / n;
     const int64_t ncl = gridDim.x / n;
@@ -209,7 +331,8 @@ cluster_kernel(RowTask t, int n, int slice_len) {
     uint64_t* xbar = reinterpret_cast<uint64_t*>(smem + 2 * nslots * 8);
     uint64_t* lbar = xbar + 2;
     const int head_bytes = ((2 * nslots * 8 + (2 + kLoadChunks) * 8 + 127) / 128) * 128;
-    float* row = reinterpret_cast<float*>(smem + head_bytes);
+    float* wbuf = reinterpret_cast<float*>(smem + head_bytes);
+    float* row = wbuf + warps * cap_w;
     float4* row4 = reinterpret_cast<float4*>(row);
 
     if (threadIdx.x == 0) {
@@ -225,10 +348,9 @@ cluster_kernel(RowTask t, int n, int slice_len) {
     const int64_t s0 = static_cast<int64_t>(rank) * slice_len;
     const int len = static_cast<int>(max(static_cast<int64_t>(0),
                                          min(static_cast<int64_t>(slice_len), C - s0)));
-    const float bound = t.entropy_bound;
-    uint32_t xk = 0;           // exchanges so far (slot buffer, phase)
+    const float bound_bits = t.entropy_bound * kLog2e;
+    Exch x{xs, xbar, 0u, warps, n, rank, t.wait_limit_ns, false};
     uint32_t lphase = 0;       // parity bit per load chunk
-    bool dead = false;         // this thread's waits timed out
     bool reported = false;
 
     for (int64_t r = cid; r < t.batch; r += ncl) {
@@ -239,7 +361,7 @@ cluster_kernel(RowTask t, int n, int slice_len) {
 
         // Stage: thread 0 issues the bulk copies; threads 0-7 fetch the
         // ragged head/tail float4s with plain loads.
-        if (threadIdx.x == 0 && !dead) {
+        if (threadIdx.x == 0 && !x.dead) {
             fence_proxy_async_smem();
             for (int c = 0; c < nch; ++c) {
                 const int qa = chunk_begin(s, nch, c);
@@ -269,8 +391,8 @@ cluster_kernel(RowTask t, int n, int slice_len) {
 
         // Max pass, chunk by chunk as the copies land.
         for (int c = 0; c < nch; ++c) {
-            if (!dead && !mbar_wait(&lbar[c], (lphase >> c) & 1u, t.wait_limit_ns))
-                dead = true;
+            if (!x.dead && !mbar_wait(&lbar[c], (lphase >> c) & 1u, x.limit))
+                x.dead = true;
             lphase ^= 1u << c;
             const int qa = chunk_begin(s, nch, c);
             const int qz = chunk_begin(s, nch, c + 1);
@@ -297,9 +419,7 @@ cluster_kernel(RowTask t, int n, int slice_len) {
                 }
             }
         }
-        const float2 mc = exchange<CLUSTER, true>(
-            make_float2(m_loc, code), xs, xbar, xk, warps, n, rank,
-            t.wait_limit_ns, dead);
+        const float2 mc = exchange<CLUSTER, true>(make_float2(m_loc, code), x);
         const float m = mc.x;
         const int row_code = static_cast<int>(mc.y);
 
@@ -310,16 +430,14 @@ cluster_kernel(RowTask t, int n, int slice_len) {
             bits = row_code == 2 ? kBitNan : kBitInf;
             write_out(row4, s, dst, 0.0f, 0.0f, true);
         } else {
-            float2 sv = exchange<CLUSTER, false>(
-                pass_sv<true>(row4, s.q4, 1.0f, m), xs, xbar, xk, warps, n,
-                rank, t.wait_limit_ns, dead);
-            float H = entropy_nats(sv, 1.0f);
+            float2 sv = exchange<CLUSTER, false>(transform_pass(row4, s.q4, m), x);
             float beta_out, inv_s;
-            if (!(H > bound)) {
+            if (!entropy_above(sv, 1.0f, bound_bits)) {
                 T_row = 1.0f;
                 beta_out = 1.0f;
                 inv_s = 1.0f / sv.x;
             } else {
+                ActiveSet a{wbuf + warp * cap_w, cap_w, 0, false, false, 0.0f};
                 float lo = t.t_min, hi = t.hi0;
                 bool lo_eval = false;
                 bool hi_eval = hi == 1.0f;   // H(1) > bound is known
@@ -331,14 +449,15 @@ cluster_kernel(RowTask t, int n, int slice_len) {
                         // end whose side is already known, so every further
                         // step repeats the same evaluation.
                         if ((mid == lo && lo_eval) || (mid == hi && hi_eval)) break;
-                        const float b = 1.0f / mid;
-                        sv = exchange<CLUSTER, false>(
-                            pass_sv<false>(row4, s.q4, b, 0.0f), xs, xbar, xk,
-                            warps, n, rank, t.wait_limit_ns, dead);
-                        H = entropy_nats(sv, b);
-                        if (H > bound) {
+                        const float b = __frcp_rn(mid);
+                        sv = search_pass<CLUSTER>(row4, s.q4, b, a, x);
+                        if (entropy_above(sv, b, bound_bits)) {
                             hi = mid;
                             hi_eval = true;
+                            if (a.cap > 0 && t.prune_k > 0.0f) {
+                                a.thr = -t.prune_k * hi;
+                                a.refilter = true;
+                            }
                         } else {
                             lo = mid;
                             lo_eval = true;
@@ -346,15 +465,12 @@ cluster_kernel(RowTask t, int n, int slice_len) {
                         }
                     }
                 }
-                const float b_lo = 1.0f / lo;
+                const float b_lo = __frcp_rn(lo);
                 if (!lo_eval) {
                     // lo is still t_min: evaluate it (section 5.4 check).
-                    sv = exchange<CLUSTER, false>(
-                        pass_sv<false>(row4, s.q4, b_lo, 0.0f), xs, xbar, xk,
-                        warps, n, rank, t.wait_limit_ns, dead);
-                    H = entropy_nats(sv, b_lo);
+                    sv = search_pass<CLUSTER>(row4, s.q4, b_lo, a, x);
                     s_lo = sv.x;
-                    if (H > bound) bits |= kBitOverflow;
+                    if (entropy_above(sv, b_lo, bound_bits)) bits |= kBitOverflow;
                 }
                 T_row = lo;
                 beta_out = b_lo;
@@ -366,14 +482,14 @@ cluster_kernel(RowTask t, int n, int slice_len) {
             if (t.t_out) t.t_out[r] = T_row;
             raise_error(t.err, bits);
         }
-        if (dead && !reported) {
+        if (x.dead && !reported) {
             raise_error(t.err, kBitTimeout);
             reported = true;
         }
         // The slice buffer is rewritten by the next row's copies.
         __syncthreads();
     }
-    if (dead && threadIdx.x == 0) {
+    if (x.dead && threadIdx.x == 0) {
         // Give copies still in flight a bounded chance to land before exit.
         for (int c = 0; c < kLoadChunks; ++c)
             mbar_wait(&lbar[c], ((lphase >> c) & 1u) ^ 1u, t.wait_limit_ns);
@@ -384,8 +500,9 @@ cluster_kernel(RowTask t, int n, int slice_len) {
 }  // namespace
 
 cudaError_t launch_cluster(const RowTask& task, int cluster_size,
-                           int slice_len, int threads, int smem_bytes,
-                           int64_t grid_ctas, cudaStream_t stream) {
+                           int slice_len, int threads, int cap_w,
+                           int smem_bytes, int64_t grid_ctas,
+                           cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid_ctas), 1, 1);
     cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
@@ -408,7 +525,8 @@ cudaError_t launch_cluster(const RowTask& task, int cluster_size,
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, kern, task, cluster_size, slice_len);
+        return cudaLaunchKernelEx(&cfg, kern, task, cluster_size, slice_len,
+                                  cap_w);
     }
     auto kern = cluster_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(
@@ -416,7 +534,7 @@ cudaError_t launch_cluster(const RowTask& task, int cluster_size,
     if (e != cudaSuccess) return e;
     cfg.attrs = nullptr;
     cfg.numAttrs = 0;
-    return cudaLaunchKernelEx(&cfg, kern, task, 1, slice_len);
+    return cudaLaunchKernelEx(&cfg, kern, task, 1, slice_len, cap_w);
 }
 
 }  // namespace cs

@@ -9,9 +9,9 @@
 // log2 e, then one register pass per bisection step giving
 // S = sum 2^(beta y) and V = sum y 2^(beta y), H = ln 2 (log2 S - beta V/S).
 // The per-step reduction is a butterfly over the G lanes (all lanes end
-// with bit-identical sums, so they take the same decision); the decision
-// uses the MUFU lg2 and rcp units, the output normalisation an exact
-// reciprocal.
+// with bit-identical sums, so they take the same decision); H > bound is
+// decided without a division as S (log2 S - bound log2 e) - beta V > 0,
+// with log2 on the MUFU lg2 unit.
 #include <math.h>
 
 #include "cs_device.cuh"
@@ -43,28 +43,12 @@ __device__ __forceinline__ float2 group_max2(float2 v, unsigned mask) {
 
 template <int E4>
 __device__ __forceinline__ float2 reg_pass(const float4 (&y)[E4], float beta) {
-    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-    float v0 = 0.f, v1 = 0.f, v2 = 0.f, v3 = 0.f;
+    SV4 acc;
+    acc.zero();
+    const float2 b2 = make_float2(beta, beta);
 #pragma unroll
-    for (int i = 0; i < E4; ++i) {
-        const float e0 = ex2(y[i].x * beta);
-        const float e1 = ex2(y[i].y * beta);
-        const float e2 = ex2(y[i].z * beta);
-        const float e3 = ex2(y[i].w * beta);
-        s0 += e0;
-        s1 += e1;
-        s2 += e2;
-        s3 += e3;
-        v0 = fmaf(e0, y[i].x, v0);
-        v1 = fmaf(e1, y[i].y, v1);
-        v2 = fmaf(e2, y[i].z, v2);
-        v3 = fmaf(e3, y[i].w, v3);
-    }
-    return make_float2((s0 + s1) + (s2 + s3), (v0 + v1) + (v2 + v3));
-}
-
-__device__ __forceinline__ float entropy_nats_fast(float2 sv, float beta) {
-    return kLn2 * (lg2_approx(sv.x) - beta * sv.y * rcp_approx(sv.x));
+    for (int i = 0; i < E4; ++i) acc.add(y[i], b2);
+    return acc.total();
 }
 
 template <int G, int E4>
@@ -76,7 +60,7 @@ rowgroup_kernel(RowTask t, int vec) {
         G == 32 ? 0xffffffffu : (((1u << G) - 1u) << (lane & ~(G - 1)));
     const int C = t.num_classes;
     const int Q = (C + 3) >> 2;  // float4 slots per row
-    const float bound = t.entropy_bound;
+    const float bound_bits = t.entropy_bound * kLog2e;
     const int64_t groups_per_grid =
         (static_cast<int64_t>(gridDim.x) * blockDim.x) / G;
 
@@ -151,8 +135,7 @@ rowgroup_kernel(RowTask t, int vec) {
                 y[i].w = fmaxf((y[i].w - m) * kLog2e, kYFloor);
             }
             float2 sv = group_sum2<G>(reg_pass<E4>(y, 1.0f), gmask);
-            float H = entropy_nats_fast(sv, 1.0f);
-            if (!(H > bound)) {
+            if (!entropy_above(sv, 1.0f, bound_bits)) {
                 T_row = 1.0f;
                 beta_out = 1.0f;
                 inv_s = 1.0f / sv.x;
@@ -165,10 +148,9 @@ rowgroup_kernel(RowTask t, int vec) {
                     for (int k = 0; k < t.max_iter; ++k) {
                         const float mid = 0.5f * (lo + hi);
                         if ((mid == lo && lo_eval) || (mid == hi && hi_eval)) break;
-                        const float b = 1.0f / mid;
+                        const float b = __frcp_rn(mid);
                         sv = group_sum2<G>(reg_pass<E4>(y, b), gmask);
-                        H = entropy_nats_fast(sv, b);
-                        if (H > bound) {
+                        if (entropy_above(sv, b, bound_bits)) {
                             hi = mid;
                             hi_eval = true;
                         } else {
@@ -178,12 +160,11 @@ rowgroup_kernel(RowTask t, int vec) {
                         }
                     }
                 }
-                const float b_lo = 1.0f / lo;
+                const float b_lo = __frcp_rn(lo);
                 if (!lo_eval) {
                     sv = group_sum2<G>(reg_pass<E4>(y, b_lo), gmask);
-                    H = entropy_nats_fast(sv, b_lo);
                     s_lo = sv.x;
-                    if (H > bound) bits |= kBitOverflow;
+                    if (entropy_above(sv, b_lo, bound_bits)) bits |= kBitOverflow;
                 }
                 T_row = lo;
                 beta_out = b_lo;
@@ -199,10 +180,13 @@ rowgroup_kernel(RowTask t, int vec) {
                 if (q < Q) {
                     float4 p = make_float4(0.f, 0.f, 0.f, 0.f);
                     if (!zero) {
-                        p.x = ex2(y[i].x * beta_out) * inv_s;
-                        p.y = ex2(y[i].y * beta_out) * inv_s;
-                        p.z = ex2(y[i].z * beta_out) * inv_s;
-                        p.w = ex2(y[i].w * beta_out) * inv_s;
+                        const float2 b2 = make_float2(beta_out, beta_out);
+                        const float2 i2 = make_float2(inv_s, inv_s);
+                        const float2 x01 = mul2(make_float2(y[i].x, y[i].y), b2);
+                        const float2 x23 = mul2(make_float2(y[i].z, y[i].w), b2);
+                        const float2 p01 = mul2(make_float2(ex2(x01.x), ex2(x01.y)), i2);
+                        const float2 p23 = mul2(make_float2(ex2(x23.x), ex2(x23.y)), i2);
+                        p = make_float4(p01.x, p01.y, p23.x, p23.y);
                     }
                     __stcs(d4 + q, p);
                 }

@@ -47,8 +47,7 @@ typedef int32_t cs_status;
 #define CS_ERR_CUDA 9             /* a CUDA call failed (launch, attribute)  */
 #define CS_ERR_TIMEOUT 10         /* a bounded device wait gave up (async)  */
 
-/* Kernel variants (cs_plan.variant, and the `variant` argument of
- * cs_constrained_softmax_variant). */
+/* Kernel variants (cs_options.variant, cs_plan.variant). */
 #define CS_VARIANT_AUTO 0
 #define CS_VARIANT_ROWGROUP 1 /* 1-32 lanes per row, row in registers      */
 #define CS_VARIANT_CLUSTER 2  /* 1-16 CTAs per row, row in shared memory,
@@ -59,7 +58,19 @@ typedef int32_t cs_status;
  * in shared memory. */
 #define CS_MAX_NUM_CLASSES 850000
 
-/* What a launch of the given shape uses.  Filled by cs_plan / cs_plan_host. */
+/* Launch options; an all-zero struct (or NULL) means "automatic". */
+typedef struct cs_options {
+    int32_t variant;   /* CS_VARIANT_AUTO, _ROWGROUP or _CLUSTER            */
+    int32_t param;     /* rowgroup: lanes per row (1, 2, 4, 8, 16, 32);
+                          cluster: CTAs per row (1..16); 0 = automatic      */
+    int32_t threads;   /* cluster: threads per CTA (multiple of 32,
+                          64..1024); 0 = automatic                          */
+    int32_t full_scan; /* cluster: 1 = evaluate every class at every
+                          bisection step (no active set); 0 = active set   */
+} cs_options;
+
+/* What a launch of the given shape uses.  Filled by cs_plan_launch /
+ * cs_plan_host. */
 typedef struct cs_plan {
     int32_t variant;         /* CS_VARIANT_ROWGROUP or CS_VARIANT_CLUSTER   */
     int32_t lanes_per_row;   /* rowgroup: lanes that share one row          */
@@ -69,6 +80,8 @@ typedef struct cs_plan {
     int32_t threads_per_cta;
     int32_t smem_bytes;      /* dynamic shared memory per CTA               */
     int32_t ctas_per_sm;     /* CTAs resident per SM by the plan's limits   */
+    int32_t warp_buffer;     /* cluster: active-set floats per warp (0: off) */
+    float prune_k;           /* cluster: active-set threshold K (0: off)    */
     int64_t grid_ctas;       /* CTAs in the launch                          */
 } cs_plan;
 
@@ -110,20 +123,18 @@ cs_status cs_constrained_softmax(const float* logits, float* out,
                                  int32_t max_iter, float* t_out, void* stream);
 
 /*
- * Same operation with the kernel variant chosen by the caller (tests and
- * benchmarks use it to run every variant on every shape).
- * variant  CS_VARIANT_AUTO, CS_VARIANT_ROWGROUP or CS_VARIANT_CLUSTER.
- * param    rowgroup: lanes per row (1, 2, 4, 8, 16 or 32; 0 = automatic).
- *          cluster: CTAs per row (1..16; 0 = automatic).
+ * Same operation with launch options (tests and benchmarks use them to run
+ * every variant on every shape).  options may be NULL (automatic).
  * A variant that cannot hold the row returns CS_ERR_OOM (rowgroup: more than
- * 32 classes per lane; cluster: slice larger than a CTA's shared memory).
+ * 32 classes per lane; cluster: slice larger than a CTA's shared memory);
+ * malformed options return CS_ERR_INVALID_ARG.
  */
-cs_status cs_constrained_softmax_variant(const float* logits, float* out,
-                                         int64_t batch, int32_t num_classes,
-                                         float entropy_bound, float t_min,
-                                         float t_max, int32_t max_iter,
-                                         float* t_out, int32_t variant,
-                                         int32_t param, void* stream);
+cs_status cs_constrained_softmax_ex(const float* logits, float* out,
+                                    int64_t batch, int32_t num_classes,
+                                    float entropy_bound, float t_min,
+                                    float t_max, int32_t max_iter,
+                                    float* t_out, const cs_options* options,
+                                    void* stream);
 
 /*
  * Reads and clears the calling thread's current device's error word after
@@ -137,16 +148,16 @@ cs_status cs_constrained_softmax_variant(const float* logits, float* out,
  */
 cs_status cs_get_error(int32_t* code_mask, void* stream);
 
-/* The plan cs_constrained_softmax_variant would launch on the current
- * device (queries device attributes; no launch).  Same argument rules. */
-cs_status cs_plan_launch(int64_t batch, int32_t num_classes, int32_t variant,
-                         int32_t param, cs_plan* plan);
+/* The plan cs_constrained_softmax_ex would launch on the current device
+ * (queries device attributes; no launch).  options may be NULL. */
+cs_status cs_plan_launch(int64_t batch, int32_t num_classes,
+                         const cs_options* options, cs_plan* plan);
 
 /* The same planning on given device limits, host-only (no CUDA call):
  * sm_count SMs, smem_per_block_optin bytes of dynamic shared memory per CTA,
  * smem_per_sm bytes per SM, max_cluster CTAs per cluster. */
-cs_status cs_plan_host(int64_t batch, int32_t num_classes, int32_t variant,
-                       int32_t param, int32_t sm_count,
+cs_status cs_plan_host(int64_t batch, int32_t num_classes,
+                       const cs_options* options, int32_t sm_count,
                        int32_t smem_per_block_optin, int32_t smem_per_sm,
                        int32_t max_cluster, cs_plan* plan);
 

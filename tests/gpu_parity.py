@@ -2,8 +2,14 @@
 
 Acceptance (per row, on the same seeded inputs):
   * the temperature: equal to the oracle's (as fp32), or within one final
-    bisection interval plus 4 fp32 ulps of it; when it differs, the GPU's
-    probabilities are compared with the oracle's fp64 softmax(l / T_gpu);
+    bisection interval plus 4 fp32 ulps of it, or else an endpoint that a
+    bisection whose H is exact to EPS_H would also return: H(T_gpu) <=
+    bound + EPS_H and H(T_gpu + interval + 4 ulps) >= bound - EPS_H, with H
+    the oracle's fp64 entropy.  (The GPU decides H > bound in fp32; near the
+    crossing its H is off by ~1e-7 nats, which moves T by that over dH/dT --
+    more than the final interval once max_iter is large.)  When T differs,
+    the GPU's probabilities are compared with the oracle's fp64
+    softmax(l / T_gpu);
   * probabilities: elementwise |dp| <= 2e-5;
   * entropy of the output (fp64, scipy.special.entr): |dH| <= 1e-4, and
     H(out) <= bound + 1e-4 whenever the oracle found the bound achievable;
@@ -22,13 +28,15 @@ import oracle
 P_TOL = 2e-5
 H_TOL = 1e-4
 T_ULPS = 4
+EPS_H = 1e-6
 
 ERR_BIT = {1: 1 << 1, 2: 1 << 2, 3: 1 << 3}
 TIMEOUT_BIT = 1 << 10
 
 
 def run_gpu(x: np.ndarray, entropy_bound=0.2, t_min=0.01, t_max=10.0,
-            max_iter=20, variant="auto", param=0, in_offset=0, out_offset=0):
+            max_iter=20, variant="auto", param=0, in_offset=0, out_offset=0,
+            threads=0, full_scan=False):
     """Runs the CUDA path through the C ABI; returns (p, T, error_mask).
     in_offset/out_offset shift the tensors by that many floats inside their
     allocations (to exercise unaligned rows)."""
@@ -47,7 +55,7 @@ def run_gpu(x: np.ndarray, entropy_bound=0.2, t_min=0.01, t_max=10.0,
     cs.get_error()  # clear
     cs.constrained_softmax(xin, entropy_bound, t_min, t_max, max_iter,
                            out=out, t_out=t_out, variant=variant,
-                           param=param)
+                           param=param, threads=threads, full_scan=full_scan)
     bits = cs.get_error()
     mask = 0
     for name, bit in cs.ERROR_BITS.items():
@@ -74,7 +82,8 @@ def compare(x: np.ndarray, p_gpu: np.ndarray, T_gpu: np.ndarray, mask: int,
     """Asserts parity row by row; returns summary statistics."""
     B = x.shape[0]
     bound32 = float(np.float32(entropy_bound))
-    stats = {"rows": B, "T_equal": 0, "T_within": 0, "max_dp": 0.0,
+    stats = {"rows": B, "T_equal": 0, "T_within": 0, "T_zone": 0,
+             "max_dp": 0.0,
              "max_dH": 0.0}
     want_mask = 0
     for b in range(B):
@@ -92,9 +101,17 @@ def compare(x: np.ndarray, p_gpu: np.ndarray, T_gpu: np.ndarray, mask: int,
             p_ref = ref.p[b]
         else:
             tol = t_tolerance(To, t_min, t_max, max_iter)
-            assert abs(Tg - To) <= tol, \
-                f"row {b}: T_gpu={Tg!r} T_oracle={To!r} tol={tol:.3g}"
-            stats["T_within"] += 1
+            if abs(Tg - To) <= tol:
+                stats["T_within"] += 1
+            else:
+                H_at = oracle.entropy(x[b], Tg)
+                H_up = oracle.entropy(x[b], Tg + t_tolerance(Tg, t_min, t_max,
+                                                             max_iter))
+                assert H_at <= bound32 + EPS_H and H_up >= bound32 - EPS_H, (
+                    f"row {b}: T_gpu={Tg!r} T_oracle={To!r} tol={tol:.3g} "
+                    f"H(T_gpu)-bound={H_at - bound32:.3g} "
+                    f"H(T_gpu+w)-bound={H_up - bound32:.3g}")
+                stats["T_zone"] += 1
             p_ref = oracle.softmax(x[b], Tg)
         dp = float(np.max(np.abs(p_gpu[b].astype(np.float64) - p_ref)))
         assert dp <= P_TOL, f"row {b}: max |dp| = {dp:.3g}"

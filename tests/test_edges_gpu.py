@@ -121,6 +121,9 @@ def test_batch_zero_and_argument_errors():
     assert e.value.status == 8
     assert cs.cs_constrained_softmax(x.data_ptr(), 0, 4, 10, 0.2, 0.01, 10.0,
                                      20, None, None) == 8
+    assert cs.cs_constrained_softmax_ex(x.data_ptr(), x.data_ptr() + 4096, 4,
+                                        10, 0.2, 0.01, 10.0, 20, None,
+                                        cs.options(2, 0, 33, 0), None) == 8
     big = torch.zeros((1, 900000), device=dev)
     with pytest.raises(cs.CsError) as e:
         cs.constrained_softmax(big)

@@ -33,14 +33,17 @@ def test_small_4x1000(variant, param):
     compare(x, p, T, mask, _oracle(x, w), **_params(w))
 
 
-@pytest.mark.parametrize("variant,param", [("auto", 0), ("cluster", 2),
-                                           ("cluster", 4), ("cluster", 8)])
-def test_latency_32x50000(variant, param):
+@pytest.mark.parametrize("variant,param,threads,full_scan", [
+    ("auto", 0, 0, False), ("cluster", 1, 0, True), ("cluster", 2, 0, False),
+    ("cluster", 4, 0, False), ("cluster", 4, 256, False),
+    ("cluster", 8, 0, False), ("cluster", 4, 0, True)])
+def test_latency_32x50000(variant, param, threads, full_scan):
     w = wl.LATENCY
     x = wl.generate(w)
-    p, T, mask = run_gpu(x, variant=variant, param=param, **_params(w))
+    p, T, mask = run_gpu(x, variant=variant, param=param, threads=threads,
+                         full_scan=full_scan, **_params(w))
     stats = compare(x, p, T, mask, _oracle(x, w), **_params(w))
-    assert stats["T_equal"] >= 28
+    assert stats["T_zone"] <= 3
 
 
 def test_moe_router_full():
@@ -48,10 +51,10 @@ def test_moe_router_full():
     x = wl.generate(w)
     p, T, mask = run_gpu(x, **_params(w))
     stats = compare(x, p, T, mask, _oracle(x, w), **_params(w))
-    assert stats["T_equal"] >= 0.95 * w.batch
+    assert stats["T_zone"] <= 0.01 * w.batch
 
 
-@pytest.mark.parametrize("lanes", [1, 2, 4, 8, 16, 32])
+@pytest.mark.parametrize("lanes", [2, 4, 8, 16, 32])
 def test_moe_router_lanes(lanes):
     w = wl.ROUTER
     rows = np.arange(2048)
@@ -67,14 +70,16 @@ def test_moe_router_cluster_variant():
     compare(x, p, T, mask, _oracle(x, w), **_params(w))
 
 
-@pytest.mark.parametrize("param", [0, 4, 8, 16])
-def test_long_rows_sampled(param):
+@pytest.mark.parametrize("param,full_scan", [(0, False), (4, False),
+                                             (8, False), (16, False),
+                                             (4, True)])
+def test_long_rows_sampled(param, full_scan):
     """256 x 131072 launched whole; rows sampled for the oracle, always
     including constant, spiked and normal rows."""
     w = wl.LONG
     x = wl.generate(w)
     p, T, mask = run_gpu(x, variant="cluster" if param else "auto",
-                         param=param, **_params(w))
+                         param=param, full_scan=full_scan, **_params(w))
     kinds = wl.row_kinds(w)
     pick = sorted(set(wl.sample_rows(w, 10).tolist())
                   | set(np.flatnonzero(kinds == 2)[:3].tolist())
@@ -101,10 +106,12 @@ def test_long_rows_no_search_branch():
 
 
 @pytest.mark.parametrize("bound,iters", wl.SWEEP_POINTS)
-def test_sweep_sampled(bound, iters):
+@pytest.mark.parametrize("param,threads", [(0, 0), (2, 512)])
+def test_sweep_sampled(bound, iters, param, threads):
     w = wl.SWEEP.with_(entropy_bound=bound, max_iter=iters)
     x = wl.generate(w)
-    p, T, mask = run_gpu(x, **_params(w))
+    p, T, mask = run_gpu(x, variant="cluster" if param else "auto",
+                         param=param, threads=threads, **_params(w))
     pick = wl.sample_rows(w, 24)
     ref = _oracle(x[pick], w)
     compare(x[pick], p[pick], T[pick], mask, ref, check_mask=False,
