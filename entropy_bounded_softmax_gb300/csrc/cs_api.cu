@@ -31,6 +31,7 @@ constexpr int kAutoRowgroupE4 = 4;     // 16 classes per lane
 constexpr int kAutoRowgroupMaxClasses = 512;
 constexpr int kMaxIter = 1024;
 constexpr int64_t kMaxGridX = 2147483647;
+constexpr int64_t kMinWideSlice = 2048;
 
 struct DeviceInfo {
     std::atomic<bool> ready{false};
@@ -137,12 +138,13 @@ cs_status plan_rowgroup(int64_t batch, int32_t C, int32_t param,
     return CS_OK;
 }
 
-// Cluster plan for n CTAs per row: slice, threads, active-set buffer and
+// Cluster plan for n CTAs per row: slice, threads, active-set segments and
 // shared memory.  Returns false if it does not fit smem_optin.
-bool cluster_geometry(int32_t C, int n, int threads_req, bool prune,
-                      int smem_optin, cs_plan* p) {
+bool cluster_geometry(int64_t batch, int32_t C, int n, int threads_req,
+                      bool prune, int sm_count, int smem_optin, cs_plan* p) {
     const int64_t L = ceil_div(ceil_div(C, n), 4) * 4;
-    const int threads = threads_req ? threads_req : cs::cluster_threads_for(L);
+    const int threads = threads_req
+        ? threads_req : cs::cluster_threads_for(L, batch * n, sm_count);
     const int warps = threads / 32;
     const int64_t base = cs::cluster_smem_bytes(L, threads, n, 0);
     if (base > smem_optin) return false;
@@ -165,7 +167,6 @@ bool cluster_geometry(int32_t C, int n, int threads_req, bool prune,
 cs_status plan_cluster(int64_t batch, int32_t C, const cs_options& o,
                        int sm_count, int smem_optin, int smem_per_sm,
                        int max_cluster, cs_plan* p) {
-    (void)sm_count;
     if (o.threads != 0 &&
         (o.threads < 64 || o.threads > cs::kClusterMaxThreads || o.threads % 32))
         return CS_ERR_INVALID_ARG;
@@ -174,14 +175,27 @@ cs_status plan_cluster(int64_t batch, int32_t C, const cs_options& o,
     *p = cs_plan{};
     p->variant = CS_VARIANT_CLUSTER;
     if (o.param == 0) {
+        // Smallest cluster whose slices are at most kTargetSlice classes
+        // (and fit), widened while the launch has fewer CTAs than SMs.
+        int n0 = static_cast<int>(ceil_div(C, cs::kTargetSlice));
+        if (n0 > max_cluster) n0 = max_cluster;
+        if (n0 < 1) n0 = 1;
+        // Widen only while every CTA keeps at least kMinWideSlice classes.
+        const int64_t rows = batch > 0 ? batch : 1;
+        int64_t widen = sm_count / rows;
+        if (widen > C / kMinWideSlice) widen = C / kMinWideSlice;
+        if (widen > max_cluster) widen = max_cluster;
+        if (widen > n0) n0 = static_cast<int>(widen);
         bool ok = false;
-        for (int c = 1; c <= max_cluster && !ok; ++c)
-            ok = cluster_geometry(C, c, o.threads, prune, smem_optin, p);
+        for (int c = n0; c <= max_cluster && !ok; ++c)
+            ok = cluster_geometry(batch, C, c, o.threads, prune, sm_count,
+                                  smem_optin, p);
         if (!ok) return CS_ERR_OOM;
     } else {
         if (o.param < 1 || o.param > cs::kMaxCluster) return CS_ERR_INVALID_ARG;
         if (o.param > max_cluster) return CS_ERR_INVALID_ARG;
-        if (!cluster_geometry(C, o.param, o.threads, prune, smem_optin, p))
+        if (!cluster_geometry(batch, C, o.param, o.threads, prune, sm_count,
+                              smem_optin, p))
             return CS_ERR_OOM;
     }
     const int n = p->cluster_size;
@@ -287,7 +301,7 @@ cs_status cs_constrained_softmax_ex(const float* logits, float* out,
     task.t_min = t_min;
     task.hi0 = t_max < 1.0f ? t_max : 1.0f;
     task.prune_k = p.prune_k;
-    task.wait_limit_ns = cs::kWaitLimitNs;
+    task.wait_limit_cycles = cs::kWaitLimitCycles;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
@@ -361,9 +375,11 @@ cs_status cs_test_wait_timeout(int64_t limit_ns, void* stream) {
     DeviceInfo* d = nullptr;
     const cs_status st = device_info(&d);
     if (st != CS_OK) return st;
+    // The wait is bounded in SM cycles; 2.07 cycles per ns at GB300's
+    // maximum clock (a lower clock only lengthens the wait).
+    const uint64_t cycles = static_cast<uint64_t>(limit_ns) * 207 / 100;
     const cudaError_t e = cs::launch_wait_timeout(
-        d->err, static_cast<uint64_t>(limit_ns),
-        static_cast<cudaStream_t>(stream));
+        d->err, cycles, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {
         cudaGetLastError();
         return CS_ERR_CUDA;

@@ -145,30 +145,40 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
                  :: "r"(smem_addr(bar)) : "memory");
 }
 
-// One test of the phase; a thread whose phase is not complete may sleep in
-// hardware for up to kSuspendHintNs or until the phase completes.
-constexpr uint32_t kSuspendHintNs = 100000;
-
+// One test of the phase (a thread may be suspended briefly by the hardware
+// while the phase is incomplete).  CLUSTER_SCOPE: acquire at cluster scope
+// (remote st.async writes); otherwise at CTA scope.
+template <bool CLUSTER_SCOPE>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n"
-        " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
-        " selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok) : "r"(bar), "r"(parity), "r"(kSuspendHintNs) : "memory");
+    if (CLUSTER_SCOPE) {
+        asm volatile(
+            "{\n .reg .pred p;\n"
+            " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    } else {
+        asm volatile(
+            "{\n .reg .pred p;\n"
+            " mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    }
     return ok != 0;
 }
 
 // Waits for the phase with the given parity to complete, for at most
-// limit_ns nanoseconds (and at most 2^31 polls).  Returns false on timeout.
+// limit_cycles SM clock cycles (measured with clock64, which costs a few
+// cycles to read) and at most 2^31 polls.  Returns false on timeout.
+template <bool CLUSTER_SCOPE>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          uint64_t limit_ns) {
+                                          uint64_t limit_cycles) {
     const uint32_t a = smem_addr(bar);
-    if (mbar_try_wait(a, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
+    if (mbar_try_wait<CLUSTER_SCOPE>(a, parity)) return true;
+    const long long c0 = clock64();
     for (uint32_t i = 1; i < (1u << 31); ++i) {
-        if (mbar_try_wait(a, parity)) return true;
-        if ((i & 7u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
+        if (mbar_try_wait<CLUSTER_SCOPE>(a, parity)) return true;
+        if (clock64() - c0 > static_cast<long long>(limit_cycles)) return false;
     }
     return false;
 }

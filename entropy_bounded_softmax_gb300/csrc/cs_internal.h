@@ -16,8 +16,9 @@ constexpr unsigned int kBitInf = 1u << CS_ERR_INF_INPUT;
 constexpr unsigned int kBitOverflow = 1u << CS_ERR_ENTROPY_OVERFLOW;
 constexpr unsigned int kBitTimeout = 1u << CS_ERR_TIMEOUT;
 
-// Default limit of every bounded device wait (2 s).
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// Default limit of every bounded device wait, in SM cycles: 2^31 cycles,
+// about 1 s at GB300's 2.07 GHz maximum clock.
+constexpr uint64_t kWaitLimitCycles = 1ull << 31;
 
 // One launch's worth of work: every row of the matrix with the same
 // parameters (the arguments of section 2.1's signature plus t_out and the
@@ -34,7 +35,7 @@ struct RowTask {
     float t_min;
     float hi0;             // min(1, t_max): upper end of the search
     float prune_k;         // active-set threshold K (0: no pruning)
-    uint64_t wait_limit_ns;
+    uint64_t wait_limit_cycles;
 };
 
 // Cluster kernel geometry.
@@ -47,26 +48,64 @@ constexpr int kClusterMaxThreads = 1024;
 constexpr int kMaxWarpBuffer = 256;
 constexpr int kMinWarpBuffer = 64;
 
-// Dynamic shared memory of the cluster kernel for a slice of `slice_len`
-// classes, `threads` threads, cluster size `n` and `cap_w` floats of
-// active-set buffer per warp.
-inline int64_t cluster_smem_bytes(int64_t slice_len, int threads, int n,
-                                  int cap_w) {
-    const int64_t warps = threads / 32;
-    const int64_t slots = 2 * warps * n * 8;            // exchange buffers
-    const int64_t bars = (2 + kLoadChunks) * 8;         // mbarriers
-    const int64_t head = ((slots + bars + 127) / 128) * 128;
-    const int64_t wbuf = warps * cap_w * 4;
-    const int64_t row = ((slice_len + 8 + 3) / 4) * 16;  // pad + tail room
-    return head + wbuf + row;
+// Byte offsets of the cluster kernel's dynamic shared memory for `warps`
+// warps, cluster size n and cap_w floats of active segment per warp:
+// cluster slots [2][n][16] floats, per-warp exchange slots [warps] float4,
+// two broadcast float4s, per-warp segment counts, the two cluster mbarriers
+// and the load mbarriers; then (128-byte aligned) the segments and the
+// slice.
+struct ClusterSmemLayout {
+    int cslot, wslot, bcast, segcnt, cbar, lbar, wbuf, row;
+};
+
+__host__ __device__ inline ClusterSmemLayout cluster_smem_layout(int warps,
+                                                                 int n,
+                                                                 int cap_w) {
+    ClusterSmemLayout L;
+    int p = 0;
+    L.cslot = p;
+    p += 2 * n * 16 * 4;
+    L.wslot = p;
+    p += warps * 16;
+    L.bcast = p;
+    p += 2 * 16;
+    L.segcnt = p;
+    p += ((warps * 4 + 15) / 16) * 16;
+    L.cbar = p;
+    p += 2 * 8;
+    L.lbar = p;
+    p += kLoadChunks * 8;
+    L.wbuf = ((p + 127) / 128) * 128;
+    L.row = L.wbuf + warps * cap_w * 4;
+    return L;
 }
 
-inline int cluster_threads_for(int64_t slice_len) {
-    // About 16 classes per thread per pass, 128..1024 threads.
-    int64_t t = (slice_len + 15) / 16;
+// Dynamic shared memory of the cluster kernel for a slice of `slice_len`
+// classes, `threads` threads, cluster size `n` and `cap_w` floats of
+// active segment per warp (cap_w a multiple of 32).
+inline int64_t cluster_smem_bytes(int64_t slice_len, int threads, int n,
+                                  int cap_w) {
+    const ClusterSmemLayout L = cluster_smem_layout(threads / 32, n, cap_w);
+    const int64_t row = ((slice_len + 8 + 3) / 4) * 16;  // pad + tail room
+    return L.row + row;
+}
+
+// Classes per CTA the automatic plan aims for: 64 KB slices, so that
+// three CTAs share an SM and one's exchange overlaps the others' passes.
+constexpr int64_t kTargetSlice = 16384;
+
+// Automatic threads per CTA.  A launch with no more CTAs than SMs runs one
+// CTA per SM and wants many warps (about 24 classes per thread, 128-512);
+// a larger launch wants several small CTAs per SM (about 64 classes per
+// thread, 128-256).
+inline int cluster_threads_for(int64_t slice_len, int64_t ctas,
+                               int64_t sm_count) {
+    const bool latency = ctas <= sm_count;
+    int64_t t = (slice_len + (latency ? 23 : 63)) / (latency ? 24 : 64);
     t = ((t + 31) / 32) * 32;
     if (t < 128) t = 128;
-    if (t > kClusterMaxThreads) t = kClusterMaxThreads;
+    const int64_t cap = latency ? 512 : 256;
+    if (t > cap) t = cap;
     return static_cast<int>(t);
 }
 
@@ -85,7 +124,11 @@ cudaError_t launch_cluster(const RowTask& task, int cluster_size,
                            cudaStream_t stream);
 cudaError_t launch_probe_ex2(float* sink, int iters, int blocks, int threads,
                              cudaStream_t stream);
-cudaError_t launch_wait_timeout(unsigned int* err, uint64_t limit_ns,
+cudaError_t launch_wait_timeout(unsigned int* err, uint64_t limit_cycles,
                                 cudaStream_t stream);
+
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per device and
+// kernel, raised only when a launch needs more than was set before.
+cudaError_t ensure_smem_attribute(const void* func, int slot, int bytes);
 
 }  // namespace cs

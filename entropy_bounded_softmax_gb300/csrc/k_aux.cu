@@ -1,6 +1,10 @@
 // Auxiliary kernels: the ex2 throughput probe that sets the roofline of the
-// constrained softmax (its hot loop is one ex2 per class per bisection step),
-// and the bounded-wait timeout exercise.
+// constrained softmax (its hot loop is one ex2 per class per bisection step)
+// and the bounded-wait timeout exercise; plus the per-device cache of kernel
+// shared-memory attributes.
+#include <atomic>
+#include <mutex>
+
 #include "cs_device.cuh"
 
 namespace cs {
@@ -28,15 +32,15 @@ __global__ void probe_ex2_kernel(float* sink, int iters) {
 }
 
 // One CTA waits on an mbarrier that nothing ever completes; the bounded
-// wait gives up after limit_ns and the timeout is recorded.
-__global__ void wait_timeout_kernel(unsigned int* err, uint64_t limit_ns) {
+// wait gives up after limit_cycles and the timeout is recorded.
+__global__ void wait_timeout_kernel(unsigned int* err, uint64_t limit_cycles) {
     __shared__ uint64_t bar;
     if (threadIdx.x == 0) {
         mbar_init(&bar, 1u);
         fence_mbar_init();
     }
     __syncthreads();
-    const bool ok = mbar_wait(&bar, 0u, limit_ns);
+    const bool ok = mbar_wait<false>(&bar, 0u, limit_cycles);
     if (!ok && threadIdx.x == 0) raise_error(err, kBitTimeout);
 }
 
@@ -50,10 +54,41 @@ cudaError_t launch_probe_ex2(float* sink, int iters, int blocks, int threads,
     return cudaGetLastError();
 }
 
-cudaError_t launch_wait_timeout(unsigned int* err, uint64_t limit_ns,
+cudaError_t launch_wait_timeout(unsigned int* err, uint64_t limit_cycles,
                                 cudaStream_t stream) {
-    wait_timeout_kernel<<<1, 32, 0, stream>>>(err, limit_ns);
+    wait_timeout_kernel<<<1, 32, 0, stream>>>(err, limit_cycles);
     return cudaGetLastError();
+}
+
+namespace {
+constexpr int kMaxDevices = 64;
+constexpr int kSlots = 2;
+// Largest MaxDynamicSharedMemorySize set so far, per device and kernel.
+std::atomic<int> g_smem_set[kMaxDevices][kSlots];
+std::mutex g_smem_mu;
+}  // namespace
+
+cudaError_t ensure_smem_attribute(const void* func, int slot, int bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices || slot < 0 || slot >= kSlots)
+        return cudaErrorInvalidValue;
+    if (g_smem_set[dev][slot].load(std::memory_order_acquire) >= bytes)
+        return cudaSuccess;
+    std::lock_guard<std::mutex> lock(g_smem_mu);
+    if (g_smem_set[dev][slot].load(std::memory_order_relaxed) >= bytes)
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             bytes);
+    if (e != cudaSuccess) return e;
+    if (slot == 1) {
+        e = cudaFuncSetAttribute(
+            func, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
+    g_smem_set[dev][slot].store(bytes, std::memory_order_release);
+    return cudaSuccess;
 }
 
 }  // namespace cs
