@@ -50,12 +50,11 @@ constexpr int kMinWarpBuffer = 64;
 
 // Byte offsets of the cluster kernel's dynamic shared memory for `warps`
 // warps, cluster size n and cap_w floats of active segment per warp:
-// cluster slots [2][n][16] floats, per-warp exchange slots [warps] float4,
-// two broadcast float4s, per-warp segment counts, the two cluster mbarriers
-// and the load mbarriers; then (128-byte aligned) the segments and the
-// slice.
+// cluster slots [2][n] float2, per-warp exchange slots [2][warps] float2,
+// the two cluster mbarriers and the load mbarriers; then (128-byte aligned)
+// the active segments and the slice.
 struct ClusterSmemLayout {
-    int cslot, wslot, bcast, segcnt, cbar, lbar, wbuf, row;
+    int cslot, wslot, cbar, lbar, wbuf, row;
 };
 
 __host__ __device__ inline ClusterSmemLayout cluster_smem_layout(int warps,
@@ -64,13 +63,9 @@ __host__ __device__ inline ClusterSmemLayout cluster_smem_layout(int warps,
     ClusterSmemLayout L;
     int p = 0;
     L.cslot = p;
-    p += 2 * n * 16 * 4;
+    p += 2 * n * 8;
     L.wslot = p;
-    p += warps * 16;
-    L.bcast = p;
-    p += 2 * 16;
-    L.segcnt = p;
-    p += ((warps * 4 + 15) / 16) * 16;
+    p += 2 * warps * 8;
     L.cbar = p;
     p += 2 * 8;
     L.lbar = p;

@@ -20,31 +20,26 @@
 //   output  p_i = 2^(beta_lo y_i) / S(lo), reusing S(lo) from the step that
 //           set lo, written with 128-bit streaming stores.
 //
-// Slice mode.  Every warp scans its float4s of the slice.  The CTA reduces
-// with one shuffle tree per warp, a __syncthreads, warp 0 summing the
-// per-warp partials (and, in a cluster, pushing the CTA's sum to every CTA
-// with st.async and waiting on an mbarrier for the others) and a second
-// __syncthreads that broadcasts the result.  Every CTA sums in rank order,
-// so all threads of the cluster see bit-identical sums and take the same
-// decision.
+// Reduction.  Every warp reduces its (S, V) with a shuffle tree and writes
+// the pair to a slot; after one __syncthreads every warp reduces the slots
+// with a second shuffle tree.  In a cluster, warp 0 then pushes the CTA's
+// pair into every CTA (st.async, counted on an mbarrier) and every thread
+// sums the cluster's pairs in rank order once the mbarrier completes.  All
+// threads of the cluster thus see bit-identical sums and take the same
+// decision.  Slots are double-buffered, which is safe because no thread can
+// reach exchange k+2 before every thread has left exchange k.
 //
 // Active set.  Every later step evaluates at beta = 1/mid >= 1/hi, so a class
 // with y_i < -K hi contributes less than 2^-K to S (which is >= 1: the
 // maximum contributes 1) at every remaining step.  With K = 36 + log2(C)
 // all such classes together change S and beta V by less than 2^-30 of
-// their values, far below fp32 resolution.  After hi drops, a slice pass
-// also compacts each warp's still-active classes (ballot + popc) into its
-// own shared-memory segment.  If no warp anywhere in the cluster overflows
-// its segment (and the active classes are few enough for one warp per
-// CTA), the whole cluster switches in that same step to active-set mode:
-// warp 0 of each CTA runs the rest of the search alone over the segments
-// while the other warps wait for the output pass.  In that mode one
-// exchange decides up to three bisection steps: the warp evaluates the 7
-// midpoints of the next three levels (each computed exactly as the
-// one-step-at-a-time search computes it) and walks them with the same
-// decisions, so the result is that of the sequential search.  The full
-// slice stays in place for the output pass, so every p_i is still computed.
-//
+// their values, far below fp32 resolution.  After hi drops, a warp still
+// scanning the slice compacts its active classes (ballot + popc) into its
+// own shared-memory segment during the next pass; if they fit, later steps
+// read only the segment (and drop classes again whenever hi drops).  The
+// full slice stays in place for the output pass, so every p_i is still
+// computed.
+
 // Every wait is bounded (cs::kWaitLimitCycles by default).  A thread whose
 // wait times out records CS_ERR_TIMEOUT and from then on neither waits,
 // pushes nor issues copies, but keeps the kernel's control flow so that all
@@ -57,10 +52,6 @@ namespace cs {
 namespace {
 
 using namespace csd;
-
-constexpr int kSpecLevels = 3;   // bisection levels per active-set exchange
-constexpr int kSlotFloats = 16;  // cluster slot payload (>= 2 * 7)
-constexpr int kSearchWarpMax = 1024;  // active classes per CTA for one warp
 
 __device__ __forceinline__ float4 floor4() {
     return make_float4(kYFloor, kYFloor, kYFloor, kYFloor);
@@ -105,100 +96,65 @@ __device__ __forceinline__ int chunk_begin(const Slice& s, int nch, int c) {
     return s.qb0 + static_cast<int>((static_cast<int64_t>(body) * c) / nch);
 }
 
-// Shared-memory objects of one CTA (cs::cluster_smem_bytes sizes them).
+// Shared-memory objects of one CTA (cs::cluster_smem_layout places them).
 struct Smem {
-    float* cslot;     // [2][n][kSlotFloats] cluster slots (double-buffered)
-    float4* wslot;    // [warps] per-warp partials of slice-mode exchanges
-    float4* bcast;    // [2] slice-mode result; active-set result
-    int* segcnt;      // [warps] classes in each warp's active segment
+    float2* cslot;    // [2][n] cluster slots (double-buffered)
+    float2* wslot;    // [2][warps] per-warp slots (double-buffered)
     uint64_t* cbar;   // [2] cluster-exchange mbarriers
     uint64_t* lbar;   // [kLoadChunks] bulk-copy mbarriers
     float* wbuf;      // [warps][cap_w] active segments
     float4* row4;     // the slice
 };
 
-// Cluster-exchange state of one thread (only warp 0 exchanges).
-struct Clu {
+// Exchange state of one thread (every thread runs every exchange).
+struct Exch {
+    int warps;
     int n;
     uint32_t rank;
-    uint32_t xk;      // cluster exchanges so far (slot buffer and phase)
+    uint32_t lk;      // exchanges so far (per-warp slot buffer)
+    uint32_t xk;      // cluster exchanges so far (cluster slot buffer, phase)
     uint64_t limit;
     bool dead;
 };
 
-// Shuffle-tree all-reduce of the first NV entries of a over the warp; every
-// lane ends with the same (bit-identical) values.
-template <int NV, bool IS_MAX, int N>
-__device__ __forceinline__ void warp_reduce(float (&a)[N]) {
-    static_assert(NV <= N, "size");
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-#pragma unroll
-        for (int i = 0; i < NV; ++i) {
-            const float b = __shfl_xor_sync(0xffffffffu, a[i], o);
-            a[i] = IS_MAX ? fmaxf(a[i], b) : a[i] + b;
-        }
-    }
+__device__ __forceinline__ float2 combine2(float2 a, float2 b, bool is_max) {
+    return is_max ? make_float2(fmaxf(a.x, b.x), fmaxf(a.y, b.y))
+                  : make_float2(a.x + b.x, a.y + b.y);
 }
 
-// Called by warp 0 of every CTA of the cluster with the CTA's value of
-// a[0..NV) (identical in all lanes); replaces it with the cluster-wide
-// combination, formed in rank order and identical in every CTA.
-template <int NV, bool IS_MAX, int N>
-__device__ __forceinline__ void cluster_combine(float (&a)[N], const Smem& sm,
-                                                Clu& c) {
-    static_assert(NV % 2 == 0 && NV <= kSlotFloats && NV <= N, "payload");
-    const int lane = threadIdx.x & 31;
-    const uint32_t buf = c.xk & 1u;
-    const uint32_t parity = (c.xk >> 1) & 1u;
-    ++c.xk;
-    float* cs = sm.cslot + buf * c.n * kSlotFloats;
-    if (!c.dead) {
-        if (lane == 0) mbar_arrive_expect_tx(&sm.cbar[buf], c.n * NV * 4);
-        if (lane < c.n) {
-            const uint32_t bar = map_to_rank(smem_addr(&sm.cbar[buf]), lane);
-#pragma unroll
-            for (int i = 0; i < NV; i += 2) {
-                const uint32_t dst = map_to_rank(
-                    smem_addr(&cs[c.rank * kSlotFloats + i]), lane);
-                push_pair(dst, a[i], a[i + 1], bar);
-            }
-        }
-        if (!mbar_wait<true>(&sm.cbar[buf], parity, c.limit)) c.dead = true;
-    }
-#pragma unroll
-    for (int i = 0; i < NV; ++i)
-        a[i] = lane < c.n ? cs[lane * kSlotFloats + i]
-                          : (IS_MAX ? -INFINITY : 0.0f);
-    warp_reduce<NV, IS_MAX>(a);
-}
-
-// Slice-mode exchange across all warps of the CTA (and the cluster): the
-// first NV components of v are summed (or maxed) over every thread.
-template <bool CLUSTER, int NV, bool IS_MAX>
-__device__ __forceinline__ float4 slice_exchange(float4 v, const Smem& sm,
-                                                 Clu& c) {
+// Sum (or max) of every thread's v over the CTA and the cluster; returns
+// the same bits in every thread of the cluster.
+template <bool CLUSTER, bool IS_MAX>
+__device__ __forceinline__ float2 exchange(float2 v, const Smem& sm,
+                                           Exch& x) {
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int warps = blockDim.x >> 5;
-    float a[4] = {v.x, v.y, v.z, v.w};
-    warp_reduce<NV, IS_MAX>(a);
-    if (lane == 0) sm.wslot[warp] = make_float4(a[0], a[1], a[2], a[3]);
+    v = IS_MAX ? warp_max2(v) : warp_sum2(v);
+    float2* ws = sm.wslot + (x.lk & 1u) * x.warps;
+    ++x.lk;
+    if (lane == 0) ws[warp] = v;
     __syncthreads();
-    if (warp == 0) {
-        const float idn = IS_MAX ? -INFINITY : 0.0f;
-        const float4 w = lane < warps ? sm.wslot[lane]
-                                      : make_float4(idn, idn, idn, idn);
-        a[0] = w.x;
-        a[1] = w.y;
-        a[2] = w.z;
-        a[3] = w.w;
-        warp_reduce<NV, IS_MAX>(a);
-        if (CLUSTER) cluster_combine<NV, IS_MAX>(a, sm, c);
-        if (lane == 0) sm.bcast[0] = make_float4(a[0], a[1], a[2], a[3]);
+    const float idn = IS_MAX ? -INFINITY : 0.0f;
+    v = lane < x.warps ? ws[lane] : make_float2(idn, idn);
+    v = IS_MAX ? warp_max2(v) : warp_sum2(v);
+    if (CLUSTER) {
+        const uint32_t buf = x.xk & 1u;
+        const uint32_t parity = (x.xk >> 1) & 1u;
+        ++x.xk;
+        float2* cs = sm.cslot + buf * x.n;
+        if (!x.dead) {
+            if (threadIdx.x == 0) mbar_arrive_expect_tx(&sm.cbar[buf], x.n * 8);
+            if (warp == 0 && lane < x.n) {
+                const uint32_t dst = map_to_rank(smem_addr(&cs[x.rank]), lane);
+                const uint32_t bar = map_to_rank(smem_addr(&sm.cbar[buf]), lane);
+                push_pair(dst, v.x, v.y, bar);
+            }
+            if (!mbar_wait<true>(&sm.cbar[buf], parity, x.limit)) x.dead = true;
+        }
+        v = cs[0];
+        for (int r = 1; r < x.n; ++r) v = combine2(v, cs[r], IS_MAX);
     }
-    __syncthreads();
-    return sm.bcast[0];
+    return v;
 }
 
 // T = 1 pass: rewrites this thread's float4s of the slice as
@@ -256,156 +212,82 @@ __device__ __forceinline__ float2 slice_pass(const float4* row4, int q4,
             }
         }
     }
-    if (GATHER) *cnt = cw;
+    if (GATHER) {
+        *cnt = cw;
+        __syncwarp();
+    }
     return acc.total();
+}
+
+// Pass over the warp's active segment.  RECOMPACT: also drops the classes
+// below thr, compacting the segment in place (entries only move to lower
+// positions, and every lane reads its entry of a round before any lane
+// writes).
+template <bool RECOMPACT>
+__device__ __forceinline__ float2 segment_pass(float* wb, int* cnt, float beta,
+                                               float thr) {
+    const int lane = threadIdx.x & 31;
+    const unsigned lt = (1u << lane) - 1u;
+    const int c = *cnt;
+    float s = 0.0f, v = 0.0f;
+    int nc = 0;
+    for (int j0 = 0; j0 < c; j0 += 32) {
+        const int j = j0 + lane;
+        const float y = j < c ? wb[j] : kYFloor;
+        const float e = ex2(y * beta);
+        s += e;
+        v = fmaf(e, y, v);
+        if (RECOMPACT) {
+            const bool a = j < c && y >= thr;
+            const unsigned msk = __ballot_sync(0xffffffffu, a);
+            __syncwarp();
+            if (a) wb[nc + __popc(msk & lt)] = y;
+            nc += __popc(msk);
+        }
+    }
+    if (RECOMPACT) {
+        *cnt = nc;
+        __syncwarp();
+    }
+    return make_float2(s, v);
+}
+
+// What the next pass of this warp reads (uniform within the warp).
+struct ActiveSet {
+    float* wb;          // this warp's segment
+    int cap;            // its capacity (0: active set off)
+    int cnt;            // classes in the segment
+    bool in_segment;    // the warp reads its segment instead of the slice
+    bool refilter;      // hi dropped: gather (slice) or recompact (segment)
+    float thr;          // y >= thr is active (thr = -K hi)
+};
+
+__device__ __forceinline__ float2 search_partial(const float4* row4, int q4,
+                                                 float beta, ActiveSet& a) {
+    if (a.in_segment) {
+        if (a.refilter) {
+            a.refilter = false;
+            return segment_pass<true>(a.wb, &a.cnt, beta, a.thr);
+        }
+        return segment_pass<false>(a.wb, &a.cnt, beta, a.thr);
+    }
+    if (a.refilter) {
+        a.refilter = false;
+        int c = 0;
+        const float2 part = slice_pass<true>(row4, q4, beta, a.thr, a.wb,
+                                             a.cap, &c);
+        if (c <= a.cap) {
+            a.in_segment = true;
+            a.cnt = c;
+        }
+        return part;
+    }
+    return slice_pass<false>(row4, q4, beta, 0.0f, nullptr, 0, nullptr);
 }
 
 // Midpoint of the search, in the fp32 arithmetic every variant uses.
 __device__ __forceinline__ float midpoint(float lo, float hi) {
     return 0.5f * (lo + hi);
-}
-
-// Search state (identical in every thread that runs the search).
-struct Search {
-    float lo, hi, s_lo;
-    bool lo_eval, hi_eval;
-    int k;            // bisection steps taken
-};
-
-// Applies one evaluated step at `mid` with the cluster sums (S, V) at beta;
-// returns true if mid was infeasible (hi moved).
-__device__ __forceinline__ bool apply_step(Search& st, float mid, float beta,
-                                           float S, float V,
-                                           float bound_bits) {
-    ++st.k;
-    if (entropy_above(make_float2(S, V), beta, bound_bits)) {
-        st.hi = mid;
-        st.hi_eval = true;
-        return true;
-    }
-    st.lo = mid;
-    st.lo_eval = true;
-    st.s_lo = S;
-    return false;
-}
-
-// True when no step remains: max_iter steps taken, or the next fp32
-// midpoint equals an end already evaluated (every further step would
-// repeat that evaluation and change nothing).
-__device__ __forceinline__ bool search_finished(const Search& st,
-                                                int max_iter) {
-    if (st.k >= max_iter) return true;
-    const float mid = midpoint(st.lo, st.hi);
-    return (mid == st.lo && st.lo_eval) || (mid == st.hi && st.hi_eval);
-}
-
-// Active-set mode, run by warp 0 alone: evaluates the P = 2^D - 1
-// midpoints of the next D levels in one pass over the CTA's segments,
-// combines them across the cluster, then walks them with the sequential
-// search's decisions.
-template <bool CLUSTER, int D>
-__device__ __forceinline__ void active_step(Search& st, const Smem& sm,
-                                            int warps, int cap_w,
-                                            float bound_bits, int max_iter,
-                                            Clu& c) {
-    constexpr int P = (1 << D) - 1;
-    const int lane = threadIdx.x & 31;
-    // Heap of midpoints: node i (0-based) has children 2i+1 (the lower half,
-    // taken when mid_i is infeasible) and 2i+2 (the upper half).
-    float mids[P], los[P], his[P], beta[P];
-    los[0] = st.lo;
-    his[0] = st.hi;
-#pragma unroll
-    for (int i = 0; i < P; ++i) {
-        mids[i] = midpoint(los[i], his[i]);
-        beta[i] = __frcp_rn(mids[i]);
-        if (2 * i + 2 < P) {
-            los[2 * i + 1] = los[i];
-            his[2 * i + 1] = mids[i];
-            los[2 * i + 2] = mids[i];
-            his[2 * i + 2] = his[i];
-        }
-    }
-    float a[2 * P];
-#pragma unroll
-    for (int i = 0; i < 2 * P; ++i) a[i] = 0.0f;
-    for (int w = 0; w < warps; ++w) {
-        const float* seg = sm.wbuf + w * cap_w;
-        const int cnt = sm.segcnt[w];
-        for (int j = lane; j < cnt; j += 32) {
-            const float y = seg[j];
-#pragma unroll
-            for (int i = 0; i < P; ++i) {
-                const float e = ex2(y * beta[i]);
-                a[2 * i] += e;
-                a[2 * i + 1] = fmaf(e, y, a[2 * i + 1]);
-            }
-        }
-    }
-    warp_reduce<2 * P, false>(a);
-    if (CLUSTER) cluster_combine<2 * P, false>(a, sm, c);
-    int node = 0;
-#pragma unroll
-    for (int d = 0; d < D; ++d) {
-        if (search_finished(st, max_iter)) break;
-        // Select node's values with compares (no dynamic register indexing).
-        float m = mids[0], b = beta[0], S = a[0], V = a[1];
-#pragma unroll
-        for (int i = 1; i < P; ++i) {
-            if (i == node) {
-                m = mids[i];
-                b = beta[i];
-                S = a[2 * i];
-                V = a[2 * i + 1];
-            }
-        }
-        const bool infeasible = apply_step(st, m, b, S, V, bound_bits);
-        node = infeasible ? 2 * node + 1 : 2 * node + 2;
-    }
-}
-
-// Drops the classes below thr from every segment, in place (warp 0).
-__device__ __forceinline__ void refilter_segments(const Smem& sm, int warps,
-                                                  int cap_w, float thr) {
-    const int lane = threadIdx.x & 31;
-    const unsigned lt = (1u << lane) - 1u;
-    for (int w = 0; w < warps; ++w) {
-        float* seg = sm.wbuf + w * cap_w;
-        const int cnt = sm.segcnt[w];
-        int nc = 0;
-        for (int j0 = 0; j0 < cnt; j0 += 32) {
-            const int j = j0 + lane;
-            const float y = j < cnt ? seg[j] : kYFloor;
-            const bool keep = j < cnt && y >= thr;
-            const unsigned msk = __ballot_sync(0xffffffffu, keep);
-            __syncwarp();  // every lane has read its entry of this round
-            if (keep) seg[nc + __popc(msk & lt)] = y;
-            nc += __popc(msk);
-        }
-        __syncwarp();
-        if (lane == 0) sm.segcnt[w] = nc;
-        __syncwarp();
-    }
-}
-
-// S and V at beta over the active segments (warp 0), cluster-wide.
-template <bool CLUSTER>
-__device__ __forceinline__ float2 active_eval(const Smem& sm, int warps,
-                                              int cap_w, float beta, Clu& c) {
-    const int lane = threadIdx.x & 31;
-    float a[2] = {0.0f, 0.0f};
-    for (int w = 0; w < warps; ++w) {
-        const float* seg = sm.wbuf + w * cap_w;
-        const int cnt = sm.segcnt[w];
-        for (int j = lane; j < cnt; j += 32) {
-            const float e = ex2(seg[j] * beta);
-            a[0] += e;
-            a[1] = fmaf(e, seg[j], a[1]);
-        }
-    }
-    warp_reduce<2, false>(a);
-    if (CLUSTER) cluster_combine<2, false>(a, sm, c);
-    return make_float2(a[0], a[1]);
 }
 
 __device__ __forceinline__ void store_scalar_lanes(float* dst, int q, int pad,
@@ -452,7 +334,6 @@ cluster_kernel(RowTask t, int n, int slice_len, int cap_w) {
     const int nt = blockDim.x;
     const int warps = nt >> 5;
     const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
     const uint32_t rank = CLUSTER ? cluster_ctarank() : 0u;
     const int64_t cid = blockIdx.x / n;
     const int64_t ncl = gridDim.x / n;
@@ -460,10 +341,8 @@ cluster_kernel(RowTask t, int n, int slice_len, int cap_w) {
     Smem sm;
     {
         const ClusterSmemLayout L = cluster_smem_layout(warps, n, cap_w);
-        sm.cslot = reinterpret_cast<float*>(smem + L.cslot);
-        sm.wslot = reinterpret_cast<float4*>(smem + L.wslot);
-        sm.bcast = reinterpret_cast<float4*>(smem + L.bcast);
-        sm.segcnt = reinterpret_cast<int*>(smem + L.segcnt);
+        sm.cslot = reinterpret_cast<float2*>(smem + L.cslot);
+        sm.wslot = reinterpret_cast<float2*>(smem + L.wslot);
         sm.cbar = reinterpret_cast<uint64_t*>(smem + L.cbar);
         sm.lbar = reinterpret_cast<uint64_t*>(smem + L.lbar);
         sm.wbuf = reinterpret_cast<float*>(smem + L.wbuf);
@@ -487,7 +366,7 @@ cluster_kernel(RowTask t, int n, int slice_len, int cap_w) {
                                          min(static_cast<int64_t>(slice_len), C - s0)));
     const float bound_bits = t.entropy_bound * kLog2e;
     const bool prune = cap_w > 0 && t.prune_k > 0.0f;
-    Clu clu{n, rank, 0u, t.wait_limit_cycles, false};
+    Exch x{warps, n, rank, 0u, 0u, t.wait_limit_cycles, false};
     uint32_t lphase = 0;       // parity bit per load chunk
     bool reported = false;
 
@@ -499,7 +378,7 @@ cluster_kernel(RowTask t, int n, int slice_len, int cap_w) {
 
         // Stage: thread 0 issues the bulk copies; threads 0-7 fetch the
         // ragged head/tail float4s with plain loads.
-        if (threadIdx.x == 0 && !clu.dead) {
+        if (threadIdx.x == 0 && !x.dead) {
             fence_proxy_async_smem();
             for (int c = 0; c < nch; ++c) {
                 const int qa = chunk_begin(s, nch, c);
@@ -529,9 +408,9 @@ cluster_kernel(RowTask t, int n, int slice_len, int cap_w) {
 
         // Max pass, chunk by chunk as the copies land.
         for (int c = 0; c < nch; ++c) {
-            if (!clu.dead &&
-                !mbar_wait<false>(&sm.lbar[c], (lphase >> c) & 1u, clu.limit))
-                clu.dead = true;
+            if (!x.dead &&
+                !mbar_wait<false>(&sm.lbar[c], (lphase >> c) & 1u, x.limit))
+                x.dead = true;
             lphase ^= 1u << c;
             const int qa = chunk_begin(s, nch, c);
             const int qz = chunk_begin(s, nch, c + 1);
@@ -559,8 +438,7 @@ cluster_kernel(RowTask t, int n, int slice_len, int cap_w) {
                 }
             }
         }
-        const float4 mc = slice_exchange<CLUSTER, 2, true>(
-            make_float4(m_loc, code, 0.f, 0.f), sm, clu);
+        const float2 mc = exchange<CLUSTER, true>(make_float2(m_loc, code), sm, x);
         const float m = mc.x;
         const int row_code = static_cast<int>(mc.y);
 
@@ -569,112 +447,54 @@ cluster_kernel(RowTask t, int n, int slice_len, int cap_w) {
         float T_row = NAN;
         float beta_out = 0.0f, inv_s = 0.0f;
         if (row_code == 0) {
-            const float2 p1 = transform_pass(row4, s.q4, m);
-            const float4 sv = slice_exchange<CLUSTER, 2, false>(
-                make_float4(p1.x, p1.y, 0.f, 0.f), sm, clu);
-            if (!entropy_above(make_float2(sv.x, sv.y), 1.0f, bound_bits)) {
+            float2 sv = exchange<CLUSTER, false>(transform_pass(row4, s.q4, m),
+                                                 sm, x);
+            if (!entropy_above(sv, 1.0f, bound_bits)) {
                 T_row = 1.0f;
                 beta_out = 1.0f;
                 inv_s = 1.0f / sv.x;
             } else {
-                Search st{t.t_min, t.hi0, 0.0f, false, t.hi0 == 1.0f, 0};
-                bool gather = false;   // gather active classes in this step
-                bool active = false;   // switched to active-set mode
-                if (st.lo < st.hi) {
-                    // Slice mode: every warp, one step per exchange.
-                    while (!search_finished(st, t.max_iter)) {
-                        const float mid = midpoint(st.lo, st.hi);
-                        const float b = __frcp_rn(mid);
-                        float4 sv4;
-                        if (gather) {
-                            int cw = 0;
-                            const float2 pp = slice_pass<true>(
-                                row4, s.q4, b, -t.prune_k * st.hi,
-                                sm.wbuf + warp * cap_w, cap_w, &cw);
-                            if (lane == 0) sm.segcnt[warp] = cw;
-                            // z: warps that overflowed; w: classes gathered.
-                            sv4 = slice_exchange<CLUSTER, 4, false>(
-                                make_float4(pp.x, pp.y,
-                                            lane == 0 && cw > cap_w ? 1.f : 0.f,
-                                            lane == 0 ? static_cast<float>(cw) : 0.f),
-                                sm, clu);
+                ActiveSet a{sm.wbuf + warp * cap_w, prune ? cap_w : 0, 0,
+                            false, false, 0.0f};
+                float lo = t.t_min, hi = t.hi0;
+                bool lo_eval = false;
+                bool hi_eval = hi == 1.0f;   // H(1) > bound is known
+                float s_lo = 0.0f;
+                if (lo < hi) {
+                    for (int k = 0; k < t.max_iter; ++k) {
+                        const float mid = midpoint(lo, hi);
+                        // Exact early exit: the fp32 midpoint has reached an
+                        // end whose side is already known, so every further
+                        // step repeats the same evaluation.
+                        if ((mid == lo && lo_eval) || (mid == hi && hi_eval)) break;
+                        const float b = rcp_approx(mid);
+                        sv = exchange<CLUSTER, false>(
+                            search_partial(row4, s.q4, b, a), sm, x);
+                        if (entropy_above(sv, b, bound_bits)) {
+                            hi = mid;
+                            hi_eval = true;
+                            if (a.cap > 0) {
+                                a.thr = -t.prune_k * hi;
+                                a.refilter = true;
+                            }
                         } else {
-                            const float2 pp = slice_pass<false>(
-                                row4, s.q4, b, 0.0f, nullptr, 0, nullptr);
-                            sv4 = slice_exchange<CLUSTER, 2, false>(
-                                make_float4(pp.x, pp.y, 0.f, 0.f), sm, clu);
+                            lo = mid;
+                            lo_eval = true;
+                            s_lo = sv.x;
                         }
-                        const bool hi_moved =
-                            apply_step(st, mid, b, sv4.x, sv4.y, bound_bits);
-                        if (gather) {
-                            gather = false;
-                            if (sv4.z == 0.0f &&
-                                sv4.w <= static_cast<float>(kSearchWarpMax * n)) {
-                                active = true;
-                                break;
-                            }
-                        }
-                        if (prune && hi_moved) gather = true;
                     }
                 }
-                if (active) {
-                    // Active-set mode: warp 0 of each CTA finishes alone.
-                    if (warp == 0) {
-                        float filtered_hi = st.hi;
-                        refilter_segments(sm, warps, cap_w, -t.prune_k * st.hi);
-                        while (!search_finished(st, t.max_iter)) {
-                            if (st.hi < filtered_hi) {
-                                refilter_segments(sm, warps, cap_w,
-                                                  -t.prune_k * st.hi);
-                                filtered_hi = st.hi;
-                            }
-                            const int left = t.max_iter - st.k;
-                            if (left >= kSpecLevels)
-                                active_step<CLUSTER, kSpecLevels>(
-                                    st, sm, warps, cap_w, bound_bits,
-                                    t.max_iter, clu);
-                            else if (left == 2)
-                                active_step<CLUSTER, 2>(st, sm, warps, cap_w,
-                                                        bound_bits, t.max_iter,
-                                                        clu);
-                            else
-                                active_step<CLUSTER, 1>(st, sm, warps, cap_w,
-                                                        bound_bits, t.max_iter,
-                                                        clu);
-                        }
-                        if (!st.lo_eval) {
-                            // lo is still t_min: evaluate it (section 5.4).
-                            const float b_lo = __frcp_rn(st.lo);
-                            const float2 e = active_eval<CLUSTER>(
-                                sm, warps, cap_w, b_lo, clu);
-                            st.s_lo = e.x;
-                            if (entropy_above(e, b_lo, bound_bits))
-                                bits |= kBitOverflow;
-                        }
-                        if (lane == 0)
-                            sm.bcast[1] = make_float4(st.lo, st.s_lo,
-                                                      __uint_as_float(bits), 0.f);
-                    }
-                    __syncthreads();
-                    const float4 res = sm.bcast[1];
-                    st.lo = res.x;
-                    st.s_lo = res.y;
-                    bits = __float_as_uint(res.z);
-                } else if (!st.lo_eval) {
-                    // lo is still t_min: evaluate it (section 5.4).
-                    const float b_lo = __frcp_rn(st.lo);
-                    const float2 pp = slice_pass<false>(row4, s.q4, b_lo, 0.0f,
-                                                        nullptr, 0, nullptr);
-                    const float4 sv4 = slice_exchange<CLUSTER, 2, false>(
-                        make_float4(pp.x, pp.y, 0.f, 0.f), sm, clu);
-                    st.s_lo = sv4.x;
-                    if (entropy_above(make_float2(sv4.x, sv4.y), b_lo,
-                                      bound_bits))
-                        bits |= kBitOverflow;
+                const float b_lo = rcp_approx(lo);
+                if (!lo_eval) {
+                    // lo is still t_min: evaluate it (section 5.4 check).
+                    sv = exchange<CLUSTER, false>(
+                        search_partial(row4, s.q4, b_lo, a), sm, x);
+                    s_lo = sv.x;
+                    if (entropy_above(sv, b_lo, bound_bits)) bits |= kBitOverflow;
                 }
-                T_row = st.lo;
-                beta_out = __frcp_rn(st.lo);
-                inv_s = 1.0f / st.s_lo;
+                T_row = lo;
+                beta_out = b_lo;
+                inv_s = 1.0f / s_lo;
             }
         } else {
             bits = row_code == 2 ? kBitNan : kBitInf;
@@ -684,14 +504,14 @@ cluster_kernel(RowTask t, int n, int slice_len, int cap_w) {
             if (t.t_out) t.t_out[r] = T_row;
             raise_error(t.err, bits);
         }
-        if (clu.dead && !reported) {
+        if (x.dead && !reported) {
             raise_error(t.err, kBitTimeout);
             reported = true;
         }
         // The slice buffer is rewritten by the next row's copies.
         __syncthreads();
     }
-    if (clu.dead && threadIdx.x == 0) {
+    if (x.dead && threadIdx.x == 0) {
         // Give copies still in flight a bounded chance to land before exit.
         for (int c = 0; c < kLoadChunks; ++c)
             mbar_wait<false>(&sm.lbar[c], ((lphase >> c) & 1u) ^ 1u,

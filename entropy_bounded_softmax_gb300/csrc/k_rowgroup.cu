@@ -148,7 +148,7 @@ rowgroup_kernel(RowTask t, int vec) {
                     for (int k = 0; k < t.max_iter; ++k) {
                         const float mid = 0.5f * (lo + hi);
                         if ((mid == lo && lo_eval) || (mid == hi && hi_eval)) break;
-                        const float b = __frcp_rn(mid);
+                        const float b = rcp_approx(mid);
                         sv = group_sum2<G>(reg_pass<E4>(y, b), gmask);
                         if (entropy_above(sv, b, bound_bits)) {
                             hi = mid;
@@ -160,7 +160,7 @@ rowgroup_kernel(RowTask t, int vec) {
                         }
                     }
                 }
-                const float b_lo = __frcp_rn(lo);
+                const float b_lo = rcp_approx(lo);
                 if (!lo_eval) {
                     sv = group_sum2<G>(reg_pass<E4>(y, b_lo), gmask);
                     s_lo = sv.x;
