@@ -65,6 +65,9 @@ def parse_args(argv=None):
     ap.add_argument("--full-scan", action="store_true",
                     help="cluster variant: evaluate every class at every "
                          "step (no active set)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="use only the first BATCH rows of the workload "
+                         "(profiling captures); 0 = the whole workload")
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--soak-s", type=float, default=1.5,
                     help="untimed load before the timed region, for the "
@@ -529,6 +532,9 @@ def our_arm(args, w: wl.Workload) -> int:
 def main(argv=None) -> int:
     args = parse_args(argv)
     w = find_workload(args.workload)
+    if args.batch:
+        w = w.with_(batch=min(args.batch, w.batch),
+                    name=f"{w.name}[:{min(args.batch, w.batch)}]")
     if args.impl == "reference":
         return reference_arm(args, w)
     return our_arm(args, w)
