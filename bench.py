@@ -62,7 +62,7 @@ def parse_args(argv=None):
                     help="lanes per row (rowgroup) or CTAs per row (cluster)")
     ap.add_argument("--threads", type=int, default=0,
                     help="cluster variant: threads per CTA (0 = automatic)")
-    ap.add_argument("--full-scan", action="store_true",
+    ap.add_argument("--strict", action="store_true",
                     help="cluster variant: evaluate every class at every "
                          "step (no active set)")
     ap.add_argument("--batch", type=int, default=0,
@@ -333,7 +333,7 @@ def our_arm(args, w: wl.Workload) -> int:
     stream = torch.cuda.current_stream(dev)
     sptr = stream.cuda_stream
     opts = cs.options(cs.VARIANTS[args.variant], args.param, args.threads,
-                      int(args.full_scan))
+                      int(args.strict))
 
     # Inputs larger than L2 between timed launches: rotate through enough
     # input/output pairs that one pass over them is >= 3x L2.
@@ -361,7 +361,7 @@ def our_arm(args, w: wl.Workload) -> int:
         launch(i)
     torch.cuda.synchronize()
     plan = cs.plan(B, C, args.variant, args.param, args.threads,
-                   args.full_scan)
+                   args.strict)
 
     sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ
                            else 0)
@@ -429,7 +429,7 @@ def our_arm(args, w: wl.Workload) -> int:
                                       w.max_iter, return_t=True,
                                       variant=args.variant, param=args.param,
                                       threads=args.threads,
-                                      full_scan=args.full_scan)
+                                      strict=args.strict)
         h_out.copy_(p, non_blocking=True)
         h_t.copy_(T, non_blocking=True)
     torch.cuda.synchronize()
@@ -444,7 +444,7 @@ def our_arm(args, w: wl.Workload) -> int:
                                w.max_iter, out=out_e2e, t_out=t_e2e,
                                variant=args.variant, param=args.param,
                                threads=args.threads,
-                               full_scan=args.full_scan)
+                               strict=args.strict)
         h_out.copy_(out_e2e, non_blocking=True)
         h_t.copy_(t_e2e, non_blocking=True)
     e1.record(stream)
@@ -510,7 +510,7 @@ def our_arm(args, w: wl.Workload) -> int:
             "dtype": "f32", "data": "synthetic",
             "config": dict(workload_config(w, l2_note),
                            parallelism=f"replicas x{world}",
-                           variant=args.variant, full_scan=args.full_scan,
+                           variant=args.variant, strict=args.strict,
                            plan=plan),
             "roofline": roof, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "rows/s",

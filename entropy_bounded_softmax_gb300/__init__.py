@@ -60,14 +60,14 @@ def constrained_softmax(logits, entropy_bound: float = DEFAULT_ENTROPY_BOUND,
                         max_iter: int = DEFAULT_MAX_ITER,
                         return_t: bool = False, out=None, t_out=None,
                         variant: str = "auto", param: int = 0,
-                        threads: int = 0, full_scan: bool = False):
+                        threads: int = 0, strict: bool = False):
     """Entropy-bounded softmax of a CUDA fp32 [batch, num_classes] tensor.
 
     Returns the probabilities (and the per-row temperature if ``return_t``).
     ``out``/``t_out`` may be given to write into existing tensors.  The call
     is asynchronous on the current stream; per-row conditions (NaN/Inf rows,
     unsatisfiable bounds) are read with :func:`get_error`.
-    ``variant``/``param``/``threads``/``full_scan`` are the launch options
+    ``variant``/``param``/``threads``/``strict`` are the launch options
     of ``cs_constrained_softmax_ex`` (defaults: automatic).
     """
     import torch
@@ -102,7 +102,7 @@ def constrained_softmax(logits, entropy_bound: float = DEFAULT_ENTROPY_BOUND,
         st = cs_constrained_softmax_ex(
             logits.data_ptr(), out.data_ptr(), batch, num_classes,
             float(entropy_bound), float(t_min), float(t_max), int(max_iter),
-            t_ptr, options(VARIANTS[variant], param, threads, int(full_scan)),
+            t_ptr, options(VARIANTS[variant], param, threads, int(strict)),
             _stream_handle(logits.device))
     if st != 0:
         raise CsError(st, "cs_constrained_softmax")
@@ -123,11 +123,11 @@ def get_error(device=None) -> set[str]:
 
 
 def plan(batch: int, num_classes: int, variant: str = "auto",
-         param: int = 0, threads: int = 0, full_scan: bool = False) -> dict:
+         param: int = 0, threads: int = 0, strict: bool = False) -> dict:
     """The launch plan for this shape on the current device."""
     st, p = cs_plan_launch(batch, num_classes,
                            options(VARIANTS[variant], param, threads,
-                                   int(full_scan)))
+                                   int(strict)))
     if st != 0:
         raise CsError(st, "cs_plan_launch")
     return p.as_dict()

@@ -24,7 +24,7 @@ class cs_options(ctypes.Structure):
         ("variant", ctypes.c_int32),
         ("param", ctypes.c_int32),
         ("threads", ctypes.c_int32),
-        ("full_scan", ctypes.c_int32),
+        ("strict", ctypes.c_int32),
     ]
 
 
@@ -38,8 +38,6 @@ class cs_plan(ctypes.Structure):
         ("threads_per_cta", ctypes.c_int32),
         ("smem_bytes", ctypes.c_int32),
         ("ctas_per_sm", ctypes.c_int32),
-        ("warp_buffer", ctypes.c_int32),
-        ("prune_k", ctypes.c_float),
         ("grid_ctas", ctypes.c_int64),
     ]
 
@@ -121,9 +119,9 @@ def cs_constrained_softmax(logits, out, batch, num_classes, entropy_bound,
                                          max_iter, t_out, stream)
 
 
-def options(variant=0, param=0, threads=0, full_scan=0):
+def options(variant=0, param=0, threads=0, strict=0):
     """A cs_options struct (all zero = automatic)."""
-    return cs_options(int(variant), int(param), int(threads), int(full_scan))
+    return cs_options(int(variant), int(param), int(threads), int(strict))
 
 
 def _opt_ref(opt):

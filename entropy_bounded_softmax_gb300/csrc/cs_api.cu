@@ -138,29 +138,19 @@ cs_status plan_rowgroup(int64_t batch, int32_t C, int32_t param,
     return CS_OK;
 }
 
-// Cluster plan for n CTAs per row: slice, threads, active-set segments and
-// shared memory.  Returns false if it does not fit smem_optin.
+// Cluster plan for n CTAs per row: slice, threads and shared memory.
+// Returns false if it does not fit smem_optin.
 bool cluster_geometry(int64_t batch, int32_t C, int n, int threads_req,
-                      bool prune, int sm_count, int smem_optin, cs_plan* p) {
+                      int sm_count, int smem_optin, cs_plan* p) {
     const int64_t L = ceil_div(ceil_div(C, n), 4) * 4;
     const int threads = threads_req
         ? threads_req : cs::cluster_threads_for(L, batch * n, sm_count);
-    const int warps = threads / 32;
-    const int64_t base = cs::cluster_smem_bytes(L, threads, n, 0);
-    if (base > smem_optin) return false;
-    int cap = 0;
-    if (prune) {
-        int64_t room = (smem_optin - base) / (4 * warps);
-        room = (room / 32) * 32;
-        if (room > cs::kMaxWarpBuffer) room = cs::kMaxWarpBuffer;
-        if (room >= cs::kMinWarpBuffer) cap = static_cast<int>(room);
-    }
+    const int64_t smem = cs::cluster_smem_bytes(L, threads, n);
+    if (smem > smem_optin) return false;
     p->cluster_size = n;
     p->slice_len = static_cast<int32_t>(L);
     p->threads_per_cta = threads;
-    p->warp_buffer = cap;
-    p->prune_k = cap > 0 ? cs::prune_threshold(C) : 0.0f;
-    p->smem_bytes = static_cast<int32_t>(cs::cluster_smem_bytes(L, threads, n, cap));
+    p->smem_bytes = static_cast<int32_t>(smem);
     return true;
 }
 
@@ -170,8 +160,7 @@ cs_status plan_cluster(int64_t batch, int32_t C, const cs_options& o,
     if (o.threads != 0 &&
         (o.threads < 64 || o.threads > cs::kClusterMaxThreads || o.threads % 32))
         return CS_ERR_INVALID_ARG;
-    if (o.full_scan != 0 && o.full_scan != 1) return CS_ERR_INVALID_ARG;
-    const bool prune = o.full_scan == 0;
+    if (o.strict != 0 && o.strict != 1) return CS_ERR_INVALID_ARG;
     *p = cs_plan{};
     p->variant = CS_VARIANT_CLUSTER;
     if (o.param == 0) {
@@ -188,13 +177,13 @@ cs_status plan_cluster(int64_t batch, int32_t C, const cs_options& o,
         if (widen > n0) n0 = static_cast<int>(widen);
         bool ok = false;
         for (int c = n0; c <= max_cluster && !ok; ++c)
-            ok = cluster_geometry(batch, C, c, o.threads, prune, sm_count,
+            ok = cluster_geometry(batch, C, c, o.threads, sm_count,
                                   smem_optin, p);
         if (!ok) return CS_ERR_OOM;
     } else {
         if (o.param < 1 || o.param > cs::kMaxCluster) return CS_ERR_INVALID_ARG;
         if (o.param > max_cluster) return CS_ERR_INVALID_ARG;
-        if (!cluster_geometry(batch, C, o.param, o.threads, prune, sm_count,
+        if (!cluster_geometry(batch, C, o.param, o.threads, sm_count,
                               smem_optin, p))
             return CS_ERR_OOM;
     }
@@ -251,7 +240,7 @@ cs_status cs_plan_host(int64_t batch, int32_t num_classes,
                                                            : CS_VARIANT_CLUSTER;
     }
     if (o.variant == CS_VARIANT_ROWGROUP) {
-        if (o.threads != 0 || (o.full_scan != 0 && o.full_scan != 1))
+        if (o.threads != 0 || (o.strict != 0 && o.strict != 1))
             return CS_ERR_INVALID_ARG;
         return plan_rowgroup(batch, num_classes, o.param, plan);
     }
@@ -300,7 +289,7 @@ cs_status cs_constrained_softmax_ex(const float* logits, float* out,
     task.entropy_bound = entropy_bound;
     task.t_min = t_min;
     task.hi0 = t_max < 1.0f ? t_max : 1.0f;
-    task.prune_k = p.prune_k;
+    task.strict = options ? options->strict : 0;
     task.wait_limit_cycles = cs::kWaitLimitCycles;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -309,8 +298,7 @@ cs_status cs_constrained_softmax_ex(const float* logits, float* out,
         e = cs::launch_rowgroup(task, p.lanes_per_row, p.elems_per_lane, s);
     } else {
         e = cs::launch_cluster(task, p.cluster_size, p.slice_len,
-                               p.threads_per_cta, p.warp_buffer, p.smem_bytes,
-                               p.grid_ctas, s);
+                               p.threads_per_cta, p.smem_bytes, p.grid_ctas, s);
     }
     if (e != cudaSuccess) {
         cudaGetLastError();

@@ -34,53 +34,47 @@ struct RowTask {
     float entropy_bound;
     float t_min;
     float hi0;             // min(1, t_max): upper end of the search
-    float prune_k;         // active-set threshold K (0: no pruning)
+    int32_t strict;        // 1: evaluate every bisection midpoint
     uint64_t wait_limit_cycles;
 };
 
 // Cluster kernel geometry.
 constexpr int kMaxCluster = 16;
 constexpr int kLoadChunks = 8;        // bulk copies per CTA slice
-constexpr int kClusterMaxThreads = 1024;
-
-// Per-warp active-set buffer of the cluster kernel: up to this many floats
-// (8 per lane); below kMinWarpBuffer pruning is off.
-constexpr int kMaxWarpBuffer = 256;
-constexpr int kMinWarpBuffer = 64;
+constexpr int kClusterMaxThreads = 512;
+constexpr int kSlotVals = 12;         // floats per exchange slot
 
 // Byte offsets of the cluster kernel's dynamic shared memory for `warps`
-// warps, cluster size n and cap_w floats of active segment per warp:
-// cluster slots [2][n] float2, per-warp exchange slots [2][warps] float2,
-// the two cluster mbarriers and the load mbarriers; then (128-byte aligned)
-// the active segments and the slice.
+// warps and cluster size n: cluster slots [2][n][kSlotVals] floats, per-warp
+// slots [2][warps][kSlotVals], a broadcast slot, the two cluster mbarriers
+// and the load mbarriers; then (128-byte aligned) the slice.
 struct ClusterSmemLayout {
-    int cslot, wslot, cbar, lbar, wbuf, row;
+    int cslot, wslot, bcast, cbar, lbar, row;
 };
 
 __host__ __device__ inline ClusterSmemLayout cluster_smem_layout(int warps,
-                                                                 int n,
-                                                                 int cap_w) {
+                                                                 int n) {
     ClusterSmemLayout L;
     int p = 0;
     L.cslot = p;
-    p += 2 * n * 8;
+    p += 2 * n * kSlotVals * 4;
     L.wslot = p;
-    p += 2 * warps * 8;
+    p += 2 * warps * kSlotVals * 4;
+    L.bcast = p;
+    p += kSlotVals * 4;
+    p = ((p + 7) / 8) * 8;
     L.cbar = p;
     p += 2 * 8;
     L.lbar = p;
     p += kLoadChunks * 8;
-    L.wbuf = ((p + 127) / 128) * 128;
-    L.row = L.wbuf + warps * cap_w * 4;
+    L.row = ((p + 127) / 128) * 128;
     return L;
 }
 
 // Dynamic shared memory of the cluster kernel for a slice of `slice_len`
-// classes, `threads` threads, cluster size `n` and `cap_w` floats of
-// active segment per warp (cap_w a multiple of 32).
-inline int64_t cluster_smem_bytes(int64_t slice_len, int threads, int n,
-                                  int cap_w) {
-    const ClusterSmemLayout L = cluster_smem_layout(threads / 32, n, cap_w);
+// classes, `threads` threads and cluster size `n`.
+inline int64_t cluster_smem_bytes(int64_t slice_len, int threads, int n) {
+    const ClusterSmemLayout L = cluster_smem_layout(threads / 32, n);
     const int64_t row = ((slice_len + 8 + 3) / 4) * 16;  // pad + tail room
     return L.row + row;
 }
@@ -104,19 +98,11 @@ inline int cluster_threads_for(int64_t slice_len, int64_t ctas,
     return static_cast<int>(t);
 }
 
-// Active-set threshold K for rows of C classes: 36 + ceil(log2 C).
-inline float prune_threshold(int64_t C) {
-    int lg = 0;
-    while ((int64_t{1} << lg) < C) ++lg;
-    return static_cast<float>(36 + lg);
-}
-
 cudaError_t launch_rowgroup(const RowTask& task, int lanes_per_row,
                             int elems_per_lane, cudaStream_t stream);
 cudaError_t launch_cluster(const RowTask& task, int cluster_size,
-                           int slice_len, int threads, int cap_w,
-                           int smem_bytes, int64_t grid_ctas,
-                           cudaStream_t stream);
+                           int slice_len, int threads, int smem_bytes,
+                           int64_t grid_ctas, cudaStream_t stream);
 cudaError_t launch_probe_ex2(float* sink, int iters, int blocks, int threads,
                              cudaStream_t stream);
 cudaError_t launch_wait_timeout(unsigned int* err, uint64_t limit_cycles,

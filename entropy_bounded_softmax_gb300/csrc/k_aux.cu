@@ -62,7 +62,7 @@ cudaError_t launch_wait_timeout(unsigned int* err, uint64_t limit_cycles,
 
 namespace {
 constexpr int kMaxDevices = 64;
-constexpr int kSlots = 2;
+constexpr int kSlots = 4;
 // Largest MaxDynamicSharedMemorySize set so far, per device and kernel.
 std::atomic<int> g_smem_set[kMaxDevices][kSlots];
 std::mutex g_smem_mu;
@@ -82,7 +82,7 @@ cudaError_t ensure_smem_attribute(const void* func, int slot, int bytes) {
     e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              bytes);
     if (e != cudaSuccess) return e;
-    if (slot == 1) {
+    if (slot == 1 || slot == 3) {
         e = cudaFuncSetAttribute(
             func, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;

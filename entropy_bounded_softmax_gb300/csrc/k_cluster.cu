@@ -11,42 +11,33 @@
 //   max     m = max_i l_i (T-independent, computed once) and a finiteness
 //           check, exchanged across the cluster;
 //   T = 1   one pass turns the slice into y_i = (l_i - m) log2(e) in place
-//           and sums S = sum 2^y_i and V = sum y_i 2^y_i;
-//   search  each bisection step evaluates, at beta = 1/mid,
-//           S(beta) = sum 2^(beta y_i) and V(beta) = sum y_i 2^(beta y_i);
-//           with p_i = 2^(beta y_i) / S the entropy in nats is
-//           H = ln 2 (log2 S - beta V / S), and H > bound is decided as
-//           S (log2 S - bound log2 e) - beta V > 0;
-//   output  p_i = 2^(beta_lo y_i) / S(lo), reusing S(lo) from the step that
-//           set lo, written with 128-bit streaming stores.
+//           and sums S = sum 2^y_i, V = sum y_i 2^y_i, W = sum y_i^2 2^y_i;
+//           H(1) = ln2 (log2 S - V/S) decides whether a search is needed;
+//   search  rounds of the temperature search of cs_search.cuh: each round
+//           evaluates (S, V, W) at 1-3 temperatures in one pass over the
+//           slice and reduces them; the search returns the bisection's
+//           final lo and S(lo);
+//   output  p_i = 2^(beta_lo y_i) / S(lo), written with 128-bit streaming
+//           stores.
 //
-// Reduction.  Every warp reduces its (S, V) with a shuffle tree and writes
-// the pair to a slot; after one __syncthreads every warp reduces the slots
-// with a second shuffle tree.  In a cluster, warp 0 then pushes the CTA's
-// pair into every CTA (st.async, counted on an mbarrier) and every thread
-// sums the cluster's pairs in rank order once the mbarrier completes.  All
-// threads of the cluster thus see bit-identical sums and take the same
-// decision.  Slots are double-buffered, which is safe because no thread can
-// reach exchange k+2 before every thread has left exchange k.
+// Reduction.  Every warp reduces its partial sums with a shuffle tree and
+// writes them to a slot; after a __syncthreads the per-warp slots are
+// reduced by a second shuffle tree (in every warp for one pair of values,
+// else in warp 0, which broadcasts the result through shared memory after a
+// second __syncthreads).  In a cluster, warp 0 then pushes the CTA's sums
+// into every CTA (st.async, counted on an mbarrier) and the waiting threads
+// add the cluster's sums in rank order.  All threads of the cluster thus see
+// bit-identical sums and take the same decisions.  Slots are double-
+// buffered, which is safe because no thread can reach exchange k+2 before
+// every thread has left exchange k.
 //
-// Active set.  Every later step evaluates at beta = 1/mid >= 1/hi, so a class
-// with y_i < -K hi contributes less than 2^-K to S (which is >= 1: the
-// maximum contributes 1) at every remaining step.  With K = 36 + log2(C)
-// all such classes together change S and beta V by less than 2^-30 of
-// their values, far below fp32 resolution.  After hi drops, a warp still
-// scanning the slice compacts its active classes (ballot + popc) into its
-// own shared-memory segment during the next pass; if they fit, later steps
-// read only the segment (and drop classes again whenever hi drops).  The
-// full slice stays in place for the output pass, so every p_i is still
-// computed.
-
 // Every wait is bounded (cs::kWaitLimitCycles by default).  A thread whose
 // wait times out records CS_ERR_TIMEOUT and from then on neither waits,
 // pushes nor issues copies, but keeps the kernel's control flow so that all
 // threads still meet at every __syncthreads and cluster barrier.
 #include <math.h>
 
-#include "cs_device.cuh"
+#include "cs_search.cuh"
 
 namespace cs {
 namespace {
@@ -98,11 +89,11 @@ __device__ __forceinline__ int chunk_begin(const Slice& s, int nch, int c) {
 
 // Shared-memory objects of one CTA (cs::cluster_smem_layout places them).
 struct Smem {
-    float2* cslot;    // [2][n] cluster slots (double-buffered)
-    float2* wslot;    // [2][warps] per-warp slots (double-buffered)
+    float* cslot;     // [2][n][kSlotVals] cluster slots (double-buffered)
+    float* wslot;     // [2][warps][kSlotVals] per-warp slots (double-buffered)
+    float* bcast;     // [kSlotVals] broadcast of reduced sums
     uint64_t* cbar;   // [2] cluster-exchange mbarriers
     uint64_t* lbar;   // [kLoadChunks] bulk-copy mbarriers
-    float* wbuf;      // [warps][cap_w] active segments
     float4* row4;     // the slice
 };
 
@@ -117,51 +108,134 @@ struct Exch {
     bool dead;
 };
 
-__device__ __forceinline__ float2 combine2(float2 a, float2 b, bool is_max) {
-    return is_max ? make_float2(fmaxf(a.x, b.x), fmaxf(a.y, b.y))
-                  : make_float2(a.x + b.x, a.y + b.y);
+// Shuffle-tree all-reduce over the warp; every lane ends with the same
+// (bit-identical) values.
+template <int NV, bool IS_MAX>
+__device__ __forceinline__ void warp_reduce(float (&a)[NV]) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const float b = __shfl_xor_sync(0xffffffffu, a[i], o);
+            a[i] = IS_MAX ? fmaxf(a[i], b) : a[i] + b;
+        }
+    }
 }
 
-// Sum (or max) of every thread's v over the CTA and the cluster; returns
-// the same bits in every thread of the cluster.
-template <bool CLUSTER, bool IS_MAX>
-__device__ __forceinline__ float2 exchange(float2 v, const Smem& sm,
-                                           Exch& x) {
+// Cluster leg: warp 0 pushes the CTA's sums a[0..NV) into slot `rank` of
+// every CTA; the waiting threads wait for the cluster's pushes and replace
+// a with the combination over ranks, in rank order.  Every thread of the
+// CTA calls it (keeping the exchange count); only waiters wait and combine.
+template <int NV, bool IS_MAX>
+__device__ __forceinline__ void cluster_leg(float (&a)[NV], const Smem& sm,
+                                            Exch& x, bool waiter) {
+    constexpr int NE = NV + (NV & 1);   // pushed as pairs
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    v = IS_MAX ? warp_max2(v) : warp_sum2(v);
-    float2* ws = sm.wslot + (x.lk & 1u) * x.warps;
-    ++x.lk;
-    if (lane == 0) ws[warp] = v;
-    __syncthreads();
-    const float idn = IS_MAX ? -INFINITY : 0.0f;
-    v = lane < x.warps ? ws[lane] : make_float2(idn, idn);
-    v = IS_MAX ? warp_max2(v) : warp_sum2(v);
-    if (CLUSTER) {
-        const uint32_t buf = x.xk & 1u;
-        const uint32_t parity = (x.xk >> 1) & 1u;
-        ++x.xk;
-        float2* cs = sm.cslot + buf * x.n;
-        if (!x.dead) {
-            if (threadIdx.x == 0) mbar_arrive_expect_tx(&sm.cbar[buf], x.n * 8);
-            if (warp == 0 && lane < x.n) {
-                const uint32_t dst = map_to_rank(smem_addr(&cs[x.rank]), lane);
-                const uint32_t bar = map_to_rank(smem_addr(&sm.cbar[buf]), lane);
-                push_pair(dst, v.x, v.y, bar);
+    const uint32_t buf = x.xk & 1u;
+    const uint32_t parity = (x.xk >> 1) & 1u;
+    ++x.xk;
+    float* cs = sm.cslot + buf * x.n * kSlotVals;
+    if (!x.dead) {
+        if (threadIdx.x == 0) mbar_arrive_expect_tx(&sm.cbar[buf], x.n * NE * 4);
+        if (warp == 0 && lane < x.n) {
+            const uint32_t bar = map_to_rank(smem_addr(&sm.cbar[buf]), lane);
+#pragma unroll
+            for (int i = 0; i < NE; i += 2) {
+                const uint32_t dst = map_to_rank(
+                    smem_addr(&cs[x.rank * kSlotVals + i]), lane);
+                const float hi_half = (i + 1 < NV) ? a[(i + 1 < NV) ? i + 1 : 0] : 0.0f;
+                push_pair(dst, a[i], hi_half, bar);
             }
-            if (!mbar_wait<true>(&sm.cbar[buf], parity, x.limit)) x.dead = true;
         }
-        v = cs[0];
-        for (int r = 1; r < x.n; ++r) v = combine2(v, cs[r], IS_MAX);
+        if (waiter && !mbar_wait<true>(&sm.cbar[buf], parity, x.limit))
+            x.dead = true;
     }
-    return v;
+    if (waiter) {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) a[i] = cs[i];
+        for (int r = 1; r < x.n; ++r) {
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+                const float b = cs[r * kSlotVals + i];
+                a[i] = IS_MAX ? fmaxf(a[i], b) : a[i] + b;
+            }
+        }
+    }
 }
 
+// Sum (or max) over every thread of the CTA and the cluster of each thread's
+// a[0..NV); returns the same bits in every thread of the cluster.
+template <bool CLUSTER, int NV, bool IS_MAX>
+__device__ __forceinline__ void exchange(float (&a)[NV], const Smem& sm,
+                                         Exch& x) {
+    static_assert(NV <= kSlotVals, "payload");
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const float idn = IS_MAX ? -INFINITY : 0.0f;
+    warp_reduce<NV, IS_MAX>(a);
+    float* ws = sm.wslot + (x.lk & 1u) * x.warps * kSlotVals;
+    ++x.lk;
+    if (lane == 0) {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) ws[warp * kSlotVals + i] = a[i];
+    }
+    __syncthreads();
+    if (NV <= 2) {
+        // Every warp reduces the slots; the cluster leg is waited on by all.
+#pragma unroll
+        for (int i = 0; i < NV; ++i)
+            a[i] = lane < x.warps ? ws[lane * kSlotVals + i] : idn;
+        warp_reduce<NV, IS_MAX>(a);
+        if (CLUSTER) cluster_leg<NV, IS_MAX>(a, sm, x, true);
+    } else {
+        // Warp 0 reduces (and exchanges across the cluster), then
+        // broadcasts.
+        if (warp == 0) {
+#pragma unroll
+            for (int i = 0; i < NV; ++i)
+                a[i] = lane < x.warps ? ws[lane * kSlotVals + i] : idn;
+            warp_reduce<NV, IS_MAX>(a);
+        }
+        if (CLUSTER) cluster_leg<NV, IS_MAX>(a, sm, x, warp == 0);
+        if (warp == 0 && lane == 0) {
+#pragma unroll
+            for (int i = 0; i < NV; ++i) sm.bcast[i] = a[i];
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < NV; ++i) a[i] = sm.bcast[i];
+    }
+}
+
+// Accumulators of S, V and W at one inverse temperature: lanes (x, y) and
+// (z, w) of each float4 go to the two halves of a packed pair.
+struct SVW {
+    float2 s, v, w;
+    __device__ __forceinline__ void zero() {
+        s = v = w = make_float2(0.f, 0.f);
+    }
+    __device__ __forceinline__ void add(float4 y, float2 b2) {
+        const float2 y01 = make_float2(y.x, y.y);
+        const float2 y23 = make_float2(y.z, y.w);
+        const float2 x01 = mul2(y01, b2);
+        const float2 x23 = mul2(y23, b2);
+        const float2 e01 = make_float2(ex2(x01.x), ex2(x01.y));
+        const float2 e23 = make_float2(ex2(x23.x), ex2(x23.y));
+        const float2 ey01 = mul2(e01, y01);
+        const float2 ey23 = mul2(e23, y23);
+        s = add2(s, add2(e01, e23));
+        v = add2(v, add2(ey01, ey23));
+        w = fma2(ey01, y01, w);
+        w = fma2(ey23, y23, w);
+    }
+};
+
 // T = 1 pass: rewrites this thread's float4s of the slice as
-// y = max((l - m) log2 e, floor) and returns the partial (S, V) at beta = 1.
-__device__ __forceinline__ float2 transform_pass(float4* row4, int q4,
-                                                 float m) {
-    SV4 acc;
+// y = max((l - m) log2 e, floor) and returns the partial S, V, W at beta = 1.
+__device__ __forceinline__ void transform_pass(float4* row4, int q4, float m,
+                                               float (&out)[3]) {
+    SVW acc;
     acc.zero();
     const float2 one = make_float2(1.0f, 1.0f);
     for (int q = threadIdx.x; q < q4; q += blockDim.x) {
@@ -173,121 +247,65 @@ __device__ __forceinline__ float2 transform_pass(float4* row4, int q4,
         row4[q] = y;
         acc.add(y, one);
     }
-    return acc.total();
+    out[0] = acc.s.x + acc.s.y;
+    out[1] = acc.v.x + acc.v.y;
+    out[2] = acc.w.x + acc.w.y;
 }
 
-// Full pass over this thread's float4s of the slice at inverse temperature
-// beta.  Thread t owns float4s t, t + nt, ...; the loop runs a warp-uniform
-// number of times (two float4s per trip) so that GATHER can use warp votes.
-// GATHER: also appends every class with y >= thr to the warp's segment wb
-// (capacity cap); *cnt returns the warp's count, > cap on overflow.
-template <bool GATHER>
-__device__ __forceinline__ float2 slice_pass(const float4* row4, int q4,
-                                             float beta, float thr, float* wb,
-                                             int cap, int* cnt) {
-    SV4 acc;
-    acc.zero();
-    const float2 b2 = make_float2(beta, beta);
-    const int nt = blockDim.x;
-    const int lane = threadIdx.x & 31;
-    const int warp_base = threadIdx.x & ~31;
-    const unsigned lt = (1u << lane) - 1u;
-    int cw = 0;
-    for (int qb = warp_base; qb < q4; qb += 2 * nt) {
-        const int qa = qb + lane;
-        const int qc = qa + nt;
-        const float4 ya = qa < q4 ? row4[qa] : floor4();
-        const float4 yc = qc < q4 ? row4[qc] : floor4();
-        acc.add(ya, b2);
-        acc.add(yc, b2);
-        if (GATHER && cw <= cap) {
-            const float v[8] = {ya.x, ya.y, ya.z, ya.w, yc.x, yc.y, yc.z, yc.w};
+// One pass over this thread's float4s of the slice at P inverse
+// temperatures; out = {S_0, V_0, W_0, S_1, ...}.  Thread t owns float4s
+// t, t + nt, ... (two per trip).
+template <int P>
+__device__ __forceinline__ void eval_pass(const float4* row4, int q4,
+                                          const float (&beta)[kMaxPoints],
+                                          float (&out)[3 * P]) {
+    SVW acc[P];
+    float2 b2[P];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const bool a = v[k] >= thr;
-                const unsigned msk = __ballot_sync(0xffffffffu, a);
-                const int pos = cw + __popc(msk & lt);
-                if (a && pos < cap) wb[pos] = v[k];
-                cw += __popc(msk);
-            }
+    for (int p = 0; p < P; ++p) {
+        acc[p].zero();
+        b2[p] = make_float2(beta[p], beta[p]);
+    }
+    const int nt = blockDim.x;
+    for (int qa = threadIdx.x; qa < q4; qa += 2 * nt) {
+        const int qc = qa + nt;
+        const float4 ya = row4[qa];
+        const float4 yc = qc < q4 ? row4[qc] : floor4();
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+            acc[p].add(ya, b2[p]);
+            acc[p].add(yc, b2[p]);
         }
     }
-    if (GATHER) {
-        *cnt = cw;
-        __syncwarp();
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+        out[3 * p] = acc[p].s.x + acc[p].s.y;
+        out[3 * p + 1] = acc[p].v.x + acc[p].v.y;
+        out[3 * p + 2] = acc[p].w.x + acc[p].w.y;
     }
-    return acc.total();
 }
 
-// Pass over the warp's active segment.  RECOMPACT: also drops the classes
-// below thr, compacting the segment in place (entries only move to lower
-// positions, and every lane reads its entry of a round before any lane
-// writes).
-template <bool RECOMPACT>
-__device__ __forceinline__ float2 segment_pass(float* wb, int* cnt, float beta,
-                                               float thr) {
-    const int lane = threadIdx.x & 31;
-    const unsigned lt = (1u << lane) - 1u;
-    const int c = *cnt;
-    float s = 0.0f, v = 0.0f;
-    int nc = 0;
-    for (int j0 = 0; j0 < c; j0 += 32) {
-        const int j = j0 + lane;
-        const float y = j < c ? wb[j] : kYFloor;
-        const float e = ex2(y * beta);
-        s += e;
-        v = fmaf(e, y, v);
-        if (RECOMPACT) {
-            const bool a = j < c && y >= thr;
-            const unsigned msk = __ballot_sync(0xffffffffu, a);
-            __syncwarp();
-            if (a) wb[nc + __popc(msk & lt)] = y;
-            nc += __popc(msk);
-        }
+// One search round with P temperatures: pass, exchange, update.
+template <bool CLUSTER, int P>
+__device__ __forceinline__ void search_round(Search& st, const SearchCfg& cfg,
+                                             const float (&T)[kMaxPoints],
+                                             const float4* row4, int q4,
+                                             const Smem& sm, Exch& x) {
+    float beta[kMaxPoints];
+#pragma unroll
+    for (int p = 0; p < kMaxPoints; ++p) beta[p] = p < P ? rcp_approx(T[p]) : 1.0f;
+    float a[3 * P];
+    eval_pass<P>(row4, q4, beta, a);
+    exchange<CLUSTER, 3 * P, false>(a, sm, x);
+    float S[kMaxPoints], V[kMaxPoints], W[kMaxPoints];
+#pragma unroll
+    for (int p = 0; p < kMaxPoints; ++p) {
+        const int q = p < P ? p : 0;
+        S[p] = p < P ? a[3 * q] : 1.0f;
+        V[p] = p < P ? a[3 * q + 1] : 0.0f;
+        W[p] = p < P ? a[3 * q + 2] : 0.0f;
     }
-    if (RECOMPACT) {
-        *cnt = nc;
-        __syncwarp();
-    }
-    return make_float2(s, v);
-}
-
-// What the next pass of this warp reads (uniform within the warp).
-struct ActiveSet {
-    float* wb;          // this warp's segment
-    int cap;            // its capacity (0: active set off)
-    int cnt;            // classes in the segment
-    bool in_segment;    // the warp reads its segment instead of the slice
-    bool refilter;      // hi dropped: gather (slice) or recompact (segment)
-    float thr;          // y >= thr is active (thr = -K hi)
-};
-
-__device__ __forceinline__ float2 search_partial(const float4* row4, int q4,
-                                                 float beta, ActiveSet& a) {
-    if (a.in_segment) {
-        if (a.refilter) {
-            a.refilter = false;
-            return segment_pass<true>(a.wb, &a.cnt, beta, a.thr);
-        }
-        return segment_pass<false>(a.wb, &a.cnt, beta, a.thr);
-    }
-    if (a.refilter) {
-        a.refilter = false;
-        int c = 0;
-        const float2 part = slice_pass<true>(row4, q4, beta, a.thr, a.wb,
-                                             a.cap, &c);
-        if (c <= a.cap) {
-            a.in_segment = true;
-            a.cnt = c;
-        }
-        return part;
-    }
-    return slice_pass<false>(row4, q4, beta, 0.0f, nullptr, 0, nullptr);
-}
-
-// Midpoint of the search, in the fp32 arithmetic every variant uses.
-__device__ __forceinline__ float midpoint(float lo, float hi) {
-    return 0.5f * (lo + hi);
+    search_update(st, cfg, P, T, beta, S, V, W);
 }
 
 __device__ __forceinline__ void store_scalar_lanes(float* dst, int q, int pad,
@@ -327,25 +345,27 @@ __device__ __forceinline__ void write_out(const float4* row4, const Slice& s,
     }
 }
 
-template <bool CLUSTER>
-__global__ void __launch_bounds__(kClusterMaxThreads, 1)
-cluster_kernel(RowTask t, int n, int slice_len, int cap_w) {
+// MAXT: largest block the instantiation is launched with; MINB: blocks per
+// SM the register allocation must allow (256 threads x 3 blocks for the
+// throughput plans, 512 x 1 for the latency plans).
+template <bool CLUSTER, int MAXT, int MINB>
+__global__ void __launch_bounds__(MAXT, MINB)
+cluster_kernel(RowTask t, int n, int slice_len) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int nt = blockDim.x;
     const int warps = nt >> 5;
-    const int warp = threadIdx.x >> 5;
     const uint32_t rank = CLUSTER ? cluster_ctarank() : 0u;
     const int64_t cid = blockIdx.x / n;
     const int64_t ncl = gridDim.x / n;
 
     Smem sm;
     {
-        const ClusterSmemLayout L = cluster_smem_layout(warps, n, cap_w);
-        sm.cslot = reinterpret_cast<float2*>(smem + L.cslot);
-        sm.wslot = reinterpret_cast<float2*>(smem + L.wslot);
+        const ClusterSmemLayout L = cluster_smem_layout(warps, n);
+        sm.cslot = reinterpret_cast<float*>(smem + L.cslot);
+        sm.wslot = reinterpret_cast<float*>(smem + L.wslot);
+        sm.bcast = reinterpret_cast<float*>(smem + L.bcast);
         sm.cbar = reinterpret_cast<uint64_t*>(smem + L.cbar);
         sm.lbar = reinterpret_cast<uint64_t*>(smem + L.lbar);
-        sm.wbuf = reinterpret_cast<float*>(smem + L.wbuf);
         sm.row4 = reinterpret_cast<float4*>(smem + L.row);
     }
     float* row = reinterpret_cast<float*>(sm.row4);
@@ -364,8 +384,8 @@ cluster_kernel(RowTask t, int n, int slice_len, int cap_w) {
     const int64_t s0 = static_cast<int64_t>(rank) * slice_len;
     const int len = static_cast<int>(max(static_cast<int64_t>(0),
                                          min(static_cast<int64_t>(slice_len), C - s0)));
-    const float bound_bits = t.entropy_bound * kLog2e;
-    const bool prune = cap_w > 0 && t.prune_k > 0.0f;
+    const SearchCfg cfg{t.t_min, t.hi0, t.entropy_bound,
+                        t.entropy_bound * kLog2e, t.max_iter};
     Exch x{warps, n, rank, 0u, 0u, t.wait_limit_cycles, false};
     uint32_t lphase = 0;       // parity bit per load chunk
     bool reported = false;
@@ -388,7 +408,7 @@ cluster_kernel(RowTask t, int n, int slice_len, int cap_w) {
                 bulk_load(row4 + qa, src + (4 * qa - s.pad), bytes, &sm.lbar[c]);
             }
         }
-        float m_loc = -INFINITY;
+        float mc[2] = {-INFINITY, 0.0f};  // local max; NaN/Inf code
         float bad = 0.0f;  // becomes NaN if any element is NaN or +-Inf
         if (threadIdx.x < 8) {
             const int q = threadIdx.x < 4 ? s.head_q : s.tail_q;
@@ -398,7 +418,7 @@ cluster_kernel(RowTask t, int n, int slice_len, int cap_w) {
                 float v = -INFINITY;
                 if (j >= 0 && j < s.len) {
                     v = src[j];
-                    m_loc = v;
+                    mc[0] = v;
                     bad = v * 0.0f;
                 }
                 row[idx] = v;
@@ -416,7 +436,7 @@ cluster_kernel(RowTask t, int n, int slice_len, int cap_w) {
             const int qz = chunk_begin(s, nch, c + 1);
             for (int q = qa + threadIdx.x; q < qz; q += nt) {
                 const float4 v = row4[q];
-                m_loc = fmaxf(m_loc, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+                mc[0] = fmaxf(mc[0], fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
                 bad = fmaf(v.x, 0.0f, bad);
                 bad = fmaf(v.y, 0.0f, bad);
                 bad = fmaf(v.z, 0.0f, bad);
@@ -424,9 +444,8 @@ cluster_kernel(RowTask t, int n, int slice_len, int cap_w) {
             }
         }
         // Classify a non-finite row (rare): 2 = NaN seen, 1 = only Inf.
-        float code = 0.0f;
         if (bad != bad) {
-            code = 1.0f;
+            mc[1] = 1.0f;
             for (int q = threadIdx.x; q < s.q4; q += nt) {
                 const float4 v = row4[q];
                 const int j0 = 4 * q - s.pad;
@@ -434,67 +453,50 @@ cluster_kernel(RowTask t, int n, int slice_len, int cap_w) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int j = j0 + i;
-                    if (j >= 0 && j < s.len && isnan(e[i])) code = 2.0f;
+                    if (j >= 0 && j < s.len && isnan(e[i])) mc[1] = 2.0f;
                 }
             }
         }
-        const float2 mc = exchange<CLUSTER, true>(make_float2(m_loc, code), sm, x);
-        const float m = mc.x;
-        const int row_code = static_cast<int>(mc.y);
+        exchange<CLUSTER, 2, true>(mc, sm, x);
+        const float m = mc[0];
+        const int row_code = static_cast<int>(mc[1]);
 
         float* dst = t.out + r * C + s0;
         unsigned int bits = 0;
         float T_row = NAN;
         float beta_out = 0.0f, inv_s = 0.0f;
         if (row_code == 0) {
-            float2 sv = exchange<CLUSTER, false>(transform_pass(row4, s.q4, m),
-                                                 sm, x);
-            if (!entropy_above(sv, 1.0f, bound_bits)) {
+            float s1[3];
+            transform_pass(row4, s.q4, m, s1);
+            exchange<CLUSTER, 3, false>(s1, sm, x);
+            if (!entropy_above(make_float2(s1[0], s1[1]), 1.0f, cfg.bound_bits)) {
                 T_row = 1.0f;
                 beta_out = 1.0f;
-                inv_s = 1.0f / sv.x;
+                inv_s = 1.0f / s1[0];
             } else {
-                ActiveSet a{sm.wbuf + warp * cap_w, prune ? cap_w : 0, 0,
-                            false, false, 0.0f};
-                float lo = t.t_min, hi = t.hi0;
-                bool lo_eval = false;
-                bool hi_eval = hi == 1.0f;   // H(1) > bound is known
-                float s_lo = 0.0f;
-                if (lo < hi) {
-                    for (int k = 0; k < t.max_iter; ++k) {
-                        const float mid = midpoint(lo, hi);
-                        // Exact early exit: the fp32 midpoint has reached an
-                        // end whose side is already known, so every further
-                        // step repeats the same evaluation.
-                        if ((mid == lo && lo_eval) || (mid == hi && hi_eval)) break;
-                        const float b = rcp_approx(mid);
-                        sv = exchange<CLUSTER, false>(
-                            search_partial(row4, s.q4, b, a), sm, x);
-                        if (entropy_above(sv, b, bound_bits)) {
-                            hi = mid;
-                            hi_eval = true;
-                            if (a.cap > 0) {
-                                a.thr = -t.prune_k * hi;
-                                a.refilter = true;
-                            }
-                        } else {
-                            lo = mid;
-                            lo_eval = true;
-                            s_lo = sv.x;
-                        }
-                    }
+                Search st = search_begin(s1[0], s1[1], s1[2], t.strict != 0);
+                if (!(cfg.t_min < cfg.hi0)) {
+                    // No interval to halve: T = t_min (section 5.4 check).
+                    st.final_round = true;
+                    st.final_check = true;
+                    st.T_out = cfg.t_min;
+                    float T1[kMaxPoints] = {cfg.t_min, 0.f, 0.f};
+                    search_round<CLUSTER, 1>(st, cfg, T1, row4, s.q4, sm, x);
                 }
-                const float b_lo = rcp_approx(lo);
-                if (!lo_eval) {
-                    // lo is still t_min: evaluate it (section 5.4 check).
-                    sv = exchange<CLUSTER, false>(
-                        search_partial(row4, s.q4, b_lo, a), sm, x);
-                    s_lo = sv.x;
-                    if (entropy_above(sv, b_lo, bound_bits)) bits |= kBitOverflow;
+                while (!st.done) {
+                    float T[kMaxPoints];
+                    const int np = search_plan(st, cfg, T);
+                    if (np == 1)
+                        search_round<CLUSTER, 1>(st, cfg, T, row4, s.q4, sm, x);
+                    else if (np == 2)
+                        search_round<CLUSTER, 2>(st, cfg, T, row4, s.q4, sm, x);
+                    else if (np == 3)
+                        search_round<CLUSTER, 3>(st, cfg, T, row4, s.q4, sm, x);
                 }
-                T_row = lo;
-                beta_out = b_lo;
-                inv_s = 1.0f / s_lo;
+                if (st.overflow) bits |= kBitOverflow;
+                T_row = st.T_out;
+                beta_out = rcp_approx(st.T_out);
+                inv_s = 1.0f / st.S_out;
             }
         } else {
             bits = row_code == 2 ? kBitNan : kBitInf;
@@ -520,39 +522,51 @@ cluster_kernel(RowTask t, int n, int slice_len, int cap_w) {
     if (CLUSTER) cluster_sync();
 }
 
-}  // namespace
-
-cudaError_t launch_cluster(const RowTask& task, int cluster_size,
-                           int slice_len, int threads, int cap_w,
-                           int smem_bytes, int64_t grid_ctas,
-                           cudaStream_t stream) {
+template <bool CLUSTER, int MAXT, int MINB>
+cudaError_t launch_one(const RowTask& task, int cluster_size, int slice_len,
+                       int threads, int smem_bytes, int64_t grid_ctas,
+                       cudaStream_t stream, int attr_slot) {
+    auto kern = cluster_kernel<CLUSTER, MAXT, MINB>;
+    cudaError_t e = ensure_smem_attribute(reinterpret_cast<const void*>(kern),
+                                          attr_slot, smem_bytes);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid_ctas), 1, 1);
     cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
-    if (cluster_size > 1) {
-        auto kern = cluster_kernel<true>;
-        cudaError_t e = ensure_smem_attribute(
-            reinterpret_cast<const void*>(kern), 1, smem_bytes);
-        if (e != cudaSuccess) return e;
+    if (CLUSTER) {
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = static_cast<unsigned>(cluster_size);
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, kern, task, cluster_size, slice_len,
-                                  cap_w);
+    } else {
+        cfg.attrs = nullptr;
+        cfg.numAttrs = 0;
     }
-    auto kern = cluster_kernel<false>;
-    cudaError_t e = ensure_smem_attribute(reinterpret_cast<const void*>(kern),
-                                          0, smem_bytes);
-    if (e != cudaSuccess) return e;
-    cfg.attrs = nullptr;
-    cfg.numAttrs = 0;
-    return cudaLaunchKernelEx(&cfg, kern, task, 1, slice_len, cap_w);
+    return cudaLaunchKernelEx(&cfg, kern, task, cluster_size, slice_len);
+}
+
+}  // namespace
+
+cudaError_t launch_cluster(const RowTask& task, int cluster_size,
+                           int slice_len, int threads, int smem_bytes,
+                           int64_t grid_ctas, cudaStream_t stream) {
+    const bool narrow = threads <= 256;
+    if (cluster_size > 1)
+        return narrow ? launch_one<true, 256, 3>(task, cluster_size, slice_len,
+                                                 threads, smem_bytes, grid_ctas,
+                                                 stream, 1)
+                      : launch_one<true, 512, 1>(task, cluster_size, slice_len,
+                                                 threads, smem_bytes, grid_ctas,
+                                                 stream, 3);
+    return narrow ? launch_one<false, 256, 3>(task, 1, slice_len, threads,
+                                              smem_bytes, grid_ctas, stream, 0)
+                  : launch_one<false, 512, 1>(task, 1, slice_len, threads,
+                                              smem_bytes, grid_ctas, stream, 2);
 }
 
 }  // namespace cs

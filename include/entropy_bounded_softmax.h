@@ -13,7 +13,12 @@
  *   3. otherwise bisect T on [t_min, min(1, t_max)] for exactly max_iter
  *      steps: mid = (lo + hi) / 2; H(mid) > entropy_bound moves hi to mid,
  *      otherwise lo moves to mid.  Temperatures above 1 are never searched
- *      because H is nondecreasing in T (section 2.1 step 4);
+ *      because H is nondecreasing in T (section 2.1 step 4).  By default
+ *      the kernels evaluate H only where needed: a midpoint at or below an
+ *      evaluated feasible temperature is feasible, and one at or above an
+ *      evaluated infeasible temperature is infeasible, so once safeguarded
+ *      Newton steps have bracketed the crossing tightly every decision of
+ *      the bisection is known (cs_options.strict evaluates each midpoint);
  *   4. write softmax(l / lo) and report T = lo.  If even lo = t_min violates
  *      the bound, the row still gets softmax(l / t_min), the lowest entropy
  *      reachable (section 5.4), and ENTROPY_OVERFLOW is raised.
@@ -64,9 +69,11 @@ typedef struct cs_options {
     int32_t param;     /* rowgroup: lanes per row (1, 2, 4, 8, 16, 32);
                           cluster: CTAs per row (1..16); 0 = automatic      */
     int32_t threads;   /* cluster: threads per CTA (multiple of 32,
-                          64..1024); 0 = automatic                          */
-    int32_t full_scan; /* cluster: 1 = evaluate every class at every
-                          bisection step (no active set); 0 = active set   */
+                          64..512); 0 = automatic                           */
+    int32_t strict;    /* 1 = evaluate H at every bisection midpoint, one
+                          pass per step; 0 = settle the midpoints outside
+                          an evaluated bracket by monotonicity (same result,
+                          fewer passes)                                     */
 } cs_options;
 
 /* What a launch of the given shape uses.  Filled by cs_plan_launch /
@@ -80,8 +87,6 @@ typedef struct cs_plan {
     int32_t threads_per_cta;
     int32_t smem_bytes;      /* dynamic shared memory per CTA               */
     int32_t ctas_per_sm;     /* CTAs resident per SM by the plan's limits   */
-    int32_t warp_buffer;     /* cluster: active-set floats per warp (0: off) */
-    float prune_k;           /* cluster: active-set threshold K (0: off)    */
     int64_t grid_ctas;       /* CTAs in the launch                          */
 } cs_plan;
 

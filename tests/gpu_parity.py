@@ -36,7 +36,7 @@ TIMEOUT_BIT = 1 << 10
 
 def run_gpu(x: np.ndarray, entropy_bound=0.2, t_min=0.01, t_max=10.0,
             max_iter=20, variant="auto", param=0, in_offset=0, out_offset=0,
-            threads=0, full_scan=False):
+            threads=0, strict=False):
     """Runs the CUDA path through the C ABI; returns (p, T, error_mask).
     in_offset/out_offset shift the tensors by that many floats inside their
     allocations (to exercise unaligned rows)."""
@@ -55,7 +55,7 @@ def run_gpu(x: np.ndarray, entropy_bound=0.2, t_min=0.01, t_max=10.0,
     cs.get_error()  # clear
     cs.constrained_softmax(xin, entropy_bound, t_min, t_max, max_iter,
                            out=out, t_out=t_out, variant=variant,
-                           param=param, threads=threads, full_scan=full_scan)
+                           param=param, threads=threads, strict=strict)
     bits = cs.get_error()
     mask = 0
     for name, bit in cs.ERROR_BITS.items():

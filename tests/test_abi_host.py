@@ -89,10 +89,10 @@ def test_check_args(args, status):
     assert cs.cs_check_args(*args) == status
 
 
-def plan(batch, classes, variant=0, param=0, threads=0, full_scan=0, **dev):
+def plan(batch, classes, variant=0, param=0, threads=0, strict=0, **dev):
     d = dict(GB300, **dev)
     st, p = cs.cs_plan_host(batch, classes,
-                            cs.options(variant, param, threads, full_scan),
+                            cs.options(variant, param, threads, strict),
                             d["sm_count"], d["smem_per_block_optin"],
                             d["smem_per_sm"], d["max_cluster"])
     return st, p.as_dict()
@@ -156,8 +156,8 @@ def test_forced_variants_and_limits():
     assert st == C["CS_ERR_INVALID_ARG"]
     st, _ = plan(8, 850000, C["CS_VARIANT_CLUSTER"], 0, max_cluster=8)
     assert st == C["CS_ERR_OOM"]
-    for bad in (dict(threads=48), dict(threads=1056), dict(threads=100),
-                dict(full_scan=2)):
+    for bad in (dict(threads=48), dict(threads=544), dict(threads=100),
+                dict(strict=2)):
         st, _ = plan(8, 50000, C["CS_VARIANT_CLUSTER"], 0, **bad)
         assert st == C["CS_ERR_INVALID_ARG"], bad
     st, _ = plan(8, 64, C["CS_VARIANT_ROWGROUP"], 0, threads=256)
@@ -170,24 +170,12 @@ def test_null_options_mean_automatic():
     assert st1 == st2 == 0 and p1.as_dict() == p2
 
 
-def test_active_set_plan():
-    st, p = plan(32, 50000)
-    assert st == 0 and p["warp_buffer"] >= 64 and p["warp_buffer"] % 32 == 0
-    assert p["prune_k"] == 36 + 16              # ceil(log2 50000) = 16
-    assert p["smem_bytes"] <= GB300["smem_per_block_optin"]
-    st, q = plan(32, 50000, full_scan=1)
-    assert st == 0 and q["warp_buffer"] == 0 and q["prune_k"] == 0.0
-    assert q["smem_bytes"] < p["smem_bytes"]
+def test_strict_option_is_checked():
+    st, _ = plan(32, 50000, strict=1)
+    assert st == 0
+    st, _ = plan(32, 50000, strict=2)
+    assert st == C["CS_ERR_INVALID_ARG"]
     st, p = plan(8, 4096, C["CS_VARIANT_CLUSTER"], 2, threads=512)
     assert st == 0 and p["threads_per_cta"] == 512 and p["cluster_size"] == 2
-
-
-def test_constrained_softmax_rejects_cpu_tensors():
-    import torch
-    with pytest.raises(ValueError):
-        cs.constrained_softmax(torch.zeros(2, 3))
-
-
-def test_missing_library_fails_loudly(tmp_path):
-    with pytest.raises(RuntimeError, match="no fallback"):
-        _lib.load(str(tmp_path / "libcsoftmax.so"))
+    st, _ = plan(8, 4096, C["CS_VARIANT_CLUSTER"], 2, threads=1024)
+    assert st == C["CS_ERR_INVALID_ARG"]
