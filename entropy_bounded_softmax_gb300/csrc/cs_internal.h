@@ -83,18 +83,17 @@ inline int64_t cluster_smem_bytes(int64_t slice_len, int threads, int n) {
 // three CTAs share an SM and one's exchange overlaps the others' passes.
 constexpr int64_t kTargetSlice = 16384;
 
-// Automatic threads per CTA.  A launch with no more CTAs than SMs runs one
-// CTA per SM and wants many warps (about 24 classes per thread, 128-512);
-// a larger launch wants several small CTAs per SM (about 64 classes per
-// thread, 128-256).
+// Automatic threads per CTA: about 48 classes per thread for a launch with
+// no more CTAs than SMs (one CTA per SM, all of its time on one row),
+// about 64 for larger launches (several CTAs share an SM); 128-256 threads
+// either way, where the per-round reductions stay short.
 inline int cluster_threads_for(int64_t slice_len, int64_t ctas,
                                int64_t sm_count) {
-    const bool latency = ctas <= sm_count;
-    int64_t t = (slice_len + (latency ? 23 : 63)) / (latency ? 24 : 64);
+    const int64_t per = ctas <= sm_count ? 48 : 64;
+    int64_t t = (slice_len + per - 1) / per;
     t = ((t + 31) / 32) * 32;
     if (t < 128) t = 128;
-    const int64_t cap = latency ? 512 : 256;
-    if (t > cap) t = cap;
+    if (t > 256) t = 256;
     return static_cast<int>(t);
 }
 

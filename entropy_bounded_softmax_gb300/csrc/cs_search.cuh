@@ -12,7 +12,11 @@
 // safeguarded Newton points for log H(beta) = log bound (beta = 1/T), the
 // bracket's geometric midpoint when Newton leaves it, t_min when the root
 // approaches it, and, once Newton has converged, the two ends of the
-// bisection path predicted from the Newton point.  When every midpoint is
+// bisection path predicted from the Newton point.  Midpoints that remain
+// unsettled after that (they lie where fp32 evaluations of H are within
+// rounding of the bound) are evaluated directly, each together with both
+// of its possible successors, two bisection levels per round.  The replay
+// keeps a cursor, so every decision is taken once.  When every midpoint is
 // settled, the bisection's final lo is known; its S (for the output) comes
 // from the evaluation at lo, made in one last round if lo was not evaluated
 // already.  The result is the bisection's: each of its decisions is either
@@ -47,23 +51,33 @@ __device__ __forceinline__ float midpoint(float lo, float hi) {
     return 0.5f * (lo + hi);
 }
 
-struct BisectPath {
+// Position of the replayed bisection: its lo and hi, whether each has been
+// decided (for the fp32 early stop) and the steps taken.
+struct Cursor {
     float lo, hi;
-    bool lo_eval;      // lo was set by a (settled) feasible decision
-    bool settled;      // every decision was settled
-    float unsettled;   // first unsettled midpoint (when !settled)
+    bool lo_eval, hi_eval;
+    int k;
 };
 
-// Replays the bisection.  Decisions: m >= B infeasible, m <= A feasible
-// (A = 0: none known); otherwise [m > Tp] when use_pred, else stop.
-__device__ __forceinline__ BisectPath replay(const SearchCfg& c, float A,
-                                             float B, bool use_pred,
-                                             float Tp) {
-    BisectPath p{c.t_min, c.hi0, false, true, 0.0f};
-    bool hi_eval = c.hi0 == 1.0f;
-    for (int k = 0; k < c.max_iter; ++k) {
-        const float m = midpoint(p.lo, p.hi);
-        if ((m == p.lo && p.lo_eval) || (m == p.hi && hi_eval)) break;
+__device__ __forceinline__ Cursor cursor_begin(const SearchCfg& c) {
+    return Cursor{c.t_min, c.hi0, false, c.hi0 == 1.0f, 0};
+}
+
+// Advances the replay while its decisions are settled: m >= B infeasible,
+// m <= A feasible (A = 0: none known); with use_pred, the rest by
+// [m > Tp].  Returns true and the midpoint in *um if it stopped at an
+// unsettled midpoint, false when the bisection is complete.
+__device__ __forceinline__ bool advance(Cursor& cu, const SearchCfg& c,
+                                        float A, float B, bool use_pred,
+                                        float Tp, float* um) {
+    while (cu.k < c.max_iter) {
+        const float m = midpoint(cu.lo, cu.hi);
+        if ((m == cu.lo && cu.lo_eval) || (m == cu.hi && cu.hi_eval)) {
+            // The fp32 midpoint repeats a decided end: every further step
+            // would repeat that decision.
+            cu.k = c.max_iter;
+            break;
+        }
         bool inf;
         if (m >= B) {
             inf = true;
@@ -72,23 +86,24 @@ __device__ __forceinline__ BisectPath replay(const SearchCfg& c, float A,
         } else if (use_pred) {
             inf = m > Tp;
         } else {
-            p.settled = false;
-            p.unsettled = m;
-            return p;
+            *um = m;
+            return true;
         }
         if (inf) {
-            p.hi = m;
-            hi_eval = true;
+            cu.hi = m;
+            cu.hi_eval = true;
         } else {
-            p.lo = m;
-            p.lo_eval = true;
+            cu.lo = m;
+            cu.lo_eval = true;
         }
+        ++cu.k;
     }
-    return p;
+    return false;
 }
 
 // Per-row search state; identical in every thread working on the row.
 struct Search {
+    Cursor cur;         // the replayed bisection
     float A, SA;        // largest feasible T evaluated, its S (A = 0: none)
     float B;            // smallest infeasible T evaluated
     float bc, Hc, dHc;  // Newton anchor: beta, H (nats), dH/dbeta
@@ -98,6 +113,7 @@ struct Search {
     bool final_check;   // ... which is t_min, never moved: flag if infeasible
     bool done;
     bool strict;        // evaluate unsettled midpoints one by one
+    bool endgame;       // Newton has converged: bisect the unsettled rest
     int rounds;
     float T_out, S_out;
     bool overflow;      // section 5.4: even t_min violates the bound
@@ -116,9 +132,11 @@ __device__ __forceinline__ float entropy_slope(float S, float V, float W,
 
 // Starts the search after the T = 1 evaluation (S1, V1, W1), which found
 // H(1) > bound.
-__device__ __forceinline__ Search search_begin(float S1, float V1, float W1,
+__device__ __forceinline__ Search search_begin(const SearchCfg& c, float S1,
+                                               float V1, float W1,
                                                bool strict) {
     Search s;
+    s.cur = cursor_begin(c);
     s.A = 0.0f;
     s.SA = 0.0f;
     s.B = 1.0f;
@@ -132,6 +150,7 @@ __device__ __forceinline__ Search search_begin(float S1, float V1, float W1,
     s.final_check = false;
     s.done = false;
     s.strict = strict;
+    s.endgame = false;
     s.rounds = 0;
     s.T_out = 0.0f;
     s.S_out = 0.0f;
@@ -143,11 +162,11 @@ __device__ __forceinline__ Search search_begin(float S1, float V1, float W1,
 // with T_out, S_out and overflow set).
 __device__ __forceinline__ int search_plan(Search& s, const SearchCfg& c,
                                            float (&T)[kMaxPoints]) {
-    const BisectPath path = replay(c, s.A, s.B, false, 0.0f);
-    if (path.settled) {
-        const float lo = path.lo;
+    float um = 0.0f;
+    if (!advance(s.cur, c, s.A, s.B, false, 0.0f, &um)) {
+        const float lo = s.cur.lo;
         s.T_out = lo;
-        if (!path.lo_eval) {
+        if (!s.cur.lo_eval) {
             // lo never moved: it is t_min, whose own evaluation decides the
             // degradation flag (section 5.4).
             if (s.tmin_done) {
@@ -166,13 +185,24 @@ __device__ __forceinline__ int search_plan(Search& s, const SearchCfg& c,
             return 0;
         }
         s.final_round = true;
-        s.final_check = !path.lo_eval;
+        s.final_check = !s.cur.lo_eval;
         T[0] = lo;
         return 1;
     }
     if (s.strict || s.rounds >= kMaxNewtonRounds) {
-        T[0] = path.unsettled;
+        T[0] = um;
         return 1;
+    }
+    if (s.endgame) {
+        // The unsettled midpoint and both midpoints that can follow it.
+        int np = 0;
+        T[np++] = um;
+        const float m_inf = midpoint(s.cur.lo, um);   // if um is infeasible
+        const float m_feas = midpoint(um, s.cur.hi);  // if um is feasible
+        const float Tlo = s.A > 0.0f ? s.A : 0.0f;
+        if (m_inf > Tlo && m_inf < s.B && m_inf != um) T[np++] = m_inf;
+        if (m_feas > Tlo && m_feas < s.B && m_feas != um) T[np++] = m_feas;
+        return np;
     }
     // Safeguarded Newton for log H = log bound in beta (plain Newton on H
     // when the bound is not positive), kept inside the bracket in beta,
@@ -193,7 +223,7 @@ __device__ __forceinline__ int search_plan(Search& s, const SearchCfg& c,
     if (!(Tn > Tlo && Tn < s.B)) {
         // Rounding put the point on an end: take the bracket's midpoint.
         Tn = midpoint(Tlo, s.B);
-        if (!(Tn > Tlo && Tn < s.B)) Tn = path.unsettled;
+        if (!(Tn > Tlo && Tn < s.B)) Tn = um;
     }
     int np = 0;
     T[np++] = Tn;
@@ -203,12 +233,15 @@ __device__ __forceinline__ int search_plan(Search& s, const SearchCfg& c,
     if (np == 1 && fabsf(bn - s.bc) <= 1e-3f * s.bc) {
         // Newton has converged: also evaluate the ends of the bisection path
         // it predicts, so the next replay can settle every decision.
-        const BisectPath pred = replay(c, s.A, s.B, true, Tn);
+        Cursor pred = s.cur;
+        float dummy;
+        advance(pred, c, s.A, s.B, true, Tn, &dummy);
         if (pred.lo > s.A && pred.lo < s.B && pred.lo != Tn &&
             pred.lo >= c.t_min)
             T[np++] = pred.lo;
         if (pred.hi > s.A && pred.hi < s.B && pred.hi != Tn && np < kMaxPoints)
             T[np++] = pred.hi;
+        s.endgame = true;
     }
     return np;
 }

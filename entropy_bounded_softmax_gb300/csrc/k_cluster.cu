@@ -474,7 +474,7 @@ cluster_kernel(RowTask t, int n, int slice_len) {
                 beta_out = 1.0f;
                 inv_s = 1.0f / s1[0];
             } else {
-                Search st = search_begin(s1[0], s1[1], s1[2], t.strict != 0);
+                Search st = search_begin(cfg, s1[0], s1[1], s1[2], t.strict != 0);
                 if (!(cfg.t_min < cfg.hi0)) {
                     // No interval to halve: T = t_min (section 5.4 check).
                     st.final_round = true;
