@@ -213,9 +213,9 @@ __device__ __forceinline__ int search_plan(Search& s, const SearchCfg& c,
     if (c.bound > 0.0f && s.Hc > 0.0f) {
         const float g = lg2_approx(s.Hc) - lg2_approx(c.bound);   // log2 units
         const float gp = s.dHc * rcp_approx(s.Hc) * kLog2e;
-        bn = gp < 0.0f ? s.bc - g / gp : NAN;
+        bn = gp < 0.0f ? s.bc - g * rcp_approx(gp) : NAN;
     } else {
-        bn = s.dHc < 0.0f ? s.bc - (s.Hc - c.bound) / s.dHc : NAN;
+        bn = s.dHc < 0.0f ? s.bc - (s.Hc - c.bound) * rcp_approx(s.dHc) : NAN;
     }
     if (!(bn > b_inf && bn < b_feas)) bn = sqrtf(b_inf * b_feas);
     float Tn = rcp_approx(bn);

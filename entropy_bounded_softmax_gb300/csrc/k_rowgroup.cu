@@ -75,7 +75,7 @@ template <int G, int E4, int P>
 __device__ __forceinline__ void group_round(Search& st, const SearchCfg& cfg,
                                             const float (&T)[kMaxPoints],
                                             const float4 (&y)[E4],
-                                            unsigned gmask) {
+                                            unsigned gmask, int np) {
     float beta[kMaxPoints];
 #pragma unroll
     for (int p = 0; p < kMaxPoints; ++p) beta[p] = p < P ? rcp_approx(T[p]) : 1.0f;
@@ -90,11 +90,11 @@ __device__ __forceinline__ void group_round(Search& st, const SearchCfg& cfg,
         V[p] = p < P ? a[3 * q + 1] : 0.0f;
         W[p] = p < P ? a[3 * q + 2] : 0.0f;
     }
-    search_update(st, cfg, P, T, beta, S, V, W);
+    search_update(st, cfg, np, T, beta, S, V, W);
 }
 
 template <int G, int E4>
-__global__ void __launch_bounds__(256, E4 <= 4 ? 4 : 2)
+__global__ void __launch_bounds__(256, E4 <= 2 ? 4 : (E4 <= 4 ? 3 : 2))
 rowgroup_kernel(RowTask t, int vec) {
     const int lane = threadIdx.x & 31;
     const int sub = lane & (G - 1);
@@ -195,17 +195,33 @@ rowgroup_kernel(RowTask t, int vec) {
                     st.final_check = true;
                     st.T_out = cfg.t_min;
                     const float T1[kMaxPoints] = {cfg.t_min, 0.f, 0.f};
-                    group_round<G, E4, 1>(st, cfg, T1, y, gmask);
+                    group_round<G, E4, 1>(st, cfg, T1, y, gmask, 1);
                 }
-                while (!st.done) {
+                // The rows of a warp run their rounds together with the
+                // warp's largest point count (padding repeats a point), so
+                // the warp never executes several round shapes one after
+                // the other.
+                const unsigned active = __activemask();
+                bool running = true;
+                while (__any_sync(active, running)) {
                     float T[kMaxPoints];
-                    const int np = search_plan(st, cfg, T);
-                    if (np == 1)
-                        group_round<G, E4, 1>(st, cfg, T, y, gmask);
-                    else if (np == 2)
-                        group_round<G, E4, 2>(st, cfg, T, y, gmask);
-                    else if (np == 3)
-                        group_round<G, E4, 3>(st, cfg, T, y, gmask);
+                    int np = 0;
+                    if (running) {
+                        np = search_plan(st, cfg, T);
+                        if (np == 0) running = false;
+                    }
+                    const int npw = __reduce_max_sync(active, np);
+                    if (npw == 0) break;
+                    if (running) {
+                        for (int i = np; i < kMaxPoints; ++i) T[i] = T[0];
+                        if (npw == 1)
+                            group_round<G, E4, 1>(st, cfg, T, y, gmask, np);
+                        else if (npw == 2)
+                            group_round<G, E4, 2>(st, cfg, T, y, gmask, np);
+                        else
+                            group_round<G, E4, 3>(st, cfg, T, y, gmask, np);
+                        if (st.done) running = false;
+                    }
                 }
                 if (st.overflow) bits |= kBitOverflow;
                 T_row = st.T_out;
