@@ -5,15 +5,15 @@
 //
 // Method: "BURT-IMMA CUDA Kernel API Reference", section 2.1
 // `constrained_softmax`, Description steps 1-4, with sections 5.3 and 5.4;
-// the steps are the same as in the cluster kernel: max once, y = (l - m)
-// log2 e, then the temperature search of cs_search.cuh, whose rounds are
-// register passes giving S = sum 2^(beta y), V = sum y 2^(beta y) and
-// W = sum y^2 2^(beta y) at 1-3 temperatures.  The per-round reduction is a
-// butterfly over the G lanes (all lanes end with bit-identical sums, so
-// they take the same decisions).
+// max once, y = (l - m) log2 e, then the bisection itself, one register
+// pass per midpoint giving S = sum 2^(beta y) and V = sum y 2^(beta y),
+// H = ln 2 (log2 S - beta V/S).  The per-step reduction is a butterfly over
+// the G lanes (all lanes end with bit-identical sums, so they take the same
+// decision); H > bound is decided without a division as
+// S (log2 S - bound log2 e) - beta V > 0, with log2 on the MUFU lg2 unit.
 #include <math.h>
 
-#include "cs_search.cuh"
+#include "cs_device.cuh"
 
 namespace cs {
 namespace {
@@ -30,71 +30,29 @@ __device__ __forceinline__ float2 group_max2(float2 v, unsigned mask) {
     return v;
 }
 
-// (S, V, W) of this lane's classes at P inverse temperatures, into
-// out = {S_0, V_0, W_0, S_1, ...}.
-template <int E4, int P>
-__device__ __forceinline__ void reg_eval(const float4 (&y)[E4],
-                                         const float (&beta)[kMaxPoints],
-                                         float (&out)[3 * P]) {
-#pragma unroll
-    for (int p = 0; p < P; ++p) {
-        const float2 b2 = make_float2(beta[p], beta[p]);
-        float2 s = make_float2(0.f, 0.f), v = s, w = s;
-#pragma unroll
-        for (int i = 0; i < E4; ++i) {
-            const float2 y01 = make_float2(y[i].x, y[i].y);
-            const float2 y23 = make_float2(y[i].z, y[i].w);
-            const float2 x01 = mul2(y01, b2);
-            const float2 x23 = mul2(y23, b2);
-            const float2 e01 = make_float2(ex2(x01.x), ex2(x01.y));
-            const float2 e23 = make_float2(ex2(x23.x), ex2(x23.y));
-            const float2 ey01 = mul2(e01, y01);
-            const float2 ey23 = mul2(e23, y23);
-            s = add2(s, add2(e01, e23));
-            v = add2(v, add2(ey01, ey23));
-            w = fma2(ey01, y01, w);
-            w = fma2(ey23, y23, w);
-        }
-        out[3 * p] = s.x + s.y;
-        out[3 * p + 1] = v.x + v.y;
-        out[3 * p + 2] = w.x + w.y;
-    }
-}
-
-template <int G, int NV>
-__device__ __forceinline__ void group_sum(float (&a)[NV], unsigned mask) {
+template <int G>
+__device__ __forceinline__ float2 group_sum2(float2 v, unsigned mask) {
 #pragma unroll
     for (int o = G / 2; o > 0; o >>= 1) {
-#pragma unroll
-        for (int i = 0; i < NV; ++i) a[i] += __shfl_xor_sync(mask, a[i], o);
+        v.x += __shfl_xor_sync(mask, v.x, o);
+        v.y += __shfl_xor_sync(mask, v.y, o);
     }
+    return v;
 }
 
-// One search round of the row with P temperatures (all lanes of the group).
-template <int G, int E4, int P>
-__device__ __forceinline__ void group_round(Search& st, const SearchCfg& cfg,
-                                            const float (&T)[kMaxPoints],
-                                            const float4 (&y)[E4],
-                                            unsigned gmask, int np) {
-    float beta[kMaxPoints];
+// (S, V) of this lane's classes at inverse temperature beta.
+template <int E4>
+__device__ __forceinline__ float2 reg_pass(const float4 (&y)[E4], float beta) {
+    SV4 acc;
+    acc.zero();
+    const float2 b2 = make_float2(beta, beta);
 #pragma unroll
-    for (int p = 0; p < kMaxPoints; ++p) beta[p] = p < P ? rcp_approx(T[p]) : 1.0f;
-    float a[3 * P];
-    reg_eval<E4, P>(y, beta, a);
-    group_sum<G, 3 * P>(a, gmask);
-    float S[kMaxPoints], V[kMaxPoints], W[kMaxPoints];
-#pragma unroll
-    for (int p = 0; p < kMaxPoints; ++p) {
-        const int q = p < P ? p : 0;
-        S[p] = p < P ? a[3 * q] : 1.0f;
-        V[p] = p < P ? a[3 * q + 1] : 0.0f;
-        W[p] = p < P ? a[3 * q + 2] : 0.0f;
-    }
-    search_update(st, cfg, np, T, beta, S, V, W);
+    for (int i = 0; i < E4; ++i) acc.add(y[i], b2);
+    return acc.total();
 }
 
 template <int G, int E4>
-__global__ void __launch_bounds__(256, E4 <= 2 ? 4 : (E4 <= 4 ? 3 : 2))
+__global__ void __launch_bounds__(256)
 rowgroup_kernel(RowTask t, int vec) {
     const int lane = threadIdx.x & 31;
     const int sub = lane & (G - 1);
@@ -102,8 +60,7 @@ rowgroup_kernel(RowTask t, int vec) {
         G == 32 ? 0xffffffffu : (((1u << G) - 1u) << (lane & ~(G - 1)));
     const int C = t.num_classes;
     const int Q = (C + 3) >> 2;  // float4 slots per row
-    const SearchCfg cfg{t.t_min, t.hi0, t.entropy_bound,
-                        t.entropy_bound * kLog2e, t.max_iter};
+    const float bound_bits = t.entropy_bound * kLog2e;
     const int64_t groups_per_grid =
         (static_cast<int64_t>(gridDim.x) * blockDim.x) / G;
 
@@ -177,56 +134,47 @@ rowgroup_kernel(RowTask t, int vec) {
                 y[i].z = fmaxf((y[i].z - m) * kLog2e, kYFloor);
                 y[i].w = fmaxf((y[i].w - m) * kLog2e, kYFloor);
             }
-            float s1[3];
-            {
-                const float one[kMaxPoints] = {1.0f, 1.0f, 1.0f};
-                reg_eval<E4, 1>(y, one, s1);
-            }
-            group_sum<G, 3>(s1, gmask);
-            if (!entropy_above(make_float2(s1[0], s1[1]), 1.0f, cfg.bound_bits)) {
+            float2 sv = group_sum2<G>(reg_pass<E4>(y, 1.0f), gmask);
+            if (!entropy_above(sv, 1.0f, bound_bits)) {
                 T_row = 1.0f;
                 beta_out = 1.0f;
-                inv_s = 1.0f / s1[0];
+                inv_s = 1.0f / sv.x;
             } else {
-                Search st = search_begin(cfg, s1[0], s1[1], s1[2], t.strict != 0);
-                if (!(cfg.t_min < cfg.hi0)) {
-                    // No interval to halve: T = t_min (section 5.4 check).
-                    st.final_round = true;
-                    st.final_check = true;
-                    st.T_out = cfg.t_min;
-                    const float T1[kMaxPoints] = {cfg.t_min, 0.f, 0.f};
-                    group_round<G, E4, 1>(st, cfg, T1, y, gmask, 1);
-                }
-                // The rows of a warp run their rounds together with the
-                // warp's largest point count (padding repeats a point), so
-                // the warp never executes several round shapes one after
-                // the other.
-                const unsigned active = __activemask();
-                bool running = true;
-                while (__any_sync(active, running)) {
-                    float T[kMaxPoints];
-                    int np = 0;
-                    if (running) {
-                        np = search_plan(st, cfg, T);
-                        if (np == 0) running = false;
-                    }
-                    const int npw = __reduce_max_sync(active, np);
-                    if (npw == 0) break;
-                    if (running) {
-                        for (int i = np; i < kMaxPoints; ++i) T[i] = T[0];
-                        if (npw == 1)
-                            group_round<G, E4, 1>(st, cfg, T, y, gmask, np);
-                        else if (npw == 2)
-                            group_round<G, E4, 2>(st, cfg, T, y, gmask, np);
-                        else
-                            group_round<G, E4, 3>(st, cfg, T, y, gmask, np);
-                        if (st.done) running = false;
+                // One evaluation per midpoint: for rows this narrow a pass
+                // costs less than the bookkeeping that settling midpoints
+                // without evaluation would need.
+                float lo = t.t_min, hi = t.hi0;
+                bool lo_eval = false;
+                bool hi_eval = hi == 1.0f;   // H(1) > bound is known
+                float s_lo = 0.0f;
+                if (lo < hi) {
+                    for (int k = 0; k < t.max_iter; ++k) {
+                        const float mid = 0.5f * (lo + hi);
+                        // Exact early exit: the fp32 midpoint repeats an
+                        // end already decided, and so would every later one.
+                        if ((mid == lo && lo_eval) || (mid == hi && hi_eval)) break;
+                        const float b = rcp_approx(mid);
+                        sv = group_sum2<G>(reg_pass<E4>(y, b), gmask);
+                        if (entropy_above(sv, b, bound_bits)) {
+                            hi = mid;
+                            hi_eval = true;
+                        } else {
+                            lo = mid;
+                            lo_eval = true;
+                            s_lo = sv.x;
+                        }
                     }
                 }
-                if (st.overflow) bits |= kBitOverflow;
-                T_row = st.T_out;
-                beta_out = rcp_approx(st.T_out);
-                inv_s = 1.0f / st.S_out;
+                const float b_lo = rcp_approx(lo);
+                if (!lo_eval) {
+                    // lo is still t_min: evaluate it (section 5.4 check).
+                    sv = group_sum2<G>(reg_pass<E4>(y, b_lo), gmask);
+                    s_lo = sv.x;
+                    if (entropy_above(sv, b_lo, bound_bits)) bits |= kBitOverflow;
+                }
+                T_row = lo;
+                beta_out = b_lo;
+                inv_s = 1.0f / s_lo;
             }
         }
         const bool zero = row_code != 0;
