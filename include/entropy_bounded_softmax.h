@@ -14,11 +14,13 @@
  *      steps: mid = (lo + hi) / 2; H(mid) > entropy_bound moves hi to mid,
  *      otherwise lo moves to mid.  Temperatures above 1 are never searched
  *      because H is nondecreasing in T (section 2.1 step 4).  By default
- *      the kernels evaluate H only where needed: a midpoint at or below an
- *      evaluated feasible temperature is feasible, and one at or above an
- *      evaluated infeasible temperature is infeasible, so once safeguarded
- *      Newton steps have bracketed the crossing tightly every decision of
- *      the bisection is known (cs_options.strict evaluates each midpoint);
+ *      the cluster kernel evaluates H only where needed: a midpoint at or
+ *      below an evaluated feasible temperature is feasible, and one at or
+ *      above an evaluated infeasible temperature is infeasible, so once
+ *      safeguarded Newton steps have bracketed the crossing tightly every
+ *      decision of the bisection is known (cs_options.strict evaluates each
+ *      midpoint).  The row-group kernel, whose rows are a few registers
+ *      per lane, evaluates every midpoint;
  *   4. write softmax(l / lo) and report T = lo.  If even lo = t_min violates
  *      the bound, the row still gets softmax(l / t_min), the lowest entropy
  *      reachable (section 5.4), and ENTROPY_OVERFLOW is raised.
@@ -70,10 +72,12 @@ typedef struct cs_options {
                           cluster: CTAs per row (1..16); 0 = automatic      */
     int32_t threads;   /* cluster: threads per CTA (multiple of 32,
                           64..512); 0 = automatic                           */
-    int32_t strict;    /* 1 = evaluate H at every bisection midpoint, one
-                          pass per step; 0 = settle the midpoints outside
-                          an evaluated bracket by monotonicity (same result,
-                          fewer passes)                                     */
+    int32_t strict;    /* cluster: 1 = evaluate H at every bisection
+                          midpoint, one pass per step; 0 = settle the
+                          midpoints outside an evaluated bracket by
+                          monotonicity (same result, fewer passes).  The
+                          row-group kernel always evaluates every midpoint;
+                          0 or 1 is accepted there                          */
 } cs_options;
 
 /* What a launch of the given shape uses.  Filled by cs_plan_launch /
