@@ -246,14 +246,21 @@ __device__ __forceinline__ int search_plan(Search& s, const SearchCfg& c,
     return np;
 }
 
+// Whether the round just planned is followed by a Newton step, which needs
+// the slope (hence W) at the round's first point.
+__device__ __forceinline__ bool newton_next(const Search& s) {
+    return !s.final_round && !s.strict && !s.endgame &&
+           s.rounds + 1 < kMaxNewtonRounds;
+}
+
 // Records the round's evaluations: T[i] at beta[i] = rcp_approx(T[i]) gave
-// the row sums S, V, W (arrays of length np).
+// the row sums S, V (arrays of length np) and, when has_w, W[0] at T[0].
 __device__ __forceinline__ void search_update(Search& s, const SearchCfg& c,
                                               int np,
                                               const float (&T)[kMaxPoints],
                                               const float (&beta)[kMaxPoints],
                                               const float* S, const float* V,
-                                              const float* W) {
+                                              const float* W, bool has_w) {
 #pragma unroll
     for (int i = 0; i < kMaxPoints; ++i) {
         if (i >= np) break;
@@ -279,10 +286,13 @@ __device__ __forceinline__ void search_update(Search& s, const SearchCfg& c,
         s.done = true;
         return;
     }
-    // The Newton anchor moves to the round's first point.
-    s.bc = beta[0];
-    s.Hc = entropy_nats(S[0], V[0], beta[0]);
-    s.dHc = entropy_slope(S[0], V[0], W[0], beta[0]);
+    // The Newton anchor moves to the round's first point (only used when
+    // a Newton step follows, which is when W was accumulated).
+    if (has_w) {
+        s.bc = beta[0];
+        s.Hc = entropy_nats(S[0], V[0], beta[0]);
+        s.dHc = entropy_slope(S[0], V[0], W[0], beta[0]);
+    }
     ++s.rounds;
 }
 

@@ -14,22 +14,22 @@
 //           and sums S = sum 2^y_i, V = sum y_i 2^y_i, W = sum y_i^2 2^y_i;
 //           H(1) = ln2 (log2 S - V/S) decides whether a search is needed;
 //   search  rounds of the temperature search of cs_search.cuh: each round
-//           evaluates (S, V, W) at 1-3 temperatures in one pass over the
-//           slice and reduces them; the search returns the bisection's
-//           final lo and S(lo);
+//           evaluates (S, V) at 1-3 temperatures in one pass over the slice
+//           (plus W at the first one when a Newton step follows) and
+//           reduces them; the search returns the bisection's final lo and
+//           S(lo);
 //   output  p_i = 2^(beta_lo y_i) / S(lo), written with 128-bit streaming
 //           stores.
 //
 // Reduction.  Every warp reduces its partial sums with a shuffle tree and
-// writes them to a slot; after a __syncthreads the per-warp slots are
-// reduced by a second shuffle tree (in every warp for one pair of values,
-// else in warp 0, which broadcasts the result through shared memory after a
-// second __syncthreads).  In a cluster, warp 0 then pushes the CTA's sums
-// into every CTA (st.async, counted on an mbarrier) and the waiting threads
-// add the cluster's sums in rank order.  All threads of the cluster thus see
-// bit-identical sums and take the same decisions.  Slots are double-
-// buffered, which is safe because no thread can reach exchange k+2 before
-// every thread has left exchange k.
+// writes them to a slot; after a __syncthreads warp 0 reduces the per-warp
+// slots with a second shuffle tree.  In a cluster, warp 0 then pushes the
+// CTA's sums into every CTA (st.async, counted on an mbarrier), waits for
+// the cluster's pushes and adds them in rank order.  Warp 0 broadcasts the
+// result through shared memory after a second __syncthreads.  All threads of
+// the cluster thus see bit-identical sums and take the same decisions.
+// Slots are double-buffered, which is safe because no thread can reach
+// exchange k+2 before every thread has left exchange k.
 //
 // Every wait is bounded (cs::kWaitLimitCycles by default).  A thread whose
 // wait times out records CS_ERR_TIMEOUT and from then on neither waits,
@@ -43,10 +43,6 @@ namespace cs {
 namespace {
 
 using namespace csd;
-
-__device__ __forceinline__ float4 floor4() {
-    return make_float4(kYFloor, kYFloor, kYFloor, kYFloor);
-}
 
 // Geometry of one CTA's slice in shared memory.  Element j of the slice
 // lives at row[pad + j], so 16-byte aligned global addresses land on
@@ -181,36 +177,34 @@ __device__ __forceinline__ void exchange(float (&a)[NV], const Smem& sm,
         for (int i = 0; i < NV; ++i) ws[warp * kSlotVals + i] = a[i];
     }
     __syncthreads();
-    if (NV <= 2) {
-        // Every warp reduces the slots; the cluster leg is waited on by all.
+    // Warp 0 reduces the per-warp slots (and exchanges across the cluster),
+    // then broadcasts.  (Letting every warp reduce the slots and wait on the
+    // cluster barrier saves one CTA barrier but measured slower: the extra
+    // reductions and waiters cost more than the barrier.)
+    if (warp == 0) {
 #pragma unroll
         for (int i = 0; i < NV; ++i)
             a[i] = lane < x.warps ? ws[lane * kSlotVals + i] : idn;
         warp_reduce<NV, IS_MAX>(a);
-        if (CLUSTER) cluster_leg<NV, IS_MAX>(a, sm, x, true);
-    } else {
-        // Warp 0 reduces (and exchanges across the cluster), then
-        // broadcasts.
-        if (warp == 0) {
-#pragma unroll
-            for (int i = 0; i < NV; ++i)
-                a[i] = lane < x.warps ? ws[lane * kSlotVals + i] : idn;
-            warp_reduce<NV, IS_MAX>(a);
-        }
-        if (CLUSTER) cluster_leg<NV, IS_MAX>(a, sm, x, warp == 0);
-        if (warp == 0 && lane == 0) {
-#pragma unroll
-            for (int i = 0; i < NV; ++i) sm.bcast[i] = a[i];
-        }
-        __syncthreads();
-#pragma unroll
-        for (int i = 0; i < NV; ++i) a[i] = sm.bcast[i];
     }
+    if (CLUSTER) cluster_leg<NV, IS_MAX>(a, sm, x, warp == 0);
+    if (warp == 0 && lane == 0) {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) sm.bcast[i] = a[i];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < NV; ++i) a[i] = sm.bcast[i];
 }
 
-// Accumulators of S, V and W at one inverse temperature: lanes (x, y) and
-// (z, w) of each float4 go to the two halves of a packed pair.
-struct SVW {
+// Accumulators of S, V and (optionally) W at one inverse temperature: lanes
+// (x, y) and (z, w) of each float4 go to the two halves of a packed pair.
+// Each packed fp32x2 operation occupies both FMA sub-pipes, so the pass
+// with W (10 packed operations per float4) is bound by the FMA pipes and
+// the one without (6 per float4) by the ex2 unit: W is accumulated only
+// where a Newton step will use it.
+template <bool WITH_W>
+struct Acc {
     float2 s, v, w;
     __device__ __forceinline__ void zero() {
         s = v = w = make_float2(0.f, 0.f);
@@ -222,12 +216,17 @@ struct SVW {
         const float2 x23 = mul2(y23, b2);
         const float2 e01 = make_float2(ex2(x01.x), ex2(x01.y));
         const float2 e23 = make_float2(ex2(x23.x), ex2(x23.y));
-        const float2 ey01 = mul2(e01, y01);
-        const float2 ey23 = mul2(e23, y23);
         s = add2(s, add2(e01, e23));
-        v = add2(v, add2(ey01, ey23));
-        w = fma2(ey01, y01, w);
-        w = fma2(ey23, y23, w);
+        if (WITH_W) {
+            const float2 ey01 = mul2(e01, y01);
+            const float2 ey23 = mul2(e23, y23);
+            v = add2(v, add2(ey01, ey23));
+            w = fma2(ey01, y01, w);
+            w = fma2(ey23, y23, w);
+        } else {
+            v = fma2(e01, y01, v);
+            v = fma2(e23, y23, v);
+        }
     }
 };
 
@@ -235,7 +234,7 @@ struct SVW {
 // y = max((l - m) log2 e, floor) and returns the partial S, V, W at beta = 1.
 __device__ __forceinline__ void transform_pass(float4* row4, int q4, float m,
                                                float (&out)[3]) {
-    SVW acc;
+    Acc<true> acc;
     acc.zero();
     const float2 one = make_float2(1.0f, 1.0f);
     for (int q = threadIdx.x; q < q4; q += blockDim.x) {
@@ -252,41 +251,65 @@ __device__ __forceinline__ void transform_pass(float4* row4, int q4, float m,
     out[2] = acc.w.x + acc.w.y;
 }
 
+// Number of partial sums a pass at P temperatures produces: S and V per
+// point, plus W of point 0 when W0.
+template <int P, bool W0>
+struct PassOut {
+    static constexpr int kN = 2 * P + (W0 ? 1 : 0);
+    // Index of point p's S (its V follows).
+    static __device__ __forceinline__ constexpr int s_idx(int p) {
+        return p == 0 ? 0 : 2 * p + (W0 ? 1 : 0);
+    }
+};
+
 // One pass over this thread's float4s of the slice at P inverse
-// temperatures; out = {S_0, V_0, W_0, S_1, ...}.  Thread t owns float4s
-// t, t + nt, ... (two per trip).
-template <int P>
+// temperatures; out holds PassOut<P, W0>'s layout (W of point 0 at index 2).
+// Thread t owns float4s t, t + nt, ... (two per trip; a last single one).
+template <int P, bool W0>
 __device__ __forceinline__ void eval_pass(const float4* row4, int q4,
                                           const float (&beta)[kMaxPoints],
-                                          float (&out)[3 * P]) {
-    SVW acc[P];
+                                          float (&out)[PassOut<P, W0>::kN]) {
+    Acc<W0> a0;
+    Acc<false> ap[P > 1 ? P - 1 : 1];
     float2 b2[P];
+    a0.zero();
 #pragma unroll
     for (int p = 0; p < P; ++p) {
-        acc[p].zero();
+        if (p > 0) ap[p - 1].zero();
         b2[p] = make_float2(beta[p], beta[p]);
     }
     const int nt = blockDim.x;
-    for (int qa = threadIdx.x; qa < q4; qa += 2 * nt) {
-        const int qc = qa + nt;
-        const float4 ya = row4[qa];
-        const float4 yc = qc < q4 ? row4[qc] : floor4();
+    int q = threadIdx.x;
+    for (; q + nt < q4; q += 2 * nt) {
+        const float4 ya = row4[q];
+        const float4 yc = row4[q + nt];
+        a0.add(ya, b2[0]);
+        a0.add(yc, b2[0]);
 #pragma unroll
-        for (int p = 0; p < P; ++p) {
-            acc[p].add(ya, b2[p]);
-            acc[p].add(yc, b2[p]);
+        for (int p = 1; p < P; ++p) {
+            ap[p - 1].add(ya, b2[p]);
+            ap[p - 1].add(yc, b2[p]);
         }
     }
+    if (q < q4) {
+        const float4 ya = row4[q];
+        a0.add(ya, b2[0]);
 #pragma unroll
-    for (int p = 0; p < P; ++p) {
-        out[3 * p] = acc[p].s.x + acc[p].s.y;
-        out[3 * p + 1] = acc[p].v.x + acc[p].v.y;
-        out[3 * p + 2] = acc[p].w.x + acc[p].w.y;
+        for (int p = 1; p < P; ++p) ap[p - 1].add(ya, b2[p]);
+    }
+    out[0] = a0.s.x + a0.s.y;
+    out[1] = a0.v.x + a0.v.y;
+    if (W0) out[2 % PassOut<P, W0>::kN] = a0.w.x + a0.w.y;
+#pragma unroll
+    for (int p = 1; p < P; ++p) {
+        out[PassOut<P, W0>::s_idx(p)] = ap[p - 1].s.x + ap[p - 1].s.y;
+        out[PassOut<P, W0>::s_idx(p) + 1] = ap[p - 1].v.x + ap[p - 1].v.y;
     }
 }
 
-// One search round with P temperatures: pass, exchange, update.
-template <bool CLUSTER, int P>
+// One search round with P temperatures: pass, exchange, update.  W0: the
+// next round takes a Newton step from point 0, which needs its W.
+template <bool CLUSTER, int P, bool W0>
 __device__ __forceinline__ void search_round(Search& st, const SearchCfg& cfg,
                                              const float (&T)[kMaxPoints],
                                              const float4* row4, int q4,
@@ -294,18 +317,20 @@ __device__ __forceinline__ void search_round(Search& st, const SearchCfg& cfg,
     float beta[kMaxPoints];
 #pragma unroll
     for (int p = 0; p < kMaxPoints; ++p) beta[p] = p < P ? rcp_approx(T[p]) : 1.0f;
-    float a[3 * P];
-    eval_pass<P>(row4, q4, beta, a);
-    exchange<CLUSTER, 3 * P, false>(a, sm, x);
+    constexpr int NV = PassOut<P, W0>::kN;
+    float a[NV];
+    eval_pass<P, W0>(row4, q4, beta, a);
+    exchange<CLUSTER, NV, false>(a, sm, x);
     float S[kMaxPoints], V[kMaxPoints], W[kMaxPoints];
 #pragma unroll
     for (int p = 0; p < kMaxPoints; ++p) {
-        const int q = p < P ? p : 0;
-        S[p] = p < P ? a[3 * q] : 1.0f;
-        V[p] = p < P ? a[3 * q + 1] : 0.0f;
-        W[p] = p < P ? a[3 * q + 2] : 0.0f;
+        const int i = PassOut<P, W0>::s_idx(p < P ? p : 0);
+        S[p] = p < P ? a[i] : 1.0f;
+        V[p] = p < P ? a[i + 1] : 0.0f;
+        W[p] = 0.0f;
     }
-    search_update(st, cfg, P, T, beta, S, V, W);
+    if (W0) W[0] = a[2 % NV];
+    search_update(st, cfg, P, T, beta, S, V, W, W0);
 }
 
 __device__ __forceinline__ void store_scalar_lanes(float* dst, int q, int pad,
@@ -481,17 +506,22 @@ cluster_kernel(RowTask t, int n, int slice_len) {
                     st.final_check = true;
                     st.T_out = cfg.t_min;
                     float T1[kMaxPoints] = {cfg.t_min, 0.f, 0.f};
-                    search_round<CLUSTER, 1>(st, cfg, T1, row4, s.q4, sm, x);
+                    search_round<CLUSTER, 1, false>(st, cfg, T1, row4, s.q4, sm, x);
                 }
                 while (!st.done) {
                     float T[kMaxPoints];
                     const int np = search_plan(st, cfg, T);
-                    if (np == 1)
-                        search_round<CLUSTER, 1>(st, cfg, T, row4, s.q4, sm, x);
+                    const bool w0 = newton_next(st);
+                    if (np == 1 && w0)
+                        search_round<CLUSTER, 1, true>(st, cfg, T, row4, s.q4, sm, x);
+                    else if (np == 1)
+                        search_round<CLUSTER, 1, false>(st, cfg, T, row4, s.q4, sm, x);
+                    else if (np == 2 && w0)
+                        search_round<CLUSTER, 2, true>(st, cfg, T, row4, s.q4, sm, x);
                     else if (np == 2)
-                        search_round<CLUSTER, 2>(st, cfg, T, row4, s.q4, sm, x);
+                        search_round<CLUSTER, 2, false>(st, cfg, T, row4, s.q4, sm, x);
                     else if (np == 3)
-                        search_round<CLUSTER, 3>(st, cfg, T, row4, s.q4, sm, x);
+                        search_round<CLUSTER, 3, false>(st, cfg, T, row4, s.q4, sm, x);
                 }
                 if (st.overflow) bits |= kBitOverflow;
                 T_row = st.T_out;
