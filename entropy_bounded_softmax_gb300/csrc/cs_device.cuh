@@ -1,5 +1,5 @@
 // Device helpers shared by the kernels of libcsoftmax: the ex2/lg2 units,
-// mbarriers with bounded waits, bulk global->shared copies, DSMEM pushes and
+// mbarriers with bounded waits, DSMEM pushes and
 // warp/group reductions.  sm_103a only; inline PTX where CUDA has no
 // intrinsic.
 #pragma once
@@ -127,12 +127,6 @@ __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
-// Orders this CTA's generic-proxy shared-memory accesses before later
-// async-proxy (bulk copy) accesses.
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar,
                                                       uint32_t bytes) {
     asm volatile(
@@ -181,18 +175,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
         if (clock64() - c0 > static_cast<long long>(limit_cycles)) return false;
     }
     return false;
-}
-
-// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned)
-// from global memory into this CTA's shared memory; completion is counted
-// on `bar` as transaction bytes.
-__device__ __forceinline__ void bulk_load(void* dst, const void* src,
-                                          uint32_t bytes, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
-        "[%0], [%1], %2, [%3];"
-        :: "r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
-        : "memory");
 }
 
 // ------------------------------------------------------------------ cluster

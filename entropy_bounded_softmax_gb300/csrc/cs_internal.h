@@ -40,7 +40,6 @@ struct RowTask {
 
 // Cluster kernel geometry.
 constexpr int kMaxCluster = 16;
-constexpr int kLoadChunks = 8;        // bulk copies per CTA slice
 constexpr int kClusterMaxThreads = 512;
 constexpr int kSlotVals = 12;         // floats per exchange slot
 
@@ -49,7 +48,7 @@ constexpr int kSlotVals = 12;         // floats per exchange slot
 // slots [2][warps][kSlotVals], a broadcast slot, the two cluster mbarriers
 // and the load mbarriers; then (128-byte aligned) the slice.
 struct ClusterSmemLayout {
-    int cslot, wslot, bcast, cbar, lbar, row;
+    int cslot, wslot, bcast, cbar, row;
 };
 
 __host__ __device__ inline ClusterSmemLayout cluster_smem_layout(int warps,
@@ -65,8 +64,6 @@ __host__ __device__ inline ClusterSmemLayout cluster_smem_layout(int warps,
     p = ((p + 7) / 8) * 8;
     L.cbar = p;
     p += 2 * 8;
-    L.lbar = p;
-    p += kLoadChunks * 8;
     L.row = ((p + 127) / 128) * 128;
     return L;
 }

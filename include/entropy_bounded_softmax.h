@@ -99,8 +99,8 @@ typedef struct cs_plan {
  *
  * logits   device pointer, [batch, num_classes] fp32, row-major, contiguous.
  *          Read only.  Any 4-byte alignment is accepted; 16-byte aligned
- *          rows (num_classes % 4 == 0 and an aligned base) take the bulk-copy
- *          and 128-bit store path.
+ *          rows (num_classes % 4 == 0 and an aligned base) take the 128-bit
+ *          load and store path.
  * out      device pointer, [batch, num_classes] fp32, written completely.
  *          Must not overlap logits (the page declares both __restrict__).
  * batch    rows; 0 is a no-op that returns CS_OK.
