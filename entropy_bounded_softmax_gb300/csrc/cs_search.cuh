@@ -114,6 +114,9 @@ struct Search {
     bool done;
     bool strict;        // evaluate unsettled midpoints one by one
     bool endgame;       // Newton has converged: bisect the unsettled rest
+    bool pred_valid;    // pred holds the path predicted at convergence
+    Cursor pred;        // ... whose ends are being evaluated this round
+    float S_plo;        // S at pred.lo, once evaluated (0: not yet)
     int rounds;
     float T_out, S_out;
     bool overflow;      // section 5.4: even t_min violates the bound
@@ -151,6 +154,9 @@ __device__ __forceinline__ Search search_begin(const SearchCfg& c, float S1,
     s.done = false;
     s.strict = strict;
     s.endgame = false;
+    s.pred_valid = false;
+    s.pred = s.cur;
+    s.S_plo = 0.0f;
     s.rounds = 0;
     s.T_out = 0.0f;
     s.S_out = 0.0f;
@@ -163,6 +169,16 @@ __device__ __forceinline__ Search search_begin(const SearchCfg& c, float S1,
 __device__ __forceinline__ int search_plan(Search& s, const SearchCfg& c,
                                            float (&T)[kMaxPoints]) {
     float um = 0.0f;
+    if (s.pred_valid) {
+        // The path predicted at convergence is the bisection's if its ends
+        // were evaluated on the predicted sides: every predicted-feasible
+        // midpoint is then <= A and every predicted-infeasible one >= B, so
+        // the replay would take exactly the predicted decisions.
+        s.pred_valid = false;
+        if ((!s.pred.lo_eval || s.A >= s.pred.lo) &&
+            (!s.pred.hi_eval || s.B <= s.pred.hi))
+            s.cur = s.pred;
+    }
     if (!advance(s.cur, c, s.A, s.B, false, 0.0f, &um)) {
         const float lo = s.cur.lo;
         s.T_out = lo;
@@ -181,6 +197,10 @@ __device__ __forceinline__ int search_plan(Search& s, const SearchCfg& c,
             return 0;
         } else if (s.tmin_done && lo == c.t_min) {
             s.S_out = s.S_tmin;
+            s.done = true;
+            return 0;
+        } else if (s.S_plo > 0.0f && lo == s.pred.lo) {
+            s.S_out = s.S_plo;
             s.done = true;
             return 0;
         }
@@ -236,6 +256,8 @@ __device__ __forceinline__ int search_plan(Search& s, const SearchCfg& c,
         Cursor pred = s.cur;
         float dummy;
         advance(pred, c, s.A, s.B, true, Tn, &dummy);
+        s.pred = pred;
+        s.pred_valid = true;
         if (pred.lo > s.A && pred.lo < s.B && pred.lo != Tn &&
             pred.lo >= c.t_min)
             T[np++] = pred.lo;
@@ -271,6 +293,7 @@ __device__ __forceinline__ void search_update(Search& s, const SearchCfg& c,
             s.tmin_inf = inf;
             s.S_tmin = S[i];
         }
+        if (s.pred_valid && T[i] == s.pred.lo) s.S_plo = S[i];
         if (inf) {
             if (T[i] < s.B) s.B = T[i];
         } else if (T[i] > s.A) {
