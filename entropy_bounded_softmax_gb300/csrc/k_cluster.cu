@@ -162,7 +162,6 @@ __device__ __forceinline__ void exchange(float (&a)[NV], const Smem& sm,
     static_assert(NV <= kSlotVals, "payload");
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const float idn = IS_MAX ? -INFINITY : 0.0f;
     warp_reduce<NV, IS_MAX>(a);
     float* ws = sm.wslot + (x.lk & 1u) * x.warps * kSlotVals;
     ++x.lk;
@@ -176,10 +175,21 @@ __device__ __forceinline__ void exchange(float (&a)[NV], const Smem& sm,
     // cluster barrier saves one CTA barrier but measured slower: the extra
     // reductions and waiters cost more than the barrier.)
     if (warp == 0) {
+        // Lane groups of w2 >= warps lanes (a power of two) each hold every
+        // warp's slot and reduce it with a log2(w2)-level shuffle tree.
+        const float idn = IS_MAX ? -INFINITY : 0.0f;
+        const int w2 = x.warps <= 4 ? 4 : (x.warps <= 8 ? 8 : 16);
+        const int sl = lane & (w2 - 1);
 #pragma unroll
         for (int i = 0; i < NV; ++i)
-            a[i] = lane < x.warps ? ws[lane * kSlotVals + i] : idn;
-        warp_reduce<NV, IS_MAX>(a);
+            a[i] = sl < x.warps ? ws[sl * kSlotVals + i] : idn;
+        for (int o = w2 >> 1; o > 0; o >>= 1) {
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+                const float b = __shfl_xor_sync(0xffffffffu, a[i], o);
+                a[i] = IS_MAX ? fmaxf(a[i], b) : a[i] + b;
+            }
+        }
     }
     if (CLUSTER) cluster_leg<NV, IS_MAX>(a, sm, x, warp == 0);
     if (warp == 0 && lane == 0) {
@@ -231,12 +241,27 @@ __device__ __forceinline__ void transform_pass(float4* row4, int q4, float m,
     Acc<true> acc;
     acc.zero();
     const float2 one = make_float2(1.0f, 1.0f);
-    for (int q = threadIdx.x; q < q4; q += blockDim.x) {
-        float4 y = row4[q];
-        y.x = fmaxf((y.x - m) * kLog2e, kYFloor);
-        y.y = fmaxf((y.y - m) * kLog2e, kYFloor);
-        y.z = fmaxf((y.z - m) * kLog2e, kYFloor);
-        y.w = fmaxf((y.w - m) * kLog2e, kYFloor);
+    auto to_y = [m](float4 l) {
+        return make_float4(fmaxf((l.x - m) * kLog2e, kYFloor),
+                           fmaxf((l.y - m) * kLog2e, kYFloor),
+                           fmaxf((l.z - m) * kLog2e, kYFloor),
+                           fmaxf((l.w - m) * kLog2e, kYFloor));
+    };
+    // Four float4s per trip (independent chains), then the rest one by one.
+    const int nt = blockDim.x;
+    int q = threadIdx.x;
+    for (; q + 3 * nt < q4; q += 4 * nt) {
+        float4 y[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) y[i] = to_y(row4[q + i * nt]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            row4[q + i * nt] = y[i];
+            acc.add(y[i], one);
+        }
+    }
+    for (; q < q4; q += nt) {
+        const float4 y = to_y(row4[q]);
         row4[q] = y;
         acc.add(y, one);
     }
@@ -258,7 +283,7 @@ struct PassOut {
 
 // One pass over this thread's float4s of the slice at P inverse
 // temperatures; out holds PassOut<P, W0>'s layout (W of point 0 at index 2).
-// Thread t owns float4s t, t + nt, ... (two per trip; a last single one).
+// Thread t owns float4s t, t + nt, ... (four per trip, then one by one).
 template <int P, bool W0>
 __device__ __forceinline__ void eval_pass(const float4* row4, int q4,
                                           const float (&beta)[kMaxPoints],
@@ -274,18 +299,18 @@ __device__ __forceinline__ void eval_pass(const float4* row4, int q4,
     }
     const int nt = blockDim.x;
     int q = threadIdx.x;
-    for (; q + nt < q4; q += 2 * nt) {
-        const float4 ya = row4[q];
-        const float4 yc = row4[q + nt];
-        a0.add(ya, b2[0]);
-        a0.add(yc, b2[0]);
+    for (; q + 3 * nt < q4; q += 4 * nt) {
+        float4 y[4];
 #pragma unroll
-        for (int p = 1; p < P; ++p) {
-            ap[p - 1].add(ya, b2[p]);
-            ap[p - 1].add(yc, b2[p]);
+        for (int i = 0; i < 4; ++i) y[i] = row4[q + i * nt];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            a0.add(y[i], b2[0]);
+#pragma unroll
+            for (int p = 1; p < P; ++p) ap[p - 1].add(y[i], b2[p]);
         }
     }
-    if (q < q4) {
+    for (; q < q4; q += nt) {
         const float4 ya = row4[q];
         a0.add(ya, b2[0]);
 #pragma unroll
@@ -346,22 +371,39 @@ __device__ __forceinline__ void write_out(const float4* row4, const Slice& s,
     const bool vec = pad_o == s.pad;
     const float2 b2 = make_float2(beta, beta);
     const float2 i2 = make_float2(inv_s, inv_s);
-    for (int q = threadIdx.x; q < s.q4; q += blockDim.x) {
-        float4 p = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (!zero) {
-            const float4 y = row4[q];
-            const float2 x01 = mul2(make_float2(y.x, y.y), b2);
-            const float2 x23 = mul2(make_float2(y.z, y.w), b2);
-            const float2 p01 = mul2(make_float2(ex2(x01.x), ex2(x01.y)), i2);
-            const float2 p23 = mul2(make_float2(ex2(x23.x), ex2(x23.y)), i2);
-            p = make_float4(p01.x, p01.y, p23.x, p23.y);
-        }
-        if (vec && q >= s.qb0 && q < s.qb1) {
-            __stcs(reinterpret_cast<float4*>(dst + (4 * q - s.pad)), p);
-        } else {
-            store_scalar_lanes(dst, q, s.pad, s.len, p);
-        }
+    auto prob = [&](int q) {
+        if (zero) return make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 y = row4[q];
+        const float2 x01 = mul2(make_float2(y.x, y.y), b2);
+        const float2 x23 = mul2(make_float2(y.z, y.w), b2);
+        const float2 p01 = mul2(make_float2(ex2(x01.x), ex2(x01.y)), i2);
+        const float2 p23 = mul2(make_float2(ex2(x23.x), ex2(x23.y)), i2);
+        return make_float4(p01.x, p01.y, p23.x, p23.y);
+    };
+    const int nt = blockDim.x;
+    if (!vec) {
+        // The output's alignment differs from the input's: element stores.
+        for (int q = threadIdx.x; q < s.q4; q += nt)
+            store_scalar_lanes(dst, q, s.pad, s.len, prob(q));
+        return;
     }
+    // Aligned body, four float4s per trip; then the ragged head and tail.
+    float* const db = dst - s.pad;  // float4 q of the body is at db + 4q
+    int q = s.qb0 + threadIdx.x;
+    for (; q + 3 * nt < s.qb1; q += 4 * nt) {
+        float4 p[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) p[i] = prob(q + i * nt);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            __stcs(reinterpret_cast<float4*>(db + 4 * (q + i * nt)), p[i]);
+    }
+    for (; q < s.qb1; q += nt)
+        __stcs(reinterpret_cast<float4*>(db + 4 * q), prob(q));
+    if (threadIdx.x == 0 && s.head_q >= 0)
+        store_scalar_lanes(dst, s.head_q, s.pad, s.len, prob(s.head_q));
+    if (threadIdx.x == nt - 1 && s.tail_q >= 0)
+        store_scalar_lanes(dst, s.tail_q, s.pad, s.len, prob(s.tail_q));
 }
 
 // MAXT: largest block the instantiation is launched with; MINB: blocks per
