@@ -63,8 +63,8 @@ def parse_args(argv=None):
     ap.add_argument("--threads", type=int, default=0,
                     help="cluster variant: threads per CTA (0 = automatic)")
     ap.add_argument("--strict", action="store_true",
-                    help="cluster variant: evaluate every unsettled "
-                         "bisection midpoint one at a time")
+                    help="cluster variant: halve the bracket one "
+                         "evaluation per round (the bisection itself)")
     ap.add_argument("--batch", type=int, default=0,
                     help="use only the first BATCH rows of the workload "
                          "(profiling captures); 0 = the whole workload")

@@ -1,27 +1,36 @@
 // The temperature search shared by the kernels: the result of the page's
 // bisection ("BURT-IMMA CUDA Kernel API Reference", section 2.1 Description
 // step 3: max_iter halvings of [t_min, min(1, t_max)], hi moves to an
-// infeasible midpoint, lo to a feasible one) computed with few evaluations.
+// infeasible midpoint, lo to a feasible one).
 //
-// H(T) is nondecreasing in T (section 2.1 step 4), so once evaluations have
-// found a feasible A and an infeasible B, every midpoint m <= A is feasible
-// and every m >= B infeasible without being evaluated.  The search keeps that
-// bracket and replays the bisection's midpoint sequence (same fp32
-// arithmetic, same early stop) with the decisions it settles; only
-// midpoints inside (A, B) are unknown.  To shrink the bracket it evaluates
-// safeguarded Newton points for log H(beta) = log bound (beta = 1/T), the
-// bracket's geometric midpoint when Newton leaves it, t_min when the root
-// approaches it, and, once Newton has converged, the two ends of the
-// bisection path predicted from the Newton point.  Midpoints that remain
-// unsettled after that (they lie where fp32 evaluations of H are within
-// rounding of the bound) are evaluated directly, each together with both
-// of its possible successors, two bisection levels per round.  The replay
-// keeps a cursor, so every decision is taken once.  When every midpoint is
-// settled, the bisection's final lo is known; its S (for the output) comes
-// from the evaluation at lo, made in one last round if lo was not evaluated
-// already.  The result is the bisection's: each of its decisions is either
-// evaluated or implied by evaluations and the monotonicity of H.  A strict
-// mode evaluates every unsettled midpoint one at a time instead.
+// The grid.  After K = max_iter halvings every point the bisection can
+// reach is lo0 + j (hi0 - lo0) / 2^K for an integer j in [0, 2^K]
+// (lo0 = t_min, hi0 = min(1, t_max)); the kernels use those exact dyadic
+// points, rounded once to fp32, rather than repeated fp32 halving (the
+// page gives no precision for mid; an fp64 bisection's midpoints are the
+// same dyadic points).  For K > 24 the points are closer together than
+// fp32 resolves over most of the range, and the grid is the fp32 numbers
+// of [lo0, hi0] themselves (index = bit-pattern offset from lo0).  A
+// halving is then an integer midpoint of a bracket of indices [jl, jh]:
+// jl feasible (or 0, t_min, not evaluated), jh infeasible (or the top,
+// hi0, which the bisection never evaluates).
+//
+// The result.  H(T) is nondecreasing in T (section 2.1 step 4), so the
+// bisection's final lo is the largest grid point whose H is within the
+// bound (t_min if none): the bracket can be closed from evaluations inside
+// it in any order, and once jh = jl + 1 the result is G(jl).  The default
+// search therefore evaluates safeguarded Newton points for
+// log H(beta) = log bound (beta = 1/T) placed on the grid, t_min when the
+// root approaches it, then, once Newton has converged, the grid points on
+// both sides of the Newton point; if the bracket is still open
+// (evaluations of H in fp32 are within rounding of the bound there) it
+// splits the bracket into quarters, two halvings per round.  With one
+// point per round (narrow rows, where a pass costs little next to
+// divergent bookkeeping) the Newton point is evaluated alone and the
+// neighbours follow one by one, with doubling strides.  The strict mode
+// evaluates the bracket's midpoint, one halving per round.  The output
+// needs S at the result, kept from the evaluation that set jl (or taken in
+// one last round at t_min, which also decides the section 5.4 flag).
 //
 // One evaluation at inverse temperature beta yields, over the row's
 // y = (l - max) log2 e:  S = sum 2^(beta y),  V = sum y 2^(beta y),
@@ -35,88 +44,79 @@
 
 namespace csd {
 
-constexpr int kMaxPoints = 3;       // temperatures evaluated per round
-constexpr int kMaxNewtonRounds = 40;  // then evaluate midpoints one by one
+constexpr int kMaxPoints = 3;         // temperatures evaluated per round
+constexpr int kMaxNewtonRounds = 40;  // then halve the bracket round by round
+constexpr int kMaxExactLevels = 24;   // grid indices exact in fp32 up to 2^24
+
+// The bisection's grid (see the file comment).
+struct Grid {
+    float lo0;       // index 0: t_min
+    float step_hi;   // (hi0 - lo0) / 2^K = step_hi + step_lo exactly
+    float step_lo;
+    float inv_step;  // 1 / step_hi, to place a temperature on the grid
+    int lo_bits;     // fine grid: bit pattern of lo0
+    int top;         // index of hi0
+    bool fine;       // K > 24: every fp32 value of [lo0, hi0] is a point
+
+    // Grid point j, 0 <= j <= top; nondecreasing in j.
+    __device__ __forceinline__ float at(int j) const {
+        if (fine) return __int_as_float(lo_bits + j);
+        const float fj = static_cast<float>(j);
+        return fmaf(fj, step_hi, fmaf(fj, step_lo, lo0));
+    }
+    // An index whose point is within about one step of T (lo0 < T).
+    __device__ __forceinline__ int near(float T) const {
+        if (fine) return __float_as_int(T) - lo_bits;
+        return __float2int_rd(fminf((T - lo0) * inv_step, 2.0e9f));
+    }
+};
+
+// Grid of max_iter halvings of [lo0, hi0]; requires 0 < lo0 < hi0.
+__device__ __forceinline__ Grid make_grid(float lo0, float hi0, int max_iter) {
+    Grid g;
+    g.lo0 = lo0;
+    g.lo_bits = __float_as_int(lo0);
+    g.fine = max_iter > kMaxExactLevels;
+    if (g.fine) {
+        g.top = __float_as_int(hi0) - g.lo_bits;
+        g.step_hi = g.step_lo = g.inv_step = 0.0f;
+    } else {
+        // hi0 - lo0 = s + e exactly (two-sum), scaled by 2^-K exactly.
+        const float s = hi0 - lo0;
+        const float bv = s - hi0;
+        const float e = (hi0 - (s - bv)) + (-lo0 - bv);
+        const float scale = __int_as_float((127 - max_iter) << 23);
+        g.step_hi = s * scale;
+        g.step_lo = e * scale;
+        g.inv_step = 1.0f / g.step_hi;
+        g.top = 1 << max_iter;
+    }
+    return g;
+}
 
 struct SearchCfg {
     float t_min;
     float hi0;          // min(1, t_max)
     float bound;        // nats
     float bound_bits;   // bound * log2 e
-    int max_iter;
+    Grid g;
 };
 
-// Midpoint of the bisection, in the fp32 arithmetic every variant uses.
-__device__ __forceinline__ float midpoint(float lo, float hi) {
-    return 0.5f * (lo + hi);
-}
-
-// Position of the replayed bisection: its lo and hi, whether each has been
-// decided (for the fp32 early stop) and the steps taken.
-struct Cursor {
-    float lo, hi;
-    bool lo_eval, hi_eval;
-    int k;
-};
-
-__device__ __forceinline__ Cursor cursor_begin(const SearchCfg& c) {
-    return Cursor{c.t_min, c.hi0, false, c.hi0 == 1.0f, 0};
-}
-
-// Advances the replay while its decisions are settled: m >= B infeasible,
-// m <= A feasible (A = 0: none known); with use_pred, the rest by
-// [m > Tp].  Returns true and the midpoint in *um if it stopped at an
-// unsettled midpoint, false when the bisection is complete.
-__device__ __forceinline__ bool advance(Cursor& cu, const SearchCfg& c,
-                                        float A, float B, bool use_pred,
-                                        float Tp, float* um) {
-    while (cu.k < c.max_iter) {
-        const float m = midpoint(cu.lo, cu.hi);
-        if ((m == cu.lo && cu.lo_eval) || (m == cu.hi && cu.hi_eval)) {
-            // The fp32 midpoint repeats a decided end: every further step
-            // would repeat that decision.
-            cu.k = c.max_iter;
-            break;
-        }
-        bool inf;
-        if (m >= B) {
-            inf = true;
-        } else if (A > 0.0f && m <= A) {
-            inf = false;
-        } else if (use_pred) {
-            inf = m > Tp;
-        } else {
-            *um = m;
-            return true;
-        }
-        if (inf) {
-            cu.hi = m;
-            cu.hi_eval = true;
-        } else {
-            cu.lo = m;
-            cu.lo_eval = true;
-        }
-        ++cu.k;
-    }
-    return false;
-}
-
-// Per-row search state; identical in every thread working on the row.
+// Per-row search state; identical in every thread that plans for the row.
 struct Search {
-    Cursor cur;         // the replayed bisection
-    float A, SA;        // largest feasible T evaluated, its S (A = 0: none)
-    float B;            // smallest infeasible T evaluated
-    float bc, Hc, dHc;  // Newton anchor: beta, H (nats), dH/dbeta
-    float S_tmin;       // S at t_min, if evaluated
-    bool tmin_done, tmin_inf;
-    bool final_round;   // this round evaluates the final lo
-    bool final_check;   // ... which is t_min, never moved: flag if infeasible
+    int jl, jh;         // bracket of grid indices
+    bool jl_eval;       // G(jl) was evaluated feasible (else jl = 0, unseen)
+    bool tmin_inf;      // t_min was evaluated infeasible (section 5.4)
+    bool final_round;   // this round evaluates t_min for the result
     bool done;
-    bool strict;        // evaluate unsettled midpoints one by one
-    bool endgame;       // Newton has converged: bisect the unsettled rest
-    bool pred_valid;    // pred holds the path predicted at convergence
-    Cursor pred;        // ... whose ends are being evaluated this round
-    float S_plo;        // S at pred.lo, once evaluated (0: not yet)
+    bool strict;        // halve the bracket one evaluation per round
+    bool endgame;       // Newton has converged: quarter the bracket
+    bool single;        // one point per round
+    int jlast;          // single: the index evaluated last
+    int stride;         // single: the next neighbour step
+    float SA;           // S at G(jl) when jl_eval
+    float S_tmin;       // S at t_min when tmin_inf
+    float bc, Hc, dHc;  // Newton anchor: beta, H (nats), dH/dbeta
     int rounds;
     float T_out, S_out;
     bool overflow;      // section 5.4: even t_min violates the bound
@@ -137,26 +137,24 @@ __device__ __forceinline__ float entropy_slope(float S, float V, float W,
 // H(1) > bound.
 __device__ __forceinline__ Search search_begin(const SearchCfg& c, float S1,
                                                float V1, float W1,
-                                               bool strict) {
+                                               bool strict, bool single) {
     Search s;
-    s.cur = cursor_begin(c);
-    s.A = 0.0f;
-    s.SA = 0.0f;
-    s.B = 1.0f;
-    s.bc = 1.0f;
-    s.Hc = entropy_nats(S1, V1, 1.0f);
-    s.dHc = entropy_slope(S1, V1, W1, 1.0f);
-    s.S_tmin = 0.0f;
-    s.tmin_done = false;
+    s.jl = 0;
+    s.jh = c.g.top;
+    s.jl_eval = false;
     s.tmin_inf = false;
     s.final_round = false;
-    s.final_check = false;
     s.done = false;
     s.strict = strict;
     s.endgame = false;
-    s.pred_valid = false;
-    s.pred = s.cur;
-    s.S_plo = 0.0f;
+    s.single = single;
+    s.jlast = -1;
+    s.stride = 1;
+    s.SA = 0.0f;
+    s.S_tmin = 0.0f;
+    s.bc = 1.0f;
+    s.Hc = entropy_nats(S1, V1, 1.0f);
+    s.dHc = entropy_slope(S1, V1, W1, 1.0f);
     s.rounds = 0;
     s.T_out = 0.0f;
     s.S_out = 0.0f;
@@ -164,107 +162,109 @@ __device__ __forceinline__ Search search_begin(const SearchCfg& c, float S1,
     return s;
 }
 
-// Chooses the temperatures of the next round; returns how many (0: done,
-// with T_out, S_out and overflow set).
+// Chooses the grid points of the next round (indices J, temperatures T);
+// returns how many (0: done, with T_out, S_out and overflow set).
 __device__ __forceinline__ int search_plan(Search& s, const SearchCfg& c,
-                                           float (&T)[kMaxPoints]) {
-    float um = 0.0f;
-    if (s.pred_valid) {
-        // The path predicted at convergence is the bisection's if its ends
-        // were evaluated on the predicted sides: every predicted-feasible
-        // midpoint is then <= A and every predicted-infeasible one >= B, so
-        // the replay would take exactly the predicted decisions.
-        s.pred_valid = false;
-        if ((!s.pred.lo_eval || s.A >= s.pred.lo) &&
-            (!s.pred.hi_eval || s.B <= s.pred.hi))
-            s.cur = s.pred;
+                                           float (&T)[kMaxPoints],
+                                           int (&J)[kMaxPoints]) {
+    const Grid& g = c.g;
+    if (s.tmin_inf) {
+        // Every grid point is infeasible: lo never moves (section 5.4).
+        s.T_out = g.lo0;
+        s.S_out = s.S_tmin;
+        s.overflow = true;
+        s.done = true;
+        return 0;
     }
-    if (!advance(s.cur, c, s.A, s.B, false, 0.0f, &um)) {
-        const float lo = s.cur.lo;
-        s.T_out = lo;
-        if (!s.cur.lo_eval) {
-            // lo never moved: it is t_min, whose own evaluation decides the
-            // degradation flag (section 5.4).
-            if (s.tmin_done) {
-                s.S_out = s.S_tmin;
-                s.overflow = s.tmin_inf;
-                s.done = true;
-                return 0;
-            }
-        } else if (s.A > 0.0f && lo == s.A) {
+    if (s.jh - s.jl <= 1) {
+        s.T_out = g.at(s.jl);
+        if (s.jl_eval) {
             s.S_out = s.SA;
             s.done = true;
             return 0;
-        } else if (s.tmin_done && lo == c.t_min) {
-            s.S_out = s.S_tmin;
-            s.done = true;
-            return 0;
-        } else if (s.S_plo > 0.0f && lo == s.pred.lo) {
-            s.S_out = s.S_plo;
-            s.done = true;
-            return 0;
         }
+        // lo stayed at t_min without an evaluation there: one more for its
+        // S and the section 5.4 check.
         s.final_round = true;
-        s.final_check = !s.cur.lo_eval;
-        T[0] = lo;
+        J[0] = 0;
+        T[0] = g.lo0;
         return 1;
     }
     if (s.strict || s.rounds >= kMaxNewtonRounds) {
-        T[0] = um;
+        J[0] = s.jl + ((s.jh - s.jl) >> 1);
+        T[0] = g.at(J[0]);
+        return 1;
+    }
+    if (s.endgame && s.single) {
+        // Step from the end the last evaluation moved towards the other,
+        // doubling the step, capped at half the bracket.
+        const int d = s.jh - s.jl;
+        const int step = max(min(s.stride, d >> 1), 1);
+        if (s.jl == s.jlast)
+            J[0] = s.jl + step;
+        else if (s.jh == s.jlast)
+            J[0] = s.jh - step;
+        else
+            J[0] = s.jl + (d >> 1);
+        s.stride *= 2;
+        s.jlast = J[0];
+        T[0] = g.at(J[0]);
         return 1;
     }
     if (s.endgame) {
-        // The unsettled midpoint and both midpoints that can follow it.
+        // The bracket's midpoint and quarter points: two halvings per round.
+        const int d = s.jh - s.jl;
+        const int m = s.jl + (d >> 1);
         int np = 0;
-        T[np++] = um;
-        const float m_inf = midpoint(s.cur.lo, um);   // if um is infeasible
-        const float m_feas = midpoint(um, s.cur.hi);  // if um is feasible
-        const float Tlo = s.A > 0.0f ? s.A : 0.0f;
-        if (m_inf > Tlo && m_inf < s.B && m_inf != um) T[np++] = m_inf;
-        if (m_feas > Tlo && m_feas < s.B && m_feas != um) T[np++] = m_feas;
+        J[np++] = m;
+        const int a = s.jl + (d >> 2);
+        const int b = m + ((s.jh - m) >> 1);
+        if (a > s.jl && a < m) J[np++] = a;
+        if (b > m && b < s.jh) J[np++] = b;
+#pragma unroll
+        for (int i = 0; i < kMaxPoints; ++i)
+            if (i < np) T[i] = g.at(J[i]);
         return np;
     }
     // Safeguarded Newton for log H = log bound in beta (plain Newton on H
-    // when the bound is not positive), kept inside the bracket in beta,
-    // (1/B, 1/A) or (1/B, 1/t_min) while no feasible point is known.
-    const float b_inf = rcp_approx(s.B);
-    const float b_feas = rcp_approx(s.A > 0.0f ? s.A : c.t_min);
+    // when the bound is not positive), kept inside the bracket in beta.
+    const float T_feas = s.jl_eval ? g.at(s.jl) : g.lo0;
+    const float b_inf = rcp_approx(g.at(s.jh));
+    const float b_feas = rcp_approx(T_feas);
     float bn;
     if (c.bound > 0.0f && s.Hc > 0.0f) {
-        const float g = lg2_approx(s.Hc) - lg2_approx(c.bound);   // log2 units
+        const float gl = lg2_approx(s.Hc) - lg2_approx(c.bound);  // log2 units
         const float gp = s.dHc * rcp_approx(s.Hc) * kLog2e;
-        bn = gp < 0.0f ? s.bc - g * rcp_approx(gp) : NAN;
+        bn = gp < 0.0f ? s.bc - gl * rcp_approx(gp) : NAN;
     } else {
         bn = s.dHc < 0.0f ? s.bc - (s.Hc - c.bound) * rcp_approx(s.dHc) : NAN;
     }
     if (!(bn > b_inf && bn < b_feas)) bn = sqrtf(b_inf * b_feas);
-    float Tn = rcp_approx(bn);
-    const float Tlo = s.A > 0.0f ? s.A : c.t_min;
-    if (!(Tn > Tlo && Tn < s.B)) {
-        // Rounding put the point on an end: take the bracket's midpoint.
-        Tn = midpoint(Tlo, s.B);
-        if (!(Tn > Tlo && Tn < s.B)) Tn = um;
-    }
+    const float Tn = rcp_approx(bn);
+    // The grid point at or just below Tn, strictly inside the bracket.
+    int jn = Tn > g.lo0 ? g.near(Tn) : 0;
+    jn = min(max(jn, s.jl + 1), s.jh - 1);
     int np = 0;
-    T[np++] = Tn;
-    if (!s.tmin_done && s.A == 0.0f && Tn <= 4.0f * c.t_min && Tn != c.t_min &&
-        c.t_min < s.B)
-        T[np++] = c.t_min;
+    const bool probe = !s.jl_eval && Tn <= 4.0f * g.lo0;  // t_min probe
+    if (s.single) {
+        J[0] = probe ? 0 : jn;
+        T[0] = g.at(J[0]);
+        s.jlast = J[0];
+        if (!probe && fabsf(bn - s.bc) <= 1e-3f * s.bc) s.endgame = true;
+        return 1;
+    }
+    J[np++] = jn;
+    if (probe) J[np++] = 0;
     if (np == 1 && fabsf(bn - s.bc) <= 1e-3f * s.bc) {
-        // Newton has converged: also evaluate the ends of the bisection path
-        // it predicts, so the next replay can settle every decision.
-        Cursor pred = s.cur;
-        float dummy;
-        advance(pred, c, s.A, s.B, true, Tn, &dummy);
-        s.pred = pred;
-        s.pred_valid = true;
-        if (pred.lo > s.A && pred.lo < s.B && pred.lo != Tn &&
-            pred.lo >= c.t_min)
-            T[np++] = pred.lo;
-        if (pred.hi > s.A && pred.hi < s.B && pred.hi != Tn && np < kMaxPoints)
-            T[np++] = pred.hi;
+        // Newton has converged: also evaluate the neighbours, which close
+        // the bracket when the crossing lies next to jn.
+        if (jn + 1 < s.jh) J[np++] = jn + 1;
+        if (jn - 1 > s.jl) J[np++] = jn - 1;
         s.endgame = true;
     }
+#pragma unroll
+    for (int i = 0; i < kMaxPoints; ++i)
+        if (i < np) T[i] = g.at(J[i]);
     return np;
 }
 
@@ -275,39 +275,50 @@ __device__ __forceinline__ bool newton_next(const Search& s) {
            s.rounds + 1 < kMaxNewtonRounds;
 }
 
-// Records the round's evaluations: T[i] at beta[i] = rcp_approx(T[i]) gave
-// the row sums S, V (arrays of length np) and, when has_w, W[0] at T[0].
+// Records the round's evaluations: grid point J[i] (temperature T[i], at
+// beta[i] = rcp_approx(T[i])) gave the row sums S[i], V[i], and, when
+// has_w, W[0].  Feasible points raise jl, then infeasible ones lower jh;
+// a point the bracket no longer contains is already decided and skipped,
+// so fp32 evaluations that disagree with monotonicity at the crossing
+// cannot invert the bracket.
 __device__ __forceinline__ void search_update(Search& s, const SearchCfg& c,
                                               int np,
-                                              const float (&T)[kMaxPoints],
+                                              const int (&J)[kMaxPoints],
                                               const float (&beta)[kMaxPoints],
-                                              const float* S, const float* V,
-                                              const float* W, bool has_w) {
+                                              const float (&S)[kMaxPoints],
+                                              const float (&V)[kMaxPoints],
+                                              const float (&W)[kMaxPoints],
+                                              bool has_w) {
+    bool inf[kMaxPoints];
+#pragma unroll
+    for (int i = 0; i < kMaxPoints; ++i)
+        inf[i] = i < np && entropy_above(make_float2(S[i], V[i]), beta[i],
+                                         c.bound_bits);
+    if (s.final_round) {
+        s.S_out = S[0];
+        s.overflow = inf[0];
+        s.done = true;
+        return;
+    }
 #pragma unroll
     for (int i = 0; i < kMaxPoints; ++i) {
-        if (i >= np) break;
-        const bool inf = entropy_above(make_float2(S[i], V[i]), beta[i],
-                                       c.bound_bits);
-        if (T[i] == c.t_min) {
-            s.tmin_done = true;
-            s.tmin_inf = inf;
-            s.S_tmin = S[i];
-        }
-        if (s.pred_valid && T[i] == s.pred.lo) s.S_plo = S[i];
-        if (inf) {
-            if (T[i] < s.B) s.B = T[i];
-        } else if (T[i] > s.A) {
-            s.A = T[i];
+        if (i >= np || inf[i]) continue;
+        const bool inside = J[i] > s.jl || (J[i] == 0 && !s.jl_eval);
+        if (inside && J[i] < s.jh) {
+            s.jl = J[i];
+            s.jl_eval = true;
             s.SA = S[i];
         }
     }
-    if (s.final_round) {
-        s.S_out = S[0];
-        s.overflow = s.final_check &&
-                     entropy_above(make_float2(S[0], V[0]), beta[0],
-                                   c.bound_bits);
-        s.done = true;
-        return;
+#pragma unroll
+    for (int i = 0; i < kMaxPoints; ++i) {
+        if (i >= np || !inf[i]) continue;
+        if (J[i] == 0 && !s.jl_eval) {
+            s.tmin_inf = true;
+            s.S_tmin = S[i];
+        } else if (J[i] > s.jl && J[i] < s.jh) {
+            s.jh = J[i];
+        }
     }
     // The Newton anchor moves to the round's first point (only used when
     // a Newton step follows, which is when W was accumulated).

@@ -331,6 +331,7 @@ __device__ __forceinline__ void eval_pass(const float4* row4, int q4,
 template <bool CLUSTER, int P, bool W0>
 __device__ __forceinline__ void search_round(Search& st, const SearchCfg& cfg,
                                              const float (&T)[kMaxPoints],
+                                             const int (&J)[kMaxPoints],
                                              const float4* row4, int q4,
                                              const Smem& sm, Exch& x) {
     float beta[kMaxPoints];
@@ -349,7 +350,7 @@ __device__ __forceinline__ void search_round(Search& st, const SearchCfg& cfg,
         W[p] = 0.0f;
     }
     if (W0) W[0] = a[2 % NV];
-    search_update(st, cfg, P, T, beta, S, V, W, W0);
+    search_update(st, cfg, P, J, beta, S, V, W, W0);
 }
 
 __device__ __forceinline__ void store_scalar_lanes(float* dst, int q, int pad,
@@ -444,7 +445,8 @@ cluster_kernel(RowTask t, int n, int slice_len) {
     const int len = static_cast<int>(max(static_cast<int64_t>(0),
                                          min(static_cast<int64_t>(slice_len), C - s0)));
     const SearchCfg cfg{t.t_min, t.hi0, t.entropy_bound,
-                        t.entropy_bound * kLog2e, t.max_iter};
+                        t.entropy_bound * kLog2e,
+                        make_grid(t.t_min, fmaxf(t.hi0, t.t_min), t.max_iter)};
     Exch x{warps, n, rank, 0u, 0u, t.wait_limit_cycles, false};
     bool reported = false;
 
@@ -533,29 +535,30 @@ cluster_kernel(RowTask t, int n, int slice_len) {
                 beta_out = 1.0f;
                 inv_s = 1.0f / s1[0];
             } else {
-                Search st = search_begin(cfg, s1[0], s1[1], s1[2], t.strict != 0);
+                Search st = search_begin(cfg, s1[0], s1[1], s1[2], t.strict != 0, false);
                 if (!(cfg.t_min < cfg.hi0)) {
                     // No interval to halve: T = t_min (section 5.4 check).
                     st.final_round = true;
-                    st.final_check = true;
                     st.T_out = cfg.t_min;
-                    float T1[kMaxPoints] = {cfg.t_min, 0.f, 0.f};
-                    search_round<CLUSTER, 1, false>(st, cfg, T1, row4, s.q4, sm, x);
+                    const float T1[kMaxPoints] = {cfg.t_min, 0.f, 0.f};
+                    const int J1[kMaxPoints] = {0, 0, 0};
+                    search_round<CLUSTER, 1, false>(st, cfg, T1, J1, row4, s.q4, sm, x);
                 }
                 while (!st.done) {
                     float T[kMaxPoints];
-                    const int np = search_plan(st, cfg, T);
+                    int J[kMaxPoints];
+                    const int np = search_plan(st, cfg, T, J);
                     const bool w0 = newton_next(st);
                     if (np == 1 && w0)
-                        search_round<CLUSTER, 1, true>(st, cfg, T, row4, s.q4, sm, x);
+                        search_round<CLUSTER, 1, true>(st, cfg, T, J, row4, s.q4, sm, x);
                     else if (np == 1)
-                        search_round<CLUSTER, 1, false>(st, cfg, T, row4, s.q4, sm, x);
+                        search_round<CLUSTER, 1, false>(st, cfg, T, J, row4, s.q4, sm, x);
                     else if (np == 2 && w0)
-                        search_round<CLUSTER, 2, true>(st, cfg, T, row4, s.q4, sm, x);
+                        search_round<CLUSTER, 2, true>(st, cfg, T, J, row4, s.q4, sm, x);
                     else if (np == 2)
-                        search_round<CLUSTER, 2, false>(st, cfg, T, row4, s.q4, sm, x);
+                        search_round<CLUSTER, 2, false>(st, cfg, T, J, row4, s.q4, sm, x);
                     else if (np == 3)
-                        search_round<CLUSTER, 3, false>(st, cfg, T, row4, s.q4, sm, x);
+                        search_round<CLUSTER, 3, false>(st, cfg, T, J, row4, s.q4, sm, x);
                 }
                 if (st.overflow) bits |= kBitOverflow;
                 T_row = st.T_out;

@@ -5,15 +5,16 @@
 //
 // Method: "BURT-IMMA CUDA Kernel API Reference", section 2.1
 // `constrained_softmax`, Description steps 1-4, with sections 5.3 and 5.4;
-// max once, y = (l - m) log2 e, then the bisection itself, one register
-// pass per midpoint giving S = sum 2^(beta y) and V = sum y 2^(beta y),
+// max once, y = (l - m) log2 e, then the bisection itself on the grid of
+// cs_search.cuh, one register pass per halving giving S = sum 2^(beta y)
+// and V = sum y 2^(beta y),
 // H = ln 2 (log2 S - beta V/S).  The per-step reduction is a butterfly over
 // the G lanes (all lanes end with bit-identical sums, so they take the same
 // decision); H > bound is decided without a division as
 // S (log2 S - bound log2 e) - beta V > 0, with log2 on the MUFU lg2 unit.
 #include <math.h>
 
-#include "cs_device.cuh"
+#include "cs_search.cuh"
 
 namespace cs {
 namespace {
@@ -61,6 +62,8 @@ rowgroup_kernel(RowTask t, int vec) {
     const int C = t.num_classes;
     const int Q = (C + 3) >> 2;  // float4 slots per row
     const float bound_bits = t.entropy_bound * kLog2e;
+    const SearchCfg cfg{t.t_min, t.hi0, t.entropy_bound, bound_bits,
+                        make_grid(t.t_min, fmaxf(t.hi0, t.t_min), t.max_iter)};
     const int64_t groups_per_grid =
         (static_cast<int64_t>(gridDim.x) * blockDim.x) / G;
 
@@ -140,33 +143,31 @@ rowgroup_kernel(RowTask t, int vec) {
                 beta_out = 1.0f;
                 inv_s = 1.0f / sv.x;
             } else {
-                // One evaluation per midpoint: for rows this narrow a pass
-                // costs less than the bookkeeping that settling midpoints
-                // without evaluation would need.
-                float lo = t.t_min, hi = t.hi0;
-                bool lo_eval = false;
-                bool hi_eval = hi == 1.0f;   // H(1) > bound is known
+                // The bisection on the grid of cs_search.cuh, one evaluation
+                // per halving: for rows this narrow a pass costs less than
+                // the bookkeeping (and the divergence between the rows of a
+                // warp) that settling halvings without evaluation needs.
+                const Grid& g = cfg.g;
+                int jl = 0, jh = g.top;
+                bool jl_eval = false;
                 float s_lo = 0.0f;
-                if (lo < hi) {
-                    for (int k = 0; k < t.max_iter; ++k) {
-                        const float mid = 0.5f * (lo + hi);
-                        // Exact early exit: the fp32 midpoint repeats an
-                        // end already decided, and so would every later one.
-                        if ((mid == lo && lo_eval) || (mid == hi && hi_eval)) break;
-                        const float b = rcp_approx(mid);
+                if (cfg.t_min < cfg.hi0) {
+                    while (jh - jl > 1) {
+                        const int jm = jl + ((jh - jl) >> 1);
+                        const float b = rcp_approx(g.at(jm));
                         sv = group_sum2<G>(reg_pass<E4>(y, b), gmask);
                         if (entropy_above(sv, b, bound_bits)) {
-                            hi = mid;
-                            hi_eval = true;
+                            jh = jm;
                         } else {
-                            lo = mid;
-                            lo_eval = true;
+                            jl = jm;
+                            jl_eval = true;
                             s_lo = sv.x;
                         }
                     }
                 }
+                const float lo = jl_eval ? g.at(jl) : t.t_min;
                 const float b_lo = rcp_approx(lo);
-                if (!lo_eval) {
+                if (!jl_eval) {
                     // lo is still t_min: evaluate it (section 5.4 check).
                     sv = group_sum2<G>(reg_pass<E4>(y, b_lo), gmask);
                     s_lo = sv.x;

@@ -13,20 +13,22 @@
  *   3. otherwise bisect T on [t_min, min(1, t_max)] for exactly max_iter
  *      steps: mid = (lo + hi) / 2; H(mid) > entropy_bound moves hi to mid,
  *      otherwise lo moves to mid.  Temperatures above 1 are never searched
- *      because H is nondecreasing in T (section 2.1 step 4).  By default
- *      the cluster kernel evaluates H only where needed: a midpoint at or
- *      below an evaluated feasible temperature is feasible, and one at or
- *      above an evaluated infeasible temperature is infeasible, so once
- *      safeguarded Newton steps have bracketed the crossing tightly every
- *      decision of the bisection is known (cs_options.strict evaluates each
- *      midpoint).  The row-group kernel, whose rows are a few registers
- *      per lane, evaluates every midpoint;
+ *      because H is nondecreasing in T (section 2.1 step 4).  The
+ *      midpoints are the exact dyadic points t_min + j (hi0 - t_min) / 2^K
+ *      (K = max_iter) rounded once to fp32; for max_iter > 24, where fp32
+ *      cannot resolve those points, every fp32 value of the interval.
+ *      Since H is monotone the result is the largest such point whose H is
+ *      within the bound (t_min if none).  By default the cluster kernel
+ *      finds it from a bracket of grid points closed by safeguarded Newton
+ *      steps, evaluating H only where needed (cs_options.strict halves the
+ *      bracket one evaluation at a time, i.e. bisects).  The row-group
+ *      kernel, whose rows are a few registers per lane, bisects;
  *   4. write softmax(l / lo) and report T = lo.  If even lo = t_min violates
  *      the bound, the row still gets softmax(l / t_min), the lowest entropy
  *      reachable (section 5.4), and ENTROPY_OVERFLOW is raised.
  *
  * Arithmetic is fp32 with the exponential on the hardware ex2 unit; the
- * bookkeeping of lo, hi and mid is fp32 as well.
+ * grid points are indexed by integers and evaluated in fp32.
  *
  * All functions are thread-safe.  No function allocates device memory per
  * call; the library's only device object is one 32-bit error word per GPU.
@@ -72,12 +74,12 @@ typedef struct cs_options {
                           cluster: CTAs per row (1..16); 0 = automatic      */
     int32_t threads;   /* cluster: threads per CTA (multiple of 32,
                           64..512); 0 = automatic                           */
-    int32_t strict;    /* cluster: 1 = evaluate H at every bisection
-                          midpoint, one pass per step; 0 = settle the
-                          midpoints outside an evaluated bracket by
-                          monotonicity (same result, fewer passes).  The
-                          row-group kernel always evaluates every midpoint;
-                          0 or 1 is accepted there                          */
+    int32_t strict;    /* cluster: 1 = bisect (H evaluated at every
+                          midpoint, one pass per halving); 0 = close the
+                          bracket from Newton-placed evaluations (same
+                          result for monotone H, fewer passes).  The
+                          row-group kernel always bisects; 0 or 1 is
+                          accepted there                                    */
 } cs_options;
 
 /* What a launch of the given shape uses.  Filled by cs_plan_launch /

@@ -123,8 +123,8 @@ def test_sweep_sampled(bound, iters, param, threads):
                                        ("moe_router_65536x64", 4096),
                                        ("sweep_4096x32000", 256)])
 def test_settled_search_matches_strict_bisection(name, rows):
-    """The default search (midpoints outside an evaluated bracket settled by
-    monotonicity) returns the temperature of the strict search (H evaluated
+    """The default search (a bracket of grid points closed by Newton-placed
+    evaluations) returns the temperature of the strict search (H evaluated
     at every midpoint) on every row, up to fp32 ties at the crossing, which
     the oracle then arbitrates."""
     w = wl.WORKLOADS[name]
