@@ -24,7 +24,9 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int kProbeThreads = 512;
 constexpr int kProbeBlocksPerSm = 4;
-constexpr int kRowgroupThreads = 256;
+// Row-group CTAs of two warps: the block scheduler refills SMs at a fine
+// grain, which shortens the launch's tail (rows end at different rounds).
+constexpr int kRowgroupThreads = 64;
 constexpr int kRowgroupMaxLanes = 32;
 constexpr int kRowgroupMaxE4 = 8;      // 32 classes per lane
 constexpr int kAutoRowgroupE4 = 4;     // 16 classes per lane
@@ -131,7 +133,10 @@ cs_status plan_rowgroup(int64_t batch, int32_t C, int32_t param,
     p->lanes_per_row = G;
     p->elems_per_lane = 4 * e4;
     p->threads_per_cta = kRowgroupThreads;
-    p->ctas_per_sm = 2048 / kRowgroupThreads;
+    // Registers bound residency: at most 64 per thread (80 for 32 classes
+    // per lane) out of 65536 per SM.
+    p->ctas_per_sm = 65536 / ((e4 >= 8 ? 80 : 64) * kRowgroupThreads);
+    if (p->ctas_per_sm > 32) p->ctas_per_sm = 32;
     int64_t blocks = ceil_div(batch * G, kRowgroupThreads);
     if (blocks > kMaxGridX) blocks = kMaxGridX;
     p->grid_ctas = blocks;

@@ -52,8 +52,54 @@ __device__ __forceinline__ float2 reg_pass(const float4 (&y)[E4], float beta) {
     return acc.total();
 }
 
+template <int G>
+__device__ __forceinline__ float3 group_sum3(float3 v, unsigned mask) {
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) {
+        v.x += __shfl_xor_sync(mask, v.x, o);
+        v.y += __shfl_xor_sync(mask, v.y, o);
+        v.z += __shfl_xor_sync(mask, v.z, o);
+    }
+    return v;
+}
+
+// (S, V, W) of this lane's classes at inverse temperature beta, with
+// W = sum y^2 2^(beta y) for the Newton slope.  S and V take exactly the
+// arithmetic of reg_pass, so a grid point gets the same decision whichever
+// pass evaluates it.
+template <int E4>
+__device__ __forceinline__ float3 reg_pass3(const float4 (&y)[E4], float beta) {
+    SV4 acc;
+    acc.zero();
+    float2 w = make_float2(0.f, 0.f);
+    const float2 b2 = make_float2(beta, beta);
+#pragma unroll
+    for (int i = 0; i < E4; ++i) {
+        const float2 y01 = make_float2(y[i].x, y[i].y);
+        const float2 y23 = make_float2(y[i].z, y[i].w);
+        const float2 x01 = mul2(y01, b2);
+        const float2 x23 = mul2(y23, b2);
+        const float2 e01 = make_float2(ex2(x01.x), ex2(x01.y));
+        const float2 e23 = make_float2(ex2(x23.x), ex2(x23.y));
+        acc.s01 = add2(acc.s01, e01);
+        acc.s23 = add2(acc.s23, e23);
+        acc.v01 = fma2(e01, y01, acc.v01);
+        acc.v23 = fma2(e23, y23, acc.v23);
+        w = fma2(mul2(e01, y01), y01, w);
+        w = fma2(mul2(e23, y23), y23, w);
+    }
+    const float2 sv = acc.total();
+    return make_float3(sv.x, sv.y, w.x + w.y);
+}
+
+// Rounds of Newton steps every searching row takes before the fallback.
+constexpr int kRowNewtonRounds = 5;
+
+// At most 64 registers a thread (32 warps per SM, which the latency of each
+// row's dependent reduce-and-decide chain needs), or 80 when a lane holds
+// 32 classes.
 template <int G, int E4>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(64, E4 >= 8 ? 12 : 16)
 rowgroup_kernel(RowTask t, int vec) {
     const int lane = threadIdx.x & 31;
     const int sub = lane & (G - 1);
@@ -137,21 +183,20 @@ rowgroup_kernel(RowTask t, int vec) {
                 y[i].z = fmaxf((y[i].z - m) * kLog2e, kYFloor);
                 y[i].w = fmaxf((y[i].w - m) * kLog2e, kYFloor);
             }
-            float2 sv = group_sum2<G>(reg_pass<E4>(y, 1.0f), gmask);
+            const float3 r1 = group_sum3<G>(reg_pass3<E4>(y, 1.0f), gmask);
+            float2 sv = make_float2(r1.x, r1.y);
             if (!entropy_above(sv, 1.0f, bound_bits)) {
                 T_row = 1.0f;
                 beta_out = 1.0f;
                 inv_s = 1.0f / sv.x;
             } else {
-                // The bisection on the grid of cs_search.cuh, one evaluation
-                // per halving: for rows this narrow a pass costs less than
-                // the bookkeeping (and the divergence between the rows of a
-                // warp) that settling halvings without evaluation needs.
                 const Grid& g = cfg.g;
                 int jl = 0, jh = g.top;
-                bool jl_eval = false;
+                bool jl_eval = false;   // G(jl) evaluated feasible
+                bool tmin_inf = false;  // t_min evaluated infeasible
                 float s_lo = 0.0f;
-                if (cfg.t_min < cfg.hi0) {
+                if (cfg.t_min < cfg.hi0 && t.strict) {
+                    // Strict: the bisection, one evaluation per halving.
                     while (jh - jl > 1) {
                         const int jm = jl + ((jh - jl) >> 1);
                         const float b = rcp_approx(g.at(jm));
@@ -164,10 +209,91 @@ rowgroup_kernel(RowTask t, int vec) {
                             s_lo = sv.x;
                         }
                     }
+                } else if (cfg.t_min < cfg.hi0) {
+                    // The bracket search of cs_search.cuh in a lean form
+                    // for rows this narrow: every searching row takes the
+                    // same rounds of one grid point each, so the rows of a
+                    // warp stay together.  Up to kRowNewtonRounds Newton
+                    // steps on log H(beta) from the last point evaluated,
+                    // kept inside the bracket (b_inf, b_feas) in beta and
+                    // placed on the grid point at or below; t_min when the
+                    // step comes within 4 t_min of it.  Then, only if the
+                    // bracket is still open, one point per round stepping
+                    // from the end moved last with doubling strides.
+                    float b = 1.0f, S = r1.x, V = r1.y, W = r1.z;
+                    float b_inf = rcp_approx(cfg.hi0);
+                    float b_feas = rcp_approx(cfg.t_min);
+                    const float lg2_bound = lg2_approx(t.entropy_bound);
+                    const bool log_newton = t.entropy_bound > 0.0f;
+                    int jlast = -1;
+                    for (int k = 0; k < kRowNewtonRounds && jh - jl > 1 && !tmin_inf; ++k) {
+                        const float is = rcp_approx(S);
+                        const float ey = V * is;
+                        const float H = kLn2 * (lg2_approx(S) - b * ey);
+                        const float dH = -b * (kLn2 * kLn2) * fmaxf(fmaf(W, is, -ey * ey), 0.0f);
+                        float bn;
+                        if (log_newton && H > 0.0f) {
+                            const float gl = lg2_approx(H) - lg2_bound;
+                            const float gp = dH * rcp_approx(H) * kLog2e;
+                            bn = b - gl * rcp_approx(gp);
+                        } else {
+                            bn = b - (H - t.entropy_bound) * rcp_approx(dH);
+                        }
+                        if (!(bn > b_inf && bn < b_feas)) bn = sqrtf(b_inf * b_feas);
+                        const float Tn = rcp_approx(bn);
+                        const bool probe = !jl_eval && Tn <= 4.0f * cfg.t_min;
+                        int jn = Tn > cfg.t_min ? g.near(Tn) : 0;
+                        jn = probe ? 0 : min(max(jn, jl + 1), jh - 1);
+                        b = rcp_approx(probe ? cfg.t_min : g.at(jn));
+                        const float3 r = group_sum3<G>(reg_pass3<E4>(y, b), gmask);
+                        S = r.x;
+                        V = r.y;
+                        W = r.z;
+                        const bool inf = entropy_above(make_float2(S, V), b, bound_bits);
+                        jlast = jn;
+                        if (probe) {
+                            if (inf) {
+                                tmin_inf = true;
+                                s_lo = S;
+                            } else {
+                                jl_eval = true;
+                                s_lo = S;
+                                b_feas = b;
+                            }
+                        } else if (inf) {
+                            jh = jn;
+                            b_inf = b;
+                        } else {
+                            jl = jn;
+                            jl_eval = true;
+                            s_lo = S;
+                            b_feas = b;
+                        }
+                    }
+                    int stride = 1;
+                    while (jh - jl > 1 && !tmin_inf) {
+                        const int d = jh - jl;
+                        const int step = max(min(stride, d >> 1), 1);
+                        const int jm = jl == jlast ? jl + step
+                                     : jh == jlast ? jh - step : jl + (d >> 1);
+                        stride *= 2;
+                        jlast = jm;
+                        const float bm = rcp_approx(g.at(jm));
+                        sv = group_sum2<G>(reg_pass<E4>(y, bm), gmask);
+                        if (entropy_above(sv, bm, bound_bits)) {
+                            jh = jm;
+                        } else {
+                            jl = jm;
+                            jl_eval = true;
+                            s_lo = sv.x;
+                        }
+                    }
                 }
                 const float lo = jl_eval ? g.at(jl) : t.t_min;
                 const float b_lo = rcp_approx(lo);
-                if (!jl_eval) {
+                if (tmin_inf) {
+                    bits |= kBitOverflow;
+                } else if (!jl_eval) {
                     // lo is still t_min: evaluate it (section 5.4 check).
                     sv = group_sum2<G>(reg_pass<E4>(y, b_lo), gmask);
                     s_lo = sv.x;
@@ -233,7 +359,7 @@ cudaError_t launch_g(const RowTask& t, int e4, int vec, dim3 grid, dim3 block,
 
 }  // namespace
 
-constexpr int kRowgroupThreads = 256;
+constexpr int kRowgroupThreads = 64;  // as the planner in cs_api.cu
 constexpr int64_t kMaxGridX = 2147483647;
 
 cudaError_t launch_rowgroup(const RowTask& t, int lanes_per_row,
