@@ -99,6 +99,7 @@ struct SearchCfg {
     float hi0;          // min(1, t_max)
     float bound;        // nats
     float bound_bits;   // bound * log2 e
+    float lg2_bound;    // log2(bound) when bound > 0
     Grid g;
 };
 
@@ -116,19 +117,22 @@ struct Search {
     int stride;         // single: the next neighbour step
     float SA;           // S at G(jl) when jl_eval
     float S_tmin;       // S at t_min when tmin_inf
+    float b_jl, b_jh;   // beta of the bracket's ends (t_min while !jl_eval)
     float bc, Hc, dHc;  // Newton anchor: beta, H (nats), dH/dbeta
     int rounds;
     float T_out, S_out;
     bool overflow;      // section 5.4: even t_min violates the bound
 };
 
-__device__ __forceinline__ float entropy_nats(float S, float V, float beta) {
-    return kLn2 * (lg2_approx(S) - beta * V * rcp_approx(S));
+// H (nats) and dH/dbeta at beta from the sums, given ls = log2 S and
+// is = 1 / S.
+__device__ __forceinline__ float entropy_nats(float ls, float is, float V,
+                                              float beta) {
+    return kLn2 * (ls - beta * V * is);
 }
 
-__device__ __forceinline__ float entropy_slope(float S, float V, float W,
+__device__ __forceinline__ float entropy_slope(float is, float V, float W,
                                                float beta) {
-    const float is = rcp_approx(S);
     const float ey = V * is;
     return -beta * (kLn2 * kLn2) * fmaxf(W * is - ey * ey, 0.0f);
 }
@@ -152,9 +156,12 @@ __device__ __forceinline__ Search search_begin(const SearchCfg& c, float S1,
     s.stride = 1;
     s.SA = 0.0f;
     s.S_tmin = 0.0f;
+    s.b_jl = rcp_approx(c.t_min);
+    s.b_jh = rcp_approx(c.hi0);
+    const float is = rcp_approx(S1);
     s.bc = 1.0f;
-    s.Hc = entropy_nats(S1, V1, 1.0f);
-    s.dHc = entropy_slope(S1, V1, W1, 1.0f);
+    s.Hc = entropy_nats(lg2_approx(S1), is, V1, 1.0f);
+    s.dHc = entropy_slope(is, V1, W1, 1.0f);
     s.rounds = 0;
     s.T_out = 0.0f;
     s.S_out = 0.0f;
@@ -228,14 +235,14 @@ __device__ __forceinline__ int search_plan(Search& s, const SearchCfg& c,
     }
     // Safeguarded Newton for log H = log bound in beta (plain Newton on H
     // when the bound is not positive), kept inside the bracket in beta.
-    const float T_feas = s.jl_eval ? g.at(s.jl) : g.lo0;
-    const float b_inf = rcp_approx(g.at(s.jh));
-    const float b_feas = rcp_approx(T_feas);
+    const float b_inf = s.b_jh;
+    const float b_feas = s.b_jl;
     float bn;
     if (c.bound > 0.0f && s.Hc > 0.0f) {
-        const float gl = lg2_approx(s.Hc) - lg2_approx(c.bound);  // log2 units
-        const float gp = s.dHc * rcp_approx(s.Hc) * kLog2e;
-        bn = gp < 0.0f ? s.bc - gl * rcp_approx(gp) : NAN;
+        // log2 H - log2 bound over its slope, in one reciprocal:
+        // bn = bc - (lg2 H - lg2 bound) H / (dH log2 e).
+        const float gl = lg2_approx(s.Hc) - c.lg2_bound;  // log2 units
+        bn = s.dHc < 0.0f ? s.bc - gl * s.Hc * rcp_approx(s.dHc * kLog2e) : NAN;
     } else {
         bn = s.dHc < 0.0f ? s.bc - (s.Hc - c.bound) * rcp_approx(s.dHc) : NAN;
     }
@@ -308,6 +315,7 @@ __device__ __forceinline__ void search_update(Search& s, const SearchCfg& c,
             s.jl = J[i];
             s.jl_eval = true;
             s.SA = S[i];
+            s.b_jl = beta[i];
         }
     }
 #pragma unroll
@@ -318,14 +326,16 @@ __device__ __forceinline__ void search_update(Search& s, const SearchCfg& c,
             s.S_tmin = S[i];
         } else if (J[i] > s.jl && J[i] < s.jh) {
             s.jh = J[i];
+            s.b_jh = beta[i];
         }
     }
     // The Newton anchor moves to the round's first point (only used when
     // a Newton step follows, which is when W was accumulated).
     if (has_w) {
+        const float is = rcp_approx(S[0]);
         s.bc = beta[0];
-        s.Hc = entropy_nats(S[0], V[0], beta[0]);
-        s.dHc = entropy_slope(S[0], V[0], W[0], beta[0]);
+        s.Hc = entropy_nats(lg2_approx(S[0]), is, V[0], beta[0]);
+        s.dHc = entropy_slope(is, V[0], W[0], beta[0]);
     }
     ++s.rounds;
 }

@@ -7,11 +7,14 @@
 // sections 5.3 and 5.4.  Per row:
 //   stage   every thread loads its part of the slice with 128-bit loads
 //           (eight in flight per thread), stores it to shared memory and
-//           folds it into m = max_i l_i (T-independent, computed once) and
-//           a finiteness check, which are exchanged across the cluster;
-//   T = 1   one pass turns the slice into y_i = (l_i - m) log2(e) in place
-//           and sums S = sum 2^y_i, V = sum y_i 2^y_i, W = sum y_i^2 2^y_i;
-//           H(1) = ln2 (log2 S - V/S) decides whether a search is needed;
+//           folds it into its own max m_t and a finiteness check;
+//   T = 1   one pass turns the thread's classes into y_i = (l_i - m_t)
+//           log2(e) in place and sums S = sum 2^y_i, V = sum y_i 2^y_i,
+//           W = sum y_i^2 2^y_i; a single reduction then forms the row's max
+//           m = max_i l_i (T-independent, computed once) and S, V, W
+//           rescaled to it, and H(1) = ln2 (log2 S - V/S) decides whether a
+//           search is needed.  Each thread keeps its offset d = (m_t - m)
+//           log2 e and every later pass uses beta (y + d);
 //   search  rounds of the temperature search of cs_search.cuh: each round
 //           evaluates (S, V) at 1-3 temperatures in one pass over the slice
 //           (plus W at the first one when a Newton step follows) and
@@ -98,17 +101,70 @@ struct Exch {
     bool dead;
 };
 
+// Reduction operators.  combine(a, b) must give the same bits as
+// combine(b, a), so that both lanes of every shuffle-tree exchange agree and
+// every lane ends with the same result.
+struct OpSum {
+    template <int NV>
+    static __device__ __forceinline__ void identity(float (&a)[NV]) {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) a[i] = 0.0f;
+    }
+    template <int NV>
+    static __device__ __forceinline__ void combine(float (&a)[NV],
+                                                   const float (&b)[NV]) {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) a[i] = a[i] + b[i];
+    }
+};
+
+// Partial softmax statistics of a set of classes: {m, S, V, W, code} with
+// m the set's max, y = (l - m) log2 e, S = sum 2^y, V = sum y 2^y,
+// W = sum y^2 2^y, and code the set's NaN/Inf code.  Combining rescales
+// both sides to the larger max: with d = (m_i - m) log2 e <= 0, a side
+// contributes 2^d S_i, 2^d (V_i + d S_i) and 2^d (W_i + 2 d V_i + d^2 S_i).
+// An empty side (S = 0) contributes nothing.  Explicit roundings keep the
+// compiler from contracting the two sides differently.
+struct OpSoftmax {
+    static __device__ __forceinline__ void identity(float (&a)[5]) {
+        a[0] = -INFINITY;
+        a[1] = a[2] = a[3] = a[4] = 0.0f;
+    }
+    static __device__ __forceinline__ void side(const float (&a)[5], float m,
+                                                float& tS, float& tV,
+                                                float& tW) {
+        const float d = __fmul_rn(__fsub_rn(a[0], m), kLog2e);
+        const float f = ex2(d);
+        const bool live = a[1] > 0.0f;
+        tS = live ? __fmul_rn(f, a[1]) : 0.0f;
+        tV = live ? __fmul_rn(f, __fmaf_rn(d, a[1], a[2])) : 0.0f;
+        tW = live ? __fmul_rn(f, __fmaf_rn(d, __fmaf_rn(d, a[1], __fmul_rn(2.0f, a[2])), a[3]))
+                  : 0.0f;
+    }
+    static __device__ __forceinline__ void combine(float (&a)[5],
+                                                   const float (&b)[5]) {
+        const float m = fmaxf(a[0], b[0]);
+        float aS, aV, aW, bS, bV, bW;
+        side(a, m, aS, aV, aW);
+        side(b, m, bS, bV, bW);
+        a[0] = m;
+        a[1] = __fadd_rn(aS, bS);
+        a[2] = __fadd_rn(aV, bV);
+        a[3] = __fadd_rn(aW, bW);
+        a[4] = fmaxf(a[4], b[4]);
+    }
+};
+
 // Shuffle-tree all-reduce over the warp; every lane ends with the same
 // (bit-identical) values.
-template <int NV, bool IS_MAX>
+template <class Op, int NV>
 __device__ __forceinline__ void warp_reduce(float (&a)[NV]) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
+        float b[NV];
 #pragma unroll
-        for (int i = 0; i < NV; ++i) {
-            const float b = __shfl_xor_sync(0xffffffffu, a[i], o);
-            a[i] = IS_MAX ? fmaxf(a[i], b) : a[i] + b;
-        }
+        for (int i = 0; i < NV; ++i) b[i] = __shfl_xor_sync(0xffffffffu, a[i], o);
+        Op::combine(a, b);
     }
 }
 
@@ -116,7 +172,7 @@ __device__ __forceinline__ void warp_reduce(float (&a)[NV]) {
 // every CTA; the waiting threads wait for the cluster's pushes and replace
 // a with the combination over ranks, in rank order.  Every thread of the
 // CTA calls it (keeping the exchange count); only waiters wait and combine.
-template <int NV, bool IS_MAX>
+template <class Op, int NV>
 __device__ __forceinline__ void cluster_leg(float (&a)[NV], const Smem& sm,
                                             Exch& x, bool waiter) {
     constexpr int NE = NV + (NV & 1);   // pushed as pairs
@@ -145,24 +201,23 @@ __device__ __forceinline__ void cluster_leg(float (&a)[NV], const Smem& sm,
 #pragma unroll
         for (int i = 0; i < NV; ++i) a[i] = cs[i];
         for (int r = 1; r < x.n; ++r) {
+            float b[NV];
 #pragma unroll
-            for (int i = 0; i < NV; ++i) {
-                const float b = cs[r * kSlotVals + i];
-                a[i] = IS_MAX ? fmaxf(a[i], b) : a[i] + b;
-            }
+            for (int i = 0; i < NV; ++i) b[i] = cs[r * kSlotVals + i];
+            Op::combine(a, b);
         }
     }
 }
 
-// Sum (or max) over every thread of the CTA and the cluster of each thread's
-// a[0..NV); returns the same bits in every thread of the cluster.
-template <bool CLUSTER, int NV, bool IS_MAX>
+// Reduction (Op) over every thread of the CTA and the cluster of each
+// thread's a[0..NV); returns the same bits in every thread of the cluster.
+template <bool CLUSTER, class Op, int NV>
 __device__ __forceinline__ void exchange(float (&a)[NV], const Smem& sm,
                                          Exch& x) {
     static_assert(NV <= kSlotVals, "payload");
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    warp_reduce<NV, IS_MAX>(a);
+    warp_reduce<Op, NV>(a);
     float* ws = sm.wslot + (x.lk & 1u) * x.warps * kSlotVals;
     ++x.lk;
     if (lane == 0) {
@@ -177,21 +232,22 @@ __device__ __forceinline__ void exchange(float (&a)[NV], const Smem& sm,
     if (warp == 0) {
         // Lane groups of w2 >= warps lanes (a power of two) each hold every
         // warp's slot and reduce it with a log2(w2)-level shuffle tree.
-        const float idn = IS_MAX ? -INFINITY : 0.0f;
         const int w2 = x.warps <= 4 ? 4 : (x.warps <= 8 ? 8 : 16);
         const int sl = lane & (w2 - 1);
+        if (sl < x.warps) {
 #pragma unroll
-        for (int i = 0; i < NV; ++i)
-            a[i] = sl < x.warps ? ws[sl * kSlotVals + i] : idn;
+            for (int i = 0; i < NV; ++i) a[i] = ws[sl * kSlotVals + i];
+        } else {
+            Op::identity(a);
+        }
         for (int o = w2 >> 1; o > 0; o >>= 1) {
+            float b[NV];
 #pragma unroll
-            for (int i = 0; i < NV; ++i) {
-                const float b = __shfl_xor_sync(0xffffffffu, a[i], o);
-                a[i] = IS_MAX ? fmaxf(a[i], b) : a[i] + b;
-            }
+            for (int i = 0; i < NV; ++i) b[i] = __shfl_xor_sync(0xffffffffu, a[i], o);
+            Op::combine(a, b);
         }
     }
-    if (CLUSTER) cluster_leg<NV, IS_MAX>(a, sm, x, warp == 0);
+    if (CLUSTER) cluster_leg<Op, NV>(a, sm, x, warp == 0);
     if (warp == 0 && lane == 0) {
 #pragma unroll
         for (int i = 0; i < NV; ++i) sm.bcast[i] = a[i];
@@ -213,11 +269,16 @@ struct Acc {
     __device__ __forceinline__ void zero() {
         s = v = w = make_float2(0.f, 0.f);
     }
-    __device__ __forceinline__ void add(float4 y, float2 b2) {
+    // Adds the four classes of y at inverse temperature beta, b2 = {beta,
+    // beta}, with x = beta (y + d) computed as fma(y, beta, bd2), bd2 =
+    // {beta d, beta d}: y is stored relative to this thread's max, d is
+    // that max's offset from the row's (V and W are kept relative to the
+    // thread's max; thread_to_row() moves them).
+    __device__ __forceinline__ void add(float4 y, float2 b2, float2 bd2) {
         const float2 y01 = make_float2(y.x, y.y);
         const float2 y23 = make_float2(y.z, y.w);
-        const float2 x01 = mul2(y01, b2);
-        const float2 x23 = mul2(y23, b2);
+        const float2 x01 = fma2(y01, b2, bd2);
+        const float2 x23 = fma2(y23, b2, bd2);
         const float2 e01 = make_float2(ex2(x01.x), ex2(x01.y));
         const float2 e23 = make_float2(ex2(x23.x), ex2(x23.y));
         s = add2(s, add2(e01, e23));
@@ -234,18 +295,28 @@ struct Acc {
     }
 };
 
-// T = 1 pass: rewrites this thread's float4s of the slice as
-// y = max((l - m) log2 e, floor) and returns the partial S, V, W at beta = 1.
-__device__ __forceinline__ void transform_pass(float4* row4, int q4, float m,
-                                               float (&out)[3]) {
+// V and W relative to this thread's max moved to the row's: y + d for y.
+__device__ __forceinline__ void thread_to_row(float S, float& V, float* W,
+                                              float d) {
+    if (W) *W = fmaf(d, fmaf(d, S, 2.0f * V), *W);
+    V = fmaf(d, S, V);
+}
+
+// T = 1 pass over this thread's float4s of the slice (q = t, t + nt, ...,
+// the float4s it staged): rewrites them as y = max((l - m_t) log2 e, floor)
+// with m_t this thread's max, and returns {m_t, S, V, W, code} relative to
+// m_t for the softmax reduction.
+__device__ __forceinline__ void transform_pass(float4* row4, int q4, float m_t,
+                                               float code, float (&out)[5]) {
     Acc<true> acc;
     acc.zero();
     const float2 one = make_float2(1.0f, 1.0f);
-    auto to_y = [m](float4 l) {
-        return make_float4(fmaxf((l.x - m) * kLog2e, kYFloor),
-                           fmaxf((l.y - m) * kLog2e, kYFloor),
-                           fmaxf((l.z - m) * kLog2e, kYFloor),
-                           fmaxf((l.w - m) * kLog2e, kYFloor));
+    const float2 zero = make_float2(0.0f, 0.0f);
+    auto to_y = [m_t](float4 l) {
+        return make_float4(fmaxf((l.x - m_t) * kLog2e, kYFloor),
+                           fmaxf((l.y - m_t) * kLog2e, kYFloor),
+                           fmaxf((l.z - m_t) * kLog2e, kYFloor),
+                           fmaxf((l.w - m_t) * kLog2e, kYFloor));
     };
     // Four float4s per trip (independent chains), then the rest one by one.
     const int nt = blockDim.x;
@@ -257,17 +328,19 @@ __device__ __forceinline__ void transform_pass(float4* row4, int q4, float m,
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             row4[q + i * nt] = y[i];
-            acc.add(y[i], one);
+            acc.add(y[i], one, zero);
         }
     }
     for (; q < q4; q += nt) {
         const float4 y = to_y(row4[q]);
         row4[q] = y;
-        acc.add(y, one);
+        acc.add(y, one, zero);
     }
-    out[0] = acc.s.x + acc.s.y;
-    out[1] = acc.v.x + acc.v.y;
-    out[2] = acc.w.x + acc.w.y;
+    out[0] = m_t;
+    out[1] = acc.s.x + acc.s.y;
+    out[2] = acc.v.x + acc.v.y;
+    out[3] = acc.w.x + acc.w.y;
+    out[4] = code;
 }
 
 // Number of partial sums a pass at P temperatures produces: S and V per
@@ -287,15 +360,17 @@ struct PassOut {
 template <int P, bool W0>
 __device__ __forceinline__ void eval_pass(const float4* row4, int q4,
                                           const float (&beta)[kMaxPoints],
+                                          float d,
                                           float (&out)[PassOut<P, W0>::kN]) {
     Acc<W0> a0;
     Acc<false> ap[P > 1 ? P - 1 : 1];
-    float2 b2[P];
+    float2 b2[P], bd2[P];
     a0.zero();
 #pragma unroll
     for (int p = 0; p < P; ++p) {
         if (p > 0) ap[p - 1].zero();
         b2[p] = make_float2(beta[p], beta[p]);
+        bd2[p] = make_float2(beta[p] * d, beta[p] * d);
     }
     const int nt = blockDim.x;
     int q = threadIdx.x;
@@ -305,42 +380,52 @@ __device__ __forceinline__ void eval_pass(const float4* row4, int q4,
         for (int i = 0; i < 4; ++i) y[i] = row4[q + i * nt];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            a0.add(y[i], b2[0]);
+            a0.add(y[i], b2[0], bd2[0]);
 #pragma unroll
-            for (int p = 1; p < P; ++p) ap[p - 1].add(y[i], b2[p]);
+            for (int p = 1; p < P; ++p) ap[p - 1].add(y[i], b2[p], bd2[p]);
         }
     }
     for (; q < q4; q += nt) {
         const float4 ya = row4[q];
-        a0.add(ya, b2[0]);
+        a0.add(ya, b2[0], bd2[0]);
 #pragma unroll
-        for (int p = 1; p < P; ++p) ap[p - 1].add(ya, b2[p]);
+        for (int p = 1; p < P; ++p) ap[p - 1].add(ya, b2[p], bd2[p]);
     }
-    out[0] = a0.s.x + a0.s.y;
-    out[1] = a0.v.x + a0.v.y;
-    if (W0) out[2 % PassOut<P, W0>::kN] = a0.w.x + a0.w.y;
+    {
+        const float S0 = a0.s.x + a0.s.y;
+        float V0 = a0.v.x + a0.v.y;
+        float W0v = a0.w.x + a0.w.y;
+        thread_to_row(S0, V0, W0 ? &W0v : nullptr, d);
+        out[0] = S0;
+        out[1] = V0;
+        if (W0) out[2 % PassOut<P, W0>::kN] = W0v;
+    }
 #pragma unroll
     for (int p = 1; p < P; ++p) {
-        out[PassOut<P, W0>::s_idx(p)] = ap[p - 1].s.x + ap[p - 1].s.y;
-        out[PassOut<P, W0>::s_idx(p) + 1] = ap[p - 1].v.x + ap[p - 1].v.y;
+        const float Sp = ap[p - 1].s.x + ap[p - 1].s.y;
+        float Vp = ap[p - 1].v.x + ap[p - 1].v.y;
+        thread_to_row(Sp, Vp, nullptr, d);
+        out[PassOut<P, W0>::s_idx(p)] = Sp;
+        out[PassOut<P, W0>::s_idx(p) + 1] = Vp;
     }
 }
 
 // One search round with P temperatures: pass, exchange, update.  W0: the
-// next round takes a Newton step from point 0, which needs its W.
+// next round takes a Newton step from point 0, which needs its W.  d: this
+// thread's offset (its max's y relative to the row's).
 template <bool CLUSTER, int P, bool W0>
 __device__ __forceinline__ void search_round(Search& st, const SearchCfg& cfg,
                                              const float (&T)[kMaxPoints],
                                              const int (&J)[kMaxPoints],
                                              const float4* row4, int q4,
-                                             const Smem& sm, Exch& x) {
+                                             float d, const Smem& sm, Exch& x) {
     float beta[kMaxPoints];
 #pragma unroll
     for (int p = 0; p < kMaxPoints; ++p) beta[p] = p < P ? rcp_approx(T[p]) : 1.0f;
     constexpr int NV = PassOut<P, W0>::kN;
     float a[NV];
-    eval_pass<P, W0>(row4, q4, beta, a);
-    exchange<CLUSTER, NV, false>(a, sm, x);
+    eval_pass<P, W0>(row4, q4, beta, d, a);
+    exchange<CLUSTER, OpSum, NV>(a, sm, x);
     float S[kMaxPoints], V[kMaxPoints], W[kMaxPoints];
 #pragma unroll
     for (int p = 0; p < kMaxPoints; ++p) {
@@ -364,33 +449,39 @@ __device__ __forceinline__ void store_scalar_lanes(float* dst, int q, int pad,
     }
 }
 
-// Output pass: p = 2^(beta y) * inv_s (or zeros) into dst[0, len).
+// Output pass over this thread's float4s (q = t, t + nt, ...): p =
+// 2^(beta (y + d)) * inv_s (or zeros) into dst[0, len).
 __device__ __forceinline__ void write_out(const float4* row4, const Slice& s,
-                                          float* dst, float beta, float inv_s,
-                                          bool zero) {
+                                          float* dst, float beta, float d,
+                                          float inv_s, bool zero) {
     const int pad_o = static_cast<int>((reinterpret_cast<uintptr_t>(dst) >> 2) & 3);
     const bool vec = pad_o == s.pad;
     const float2 b2 = make_float2(beta, beta);
+    const float2 bd2 = make_float2(beta * d, beta * d);
     const float2 i2 = make_float2(inv_s, inv_s);
     auto prob = [&](int q) {
         if (zero) return make_float4(0.f, 0.f, 0.f, 0.f);
         const float4 y = row4[q];
-        const float2 x01 = mul2(make_float2(y.x, y.y), b2);
-        const float2 x23 = mul2(make_float2(y.z, y.w), b2);
+        const float2 x01 = fma2(make_float2(y.x, y.y), b2, bd2);
+        const float2 x23 = fma2(make_float2(y.z, y.w), b2, bd2);
         const float2 p01 = mul2(make_float2(ex2(x01.x), ex2(x01.y)), i2);
         const float2 p23 = mul2(make_float2(ex2(x23.x), ex2(x23.y)), i2);
         return make_float4(p01.x, p01.y, p23.x, p23.y);
     };
     const int nt = blockDim.x;
+    int q = threadIdx.x;
     if (!vec) {
         // The output's alignment differs from the input's: element stores.
-        for (int q = threadIdx.x; q < s.q4; q += nt)
+        for (; q < s.q4; q += nt)
             store_scalar_lanes(dst, q, s.pad, s.len, prob(q));
         return;
     }
-    // Aligned body, four float4s per trip; then the ragged head and tail.
+    // Ragged head, aligned body four float4s per trip, ragged tail.
     float* const db = dst - s.pad;  // float4 q of the body is at db + 4q
-    int q = s.qb0 + threadIdx.x;
+    if (q < s.qb0) {
+        store_scalar_lanes(dst, q, s.pad, s.len, prob(q));
+        q += nt;
+    }
     for (; q + 3 * nt < s.qb1; q += 4 * nt) {
         float4 p[4];
 #pragma unroll
@@ -401,10 +492,7 @@ __device__ __forceinline__ void write_out(const float4* row4, const Slice& s,
     }
     for (; q < s.qb1; q += nt)
         __stcs(reinterpret_cast<float4*>(db + 4 * q), prob(q));
-    if (threadIdx.x == 0 && s.head_q >= 0)
-        store_scalar_lanes(dst, s.head_q, s.pad, s.len, prob(s.head_q));
-    if (threadIdx.x == nt - 1 && s.tail_q >= 0)
-        store_scalar_lanes(dst, s.tail_q, s.pad, s.len, prob(s.tail_q));
+    if (q < s.q4) store_scalar_lanes(dst, q, s.pad, s.len, prob(q));
 }
 
 // MAXT: largest block the instantiation is launched with; MINB: blocks per
@@ -429,7 +517,6 @@ cluster_kernel(RowTask t, int n, int slice_len) {
         sm.cbar = reinterpret_cast<uint64_t*>(smem + L.cbar);
         sm.row4 = reinterpret_cast<float4*>(smem + L.row);
     }
-    float* row = reinterpret_cast<float*>(sm.row4);
     float4* row4 = sm.row4;
 
     if (threadIdx.x == 0) {
@@ -446,6 +533,7 @@ cluster_kernel(RowTask t, int n, int slice_len) {
                                          min(static_cast<int64_t>(slice_len), C - s0)));
     const SearchCfg cfg{t.t_min, t.hi0, t.entropy_bound,
                         t.entropy_bound * kLog2e,
+                        t.entropy_bound > 0.0f ? lg2_approx(t.entropy_bound) : 0.0f,
                         make_grid(t.t_min, fmaxf(t.hi0, t.t_min), t.max_iter)};
     Exch x{warps, n, rank, 0u, 0u, t.wait_limit_cycles, false};
     bool reported = false;
@@ -454,34 +542,46 @@ cluster_kernel(RowTask t, int n, int slice_len) {
         const float* src = t.logits + r * C + s0;
         const Slice s = make_slice(src, len);
 
-        // Stage: every thread loads its float4s of the slice's aligned body
-        // with 128-bit streaming loads, eight in flight at a time, stores
-        // them to shared memory and folds them into the row max and the
-        // finiteness check; threads 0-7 fetch the ragged head/tail float4s
-        // element by element.  (Bulk copies into shared memory were slower:
-        // one SM's bulk-copy traffic arrived at about 16 bytes per clock,
-        // against about 22 for plain loads with this many in flight.)
-        float mc[2] = {-INFINITY, 0.0f};  // local max; NaN/Inf code
-        float bad = 0.0f;  // becomes NaN if any element is NaN or +-Inf
+        // Stage: thread t loads float4s q = t, t + nt, ... of the slice
+        // (the float4s it owns in every later pass): the aligned body with
+        // 128-bit streaming loads, eight in flight at a time, the ragged
+        // head and tail element by element.  It stores them to shared
+        // memory and folds them into its own max and the finiteness check.
+        // (Bulk copies into shared memory were slower: one SM's bulk-copy
+        // traffic arrived at about 16 bytes per clock, against about 22 for
+        // plain loads with this many in flight.)
+        float m_t = -INFINITY;  // this thread's max
+        float bad = 0.0f;       // becomes NaN if any element is NaN or +-Inf
         bool nan_seen = false;
-        if (threadIdx.x < 8) {
-            const int q = threadIdx.x < 4 ? s.head_q : s.tail_q;
-            if (q >= 0) {
-                const int idx = 4 * q + (threadIdx.x & 3);
-                const int j = idx - s.pad;
-                float v = -INFINITY;
+        auto load_ragged = [&](int q) {
+            float e[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int j = 4 * q + i - s.pad;
+                e[i] = -INFINITY;
                 if (j >= 0 && j < s.len) {
-                    v = src[j];
-                    mc[0] = v;
-                    bad = v * 0.0f;
-                    nan_seen = isnan(v);
+                    e[i] = src[j];
+                    m_t = fmaxf(m_t, e[i]);
+                    bad = fmaf(e[i], 0.0f, bad);
+                    nan_seen = nan_seen || isnan(e[i]);
                 }
-                row[idx] = v;
             }
-        }
+            row4[q] = make_float4(e[0], e[1], e[2], e[3]);
+        };
+        auto fold = [&](float4 v) {
+            m_t = fmaxf(m_t, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+            bad = fmaf(v.x, 0.0f, bad);
+            bad = fmaf(v.y, 0.0f, bad);
+            bad = fmaf(v.z, 0.0f, bad);
+            bad = fmaf(v.w, 0.0f, bad);
+        };
         {
             const float* gb = src - s.pad;  // float4 q of the body is at gb + 4q
-            int q = s.qb0 + threadIdx.x;
+            int q = threadIdx.x;
+            if (q < s.qb0) {
+                load_ragged(q);
+                q += nt;
+            }
             for (; q + 7 * nt < s.qb1; q += 8 * nt) {
                 float4 v[8];
 #pragma unroll
@@ -490,59 +590,57 @@ cluster_kernel(RowTask t, int n, int slice_len) {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     row4[q + i * nt] = v[i];
-                    mc[0] = fmaxf(mc[0], fmaxf(fmaxf(v[i].x, v[i].y), fmaxf(v[i].z, v[i].w)));
-                    bad = fmaf(v[i].x, 0.0f, bad);
-                    bad = fmaf(v[i].y, 0.0f, bad);
-                    bad = fmaf(v[i].z, 0.0f, bad);
-                    bad = fmaf(v[i].w, 0.0f, bad);
+                    fold(v[i]);
                 }
             }
             for (; q < s.qb1; q += nt) {
                 const float4 v = __ldcs(reinterpret_cast<const float4*>(gb + 4 * q));
                 row4[q] = v;
-                mc[0] = fmaxf(mc[0], fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
-                bad = fmaf(v.x, 0.0f, bad);
-                bad = fmaf(v.y, 0.0f, bad);
-                bad = fmaf(v.z, 0.0f, bad);
-                bad = fmaf(v.w, 0.0f, bad);
+                fold(v);
             }
+            if (q < s.q4) load_ragged(q);
         }
-        // Classify a non-finite row (rare): 2 = NaN seen, 1 = only Inf.
+        // Classify a non-finite slice (rare): 2 = NaN seen, 1 = only Inf.
         // Each thread rescans only the float4s it stored itself.
+        float code = 0.0f;
         if (bad != bad) {
-            mc[1] = 1.0f;
-            for (int q = s.qb0 + threadIdx.x; q < s.qb1; q += nt) {
+            for (int q = threadIdx.x < s.qb0 ? threadIdx.x + nt : threadIdx.x;
+                 q < s.qb1; q += nt) {
                 const float4 v = row4[q];
                 if (isnan(v.x) || isnan(v.y) || isnan(v.z) || isnan(v.w))
                     nan_seen = true;
             }
-            if (nan_seen) mc[1] = 2.0f;
+            code = nan_seen ? 2.0f : 1.0f;
         }
-        exchange<CLUSTER, 2, true>(mc, sm, x);
-        const float m = mc[0];
-        const int row_code = static_cast<int>(mc[1]);
+        // T = 1 pass relative to this thread's max, then one reduction that
+        // forms the row's max, its S, V, W at T = 1 (rescaled to that max)
+        // and its NaN/Inf code: no separate exchange of the max.
+        float s1[5];
+        transform_pass(row4, s.q4, m_t, code, s1);
+        exchange<CLUSTER, OpSoftmax, 5>(s1, sm, x);
+        const float m = s1[0];
+        const int row_code = static_cast<int>(s1[4]);
+        // This thread's y offset: y (row) = y (stored) + d.
+        const float d = m_t > -INFINITY ? (m_t - m) * kLog2e : 0.0f;
 
         float* dst = t.out + r * C + s0;
         unsigned int bits = 0;
         float T_row = NAN;
         float beta_out = 0.0f, inv_s = 0.0f;
         if (row_code == 0) {
-            float s1[3];
-            transform_pass(row4, s.q4, m, s1);
-            exchange<CLUSTER, 3, false>(s1, sm, x);
-            if (!entropy_above(make_float2(s1[0], s1[1]), 1.0f, cfg.bound_bits)) {
+            if (!entropy_above(make_float2(s1[1], s1[2]), 1.0f, cfg.bound_bits)) {
                 T_row = 1.0f;
                 beta_out = 1.0f;
-                inv_s = 1.0f / s1[0];
+                inv_s = 1.0f / s1[1];
             } else {
-                Search st = search_begin(cfg, s1[0], s1[1], s1[2], t.strict != 0, false);
+                Search st = search_begin(cfg, s1[1], s1[2], s1[3], t.strict != 0, false);
                 if (!(cfg.t_min < cfg.hi0)) {
                     // No interval to halve: T = t_min (section 5.4 check).
                     st.final_round = true;
                     st.T_out = cfg.t_min;
                     const float T1[kMaxPoints] = {cfg.t_min, 0.f, 0.f};
                     const int J1[kMaxPoints] = {0, 0, 0};
-                    search_round<CLUSTER, 1, false>(st, cfg, T1, J1, row4, s.q4, sm, x);
+                    search_round<CLUSTER, 1, false>(st, cfg, T1, J1, row4, s.q4, d, sm, x);
                 }
                 while (!st.done) {
                     float T[kMaxPoints];
@@ -550,15 +648,15 @@ cluster_kernel(RowTask t, int n, int slice_len) {
                     const int np = search_plan(st, cfg, T, J);
                     const bool w0 = newton_next(st);
                     if (np == 1 && w0)
-                        search_round<CLUSTER, 1, true>(st, cfg, T, J, row4, s.q4, sm, x);
+                        search_round<CLUSTER, 1, true>(st, cfg, T, J, row4, s.q4, d, sm, x);
                     else if (np == 1)
-                        search_round<CLUSTER, 1, false>(st, cfg, T, J, row4, s.q4, sm, x);
+                        search_round<CLUSTER, 1, false>(st, cfg, T, J, row4, s.q4, d, sm, x);
                     else if (np == 2 && w0)
-                        search_round<CLUSTER, 2, true>(st, cfg, T, J, row4, s.q4, sm, x);
+                        search_round<CLUSTER, 2, true>(st, cfg, T, J, row4, s.q4, d, sm, x);
                     else if (np == 2)
-                        search_round<CLUSTER, 2, false>(st, cfg, T, J, row4, s.q4, sm, x);
+                        search_round<CLUSTER, 2, false>(st, cfg, T, J, row4, s.q4, d, sm, x);
                     else if (np == 3)
-                        search_round<CLUSTER, 3, false>(st, cfg, T, J, row4, s.q4, sm, x);
+                        search_round<CLUSTER, 3, false>(st, cfg, T, J, row4, s.q4, d, sm, x);
                 }
                 if (st.overflow) bits |= kBitOverflow;
                 T_row = st.T_out;
@@ -568,7 +666,7 @@ cluster_kernel(RowTask t, int n, int slice_len) {
         } else {
             bits = row_code == 2 ? kBitNan : kBitInf;
         }
-        write_out(row4, s, dst, beta_out, inv_s, row_code != 0);
+        write_out(row4, s, dst, beta_out, d, inv_s, row_code != 0);
         if (rank == 0 && threadIdx.x == 0) {
             if (t.t_out) t.t_out[r] = T_row;
             raise_error(t.err, bits);

@@ -109,6 +109,7 @@ rowgroup_kernel(RowTask t, int vec) {
     const int Q = (C + 3) >> 2;  // float4 slots per row
     const float bound_bits = t.entropy_bound * kLog2e;
     const SearchCfg cfg{t.t_min, t.hi0, t.entropy_bound, bound_bits,
+                        t.entropy_bound > 0.0f ? lg2_approx(t.entropy_bound) : 0.0f,
                         make_grid(t.t_min, fmaxf(t.hi0, t.t_min), t.max_iter)};
     const int64_t groups_per_grid =
         (static_cast<int64_t>(gridDim.x) * blockDim.x) / G;
