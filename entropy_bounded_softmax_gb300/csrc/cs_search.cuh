@@ -24,7 +24,9 @@
 // root approaches it, then, once Newton has converged, the grid points on
 // both sides of the Newton point; if the bracket is still open
 // (evaluations of H in fp32 are within rounding of the bound there) it
-// splits the bracket into quarters, two halvings per round.  With one
+// splits the bracket into quarters, two halvings per round, or, on the
+// fine grid when the last round moved only one end, gallops away from that
+// end with strides growing eightfold.  With one
 // point per round (narrow rows, where a pass costs little next to
 // divergent bookkeeping) the Newton point is evaluated alone and the
 // neighbours follow one by one, with doubling strides.  The strict mode
@@ -114,7 +116,8 @@ struct Search {
     bool endgame;       // Newton has converged: quarter the bracket
     bool single;        // one point per round
     int jlast;          // single: the index evaluated last
-    int stride;         // single: the next neighbour step
+    int stride;         // the next galloping step
+    int jl_prev, jh_prev;  // the bracket when the last round was planned
     float SA;           // S at G(jl) when jl_eval
     float S_tmin;       // S at t_min when tmin_inf
     float b_jl, b_jh;   // beta of the bracket's ends (t_min while !jl_eval)
@@ -154,6 +157,8 @@ __device__ __forceinline__ Search search_begin(const SearchCfg& c, float S1,
     s.single = single;
     s.jlast = -1;
     s.stride = 1;
+    s.jl_prev = s.jl;
+    s.jh_prev = s.jh;
     s.SA = 0.0f;
     s.S_tmin = 0.0f;
     s.b_jl = rcp_approx(c.t_min);
@@ -219,6 +224,35 @@ __device__ __forceinline__ int search_plan(Search& s, const SearchCfg& c,
         return 1;
     }
     if (s.endgame) {
+        const bool lo_moved = s.jl != s.jl_prev, hi_moved = s.jh != s.jh_prev;
+        s.jl_prev = s.jl;
+        s.jh_prev = s.jh;
+        if (g.fine && lo_moved != hi_moved) {
+            // Fine grid (every fp32 value a point, so a converged Newton
+            // point is still many points off) and only one end moved last
+            // round: the crossing is most likely just past that end.  Gallop
+            // from it towards the other end, 1, 2 and 4 strides out, the
+            // stride growing eightfold per round (when the bracket is
+            // shorter than a stride, quarter it instead).  On the coarser
+            // exact grid the converged round almost always closes the
+            // bracket, and quartering measured as fast.
+            const int d = s.jh - s.jl;
+            s.stride = max(s.stride, 2);
+            int np = 0;
+#pragma unroll
+            for (int k = 0; k < kMaxPoints; ++k) {
+                const int off = s.stride << k;
+                if (off >= d) break;
+                J[np++] = lo_moved ? s.jl + off : s.jh - off;
+            }
+            if (s.stride < (1 << 26)) s.stride <<= 3;
+            if (np > 0) {
+#pragma unroll
+                for (int i = 0; i < kMaxPoints; ++i)
+                    if (i < np) T[i] = g.at(J[i]);
+                return np;
+            }
+        }
         // The bracket's midpoint and quarter points: two halvings per round.
         const int d = s.jh - s.jl;
         const int m = s.jl + (d >> 1);
@@ -252,6 +286,8 @@ __device__ __forceinline__ int search_plan(Search& s, const SearchCfg& c,
     int jn = Tn > g.lo0 ? g.near(Tn) : 0;
     jn = min(max(jn, s.jl + 1), s.jh - 1);
     int np = 0;
+    s.jl_prev = s.jl;
+    s.jh_prev = s.jh;
     const bool probe = !s.jl_eval && Tn <= 4.0f * g.lo0;  // t_min probe
     if (s.single) {
         J[0] = probe ? 0 : jn;
