@@ -55,7 +55,7 @@ class Workload:
 SMALL = Workload("small_4x1000", 4, 1000, "normal", 1.0, 1001,
                  note="batch 4, 1000 classes, N(0,1)")
 LATENCY = Workload("latency_32x50000", 32, 50000, "normal", 2.0, 1002,
-                   note="batch 32, 50000 classes, N(0,2^2); one CTA per row")
+                   note="batch 32, 50000 classes, N(0,2^2)")
 ROUTER = Workload("moe_router_65536x64", 65536, 64, "router", 1.0, 1003,
                   note="65536 tokens, 64 experts, N(0,1) plus one expert per "
                        "row boosted by U(0,3)")
