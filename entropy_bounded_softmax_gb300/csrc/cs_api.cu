@@ -175,8 +175,14 @@ cs_status plan_cluster(int64_t batch, int32_t C, const cs_options& o,
         if (n0 > max_cluster) n0 = max_cluster;
         if (n0 < 1) n0 = 1;
         // Widen only while every CTA keeps at least kMinWideSlice classes.
+        // Few rows: one CTA per SM, rounded up when that oversubscribes the
+        // SMs by at most a quarter (the extra CTAs share SMs; shorter slices
+        // shorten every pass of a latency-bound launch: 32 x 50000 runs in
+        // clusters of 5, 160 CTAs, 8% faster than in clusters of 4).
         const int64_t rows = batch > 0 ? batch : 1;
         int64_t widen = sm_count / rows;
+        const int64_t up = ceil_div(sm_count, rows);
+        if (up > widen && rows * up * 4 <= sm_count * 5) widen = up;
         if (widen > C / kMinWideSlice) widen = C / kMinWideSlice;
         if (widen > max_cluster) widen = max_cluster;
         if (widen > n0) n0 = static_cast<int>(widen);

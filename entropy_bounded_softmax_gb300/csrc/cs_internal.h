@@ -80,13 +80,14 @@ inline int64_t cluster_smem_bytes(int64_t slice_len, int threads, int n) {
 // three CTAs share an SM and one's exchange overlaps the others' passes.
 constexpr int64_t kTargetSlice = 16384;
 
-// Automatic threads per CTA: about 48 classes per thread for a launch with
-// no more CTAs than SMs (one CTA per SM, all of its time on one row),
-// about 64 for larger launches (several CTAs share an SM); 128-256 threads
-// either way, where the per-round reductions stay short.
+// Automatic threads per CTA: about 40 classes per thread for a launch with
+// about one CTA per SM (up to a quarter more CTAs than SMs; all of a CTA's
+// time goes to one row), about 64 for larger launches (several CTAs share
+// an SM); 128-256 threads either way, where the per-round reductions stay
+// short.
 inline int cluster_threads_for(int64_t slice_len, int64_t ctas,
                                int64_t sm_count) {
-    const int64_t per = ctas <= sm_count ? 48 : 64;
+    const int64_t per = ctas * 4 <= sm_count * 5 ? 40 : 64;
     int64_t t = (slice_len + per - 1) / per;
     t = ((t + 31) / 32) * 32;
     if (t < 128) t = 128;
