@@ -107,6 +107,9 @@ cudaError_t launch_wait_timeout(unsigned int* err, uint64_t limit_cycles,
 
 // cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per device and
 // kernel, raised only when a launch needs more than was set before.
-cudaError_t ensure_smem_attribute(const void* func, int slot, int bytes);
+// slot: one per kernel instantiation; cluster: it is launched in clusters
+// (also allows cluster sizes above 8).
+cudaError_t ensure_smem_attribute(const void* func, int slot, int bytes,
+                                  bool cluster);
 
 }  // namespace cs

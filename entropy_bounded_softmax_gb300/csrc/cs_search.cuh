@@ -376,4 +376,124 @@ __device__ __forceinline__ void search_update(Search& s, const SearchCfg& c,
     ++s.rounds;
 }
 
+// Newton rounds every searching narrow row takes before the fallback.
+constexpr int kNarrowNewtonRounds = 5;
+
+// The search for narrow rows, one grid point per round (the row-group
+// kernel, whose rows are a few registers per lane; a multi-point pass there
+// costs more than the rounds it saves).  Called
+// after H(1) > bound with S1, V1, W1 at beta = 1; eval3(beta) returns the
+// row's (S, V, W) at beta and eval2(beta) its (S, V).  Strict: the
+// bisection, one evaluation per halving.  Otherwise up to
+// kNarrowNewtonRounds Newton steps on log H(beta) from the last point
+// evaluated, kept inside the bracket in beta and placed on the grid point
+// at or below (t_min when the step comes within 4 t_min of it), then, only
+// while the bracket is open, points stepping from the end moved last with
+// doubling strides.  One lg2 and one reciprocal of S serve both the
+// decision and the next step.  Returns T, 1/T, 1/S(T) and the section 5.4
+// flag.
+template <class Eval3, class Eval2>
+__device__ __forceinline__ void narrow_search(const SearchCfg& cfg, float S1,
+                                              float V1, float W1, bool strict,
+                                              Eval3 eval3, Eval2 eval2,
+                                              float& T_out, float& beta_out,
+                                              float& inv_s, bool& overflow) {
+    const Grid& g = cfg.g;
+    int jl = 0, jh = g.top;
+    bool jl_eval = false;   // G(jl) evaluated feasible
+    bool tmin_inf = false;  // t_min evaluated infeasible
+    float s_lo = 0.0f;
+    if (cfg.t_min < cfg.hi0 && strict) {
+        while (jh - jl > 1) {
+            const int jm = jl + ((jh - jl) >> 1);
+            const float b = rcp_approx(g.at(jm));
+            const float2 sv = eval2(b);
+            if (entropy_above(sv, b, cfg.bound_bits)) {
+                jh = jm;
+            } else {
+                jl = jm;
+                jl_eval = true;
+                s_lo = sv.x;
+            }
+        }
+    } else if (cfg.t_min < cfg.hi0) {
+        float b = 1.0f, S = S1, V = V1, W = W1;
+        float b_inf = rcp_approx(cfg.hi0);
+        float b_feas = rcp_approx(cfg.t_min);
+        const bool log_newton = cfg.bound > 0.0f;
+        int jlast = -1;
+        for (int k = 0; k < kNarrowNewtonRounds && jh - jl > 1 && !tmin_inf; ++k) {
+            const float is = rcp_approx(S);
+            const float ey = V * is;
+            const float H = kLn2 * (lg2_approx(S) - b * ey);
+            const float dH = -b * (kLn2 * kLn2) * fmaxf(fmaf(W, is, -ey * ey), 0.0f);
+            float bn;
+            if (log_newton && H > 0.0f) {
+                const float gl = lg2_approx(H) - cfg.lg2_bound;
+                bn = b - gl * H * rcp_approx(dH * kLog2e);
+            } else {
+                bn = b - (H - cfg.bound) * rcp_approx(dH);
+            }
+            if (!(bn > b_inf && bn < b_feas)) bn = sqrtf(b_inf * b_feas);
+            const float Tn = rcp_approx(bn);
+            const bool probe = !jl_eval && Tn <= 4.0f * cfg.t_min;
+            int jn = Tn > cfg.t_min ? g.near(Tn) : 0;
+            jn = probe ? 0 : min(max(jn, jl + 1), jh - 1);
+            b = rcp_approx(probe ? cfg.t_min : g.at(jn));
+            const float3 r = eval3(b);
+            S = r.x;
+            V = r.y;
+            W = r.z;
+            const bool inf = entropy_above(make_float2(S, V), b, cfg.bound_bits);
+            jlast = jn;
+            if (probe) {
+                s_lo = S;
+                if (inf) {
+                    tmin_inf = true;
+                } else {
+                    jl_eval = true;
+                    b_feas = b;
+                }
+            } else if (inf) {
+                jh = jn;
+                b_inf = b;
+            } else {
+                jl = jn;
+                jl_eval = true;
+                s_lo = S;
+                b_feas = b;
+            }
+        }
+        int stride = 1;
+        while (jh - jl > 1 && !tmin_inf) {
+            const int d = jh - jl;
+            const int step = max(min(stride, d >> 1), 1);
+            const int jm = jl == jlast ? jl + step : jh == jlast ? jh - step : jl + (d >> 1);
+            stride *= 2;
+            jlast = jm;
+            const float bm = rcp_approx(g.at(jm));
+            const float2 sv = eval2(bm);
+            if (entropy_above(sv, bm, cfg.bound_bits)) {
+                jh = jm;
+            } else {
+                jl = jm;
+                jl_eval = true;
+                s_lo = sv.x;
+            }
+        }
+    }
+    const float lo = jl_eval ? g.at(jl) : cfg.t_min;
+    const float b_lo = rcp_approx(lo);
+    overflow = tmin_inf;
+    if (!tmin_inf && !jl_eval) {
+        // lo is still t_min: evaluate it (section 5.4 check).
+        const float2 sv = eval2(b_lo);
+        s_lo = sv.x;
+        overflow = entropy_above(sv, b_lo, cfg.bound_bits);
+    }
+    T_out = lo;
+    beta_out = b_lo;
+    inv_s = 1.0f / s_lo;
+}
+
 }  // namespace csd

@@ -62,13 +62,14 @@ cudaError_t launch_wait_timeout(unsigned int* err, uint64_t limit_cycles,
 
 namespace {
 constexpr int kMaxDevices = 64;
-constexpr int kSlots = 4;
+constexpr int kSlots = 8;
 // Largest MaxDynamicSharedMemorySize set so far, per device and kernel.
 std::atomic<int> g_smem_set[kMaxDevices][kSlots];
 std::mutex g_smem_mu;
 }  // namespace
 
-cudaError_t ensure_smem_attribute(const void* func, int slot, int bytes) {
+cudaError_t ensure_smem_attribute(const void* func, int slot, int bytes,
+                                  bool cluster) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -82,7 +83,7 @@ cudaError_t ensure_smem_attribute(const void* func, int slot, int bytes) {
     e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              bytes);
     if (e != cudaSuccess) return e;
-    if (slot == 1 || slot == 3) {
+    if (cluster) {
         e = cudaFuncSetAttribute(
             func, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;

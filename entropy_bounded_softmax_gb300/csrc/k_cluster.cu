@@ -687,7 +687,7 @@ cudaError_t launch_one(const RowTask& task, int cluster_size, int slice_len,
                        cudaStream_t stream, int attr_slot) {
     auto kern = cluster_kernel<CLUSTER, MAXT, MINB>;
     cudaError_t e = ensure_smem_attribute(reinterpret_cast<const void*>(kern),
-                                          attr_slot, smem_bytes);
+                                          attr_slot, smem_bytes, CLUSTER);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid_ctas), 1, 1);

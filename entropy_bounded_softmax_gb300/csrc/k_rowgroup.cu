@@ -92,9 +92,6 @@ __device__ __forceinline__ float3 reg_pass3(const float4 (&y)[E4], float beta) {
     return make_float3(sv.x, sv.y, w.x + w.y);
 }
 
-// Rounds of Newton steps every searching row takes before the fallback.
-constexpr int kRowNewtonRounds = 5;
-
 // At most 64 registers a thread (32 warps per SM, which the latency of each
 // row's dependent reduce-and-decide chain needs), or 80 when a lane holds
 // 32 classes.
@@ -191,118 +188,13 @@ rowgroup_kernel(RowTask t, int vec) {
                 beta_out = 1.0f;
                 inv_s = 1.0f / sv.x;
             } else {
-                const Grid& g = cfg.g;
-                int jl = 0, jh = g.top;
-                bool jl_eval = false;   // G(jl) evaluated feasible
-                bool tmin_inf = false;  // t_min evaluated infeasible
-                float s_lo = 0.0f;
-                if (cfg.t_min < cfg.hi0 && t.strict) {
-                    // Strict: the bisection, one evaluation per halving.
-                    while (jh - jl > 1) {
-                        const int jm = jl + ((jh - jl) >> 1);
-                        const float b = rcp_approx(g.at(jm));
-                        sv = group_sum2<G>(reg_pass<E4>(y, b), gmask);
-                        if (entropy_above(sv, b, bound_bits)) {
-                            jh = jm;
-                        } else {
-                            jl = jm;
-                            jl_eval = true;
-                            s_lo = sv.x;
-                        }
-                    }
-                } else if (cfg.t_min < cfg.hi0) {
-                    // The bracket search of cs_search.cuh in a lean form
-                    // for rows this narrow: every searching row takes the
-                    // same rounds of one grid point each, so the rows of a
-                    // warp stay together.  Up to kRowNewtonRounds Newton
-                    // steps on log H(beta) from the last point evaluated,
-                    // kept inside the bracket (b_inf, b_feas) in beta and
-                    // placed on the grid point at or below; t_min when the
-                    // step comes within 4 t_min of it.  Then, only if the
-                    // bracket is still open, one point per round stepping
-                    // from the end moved last with doubling strides.
-                    float b = 1.0f, S = r1.x, V = r1.y, W = r1.z;
-                    float b_inf = rcp_approx(cfg.hi0);
-                    float b_feas = rcp_approx(cfg.t_min);
-                    const float lg2_bound = lg2_approx(t.entropy_bound);
-                    const bool log_newton = t.entropy_bound > 0.0f;
-                    int jlast = -1;
-                    for (int k = 0; k < kRowNewtonRounds && jh - jl > 1 && !tmin_inf; ++k) {
-                        const float is = rcp_approx(S);
-                        const float ey = V * is;
-                        const float H = kLn2 * (lg2_approx(S) - b * ey);
-                        const float dH = -b * (kLn2 * kLn2) * fmaxf(fmaf(W, is, -ey * ey), 0.0f);
-                        float bn;
-                        if (log_newton && H > 0.0f) {
-                            const float gl = lg2_approx(H) - lg2_bound;
-                            const float gp = dH * rcp_approx(H) * kLog2e;
-                            bn = b - gl * rcp_approx(gp);
-                        } else {
-                            bn = b - (H - t.entropy_bound) * rcp_approx(dH);
-                        }
-                        if (!(bn > b_inf && bn < b_feas)) bn = sqrtf(b_inf * b_feas);
-                        const float Tn = rcp_approx(bn);
-                        const bool probe = !jl_eval && Tn <= 4.0f * cfg.t_min;
-                        int jn = Tn > cfg.t_min ? g.near(Tn) : 0;
-                        jn = probe ? 0 : min(max(jn, jl + 1), jh - 1);
-                        b = rcp_approx(probe ? cfg.t_min : g.at(jn));
-                        const float3 r = group_sum3<G>(reg_pass3<E4>(y, b), gmask);
-                        S = r.x;
-                        V = r.y;
-                        W = r.z;
-                        const bool inf = entropy_above(make_float2(S, V), b, bound_bits);
-                        jlast = jn;
-                        if (probe) {
-                            if (inf) {
-                                tmin_inf = true;
-                                s_lo = S;
-                            } else {
-                                jl_eval = true;
-                                s_lo = S;
-                                b_feas = b;
-                            }
-                        } else if (inf) {
-                            jh = jn;
-                            b_inf = b;
-                        } else {
-                            jl = jn;
-                            jl_eval = true;
-                            s_lo = S;
-                            b_feas = b;
-                        }
-                    }
-                    int stride = 1;
-                    while (jh - jl > 1 && !tmin_inf) {
-                        const int d = jh - jl;
-                        const int step = max(min(stride, d >> 1), 1);
-                        const int jm = jl == jlast ? jl + step
-                                     : jh == jlast ? jh - step : jl + (d >> 1);
-                        stride *= 2;
-                        jlast = jm;
-                        const float bm = rcp_approx(g.at(jm));
-                        sv = group_sum2<G>(reg_pass<E4>(y, bm), gmask);
-                        if (entropy_above(sv, bm, bound_bits)) {
-                            jh = jm;
-                        } else {
-                            jl = jm;
-                            jl_eval = true;
-                            s_lo = sv.x;
-                        }
-                    }
-                }
-                const float lo = jl_eval ? g.at(jl) : t.t_min;
-                const float b_lo = rcp_approx(lo);
-                if (tmin_inf) {
-                    bits |= kBitOverflow;
-                } else if (!jl_eval) {
-                    // lo is still t_min: evaluate it (section 5.4 check).
-                    sv = group_sum2<G>(reg_pass<E4>(y, b_lo), gmask);
-                    s_lo = sv.x;
-                    if (entropy_above(sv, b_lo, bound_bits)) bits |= kBitOverflow;
-                }
-                T_row = lo;
-                beta_out = b_lo;
-                inv_s = 1.0f / s_lo;
+                bool over = false;
+                narrow_search(
+                    cfg, r1.x, r1.y, r1.z, t.strict != 0,
+                    [&](float b) { return group_sum3<G>(reg_pass3<E4>(y, b), gmask); },
+                    [&](float b) { return group_sum2<G>(reg_pass<E4>(y, b), gmask); },
+                    T_row, beta_out, inv_s, over);
+                if (over) bits |= kBitOverflow;
             }
         }
         const bool zero = row_code != 0;

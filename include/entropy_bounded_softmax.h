@@ -22,7 +22,8 @@
  *      finds it from a bracket of grid points closed by safeguarded Newton
  *      steps, evaluating H only where needed (cs_options.strict halves the
  *      bracket one evaluation at a time, i.e. bisects).  The row-group
- *      kernel, whose rows are a few registers per lane, bisects;
+ *      kernel, whose rows are a few registers per lane, takes one
+ *      Newton-placed point per round;
  *   4. write softmax(l / lo) and report T = lo.  If even lo = t_min violates
  *      the bound, the row still gets softmax(l / t_min), the lowest entropy
  *      reachable (section 5.4), and ENTROPY_OVERFLOW is raised.
@@ -74,12 +75,12 @@ typedef struct cs_options {
                           cluster: CTAs per row (1..16); 0 = automatic      */
     int32_t threads;   /* cluster: threads per CTA (multiple of 32,
                           64..512); 0 = automatic                           */
-    int32_t strict;    /* cluster: 1 = bisect (H evaluated at every
-                          midpoint, one pass per halving); 0 = close the
-                          bracket from Newton-placed evaluations (same
-                          result for monotone H, fewer passes).  The
-                          row-group kernel always bisects; 0 or 1 is
-                          accepted there                                    */
+    int32_t strict;    /* 1 = bisect (H evaluated at every midpoint, one
+                          pass per halving); 0 = close the bracket from
+                          Newton-placed evaluations (same result for
+                          monotone H, fewer passes: up to 3 points per
+                          round in the cluster kernel, one in the
+                          row-group kernel)                                 */
 } cs_options;
 
 /* What a launch of the given shape uses.  Filled by cs_plan_launch /
