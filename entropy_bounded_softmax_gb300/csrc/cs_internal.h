@@ -82,12 +82,13 @@ constexpr int64_t kTargetSlice = 16384;
 
 // Automatic threads per CTA: about 40 classes per thread for a launch with
 // about one CTA per SM (up to a quarter more CTAs than SMs; all of a CTA's
-// time goes to one row), about 64 for larger launches (several CTAs share
-// an SM); 128-256 threads either way, where the per-round reductions stay
-// short.
+// time goes to one row), about 72 for larger launches (several CTAs share
+// an SM; measured: 16000-class slices run 4-5% faster on 224 threads than
+// on 256, 16384-class slices 2% slower); 128-256 threads either way, where
+// the per-round reductions stay short.
 inline int cluster_threads_for(int64_t slice_len, int64_t ctas,
                                int64_t sm_count) {
-    const int64_t per = ctas * 4 <= sm_count * 5 ? 40 : 64;
+    const int64_t per = ctas * 4 <= sm_count * 5 ? 40 : 72;
     int64_t t = (slice_len + per - 1) / per;
     t = ((t + 31) / 32) * 32;
     if (t < 128) t = 128;

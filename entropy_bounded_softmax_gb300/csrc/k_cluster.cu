@@ -331,7 +331,17 @@ __device__ __forceinline__ void transform_pass(float4* row4, int q4, float m_t,
             acc.add(y[i], one, zero);
         }
     }
-    for (; q < q4; q += nt) {
+    // At most three left: a pair, then a single.
+    if (q + nt < q4) {
+        const float4 ya = to_y(row4[q]);
+        const float4 yb = to_y(row4[q + nt]);
+        row4[q] = ya;
+        row4[q + nt] = yb;
+        acc.add(ya, one, zero);
+        acc.add(yb, one, zero);
+        q += 2 * nt;
+    }
+    if (q < q4) {
         const float4 y = to_y(row4[q]);
         row4[q] = y;
         acc.add(y, one, zero);
@@ -385,7 +395,20 @@ __device__ __forceinline__ void eval_pass(const float4* row4, int q4,
             for (int p = 1; p < P; ++p) ap[p - 1].add(y[i], b2[p], bd2[p]);
         }
     }
-    for (; q < q4; q += nt) {
+    // At most three left: a pair, then a single.
+    if (q + nt < q4) {
+        const float4 ya = row4[q];
+        const float4 yb = row4[q + nt];
+        a0.add(ya, b2[0], bd2[0]);
+        a0.add(yb, b2[0], bd2[0]);
+#pragma unroll
+        for (int p = 1; p < P; ++p) {
+            ap[p - 1].add(ya, b2[p], bd2[p]);
+            ap[p - 1].add(yb, b2[p], bd2[p]);
+        }
+        q += 2 * nt;
+    }
+    if (q < q4) {
         const float4 ya = row4[q];
         a0.add(ya, b2[0], bd2[0]);
 #pragma unroll
@@ -490,8 +513,17 @@ __device__ __forceinline__ void write_out(const float4* row4, const Slice& s,
         for (int i = 0; i < 4; ++i)
             __stcs(reinterpret_cast<float4*>(db + 4 * (q + i * nt)), p[i]);
     }
-    for (; q < s.qb1; q += nt)
+    // At most three left in the body: a pair, then a single.
+    if (q + nt < s.qb1) {
+        const float4 pa = prob(q), pb = prob(q + nt);
+        __stcs(reinterpret_cast<float4*>(db + 4 * q), pa);
+        __stcs(reinterpret_cast<float4*>(db + 4 * (q + nt)), pb);
+        q += 2 * nt;
+    }
+    if (q < s.qb1) {
         __stcs(reinterpret_cast<float4*>(db + 4 * q), prob(q));
+        q += nt;
+    }
     if (q < s.q4) store_scalar_lanes(dst, q, s.pad, s.len, prob(q));
 }
 
