@@ -8,7 +8,8 @@ nothing from the product.
 The arithmetic lives in ``constrained_softmax_oracle.c`` (plain fp64 C, libm
 ``exp``/``log``), which follows "BURT-IMMA CUDA Kernel API Reference",
 section 2.1 ``constrained_softmax`` and section 5 (error codes, NaN/Inf policy,
-graceful degradation).  This module only compiles it with gcc, marshals numpy
+graceful degradation), and the backward of section 6.3 with the temperature
+restored.  This module only compiles it with gcc, marshals numpy
 arrays in and out through ctypes, and splits a batch over threads (rows are
 independent, so the split changes no arithmetic).
 
@@ -77,6 +78,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_constrained_softmax_path.argtypes = [
         f32p, f64p, ctypes.c_int64, ctypes.c_float, ctypes.c_float,
         ctypes.c_float, ctypes.c_int32, f64p, i32p, f64p, f64p]
+    lib.oracle_constrained_softmax_backward_rows.restype = None
+    lib.oracle_constrained_softmax_backward_rows.argtypes = [
+        f64p, f64p, f64p, f64p, ctypes.c_int64, ctypes.c_int64,
+        ctypes.c_int64]
     return lib
 
 
@@ -216,6 +221,34 @@ def constrained_softmax_path(l, entropy_bound: float = 0.20,
         _ptr(Hs, ctypes.c_double))
     k = int(it[0])
     return Path(p, float(T[0]), int(flag), k, mids[:k].copy(), Hs[:k].copy())
+
+
+def constrained_softmax_backward(p, grad_output, T,
+                                 lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """Gradient of the loss with respect to the logits, in fp64.
+
+    ``p`` is the forward's output [batch, C], ``grad_output`` the upstream
+    gradient of the same shape and ``T`` the forward's per-row temperature
+    [batch].  Each row gets (1/T) p (g - <g, p>): section 6.3's
+    ConstrainedSoftmaxFunction.backward with the 1/T of softmax(l / T)
+    restored (T is piecewise constant in the logits, so it contributes no
+    term of its own); rows with T NaN (or not positive and finite) get
+    zeros.  Inputs of any float dtype are promoted exactly to fp64.
+    """
+    lib = lib or load()
+    pp = np.ascontiguousarray(np.asarray(p, dtype=np.float64))
+    gg = np.ascontiguousarray(np.asarray(grad_output, dtype=np.float64))
+    tt = np.ascontiguousarray(np.asarray(T, dtype=np.float64).reshape(-1))
+    if pp.ndim != 2 or gg.shape != pp.shape or tt.size != pp.shape[0]:
+        raise ValueError("p, grad_output: [batch, C]; T: [batch]")
+    batch, C = pp.shape
+    grad = np.empty((batch, C), dtype=np.float64)
+    if batch and C:
+        lib.oracle_constrained_softmax_backward_rows(
+            _ptr(pp, ctypes.c_double), _ptr(gg, ctypes.c_double),
+            _ptr(tt, ctypes.c_double), _ptr(grad, ctypes.c_double), 0, batch,
+            C)
+    return grad
 
 
 def search_interval(t_min: float, t_max: float) -> tuple[float, float]:

@@ -10,7 +10,9 @@
  * Source of the method: "BURT-IMMA CUDA Kernel API Reference", section 2.1
  * `constrained_softmax` (Parameters table, Description steps 1-4, Performance
  * Notes) and section 5 (5.1 Error Codes, 5.3 NaN/Inf Propagation Policy,
- * 5.4 Graceful Degradation).
+ * 5.4 Graceful Degradation); the backward follows section 6.3 (PyTorch Custom
+ * Op Integration, ConstrainedSoftmaxFunction.backward) with the 1/T of
+ * softmax(l / T) restored.
  *
  * Arithmetic: IEEE double throughout, libm exp() and log().  The fp32
  * parameters are promoted exactly to double, so both sides of any comparison
@@ -181,4 +183,43 @@ int32_t oracle_constrained_softmax_path(const float* l, double* p, int64_t C,
 {
     return one_row(l, C, (double)entropy_bound, (double)t_min, (double)t_max,
                    max_iter, p, T_out, iters_out, path_mid, path_H);
+}
+
+/*
+ * Backward of constrained_softmax: the vector-Jacobian product of section
+ * 6.3 (ConstrainedSoftmaxFunction.backward) with the temperature restored.
+ *
+ * The output is p = softmax(l / T), where T is the bisection's final lo.
+ * That lo is one of finitely many grid points chosen by the comparisons
+ * H(mid) > bound, so T is piecewise constant in l: its derivative is zero
+ * everywhere except on the measure-zero set where a comparison flips.  There
+ * dp_i/dl_k = (1/T) p_i (delta_ik - p_k), and for an upstream gradient g
+ *
+ *     grad_k = sum_i g_i dp_i/dl_k = (1/T) p_k (g_k - sum_i g_i p_i).
+ *
+ * Section 6.3 writes p (g - <g, p>): the same product without the 1/T, which
+ * is exact only where T = 1.  A row whose T is not a positive finite number
+ * (NaN: section 5.3 zeroed the row, so its output does not depend on l) gets
+ * a zero gradient.
+ *
+ * p, g and grad are row-major [*, C] doubles, T is [*]; rows
+ * [row_begin, row_end) are computed.
+ */
+void oracle_constrained_softmax_backward_rows(const double* p, const double* g,
+                                              const double* T, double* grad,
+                                              int64_t row_begin,
+                                              int64_t row_end, int64_t C)
+{
+    for (int64_t b = row_begin; b < row_end; ++b) {
+        const double* pb = p + b * C;
+        const double* gb = g + b * C;
+        double* out = grad + b * C;
+        if (!(T[b] > 0.0) || isinf(T[b])) {
+            for (int64_t k = 0; k < C; ++k) out[k] = 0.0;
+            continue;
+        }
+        double dot = 0.0;
+        for (int64_t i = 0; i < C; ++i) dot += gb[i] * pb[i];
+        for (int64_t k = 0; k < C; ++k) out[k] = pb[k] * (gb[k] - dot) / T[b];
+    }
 }

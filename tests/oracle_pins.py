@@ -10,7 +10,13 @@ AssertionError when the oracle disagrees with:
   * invariants (probabilities sum to 1, argmax kept, constant rows uniform,
     shift invariance, H monotone along the search path, C = 1),
   * the NaN/Inf and unsatisfiable-bound policy of "BURT-IMMA CUDA Kernel API
-    Reference", sections 5.1, 5.3 and 5.4.
+    Reference", sections 5.1, 5.3 and 5.4,
+  * for the backward (section 6.3 with the temperature restored): central
+    finite differences through the whole forward, search included; the
+    vector-Jacobian product of a library softmax (torch autograd, fp64) at
+    the forward's temperature; the explicit Jacobian diag(p) - p p^T at
+    T = 1; and invariants (gradients sum to 0, shift invariance in the
+    upstream gradient, zero rows where T is NaN).
 
 The same checks run against deliberately broken copies of the oracle in
 ``test_oracle_mutants.py``: every plausible mistake must fail at least one.
@@ -352,6 +358,126 @@ def check_parameter_edges(lib) -> None:
     assert r.T[0] == 1.5 and r.iters[0] == 0 and r.flags[0] == 3
 
 
+# ------------------------------------------------------------------- backward
+def _pow2_floor(x: float) -> float:
+    return 2.0 ** math.floor(math.log2(x))
+
+
+def check_backward_finite_difference(lib) -> None:
+    """d(g . p)/dl_k by central differences through the whole forward (the
+    search runs again at l +- h e_k) against the backward at the forward's
+    T.  Agreement needs both the 1/T factor and T's zero derivative away
+    from the points where a bisection comparison flips; perturbations that
+    move T are skipped (they straddle such a point)."""
+    rng = np.random.default_rng(61)
+    cases = [(2, 1.0, BOUND), (5, 3.0, BOUND), (17, 2.0, 0.5),
+             (64, 3.0, BOUND), (9, 2.0, 1e30), (12, 2.0, -1.0)]
+    checked = 0
+    for C, sigma, bound in cases:
+        x = rng.normal(0.0, sigma, size=(2, C)).astype(np.float32)
+        g = rng.normal(0.0, 1.0, size=(2, C))
+        r0 = oracle.constrained_softmax(x, bound, T_MIN, T_MAX, ITERS,
+                                        threads=1, lib=lib)
+        grad = oracle.constrained_softmax_backward(r0.p, g, r0.T, lib=lib)
+        for b in range(2):
+            T0 = r0.T[b]
+            h = _pow2_floor(T0 * 2.0 ** -12)
+            ks = range(C) if C <= 17 else rng.choice(C, 12, replace=False)
+            for k in ks:
+                xp = x[b:b + 1].copy()
+                xm = x[b:b + 1].copy()
+                xp[0, k] = np.float32(float(x[b, k]) + h)
+                xm[0, k] = np.float32(float(x[b, k]) - h)
+                assert float(xp[0, k]) - float(x[b, k]) == h
+                assert float(x[b, k]) - float(xm[0, k]) == h
+                rp = oracle.constrained_softmax(xp, bound, T_MIN, T_MAX,
+                                                ITERS, threads=1, lib=lib)
+                rm = oracle.constrained_softmax(xm, bound, T_MIN, T_MAX,
+                                                ITERS, threads=1, lib=lib)
+                if not (rp.T[0] == T0 and rm.T[0] == T0):
+                    continue
+                fd = float(g[b] @ (rp.p[0] - rm.p[0])) / (2.0 * h)
+                scale = np.max(np.abs(g[b])) / T0
+                assert abs(fd - grad[b, k]) <= 1e-6 * scale, (C, b, k, fd,
+                                                              grad[b, k])
+                checked += 1
+    assert checked >= 90
+
+
+def check_backward_library_vjp(lib) -> None:
+    """At the forward's T, the backward is the vector-Jacobian product of
+    softmax(l / T) with T held fixed, which torch's autograd computes in
+    fp64 by its own softmax backward."""
+    import torch
+    rng = np.random.default_rng(67)
+    for C, bound in ((3, BOUND), (40, BOUND), (1000, 0.5), (257, -1.0),
+                     (33, 1e30)):
+        x = rng.normal(0.0, 2.5, size=(4, C)).astype(np.float32)
+        g = rng.normal(0.0, 1.0, size=(4, C))
+        r = oracle.constrained_softmax(x, bound, T_MIN, T_MAX, ITERS,
+                                       threads=1, lib=lib)
+        grad = oracle.constrained_softmax_backward(r.p, g, r.T, lib=lib)
+        l = torch.tensor(x, dtype=torch.float64, requires_grad=True)
+        T = torch.tensor(r.T, dtype=torch.float64)[:, None]
+        out = torch.softmax(l / T, dim=1)
+        out.backward(torch.tensor(g))
+        ref = l.grad.numpy()
+        scale = np.max(np.abs(g), axis=1, keepdims=True) / r.T[:, None]
+        assert np.all(np.abs(grad - ref) <= 1e-12 * scale), C
+
+
+def check_backward_jacobian_t1(lib) -> None:
+    """Where no search is needed (T = 1) the backward is J^T g with the
+    textbook softmax Jacobian J = diag(p) - p p^T, formed explicitly."""
+    rng = np.random.default_rng(71)
+    for C in (1, 2, 6, 50):
+        x = rng.normal(0.0, 1.0, size=(3, C)).astype(np.float32)
+        g = rng.normal(0.0, 1.0, size=(3, C))
+        r = oracle.constrained_softmax(x, 1e30, T_MIN, T_MAX, ITERS,
+                                       threads=1, lib=lib)
+        assert np.all(r.T == 1.0)
+        grad = oracle.constrained_softmax_backward(r.p, g, r.T, lib=lib)
+        for b in range(3):
+            p = scipy.special.softmax(x[b].astype(np.float64))
+            J = np.diag(p) - np.outer(p, p)
+            assert np.max(np.abs(grad[b] - J.T @ g[b])) < 1e-14
+
+
+def check_backward_invariants(lib) -> None:
+    """Gradients of a row sum to zero (the probabilities sum to 1), adding a
+    constant to the upstream gradient changes nothing, the map is linear in
+    the upstream gradient, a one-hot row has zero gradient, and rows whose T
+    is not a positive finite number (NaN: the forward zeroed them) get
+    zeros."""
+    rng = np.random.default_rng(73)
+    x = rng.normal(0.0, 3.0, size=(6, 300)).astype(np.float32)
+    r = oracle.constrained_softmax(x, BOUND, T_MIN, T_MAX, ITERS, threads=1,
+                                   lib=lib)
+    assert np.all(r.T < 1.0)
+    g = rng.normal(0.0, 1.0, size=x.shape)
+    grad = oracle.constrained_softmax_backward(r.p, g, r.T, lib=lib)
+    scale = np.max(np.abs(g)) / np.min(r.T)
+    assert np.max(np.abs(grad.sum(axis=1))) <= 1e-13 * scale
+    shifted = oracle.constrained_softmax_backward(r.p, g + 3.5, r.T, lib=lib)
+    assert np.max(np.abs(shifted - grad)) <= 1e-13 * scale
+    doubled = oracle.constrained_softmax_backward(r.p, 2.0 * g, r.T, lib=lib)
+    assert np.array_equal(doubled, 2.0 * grad)
+    onehot = np.zeros((1, 5))
+    onehot[0, 2] = 1.0
+    z = oracle.constrained_softmax_backward(onehot, g[:1, :5], [0.3], lib=lib)
+    assert np.all(z == 0.0)
+    T_bad = np.array([np.nan, -1.0, 0.0, np.inf, 0.5, 1.0])
+    xb = x.copy()
+    xb[0, 7] = np.nan
+    rb = oracle.constrained_softmax(xb, BOUND, T_MIN, T_MAX, ITERS, threads=1,
+                                    lib=lib)
+    assert math.isnan(rb.T[0])
+    T_bad[0] = rb.T[0]
+    gb = oracle.constrained_softmax_backward(rb.p, g, T_bad, lib=lib)
+    assert np.all(gb[:4] == 0.0)
+    assert np.all(np.isfinite(gb[4:])) and np.any(gb[4:] != 0.0)
+
+
 ALL_CHECKS = [
     check_two_class_entropy,
     check_spike_entropy,
@@ -364,4 +490,8 @@ ALL_CHECKS = [
     check_search_path,
     check_fault_policy,
     check_parameter_edges,
+    check_backward_finite_difference,
+    check_backward_library_vjp,
+    check_backward_jacobian_t1,
+    check_backward_invariants,
 ]

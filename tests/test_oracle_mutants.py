@@ -51,6 +51,21 @@ MUTANTS = [
      "else if (0) has_inf = 1;"),
     ("bound_strict", "if (entropy_at(l, C, 1.0) <= bound) {",
      "if (entropy_at(l, C, 1.0) < bound - 1e-3) {"),
+    ("backward_without_inv_T", "out[k] = pb[k] * (gb[k] - dot) / T[b];",
+     "out[k] = pb[k] * (gb[k] - dot);"),
+    ("backward_times_T", "out[k] = pb[k] * (gb[k] - dot) / T[b];",
+     "out[k] = pb[k] * (gb[k] - dot) * T[b];"),
+    ("backward_dot_sign", "out[k] = pb[k] * (gb[k] - dot) / T[b];",
+     "out[k] = pb[k] * (gb[k] + dot) / T[b];"),
+    ("backward_no_p_factor", "out[k] = pb[k] * (gb[k] - dot) / T[b];",
+     "out[k] = (gb[k] - dot) / T[b];"),
+    ("backward_dot_skips_first",
+     "for (int64_t i = 0; i < C; ++i) dot += gb[i] * pb[i];",
+     "for (int64_t i = 1; i < C; ++i) dot += gb[i] * pb[i];"),
+    ("backward_dot_of_p_with_itself", "dot += gb[i] * pb[i];",
+     "dot += pb[i] * pb[i];"),
+    ("backward_nan_rows_not_zeroed",
+     "if (!(T[b] > 0.0) || isinf(T[b])) {", "if (0) {"),
 ]
 
 
