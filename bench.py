@@ -77,6 +77,10 @@ def parse_args(argv=None):
                     help="time plain stream launches instead of one CUDA "
                          "graph of the K launches")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--op", choices=["forward", "backward"],
+                    default="forward",
+                    help="backward: time the gradient kernel, (1/T) p "
+                         "(g - <g, p>), on the workload's shape")
     return ap.parse_args(argv)
 
 
@@ -314,6 +318,59 @@ def workload_config(w: wl.Workload, l2: str) -> dict:
             "l2": l2}
 
 
+# ----------------------------------------------------------------- timing
+def time_launches(args, torch, launch, stream, dist, local) -> dict:
+    """Soak (clock samples start), then the K timed launches: once as plain
+    stream launches and once as one CUDA graph of the same K launches (host
+    launch overhead out of the device timing), each bracketed by a barrier
+    and a synchronize; CUDA events on the launching stream."""
+    sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ
+                           else 0)
+    sampler.start()
+    t_soak = time.time()
+    i = 0
+    while time.time() - t_soak < args.soak_s:
+        for _ in range(50):
+            launch(i)
+            i += 1
+        torch.cuda.synchronize()
+
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            cap = torch.cuda.current_stream().cuda_stream
+            for j in range(args.steps):
+                launch(j, cap)
+        graph.replay()
+        torch.cuda.synchronize()
+
+    def timed(use_graph: bool) -> float:
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e_a = torch.cuda.Event(enable_timing=True)
+        e_b = torch.cuda.Event(enable_timing=True)
+        e_a.record(stream)
+        if use_graph:
+            graph.replay()
+        else:
+            for j in range(args.steps):
+                launch(j)
+        e_b.record(stream)
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        return e_a.elapsed_time(e_b)
+
+    stream_ms = timed(False)
+    ms = timed(True) if graph is not None else stream_ms
+    t_end = time.time()
+    sampler.stop()
+    return {"stream_ms": stream_ms, "ms": ms, "graph": graph, "t0": t_soak,
+            "t1": t_end, "sampler": sampler}
+
+
 # ---------------------------------------------------------------- our arm
 def our_arm(args, w: wl.Workload) -> int:
     import torch
@@ -363,53 +420,9 @@ def our_arm(args, w: wl.Workload) -> int:
     plan = cs.plan(B, C, args.variant, args.param, args.threads,
                    args.strict)
 
-    sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ
-                           else 0)
-    sampler.start()
-    t_soak = time.time()
-    i = 0
-    while time.time() - t_soak < args.soak_s:
-        for _ in range(50):
-            launch(i)
-            i += 1
-        torch.cuda.synchronize()
-
-    # The K launches of the timed region, captured once into a CUDA graph
-    # so that host launch overhead (Python, ctypes) stays out of the
-    # device timing; the same K launches are also timed as plain stream
-    # launches and reported beside it.
-    graph = None
-    if not args.no_graph:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            cap = torch.cuda.current_stream().cuda_stream
-            for j in range(args.steps):
-                launch(j, cap)
-        graph.replay()
-        torch.cuda.synchronize()
-
-    def timed(use_graph: bool) -> float:
-        if dist is not None:
-            dist.barrier()
-        torch.cuda.synchronize()
-        e_a = torch.cuda.Event(enable_timing=True)
-        e_b = torch.cuda.Event(enable_timing=True)
-        e_a.record(stream)
-        if use_graph:
-            graph.replay()
-        else:
-            for j in range(args.steps):
-                launch(j)
-        e_b.record(stream)
-        torch.cuda.synchronize()
-        if dist is not None:
-            dist.barrier()
-        return e_a.elapsed_time(e_b)
-
-    stream_ms = timed(False)
-    local_ms = timed(True) if graph is not None else stream_ms
-    t_end = time.time()
-    sampler.stop()
+    tm = time_launches(args, torch, launch, stream, dist, local)
+    stream_ms, local_ms, graph = tm["stream_ms"], tm["ms"], tm["graph"]
+    t_soak, t_end, sampler = tm["t0"], tm["t1"], tm["sampler"]
     total_ms = reduce_max(dist, local_ms, dev)
     stream_ms_max = reduce_max(dist, stream_ms, dev)
     ms_per_step = total_ms / args.steps
@@ -529,12 +542,226 @@ def our_arm(args, w: wl.Workload) -> int:
     return 0
 
 
+# --------------------------------------------------------------- backward
+BACKWARD_METRIC = ("backward rows/s and effective HBM GB/s (% of roofline) "
+                   "of grad = (1/T) p (g - <g, p>)")
+
+
+def backward_inputs_cpu(w: wl.Workload, rows: np.ndarray):
+    """p (by the oracle's softmax at the seeded T), g, T for some rows."""
+    import oracle
+    x = wl.generate(w, rows)
+    g, T = wl.backward_inputs(w, rows)
+    p = np.zeros(x.shape, dtype=np.float32)
+    for i in range(x.shape[0]):
+        if np.isfinite(T[i]):
+            p[i] = oracle.softmax(x[i], float(T[i])).astype(np.float32)
+    return p, g, T
+
+
+def run_oracle_backward_sample(w: wl.Workload, seconds: float) -> dict:
+    """The oracle's backward, as it stands (one thread), on whole rows of
+    the workload (a cycled sample of at most 256 rows, inputs prepared
+    outside the timed loop) until `seconds` have passed."""
+    import oracle
+    oracle.load()
+    rows = np.arange(min(w.batch, max(1, (1 << 24) // w.num_classes), 256))
+    p, g, T = backward_inputs_cpu(w, rows)
+    done = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.constrained_softmax_backward(p, g, T)
+        done += rows.size
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"rows": done, "seconds": dt, "rows_per_s": done / dt,
+            "sample_rows": int(rows.size)}
+
+
+def backward_reference_arm(args, w: wl.Workload) -> int:
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.load()
+    n = min(w.batch, max(1, (1 << 22) // w.num_classes))
+    rows = np.arange(n)
+    p, g, T = backward_inputs_cpu(w, rows)
+    for _ in range(args.warmup):
+        oracle.constrained_softmax_backward(p, g, T)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.constrained_softmax_backward(p, g, T)
+    dt = time.perf_counter() - t0
+    value = n * args.steps / dt
+    line = {
+        "impl": "reference", "op": "backward", "metric": BACKWARD_METRIC,
+        "value": value, "unit": "rows/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w, "cpu"),
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1,
+                         "kind": "oracle",
+                         "sample": f"the first {n} rows per step "
+                                   f"({args.steps} steps)"},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def backward_arm(args, w: wl.Workload) -> int:
+    """One step = one backward launch over the whole workload: p (the
+    forward kernel's output on the workload's logits), its temperatures and
+    a seeded upstream gradient, all resident in HBM."""
+    import torch
+    import entropy_bounded_softmax_gb300 as cs
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+
+    x = wl.generate(w)
+    g, _ = wl.backward_inputs(w)
+    B, C = x.shape
+    elems = B * C
+    io_bytes = 12 * elems + 4 * B
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+    xs = torch.from_numpy(x).to(dev)
+    p0, t0 = cs.constrained_softmax(xs, w.entropy_bound, w.t_min, w.t_max,
+                                    w.max_iter, return_t=True)
+    del xs
+    g0 = torch.from_numpy(g).to(dev)
+    nbuf = max(1, math.ceil(3 * L2_BYTES / io_bytes)) if io_bytes < 3 * L2_BYTES else 1
+    ps = [p0] + [p0.clone() for _ in range(nbuf - 1)]
+    gs = [g0] + [g0.clone() for _ in range(nbuf - 1)]
+    outs = [torch.empty_like(p0) for _ in range(nbuf)]
+    l2_note = (f"rotating {nbuf} input/output sets "
+               f"({nbuf * io_bytes / 2**20:.0f} MiB > L2)") if nbuf > 1 else \
+        f"inputs larger than L2 ({io_bytes / 2**20:.0f} MiB)"
+    opts = cs.options(cs.VARIANTS[args.variant], args.param, args.threads, 0)
+
+    def launch(i: int, stream_ptr: int = sptr) -> None:
+        k = i % nbuf
+        st = cs.cs_constrained_softmax_backward_ex(
+            ps[k].data_ptr(), gs[k].data_ptr(), t0.data_ptr(),
+            outs[k].data_ptr(), B, C, opts, stream_ptr)
+        if st != 0:
+            raise RuntimeError(f"cs_constrained_softmax_backward failed: {st}")
+
+    for i in range(max(3, args.warmup)):
+        launch(i)
+    torch.cuda.synchronize()
+    plan = cs.plan_backward(B, C, args.variant, args.param, args.threads)
+    tm = time_launches(args, torch, launch, stream, dist, local)
+    total_ms = reduce_max(dist, tm["ms"], dev)
+    stream_ms_max = reduce_max(dist, tm["stream_ms"], dev)
+    ms_per_step = total_ms / args.steps
+    value = aggregate_rows_per_s(B, world, ms_per_step * 1e-3)
+
+    # End to end through the public API: pinned host p, g and T copied in,
+    # the call, the gradient copied out, all inside the events.
+    h_p = p0.cpu().pin_memory()
+    h_g = torch.from_numpy(g).pin_memory()
+    h_t = t0.cpu().pin_memory()
+    h_out = torch.empty((B, C), dtype=torch.float32).pin_memory()
+    d_p = torch.empty_like(p0)
+    d_g = torch.empty_like(p0)
+    d_t = torch.empty_like(t0)
+    d_out = torch.empty_like(p0)
+    e_steps = max(1, args.e2e_steps)
+
+    def e2e_step():
+        d_p.copy_(h_p, non_blocking=True)
+        d_g.copy_(h_g, non_blocking=True)
+        d_t.copy_(h_t, non_blocking=True)
+        cs.constrained_softmax_backward(d_p, d_g, d_t, out=d_out,
+                                        variant=args.variant,
+                                        param=args.param,
+                                        threads=args.threads)
+        h_out.copy_(d_out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(dist, e0.elapsed_time(e1), dev) / e_steps
+    e2e_value = aggregate_rows_per_s(B, world, e2e_ms * 1e-3)
+
+    line = None
+    if rank == 0:
+        peaks = measured_peaks()
+        t_kernel = ms_per_step * 1e-3
+        hbm_rate = io_bytes / t_kernel / 1e9
+        kernel = ("bwd_cluster_kernel" if plan["variant"] == 2
+                  else "bwd_rowgroup_kernel")
+        roof = {"bound": "hbm", "unit": "GB/s", "achieved": hbm_rate,
+                "peak": peaks["hbm_gbs"], "frac": hbm_rate / peaks["hbm_gbs"],
+                "traffic": None, "kernel": kernel,
+                "algorithmic_bytes": io_bytes,
+                "peak_source": f"{peaks['source']} copy bandwidth",
+                "roofline_us": io_bytes / (peaks["hbm_gbs"] * 1e9) * 1e6}
+        cpu = None
+        if not args.no_cpu_baseline:
+            s = run_oracle_backward_sample(w, args.cpu_seconds)
+            cpu = {"value": s["rows_per_s"], "unit": "rows/s", "cores": 1,
+                   "kind": "oracle",
+                   "sample": f"{s['rows']} rows ({s['sample_rows']} distinct "
+                             f"rows of the workload, cycled) in "
+                             f"{s['seconds']:.1f} s on one thread"}
+        line = {
+            "op": "backward", "metric": BACKWARD_METRIC, "value": value,
+            "unit": "rows/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "launch": "cuda_graph" if tm["graph"] is not None else "stream",
+            "ms_per_step_stream_launches": stream_ms_max / args.steps,
+            "hbm_gbs": hbm_rate, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": dict(workload_config(w, l2_note),
+                           parallelism=f"replicas x{world}",
+                           variant=args.variant, plan=plan,
+                           upstream_gradient="N(0,1) fp32, seeded"),
+            "roofline": roof, "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "rows/s",
+                    "ms_per_step": e2e_ms,
+                    "h2d_bytes_per_step": 8 * elems + 4 * B,
+                    "d2h_bytes_per_step": 4 * elems},
+            "gpu_launches": args.steps,
+            "clocks": tm["sampler"].summary(tm["t0"], tm["t1"]),
+        }
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None) -> int:
     args = parse_args(argv)
     w = find_workload(args.workload)
     if args.batch:
         w = w.with_(batch=min(args.batch, w.batch),
                     name=f"{w.name}[:{min(args.batch, w.batch)}]")
+    if args.op == "backward":
+        if args.impl == "reference":
+            return backward_reference_arm(args, w)
+        return backward_arm(args, w)
     if args.impl == "reference":
         return reference_arm(args, w)
     return our_arm(args, w)

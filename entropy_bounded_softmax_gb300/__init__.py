@@ -3,7 +3,10 @@
 For each row of a [batch, num_classes] fp32 logit matrix: softmax and its
 entropy; if the entropy exceeds ``entropy_bound`` the temperature is bisected
 on [t_min, min(1, t_max)] for ``max_iter`` steps and softmax(l / T) is
-written ("BURT-IMMA CUDA Kernel API Reference", section 2.1).
+written ("BURT-IMMA CUDA Kernel API Reference", section 2.1).  The backward
+(section 6.3, with the 1/T of softmax(l / T) restored) gives the gradient
+with respect to the logits; :class:`ConstrainedSoftmaxFunction` joins the two
+for autograd.
 
 PyTorch supplies device memory and the current stream; the computation runs
 in the hand-written CUDA kernels of ``libcsoftmax.so`` behind a C ABI
@@ -13,19 +16,25 @@ raise if the library is missing or the tensors are not on a CUDA device.
 from __future__ import annotations
 
 from . import _lib
-from ._lib import (CONSTANTS, cs_check_args, cs_constrained_softmax,
-                   cs_constrained_softmax_ex, cs_get_error, cs_plan_host,
-                   cs_plan_launch, cs_probe_ex2, cs_probe_ex2_sink_floats,
-                   cs_status_string, cs_test_wait_timeout, cs_version,
-                   options)
+from ._lib import (CONSTANTS, cs_check_args, cs_check_backward_args,
+                   cs_constrained_softmax, cs_constrained_softmax_backward,
+                   cs_constrained_softmax_backward_ex,
+                   cs_constrained_softmax_ex, cs_get_error,
+                   cs_plan_backward_host, cs_plan_backward_launch,
+                   cs_plan_host, cs_plan_launch, cs_probe_ex2,
+                   cs_probe_ex2_sink_floats, cs_status_string,
+                   cs_test_wait_timeout, cs_version, options)
 
 __all__ = [
-    "constrained_softmax", "get_error", "plan", "version", "CsError",
-    "ERROR_BITS", "VARIANTS", "options", "cs_constrained_softmax",
-    "cs_constrained_softmax_ex", "cs_get_error", "cs_plan_launch",
-    "cs_plan_host", "cs_check_args", "cs_probe_ex2",
-    "cs_probe_ex2_sink_floats", "cs_test_wait_timeout", "cs_version",
-    "cs_status_string",
+    "constrained_softmax", "constrained_softmax_backward",
+    "ConstrainedSoftmaxFunction", "get_error", "plan", "plan_backward",
+    "version", "CsError", "ERROR_BITS", "VARIANTS", "options",
+    "cs_constrained_softmax", "cs_constrained_softmax_ex",
+    "cs_constrained_softmax_backward", "cs_constrained_softmax_backward_ex",
+    "cs_get_error", "cs_plan_launch", "cs_plan_host",
+    "cs_plan_backward_launch", "cs_plan_backward_host", "cs_check_args",
+    "cs_check_backward_args", "cs_probe_ex2", "cs_probe_ex2_sink_floats",
+    "cs_test_wait_timeout", "cs_version", "cs_status_string",
 ]
 
 # Defaults of section 2.1's signature.
@@ -109,6 +118,94 @@ def constrained_softmax(logits, entropy_bound: float = DEFAULT_ENTROPY_BOUND,
     return (out, t_out) if return_t else out
 
 
+def _check_like(name, x, ref) -> None:
+    import torch
+    if (not isinstance(x, torch.Tensor) or x.shape != ref.shape
+            or x.dtype != torch.float32 or x.device != ref.device
+            or not x.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous float32 tensor shaped "
+                         "like probs on the same device")
+
+
+def constrained_softmax_backward(probs, grad_output, t, out=None,
+                                 variant: str = "auto", param: int = 0,
+                                 threads: int = 0):
+    """Gradient with respect to the logits: (1/T) p (g - <g, p>) per row.
+
+    ``probs`` and ``t`` are the forward's output and temperatures
+    (``constrained_softmax(..., return_t=True)``), ``grad_output`` the
+    upstream gradient; all on one CUDA device, fp32, contiguous.  Rows whose
+    T is NaN (rows the forward zeroed) get zeros.  ``out`` may be given, and
+    may be ``probs`` or ``grad_output`` itself (in place).  Asynchronous on
+    the current stream.
+    """
+    import torch
+    if not isinstance(probs, torch.Tensor) or probs.device.type != "cuda":
+        raise ValueError("probs must be a CUDA tensor")
+    if probs.dim() != 2:
+        raise ValueError("probs must be 2-D [batch, num_classes]")
+    _check_like("probs", probs, probs)
+    _check_like("grad_output", grad_output, probs)
+    batch, num_classes = probs.shape
+    if (not isinstance(t, torch.Tensor) or t.shape != (batch,)
+            or t.dtype != torch.float32 or t.device != probs.device
+            or not t.is_contiguous()):
+        raise ValueError("t must be a contiguous float32 [batch] tensor on "
+                         "probs' device")
+    if out is None:
+        out = torch.empty_like(probs)
+    else:
+        _check_like("out", out, probs)
+    with torch.cuda.device(probs.device):
+        st = cs_constrained_softmax_backward_ex(
+            probs.data_ptr(), grad_output.data_ptr(), t.data_ptr(),
+            out.data_ptr(), batch, num_classes,
+            options(VARIANTS[variant], param, threads, 0),
+            _stream_handle(probs.device))
+    if st != 0:
+        raise CsError(st, "cs_constrained_softmax_backward")
+    return out
+
+
+def _autograd_function():
+    import torch
+
+    class ConstrainedSoftmaxFunction(torch.autograd.Function):
+        """Autograd wrapper of section 6.3: forward = constrained_softmax,
+        backward = constrained_softmax_backward at the forward's
+        temperatures.  ``apply(logits, entropy_bound, t_min, t_max,
+        max_iter)``; only the logits receive a gradient."""
+
+        @staticmethod
+        def forward(ctx, logits, entropy_bound=DEFAULT_ENTROPY_BOUND,
+                    t_min=DEFAULT_T_MIN, t_max=DEFAULT_T_MAX,
+                    max_iter=DEFAULT_MAX_ITER):
+            out, t = constrained_softmax(logits.contiguous(), entropy_bound,
+                                         t_min, t_max, max_iter,
+                                         return_t=True)
+            ctx.save_for_backward(out, t)
+            return out
+
+        @staticmethod
+        def backward(ctx, grad_output):
+            out, t = ctx.saved_tensors
+            grad = constrained_softmax_backward(out, grad_output.contiguous(),
+                                                t)
+            return grad, None, None, None, None
+
+    return ConstrainedSoftmaxFunction
+
+
+def __getattr__(name):
+    # The autograd class needs torch; it is built on first use so that the
+    # package imports without torch (the C ABI tests run without it).
+    if name == "ConstrainedSoftmaxFunction":
+        cls = _autograd_function()
+        globals()[name] = cls
+        return cls
+    raise AttributeError(name)
+
+
 def get_error(device=None) -> set[str]:
     """Synchronise the current stream, read and clear the device error word;
     returns the names of the conditions seen since the last call."""
@@ -130,6 +227,17 @@ def plan(batch: int, num_classes: int, variant: str = "auto",
                                    int(strict)))
     if st != 0:
         raise CsError(st, "cs_plan_launch")
+    return p.as_dict()
+
+
+def plan_backward(batch: int, num_classes: int, variant: str = "auto",
+                  param: int = 0, threads: int = 0) -> dict:
+    """The backward's launch plan for this shape on the current device."""
+    st, p = cs_plan_backward_launch(batch, num_classes,
+                                    options(VARIANTS[variant], param,
+                                            threads, 0))
+    if st != 0:
+        raise CsError(st, "cs_plan_backward_launch")
     return p.as_dict()
 
 

@@ -39,6 +39,7 @@ class cs_plan(ctypes.Structure):
         ("smem_bytes", ctypes.c_int32),
         ("ctas_per_sm", ctypes.c_int32),
         ("grid_ctas", ctypes.c_int64),
+        ("staged_tensors", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:
@@ -77,6 +78,18 @@ _SIGNATURES = {
                             _I32, _I32, _I32, ctypes.POINTER(cs_plan)]),
     "cs_check_args": (_I32, [_VP, _VP, _I64, _I32, _F32, _F32, _F32, _I32,
                              _VP]),
+    "cs_constrained_softmax_backward": (_I32, [_VP, _VP, _VP, _VP, _I64,
+                                               _I32, _VP]),
+    "cs_constrained_softmax_backward_ex": (_I32, [_VP, _VP, _VP, _VP, _I64,
+                                                  _I32,
+                                                  ctypes.POINTER(cs_options),
+                                                  _VP]),
+    "cs_plan_backward_launch": (_I32, [_I64, _I32, ctypes.POINTER(cs_options),
+                                       ctypes.POINTER(cs_plan)]),
+    "cs_plan_backward_host": (_I32, [_I64, _I32, ctypes.POINTER(cs_options),
+                                     _I32, _I32, _I32, _I32,
+                                     ctypes.POINTER(cs_plan)]),
+    "cs_check_backward_args": (_I32, [_VP, _VP, _VP, _VP, _I64, _I32]),
     "cs_probe_ex2": (_I32, [_VP, _I32, ctypes.POINTER(_I64), _VP]),
     "cs_probe_ex2_sink_floats": (_I32, []),
     "cs_test_wait_timeout": (_I32, [_I64, _VP]),
@@ -162,6 +175,41 @@ def cs_check_args(logits, out, batch, num_classes, entropy_bound, t_min,
                   t_max, max_iter, t_out) -> int:
     return load().cs_check_args(logits, out, batch, num_classes,
                                 entropy_bound, t_min, t_max, max_iter, t_out)
+
+
+def cs_constrained_softmax_backward(probs, grad_out, t, grad_in, batch,
+                                    num_classes, stream) -> int:
+    return load().cs_constrained_softmax_backward(probs, grad_out, t, grad_in,
+                                                  batch, num_classes, stream)
+
+
+def cs_constrained_softmax_backward_ex(probs, grad_out, t, grad_in, batch,
+                                       num_classes, opt, stream) -> int:
+    return load().cs_constrained_softmax_backward_ex(
+        probs, grad_out, t, grad_in, batch, num_classes, _opt_ref(opt), stream)
+
+
+def cs_plan_backward_launch(batch, num_classes, opt=None):
+    p = cs_plan()
+    st = load().cs_plan_backward_launch(batch, num_classes, _opt_ref(opt),
+                                        ctypes.byref(p))
+    return st, p
+
+
+def cs_plan_backward_host(batch, num_classes, opt, sm_count,
+                          smem_per_block_optin, smem_per_sm, max_cluster):
+    p = cs_plan()
+    st = load().cs_plan_backward_host(batch, num_classes, _opt_ref(opt),
+                                      sm_count, smem_per_block_optin,
+                                      smem_per_sm, max_cluster,
+                                      ctypes.byref(p))
+    return st, p
+
+
+def cs_check_backward_args(probs, grad_out, t, grad_in, batch,
+                           num_classes) -> int:
+    return load().cs_check_backward_args(probs, grad_out, t, grad_in, batch,
+                                         num_classes)
 
 
 def cs_probe_ex2(sink, iters, stream) -> tuple[int, int]:

@@ -19,7 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIBRARY = os.path.join(PKG, "libcsoftmax.so")
 
-SOURCES = ["cs_api.cu", "k_cluster.cu", "k_rowgroup.cu", "k_aux.cu"]
+SOURCES = ["cs_api.cu", "k_cluster.cu", "k_rowgroup.cu", "k_backward.cu",
+           "k_aux.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-I", INCLUDE, "-I", CSRC]

@@ -156,6 +156,7 @@ bool cluster_geometry(int64_t batch, int32_t C, int n, int threads_req,
     p->slice_len = static_cast<int32_t>(L);
     p->threads_per_cta = threads;
     p->smem_bytes = static_cast<int32_t>(smem);
+    p->staged_tensors = 1;
     return true;
 }
 
@@ -198,6 +199,116 @@ cs_status plan_cluster(int64_t batch, int32_t C, const cs_options& o,
                               smem_optin, p))
             return CS_ERR_OOM;
     }
+    const int n = p->cluster_size;
+    const int by_smem = static_cast<int>(smem_per_sm / (p->smem_bytes + 1024));
+    const int by_threads = 2048 / p->threads_per_cta;
+    p->ctas_per_sm = by_smem < by_threads ? by_smem : by_threads;
+    int64_t rows = batch;
+    const int64_t max_rows = kMaxGridX / n;
+    if (rows > max_rows) rows = max_rows;
+    p->grid_ctas = rows * n;
+    return CS_OK;
+}
+
+// ------------------------------------------------------------------ backward
+// Row-group backward: G lanes per row, the smallest power of two that leaves
+// at most four float4s of p (and of g) per lane; float4s counted for the
+// worst alignment of a row start (pad 3), since rows of a num_classes that
+// is not a multiple of 4 start at every alignment.
+cs_status plan_backward_rowgroup(int64_t batch, int32_t C, int32_t param,
+                                 cs_plan* p) {
+    const int64_t q = (static_cast<int64_t>(C) + 6) / 4;
+    int G = 0;
+    if (param == 0) {
+        for (int g = 1; g <= kRowgroupMaxLanes; g <<= 1) {
+            if (ceil_div(q, g) <= kAutoRowgroupE4) {
+                G = g;
+                break;
+            }
+        }
+        if (G == 0) G = kRowgroupMaxLanes;
+    } else {
+        if (param < 1 || param > kRowgroupMaxLanes || (param & (param - 1)))
+            return CS_ERR_INVALID_ARG;
+        G = param;
+    }
+    const int e4 = next_pow2(ceil_div(q, G));
+    if (e4 > kRowgroupMaxE4) return CS_ERR_OOM;
+    const int64_t blocks = ceil_div(batch * G, cs::kBwdGroupThreads);
+    if (blocks > kMaxGridX) return CS_ERR_DIM_MISMATCH;
+    *p = cs_plan{};
+    p->variant = CS_VARIANT_ROWGROUP;
+    p->lanes_per_row = G;
+    p->elems_per_lane = 4 * e4;
+    p->threads_per_cta = cs::kBwdGroupThreads;
+    // Registers bound residency: 2 x 4 e4 for the row plus about 28
+    // (ptxas: 32, 38, 60 and 90 for e4 = 1, 2, 4, 8).
+    int regs = ((8 * e4 + 28 + 7) / 8) * 8;
+    if (regs < 32) regs = 32;
+    p->ctas_per_sm = 65536 / (regs * cs::kBwdGroupThreads);
+    if (p->ctas_per_sm > 2048 / cs::kBwdGroupThreads)
+        p->ctas_per_sm = 2048 / cs::kBwdGroupThreads;
+    p->grid_ctas = blocks;
+    return CS_OK;
+}
+
+// Cluster backward geometry for n CTAs per row: p and g staged when both
+// fit, else p alone (stage_both = false); false if neither fits.
+bool backward_geometry(int32_t C, int n, int threads_req, int smem_optin,
+                       bool stage_both, cs_plan* p) {
+    const int64_t L = ceil_div(ceil_div(C, n), 4) * 4;
+    const int64_t smem = cs::backward_smem_bytes(L, stage_both);
+    if (smem > smem_optin) return false;
+    int threads = threads_req;
+    if (threads == 0) {
+        // About eight float4s of each staged tensor per thread.
+        int64_t t = ceil_div(ceil_div(L, 4), 8);
+        t = ceil_div(t, 32) * 32;
+        if (t < 64) t = 64;
+        if (t > cs::kBwdMaxThreads) t = cs::kBwdMaxThreads;
+        threads = static_cast<int>(t);
+    }
+    p->cluster_size = n;
+    p->slice_len = static_cast<int32_t>(L);
+    p->threads_per_cta = threads;
+    p->smem_bytes = static_cast<int32_t>(smem);
+    p->staged_tensors = stage_both ? 2 : 1;
+    return true;
+}
+
+cs_status plan_backward_cluster(int64_t batch, int32_t C, const cs_options& o,
+                                int sm_count, int smem_optin, int smem_per_sm,
+                                int max_cluster, cs_plan* p) {
+    if (o.threads != 0 &&
+        (o.threads < 64 || o.threads > cs::kBwdMaxThreads || o.threads % 32))
+        return CS_ERR_INVALID_ARG;
+    *p = cs_plan{};
+    p->variant = CS_VARIANT_CLUSTER;
+    bool ok = false;
+    if (o.param == 0) {
+        // Smallest cluster whose slices are at most kBwdTargetSlice classes,
+        // widened to about one CTA per SM for few rows while slices keep
+        // kMinWideSlice classes.
+        int n0 = static_cast<int>(ceil_div(C, cs::kBwdTargetSlice));
+        if (n0 > max_cluster) n0 = max_cluster;
+        if (n0 < 1) n0 = 1;
+        const int64_t rows = batch > 0 ? batch : 1;
+        int64_t widen = ceil_div(sm_count, rows);
+        if (widen > C / kMinWideSlice) widen = C / kMinWideSlice;
+        if (widen > max_cluster) widen = max_cluster;
+        if (widen > n0) n0 = static_cast<int>(widen);
+        for (int c = n0; c <= max_cluster && !ok; ++c)
+            ok = backward_geometry(C, c, o.threads, smem_optin, true, p);
+        if (!ok)
+            ok = backward_geometry(C, max_cluster, o.threads, smem_optin,
+                                   false, p);
+    } else {
+        if (o.param < 1 || o.param > cs::kMaxCluster) return CS_ERR_INVALID_ARG;
+        if (o.param > max_cluster) return CS_ERR_INVALID_ARG;
+        ok = backward_geometry(C, o.param, o.threads, smem_optin, true, p) ||
+             backward_geometry(C, o.param, o.threads, smem_optin, false, p);
+    }
+    if (!ok) return CS_ERR_OOM;
     const int n = p->cluster_size;
     const int by_smem = static_cast<int>(smem_per_sm / (p->smem_bytes + 1024));
     const int by_threads = 2048 / p->threads_per_cta;
@@ -343,6 +454,116 @@ cs_status cs_get_error(int32_t* code_mask, void* stream) {
     }
     *code_mask = static_cast<int32_t>(h);
     return CS_OK;
+}
+
+cs_status cs_check_backward_args(const float* probs, const float* grad_out,
+                                 const float* t, const float* grad_in,
+                                 int64_t batch, int32_t num_classes) {
+    if (batch < 0 || num_classes < 1) return CS_ERR_DIM_MISMATCH;
+    if (num_classes > CS_MAX_NUM_CLASSES) return CS_ERR_OOM;
+    if (batch > INT64_MAX / 4 / num_classes) return CS_ERR_DIM_MISMATCH;
+    if (batch == 0) return CS_OK;
+    if (!probs || !grad_out || !t || !grad_in) return CS_ERR_INVALID_ARG;
+    const int64_t bytes = batch * num_classes * 4;
+    if (grad_in != probs && ranges_overlap(grad_in, bytes, probs, bytes))
+        return CS_ERR_INVALID_ARG;
+    if (grad_in != grad_out && ranges_overlap(grad_in, bytes, grad_out, bytes))
+        return CS_ERR_INVALID_ARG;
+    if (ranges_overlap(t, batch * 4, grad_in, bytes)) return CS_ERR_INVALID_ARG;
+    return CS_OK;
+}
+
+cs_status cs_plan_backward_host(int64_t batch, int32_t num_classes,
+                                const cs_options* options, int32_t sm_count,
+                                int32_t smem_per_block_optin,
+                                int32_t smem_per_sm, int32_t max_cluster,
+                                cs_plan* plan) {
+    if (!plan) return CS_ERR_INVALID_ARG;
+    if (batch < 0 || num_classes < 1) return CS_ERR_DIM_MISMATCH;
+    if (num_classes > CS_MAX_NUM_CLASSES) return CS_ERR_OOM;
+    if (sm_count < 1 || smem_per_block_optin < 1 || smem_per_sm < 1 ||
+        max_cluster < 1)
+        return CS_ERR_INVALID_ARG;
+    if (max_cluster > cs::kMaxCluster) max_cluster = cs::kMaxCluster;
+    cs_options o = options ? *options : cs_options{};
+    if (o.strict != 0) return CS_ERR_INVALID_ARG;
+    if (o.variant == CS_VARIANT_AUTO) {
+        if (o.param != 0 || o.threads != 0) return CS_ERR_INVALID_ARG;
+        o.variant = num_classes <= kAutoRowgroupMaxClasses ? CS_VARIANT_ROWGROUP
+                                                           : CS_VARIANT_CLUSTER;
+    }
+    if (o.variant == CS_VARIANT_ROWGROUP) {
+        if (o.threads != 0) return CS_ERR_INVALID_ARG;
+        return plan_backward_rowgroup(batch, num_classes, o.param, plan);
+    }
+    if (o.variant == CS_VARIANT_CLUSTER)
+        return plan_backward_cluster(batch, num_classes, o, sm_count,
+                                     smem_per_block_optin, smem_per_sm,
+                                     max_cluster, plan);
+    return CS_ERR_INVALID_ARG;
+}
+
+cs_status cs_plan_backward_launch(int64_t batch, int32_t num_classes,
+                                  const cs_options* options, cs_plan* plan) {
+    DeviceInfo* d = nullptr;
+    const cs_status st = device_info(&d);
+    if (st != CS_OK) return st;
+    return cs_plan_backward_host(batch, num_classes, options, d->sm_count,
+                                 d->smem_optin, d->smem_per_sm,
+                                 d->max_cluster, plan);
+}
+
+cs_status cs_constrained_softmax_backward_ex(const float* probs,
+                                             const float* grad_out,
+                                             const float* t, float* grad_in,
+                                             int64_t batch,
+                                             int32_t num_classes,
+                                             const cs_options* options,
+                                             void* stream) {
+    cs_status st = cs_check_backward_args(probs, grad_out, t, grad_in, batch,
+                                          num_classes);
+    if (st != CS_OK) return st;
+    if (batch == 0) return CS_OK;
+    DeviceInfo* d = nullptr;
+    st = device_info(&d);
+    if (st != CS_OK) return st;
+    cs_plan p;
+    st = cs_plan_backward_host(batch, num_classes, options, d->sm_count,
+                               d->smem_optin, d->smem_per_sm, d->max_cluster,
+                               &p);
+    if (st != CS_OK) return st;
+    cs::BwdTask task;
+    task.probs = probs;
+    task.grad_out = grad_out;
+    task.t = t;
+    task.grad_in = grad_in;
+    task.batch = batch;
+    task.num_classes = num_classes;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (p.variant == CS_VARIANT_ROWGROUP) {
+        e = cs::launch_backward_rowgroup(task, p.lanes_per_row,
+                                         p.elems_per_lane, s);
+    } else {
+        e = cs::launch_backward_cluster(task, p.cluster_size, p.slice_len,
+                                        p.threads_per_cta, p.smem_bytes,
+                                        p.staged_tensors == 2, p.grid_ctas, s);
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return CS_ERR_CUDA;
+    }
+    return CS_OK;
+}
+
+cs_status cs_constrained_softmax_backward(const float* probs,
+                                          const float* grad_out,
+                                          const float* t, float* grad_in,
+                                          int64_t batch, int32_t num_classes,
+                                          void* stream) {
+    return cs_constrained_softmax_backward_ex(probs, grad_out, t, grad_in,
+                                              batch, num_classes, nullptr,
+                                              stream);
 }
 
 int32_t cs_probe_ex2_sink_floats(void) {

@@ -96,6 +96,38 @@ inline int cluster_threads_for(int64_t slice_len, int64_t ctas,
     return static_cast<int>(t);
 }
 
+// One backward launch: grad_in = (1/T) p (g - <g, p>) for every row.
+struct BwdTask {
+    const float* probs;     // [batch, C] the forward's output p
+    const float* grad_out;  // [batch, C] upstream gradient g
+    const float* t;         // [batch] the forward's temperatures
+    float* grad_in;         // [batch, C]
+    int64_t batch;
+    int32_t num_classes;
+};
+
+// Backward geometry.  Row-group CTAs of 256 threads; cluster CTAs of up to
+// 512 threads whose dynamic shared memory is a 512-byte header (the
+// exchange slots) followed by the slice of p and, when STAGE_G, of g.
+constexpr int kBwdGroupThreads = 256;
+constexpr int kBwdMaxThreads = 512;
+constexpr int kBwdSmemHeader = 512;
+// Classes per CTA the automatic backward plan aims for: 64 KB of p and g,
+// so that three CTAs share an SM and one's reduction overlaps the others'
+// loads and stores.
+constexpr int64_t kBwdTargetSlice = 8192;
+
+inline int64_t backward_smem_bytes(int64_t slice_len, bool stage_g) {
+    return kBwdSmemHeader + (slice_len / 4 + 1) * 16 * (stage_g ? 2 : 1);
+}
+
+cudaError_t launch_backward_rowgroup(const BwdTask& task, int lanes_per_row,
+                                     int elems_per_lane, cudaStream_t stream);
+cudaError_t launch_backward_cluster(const BwdTask& task, int cluster_size,
+                                    int slice_len, int threads, int smem_bytes,
+                                    bool stage_g, int64_t grid_ctas,
+                                    cudaStream_t stream);
+
 cudaError_t launch_rowgroup(const RowTask& task, int lanes_per_row,
                             int elems_per_lane, cudaStream_t stream);
 cudaError_t launch_cluster(const RowTask& task, int cluster_size,

@@ -155,3 +155,39 @@ def sample_rows(w: Workload, n: int, seed: int = 7) -> np.ndarray:
     picks = set(rng.choice(w.batch, size=n, replace=False).tolist())
     picks.update({0, w.batch - 1})
     return np.array(sorted(picks), dtype=np.int64)
+
+
+# Backward inputs.  The backward takes the forward's output p, its per-row
+# temperature T and an upstream gradient g.  g and T are drawn here; p is
+# then softmax(l / T) of the workload's logits, computed by whichever side
+# needs it (the oracle in the tests, the forward kernel in the benchmark).
+BACKWARD_T1_EVERY = 16      # rows r with r % 16 == 3 have T = 1 (no search)
+BACKWARD_NAN_EVERY = 64     # rows r with r % 64 == 5 have T = NaN (a row the
+                            # forward zeroed)
+
+
+def backward_inputs(w: Workload, rows=None) -> tuple[np.ndarray, np.ndarray]:
+    """(g, T) for the workload's rows (or ``rows``): g ~ N(0, 1) fp32 of the
+    logits' shape; T ~ U(t_min, 1) fp32 per row, except T = 1 on every 16th
+    row and NaN on every 64th.  Block k of seed s draws from
+    ``Generator(PCG64([s, k, 2]))``: g's normals, then the block's T."""
+    rows_arr = (np.arange(w.batch) if rows is None
+                else np.asarray(rows, dtype=np.int64).reshape(-1))
+    if rows_arr.size and (rows_arr.min() < 0 or rows_arr.max() >= w.batch):
+        raise IndexError("row index out of range")
+    C = w.num_classes
+    g = np.empty((rows_arr.size, C), dtype=np.float32)
+    T = np.empty(rows_arr.size, dtype=np.float32)
+    for blk in np.unique(rows_arr // BLOCK_ROWS):
+        r0 = int(blk) * BLOCK_ROWS
+        n = min(w.batch, r0 + BLOCK_ROWS) - r0
+        rng = np.random.Generator(np.random.PCG64([w.seed, int(blk), 2]))
+        gb = rng.standard_normal((n, C), dtype=np.float32)
+        tb = rng.uniform(w.t_min, 1.0, size=n).astype(np.float32)
+        r = np.arange(r0, r0 + n)
+        tb[r % BACKWARD_T1_EVERY == 3] = 1.0
+        tb[r % BACKWARD_NAN_EVERY == 5] = np.nan
+        sel = np.flatnonzero(rows_arr // BLOCK_ROWS == blk)
+        g[sel] = gb[rows_arr[sel] - r0]
+        T[sel] = tb[rows_arr[sel] - r0]
+    return g, T

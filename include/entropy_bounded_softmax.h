@@ -95,6 +95,10 @@ typedef struct cs_plan {
     int32_t smem_bytes;      /* dynamic shared memory per CTA               */
     int32_t ctas_per_sm;     /* CTAs resident per SM by the plan's limits   */
     int64_t grid_ctas;       /* CTAs in the launch                          */
+    int32_t staged_tensors;  /* cluster: row tensors a CTA keeps in shared
+                                memory (forward: 1, the logits; backward:
+                                2, p and grad_out, or 1, p alone, with
+                                grad_out read again); rowgroup: 0          */
 } cs_plan;
 
 /*
@@ -177,6 +181,83 @@ cs_status cs_plan_host(int64_t batch, int32_t num_classes,
 cs_status cs_check_args(const float* logits, const float* out, int64_t batch,
                         int32_t num_classes, float entropy_bound, float t_min,
                         float t_max, int32_t max_iter, const float* t_out);
+
+/*
+ * cs_constrained_softmax_backward -- gradient of a loss with respect to the
+ * logits of cs_constrained_softmax.  "BURT-IMMA CUDA Kernel API Reference",
+ * section 6.3 (PyTorch Custom Op Integration), gives the backward as the
+ * softmax Jacobian product p * (g - <g, p>); the forward's output is
+ * softmax(l / T), so every derivative carries 1/T, which that section leaves
+ * out and this function restores.  Per row:
+ *
+ *     grad_in = (1/T) p * (grad_out - <grad_out, p>)
+ *
+ * T is the grid point the search settles on, piecewise constant in the
+ * logits: it adds no term of its own, and this is the exact gradient
+ * wherever one exists (everywhere except where a search comparison flips).
+ *
+ * probs     device pointer, [batch, num_classes] fp32, row-major: the
+ *           forward's out.  Read only.
+ * grad_out  device pointer, [batch, num_classes] fp32: dLoss/dout.  Read
+ *           only; may overlap probs.
+ * t         device pointer, [batch] fp32: the forward's t_out.  A row whose
+ *           T is not a positive finite number gets an all-zero gradient
+ *           (the forward reports NaN for the rows section 5.3 zeroes, whose
+ *           output does not depend on the logits).
+ * grad_in   device pointer, [batch, num_classes] fp32: dLoss/dlogits,
+ *           written completely.  May be the same pointer as probs or
+ *           grad_out (computed in place); any other overlap with probs,
+ *           grad_out or t returns CS_ERR_INVALID_ARG.
+ * batch     rows; 0 is a no-op that returns CS_OK.
+ * num_classes  classes per row, 1..CS_MAX_NUM_CLASSES.
+ * stream    a cudaStream_t (NULL = the legacy default stream).
+ *
+ * Any 4-byte alignment is accepted; rows whose four tensors share 16-byte
+ * alignment take 128-bit loads and stores.  Arithmetic is fp32: the dot
+ * product is summed in fp32 (per-thread chains, then shuffle and slot
+ * trees), 1/T is the correctly rounded reciprocal.  NaN or Inf in probs or
+ * grad_out propagates by IEEE arithmetic through the row's dot product.
+ * Ownership: the caller owns every buffer; nothing is allocated.
+ * Execution: asynchronous on `stream`; never synchronises.
+ * Errors: argument problems return CS_ERR_DIM_MISMATCH / CS_ERR_INVALID_ARG /
+ * CS_ERR_OOM before anything is launched; a failed launch returns
+ * CS_ERR_CUDA.  Nothing is written to the device error word.
+ */
+cs_status cs_constrained_softmax_backward(const float* probs,
+                                          const float* grad_out,
+                                          const float* t, float* grad_in,
+                                          int64_t batch, int32_t num_classes,
+                                          void* stream);
+
+/*
+ * Same with launch options (NULL = automatic): variant CS_VARIANT_ROWGROUP
+ * (param = lanes per row, 1..32, a power of two; the row must fit 32
+ * classes per lane, else CS_ERR_OOM) or CS_VARIANT_CLUSTER (param = CTAs per
+ * row, 1..16; threads as for the forward).  strict must be 0.
+ */
+cs_status cs_constrained_softmax_backward_ex(const float* probs,
+                                             const float* grad_out,
+                                             const float* t, float* grad_in,
+                                             int64_t batch,
+                                             int32_t num_classes,
+                                             const cs_options* options,
+                                             void* stream);
+
+/* The backward's launch plan on the current device (no launch), and the
+ * same planning on given device limits, host-only (as cs_plan_host). */
+cs_status cs_plan_backward_launch(int64_t batch, int32_t num_classes,
+                                  const cs_options* options, cs_plan* plan);
+cs_status cs_plan_backward_host(int64_t batch, int32_t num_classes,
+                                const cs_options* options, int32_t sm_count,
+                                int32_t smem_per_block_optin,
+                                int32_t smem_per_sm, int32_t max_cluster,
+                                cs_plan* plan);
+
+/* Host-only argument check of cs_constrained_softmax_backward (no CUDA
+ * call). */
+cs_status cs_check_backward_args(const float* probs, const float* grad_out,
+                                 const float* t, const float* grad_in,
+                                 int64_t batch, int32_t num_classes);
 
 /*
  * Throughput probe of the ex2 unit, the unit this operation is bound by.

@@ -179,3 +179,108 @@ def test_strict_option_is_checked():
     assert st == 0 and p["threads_per_cta"] == 512 and p["cluster_size"] == 2
     st, _ = plan(8, 4096, C["CS_VARIANT_CLUSTER"], 2, threads=1024)
     assert st == C["CS_ERR_INVALID_ARG"]
+
+
+# ------------------------------------------------------------------ backward
+@pytest.mark.parametrize("args,status", [
+    ((A, B, A + 4096, B + 4096, 4, 10), 0),
+    ((A, A, A + 4096, B, 4, 10), 0),            # probs == grad_out
+    ((A, B, B + 4096, A, 4, 10), 0),            # in place over probs
+    ((A, B, A + 4096, B, 4, 10), 0),            # in place over grad_out
+    ((None, None, None, None, 0, 10), 0),
+    ((A, B, A + 4096, B + 4096, -1, 10), 6),
+    ((A, B, A + 4096, B + 4096, 4, 0), 6),
+    ((A, B, A + 4096, B + 4096, 2**62, 1000), 6),
+    ((A, B, A + 4096, B + 4096, 4, 900000), 7),
+    ((None, B, A + 4096, B + 4096, 4, 10), 8),
+    ((A, None, A + 4096, B + 4096, 4, 10), 8),
+    ((A, B, None, B + 4096, 4, 10), 8),
+    ((A, B, A + 4096, None, 4, 10), 8),
+    ((A, B, A + 4096, A + 4, 4, 10), 8),        # grad overlaps probs
+    ((A, B, A + 4096, B + 156, 4, 10), 8),      # grad overlaps grad_out
+    ((A, B, B + 4100, B + 4096, 4, 10), 8),     # t overlaps grad
+    ((A, B, A + 8, B + 4096, 4, 10), 0),        # t overlaps probs (reads)
+    ((A, B, A + 4096, B + 160, 4, 10), 0),      # adjacent
+])
+def test_check_backward_args(args, status):
+    assert cs.cs_check_backward_args(*args) == status
+
+
+def bplan(batch, classes, variant=0, param=0, threads=0, strict=0, **dev):
+    d = dict(GB300, **dev)
+    st, p = cs.cs_plan_backward_host(
+        batch, classes, cs.options(variant, param, threads, strict),
+        d["sm_count"], d["smem_per_block_optin"], d["smem_per_sm"],
+        d["max_cluster"])
+    return st, p.as_dict()
+
+
+def test_backward_plans_for_the_workloads():
+    st, p = bplan(65536, 64)
+    assert st == 0 and p["variant"] == C["CS_VARIANT_ROWGROUP"]
+    assert p["lanes_per_row"] * p["elems_per_lane"] >= 64 + 6
+    st, p = bplan(4096, 32000)
+    assert st == 0 and p["variant"] == C["CS_VARIANT_CLUSTER"]
+    assert (p["cluster_size"], p["slice_len"], p["staged_tensors"]) == \
+        (4, 8000, 2)
+    assert p["grid_ctas"] == 4096 * 4 and p["ctas_per_sm"] >= 3
+    st, p = bplan(32, 50000)
+    assert st == 0 and p["grid_ctas"] >= GB300["sm_count"]
+    st, p = bplan(256, 131072)
+    assert st == 0 and (p["cluster_size"], p["slice_len"]) == (16, 8192)
+    st, p = bplan(4, 850000)
+    assert st == 0 and p["cluster_size"] == 16 and p["staged_tensors"] == 1
+
+
+@pytest.mark.parametrize("classes", [1, 3, 17, 64, 511, 512, 513, 1000,
+                                     4099, 8193, 32000, 50001, 131072,
+                                     464000, 600000, 850000])
+@pytest.mark.parametrize("batch", [1, 8, 4096])
+def test_backward_plans_hold_the_row(classes, batch):
+    st, p = bplan(batch, classes)
+    assert st == 0
+    if p["variant"] == C["CS_VARIANT_ROWGROUP"]:
+        # Room for the row at its worst alignment (3 floats of lead-in).
+        assert p["lanes_per_row"] * p["elems_per_lane"] >= classes + 6 - 3
+        assert p["elems_per_lane"] in (4, 8, 16, 32)
+        assert p["grid_ctas"] * p["threads_per_cta"] >= \
+            batch * p["lanes_per_row"]
+    else:
+        n, L = p["cluster_size"], p["slice_len"]
+        assert 1 <= n <= 16 and L % 4 == 0 and n * L >= classes
+        assert p["smem_bytes"] <= GB300["smem_per_block_optin"]
+        assert p["smem_bytes"] >= 512 + (L // 4 + 1) * 16 * p["staged_tensors"]
+        assert p["staged_tensors"] in (1, 2)
+        assert 64 <= p["threads_per_cta"] <= 512
+        assert p["threads_per_cta"] % 32 == 0
+        assert p["grid_ctas"] == batch * n
+
+
+def test_backward_forced_variants_and_limits():
+    st, p = bplan(8, 50001, C["CS_VARIANT_CLUSTER"], 1)
+    assert st == 0 and p["staged_tensors"] == 1
+    st, p = bplan(8, 20000, C["CS_VARIANT_CLUSTER"], 1)
+    assert st == 0 and p["staged_tensors"] == 2
+    st, _ = bplan(8, 131072, C["CS_VARIANT_CLUSTER"], 1)
+    assert st == C["CS_ERR_OOM"]
+    st, _ = bplan(8, 100, C["CS_VARIANT_ROWGROUP"], 1)
+    assert st == C["CS_ERR_OOM"]
+    st, p = bplan(8, 26, C["CS_VARIANT_ROWGROUP"], 1)
+    assert st == 0 and p["elems_per_lane"] == 32
+    st, _ = bplan(8, 64, C["CS_VARIANT_ROWGROUP"], 3)
+    assert st == C["CS_ERR_INVALID_ARG"]
+    st, _ = bplan(8, 64, C["CS_VARIANT_CLUSTER"], 17)
+    assert st == C["CS_ERR_INVALID_ARG"]
+    st, _ = bplan(8, 850000, C["CS_VARIANT_CLUSTER"], 0, max_cluster=8)
+    assert st == C["CS_ERR_OOM"]
+    for bad in (dict(threads=48), dict(threads=544), dict(threads=100),
+                dict(strict=1)):
+        st, _ = bplan(8, 50000, C["CS_VARIANT_CLUSTER"], 0, **bad)
+        assert st == C["CS_ERR_INVALID_ARG"], bad
+    st, _ = bplan(8, 64, C["CS_VARIANT_AUTO"], 4)
+    assert st == C["CS_ERR_INVALID_ARG"]
+    st, _ = bplan(8, 64, C["CS_VARIANT_ROWGROUP"], 0, threads=256)
+    assert st == C["CS_ERR_INVALID_ARG"]
+    st1, p1 = cs.cs_plan_backward_host(32, 50000, None, 152, 232448, 233472,
+                                       16)
+    assert st1 == 0 and p1.as_dict() == bplan(32, 50000)[1]
