@@ -76,6 +76,30 @@ __device__ __forceinline__ void store4(float* a, int pa, int pad, int len,
     }
 }
 
+// 16-byte asynchronous copy global -> shared (L1 bypassed); completes at
+// cp_async_wait_all() of the issuing thread.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                 :: "r"(smem_addr(dst)), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// Stages float4 q of the layout (pad) of segment a (own pad pa) into
+// shared memory at dst: one asynchronous 16-byte copy when whole and
+// aligned, else element by element (zeros outside [0, len)).
+__device__ __forceinline__ void stage4(float4* dst, const float* a, int pa,
+                                       int pad, int len, int q) {
+    const int j0 = 4 * q - pad;
+    if (pa == pad && j0 >= 0 && j0 + 4 <= len) {
+        cp_async16(dst, a + j0);
+        return;
+    }
+    *dst = load4<true>(a, pa, pad, len, q);
+}
+
 // acc += p * g, lanes (x, y) and (z, w) in two packed pairs.
 __device__ __forceinline__ void dot_add(float2& a, float2& b, float4 p,
                                         float4 g) {
@@ -190,8 +214,9 @@ __device__ __forceinline__ void st_cluster(uint32_t addr, float v) {
 // `rank` owns classes [rank L, rank L + L) of the row, L = slice_len (a
 // multiple of 4), and thread i of it float4s i, i + nt, ... of that slice in
 // every phase:
-//   load     p (and g if STAGE_G) into shared memory, four float4s of each
-//            in flight per trip, accumulating p * g;
+//   load     every float4 of p (and of g if STAGE_G) the thread owns as
+//            one 16-byte asynchronous copy into shared memory, all in
+//            flight at once; after they land, the thread's sum of p * g;
 //   reduce   warp shuffle sum, per-warp slots and one __syncthreads, after
 //            which every thread adds the slots in warp order; in a cluster,
 //            thread i < n stores the CTA's sum into slot `rank` of CTA i,
@@ -236,29 +261,24 @@ bwd_cluster_kernel(BwdTask t, int n, int slice_len) {
         const int pg = pad_of(g);
         const int q4 = len > 0 ? (pad + len + 3) >> 2 : 0;
 
+        // Every float4 of the thread's share in flight at once.
+        for (int q = threadIdx.x; q < q4; q += nt) {
+            stage4(sp + q, p, pad, pad, len, q);
+            if (STAGE_G) stage4(sg + q, g, pg, pad, len, q);
+        }
+        cp_async_wait_all();
         float2 a = make_float2(0.f, 0.f), b = make_float2(0.f, 0.f);
         int q = threadIdx.x;
         for (; q + 3 * nt < q4; q += 4 * nt) {
-            float4 pv[4], gv[4];
+            float4 gv[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                pv[i] = load4<true>(p, pad, pad, len, q + i * nt);
-                gv[i] = load4<STAGE_G>(g, pg, pad, len, q + i * nt);
-            }
+            for (int i = 0; i < 4; ++i)
+                gv[i] = STAGE_G ? sg[q + i * nt] : load4<false>(g, pg, pad, len, q + i * nt);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                sp[q + i * nt] = pv[i];
-                if (STAGE_G) sg[q + i * nt] = gv[i];
-                dot_add(a, b, pv[i], gv[i]);
-            }
+            for (int i = 0; i < 4; ++i) dot_add(a, b, sp[q + i * nt], gv[i]);
         }
-        for (; q < q4; q += nt) {
-            const float4 pv = load4<true>(p, pad, pad, len, q);
-            const float4 gv = load4<STAGE_G>(g, pg, pad, len, q);
-            sp[q] = pv;
-            if (STAGE_G) sg[q] = gv;
-            dot_add(a, b, pv, gv);
-        }
+        for (; q < q4; q += nt)
+            dot_add(a, b, sp[q], STAGE_G ? sg[q] : load4<false>(g, pg, pad, len, q));
 
         float dot = (a.x + a.y) + (b.x + b.y);
 #pragma unroll
