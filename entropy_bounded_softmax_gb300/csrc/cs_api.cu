@@ -412,6 +412,9 @@ cs_status cs_constrained_softmax_ex(const float* logits, float* out,
     task.t_min = t_min;
     task.hi0 = t_max < 1.0f ? t_max : 1.0f;
     task.strict = options ? options->strict : 0;
+    // Asynchronous staging pays when several CTAs share an SM (the same
+    // threshold as the per-thread work rule of the thread count).
+    task.async_stage = p.grid_ctas * 4 > static_cast<int64_t>(d->sm_count) * 5;
     task.wait_limit_cycles = cs::kWaitLimitCycles;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);

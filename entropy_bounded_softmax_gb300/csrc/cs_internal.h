@@ -35,6 +35,7 @@ struct RowTask {
     float t_min;
     float hi0;             // min(1, t_max): upper end of the search
     int32_t strict;        // 1: evaluate every bisection midpoint
+    int32_t async_stage;   // cluster kernel: stage with asynchronous copies
     uint64_t wait_limit_cycles;
 };
 

@@ -76,17 +76,6 @@ __device__ __forceinline__ void store4(float* a, int pa, int pad, int len,
     }
 }
 
-// 16-byte asynchronous copy global -> shared (L1 bypassed); completes at
-// cp_async_wait_all() of the issuing thread.
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
-                 :: "r"(smem_addr(dst)), "l"(src) : "memory");
-}
-
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.wait_all;" ::: "memory");
-}
-
 // Stages float4 q of the layout (pad) of segment a (own pad pa) into
 // shared memory at dst: one asynchronous 16-byte copy when whole and
 // aligned, else element by element (zeros outside [0, len)).
@@ -371,14 +360,14 @@ cudaError_t launch_backward_cluster(const BwdTask& task, int cluster_size,
     if (cluster_size > 1)
         return stage_g ? launch_cl<true, true>(task, cluster_size, slice_len,
                                                threads, smem_bytes, grid_ctas,
-                                               stream, 4)
+                                               stream, 8)
                        : launch_cl<true, false>(task, cluster_size, slice_len,
                                                 threads, smem_bytes, grid_ctas,
-                                                stream, 5);
+                                                stream, 9);
     return stage_g ? launch_cl<false, true>(task, 1, slice_len, threads,
-                                            smem_bytes, grid_ctas, stream, 6)
+                                            smem_bytes, grid_ctas, stream, 10)
                    : launch_cl<false, false>(task, 1, slice_len, threads,
-                                             smem_bytes, grid_ctas, stream, 7);
+                                             smem_bytes, grid_ctas, stream, 11);
 }
 
 }  // namespace cs

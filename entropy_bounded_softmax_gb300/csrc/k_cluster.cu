@@ -529,8 +529,10 @@ __device__ __forceinline__ void write_out(const float4* row4, const Slice& s,
 
 // MAXT: largest block the instantiation is launched with; MINB: blocks per
 // SM the register allocation must allow (256 threads x 3 blocks for the
-// throughput plans, 512 x 1 for the latency plans).
-template <bool CLUSTER, int MAXT, int MINB>
+// throughput plans, 512 x 1 for the latency plans); ASYNC: stage with
+// asynchronous copies (a compile-time choice: a run-time branch between
+// the two staging loops cost the other path 1.4% at 32 x 50000).
+template <bool CLUSTER, int MAXT, int MINB, bool ASYNC>
 __global__ void __launch_bounds__(MAXT, MINB)
 cluster_kernel(RowTask t, int n, int slice_len) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -574,14 +576,18 @@ cluster_kernel(RowTask t, int n, int slice_len) {
         const float* src = t.logits + r * C + s0;
         const Slice s = make_slice(src, len);
 
-        // Stage: thread t loads float4s q = t, t + nt, ... of the slice
-        // (the float4s it owns in every later pass): the aligned body with
-        // 128-bit streaming loads, eight in flight at a time, the ragged
-        // head and tail element by element.  It stores them to shared
-        // memory and folds them into its own max and the finiteness check.
-        // (Bulk copies into shared memory were slower: one SM's bulk-copy
-        // traffic arrived at about 16 bytes per clock, against about 22 for
-        // plain loads with this many in flight.)
+        // Stage: thread t copies float4s q = t, t + nt, ... of the slice
+        // (the float4s it owns in every later pass) into shared memory and
+        // folds them into its own max and the finiteness check; the ragged
+        // head and tail go element by element.  Launches with several CTAs
+        // per SM (async_stage) copy the aligned body as 16-byte
+        // asynchronous copies, all in flight at once, and fold after they
+        // land (4096 x 32000: 4% faster, 256 x 131072: 8%); launches of
+        // about one CTA per SM load it eight float4s at a time and fold
+        // each trip as it arrives (32 x 50000: 0.5% faster than the copies,
+        // the folding overlaps the next trip).  (Bulk copies were slower:
+        // one SM's bulk-copy traffic arrived at about 16 bytes per clock,
+        // against about 22 for per-thread loads with this many in flight.)
         float m_t = -INFINITY;  // this thread's max
         float bad = 0.0f;       // becomes NaN if any element is NaN or +-Inf
         bool nan_seen = false;
@@ -614,23 +620,38 @@ cluster_kernel(RowTask t, int n, int slice_len) {
                 load_ragged(q);
                 q += nt;
             }
-            for (; q + 7 * nt < s.qb1; q += 8 * nt) {
-                float4 v[8];
+            if (ASYNC) {
+                const int qb = q;
+                for (; q < s.qb1; q += nt) cp_async16(&row4[q], gb + 4 * q);
+                if (q < s.q4) load_ragged(q);
+                cp_async_wait_all();
+                for (q = qb; q + 3 * nt < s.qb1; q += 4 * nt) {
+                    float4 v[4];
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    v[i] = __ldcs(reinterpret_cast<const float4*>(gb + 4 * (q + i * nt)));
+                    for (int i = 0; i < 4; ++i) v[i] = row4[q + i * nt];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    row4[q + i * nt] = v[i];
-                    fold(v[i]);
+                    for (int i = 0; i < 4; ++i) fold(v[i]);
                 }
+                for (; q < s.qb1; q += nt) fold(row4[q]);
+            } else {
+                for (; q + 7 * nt < s.qb1; q += 8 * nt) {
+                    float4 v[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        v[i] = __ldcs(reinterpret_cast<const float4*>(gb + 4 * (q + i * nt)));
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        row4[q + i * nt] = v[i];
+                        fold(v[i]);
+                    }
+                }
+                for (; q < s.qb1; q += nt) {
+                    const float4 v = __ldcs(reinterpret_cast<const float4*>(gb + 4 * q));
+                    row4[q] = v;
+                    fold(v);
+                }
+                if (q < s.q4) load_ragged(q);
             }
-            for (; q < s.qb1; q += nt) {
-                const float4 v = __ldcs(reinterpret_cast<const float4*>(gb + 4 * q));
-                row4[q] = v;
-                fold(v);
-            }
-            if (q < s.q4) load_ragged(q);
         }
         // Classify a non-finite slice (rare): 2 = NaN seen, 1 = only Inf.
         // Each thread rescans only the float4s it stored itself.
@@ -713,11 +734,11 @@ cluster_kernel(RowTask t, int n, int slice_len) {
     if (CLUSTER) cluster_sync();
 }
 
-template <bool CLUSTER, int MAXT, int MINB>
+template <bool CLUSTER, int MAXT, int MINB, bool ASYNC>
 cudaError_t launch_one(const RowTask& task, int cluster_size, int slice_len,
                        int threads, int smem_bytes, int64_t grid_ctas,
                        cudaStream_t stream, int attr_slot) {
-    auto kern = cluster_kernel<CLUSTER, MAXT, MINB>;
+    auto kern = cluster_kernel<CLUSTER, MAXT, MINB, ASYNC>;
     cudaError_t e = ensure_smem_attribute(reinterpret_cast<const void*>(kern),
                                           attr_slot, smem_bytes, CLUSTER);
     if (e != cudaSuccess) return e;
@@ -741,23 +762,35 @@ cudaError_t launch_one(const RowTask& task, int cluster_size, int slice_len,
     return cudaLaunchKernelEx(&cfg, kern, task, cluster_size, slice_len);
 }
 
+template <bool ASYNC>
+cudaError_t launch_cluster_as(const RowTask& task, int cluster_size,
+                              int slice_len, int threads, int smem_bytes,
+                              int64_t grid_ctas, cudaStream_t stream) {
+    const bool narrow = threads <= 256;
+    const int slot = (ASYNC ? 4 : 0) + (cluster_size > 1 ? 1 : 0) + (narrow ? 0 : 2);
+    if (cluster_size > 1)
+        return narrow ? launch_one<true, 256, 3, ASYNC>(task, cluster_size, slice_len,
+                                                        threads, smem_bytes, grid_ctas,
+                                                        stream, slot)
+                      : launch_one<true, 512, 1, ASYNC>(task, cluster_size, slice_len,
+                                                        threads, smem_bytes, grid_ctas,
+                                                        stream, slot);
+    return narrow ? launch_one<false, 256, 3, ASYNC>(task, 1, slice_len, threads,
+                                                     smem_bytes, grid_ctas, stream, slot)
+                  : launch_one<false, 512, 1, ASYNC>(task, 1, slice_len, threads,
+                                                     smem_bytes, grid_ctas, stream, slot);
+}
+
 }  // namespace
 
 cudaError_t launch_cluster(const RowTask& task, int cluster_size,
                            int slice_len, int threads, int smem_bytes,
                            int64_t grid_ctas, cudaStream_t stream) {
-    const bool narrow = threads <= 256;
-    if (cluster_size > 1)
-        return narrow ? launch_one<true, 256, 3>(task, cluster_size, slice_len,
-                                                 threads, smem_bytes, grid_ctas,
-                                                 stream, 1)
-                      : launch_one<true, 512, 1>(task, cluster_size, slice_len,
-                                                 threads, smem_bytes, grid_ctas,
-                                                 stream, 3);
-    return narrow ? launch_one<false, 256, 3>(task, 1, slice_len, threads,
-                                              smem_bytes, grid_ctas, stream, 0)
-                  : launch_one<false, 512, 1>(task, 1, slice_len, threads,
-                                              smem_bytes, grid_ctas, stream, 2);
+    return task.async_stage
+        ? launch_cluster_as<true>(task, cluster_size, slice_len, threads,
+                                  smem_bytes, grid_ctas, stream)
+        : launch_cluster_as<false>(task, cluster_size, slice_len, threads,
+                                   smem_bytes, grid_ctas, stream);
 }
 
 }  // namespace cs
