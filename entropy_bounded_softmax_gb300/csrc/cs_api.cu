@@ -253,16 +253,17 @@ cs_status plan_backward_rowgroup(int64_t batch, int32_t C, int32_t param,
 }
 
 // Cluster backward geometry for n CTAs per row: p and g staged when both
-// fit, else p alone (stage_both = false); false if neither fits.
+// fit, else p alone (stage_both = false); false if neither fits.  per: the
+// float4s of each staged tensor per thread the automatic thread count aims
+// for.
 bool backward_geometry(int32_t C, int n, int threads_req, int smem_optin,
-                       bool stage_both, cs_plan* p) {
+                       bool stage_both, int per, cs_plan* p) {
     const int64_t L = ceil_div(ceil_div(C, n), 4) * 4;
     const int64_t smem = cs::backward_smem_bytes(L, stage_both);
     if (smem > smem_optin) return false;
     int threads = threads_req;
     if (threads == 0) {
-        // About eight float4s of each staged tensor per thread.
-        int64_t t = ceil_div(ceil_div(L, 4), 8);
+        int64_t t = ceil_div(ceil_div(L, 4), per);
         t = ceil_div(t, 32) * 32;
         if (t < 64) t = 64;
         if (t > cs::kBwdMaxThreads) t = cs::kBwdMaxThreads;
@@ -287,26 +288,31 @@ cs_status plan_backward_cluster(int64_t batch, int32_t C, const cs_options& o,
     bool ok = false;
     if (o.param == 0) {
         // Smallest cluster whose slices are at most kBwdTargetSlice classes,
-        // widened to about one CTA per SM for few rows while slices keep
-        // kMinWideSlice classes.
+        // widened to about two CTAs per SM for few rows while slices keep
+        // kMinWideSlice classes (32 x 50000: clusters of 10, 5000-class
+        // slices).
         int n0 = static_cast<int>(ceil_div(C, cs::kBwdTargetSlice));
         if (n0 > max_cluster) n0 = max_cluster;
         if (n0 < 1) n0 = 1;
         const int64_t rows = batch > 0 ? batch : 1;
-        int64_t widen = ceil_div(sm_count, rows);
+        int64_t widen = ceil_div(2 * static_cast<int64_t>(sm_count), rows);
         if (widen > C / kMinWideSlice) widen = C / kMinWideSlice;
         if (widen > max_cluster) widen = max_cluster;
+        // Launches of few CTAs are latency-bound: fewer float4s per thread
+        // (32 x 50000 in clusters of 10: 6.9 us on 160 threads, 6.6 on
+        // 256); larger ones aim for eight, enough in flight per SM.
+        const int per = widen > n0 ? 5 : 8;
         if (widen > n0) n0 = static_cast<int>(widen);
         for (int c = n0; c <= max_cluster && !ok; ++c)
-            ok = backward_geometry(C, c, o.threads, smem_optin, true, p);
+            ok = backward_geometry(C, c, o.threads, smem_optin, true, per, p);
         if (!ok)
             ok = backward_geometry(C, max_cluster, o.threads, smem_optin,
-                                   false, p);
+                                   false, per, p);
     } else {
         if (o.param < 1 || o.param > cs::kMaxCluster) return CS_ERR_INVALID_ARG;
         if (o.param > max_cluster) return CS_ERR_INVALID_ARG;
-        ok = backward_geometry(C, o.param, o.threads, smem_optin, true, p) ||
-             backward_geometry(C, o.param, o.threads, smem_optin, false, p);
+        ok = backward_geometry(C, o.param, o.threads, smem_optin, true, 8, p) ||
+             backward_geometry(C, o.param, o.threads, smem_optin, false, 8, p);
     }
     if (!ok) return CS_ERR_OOM;
     const int n = p->cluster_size;
