@@ -8,8 +8,8 @@ nothing from the product.
 The arithmetic lives in ``constrained_softmax_oracle.c`` (plain fp64 C, libm
 ``exp``/``log``), which follows "BURT-IMMA CUDA Kernel API Reference",
 section 2.1 ``constrained_softmax`` and section 5 (error codes, NaN/Inf policy,
-graceful degradation), and the backward of section 6.3 with the temperature
-restored.  This module only compiles it with gcc, marshals numpy
+graceful degradation), the backward of section 6.3 with the temperature
+restored, and attention_softmax (section 2.6).  This module only compiles it with gcc, marshals numpy
 arrays in and out through ctypes, and splits a batch over threads (rows are
 independent, so the split changes no arithmetic).
 
@@ -78,6 +78,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_constrained_softmax_path.argtypes = [
         f32p, f64p, ctypes.c_int64, ctypes.c_float, ctypes.c_float,
         ctypes.c_float, ctypes.c_int32, f64p, i32p, f64p, f64p]
+    lib.oracle_attention_softmax_rows.restype = None
+    lib.oracle_attention_softmax_rows.argtypes = [
+        f32p, f32p, f64p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+        ctypes.c_int64, ctypes.c_int32, i32p]
     lib.oracle_constrained_softmax_backward_rows.restype = None
     lib.oracle_constrained_softmax_backward_rows.argtypes = [
         f64p, f64p, f64p, f64p, ctypes.c_int64, ctypes.c_int64,
@@ -249,6 +253,51 @@ def constrained_softmax_backward(p, grad_output, T,
             _ptr(tt, ctypes.c_double), _ptr(grad, ctypes.c_double), 0, batch,
             C)
     return grad
+
+
+@dataclass
+class AttentionResult:
+    p: np.ndarray        # [B, H, S, S] float64
+    flags: np.ndarray    # [B, H, S] int32, section 5.1 codes 0..2
+
+
+def attention_softmax(scores, mask=None, causal: bool = False,
+                      threads: int | None = None,
+                      lib: ctypes.CDLL | None = None) -> AttentionResult:
+    """Oracle attention_softmax (section 2.6) of fp32 scores [B, H, S, S]
+    with an optional additive fp32 mask [B, S] (the page's [B, 1, 1, S]).
+    Rows are split over threads; each row is the same C code."""
+    lib = lib or load()
+    x = np.ascontiguousarray(np.asarray(scores, dtype=np.float32))
+    if x.ndim != 4 or x.shape[2] != x.shape[3]:
+        raise ValueError("scores must be [B, H, S, S]")
+    B, H, S, _ = x.shape
+    m = None
+    if mask is not None:
+        m = np.ascontiguousarray(np.asarray(mask, dtype=np.float32))
+        m = m.reshape(B, S)
+    p = np.empty(x.shape, dtype=np.float64)
+    flags = np.empty((B, H, S), dtype=np.int32)
+    rows = B * H * S
+    if rows == 0:
+        return AttentionResult(p, flags)
+    mp = _ptr(m, ctypes.c_float) if m is not None else None
+
+    def run(r0: int, r1: int) -> None:
+        lib.oracle_attention_softmax_rows(
+            _ptr(x, ctypes.c_float), mp, _ptr(p, ctypes.c_double), r0, r1, H,
+            S, int(bool(causal)), _ptr(flags, ctypes.c_int32))
+
+    n = max(1, min(threads or default_threads(), rows))
+    if n == 1:
+        run(0, rows)
+    else:
+        edges = np.linspace(0, rows, n + 1).astype(np.int64)
+        with ThreadPoolExecutor(max_workers=n) as pool:
+            for f in [pool.submit(run, int(edges[i]), int(edges[i + 1]))
+                      for i in range(n) if edges[i + 1] > edges[i]]:
+                f.result()
+    return AttentionResult(p, flags)
 
 
 def search_interval(t_min: float, t_max: float) -> tuple[float, float]:

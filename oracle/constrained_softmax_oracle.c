@@ -12,7 +12,7 @@
  * Notes) and section 5 (5.1 Error Codes, 5.3 NaN/Inf Propagation Policy,
  * 5.4 Graceful Degradation); the backward follows section 6.3 (PyTorch Custom
  * Op Integration, ConstrainedSoftmaxFunction.backward) with the 1/T of
- * softmax(l / T) restored.
+ * softmax(l / T) restored; attention_softmax follows section 2.6.
  *
  * Arithmetic: IEEE double throughout, libm exp() and log().  The fp32
  * parameters are promoted exactly to double, so both sides of any comparison
@@ -221,5 +221,76 @@ void oracle_constrained_softmax_backward_rows(const double* p, const double* g,
         double dot = 0.0;
         for (int64_t i = 0; i < C; ++i) dot += gb[i] * pb[i];
         for (int64_t k = 0; k < C; ++k) out[k] = pb[k] * (gb[k] - dot) / T[b];
+    }
+}
+
+/*
+ * attention_softmax: section 2.6 (Signature, Parameters table, Description
+ * steps 1-3).  scores is row-major [B, H, S, S]; row r = ((b H) + h) S + i
+ * holds the scores of query i against keys j = 0..S-1.  mask is NULL or
+ * [B, S] (the page's [B, 1, 1, S]), added to every row of batch b.
+ *
+ *  1. v_j = scores[r, j] + mask[b, j], added in fp32 (the inputs' precision,
+ *     as the page's fp32 kernel adds them); a mask of -inf removes key j;
+ *  2. causal: keys j > i are removed (their scores are never used);
+ *  3. p = softmax over the kept keys with the max subtracted (fp64 here),
+ *     p_j = 0 for removed keys.
+ *
+ * Readings (stated again in the design notes):
+ *  - section 5.3 applies to the scores and the mask the row uses: a NaN
+ *    (flag 1) or an infinity (flag 2; a mask of -inf is the masking value,
+ *    not an error) zeroes the whole row; NaN wins over Inf;
+ *  - a row whose keys are all removed has no distribution: zeros, flag 0.
+ */
+/* Step 1: the score plus the mask, added in fp32. */
+static double masked_score(const float* s, const float* m, int64_t j)
+{
+    if (!m) return (double)s[j];
+    const float v = s[j] + m[j];
+    return (double)v;
+}
+
+void oracle_attention_softmax_rows(const float* scores, const float* mask,
+                                   double* out, int64_t row_begin,
+                                   int64_t row_end, int64_t H, int64_t S,
+                                   int32_t causal, int32_t* flags_out)
+{
+    for (int64_t r = row_begin; r < row_end; ++r) {
+        const int64_t b = r / (H * S);
+        const int64_t i = r % S;
+        const float* s = scores + r * S;
+        const float* m = mask ? mask + b * S : 0;
+        double* p = out + r * S;
+        /* Step 2: keys j > i are removed from a causal row. */
+        const int64_t kept_end = causal ? i + 1 : S;
+        int has_nan = 0, has_inf = 0;
+        for (int64_t j = 0; j < kept_end; ++j) {
+            if (isnan(s[j])) has_nan = 1;
+            else if (isinf(s[j])) has_inf = 1;
+            if (m) {
+                if (isnan(m[j])) has_nan = 1;
+                else if (isinf(m[j]) && m[j] > 0) has_inf = 1;
+            }
+        }
+        for (int64_t j = 0; j < S; ++j) p[j] = 0.0;
+        if (has_nan || has_inf) {
+            flags_out[r] = has_nan ? ORACLE_FLAG_NAN_INPUT : ORACLE_FLAG_INF_INPUT;
+            continue;
+        }
+        flags_out[r] = ORACLE_FLAG_NONE;
+        /* Step 3: softmax over the kept keys (a -inf value is a removed
+         * key and contributes exp(-inf) = 0). */
+        double vmax = -INFINITY;
+        for (int64_t j = 0; j < kept_end; ++j) {
+            const double v = masked_score(s, m, j);
+            if (v > vmax) vmax = v;
+        }
+        if (vmax == -INFINITY) continue;   /* every key removed */
+        double sum = 0.0;
+        for (int64_t j = 0; j < kept_end; ++j) {
+            p[j] = exp(masked_score(s, m, j) - vmax);
+            sum += p[j];
+        }
+        for (int64_t j = 0; j < kept_end; ++j) p[j] /= sum;
     }
 }

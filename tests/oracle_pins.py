@@ -16,7 +16,11 @@ AssertionError when the oracle disagrees with:
     vector-Jacobian product of a library softmax (torch autograd, fp64) at
     the forward's temperature; the explicit Jacobian diag(p) - p p^T at
     T = 1; and invariants (gradients sum to 0, shift invariance in the
-    upstream gradient, zero rows where T is NaN).
+    upstream gradient, zero rows where T is NaN),
+  * for attention_softmax (section 2.6): scipy's softmax of each row, of
+    each causal prefix and of the unmasked subset (scores plus mask added
+    in numpy fp32); the fp32 addition of a -1e9 mask; invariants and the
+    NaN/Inf policy.
 
 The same checks run against deliberately broken copies of the oracle in
 ``test_oracle_mutants.py``: every plausible mistake must fail at least one.
@@ -478,6 +482,120 @@ def check_backward_invariants(lib) -> None:
     assert np.all(np.isfinite(gb[4:])) and np.any(gb[4:] != 0.0)
 
 
+# ---------------------------------------------------------- attention_softmax
+def _scipy_rows(v: np.ndarray) -> np.ndarray:
+    return scipy.special.softmax(v.astype(np.float64), axis=-1)
+
+
+def check_attention_plain_softmax(lib) -> None:
+    """No mask, not causal: every row is the library softmax."""
+    rng = np.random.default_rng(91)
+    for B, H, S in ((1, 1, 1), (2, 3, 5), (1, 2, 64), (2, 1, 300)):
+        x = rng.normal(0.0, 3.0, (B, H, S, S)).astype(np.float32)
+        r = oracle.attention_softmax(x, threads=1, lib=lib)
+        assert np.all(r.flags == 0)
+        assert np.max(np.abs(r.p - _scipy_rows(x))) < 1e-13
+
+
+def check_attention_causal_prefix(lib) -> None:
+    """Causal row i is the library softmax of keys 0..i, zero after."""
+    rng = np.random.default_rng(92)
+    B, H, S = 2, 2, 37
+    x = rng.normal(0.0, 2.0, (B, H, S, S)).astype(np.float32)
+    r = oracle.attention_softmax(x, causal=True, threads=1, lib=lib)
+    for b in range(B):
+        for h in range(H):
+            for i in range(S):
+                ref = _scipy_rows(x[b, h, i, :i + 1])
+                assert np.max(np.abs(r.p[b, h, i, :i + 1] - ref)) < 1e-13
+                assert np.all(r.p[b, h, i, i + 1:] == 0.0)
+
+
+def check_attention_mask_subset(lib) -> None:
+    """An additive mask with -inf holes: on the kept keys the library
+    softmax of scores + mask (added in numpy fp32), zeros on the holes;
+    each batch uses its own mask row, with and without causal."""
+    rng = np.random.default_rng(93)
+    B, H, S = 3, 2, 40
+    x = rng.normal(0.0, 2.0, (B, H, S, S)).astype(np.float32)
+    mask = rng.normal(0.0, 1.0, (B, S)).astype(np.float32)
+    mask[rng.random((B, S)) < 0.3] = -np.inf
+    mask[:, 0] = 0.0
+    for causal in (False, True):
+        r = oracle.attention_softmax(x, mask, causal=causal, threads=1,
+                                     lib=lib)
+        assert np.all(r.flags == 0)
+        for b in range(B):
+            v = x[b] + mask[b][None, None, :]          # fp32 addition
+            for h in range(H):
+                for i in range(S):
+                    end = i + 1 if causal else S
+                    keep = np.flatnonzero(np.isfinite(v[h, i, :end]))
+                    ref = np.zeros(S)
+                    ref[keep] = _scipy_rows(v[h, i, keep])
+                    assert np.max(np.abs(r.p[b, h, i] - ref)) < 1e-13
+
+
+def check_attention_fp32_mask_addition(lib) -> None:
+    """The page's -1e9 mask is added in fp32: near 1e9 fp32 steps by 64, so
+    every score of magnitude below 32 vanishes into -1e9 and a fully
+    masked row becomes uniform; a partly masked row puts exactly 0 on its
+    masked keys."""
+    rng = np.random.default_rng(94)
+    B, H, S = 2, 2, 24
+    x = rng.uniform(-30.0, 30.0, (B, H, S, S)).astype(np.float32)
+    mask = np.zeros((B, S), dtype=np.float32)
+    mask[0, :] = -1e9
+    mask[1, S // 2:] = -1e9
+    r = oracle.attention_softmax(x, mask, threads=1, lib=lib)
+    assert np.all(r.p[0] == 1.0 / S)
+    assert np.all(r.p[1, :, :, S // 2:] == 0.0)
+    ref = _scipy_rows(x[1, :, :, :S // 2])
+    assert np.max(np.abs(r.p[1, :, :, :S // 2] - ref)) < 1e-13
+
+
+def check_attention_invariants_and_faults(lib) -> None:
+    """Rows sum to 1; an exactly representable shift of the scores changes
+    nothing; logits near 1000 do not overflow; NaN (flag 1) and +-Inf
+    (flag 2) in a used score or mask value zero the row (a NaN key that a
+    causal row never uses does not); a row with every key masked by -inf
+    is zeros with flag 0."""
+    rng = np.random.default_rng(95)
+    B, H, S = 2, 2, 16
+    x = (np.round(rng.normal(0.0, 2.0, (B, H, S, S)) * 1024) / 1024).astype(np.float32)
+    r = oracle.attention_softmax(x, causal=True, threads=1, lib=lib)
+    assert np.max(np.abs(r.p.sum(axis=-1) - 1.0)) < 1e-14
+    r8 = oracle.attention_softmax(x + np.float32(8.0), causal=True, threads=1,
+                                  lib=lib)
+    assert np.max(np.abs(r8.p - r.p)) < 1e-13
+    big = oracle.attention_softmax(x + np.float32(1000.0), threads=1, lib=lib)
+    assert np.all(np.isfinite(big.p))
+    assert np.max(np.abs(big.p.sum(axis=-1) - 1.0)) < 1e-14
+    y = x.copy()
+    y[0, 0, 5, 3] = np.nan          # used by row 5
+    y[0, 1, 2, 9] = np.nan          # key 9 > 2: a causal row 2 never uses it
+    y[1, 0, 7, 0] = np.inf
+    y[1, 1, 4, 4] = -np.inf
+    mask = np.zeros((B, S), dtype=np.float32)
+    rc = oracle.attention_softmax(y, causal=True, threads=1, lib=lib)
+    assert rc.flags[0, 0, 5] == 1 and np.all(rc.p[0, 0, 5] == 0.0)
+    assert rc.flags[0, 1, 2] == 0 and abs(rc.p[0, 1, 2].sum() - 1.0) < 1e-14
+    assert rc.flags[1, 0, 7] == 2 and rc.flags[1, 1, 4] == 2
+    assert np.all(rc.p[1, 1, 4] == 0.0)
+    rn = oracle.attention_softmax(y, causal=False, threads=1, lib=lib)
+    assert rn.flags[0, 1, 2] == 1
+    mask[1, 3] = np.nan
+    mask[0, 6] = np.inf
+    rm = oracle.attention_softmax(x, mask, threads=1, lib=lib)
+    assert np.all(rm.flags[1] == 1) and np.all(rm.flags[0] == 2)
+    assert np.all(rm.p == 0.0)
+    mask = np.zeros((B, S), dtype=np.float32)
+    mask[0, :] = -np.inf
+    ra = oracle.attention_softmax(x, mask, threads=1, lib=lib)
+    assert np.all(ra.flags == 0) and np.all(ra.p[0] == 0.0)
+    assert np.max(np.abs(ra.p[1].sum(axis=-1) - 1.0)) < 1e-14
+
+
 ALL_CHECKS = [
     check_two_class_entropy,
     check_spike_entropy,
@@ -494,4 +612,9 @@ ALL_CHECKS = [
     check_backward_library_vjp,
     check_backward_jacobian_t1,
     check_backward_invariants,
+    check_attention_plain_softmax,
+    check_attention_causal_prefix,
+    check_attention_mask_subset,
+    check_attention_fp32_mask_addition,
+    check_attention_invariants_and_faults,
 ]

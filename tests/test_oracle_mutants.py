@@ -66,6 +66,26 @@ MUTANTS = [
      "dot += pb[i] * pb[i];"),
     ("backward_nan_rows_not_zeroed",
      "if (!(T[b] > 0.0) || isinf(T[b])) {", "if (0) {"),
+    ("attention_causal_off_by_one",
+     "const int64_t kept_end = causal ? i + 1 : S;",
+     "const int64_t kept_end = causal ? i : S;"),
+    ("attention_causal_keeps_diagonal_out",
+     "const int64_t kept_end = causal ? i + 1 : S;",
+     "const int64_t kept_end = causal ? i + 2 : S;"),
+    ("attention_mask_of_batch_0", "const float* m = mask ? mask + b * S : 0;",
+     "const float* m = mask ? mask : 0;"),
+    ("attention_mask_ignored", "const float v = s[j] + m[j];",
+     "const float v = s[j];"),
+    ("attention_mask_added_in_fp64", "const float v = s[j] + m[j];",
+     "const double v = (double)s[j] + (double)m[j];"),
+    ("attention_no_max_subtraction",
+     "p[j] = exp(masked_score(s, m, j) - vmax);",
+     "p[j] = exp(masked_score(s, m, j));"),
+    ("attention_mask_inf_not_error",
+     "else if (isinf(m[j]) && m[j] > 0) has_inf = 1;",
+     "else if (0) has_inf = 1;"),
+    ("attention_row_index_is_head", "const int64_t i = r % S;",
+     "const int64_t i = (r / S) % S;"),
 ]
 
 
