@@ -55,7 +55,8 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=wl.LATENCY.name,
                     help="one of: " + ", ".join(
-                        list(wl.WORKLOADS) + [w.name for w in wl.sweep_workloads()]))
+                        list(wl.WORKLOADS) + [w.name for w in wl.sweep_workloads()]
+                        + list(wl.ATTENTION_WORKLOADS)))
     ap.add_argument("--variant", choices=["auto", "rowgroup", "cluster"],
                     default="auto")
     ap.add_argument("--param", type=int, default=0,
@@ -77,10 +78,12 @@ def parse_args(argv=None):
                     help="time plain stream launches instead of one CUDA "
                          "graph of the K launches")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--op", choices=["forward", "backward"],
+    ap.add_argument("--op", choices=["forward", "backward", "attention"],
                     default="forward",
                     help="backward: time the gradient kernel, (1/T) p "
-                         "(g - <g, p>), on the workload's shape")
+                         "(g - <g, p>), on the workload's shape; attention: "
+                         "time attention_softmax on an attention workload "
+                         "(default attention_32x8x512)")
     return ap.parse_args(argv)
 
 
@@ -752,8 +755,241 @@ def backward_arm(args, w: wl.Workload) -> int:
     return 0
 
 
+# -------------------------------------------------------------- attention
+ATTENTION_METRIC = ("attention_softmax rows/s and effective HBM GB/s "
+                    "(% of roofline)")
+
+
+def attention_bytes(w) -> int:
+    """Algorithmic HBM bytes of one launch: every kept score read once,
+    every output written once, the mask read once."""
+    S = w.seq_len
+    kept = w.batch * w.heads * (S * (S + 1) // 2 if w.causal else S * S)
+    mask = 4 * w.batch * S if w.mask != "none" else 0
+    return 4 * kept + 4 * w.elements + mask
+
+
+def attention_config(w, l2: str) -> dict:
+    return {"workload": w.name, "batch": w.batch, "heads": w.heads,
+            "seq_len": w.seq_len, "causal": w.causal, "mask": w.mask,
+            "scores": w.note, "seed": w.seed, "l2": l2}
+
+
+def run_oracle_attention_sample(w, x, mask, seconds: float,
+                                threads: int) -> dict:
+    """The oracle as it stands on whole (batch, head) blocks of rows of the
+    workload, cycled, until `seconds` have passed."""
+    import oracle
+    oracle.load()
+    S = w.seq_len
+    blk = x.reshape(w.batch * w.heads, S, S)
+    done = 0
+    k = 0
+    t0 = time.perf_counter()
+    while True:
+        b = (k // w.heads) % w.batch
+        one = blk[k % blk.shape[0]][None, None]
+        oracle.attention_softmax(one, None if mask is None else mask[b:b + 1],
+                                 w.causal, threads=threads)
+        done += S
+        k += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"rows": done, "seconds": dt, "rows_per_s": done / dt}
+
+
+def attention_reference_arm(args, w) -> int:
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    threads = oracle.default_threads()
+    S = w.seq_len
+    n_blocks = max(1, min(w.batch * w.heads, (1 << 22) // (S * S) or 1))
+    x = wl.generate_attention(w, np.arange(n_blocks * S)).reshape(
+        n_blocks, 1, S, S)
+    mask = wl.attention_mask(w)
+    m0 = None if mask is None else mask[:1]
+    for _ in range(args.warmup):
+        for k in range(n_blocks):
+            oracle.attention_softmax(x[k:k + 1], m0, w.causal, threads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        for k in range(n_blocks):
+            oracle.attention_softmax(x[k:k + 1], m0, w.causal, threads=threads)
+    dt = time.perf_counter() - t0
+    value = n_blocks * S * args.steps / dt
+    line = {
+        "impl": "reference", "op": "attention", "metric": ATTENTION_METRIC,
+        "value": value, "unit": "rows/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": attention_config(w, "cpu"),
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": f"{n_blocks} (batch, head) blocks of "
+                                   f"{S} rows per step ({args.steps} steps)"},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def attention_arm(args, w) -> int:
+    """One step = one attention_softmax launch over the whole workload,
+    scores and mask resident in HBM."""
+    import torch
+    import entropy_bounded_softmax_gb300 as cs
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+
+    B, H, S = w.batch, w.heads, w.seq_len
+    x = wl.generate_attention(w).reshape(B, H, S, S)
+    mask = wl.attention_mask(w)
+    io_bytes = attention_bytes(w)
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+    xs = torch.from_numpy(x).to(dev)
+    md = torch.from_numpy(mask).to(dev) if mask is not None else None
+    nbuf = max(1, math.ceil(3 * L2_BYTES / io_bytes)) if io_bytes < 3 * L2_BYTES else 1
+    ins = [xs] + [xs.clone() for _ in range(nbuf - 1)]
+    outs = [torch.empty_like(xs) for _ in range(nbuf)]
+    l2_note = (f"rotating {nbuf} score/output pairs "
+               f"({nbuf * io_bytes / 2**20:.0f} MiB > L2)") if nbuf > 1 else \
+        f"inputs larger than L2 ({io_bytes / 2**20:.0f} MiB)"
+    opts = cs.options(cs.VARIANTS[args.variant], args.param, args.threads, 0)
+    m_ptr = md.data_ptr() if md is not None else None
+
+    def launch(i: int, stream_ptr: int = sptr) -> None:
+        k = i % nbuf
+        st = cs.cs_attention_softmax_ex(ins[k].data_ptr(), outs[k].data_ptr(),
+                                        m_ptr, B, H, S, int(w.causal), opts,
+                                        stream_ptr)
+        if st != 0:
+            raise RuntimeError(f"cs_attention_softmax failed: {st}")
+
+    cs.get_error()
+    for i in range(max(3, args.warmup)):
+        launch(i)
+    torch.cuda.synchronize()
+    plan = cs.plan_attention(B, H, S, True, args.variant, args.param,
+                             args.threads)
+    tm = time_launches(args, torch, launch, stream, dist, local)
+    total_ms = reduce_max(dist, tm["ms"], dev)
+    stream_ms_max = reduce_max(dist, tm["stream_ms"], dev)
+    ms_per_step = total_ms / args.steps
+    rows = B * H * S
+    value = aggregate_rows_per_s(rows, world, ms_per_step * 1e-3)
+    err = cs.get_error()
+
+    # End to end: pinned host scores (and mask) in, the public call, the
+    # weights out.
+    h_x = torch.from_numpy(x).pin_memory()
+    h_m = torch.from_numpy(mask).pin_memory() if mask is not None else None
+    h_out = torch.empty((B, H, S, S), dtype=torch.float32).pin_memory()
+    d_x = torch.empty_like(xs)
+    d_m = torch.empty_like(md) if md is not None else None
+    d_out = torch.empty_like(xs)
+    e_steps = max(1, args.e2e_steps)
+
+    def e2e_step():
+        d_x.copy_(h_x, non_blocking=True)
+        if d_m is not None:
+            d_m.copy_(h_m, non_blocking=True)
+        cs.attention_softmax(d_x, d_m, w.causal, out=d_out,
+                             variant=args.variant, param=args.param,
+                             threads=args.threads)
+        h_out.copy_(d_out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(dist, e0.elapsed_time(e1), dev) / e_steps
+    e2e_value = aggregate_rows_per_s(rows, world, e2e_ms * 1e-3)
+
+    line = None
+    if rank == 0:
+        peaks = measured_peaks()
+        t_kernel = ms_per_step * 1e-3
+        hbm_rate = io_bytes / t_kernel / 1e9
+        kernel = ("attn_cta_kernel" if plan["variant"] == 2
+                  else "attn_rowgroup_kernel")
+        roof = {"bound": "hbm", "unit": "GB/s", "achieved": hbm_rate,
+                "peak": peaks["hbm_gbs"], "frac": hbm_rate / peaks["hbm_gbs"],
+                "traffic": None, "kernel": kernel,
+                "algorithmic_bytes": io_bytes,
+                "peak_source": f"{peaks['source']} copy bandwidth",
+                "roofline_us": io_bytes / (peaks["hbm_gbs"] * 1e9) * 1e6}
+        cpu = None
+        if not args.no_cpu_baseline:
+            import oracle
+            threads = oracle.default_threads()
+            s = run_oracle_attention_sample(w, x, mask, args.cpu_seconds,
+                                            threads)
+            cpu = {"value": s["rows_per_s"], "unit": "rows/s",
+                   "cores": threads, "kind": "oracle",
+                   "sample": f"{s['rows']} rows in whole (batch, head) "
+                             f"blocks of the workload, cycled, in "
+                             f"{s['seconds']:.1f} s"}
+        page_ms = 0.2 if w.name == "attention_32x8x512" else None
+        line = {
+            "op": "attention", "metric": ATTENTION_METRIC, "value": value,
+            "unit": "rows/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "launch": "cuda_graph" if tm["graph"] is not None else "stream",
+            "ms_per_step_stream_launches": stream_ms_max / args.steps,
+            "hbm_gbs": hbm_rate, "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "baseline_note": ("page figure 0.2 ms on an RTX 3080 for this "
+                              "shape (another machine)") if page_ms else None,
+            "dtype": "f32", "data": "synthetic",
+            "config": dict(attention_config(w, l2_note),
+                           parallelism=f"replicas x{world}",
+                           variant=args.variant, plan=plan),
+            "roofline": roof, "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "rows/s",
+                    "ms_per_step": e2e_ms,
+                    "h2d_bytes_per_step": 4 * w.elements
+                    + (4 * B * S if mask is not None else 0),
+                    "d2h_bytes_per_step": 4 * w.elements},
+            "gpu_launches": args.steps,
+            "clocks": tm["sampler"].summary(tm["t0"], tm["t1"]),
+            "device_errors": sorted(err),
+        }
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None) -> int:
     args = parse_args(argv)
+    if args.op == "attention":
+        name = args.workload if args.workload in wl.ATTENTION_WORKLOADS \
+            else wl.ATTN_PAGE.name
+        aw = wl.ATTENTION_WORKLOADS[name]
+        if args.impl == "reference":
+            return attention_reference_arm(args, aw)
+        return attention_arm(args, aw)
     w = find_workload(args.workload)
     if args.batch:
         w = w.with_(batch=min(args.batch, w.batch),

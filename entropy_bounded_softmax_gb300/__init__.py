@@ -3,7 +3,9 @@
 For each row of a [batch, num_classes] fp32 logit matrix: softmax and its
 entropy; if the entropy exceeds ``entropy_bound`` the temperature is bisected
 on [t_min, min(1, t_max)] for ``max_iter`` steps and softmax(l / T) is
-written ("BURT-IMMA CUDA Kernel API Reference", section 2.1).  The backward
+written ("BURT-IMMA CUDA Kernel API Reference", section 2.1);
+:func:`attention_softmax` is section 2.6's masked, optionally causal row
+softmax of attention scores.  The backward
 (section 6.3, with the 1/T of softmax(l / T) restored) gives the gradient
 with respect to the logits; :class:`ConstrainedSoftmaxFunction` joins the two
 for autograd.
@@ -16,10 +18,13 @@ raise if the library is missing or the tensors are not on a CUDA device.
 from __future__ import annotations
 
 from . import _lib
-from ._lib import (CONSTANTS, cs_check_args, cs_check_backward_args,
-                   cs_constrained_softmax, cs_constrained_softmax_backward,
+from ._lib import (CONSTANTS, cs_attention_softmax, cs_attention_softmax_ex,
+                   cs_check_args, cs_check_attention_args,
+                   cs_check_backward_args, cs_constrained_softmax,
+                   cs_constrained_softmax_backward,
                    cs_constrained_softmax_backward_ex,
                    cs_constrained_softmax_ex, cs_get_error,
+                   cs_plan_attention_host, cs_plan_attention_launch,
                    cs_plan_backward_host, cs_plan_backward_launch,
                    cs_plan_host, cs_plan_launch, cs_probe_ex2,
                    cs_probe_ex2_sink_floats, cs_status_string,
@@ -35,6 +40,9 @@ __all__ = [
     "cs_plan_backward_launch", "cs_plan_backward_host", "cs_check_args",
     "cs_check_backward_args", "cs_probe_ex2", "cs_probe_ex2_sink_floats",
     "cs_test_wait_timeout", "cs_version", "cs_status_string",
+    "attention_softmax", "plan_attention", "cs_attention_softmax",
+    "cs_attention_softmax_ex", "cs_plan_attention_launch",
+    "cs_plan_attention_host", "cs_check_attention_args",
 ]
 
 # Defaults of section 2.1's signature.
@@ -165,6 +173,62 @@ def constrained_softmax_backward(probs, grad_output, t, out=None,
     if st != 0:
         raise CsError(st, "cs_constrained_softmax_backward")
     return out
+
+
+def attention_softmax(scores, mask=None, causal: bool = False, out=None,
+                      variant: str = "auto", param: int = 0,
+                      threads: int = 0):
+    """Section 2.6 attention_softmax of CUDA fp32 scores [B, H, S, S].
+
+    ``mask`` is None or an additive fp32 mask of shape [B, S] or
+    [B, 1, 1, S] (0 attends; -inf, or the page's -1e9, masks); ``causal``
+    removes keys j > i from row i.  ``out`` may be given, ``scores`` itself
+    included (in place).  Asynchronous on the current stream; rows with
+    NaN/Inf inputs are zeroed and reported by :func:`get_error`.
+    """
+    import torch
+    if not isinstance(scores, torch.Tensor) or scores.device.type != "cuda":
+        raise ValueError("scores must be a CUDA tensor")
+    if (scores.dtype != torch.float32 or scores.dim() != 4
+            or scores.shape[2] != scores.shape[3] or not scores.is_contiguous()):
+        raise ValueError("scores must be a contiguous float32 [B, H, S, S] "
+                         "tensor")
+    B, H, S, _ = scores.shape
+    m_ptr = None
+    if mask is not None:
+        if (not isinstance(mask, torch.Tensor) or mask.dtype != torch.float32
+                or mask.device != scores.device or not mask.is_contiguous()
+                or mask.numel() != B * S
+                or tuple(mask.shape) not in ((B, S), (B, 1, 1, S))):
+            raise ValueError("mask must be a contiguous float32 [B, S] or "
+                             "[B, 1, 1, S] tensor on the scores' device")
+        m_ptr = mask.data_ptr()
+    if out is None:
+        out = torch.empty_like(scores)
+    elif (out.shape != scores.shape or out.dtype != torch.float32
+          or out.device != scores.device or not out.is_contiguous()):
+        raise ValueError("out must be a contiguous float32 tensor shaped like "
+                         "scores on the same device")
+    with torch.cuda.device(scores.device):
+        st = cs_attention_softmax_ex(
+            scores.data_ptr(), out.data_ptr(), m_ptr, B, H, S,
+            int(bool(causal)), options(VARIANTS[variant], param, threads, 0),
+            _stream_handle(scores.device))
+    if st != 0:
+        raise CsError(st, "cs_attention_softmax")
+    return out
+
+
+def plan_attention(batch: int, heads: int, seq_len: int, aligned: bool = True,
+                   variant: str = "auto", param: int = 0,
+                   threads: int = 0) -> dict:
+    """The attention_softmax launch plan on the current device."""
+    st, p = cs_plan_attention_launch(batch, heads, seq_len, int(aligned),
+                                     options(VARIANTS[variant], param,
+                                             threads, 0))
+    if st != 0:
+        raise CsError(st, "cs_plan_attention_launch")
+    return p.as_dict()
 
 
 def _autograd_function():

@@ -90,6 +90,18 @@ _SIGNATURES = {
                                      _I32, _I32, _I32, _I32,
                                      ctypes.POINTER(cs_plan)]),
     "cs_check_backward_args": (_I32, [_VP, _VP, _VP, _VP, _I64, _I32]),
+    "cs_attention_softmax": (_I32, [_VP, _VP, _VP, _I32, _I32, _I32, _I32,
+                                    _VP]),
+    "cs_attention_softmax_ex": (_I32, [_VP, _VP, _VP, _I32, _I32, _I32, _I32,
+                                       ctypes.POINTER(cs_options), _VP]),
+    "cs_plan_attention_launch": (_I32, [_I32, _I32, _I32, _I32,
+                                        ctypes.POINTER(cs_options),
+                                        ctypes.POINTER(cs_plan)]),
+    "cs_plan_attention_host": (_I32, [_I32, _I32, _I32, _I32,
+                                      ctypes.POINTER(cs_options), _I32, _I32,
+                                      _I32, ctypes.POINTER(cs_plan)]),
+    "cs_check_attention_args": (_I32, [_VP, _VP, _VP, _I32, _I32, _I32,
+                                       _I32]),
     "cs_probe_ex2": (_I32, [_VP, _I32, ctypes.POINTER(_I64), _VP]),
     "cs_probe_ex2_sink_floats": (_I32, []),
     "cs_test_wait_timeout": (_I32, [_I64, _VP]),
@@ -210,6 +222,42 @@ def cs_check_backward_args(probs, grad_out, t, grad_in, batch,
                            num_classes) -> int:
     return load().cs_check_backward_args(probs, grad_out, t, grad_in, batch,
                                          num_classes)
+
+
+def cs_attention_softmax(scores, out, mask, batch, heads, seq_len, causal,
+                         stream) -> int:
+    return load().cs_attention_softmax(scores, out, mask, batch, heads,
+                                       seq_len, causal, stream)
+
+
+def cs_attention_softmax_ex(scores, out, mask, batch, heads, seq_len, causal,
+                            opt, stream) -> int:
+    return load().cs_attention_softmax_ex(scores, out, mask, batch, heads,
+                                          seq_len, causal, _opt_ref(opt),
+                                          stream)
+
+
+def cs_plan_attention_launch(batch, heads, seq_len, aligned, opt=None):
+    p = cs_plan()
+    st = load().cs_plan_attention_launch(batch, heads, seq_len, aligned,
+                                         _opt_ref(opt), ctypes.byref(p))
+    return st, p
+
+
+def cs_plan_attention_host(batch, heads, seq_len, aligned, opt, sm_count,
+                           smem_per_block_optin, smem_per_sm):
+    p = cs_plan()
+    st = load().cs_plan_attention_host(batch, heads, seq_len, aligned,
+                                       _opt_ref(opt), sm_count,
+                                       smem_per_block_optin, smem_per_sm,
+                                       ctypes.byref(p))
+    return st, p
+
+
+def cs_check_attention_args(scores, out, mask, batch, heads, seq_len,
+                            causal) -> int:
+    return load().cs_check_attention_args(scores, out, mask, batch, heads,
+                                          seq_len, causal)
 
 
 def cs_probe_ex2(sink, iters, stream) -> tuple[int, int]:

@@ -326,6 +326,83 @@ cs_status plan_backward_cluster(int64_t batch, int32_t C, const cs_options& o,
     return CS_OK;
 }
 
+// ------------------------------------------------------------------ attention
+cs_status plan_attention(int32_t batch, int32_t heads, int32_t S,
+                         int32_t aligned, const cs_options& o, int sm_count,
+                         int smem_optin, int smem_per_sm, cs_plan* p) {
+    (void)sm_count;
+    if (o.strict != 0) return CS_ERR_INVALID_ARG;
+    const int64_t rows = static_cast<int64_t>(batch) * heads * S;
+    // Float4s a row spans: exact for aligned rows, else at the worst
+    // alignment of a row start.
+    int64_t q = aligned ? ceil_div(S, 4) : (static_cast<int64_t>(S) + 6) / 4;
+    if (q < 1) q = 1;
+    int variant = o.variant;
+    if (variant == CS_VARIANT_AUTO) {
+        if (o.param != 0 || o.threads != 0) return CS_ERR_INVALID_ARG;
+        variant = q <= kRowgroupMaxLanes * kRowgroupMaxE4 ? CS_VARIANT_ROWGROUP
+                                                          : CS_VARIANT_CLUSTER;
+    }
+    *p = cs_plan{};
+    if (variant == CS_VARIANT_ROWGROUP) {
+        if (o.threads != 0) return CS_ERR_INVALID_ARG;
+        int G = 0;
+        if (o.param == 0) {
+            for (int g = 1; g <= kRowgroupMaxLanes; g <<= 1) {
+                if (ceil_div(q, g) <= kAutoRowgroupE4) {
+                    G = g;
+                    break;
+                }
+            }
+            if (G == 0) G = kRowgroupMaxLanes;
+        } else {
+            if (o.param < 1 || o.param > kRowgroupMaxLanes || (o.param & (o.param - 1)))
+                return CS_ERR_INVALID_ARG;
+            G = o.param;
+        }
+        const int e4 = next_pow2(ceil_div(q, G));
+        if (e4 > kRowgroupMaxE4) return CS_ERR_OOM;
+        const int64_t blocks = ceil_div(rows * G, cs::kAttnGroupThreads);
+        if (blocks > kMaxGridX) return CS_ERR_DIM_MISMATCH;
+        p->variant = CS_VARIANT_ROWGROUP;
+        p->lanes_per_row = G;
+        p->elems_per_lane = 4 * e4;
+        p->threads_per_cta = cs::kAttnGroupThreads;
+        int regs = ((4 * e4 + 30 + 7) / 8) * 8;
+        p->ctas_per_sm = 65536 / (regs * cs::kAttnGroupThreads);
+        if (p->ctas_per_sm > 2048 / cs::kAttnGroupThreads)
+            p->ctas_per_sm = 2048 / cs::kAttnGroupThreads;
+        p->grid_ctas = blocks;
+        return CS_OK;
+    }
+    if (variant != CS_VARIANT_CLUSTER) return CS_ERR_INVALID_ARG;
+    if (o.param != 0 && o.param != 1) return CS_ERR_INVALID_ARG;
+    if (o.threads != 0 &&
+        (o.threads < 64 || o.threads > cs::kAttnMaxThreads || o.threads % 32))
+        return CS_ERR_INVALID_ARG;
+    const int64_t smem = cs::attention_smem_bytes(S);
+    if (smem > smem_optin) return CS_ERR_OOM;
+    int threads = o.threads;
+    if (threads == 0) {
+        // About eight float4s per thread.
+        int64_t t = ceil_div(ceil_div(q, 8), 32) * 32;
+        if (t < 64) t = 64;
+        if (t > cs::kAttnMaxThreads) t = cs::kAttnMaxThreads;
+        threads = static_cast<int>(t);
+    }
+    p->variant = CS_VARIANT_CLUSTER;
+    p->cluster_size = 1;
+    p->slice_len = S;
+    p->threads_per_cta = threads;
+    p->smem_bytes = static_cast<int32_t>(smem);
+    p->staged_tensors = 1;
+    const int by_smem = static_cast<int>(smem_per_sm / (smem + 1024));
+    const int by_threads = 2048 / threads;
+    p->ctas_per_sm = by_smem < by_threads ? by_smem : by_threads;
+    p->grid_ctas = rows < kMaxGridX ? rows : kMaxGridX;
+    return CS_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -573,6 +650,106 @@ cs_status cs_constrained_softmax_backward(const float* probs,
     return cs_constrained_softmax_backward_ex(probs, grad_out, t, grad_in,
                                               batch, num_classes, nullptr,
                                               stream);
+}
+
+cs_status cs_check_attention_args(const float* scores, const float* out,
+                                  const float* mask, int32_t batch,
+                                  int32_t heads, int32_t seq_len,
+                                  int32_t causal) {
+    if (batch < 0 || heads < 0 || seq_len < 0) return CS_ERR_DIM_MISMATCH;
+    if (causal != 0 && causal != 1) return CS_ERR_INVALID_ARG;
+    if (seq_len > CS_MAX_SEQ_LEN) return CS_ERR_OOM;
+    const int64_t rows = static_cast<int64_t>(batch) * heads * seq_len;
+    if (rows == 0) return CS_OK;
+    if (rows > INT64_MAX / 4 / seq_len) return CS_ERR_DIM_MISMATCH;
+    if (!scores || !out) return CS_ERR_INVALID_ARG;
+    const int64_t bytes = rows * seq_len * 4;
+    if (out != scores && ranges_overlap(out, bytes, scores, bytes))
+        return CS_ERR_INVALID_ARG;
+    if (mask && ranges_overlap(mask, static_cast<int64_t>(batch) * seq_len * 4,
+                               out, bytes))
+        return CS_ERR_INVALID_ARG;
+    return CS_OK;
+}
+
+cs_status cs_plan_attention_host(int32_t batch, int32_t heads,
+                                 int32_t seq_len, int32_t aligned,
+                                 const cs_options* options, int32_t sm_count,
+                                 int32_t smem_per_block_optin,
+                                 int32_t smem_per_sm, cs_plan* plan) {
+    if (!plan) return CS_ERR_INVALID_ARG;
+    if (batch < 0 || heads < 0 || seq_len < 1) return CS_ERR_DIM_MISMATCH;
+    if (seq_len > CS_MAX_SEQ_LEN) return CS_ERR_OOM;
+    if (aligned != 0 && aligned != 1) return CS_ERR_INVALID_ARG;
+    if (sm_count < 1 || smem_per_block_optin < 1 || smem_per_sm < 1)
+        return CS_ERR_INVALID_ARG;
+    const cs_options o = options ? *options : cs_options{};
+    return plan_attention(batch, heads, seq_len, aligned, o, sm_count,
+                          smem_per_block_optin, smem_per_sm, plan);
+}
+
+cs_status cs_plan_attention_launch(int32_t batch, int32_t heads,
+                                   int32_t seq_len, int32_t aligned,
+                                   const cs_options* options, cs_plan* plan) {
+    DeviceInfo* d = nullptr;
+    const cs_status st = device_info(&d);
+    if (st != CS_OK) return st;
+    return cs_plan_attention_host(batch, heads, seq_len, aligned, options,
+                                  d->sm_count, d->smem_optin, d->smem_per_sm,
+                                  plan);
+}
+
+cs_status cs_attention_softmax_ex(const float* scores, float* out,
+                                  const float* mask, int32_t batch,
+                                  int32_t heads, int32_t seq_len,
+                                  int32_t causal, const cs_options* options,
+                                  void* stream) {
+    cs_status st = cs_check_attention_args(scores, out, mask, batch, heads,
+                                           seq_len, causal);
+    if (st != CS_OK) return st;
+    const int64_t rows = static_cast<int64_t>(batch) * heads * seq_len;
+    if (rows == 0) return CS_OK;
+    DeviceInfo* d = nullptr;
+    st = device_info(&d);
+    if (st != CS_OK) return st;
+    const bool aligned = seq_len % 4 == 0 &&
+                         (reinterpret_cast<uintptr_t>(scores) & 15) == 0 &&
+                         (reinterpret_cast<uintptr_t>(out) & 15) == 0;
+    cs_plan p;
+    st = cs_plan_attention_host(batch, heads, seq_len, aligned ? 1 : 0,
+                                options, d->sm_count, d->smem_optin,
+                                d->smem_per_sm, &p);
+    if (st != CS_OK) return st;
+    cs::AttnTask task;
+    task.scores = scores;
+    task.out = out;
+    task.mask = mask;
+    task.err = d->err;
+    task.rows = rows;
+    task.heads = heads;
+    task.seq_len = seq_len;
+    task.causal = causal;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (p.variant == CS_VARIANT_ROWGROUP)
+        e = cs::launch_attention_rowgroup(task, p.lanes_per_row,
+                                          p.elems_per_lane, s);
+    else
+        e = cs::launch_attention_cta(task, p.threads_per_cta, p.smem_bytes,
+                                     p.grid_ctas, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return CS_ERR_CUDA;
+    }
+    return CS_OK;
+}
+
+cs_status cs_attention_softmax(const float* scores, float* out,
+                               const float* mask, int32_t batch,
+                               int32_t heads, int32_t seq_len,
+                               int32_t causal, void* stream) {
+    return cs_attention_softmax_ex(scores, out, mask, batch, heads, seq_len,
+                                   causal, nullptr, stream);
 }
 
 int32_t cs_probe_ex2_sink_floats(void) {

@@ -129,6 +129,35 @@ cudaError_t launch_backward_cluster(const BwdTask& task, int cluster_size,
                                     bool stage_g, int64_t grid_ctas,
                                     cudaStream_t stream);
 
+// One attention_softmax launch: rows = B H S rows of S scores.
+struct AttnTask {
+    const float* scores;   // [B, H, S, S]
+    float* out;            // [B, H, S, S]
+    const float* mask;     // [B, S] or null
+    unsigned int* err;     // device error word
+    int64_t rows;          // B H S
+    int32_t heads;
+    int32_t seq_len;
+    int32_t causal;
+};
+
+// attention_softmax geometry: row-group CTAs of 256 threads; row-CTA
+// kernel of up to 512 threads with a 512-byte header (reduction slots)
+// before the row in shared memory.
+constexpr int kAttnGroupThreads = 256;
+constexpr int kAttnMaxThreads = 512;
+constexpr int kAttnSmemHeader = 512;
+
+inline int64_t attention_smem_bytes(int64_t seq_len) {
+    return kAttnSmemHeader + ((seq_len + 6) / 4 + 1) * 16;
+}
+
+cudaError_t launch_attention_rowgroup(const AttnTask& task, int lanes_per_row,
+                                      int elems_per_lane, cudaStream_t stream);
+cudaError_t launch_attention_cta(const AttnTask& task, int threads,
+                                 int smem_bytes, int64_t grid_ctas,
+                                 cudaStream_t stream);
+
 cudaError_t launch_rowgroup(const RowTask& task, int lanes_per_row,
                             int elems_per_lane, cudaStream_t stream);
 cudaError_t launch_cluster(const RowTask& task, int cluster_size,

@@ -191,3 +191,76 @@ def backward_inputs(w: Workload, rows=None) -> tuple[np.ndarray, np.ndarray]:
         g[sel] = gb[rows_arr[sel] - r0]
         T[sel] = tb[rows_arr[sel] - r0]
     return g, T
+
+
+# attention_softmax workloads ("BURT-IMMA CUDA Kernel API Reference",
+# section 2.6 Performance Notes and section 7.1: batch 32, 8 heads, seq_len
+# 512), plus a causal variant and a long-row case past the page's 2048-key
+# two-pass threshold.  Scores ~ N(0, 1) fp32 (scaled dot products).  Mask:
+# each batch keeps its first L_b keys, L_b ~ U{S/2, ..., S}, and masks the
+# rest with the page's -1e9 (or -inf for mask="neg_inf").
+@dataclass(frozen=True)
+class AttentionWorkload:
+    name: str
+    batch: int
+    heads: int
+    seq_len: int
+    causal: bool
+    mask: str = "neg_1e9"      # "none" | "neg_1e9" | "neg_inf"
+    seed: int = 2000
+    note: str = ""
+
+    @property
+    def rows(self) -> int:
+        return self.batch * self.heads * self.seq_len
+
+    @property
+    def elements(self) -> int:
+        return self.rows * self.seq_len
+
+
+ATTN_PAGE = AttentionWorkload(
+    "attention_32x8x512", 32, 8, 512, False, "neg_1e9", 2001,
+    note="batch 32, 8 heads, seq_len 512, N(0,1) scores, -1e9 padding mask")
+ATTN_PAGE_CAUSAL = AttentionWorkload(
+    "attention_32x8x512_causal", 32, 8, 512, True, "neg_1e9", 2002,
+    note="as attention_32x8x512, causal")
+ATTN_LONG = AttentionWorkload(
+    "attention_2x8x4096_causal", 2, 8, 4096, True, "neg_inf", 2003,
+    note="batch 2, 8 heads, seq_len 4096, causal, -inf padding mask")
+ATTENTION_WORKLOADS = {w.name: w for w in (ATTN_PAGE, ATTN_PAGE_CAUSAL,
+                                           ATTN_LONG)}
+
+
+def attention_mask(w: AttentionWorkload) -> np.ndarray | None:
+    """The [B, S] fp32 additive mask (None for mask="none")."""
+    if w.mask == "none":
+        return None
+    rng = np.random.Generator(np.random.PCG64([w.seed, 1 << 30]))
+    S = w.seq_len
+    lengths = rng.integers(S // 2, S + 1, size=w.batch)
+    value = np.float32(-1e9) if w.mask == "neg_1e9" else np.float32(-np.inf)
+    m = np.zeros((w.batch, S), dtype=np.float32)
+    for b in range(w.batch):
+        m[b, lengths[b]:] = value
+    return m
+
+
+def generate_attention(w: AttentionWorkload, rows=None) -> np.ndarray:
+    """Scores of the workload's rows (flattened row index r = (b H + h) S +
+    i), shape [n, S]; all rows when ``rows`` is None.  Rows are drawn in
+    blocks of BLOCK_ROWS from Generator(PCG64([seed, block]))."""
+    S = w.seq_len
+    rows_arr = (np.arange(w.rows) if rows is None
+                else np.asarray(rows, dtype=np.int64).reshape(-1))
+    if rows_arr.size and (rows_arr.min() < 0 or rows_arr.max() >= w.rows):
+        raise IndexError("row index out of range")
+    out = np.empty((rows_arr.size, S), dtype=np.float32)
+    for blk in np.unique(rows_arr // BLOCK_ROWS):
+        r0 = int(blk) * BLOCK_ROWS
+        n = min(w.rows, r0 + BLOCK_ROWS) - r0
+        rng = _block_rng(w.seed, int(blk))
+        xb = rng.standard_normal((n, S), dtype=np.float32)
+        sel = np.flatnonzero(rows_arr // BLOCK_ROWS == blk)
+        out[sel] = xb[rows_arr[sel] - r0]
+    return out

@@ -68,6 +68,10 @@ typedef int32_t cs_status;
  * in shared memory. */
 #define CS_MAX_NUM_CLASSES 850000
 
+/* Largest seq_len cs_attention_softmax accepts: one CTA holding a row in
+ * shared memory. */
+#define CS_MAX_SEQ_LEN 57344
+
 /* Launch options; an all-zero struct (or NULL) means "automatic". */
 typedef struct cs_options {
     int32_t variant;   /* CS_VARIANT_AUTO, _ROWGROUP or _CLUSTER            */
@@ -258,6 +262,74 @@ cs_status cs_plan_backward_host(int64_t batch, int32_t num_classes,
 cs_status cs_check_backward_args(const float* probs, const float* grad_out,
                                  const float* t, const float* grad_in,
                                  int64_t batch, int32_t num_classes);
+
+/*
+ * cs_attention_softmax -- section 2.6 `attention_softmax`.  For every row
+ * (b, h, i) of the scores, with keys j = 0..seq_len-1:
+ *
+ *   1. v_j = scores[b, h, i, j] + mask[b, j], added in fp32 (mask NULL
+ *      adds nothing); a mask value of -inf removes key j, and the page's
+ *      -1e9 works as written (near 1e9 fp32 steps by 64);
+ *   2. causal: keys j > i are removed and never read;
+ *   3. out = softmax over the kept keys with the max subtracted (exp on the
+ *      ex2 unit, fp32 sums); removed keys get exactly 0.
+ *
+ * scores   device pointer, [batch, heads, seq_len, seq_len] fp32,
+ *          row-major.  Read only.
+ * out      device pointer, same shape, written completely.  May be the same
+ *          pointer as scores (in place, which section 2.6 allows); any
+ *          other overlap returns CS_ERR_INVALID_ARG.
+ * mask     device pointer, [batch, seq_len] fp32 (section 2.6's
+ *          [batch, 1, 1, seq_len]), or NULL.  Read only; must not overlap
+ *          out.
+ * batch, heads, seq_len  >= 0 (no rows: a no-op returning CS_OK);
+ *          seq_len <= CS_MAX_SEQ_LEN.
+ * causal   0 or 1.
+ * stream   a cudaStream_t (NULL = the legacy default stream).
+ *
+ * Any 4-byte alignment is accepted; rows that start 16-byte aligned (an
+ * aligned base and seq_len % 4 == 0) take 128-bit loads and stores.
+ * Section 5.3: a NaN or an infinity among the scores and mask values a row
+ * uses (a mask of -inf excepted) zeroes that row and ORs CS_ERR_NAN_INPUT
+ * (a NaN was seen) or CS_ERR_INF_INPUT into the error word (cs_get_error).
+ * A row whose keys are all removed is written as zeros without a flag.
+ * Ownership, execution and argument errors: as cs_constrained_softmax.
+ */
+cs_status cs_attention_softmax(const float* scores, float* out,
+                               const float* mask, int32_t batch,
+                               int32_t heads, int32_t seq_len,
+                               int32_t causal, void* stream);
+
+/*
+ * Same with launch options (NULL = automatic): CS_VARIANT_ROWGROUP (param =
+ * lanes per row, 1..32, a power of two; at most 32 scores per lane, else
+ * CS_ERR_OOM) or CS_VARIANT_CLUSTER, which here means one CTA per row
+ * (param 0 or 1; threads as for the forward).  strict must be 0.
+ */
+cs_status cs_attention_softmax_ex(const float* scores, float* out,
+                                  const float* mask, int32_t batch,
+                                  int32_t heads, int32_t seq_len,
+                                  int32_t causal, const cs_options* options,
+                                  void* stream);
+
+/* The attention launch plan on the current device (no launch), and the
+ * same planning on given device limits, host-only.  aligned = 1 when every
+ * row starts 16-byte aligned (aligned scores and out, seq_len % 4 == 0),
+ * which lets the row-group plan count float4s exactly. */
+cs_status cs_plan_attention_launch(int32_t batch, int32_t heads,
+                                   int32_t seq_len, int32_t aligned,
+                                   const cs_options* options, cs_plan* plan);
+cs_status cs_plan_attention_host(int32_t batch, int32_t heads,
+                                 int32_t seq_len, int32_t aligned,
+                                 const cs_options* options, int32_t sm_count,
+                                 int32_t smem_per_block_optin,
+                                 int32_t smem_per_sm, cs_plan* plan);
+
+/* Host-only argument check of cs_attention_softmax (no CUDA call). */
+cs_status cs_check_attention_args(const float* scores, const float* out,
+                                  const float* mask, int32_t batch,
+                                  int32_t heads, int32_t seq_len,
+                                  int32_t causal);
 
 /*
  * Throughput probe of the ex2 unit, the unit this operation is bound by.

@@ -82,6 +82,9 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_attention_softmax_rows.argtypes = [
         f32p, f32p, f64p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
         ctypes.c_int64, ctypes.c_int32, i32p]
+    lib.oracle_attention_softmax_row.restype = ctypes.c_int32
+    lib.oracle_attention_softmax_row.argtypes = [
+        f32p, f32p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, f64p]
     lib.oracle_constrained_softmax_backward_rows.restype = None
     lib.oracle_constrained_softmax_backward_rows.argtypes = [
         f64p, f64p, f64p, f64p, ctypes.c_int64, ctypes.c_int64,
@@ -298,6 +301,25 @@ def attention_softmax(scores, mask=None, causal: bool = False,
                       for i in range(n) if edges[i + 1] > edges[i]]:
                 f.result()
     return AttentionResult(p, flags)
+
+
+def attention_softmax_row(s, i: int, mask_row=None, causal: bool = False,
+                          lib: ctypes.CDLL | None = None):
+    """One row of attention_softmax: fp32 scores s [S] of query i, the
+    batch's mask row [S] or None.  Returns (p [S] float64, flag)."""
+    lib = lib or load()
+    row = _as_row(s)
+    m = None
+    if mask_row is not None:
+        m = np.ascontiguousarray(np.asarray(mask_row, dtype=np.float32).reshape(-1))
+        if m.size != row.size:
+            raise ValueError("mask row must match the scores row")
+    p = np.empty(row.size, dtype=np.float64)
+    flag = lib.oracle_attention_softmax_row(
+        _ptr(row, ctypes.c_float), _ptr(m, ctypes.c_float) if m is not None
+        else None, row.size, int(i), int(bool(causal)),
+        _ptr(p, ctypes.c_double))
+    return p, int(flag)
 
 
 def search_interval(t_min: float, t_max: float) -> tuple[float, float]:

@@ -250,6 +250,42 @@ static double masked_score(const float* s, const float* m, int64_t j)
     return (double)v;
 }
 
+/* One row: query i against keys 0..S-1; s the row's scores, m the batch's
+ * mask row or NULL; writes p[0..S) and returns the flag. */
+static int32_t attention_row(const float* s, const float* m, int64_t S,
+                             int64_t i, int32_t causal, double* p)
+{
+    /* Step 2: keys j > i are removed from a causal row. */
+    const int64_t kept_end = causal ? i + 1 : S;
+    int has_nan = 0, has_inf = 0;
+    for (int64_t j = 0; j < kept_end; ++j) {
+        if (isnan(s[j])) has_nan = 1;
+        else if (isinf(s[j])) has_inf = 1;
+        if (m) {
+            if (isnan(m[j])) has_nan = 1;
+            else if (isinf(m[j]) && m[j] > 0) has_inf = 1;
+        }
+    }
+    for (int64_t j = 0; j < S; ++j) p[j] = 0.0;
+    if (has_nan || has_inf)
+        return has_nan ? ORACLE_FLAG_NAN_INPUT : ORACLE_FLAG_INF_INPUT;
+    /* Step 3: softmax over the kept keys (a -inf value is a removed key
+     * and contributes exp(-inf) = 0). */
+    double vmax = -INFINITY;
+    for (int64_t j = 0; j < kept_end; ++j) {
+        const double v = masked_score(s, m, j);
+        if (v > vmax) vmax = v;
+    }
+    if (vmax == -INFINITY) return ORACLE_FLAG_NONE;   /* every key removed */
+    double sum = 0.0;
+    for (int64_t j = 0; j < kept_end; ++j) {
+        p[j] = exp(masked_score(s, m, j) - vmax);
+        sum += p[j];
+    }
+    for (int64_t j = 0; j < kept_end; ++j) p[j] /= sum;
+    return ORACLE_FLAG_NONE;
+}
+
 void oracle_attention_softmax_rows(const float* scores, const float* mask,
                                    double* out, int64_t row_begin,
                                    int64_t row_end, int64_t H, int64_t S,
@@ -258,39 +294,17 @@ void oracle_attention_softmax_rows(const float* scores, const float* mask,
     for (int64_t r = row_begin; r < row_end; ++r) {
         const int64_t b = r / (H * S);
         const int64_t i = r % S;
-        const float* s = scores + r * S;
         const float* m = mask ? mask + b * S : 0;
-        double* p = out + r * S;
-        /* Step 2: keys j > i are removed from a causal row. */
-        const int64_t kept_end = causal ? i + 1 : S;
-        int has_nan = 0, has_inf = 0;
-        for (int64_t j = 0; j < kept_end; ++j) {
-            if (isnan(s[j])) has_nan = 1;
-            else if (isinf(s[j])) has_inf = 1;
-            if (m) {
-                if (isnan(m[j])) has_nan = 1;
-                else if (isinf(m[j]) && m[j] > 0) has_inf = 1;
-            }
-        }
-        for (int64_t j = 0; j < S; ++j) p[j] = 0.0;
-        if (has_nan || has_inf) {
-            flags_out[r] = has_nan ? ORACLE_FLAG_NAN_INPUT : ORACLE_FLAG_INF_INPUT;
-            continue;
-        }
-        flags_out[r] = ORACLE_FLAG_NONE;
-        /* Step 3: softmax over the kept keys (a -inf value is a removed
-         * key and contributes exp(-inf) = 0). */
-        double vmax = -INFINITY;
-        for (int64_t j = 0; j < kept_end; ++j) {
-            const double v = masked_score(s, m, j);
-            if (v > vmax) vmax = v;
-        }
-        if (vmax == -INFINITY) continue;   /* every key removed */
-        double sum = 0.0;
-        for (int64_t j = 0; j < kept_end; ++j) {
-            p[j] = exp(masked_score(s, m, j) - vmax);
-            sum += p[j];
-        }
-        for (int64_t j = 0; j < kept_end; ++j) p[j] /= sum;
+        flags_out[r] = attention_row(scores + r * S, m, S, i, causal,
+                                     out + r * S);
     }
+}
+
+/* Public: one row given its query index i (for sampled rows of launches
+ * too large to recompute whole). */
+int32_t oracle_attention_softmax_row(const float* s, const float* m,
+                                     int64_t S, int64_t i, int32_t causal,
+                                     double* p)
+{
+    return attention_row(s, m, S, i, causal, p);
 }

@@ -534,6 +534,11 @@ def check_attention_mask_subset(lib) -> None:
                     ref = np.zeros(S)
                     ref[keep] = _scipy_rows(v[h, i, keep])
                     assert np.max(np.abs(r.p[b, h, i] - ref)) < 1e-13
+                    if (i + h) % 7 == 0:
+                        one, flag = oracle.attention_softmax_row(
+                            x[b, h, i], i, mask[b], causal, lib=lib)
+                        assert flag == 0
+                        assert np.max(np.abs(one - ref)) < 1e-13
 
 
 def check_attention_fp32_mask_addition(lib) -> None:

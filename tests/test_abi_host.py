@@ -284,3 +284,84 @@ def test_backward_forced_variants_and_limits():
     st1, p1 = cs.cs_plan_backward_host(32, 50000, None, 152, 232448, 233472,
                                        16)
     assert st1 == 0 and p1.as_dict() == bplan(32, 50000)[1]
+
+
+# ----------------------------------------------------------------- attention
+@pytest.mark.parametrize("args,status", [
+    ((A, B, None, 2, 2, 8, 0), 0),
+    ((A, A, None, 2, 2, 8, 1), 0),                # in place
+    ((A, B, A + 8192, 2, 2, 8, 0), 0),            # mask beside the scores
+    ((None, None, None, 0, 2, 8, 0), 0),
+    ((None, None, None, 2, 0, 8, 0), 0),
+    ((None, None, None, 2, 2, 0, 0), 0),
+    ((A, B, None, -1, 2, 8, 0), 6),
+    ((A, B, None, 2, -2, 8, 0), 6),
+    ((A, B, None, 2, 2, -8, 0), 6),
+    ((A, B, None, 2, 2, 8, 2), 8),                # causal not 0/1
+    ((A, B, None, 1, 1, 60000, 0), 7),
+    ((None, B, None, 2, 2, 8, 0), 8),
+    ((A, None, None, 2, 2, 8, 0), 8),
+    ((A, A + 16, None, 2, 2, 8, 0), 8),           # partial overlap
+    ((A, B, B + 64, 2, 2, 8, 0), 8),              # mask overlaps out
+    ((A, B, A + 64, 2, 2, 8, 0), 0),              # mask overlaps scores
+])
+def test_check_attention_args(args, status):
+    assert cs.cs_check_attention_args(*args) == status
+
+
+def aplan(batch, heads, S, aligned=1, variant=0, param=0, threads=0,
+          strict=0):
+    st, p = cs.cs_plan_attention_host(
+        batch, heads, S, aligned, cs.options(variant, param, threads, strict),
+        GB300["sm_count"], GB300["smem_per_block_optin"],
+        GB300["smem_per_sm"])
+    return st, p.as_dict()
+
+
+def test_attention_plans_for_the_workloads():
+    st, p = aplan(32, 8, 512)
+    assert st == 0 and p["variant"] == C["CS_VARIANT_ROWGROUP"]
+    assert (p["lanes_per_row"], p["elems_per_lane"]) == (32, 16)
+    assert p["grid_ctas"] * p["threads_per_cta"] == 32 * 8 * 512 * 32
+    st, p = aplan(2, 8, 4096)
+    assert st == 0 and p["variant"] == C["CS_VARIANT_CLUSTER"]
+    assert p["cluster_size"] == 1 and p["grid_ctas"] == 2 * 8 * 4096
+    assert p["smem_bytes"] >= 512 + 4096 * 4
+
+
+@pytest.mark.parametrize("S", [1, 2, 3, 5, 64, 127, 512, 1017, 1018, 1024,
+                               1025, 4096, 57344])
+@pytest.mark.parametrize("aligned", [0, 1])
+def test_attention_plans_hold_the_row(S, aligned):
+    st, p = aplan(1, 1, S, aligned)
+    assert st == 0
+    if p["variant"] == C["CS_VARIANT_ROWGROUP"]:
+        q = (S + 3) // 4 if aligned else (S + 6) // 4
+        assert p["lanes_per_row"] * p["elems_per_lane"] >= 4 * q
+    else:
+        assert p["smem_bytes"] <= GB300["smem_per_block_optin"]
+        assert p["smem_bytes"] >= 512 + 16 * ((S + 6) // 4)
+        assert 64 <= p["threads_per_cta"] <= 512
+        assert p["threads_per_cta"] % 32 == 0
+
+
+def test_attention_forced_variants_and_limits():
+    st, _ = aplan(1, 1, 100, 1, C["CS_VARIANT_ROWGROUP"], 1)
+    assert st == C["CS_ERR_OOM"]
+    st, p = aplan(1, 1, 32, 1, C["CS_VARIANT_ROWGROUP"], 1)
+    assert st == 0 and p["elems_per_lane"] == 32
+    st, _ = aplan(1, 1, 64, 1, C["CS_VARIANT_ROWGROUP"], 3)
+    assert st == C["CS_ERR_INVALID_ARG"]
+    st, _ = aplan(1, 1, 64, 1, C["CS_VARIANT_CLUSTER"], 2)
+    assert st == C["CS_ERR_INVALID_ARG"]
+    st, p = aplan(1, 1, 64, 1, C["CS_VARIANT_CLUSTER"], 1, 96)
+    assert st == 0 and p["threads_per_cta"] == 96
+    for bad in (dict(threads=48), dict(threads=544), dict(strict=1)):
+        st, _ = aplan(1, 1, 2048, 1, C["CS_VARIANT_CLUSTER"], 0, **bad)
+        assert st == C["CS_ERR_INVALID_ARG"], bad
+    st, _ = aplan(1, 1, 64, 1, C["CS_VARIANT_AUTO"], 4)
+    assert st == C["CS_ERR_INVALID_ARG"]
+    st, _ = aplan(1, 1, 64, 2)
+    assert st == C["CS_ERR_INVALID_ARG"]
+    st, _ = aplan(1, 1, 60000)
+    assert st == C["CS_ERR_OOM"]
