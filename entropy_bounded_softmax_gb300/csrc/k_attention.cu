@@ -70,29 +70,44 @@ __device__ __forceinline__ void store4(float* a, int pa, int pad, int len,
 }
 
 // Step 1 on four lanes: v = s + m (m = 0 without a mask).  bad becomes NaN
-// when a score is NaN or infinite or a mask value is NaN or +inf, and nan
-// becomes 1 when any of them is NaN; lanes past the kept keys hold
-// s = -inf, m = 0 and are not checked.
+// when a score is NaN or infinite or a mask value is NaN or +inf; lanes
+// past the kept keys hold s = -inf, m = 0 and are not checked.  Whether a
+// NaN was among them (the error code) is settled on the rare path by
+// rescan_nan().
 struct Step1 {
     float bad = 0.0f;
-    float nan = 0.0f;
-    __device__ __forceinline__ float one(float s, float m, bool kept) {
+    __device__ __forceinline__ float one(float s, float m, bool kept,
+                                         bool masked) {
         if (kept) {
             bad = fmaf(s, 0.0f, bad);
-            bad = fmaf(m == -INFINITY ? 0.0f : m, 0.0f, bad);
-            if (s != s || m != m) nan = 1.0f;
+            if (masked) bad = fmaf(m == -INFINITY ? 0.0f : m, 0.0f, bad);
         }
         return __fadd_rn(s, m);
     }
+    template <bool MASKED>
     __device__ __forceinline__ float4 apply(float4 s, float4 m, int q,
                                             int pad, int end) {
         const int j0 = 4 * q - pad;
-        return make_float4(one(s.x, m.x, j0 >= 0 && j0 < end),
-                           one(s.y, m.y, j0 + 1 >= 0 && j0 + 1 < end),
-                           one(s.z, m.z, j0 + 2 >= 0 && j0 + 2 < end),
-                           one(s.w, m.w, j0 + 3 >= 0 && j0 + 3 < end));
+        if (j0 >= 0 && j0 + 4 <= end)     // whole float4 kept
+            return make_float4(one(s.x, m.x, true, MASKED),
+                               one(s.y, m.y, true, MASKED),
+                               one(s.z, m.z, true, MASKED),
+                               one(s.w, m.w, true, MASKED));
+        return make_float4(one(s.x, m.x, j0 >= 0 && j0 < end, MASKED),
+                           one(s.y, m.y, j0 + 1 >= 0 && j0 + 1 < end, MASKED),
+                           one(s.z, m.z, j0 + 2 >= 0 && j0 + 2 < end, MASKED),
+                           one(s.w, m.w, j0 + 3 >= 0 && j0 + 3 < end, MASKED));
     }
 };
+
+// Rare path of a row with a non-finite input: whether a NaN is among its
+// kept scores and mask values (read again from global memory, before any
+// of the row is written).
+__device__ bool rescan_nan(const float* s, const float* m, int end) {
+    bool nan = false;
+    for (int j = 0; j < end; ++j) nan = nan || isnan(s[j]) || (m && isnan(m[j]));
+    return nan;
+}
 
 __device__ __forceinline__ float max4(float4 v) {
     return fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
@@ -157,29 +172,42 @@ attn_rowgroup_kernel(AttnTask t) {
     for (int k = 0; k < E; ++k) {
         const int q = lane + k * G;
         if (q < qk) {
-            const float4 mv = x.m ? load4f<false>(x.m, pm, pad, x.end, q, 0.0f)
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-            v[k] = st.apply(v[k], mv, q, pad, x.end);
+            if (x.m)
+                v[k] = st.apply<true>(v[k], load4f<false>(x.m, pm, pad, x.end, q, 0.0f),
+                                      q, pad, x.end);
+            else
+                v[k] = st.apply<false>(v[k], make_float4(0.f, 0.f, 0.f, 0.f), q,
+                                       pad, x.end);
         }
         mx = fmaxf(mx, max4(v[k]));
     }
-    float bad = st.bad, nan = st.nan;
+    float bad = st.bad;
 #pragma unroll
     for (int o = G >> 1; o > 0; o >>= 1) {
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         bad += __shfl_xor_sync(0xffffffffu, bad, o);
-        nan = fmaxf(nan, __shfl_xor_sync(0xffffffffu, nan, o));
     }
     const bool zero = bad != bad || mx == -INFINITY;
     float2 sum = make_float2(0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < E; ++k) {
-        v[k] = exp4(v[k], zero ? 0.0f : mx);
-        sum = add2(sum, add2(make_float2(v[k].x, v[k].y), make_float2(v[k].z, v[k].w)));
+        const int q = lane + k * G;
+        if (q < qk && !zero) {
+            v[k] = exp4(v[k], mx);
+            sum = add2(sum, add2(make_float2(v[k].x, v[k].y), make_float2(v[k].z, v[k].w)));
+        }
     }
     float tot = sum.x + sum.y;
 #pragma unroll
     for (int o = G >> 1; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    // The row's error code, read before any of it is written (in place).
+    unsigned int code = 0;
+    if (bad != bad) {
+        const unsigned int gmask = (G == 32 ? 0xffffffffu : ((1u << G) - 1u))
+                                   << ((threadIdx.x & 31) & ~(G - 1));
+        if (lane == 0 && live) code = rescan_nan(x.s, x.m, x.end) ? kBitNan : kBitInf;
+        __syncwarp(gmask);
+    }
     if (!live) return;
     const float inv = zero ? 0.0f : __frcp_rn(tot);
     const int po = pad_of(x.o);
@@ -189,7 +217,7 @@ attn_rowgroup_kernel(AttnTask t) {
         if (q < q4) store4(x.o, po, pad, S, q, (q < qk && !zero) ? scale4(v[k], inv)
                                                                  : make_float4(0.f, 0.f, 0.f, 0.f));
     }
-    if (lane == 0 && bad != bad) raise_error(t.err, nan > 0.0f ? kBitNan : kBitInf);
+    if (lane == 0) raise_error(t.err, code);
 }
 
 template <int G, int E>
@@ -270,32 +298,39 @@ attn_cta_kernel(AttnTask t) {
         Step1 st;
         float mx = -INFINITY;
         for (int q = threadIdx.x; q < qk; q += nt) {
-            const float4 mv = x.m ? load4f<false>(x.m, pm, pad, x.end, q, 0.0f)
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-            const float4 v = st.apply(row4[q], mv, q, pad, x.end);
+            const float4 v = x.m
+                ? st.apply<true>(row4[q], load4f<false>(x.m, pm, pad, x.end, q, 0.0f),
+                                 q, pad, x.end)
+                : st.apply<false>(row4[q], make_float4(0.f, 0.f, 0.f, 0.f), q,
+                                  pad, x.end);
             row4[q] = v;
             mx = fmaxf(mx, max4(v));
         }
-        float bad = st.bad, nan = st.nan;
-        cta_reduce(mx, bad, nan, slot_a);
+        float bad = st.bad, unused_d = 0.0f;
+        cta_reduce(mx, bad, unused_d, slot_a);
         const bool zero = bad != bad || mx == -INFINITY;
         // Pass 2: 2^y in place and the thread's sum.
         float2 sum = make_float2(0.f, 0.f);
-        for (int q = threadIdx.x; q < qk; q += nt) {
-            const float4 e = exp4(row4[q], zero ? 0.0f : mx);
+        for (int q = threadIdx.x; q < (zero ? 0 : qk); q += nt) {
+            const float4 e = exp4(row4[q], mx);
             row4[q] = e;
             sum = add2(sum, add2(make_float2(e.x, e.y), make_float2(e.z, e.w)));
         }
-        float unused_a = -INFINITY, tot = sum.x + sum.y, unused_d = 0.0f;
-        cta_reduce(unused_a, tot, unused_d, slot_b);
+        float unused_a = -INFINITY, tot = sum.x + sum.y, unused_b = 0.0f;
+        cta_reduce(unused_a, tot, unused_b, slot_b);
         const float inv = zero ? 0.0f : __frcp_rn(tot);
+        // The row's error code, read before any of it is written (in place).
+        unsigned int code = 0;
+        if (bad != bad) {
+            if (threadIdx.x == 0) code = rescan_nan(x.s, x.m, x.end) ? kBitNan : kBitInf;
+            __syncthreads();
+        }
         // Pass 3: the output, zeros past the kept keys and on zeroed rows.
         const int po = pad_of(x.o);
         const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int q = threadIdx.x; q < q4; q += nt)
             store4(x.o, po, pad, S, q, (q < qk && !zero) ? scale4(row4[q], inv) : z);
-        if (threadIdx.x == 0 && bad != bad)
-            raise_error(t.err, nan > 0.0f ? kBitNan : kBitInf);
+        if (threadIdx.x == 0) raise_error(t.err, code);
         // The row buffer and slots are rewritten by the next row.
         __syncthreads();
     }
