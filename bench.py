@@ -8,7 +8,9 @@ CUDA Kernel API Reference" (section 2.1 Performance Notes, section 7.1:
 0.8 ms on an RTX 3080).  Prints one JSON line:
   value       rows/s over all GPUs (device-timed, CUDA events);
   e2e         rows/s through the public API with pinned-host inputs, H2D
-              and D2H copies inside the timed region;
+              and D2H copies of every step inside the timed region
+              (consecutive steps on two streams, so that copies overlap the
+              neighbouring steps; the serial figure is reported beside it);
   roofline    the kernel against the slower of HBM (8 bytes per class) and
               the ex2 unit ((1 + bisection steps) ex2 per class per row),
               both peaks measured on this GPU (HBM: the copy bandwidth
@@ -374,6 +376,53 @@ def time_launches(args, torch, launch, stream, dist, local) -> dict:
             "t1": t_end, "sampler": sampler}
 
 
+# -------------------------------------------------------------------- e2e
+E2E_SLOTS = 2
+
+
+def time_e2e(torch, make_slot, step, stream, e_steps: int) -> dict:
+    """End-to-end steps through the public API.  make_slot() returns one
+    set of device and pinned-host buffers; step(slot) enqueues one whole
+    step on the current stream: the host-to-device copy of its inputs, the
+    call, the device-to-host copy of its result.  Timed twice with CUDA
+    events on `stream`: pipelined (consecutive steps alternate between
+    E2E_SLOTS streams and buffer sets, so one step's copies overlap the
+    neighbouring steps' call and copies, as a serving loop would run them)
+    and serial (every step on one stream).  Returns ms per step of each."""
+    slots = [make_slot() for _ in range(E2E_SLOTS)]
+    streams = [torch.cuda.Stream(device=stream.device)
+               for _ in range(E2E_SLOTS)]
+
+    def run(n: int, pipelined: bool) -> float:
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for st in streams:
+            st.wait_event(e0)
+        for i in range(n):
+            k = i % E2E_SLOTS if pipelined else 0
+            with torch.cuda.stream(streams[k]):
+                step(slots[k])
+        for st in streams:
+            stream.wait_stream(st)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    run(3, True)
+    run(3, False)
+    return {"pipelined": run(e_steps, True), "serial": run(e_steps, False)}
+
+
+def e2e_entry(value: float, ms: dict, h2d: int, d2h: int) -> dict:
+    return {"value": value, "unit": "rows/s", "ms_per_step": ms["pipelined"],
+            "ms_per_step_serial": ms["serial"],
+            "pipeline": f"{E2E_SLOTS} streams, one buffer set each; "
+                        "every step copies its inputs in and its result out",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
 # ---------------------------------------------------------------- our arm
 def our_arm(args, w: wl.Workload) -> int:
     import torch
@@ -435,38 +484,26 @@ def our_arm(args, w: wl.Workload) -> int:
     # End to end through the public API: pinned host input, H2D copy, the
     # call, D2H of the probabilities and temperatures, all inside events.
     h_in = torch.from_numpy(x).pin_memory()
-    h_out = torch.empty((B, C), dtype=torch.float32).pin_memory()
-    h_t = torch.empty(B, dtype=torch.float32).pin_memory()
-    d_in = torch.empty((B, C), dtype=torch.float32, device=dev)
-    e_steps = max(1, args.e2e_steps)
-    for _ in range(3):
-        d_in.copy_(h_in, non_blocking=True)
-        p, T = cs.constrained_softmax(d_in, w.entropy_bound, w.t_min, w.t_max,
-                                      w.max_iter, return_t=True,
-                                      variant=args.variant, param=args.param,
-                                      threads=args.threads,
-                                      strict=args.strict)
-        h_out.copy_(p, non_blocking=True)
-        h_t.copy_(T, non_blocking=True)
-    torch.cuda.synchronize()
-    out_e2e = torch.empty((B, C), dtype=torch.float32, device=dev)
-    t_e2e = torch.empty(B, dtype=torch.float32, device=dev)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e_steps):
-        d_in.copy_(h_in, non_blocking=True)
-        cs.constrained_softmax(d_in, w.entropy_bound, w.t_min, w.t_max,
-                               w.max_iter, out=out_e2e, t_out=t_e2e,
+
+    def make_slot():
+        return {"d_in": torch.empty((B, C), dtype=torch.float32, device=dev),
+                "out": torch.empty((B, C), dtype=torch.float32, device=dev),
+                "t": torch.empty(B, dtype=torch.float32, device=dev),
+                "h_out": torch.empty((B, C), dtype=torch.float32).pin_memory(),
+                "h_t": torch.empty(B, dtype=torch.float32).pin_memory()}
+
+    def e2e_step(sl):
+        sl["d_in"].copy_(h_in, non_blocking=True)
+        cs.constrained_softmax(sl["d_in"], w.entropy_bound, w.t_min, w.t_max,
+                               w.max_iter, out=sl["out"], t_out=sl["t"],
                                variant=args.variant, param=args.param,
-                               threads=args.threads,
-                               strict=args.strict)
-        h_out.copy_(out_e2e, non_blocking=True)
-        h_t.copy_(t_e2e, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = reduce_max(dist, e0.elapsed_time(e1), dev) / e_steps
-    e2e_value = aggregate_rows_per_s(B, world, e2e_ms * 1e-3)
+                               threads=args.threads, strict=args.strict)
+        sl["h_out"].copy_(sl["out"], non_blocking=True)
+        sl["h_t"].copy_(sl["t"], non_blocking=True)
+
+    e2e = time_e2e(torch, make_slot, e2e_step, stream, max(1, args.e2e_steps))
+    e2e = {k: reduce_max(dist, v, dev) for k, v in e2e.items()}
+    e2e_value = aggregate_rows_per_s(B, world, e2e["pipelined"] * 1e-3)
 
     line = None
     if rank == 0:
@@ -529,10 +566,7 @@ def our_arm(args, w: wl.Workload) -> int:
                            variant=args.variant, strict=args.strict,
                            plan=plan),
             "roofline": roof, "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": "rows/s",
-                    "ms_per_step": e2e_ms,
-                    "h2d_bytes_per_step": 4 * elems,
-                    "d2h_bytes_per_step": 4 * elems + 4 * B},
+            "e2e": e2e_entry(e2e_value, e2e, 4 * elems, 4 * elems + 4 * B),
             "gpu_launches": args.steps,
             "clocks": clocks,
             "device_errors": sorted(err),
@@ -675,35 +709,25 @@ def backward_arm(args, w: wl.Workload) -> int:
     h_p = p0.cpu().pin_memory()
     h_g = torch.from_numpy(g).pin_memory()
     h_t = t0.cpu().pin_memory()
-    h_out = torch.empty((B, C), dtype=torch.float32).pin_memory()
-    d_p = torch.empty_like(p0)
-    d_g = torch.empty_like(p0)
-    d_t = torch.empty_like(t0)
-    d_out = torch.empty_like(p0)
-    e_steps = max(1, args.e2e_steps)
 
-    def e2e_step():
-        d_p.copy_(h_p, non_blocking=True)
-        d_g.copy_(h_g, non_blocking=True)
-        d_t.copy_(h_t, non_blocking=True)
-        cs.constrained_softmax_backward(d_p, d_g, d_t, out=d_out,
-                                        variant=args.variant,
+    def make_slot():
+        return {"p": torch.empty_like(p0), "g": torch.empty_like(p0),
+                "t": torch.empty_like(t0), "out": torch.empty_like(p0),
+                "h_out": torch.empty((B, C), dtype=torch.float32).pin_memory()}
+
+    def e2e_step(sl):
+        sl["p"].copy_(h_p, non_blocking=True)
+        sl["g"].copy_(h_g, non_blocking=True)
+        sl["t"].copy_(h_t, non_blocking=True)
+        cs.constrained_softmax_backward(sl["p"], sl["g"], sl["t"],
+                                        out=sl["out"], variant=args.variant,
                                         param=args.param,
                                         threads=args.threads)
-        h_out.copy_(d_out, non_blocking=True)
+        sl["h_out"].copy_(sl["out"], non_blocking=True)
 
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = reduce_max(dist, e0.elapsed_time(e1), dev) / e_steps
-    e2e_value = aggregate_rows_per_s(B, world, e2e_ms * 1e-3)
+    e2e = time_e2e(torch, make_slot, e2e_step, stream, max(1, args.e2e_steps))
+    e2e = {k: reduce_max(dist, v, dev) for k, v in e2e.items()}
+    e2e_value = aggregate_rows_per_s(B, world, e2e["pipelined"] * 1e-3)
 
     line = None
     if rank == 0:
@@ -740,10 +764,7 @@ def backward_arm(args, w: wl.Workload) -> int:
                            variant=args.variant, plan=plan,
                            upstream_gradient="N(0,1) fp32, seeded"),
             "roofline": roof, "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": "rows/s",
-                    "ms_per_step": e2e_ms,
-                    "h2d_bytes_per_step": 8 * elems + 4 * B,
-                    "d2h_bytes_per_step": 4 * elems},
+            "e2e": e2e_entry(e2e_value, e2e, 8 * elems + 4 * B, 4 * elems),
             "gpu_launches": args.steps,
             "clocks": tm["sampler"].summary(tm["t0"], tm["t1"]),
         }
@@ -895,33 +916,26 @@ def attention_arm(args, w) -> int:
     # weights out.
     h_x = torch.from_numpy(x).pin_memory()
     h_m = torch.from_numpy(mask).pin_memory() if mask is not None else None
-    h_out = torch.empty((B, H, S, S), dtype=torch.float32).pin_memory()
-    d_x = torch.empty_like(xs)
-    d_m = torch.empty_like(md) if md is not None else None
-    d_out = torch.empty_like(xs)
-    e_steps = max(1, args.e2e_steps)
 
-    def e2e_step():
-        d_x.copy_(h_x, non_blocking=True)
-        if d_m is not None:
-            d_m.copy_(h_m, non_blocking=True)
-        cs.attention_softmax(d_x, d_m, w.causal, out=d_out,
+    def make_slot():
+        return {"x": torch.empty_like(xs),
+                "m": torch.empty_like(md) if md is not None else None,
+                "out": torch.empty_like(xs),
+                "h_out": torch.empty((B, H, S, S),
+                                     dtype=torch.float32).pin_memory()}
+
+    def e2e_step(sl):
+        sl["x"].copy_(h_x, non_blocking=True)
+        if sl["m"] is not None:
+            sl["m"].copy_(h_m, non_blocking=True)
+        cs.attention_softmax(sl["x"], sl["m"], w.causal, out=sl["out"],
                              variant=args.variant, param=args.param,
                              threads=args.threads)
-        h_out.copy_(d_out, non_blocking=True)
+        sl["h_out"].copy_(sl["out"], non_blocking=True)
 
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = reduce_max(dist, e0.elapsed_time(e1), dev) / e_steps
-    e2e_value = aggregate_rows_per_s(rows, world, e2e_ms * 1e-3)
+    e2e = time_e2e(torch, make_slot, e2e_step, stream, max(1, args.e2e_steps))
+    e2e = {k: reduce_max(dist, v, dev) for k, v in e2e.items()}
+    e2e_value = aggregate_rows_per_s(rows, world, e2e["pipelined"] * 1e-3)
 
     line = None
     if rank == 0:
@@ -964,11 +978,9 @@ def attention_arm(args, w) -> int:
                            parallelism=f"replicas x{world}",
                            variant=args.variant, plan=plan),
             "roofline": roof, "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": "rows/s",
-                    "ms_per_step": e2e_ms,
-                    "h2d_bytes_per_step": 4 * w.elements
-                    + (4 * B * S if mask is not None else 0),
-                    "d2h_bytes_per_step": 4 * w.elements},
+            "e2e": e2e_entry(e2e_value, e2e,
+                             4 * w.elements + (4 * B * S if mask is not None else 0),
+                             4 * w.elements),
             "gpu_launches": args.steps,
             "clocks": tm["sampler"].summary(tm["t0"], tm["t1"]),
             "device_errors": sorted(err),
