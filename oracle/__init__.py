@@ -9,7 +9,8 @@ The arithmetic lives in ``constrained_softmax_oracle.c`` (plain fp64 C, libm
 ``exp``/``log``), which follows "BURT-IMMA CUDA Kernel API Reference",
 section 2.1 ``constrained_softmax`` and section 5 (error codes, NaN/Inf policy,
 graceful degradation), the backward of section 6.3 with the temperature
-restored, and attention_softmax (section 2.6).  This module only compiles it with gcc, marshals numpy
+restored, attention_softmax (section 2.6) and biencoder_attention (section
+2.5).  This module only compiles it with gcc, marshals numpy
 arrays in and out through ctypes, and splits a batch over threads (rows are
 independent, so the split changes no arithmetic).
 
@@ -85,6 +86,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_attention_softmax_row.restype = ctypes.c_int32
     lib.oracle_attention_softmax_row.argtypes = [
         f32p, f32p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, f64p]
+    lib.oracle_biencoder_scores.restype = None
+    lib.oracle_biencoder_scores.argtypes = [
+        f32p, f32p, f32p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+        ctypes.c_int64, ctypes.c_float]
     lib.oracle_constrained_softmax_backward_rows.restype = None
     lib.oracle_constrained_softmax_backward_rows.argtypes = [
         f64p, f64p, f64p, f64p, ctypes.c_int64, ctypes.c_int64,
@@ -320,6 +325,54 @@ def attention_softmax_row(s, i: int, mask_row=None, causal: bool = False,
         else None, row.size, int(i), int(bool(causal)),
         _ptr(p, ctypes.c_double))
     return p, int(flag)
+
+
+@dataclass
+class BiencoderResult:
+    out: np.ndarray      # [B, H, Q, D] float64
+    scores: np.ndarray   # [B, H, Q, K] float32 (step 1)
+    attn: Result         # step 2 on the [B H Q, K] score rows
+
+
+def biencoder_scores(query, keys, scale: float,
+                     lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """Step 1 of section 2.5 in fp32 as fixed by the oracle's reading:
+    per score one fused multiply-add per d in order, then * scale."""
+    lib = lib or load()
+    q = np.ascontiguousarray(np.asarray(query, dtype=np.float32))
+    k = np.ascontiguousarray(np.asarray(keys, dtype=np.float32))
+    if q.ndim != 4 or k.ndim != 4 or q.shape[:2] != k.shape[:2] \
+            or q.shape[3] != k.shape[3]:
+        raise ValueError("query [B, H, Q, D] and keys [B, H, K, D]")
+    B, H, Q, D = q.shape
+    K = k.shape[2]
+    s = np.empty((B, H, Q, K), dtype=np.float32)
+    if s.size:
+        lib.oracle_biencoder_scores(_ptr(q, ctypes.c_float),
+                                    _ptr(k, ctypes.c_float),
+                                    _ptr(s, ctypes.c_float), B * H, Q, K, D,
+                                    float(np.float32(scale)))
+    return s
+
+
+def biencoder_attention(query, keys, values, scale: float,
+                        entropy_bound: float = 0.20, t_min: float = 0.01,
+                        t_max: float = 10.0, max_iter: int = 20,
+                        lib: ctypes.CDLL | None = None) -> BiencoderResult:
+    """Section 2.5 biencoder_attention: scores (step 1, fp32 as above), the
+    oracle constrained softmax of every score row (step 2, fp64), then
+    attn @ values in fp64 (step 3, a library matmul)."""
+    lib = lib or load()
+    s = biencoder_scores(query, keys, scale, lib=lib)
+    B, H, Q, K = s.shape
+    v = np.asarray(values, dtype=np.float32)
+    if v.shape[:3] != (B, H, K):
+        raise ValueError("values must be [B, H, K, D]")
+    attn = constrained_softmax(s.reshape(B * H * Q, K), entropy_bound, t_min,
+                               t_max, max_iter, lib=lib)
+    p = attn.p.reshape(B, H, Q, K)
+    out = np.einsum("bhqk,bhkd->bhqd", p, v.astype(np.float64))
+    return BiencoderResult(out, s, attn)
 
 
 def search_interval(t_min: float, t_max: float) -> tuple[float, float]:

@@ -12,7 +12,8 @@
  * Notes) and section 5 (5.1 Error Codes, 5.3 NaN/Inf Propagation Policy,
  * 5.4 Graceful Degradation); the backward follows section 6.3 (PyTorch Custom
  * Op Integration, ConstrainedSoftmaxFunction.backward) with the 1/T of
- * softmax(l / T) restored; attention_softmax follows section 2.6.
+ * softmax(l / T) restored; attention_softmax follows section 2.6 and
+ * biencoder_attention section 2.5.
  *
  * Arithmetic: IEEE double throughout, libm exp() and log().  The fp32
  * parameters are promoted exactly to double, so both sides of any comparison
@@ -307,4 +308,34 @@ int32_t oracle_attention_softmax_row(const float* s, const float* m,
                                      double* p)
 {
     return attention_row(s, m, S, i, causal, p);
+}
+
+/*
+ * biencoder_attention: section 2.5 (Signature, Parameters table,
+ * Description steps 1-3).  query [BH, Q, D], keys and values [BH, K, D]
+ * (BH = batch x heads), all row-major fp32.
+ *
+ * Step 1, scores = query @ keys^T * scale.  The page's kernel is fp32 and
+ * the constrained softmax's search turns its logits into a grid index, so
+ * the scores are fixed to one fp32 evaluation (the reading stated in the
+ * design notes): s = sum over d = 0..D-1 of q_d k_d, accumulated with one
+ * fused multiply-add per term in that order from 0, then one fp32 multiply
+ * by scale.  Steps 2-3 (the constrained softmax of each row of scores and
+ * attn @ values) are computed in fp64 by the caller from these scores.
+ */
+void oracle_biencoder_scores(const float* q, const float* k, float* scores,
+                             int64_t BH, int64_t Q, int64_t K, int64_t D,
+                             float scale)
+{
+    for (int64_t bh = 0; bh < BH; ++bh) {
+        for (int64_t i = 0; i < Q; ++i) {
+            const float* qi = q + (bh * Q + i) * D;
+            for (int64_t j = 0; j < K; ++j) {
+                const float* kj = k + (bh * K + j) * D;
+                float s = 0.0f;
+                for (int64_t d = 0; d < D; ++d) s = fmaf(qi[d], kj[d], s);
+                scores[(bh * Q + i) * K + j] = s * scale;
+            }
+        }
+    }
 }

@@ -20,7 +20,11 @@ AssertionError when the oracle disagrees with:
   * for attention_softmax (section 2.6): scipy's softmax of each row, of
     each causal prefix and of the unmasked subset (scores plus mask added
     in numpy fp32); the fp32 addition of a -1e9 mask; invariants and the
-    NaN/Inf policy.
+    NaN/Inf policy,
+  * for biencoder_attention (section 2.5): the fp32 scores against fp64
+    matmul within the dot product's rounding bound, one-hot queries, the
+    fp32 accumulation order, scipy's softmax and a matmul when no row
+    searches, convex combinations of the value rows, a single context item.
 
 The same checks run against deliberately broken copies of the oracle in
 ``test_oracle_mutants.py``: every plausible mistake must fail at least one.
@@ -601,6 +605,68 @@ def check_attention_invariants_and_faults(lib) -> None:
     assert np.max(np.abs(ra.p[1].sum(axis=-1) - 1.0)) < 1e-14
 
 
+# -------------------------------------------------------- biencoder_attention
+def _bienc_inputs(seed, B=2, H=2, Q=6, K=5, D=16, sigma=1.0):
+    rng = np.random.default_rng(seed)
+    q = rng.normal(0.0, sigma, (B, H, Q, D)).astype(np.float32)
+    k = rng.normal(0.0, sigma, (B, H, K, D)).astype(np.float32)
+    v = rng.normal(0.0, 1.0, (B, H, K, D)).astype(np.float32)
+    return q, k, v
+
+
+def check_biencoder_scores(lib) -> None:
+    """Step 1 against fp64 matmul (numpy): each fp32 score is within the
+    rounding bound of a D-term dot product, (D + 1) u sum |q_d k_d| scale,
+    of the exact q . k scale; and a query equal to a one-hot e_d picks
+    k_d exactly."""
+    u = 2.0 ** -24
+    for seed, D in ((101, 16), (102, 64), (103, 3)):
+        q, k, _ = _bienc_inputs(seed, D=D)
+        scale = np.float32(1.0 / np.sqrt(D))
+        s = oracle.biencoder_scores(q, k, scale, lib=lib)
+        exact = np.einsum("bhqd,bhkd->bhqk", q.astype(np.float64),
+                          k.astype(np.float64)) * float(scale)
+        absd = np.einsum("bhqd,bhkd->bhqk", np.abs(q.astype(np.float64)),
+                         np.abs(k.astype(np.float64))) * float(scale)
+        assert np.all(np.abs(s - exact) <= (D + 2) * u * absd + 1e-30)
+    q, k, _ = _bienc_inputs(104, Q=4, K=3, D=4)
+    q[:] = 0.0
+    for i in range(4):
+        q[:, :, i, i] = 1.0
+    s = oracle.biencoder_scores(q, k, 1.0, lib=lib)
+    assert np.array_equal(s[:, :, :, :], np.swapaxes(k, 2, 3)[:, :, :4, :])
+    # The fp32 order of the reading: 2^24 + 1 + 1 + 1 accumulated term by
+    # term in fp32 stays at 2^24 (each +1 is a tie rounded to even), where
+    # the exact sum 2^24 + 3 rounds to 2^24 + 4.
+    q = np.ones((1, 1, 1, 4), dtype=np.float32)
+    k = np.array([[[[2.0 ** 24, 1.0, 1.0, 1.0]]]], dtype=np.float32)
+    s = oracle.biencoder_scores(q, k, 1.0, lib=lib)
+    assert s[0, 0, 0, 0] == np.float32(2.0 ** 24)
+
+
+def check_biencoder_composition(lib) -> None:
+    """Steps 2-3: the attention rows are the oracle constrained softmax of
+    the step-1 scores (pinned above); with a bound no row exceeds the
+    attention is scipy's softmax, and every output row is attn @ values,
+    a convex combination of value rows (inside their per-column range); a
+    single context item returns its value row exactly."""
+    q, k, v = _bienc_inputs(111, Q=7, K=9, D=12, sigma=2.0)
+    r = oracle.biencoder_attention(q, k, v, 0.5, 1e30, lib=lib)
+    ref = _scipy_rows(r.scores)
+    assert np.max(np.abs(r.attn.p.reshape(ref.shape) - ref)) < 1e-13
+    out = np.einsum("bhqk,bhkd->bhqd", ref, v.astype(np.float64))
+    assert np.max(np.abs(r.out - out)) < 1e-12
+    r = oracle.biencoder_attention(q, k, v, 0.5, 0.2, lib=lib)
+    assert np.sum(r.attn.T < 1.0) >= 10
+    lo = v.min(axis=2, keepdims=True).astype(np.float64)
+    hi = v.max(axis=2, keepdims=True).astype(np.float64)
+    assert np.all(r.out >= lo - 1e-12) and np.all(r.out <= hi + 1e-12)
+    q1, k1, v1 = _bienc_inputs(112, K=1)
+    r1 = oracle.biencoder_attention(q1, k1, v1, 0.25, 0.2, lib=lib)
+    assert np.array_equal(r1.out, np.broadcast_to(v1.astype(np.float64),
+                                                  r1.out.shape))
+
+
 ALL_CHECKS = [
     check_two_class_entropy,
     check_spike_entropy,
@@ -622,4 +688,6 @@ ALL_CHECKS = [
     check_attention_mask_subset,
     check_attention_fp32_mask_addition,
     check_attention_invariants_and_faults,
+    check_biencoder_scores,
+    check_biencoder_composition,
 ]

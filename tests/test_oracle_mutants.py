@@ -86,6 +86,18 @@ MUTANTS = [
      "else if (0) has_inf = 1;"),
     ("attention_row_index_is_head", "const int64_t i = r % S;",
      "const int64_t i = (r / S) % S;"),
+    ("biencoder_scale_missing",
+     "scores[(bh * Q + i) * K + j] = s * scale;",
+     "scores[(bh * Q + i) * K + j] = s;"),
+    ("biencoder_keys_transposed",
+     "const float* kj = k + (bh * K + j) * D;",
+     "const float* kj = k + (bh * K) * D + j;"),
+    ("biencoder_dot_skips_last",
+     "for (int64_t d = 0; d < D; ++d) s = fmaf(qi[d], kj[d], s);",
+     "for (int64_t d = 0; d + 1 < D; ++d) s = fmaf(qi[d], kj[d], s);"),
+    ("biencoder_dot_in_double",
+     "for (int64_t d = 0; d < D; ++d) s = fmaf(qi[d], kj[d], s);",
+     "double t = 0.0; for (int64_t d = 0; d < D; ++d) t += (double)qi[d] * kj[d]; s = (float)t;"),
 ]
 
 
