@@ -58,7 +58,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default=wl.LATENCY.name,
                     help="one of: " + ", ".join(
                         list(wl.WORKLOADS) + [w.name for w in wl.sweep_workloads()]
-                        + list(wl.ATTENTION_WORKLOADS)))
+                        + list(wl.ATTENTION_WORKLOADS)
+                        + list(wl.BIENCODER_WORKLOADS)))
     ap.add_argument("--variant", choices=["auto", "rowgroup", "cluster"],
                     default="auto")
     ap.add_argument("--param", type=int, default=0,
@@ -80,12 +81,15 @@ def parse_args(argv=None):
                     help="time plain stream launches instead of one CUDA "
                          "graph of the K launches")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--op", choices=["forward", "backward", "attention"],
+    ap.add_argument("--op", choices=["forward", "backward", "attention",
+                                     "biencoder"],
                     default="forward",
                     help="backward: time the gradient kernel, (1/T) p "
                          "(g - <g, p>), on the workload's shape; attention: "
                          "time attention_softmax on an attention workload "
-                         "(default attention_32x8x512)")
+                         "(default attention_32x8x512); biencoder: the fused "
+                         "biencoder_attention (default "
+                         "biencoder_32x8x512x64x64)")
     return ap.parse_args(argv)
 
 
@@ -993,8 +997,222 @@ def attention_arm(args, w) -> int:
     return 0
 
 
+# -------------------------------------------------------------- biencoder
+BIENC_METRIC = ("biencoder_attention query rows/s, with its ex2, fp32 FMA "
+                "and HBM rooflines")
+# fp32 FMA peak of the SIMT pipes, from unit counts: 152 SMs x 128 fp32
+# lanes x 2 flops per FMA at the 2.07 GHz maximum SM clock.
+FP32_SIMT_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def bienc_config(w, l2: str) -> dict:
+    return {"workload": w.name, "batch": w.batch, "heads": w.heads,
+            "query_len": w.query_len, "context_len": w.context_len,
+            "d_head": w.d_head, "entropy_bound": w.entropy_bound,
+            "inputs": w.note, "seed": w.seed, "l2": l2}
+
+
+def bienc_reference_arm(args, w) -> int:
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.load()
+    q, k, v = wl.generate_biencoder(w)
+    scale = 1.0 / math.sqrt(w.d_head)
+    # Each step: the oracle on one (batch, head) pair's queries.
+    for i in range(args.warmup):
+        b, h = divmod(i % (w.batch * w.heads), w.heads)
+        oracle.biencoder_attention(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1],
+                                   v[b:b + 1, h:h + 1], scale, w.entropy_bound)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        b, h = divmod(i % (w.batch * w.heads), w.heads)
+        oracle.biencoder_attention(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1],
+                                   v[b:b + 1, h:h + 1], scale, w.entropy_bound)
+    dt = time.perf_counter() - t0
+    value = w.query_len * args.steps / dt
+    threads = oracle.default_threads()
+    line = {
+        "impl": "reference", "op": "biencoder", "metric": BIENC_METRIC,
+        "value": value, "unit": "rows/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": bienc_config(w, "cpu"),
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": f"one (batch, head) pair of {w.query_len} "
+                                   f"queries per step ({args.steps} steps)"},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def bienc_arm(args, w) -> int:
+    """One step = one fused biencoder_attention launch over the workload,
+    inputs resident in HBM."""
+    import torch
+    import entropy_bounded_softmax_gb300 as cs
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    q, k, v = wl.generate_biencoder(w)
+    B, H, Q, K, D = w.batch, w.heads, w.query_len, w.context_len, w.d_head
+    scale = 1.0 / math.sqrt(D)
+    io_bytes = 4 * (2 * B * H * Q * D + 2 * B * H * K * D)
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+    qs, ks, vs = (torch.from_numpy(a).to(dev) for a in (q, k, v))
+    nbuf = max(1, math.ceil(3 * L2_BYTES / io_bytes)) if io_bytes < 3 * L2_BYTES else 1
+    sets = [(qs, ks, vs)] + [tuple(a.clone() for a in (qs, ks, vs))
+                             for _ in range(nbuf - 1)]
+    outs = [torch.empty_like(qs) for _ in range(nbuf)]
+    l2_note = (f"rotating {nbuf} input/output sets "
+               f"({nbuf * io_bytes / 2**20:.0f} MiB > L2)") if nbuf > 1 else \
+        f"inputs larger than L2 ({io_bytes / 2**20:.0f} MiB)"
+
+    def launch(i: int, stream_ptr: int = sptr) -> None:
+        j = i % nbuf
+        a, b_, c = sets[j]
+        st = cs.cs_biencoder_attention(a.data_ptr(), b_.data_ptr(),
+                                       c.data_ptr(), outs[j].data_ptr(), B, Q,
+                                       K, D, H, scale, w.entropy_bound,
+                                       stream_ptr)
+        if st != 0:
+            raise RuntimeError(f"cs_biencoder_attention failed: {st}")
+
+    cs.get_error()
+    for i in range(max(3, args.warmup)):
+        launch(i)
+    torch.cuda.synchronize()
+    st, plan = cs.cs_plan_biencoder_host(B, Q, K, D, H, None, 232448)
+    plan = plan.as_dict()
+    tm = time_launches(args, torch, launch, stream, dist, local)
+    total_ms = reduce_max(dist, tm["ms"], dev)
+    stream_ms_max = reduce_max(dist, tm["stream_ms"], dev)
+    ms_per_step = total_ms / args.steps
+    rows = B * H * Q
+    value = aggregate_rows_per_s(rows, world, ms_per_step * 1e-3)
+    err = cs.get_error()
+
+    h_q, h_k, h_v = (torch.from_numpy(a).pin_memory() for a in (q, k, v))
+
+    def make_slot():
+        return {"q": torch.empty_like(qs), "k": torch.empty_like(ks),
+                "v": torch.empty_like(vs), "out": torch.empty_like(qs),
+                "h_out": torch.empty(q.shape, dtype=torch.float32).pin_memory()}
+
+    def e2e_step(sl):
+        sl["q"].copy_(h_q, non_blocking=True)
+        sl["k"].copy_(h_k, non_blocking=True)
+        sl["v"].copy_(h_v, non_blocking=True)
+        cs.biencoder_attention(sl["q"], sl["k"], sl["v"], scale,
+                               w.entropy_bound, out=sl["out"])
+        sl["h_out"].copy_(sl["out"], non_blocking=True)
+
+    e2e = time_e2e(torch, make_slot, e2e_step, stream, max(1, args.e2e_steps))
+    e2e = {kk: reduce_max(dist, vv, dev) for kk, vv in e2e.items()}
+    e2e_value = aggregate_rows_per_s(rows, world, e2e["pipelined"] * 1e-3)
+
+    line = None
+    if rank == 0:
+        import oracle
+        peaks = measured_peaks()
+        ex2_peak = probe_ex2_peak(torch, cs, sptr)
+        t_kernel = ms_per_step * 1e-3
+        # Searched rows from the oracle's step-1 scores on a sample of
+        # (batch, head) pairs, scaled to the launch.
+        nbh = min(8, B * H)
+        sc = oracle.biencoder_scores(q.reshape(B * H, 1, Q, D)[:nbh],
+                                     k.reshape(B * H, 1, K, D)[:nbh], scale)
+        import scipy.special
+        pr = scipy.special.softmax(sc.reshape(-1, K).astype(np.float64), axis=1)
+        Hs = scipy.special.entr(pr).sum(axis=1)
+        searched = float(np.mean(Hs > np.float32(w.entropy_bound))) * rows
+        exps = (rows + searched * 20) * K
+        flops = 4.0 * rows * K * D
+        t_hbm = io_bytes / (peaks["hbm_gbs"] * 1e9)
+        t_ex2 = exps / ex2_peak
+        t_fma = flops / (FP32_SIMT_TFLOPS * 1e12)
+        bound = max(("hbm", t_hbm), ("ex2", t_ex2), ("fma", t_fma),
+                    key=lambda kv: kv[1])
+        roof = {"bound": "hbm" if bound[0] == "hbm" else "alu",
+                "limit": bound[0],
+                "unit": {"hbm": "GB/s", "ex2": "Gex2/s", "fma": "TFLOP/s"}[bound[0]],
+                "achieved": {"hbm": io_bytes / t_kernel / 1e9,
+                             "ex2": exps / t_kernel / 1e9,
+                             "fma": flops / t_kernel / 1e12}[bound[0]],
+                "peak": {"hbm": peaks["hbm_gbs"], "ex2": ex2_peak / 1e9,
+                         "fma": FP32_SIMT_TFLOPS}[bound[0]],
+                "frac": bound[1] / t_kernel, "traffic": None,
+                "kernel": "bienc_kernel", "algorithmic_bytes": io_bytes,
+                "algorithmic_ex2": exps, "algorithmic_flops": flops,
+                "roofline_us": {"hbm": t_hbm * 1e6, "ex2": t_ex2 * 1e6,
+                                "fma": t_fma * 1e6},
+                "peak_source": "hbm: measured copy bandwidth; ex2: probe; "
+                               "fma: 152 SMs x 128 lanes x 2 flops x 2.07 GHz"}
+        cpu = None
+        if not args.no_cpu_baseline:
+            t0 = time.perf_counter()
+            n = 0
+            while time.perf_counter() - t0 < args.cpu_seconds:
+                b, h = divmod(n % (B * H), H)
+                oracle.biencoder_attention(q[b:b + 1, h:h + 1],
+                                           k[b:b + 1, h:h + 1],
+                                           v[b:b + 1, h:h + 1], scale,
+                                           w.entropy_bound)
+                n += 1
+            dt = time.perf_counter() - t0
+            cpu = {"value": n * Q / dt, "unit": "rows/s",
+                   "cores": oracle.default_threads(), "kind": "oracle",
+                   "sample": f"{n} (batch, head) pairs of {Q} queries in "
+                             f"{dt:.1f} s"}
+        line = {
+            "op": "biencoder", "metric": BIENC_METRIC, "value": value,
+            "unit": "rows/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "launch": "cuda_graph" if tm["graph"] is not None else "stream",
+            "ms_per_step_stream_launches": stream_ms_max / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "baseline_note": ("page figure 0.5 ms on an RTX 3080 for this "
+                              "shape (another machine)")
+            if w.name == "biencoder_32x8x512x64x64" else None,
+            "dtype": "f32", "data": "synthetic",
+            "config": dict(bienc_config(w, l2_note),
+                           parallelism=f"replicas x{world}", plan=plan),
+            "roofline": roof, "cpu_baseline": cpu,
+            "e2e": e2e_entry(e2e_value, e2e,
+                             4 * (B * H * Q * D + 2 * B * H * K * D),
+                             4 * B * H * Q * D),
+            "gpu_launches": args.steps,
+            "clocks": tm["sampler"].summary(tm["t0"], tm["t1"]),
+            "device_errors": sorted(err),
+        }
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None) -> int:
     args = parse_args(argv)
+    if args.op == "biencoder":
+        name = args.workload if args.workload in wl.BIENCODER_WORKLOADS \
+            else wl.BIENC_PAGE.name
+        bw = wl.BIENCODER_WORKLOADS[name]
+        if args.impl == "reference":
+            return bienc_reference_arm(args, bw)
+        return bienc_arm(args, bw)
     if args.op == "attention":
         name = args.workload if args.workload in wl.ATTENTION_WORKLOADS \
             else wl.ATTN_PAGE.name

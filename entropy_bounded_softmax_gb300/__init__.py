@@ -19,6 +19,8 @@ from __future__ import annotations
 
 from . import _lib
 from ._lib import (CONSTANTS, cs_attention_softmax, cs_attention_softmax_ex,
+                   cs_biencoder_attention, cs_biencoder_attention_ex,
+                   cs_check_biencoder_args, cs_plan_biencoder_host,
                    cs_check_args, cs_check_attention_args,
                    cs_check_backward_args, cs_constrained_softmax,
                    cs_constrained_softmax_backward,
@@ -43,6 +45,9 @@ __all__ = [
     "attention_softmax", "plan_attention", "cs_attention_softmax",
     "cs_attention_softmax_ex", "cs_plan_attention_launch",
     "cs_plan_attention_host", "cs_check_attention_args",
+    "biencoder_attention", "cs_biencoder_attention",
+    "cs_biencoder_attention_ex", "cs_plan_biencoder_host",
+    "cs_check_biencoder_args",
 ]
 
 # Defaults of section 2.1's signature.
@@ -217,6 +222,56 @@ def attention_softmax(scores, mask=None, causal: bool = False, out=None,
     if st != 0:
         raise CsError(st, "cs_attention_softmax")
     return out
+
+
+def biencoder_attention(query, keys, values, scale=None,
+                        entropy_bound: float = DEFAULT_ENTROPY_BOUND,
+                        t_min: float = DEFAULT_T_MIN,
+                        t_max: float = DEFAULT_T_MAX,
+                        max_iter: int = DEFAULT_MAX_ITER, out=None,
+                        return_attn: bool = False, return_t: bool = False,
+                        lanes: int = 0):
+    """Section 2.5 biencoder_attention, fused: scores = query @ keys^T *
+    scale (default 1/sqrt(d_head)), the constrained softmax of every score
+    row, then attn @ values.  query [B, H, Q, D], keys and values
+    [B, H, K, D], CUDA fp32 contiguous.  Returns the output [B, H, Q, D]
+    (and the weights [B, H, Q, K] and temperatures [B, H, Q] when asked).
+    Asynchronous on the current stream."""
+    import math
+    import torch
+    for name, x in (("query", query), ("keys", keys), ("values", values)):
+        if (not isinstance(x, torch.Tensor) or x.device.type != "cuda"
+                or x.dtype != torch.float32 or x.dim() != 4
+                or not x.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CUDA float32 "
+                             "4-D tensor")
+    B, H, Q, D = query.shape
+    K = keys.shape[2]
+    if keys.shape != (B, H, K, D) or values.shape != (B, H, K, D):
+        raise ValueError("keys and values must be [B, H, K, D]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(query)
+    attn = t = None
+    if return_attn:
+        attn = torch.empty((B, H, Q, K), dtype=torch.float32,
+                           device=query.device)
+    if return_t:
+        t = torch.empty((B, H, Q), dtype=torch.float32, device=query.device)
+    opt = options(VARIANTS["rowgroup"] if lanes else 0, lanes, 0, 0)
+    with torch.cuda.device(query.device):
+        st = cs_biencoder_attention_ex(
+            query.data_ptr(), keys.data_ptr(), values.data_ptr(),
+            out.data_ptr(), B, Q, K, D, H, float(scale), float(entropy_bound),
+            float(t_min), float(t_max), int(max_iter),
+            attn.data_ptr() if attn is not None else None,
+            t.data_ptr() if t is not None else None, opt,
+            _stream_handle(query.device))
+    if st != 0:
+        raise CsError(st, "cs_biencoder_attention")
+    res = (out,) + ((attn,) if return_attn else ()) + ((t,) if return_t else ())
+    return res if len(res) > 1 else out
 
 
 def plan_attention(batch: int, heads: int, seq_len: int, aligned: bool = True,

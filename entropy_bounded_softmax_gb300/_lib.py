@@ -102,6 +102,18 @@ _SIGNATURES = {
                                       _I32, ctypes.POINTER(cs_plan)]),
     "cs_check_attention_args": (_I32, [_VP, _VP, _VP, _I32, _I32, _I32,
                                        _I32]),
+    "cs_biencoder_attention": (_I32, [_VP, _VP, _VP, _VP, _I32, _I32, _I32,
+                                      _I32, _I32, _F32, _F32, _VP]),
+    "cs_biencoder_attention_ex": (_I32, [_VP, _VP, _VP, _VP, _I32, _I32,
+                                         _I32, _I32, _I32, _F32, _F32, _F32,
+                                         _F32, _I32, _VP, _VP,
+                                         ctypes.POINTER(cs_options), _VP]),
+    "cs_plan_biencoder_host": (_I32, [_I32, _I32, _I32, _I32, _I32,
+                                      ctypes.POINTER(cs_options), _I32,
+                                      ctypes.POINTER(cs_plan)]),
+    "cs_check_biencoder_args": (_I32, [_VP, _VP, _VP, _VP, _I32, _I32, _I32,
+                                       _I32, _I32, _F32, _F32, _F32, _F32,
+                                       _I32, _VP, _VP]),
     "cs_probe_ex2": (_I32, [_VP, _I32, ctypes.POINTER(_I64), _VP]),
     "cs_probe_ex2_sink_floats": (_I32, []),
     "cs_test_wait_timeout": (_I32, [_I64, _VP]),
@@ -258,6 +270,44 @@ def cs_check_attention_args(scores, out, mask, batch, heads, seq_len,
                             causal) -> int:
     return load().cs_check_attention_args(scores, out, mask, batch, heads,
                                           seq_len, causal)
+
+
+def cs_biencoder_attention(query, keys, values, output, batch_size,
+                           query_len, context_len, d_head, num_heads, scale,
+                           entropy_bound, stream) -> int:
+    return load().cs_biencoder_attention(query, keys, values, output,
+                                         batch_size, query_len, context_len,
+                                         d_head, num_heads, scale,
+                                         entropy_bound, stream)
+
+
+def cs_biencoder_attention_ex(query, keys, values, output, batch_size,
+                              query_len, context_len, d_head, num_heads,
+                              scale, entropy_bound, t_min, t_max, max_iter,
+                              attn_out, t_out, opt, stream) -> int:
+    return load().cs_biencoder_attention_ex(
+        query, keys, values, output, batch_size, query_len, context_len,
+        d_head, num_heads, scale, entropy_bound, t_min, t_max, max_iter,
+        attn_out, t_out, _opt_ref(opt), stream)
+
+
+def cs_plan_biencoder_host(batch_size, query_len, context_len, d_head,
+                           num_heads, opt, smem_per_block_optin):
+    p = cs_plan()
+    st = load().cs_plan_biencoder_host(batch_size, query_len, context_len,
+                                       d_head, num_heads, _opt_ref(opt),
+                                       smem_per_block_optin, ctypes.byref(p))
+    return st, p
+
+
+def cs_check_biencoder_args(query, keys, values, output, batch_size,
+                            query_len, context_len, d_head, num_heads, scale,
+                            entropy_bound, t_min, t_max, max_iter, attn_out,
+                            t_out) -> int:
+    return load().cs_check_biencoder_args(
+        query, keys, values, output, batch_size, query_len, context_len,
+        d_head, num_heads, scale, entropy_bound, t_min, t_max, max_iter,
+        attn_out, t_out)
 
 
 def cs_probe_ex2(sink, iters, stream) -> tuple[int, int]:

@@ -752,6 +752,164 @@ cs_status cs_attention_softmax(const float* scores, float* out,
                                    causal, nullptr, stream);
 }
 
+cs_status cs_check_biencoder_args(const float* query,
+                                  const float* context_keys,
+                                  const float* context_values,
+                                  const float* output, int32_t batch_size,
+                                  int32_t query_len, int32_t context_len,
+                                  int32_t d_head, int32_t num_heads,
+                                  float scale, float entropy_bound,
+                                  float t_min, float t_max, int32_t max_iter,
+                                  const float* attn_out, const float* t_out) {
+    if (batch_size < 0 || query_len < 0 || num_heads < 0 || context_len < 1 ||
+        d_head < 1)
+        return CS_ERR_DIM_MISMATCH;
+    if (context_len > cs::kBiencMaxContext || d_head > cs::kBiencMaxDHead)
+        return CS_ERR_OOM;
+    if (d_head % 4 != 0) return CS_ERR_INVALID_ARG;
+    if (!isfinite(scale)) return CS_ERR_INVALID_ARG;
+    // The search parameters, as for cs_constrained_softmax.
+    const cs_status st = cs_check_args(nullptr, nullptr, 0, context_len,
+                                       entropy_bound, t_min, t_max, max_iter,
+                                       nullptr);
+    if (st != CS_OK) return st;
+    const int64_t bh = static_cast<int64_t>(batch_size) * num_heads;
+    const int64_t rows = bh * query_len;
+    if (rows == 0) return CS_OK;
+    if (!query || !context_keys || !context_values || !output)
+        return CS_ERR_INVALID_ARG;
+    const void* ptrs[4] = {query, context_keys, context_values, output};
+    for (const void* ptr : ptrs)
+        if (reinterpret_cast<uintptr_t>(ptr) & 15) return CS_ERR_INVALID_ARG;
+    const int64_t qb = rows * d_head * 4;
+    const int64_t kb = bh * context_len * d_head * 4;
+    if (ranges_overlap(output, qb, query, qb) ||
+        ranges_overlap(output, qb, context_keys, kb) ||
+        ranges_overlap(output, qb, context_values, kb))
+        return CS_ERR_INVALID_ARG;
+    const int64_t ab = rows * context_len * 4;
+    if (attn_out && (ranges_overlap(attn_out, ab, output, qb) ||
+                     ranges_overlap(attn_out, ab, query, qb) ||
+                     ranges_overlap(attn_out, ab, context_keys, kb) ||
+                     ranges_overlap(attn_out, ab, context_values, kb)))
+        return CS_ERR_INVALID_ARG;
+    if (t_out && (ranges_overlap(t_out, rows * 4, output, qb) ||
+                  ranges_overlap(t_out, rows * 4, query, qb) ||
+                  ranges_overlap(t_out, rows * 4, context_keys, kb) ||
+                  ranges_overlap(t_out, rows * 4, context_values, kb) ||
+                  (attn_out && ranges_overlap(t_out, rows * 4, attn_out, ab))))
+        return CS_ERR_INVALID_ARG;
+    return CS_OK;
+}
+
+cs_status cs_plan_biencoder_host(int32_t batch_size, int32_t query_len,
+                                 int32_t context_len, int32_t d_head,
+                                 int32_t num_heads, const cs_options* options,
+                                 int32_t smem_per_block_optin, cs_plan* plan) {
+    if (!plan) return CS_ERR_INVALID_ARG;
+    if (batch_size < 0 || query_len < 0 || num_heads < 0 || context_len < 1 ||
+        d_head < 1)
+        return CS_ERR_DIM_MISMATCH;
+    if (context_len > cs::kBiencMaxContext || d_head > cs::kBiencMaxDHead)
+        return CS_ERR_OOM;
+    if (d_head % 4 != 0) return CS_ERR_INVALID_ARG;
+    const cs_options o = options ? *options : cs_options{};
+    if (o.threads != 0 || o.strict != 0) return CS_ERR_INVALID_ARG;
+    int G = 0;
+    if (o.variant == CS_VARIANT_AUTO) {
+        if (o.param != 0) return CS_ERR_INVALID_ARG;
+        G = 1;
+        while (8 * G < context_len) G <<= 1;
+    } else if (o.variant == CS_VARIANT_ROWGROUP) {
+        G = o.param;
+        if (G < 1 || G > kRowgroupMaxLanes || (G & (G - 1)))
+            return CS_ERR_INVALID_ARG;
+        if (8 * G < context_len) return CS_ERR_OOM;
+    } else {
+        return CS_ERR_INVALID_ARG;
+    }
+    const int64_t smem = cs::bienc_smem_bytes(context_len, d_head, G);
+    if (smem > smem_per_block_optin) return CS_ERR_OOM;
+    const int64_t rows_per_cta = cs::kBiencThreads / G;
+    const int64_t tiles = ceil_div(query_len, rows_per_cta);
+    const int64_t grid = static_cast<int64_t>(batch_size) * num_heads * tiles;
+    if (grid > kMaxGridX) return CS_ERR_DIM_MISMATCH;
+    *plan = cs_plan{};
+    plan->variant = CS_VARIANT_ROWGROUP;
+    plan->lanes_per_row = G;
+    plan->elems_per_lane = 8;
+    plan->threads_per_cta = cs::kBiencThreads;
+    plan->smem_bytes = static_cast<int32_t>(smem);
+    plan->grid_ctas = grid;
+    plan->staged_tensors = 3;
+    return CS_OK;
+}
+
+cs_status cs_biencoder_attention_ex(const float* query,
+                                    const float* context_keys,
+                                    const float* context_values,
+                                    float* output, int32_t batch_size,
+                                    int32_t query_len, int32_t context_len,
+                                    int32_t d_head, int32_t num_heads,
+                                    float scale, float entropy_bound,
+                                    float t_min, float t_max,
+                                    int32_t max_iter, float* attn_out,
+                                    float* t_out, const cs_options* options,
+                                    void* stream) {
+    cs_status st = cs_check_biencoder_args(
+        query, context_keys, context_values, output, batch_size, query_len,
+        context_len, d_head, num_heads, scale, entropy_bound, t_min, t_max,
+        max_iter, attn_out, t_out);
+    if (st != CS_OK) return st;
+    const int64_t bh = static_cast<int64_t>(batch_size) * num_heads;
+    if (bh * query_len == 0) return CS_OK;
+    DeviceInfo* d = nullptr;
+    st = device_info(&d);
+    if (st != CS_OK) return st;
+    cs_plan p;
+    st = cs_plan_biencoder_host(batch_size, query_len, context_len, d_head,
+                                num_heads, options, d->smem_optin, &p);
+    if (st != CS_OK) return st;
+    cs::BiencTask task;
+    task.q = query;
+    task.k = context_keys;
+    task.v = context_values;
+    task.out = output;
+    task.attn_out = attn_out;
+    task.t_out = t_out;
+    task.err = d->err;
+    task.BH = static_cast<int32_t>(bh);
+    task.Q = query_len;
+    task.K = context_len;
+    task.D = d_head;
+    task.scale = scale;
+    task.entropy_bound = entropy_bound;
+    task.t_min = t_min;
+    task.hi0 = t_max < 1.0f ? t_max : 1.0f;
+    task.max_iter = max_iter;
+    const cudaError_t e = cs::launch_bienc(task, p.lanes_per_row, p.smem_bytes,
+                                           static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return CS_ERR_CUDA;
+    }
+    return CS_OK;
+}
+
+cs_status cs_biencoder_attention(const float* query,
+                                 const float* context_keys,
+                                 const float* context_values, float* output,
+                                 int32_t batch_size, int32_t query_len,
+                                 int32_t context_len, int32_t d_head,
+                                 int32_t num_heads, float scale,
+                                 float entropy_bound, void* stream) {
+    return cs_biencoder_attention_ex(query, context_keys, context_values,
+                                     output, batch_size, query_len,
+                                     context_len, d_head, num_heads, scale,
+                                     entropy_bound, 0.01f, 10.0f, 20, nullptr,
+                                     nullptr, nullptr, stream);
+}
+
 int32_t cs_probe_ex2_sink_floats(void) {
     DeviceInfo* d = nullptr;
     if (device_info(&d) != CS_OK) return -1;

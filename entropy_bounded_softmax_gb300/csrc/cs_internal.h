@@ -158,6 +158,46 @@ cudaError_t launch_attention_cta(const AttnTask& task, int threads,
                                  int smem_bytes, int64_t grid_ctas,
                                  cudaStream_t stream);
 
+// One biencoder_attention launch: BH = batch x heads pairs of query
+// [Q, D], keys and values [K, D].
+struct BiencTask {
+    const float* q;
+    const float* k;
+    const float* v;
+    float* out;            // [BH, Q, D]
+    float* attn_out;       // [BH, Q, K] or null
+    float* t_out;          // [BH, Q] or null
+    unsigned int* err;     // device error word
+    int32_t BH;
+    int32_t Q;
+    int32_t K;
+    int32_t D;
+    float scale;
+    float entropy_bound;
+    float t_min;
+    float hi0;             // min(1, t_max)
+    int32_t max_iter;
+};
+
+// biencoder_attention geometry: 256-thread CTAs, G lanes per query row
+// holding eight context items each (K <= 8 G <= 256); keys transposed in
+// shared memory with rows of kp (K rounded up to 4) floats.
+constexpr int kBiencThreads = 256;
+constexpr int kBiencMaxContext = 256;
+constexpr int kBiencMaxDHead = 256;
+
+__host__ __device__ inline int bienc_kp(int K) { return (K + 3) & ~3; }
+
+inline int64_t bienc_smem_bytes(int K, int D, int G) {
+    const int64_t R = kBiencThreads / G;
+    const int64_t kp = bienc_kp(K);
+    return 4 * (D * kp + static_cast<int64_t>(K) * D + R * (D + 4) +
+                R * (kp + 4));
+}
+
+cudaError_t launch_bienc(const BiencTask& task, int lanes_per_row,
+                         int smem_bytes, cudaStream_t stream);
+
 cudaError_t launch_rowgroup(const RowTask& task, int lanes_per_row,
                             int elems_per_lane, cudaStream_t stream);
 cudaError_t launch_cluster(const RowTask& task, int cluster_size,

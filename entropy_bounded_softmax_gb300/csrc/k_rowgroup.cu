@@ -14,83 +14,12 @@
 // S (log2 S - bound log2 e) - beta V > 0, with log2 on the MUFU lg2 unit.
 #include <math.h>
 
-#include "cs_search.cuh"
+#include "cs_rowgroup.cuh"
 
 namespace cs {
 namespace {
 
 using namespace csd;
-
-template <int G>
-__device__ __forceinline__ float2 group_max2(float2 v, unsigned mask) {
-#pragma unroll
-    for (int o = G / 2; o > 0; o >>= 1) {
-        v.x = fmaxf(v.x, __shfl_xor_sync(mask, v.x, o));
-        v.y = fmaxf(v.y, __shfl_xor_sync(mask, v.y, o));
-    }
-    return v;
-}
-
-template <int G>
-__device__ __forceinline__ float2 group_sum2(float2 v, unsigned mask) {
-#pragma unroll
-    for (int o = G / 2; o > 0; o >>= 1) {
-        v.x += __shfl_xor_sync(mask, v.x, o);
-        v.y += __shfl_xor_sync(mask, v.y, o);
-    }
-    return v;
-}
-
-// (S, V) of this lane's classes at inverse temperature beta.
-template <int E4>
-__device__ __forceinline__ float2 reg_pass(const float4 (&y)[E4], float beta) {
-    SV4 acc;
-    acc.zero();
-    const float2 b2 = make_float2(beta, beta);
-#pragma unroll
-    for (int i = 0; i < E4; ++i) acc.add(y[i], b2);
-    return acc.total();
-}
-
-template <int G>
-__device__ __forceinline__ float3 group_sum3(float3 v, unsigned mask) {
-#pragma unroll
-    for (int o = G / 2; o > 0; o >>= 1) {
-        v.x += __shfl_xor_sync(mask, v.x, o);
-        v.y += __shfl_xor_sync(mask, v.y, o);
-        v.z += __shfl_xor_sync(mask, v.z, o);
-    }
-    return v;
-}
-
-// (S, V, W) of this lane's classes at inverse temperature beta, with
-// W = sum y^2 2^(beta y) for the Newton slope.  S and V take exactly the
-// arithmetic of reg_pass, so a grid point gets the same decision whichever
-// pass evaluates it.
-template <int E4>
-__device__ __forceinline__ float3 reg_pass3(const float4 (&y)[E4], float beta) {
-    SV4 acc;
-    acc.zero();
-    float2 w = make_float2(0.f, 0.f);
-    const float2 b2 = make_float2(beta, beta);
-#pragma unroll
-    for (int i = 0; i < E4; ++i) {
-        const float2 y01 = make_float2(y[i].x, y[i].y);
-        const float2 y23 = make_float2(y[i].z, y[i].w);
-        const float2 x01 = mul2(y01, b2);
-        const float2 x23 = mul2(y23, b2);
-        const float2 e01 = make_float2(ex2(x01.x), ex2(x01.y));
-        const float2 e23 = make_float2(ex2(x23.x), ex2(x23.y));
-        acc.s01 = add2(acc.s01, e01);
-        acc.s23 = add2(acc.s23, e23);
-        acc.v01 = fma2(e01, y01, acc.v01);
-        acc.v23 = fma2(e23, y23, acc.v23);
-        w = fma2(mul2(e01, y01), y01, w);
-        w = fma2(mul2(e23, y23), y23, w);
-    }
-    const float2 sv = acc.total();
-    return make_float3(sv.x, sv.y, w.x + w.y);
-}
 
 // At most 64 registers a thread (32 warps per SM, which the latency of each
 // row's dependent reduce-and-decide chain needs), or 80 when a lane holds
@@ -154,50 +83,12 @@ rowgroup_kernel(RowTask t, int vec) {
                 y[i] = make_float4(e[0], e[1], e[2], e[3]);
             }
         }
-        float code = 0.0f;
-        if (bad != bad) {
-            code = 1.0f;
-#pragma unroll
-            for (int i = 0; i < E4; ++i) {
-                if (isnan(y[i].x) || isnan(y[i].y) || isnan(y[i].z) ||
-                    isnan(y[i].w))
-                    code = 2.0f;
-            }
-        }
-        const float2 mc = group_max2<G>(make_float2(m, code), gmask);
-        m = mc.x;
-        const int row_code = static_cast<int>(mc.y);
-
-        unsigned int bits = 0;
-        float T_row = NAN;
-        float beta_out = 0.0f, inv_s = 0.0f;
-        if (row_code != 0) {
-            bits = row_code == 2 ? kBitNan : kBitInf;
-        } else {
-#pragma unroll
-            for (int i = 0; i < E4; ++i) {
-                y[i].x = fmaxf((y[i].x - m) * kLog2e, kYFloor);
-                y[i].y = fmaxf((y[i].y - m) * kLog2e, kYFloor);
-                y[i].z = fmaxf((y[i].z - m) * kLog2e, kYFloor);
-                y[i].w = fmaxf((y[i].w - m) * kLog2e, kYFloor);
-            }
-            const float3 r1 = group_sum3<G>(reg_pass3<E4>(y, 1.0f), gmask);
-            float2 sv = make_float2(r1.x, r1.y);
-            if (!entropy_above(sv, 1.0f, bound_bits)) {
-                T_row = 1.0f;
-                beta_out = 1.0f;
-                inv_s = 1.0f / sv.x;
-            } else {
-                bool over = false;
-                narrow_search(
-                    cfg, r1.x, r1.y, r1.z, t.strict != 0,
-                    [&](float b) { return group_sum3<G>(reg_pass3<E4>(y, b), gmask); },
-                    [&](float b) { return group_sum2<G>(reg_pass<E4>(y, b), gmask); },
-                    T_row, beta_out, inv_s, over);
-                if (over) bits |= kBitOverflow;
-            }
-        }
-        const bool zero = row_code != 0;
+        const RowSolution sol = solve_row<G, E4>(y, m, bad, cfg, bound_bits,
+                                                 t.strict != 0, gmask);
+        const unsigned int bits = sol.bits;
+        const float T_row = sol.T_row;
+        const float beta_out = sol.beta_out, inv_s = sol.inv_s;
+        const bool zero = sol.zero;
         if (vec) {
             float4* d4 = reinterpret_cast<float4*>(dst);
 #pragma unroll

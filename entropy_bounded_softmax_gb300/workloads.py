@@ -264,3 +264,45 @@ def generate_attention(w: AttentionWorkload, rows=None) -> np.ndarray:
         sel = np.flatnonzero(rows_arr // BLOCK_ROWS == blk)
         out[sel] = xb[rows_arr[sel] - r0]
     return out
+
+
+# biencoder_attention workloads ("BURT-IMMA CUDA Kernel API Reference",
+# section 2.5 Performance Notes and section 7.1: batch 32, query_len 512,
+# context_len 64, d_head 64, 8 heads).  query, keys, values ~ N(0, 1) fp32;
+# with scale 1/sqrt(d_head) the scores are about N(0, 1).
+@dataclass(frozen=True)
+class BiencoderWorkload:
+    name: str
+    batch: int
+    heads: int
+    query_len: int
+    context_len: int
+    d_head: int
+    seed: int = 3000
+    entropy_bound: float = 0.20
+    note: str = ""
+
+    @property
+    def rows(self) -> int:
+        return self.batch * self.heads * self.query_len
+
+
+BIENC_PAGE = BiencoderWorkload(
+    "biencoder_32x8x512x64x64", 32, 8, 512, 64, 64, 3001,
+    note="batch 32, 8 heads, 512 queries, 64 context items, d_head 64, "
+         "N(0,1) inputs")
+BIENC_WIDE = BiencoderWorkload(
+    "biencoder_4x8x1024x256x64", 4, 8, 1024, 256, 64, 3002,
+    note="batch 4, 8 heads, 1024 queries, 256 context items, d_head 64")
+BIENCODER_WORKLOADS = {w.name: w for w in (BIENC_PAGE, BIENC_WIDE)}
+
+
+def generate_biencoder(w: BiencoderWorkload):
+    """(query [B, H, Q, D], keys [B, H, K, D], values [B, H, K, D]) fp32,
+    drawn in that order from Generator(PCG64([seed, 0]))."""
+    rng = np.random.Generator(np.random.PCG64([w.seed, 0]))
+    B, H, Q, K, D = w.batch, w.heads, w.query_len, w.context_len, w.d_head
+    q = rng.standard_normal((B, H, Q, D), dtype=np.float32)
+    k = rng.standard_normal((B, H, K, D), dtype=np.float32)
+    v = rng.standard_normal((B, H, K, D), dtype=np.float32)
+    return q, k, v

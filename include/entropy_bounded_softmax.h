@@ -332,6 +332,83 @@ cs_status cs_check_attention_args(const float* scores, const float* out,
                                   int32_t causal);
 
 /*
+ * cs_biencoder_attention -- section 2.5 `biencoder_attention`, fused.  For
+ * every batch b, head h and query i:
+ *
+ *   1. scores_j = (query_i . key_j) * scale, j < context_len.  The dot
+ *      product is evaluated in fp32 as one fused multiply-add per d in
+ *      order d = 0..d_head-1 from 0, then one fp32 multiply by scale: the
+ *      page's kernel is fp32 and the search turns these logits into a grid
+ *      point, so the evaluation is fixed rather than left to a GEMM's
+ *      blocking;
+ *   2. attn = constrained_softmax(scores, entropy_bound) per query row
+ *      (cs_constrained_softmax's operation, including its NaN/Inf and
+ *      unsatisfiable-bound policy and error bits);
+ *   3. output_i = sum_j attn_j value_j.
+ *
+ * query    device pointer, [batch, num_heads, query_len, d_head] fp32.
+ * context_keys, context_values  device pointers, [batch, num_heads,
+ *          context_len, d_head] fp32.  All three read only.
+ * output   device pointer, [batch, num_heads, query_len, d_head] fp32,
+ *          written completely; must not overlap the inputs.
+ * batch_size, query_len, num_heads >= 0 (no rows: a no-op returning CS_OK);
+ * context_len 1..256; d_head 1..256 and a multiple of 4 (else
+ *          CS_ERR_INVALID_ARG); larger shapes return CS_ERR_OOM.
+ * scale    finite (the page passes 1/sqrt(d_head)).
+ * entropy_bound  as for cs_constrained_softmax (page default 0.20); the
+ *          search takes the section 2.1 defaults t_min 0.01, t_max 10.0,
+ *          max_iter 20.
+ * stream   a cudaStream_t (NULL = the legacy default stream).
+ *
+ * Any 16-byte alignment of the bases is required (float4 staging);
+ * otherwise CS_ERR_INVALID_ARG.  Ownership, execution, errors: as
+ * cs_constrained_softmax; no intermediate goes to global memory.
+ */
+cs_status cs_biencoder_attention(const float* query,
+                                 const float* context_keys,
+                                 const float* context_values, float* output,
+                                 int32_t batch_size, int32_t query_len,
+                                 int32_t context_len, int32_t d_head,
+                                 int32_t num_heads, float scale,
+                                 float entropy_bound, void* stream);
+
+/*
+ * The same with the search parameters of cs_constrained_softmax and two
+ * optional outputs: attn_out [batch, num_heads, query_len, context_len]
+ * (the weights of step 2) and t_out [batch, num_heads, query_len] (each
+ * row's temperature), either may be NULL.  options: CS_VARIANT_AUTO or
+ * CS_VARIANT_ROWGROUP with param = lanes per query row (a power of two,
+ * 8 x lanes >= context_len); threads and strict must be 0.
+ */
+cs_status cs_biencoder_attention_ex(const float* query,
+                                    const float* context_keys,
+                                    const float* context_values,
+                                    float* output, int32_t batch_size,
+                                    int32_t query_len, int32_t context_len,
+                                    int32_t d_head, int32_t num_heads,
+                                    float scale, float entropy_bound,
+                                    float t_min, float t_max,
+                                    int32_t max_iter, float* attn_out,
+                                    float* t_out, const cs_options* options,
+                                    void* stream);
+
+/* Host-only plan (lanes per query row, CTAs, shared memory) for the given
+ * limits, and host-only argument check of cs_biencoder_attention_ex. */
+cs_status cs_plan_biencoder_host(int32_t batch_size, int32_t query_len,
+                                 int32_t context_len, int32_t d_head,
+                                 int32_t num_heads, const cs_options* options,
+                                 int32_t smem_per_block_optin, cs_plan* plan);
+cs_status cs_check_biencoder_args(const float* query,
+                                  const float* context_keys,
+                                  const float* context_values,
+                                  const float* output, int32_t batch_size,
+                                  int32_t query_len, int32_t context_len,
+                                  int32_t d_head, int32_t num_heads,
+                                  float scale, float entropy_bound,
+                                  float t_min, float t_max, int32_t max_iter,
+                                  const float* attn_out, const float* t_out);
+
+/*
  * Throughput probe of the ex2 unit, the unit this operation is bound by.
  * Launches one kernel over all SMs in which every thread runs `iters`
  * rounds of 8 independent ex2.approx.ftz.f32 chains; *ex2_count receives

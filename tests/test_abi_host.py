@@ -365,3 +365,57 @@ def test_attention_forced_variants_and_limits():
     assert st == C["CS_ERR_INVALID_ARG"]
     st, _ = aplan(1, 1, 60000)
     assert st == C["CS_ERR_OOM"]
+
+
+# ---------------------------------------------------------- biencoder_attention
+Q0, K0, V0, O0 = 1 << 20, 1 << 24, 1 << 26, 1 << 28
+
+
+@pytest.mark.parametrize("args,status", [
+    ((Q0, K0, V0, O0, 2, 8, 64, 64, 4, 0.125, 0.2, 0.01, 10.0, 20, None, None), 0),
+    ((None, None, None, None, 0, 8, 64, 64, 4, 0.125, 0.2, 0.01, 10.0, 20, None, None), 0),
+    ((Q0, K0, V0, O0, 2, 8, 0, 64, 4, 0.125, 0.2, 0.01, 10.0, 20, None, None), 6),
+    ((Q0, K0, V0, O0, -1, 8, 64, 64, 4, 0.125, 0.2, 0.01, 10.0, 20, None, None), 6),
+    ((Q0, K0, V0, O0, 2, 8, 257, 64, 4, 0.125, 0.2, 0.01, 10.0, 20, None, None), 7),
+    ((Q0, K0, V0, O0, 2, 8, 64, 260, 4, 0.125, 0.2, 0.01, 10.0, 20, None, None), 7),
+    ((Q0, K0, V0, O0, 2, 8, 64, 62, 4, 0.125, 0.2, 0.01, 10.0, 20, None, None), 8),
+    ((Q0, K0, V0, O0, 2, 8, 64, 64, 4, float("inf"), 0.2, 0.01, 10.0, 20, None, None), 8),
+    ((Q0, K0, V0, O0, 2, 8, 64, 64, 4, 0.125, float("nan"), 0.01, 10.0, 20, None, None), 8),
+    ((Q0, K0, V0, O0, 2, 8, 64, 64, 4, 0.125, 0.2, 0.0, 10.0, 20, None, None), 8),
+    ((Q0 + 4, K0, V0, O0, 2, 8, 64, 64, 4, 0.125, 0.2, 0.01, 10.0, 20, None, None), 8),
+    ((Q0, K0, V0, Q0, 2, 8, 64, 64, 4, 0.125, 0.2, 0.01, 10.0, 20, None, None), 8),
+    ((Q0, K0, V0, K0 + 16, 2, 8, 64, 64, 4, 0.125, 0.2, 0.01, 10.0, 20, None, None), 8),
+    ((Q0, K0, V0, O0, 2, 8, 64, 64, 4, 0.125, 0.2, 0.01, 10.0, 20, O0 + 64, None), 8),
+    ((Q0, K0, V0, O0, 2, 8, 64, 64, 4, 0.125, 0.2, 0.01, 10.0, 20, None, V0), 8),
+    ((Q0, K0, V0, O0, 2, 8, 64, 64, 4, 0.125, 0.2, 0.01, 10.0, 20, 1 << 30, (1 << 30) + 16384 * 4), 0),
+])
+def test_check_biencoder_args(args, status):
+    assert cs.cs_check_biencoder_args(*args) == status
+
+
+def test_biencoder_plans():
+    st, p = cs.cs_plan_biencoder_host(32, 512, 64, 64, 8, None, 232448)
+    p = p.as_dict()
+    assert st == 0 and p["lanes_per_row"] == 8 and p["threads_per_cta"] == 256
+    assert p["grid_ctas"] == 32 * 8 * (512 // 32)
+    st, p = cs.cs_plan_biencoder_host(4, 1024, 256, 64, 8, None, 232448)
+    assert st == 0 and p.lanes_per_row == 32
+    assert p.smem_bytes <= 232448
+    st, _ = cs.cs_plan_biencoder_host(4, 1024, 256, 128, 8, None, 232448)
+    assert st == C["CS_ERR_OOM"]            # keys and values exceed smem
+    for K in (1, 8, 9, 64, 65, 256):
+        st, p = cs.cs_plan_biencoder_host(1, 10, K, 16, 1, None, 232448)
+        assert st == 0 and 8 * p.lanes_per_row >= K
+        assert p.lanes_per_row == 1 or 4 * p.lanes_per_row < K
+    st, _ = cs.cs_plan_biencoder_host(1, 10, 40, 16, 1,
+                                      cs.options(C["CS_VARIANT_ROWGROUP"], 4),
+                                      232448)
+    assert st == C["CS_ERR_OOM"]
+    st, p = cs.cs_plan_biencoder_host(1, 10, 40, 16, 1,
+                                      cs.options(C["CS_VARIANT_ROWGROUP"], 8),
+                                      232448)
+    assert st == 0 and p.lanes_per_row == 8
+    st, _ = cs.cs_plan_biencoder_host(1, 10, 40, 16, 1,
+                                      cs.options(C["CS_VARIANT_CLUSTER"], 1),
+                                      232448)
+    assert st == C["CS_ERR_INVALID_ARG"]
