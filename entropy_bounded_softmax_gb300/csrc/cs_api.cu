@@ -830,9 +830,11 @@ cs_status cs_plan_biencoder_host(int32_t batch_size, int32_t query_len,
     }
     const int64_t smem = cs::bienc_smem_bytes(context_len, d_head, G);
     if (smem > smem_per_block_optin) return CS_ERR_OOM;
-    const int64_t rows_per_cta = cs::kBiencThreads / G;
-    const int64_t tiles = ceil_div(query_len, rows_per_cta);
-    const int64_t grid = static_cast<int64_t>(batch_size) * num_heads * tiles;
+    const int64_t rows_per_tile = cs::kBiencThreads / G;
+    const int64_t tiles = ceil_div(query_len, rows_per_tile);
+    const int64_t per = cs::bienc_tiles_per_cta(query_len, G);
+    const int64_t grid = static_cast<int64_t>(batch_size) * num_heads *
+                         ceil_div(tiles, per);
     if (grid > kMaxGridX) return CS_ERR_DIM_MISMATCH;
     *plan = cs_plan{};
     plan->variant = CS_VARIANT_ROWGROUP;

@@ -195,6 +195,16 @@ inline int64_t bienc_smem_bytes(int K, int D, int G) {
                 R * (kp + 4));
 }
 
+// Query tiles one CTA works through with its staged keys and values:
+// about 128 query rows, at most the pair's whole query range.
+inline int bienc_tiles_per_cta(int Q, int G) {
+    const int R = kBiencThreads / G;
+    const int tiles = (Q + R - 1) / R;
+    int per = (128 + R - 1) / R;
+    if (per > tiles) per = tiles;
+    return per < 1 ? 1 : per;
+}
+
 cudaError_t launch_bienc(const BiencTask& task, int lanes_per_row,
                          int smem_bytes, cudaStream_t stream);
 

@@ -10,9 +10,9 @@
 // live in registers and shared memory); optionally the weights and the
 // temperatures are written out too.
 //
-// One CTA per bh and tile of R = 256 / G query rows: the keys (transposed,
-// d-major) and values of bh and the tile's queries are staged in shared
-// memory once.  G lanes share a query row: lane `sub` owns keys
+// One CTA per bh and run of query tiles (R = 256 / G rows a tile, about
+// 128 rows a CTA): the keys (transposed, d-major) and values of bh are
+// staged in shared memory once, then each tile's queries in turn.  G lanes share a query row: lane `sub` owns keys
 // j = 4 (i G + sub) + c (i < 2, c < 4), eight per lane, read as float4s of
 // the transposed keys, and output columns 4 (sub + k G) .. + 3.
 #include <math.h>
@@ -35,7 +35,7 @@ struct BiencSmem {
 
 template <int G>
 __global__ void __launch_bounds__(kBiencThreads)
-bienc_kernel(BiencTask t, int tiles) {
+bienc_kernel(BiencTask t, int tiles, int tiles_per_cta) {
     constexpr int R = kBiencThreads / G;
     extern __shared__ __align__(16) float smem_f[];
     const int K = t.K, D = t.D;
@@ -46,118 +46,127 @@ bienc_kernel(BiencTask t, int tiles) {
     sm.qs = sm.vs + K * D;
     sm.ps = sm.qs + R * (D + 4);
 
-    const int64_t bh = blockIdx.x / tiles;
-    const int i0 = (blockIdx.x % tiles) * R;
-    const int nrows = min(R, t.Q - i0);
+    const int ctas_per_bh = (tiles + tiles_per_cta - 1) / tiles_per_cta;
+    const int64_t bh = blockIdx.x / ctas_per_bh;
+    const int tile0 = (blockIdx.x % ctas_per_bh) * tiles_per_cta;
+    const int tile1 = min(tiles, tile0 + tiles_per_cta);
     const float* kg = t.k + bh * K * D;
     const float* vg = t.v + bh * K * D;
-    const float* qg = t.q + (bh * t.Q + i0) * D;
 
-    // Stage: keys transposed (zero past K), values, the tile's queries.
+    // Stage the keys (transposed, zero past K) and values of bh once.
     for (int e = threadIdx.x; e < K * D; e += blockDim.x)
         sm.kt[(e % D) * kp + e / D] = __ldg(kg + e);
     for (int e = threadIdx.x; e < D * (kp - K); e += blockDim.x)
         sm.kt[(e / (kp - K)) * kp + K + e % (kp - K)] = 0.0f;
     for (int e = threadIdx.x; e < K * D; e += blockDim.x) sm.vs[e] = __ldg(vg + e);
-    for (int e = threadIdx.x; e < nrows * D; e += blockDim.x)
-        sm.qs[(e / D) * (D + 4) + e % D] = __ldcs(qg + e);
-    __syncthreads();
 
-    const int lane = threadIdx.x & 31;
-    const int sub = lane & (G - 1);
-    const int rr = threadIdx.x / G;
-    const unsigned gmask =
-        G == 32 ? 0xffffffffu : (((1u << G) - 1u) << (lane & ~(G - 1)));
-    const bool live = rr < nrows;
-    const float* qr = sm.qs + (live ? rr : 0) * (D + 4);
+    for (int tile = tile0; tile < tile1; ++tile) {
+        const int i0 = tile * R;
+        const int nrows = min(R, t.Q - i0);
+        const float* qg = t.q + (bh * t.Q + i0) * D;
+        // The tile's queries (the previous tile's readers are done: the
+        // __syncthreads at the end of the loop).
+        for (int e = threadIdx.x; e < nrows * D; e += blockDim.x)
+            sm.qs[(e / D) * (D + 4) + e % D] = __ldcs(qg + e);
+        __syncthreads();
 
-    // Step 1: eight scores per lane, each an in-order fma chain over d.
-    float4 acc[kBiencE4];
+        const int lane = threadIdx.x & 31;
+        const int sub = lane & (G - 1);
+        const int rr = threadIdx.x / G;
+        const unsigned gmask =
+            G == 32 ? 0xffffffffu : (((1u << G) - 1u) << (lane & ~(G - 1)));
+        const bool live = rr < nrows;
+        const float* qr = sm.qs + (live ? rr : 0) * (D + 4);
+
+        // Step 1: eight scores per lane, each an in-order fma chain over d.
+        float4 acc[kBiencE4];
 #pragma unroll
-    for (int i = 0; i < kBiencE4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int d4 = 0; d4 < D; d4 += 4) {
-        const float4 qv = *reinterpret_cast<const float4*>(qr + d4);
-        const float qd[4] = {qv.x, qv.y, qv.z, qv.w};
+        for (int i = 0; i < kBiencE4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int d4 = 0; d4 < D; d4 += 4) {
+            const float4 qv = *reinterpret_cast<const float4*>(qr + d4);
+            const float qd[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
-        for (int dd = 0; dd < 4; ++dd) {
-            const float* krow = sm.kt + (d4 + dd) * kp;
+            for (int dd = 0; dd < 4; ++dd) {
+                const float* krow = sm.kt + (d4 + dd) * kp;
 #pragma unroll
-            for (int i = 0; i < kBiencE4; ++i) {
-                const int j0 = 4 * (i * G + sub);
-                if (j0 < kp) {
-                    const float4 kv = *reinterpret_cast<const float4*>(krow + j0);
-                    acc[i].x = fmaf(qd[dd], kv.x, acc[i].x);
-                    acc[i].y = fmaf(qd[dd], kv.y, acc[i].y);
-                    acc[i].z = fmaf(qd[dd], kv.z, acc[i].z);
-                    acc[i].w = fmaf(qd[dd], kv.w, acc[i].w);
+                for (int i = 0; i < kBiencE4; ++i) {
+                    const int j0 = 4 * (i * G + sub);
+                    if (j0 < kp) {
+                        const float4 kv = *reinterpret_cast<const float4*>(krow + j0);
+                        acc[i].x = fmaf(qd[dd], kv.x, acc[i].x);
+                        acc[i].y = fmaf(qd[dd], kv.y, acc[i].y);
+                        acc[i].z = fmaf(qd[dd], kv.z, acc[i].z);
+                        acc[i].w = fmaf(qd[dd], kv.w, acc[i].w);
+                    }
                 }
             }
         }
-    }
-    float4 y[kBiencE4];
-    float m = -INFINITY, bad = 0.0f;
+        float4 y[kBiencE4];
+        float m = -INFINITY, bad = 0.0f;
 #pragma unroll
-    for (int i = 0; i < kBiencE4; ++i) {
-        const float a[4] = {acc[i].x, acc[i].y, acc[i].z, acc[i].w};
-        float s[4];
+        for (int i = 0; i < kBiencE4; ++i) {
+            const float a[4] = {acc[i].x, acc[i].y, acc[i].z, acc[i].w};
+            float s[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const int j = 4 * (i * G + sub) + c;
-            s[c] = -INFINITY;
-            if (live && j < K) {
-                s[c] = __fmul_rn(a[c], t.scale);
-                m = fmaxf(m, s[c]);
-                bad = fmaf(s[c], 0.0f, bad);
+            for (int c = 0; c < 4; ++c) {
+                const int j = 4 * (i * G + sub) + c;
+                s[c] = -INFINITY;
+                if (live && j < K) {
+                    s[c] = __fmul_rn(a[c], t.scale);
+                    m = fmaxf(m, s[c]);
+                    bad = fmaf(s[c], 0.0f, bad);
+                }
             }
+            y[i] = make_float4(s[0], s[1], s[2], s[3]);
         }
-        y[i] = make_float4(s[0], s[1], s[2], s[3]);
-    }
 
-    // Step 2: the row's constrained softmax.
-    const SearchCfg cfg{t.t_min, t.hi0, t.entropy_bound,
-                        t.entropy_bound * kLog2e,
-                        t.entropy_bound > 0.0f ? lg2_approx(t.entropy_bound) : 0.0f,
-                        make_grid(t.t_min, fmaxf(t.hi0, t.t_min), t.max_iter)};
-    RowSolution sol{NAN, 0.0f, 0.0f, 0u, true};
-    if (live)   // uniform over the lane group
-        sol = solve_row<G, kBiencE4>(y, m, bad, cfg, t.entropy_bound * kLog2e,
-                                     false, gmask);
-    float* pr = sm.ps + (live ? rr : 0) * (kp + 4);
-    const int64_t row = bh * t.Q + i0 + rr;
+        // Step 2: the row's constrained softmax.
+        const SearchCfg cfg{t.t_min, t.hi0, t.entropy_bound,
+                            t.entropy_bound * kLog2e,
+                            t.entropy_bound > 0.0f ? lg2_approx(t.entropy_bound) : 0.0f,
+                            make_grid(t.t_min, fmaxf(t.hi0, t.t_min), t.max_iter)};
+        RowSolution sol{NAN, 0.0f, 0.0f, 0u, true};
+        if (live)   // uniform over the lane group
+            sol = solve_row<G, kBiencE4>(y, m, bad, cfg, t.entropy_bound * kLog2e,
+                                         false, gmask);
+        float* pr = sm.ps + (live ? rr : 0) * (kp + 4);
+        const int64_t row = bh * t.Q + i0 + rr;
 #pragma unroll
-    for (int i = 0; i < kBiencE4; ++i) {
-        const float yy[4] = {y[i].x, y[i].y, y[i].z, y[i].w};
+        for (int i = 0; i < kBiencE4; ++i) {
+            const float yy[4] = {y[i].x, y[i].y, y[i].z, y[i].w};
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const int j = 4 * (i * G + sub) + c;
-            if (live && j < K) {
-                const float p = sol.zero ? 0.0f : ex2(yy[c] * sol.beta_out) * sol.inv_s;
-                pr[j] = p;
-                if (t.attn_out) __stcs(t.attn_out + row * K + j, p);
+            for (int c = 0; c < 4; ++c) {
+                const int j = 4 * (i * G + sub) + c;
+                if (live && j < K) {
+                    const float p = sol.zero ? 0.0f : ex2(yy[c] * sol.beta_out) * sol.inv_s;
+                    pr[j] = p;
+                    if (t.attn_out) __stcs(t.attn_out + row * K + j, p);
+                }
             }
         }
-    }
-    __syncwarp(gmask);
+        __syncwarp(gmask);
 
-    // Step 3: four output columns at a time, keys in order.
-    if (live) {
-        float* og = t.out + row * D;
-        for (int c0 = 4 * sub; c0 < D; c0 += 4 * G) {
-            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int j = 0; j < K; ++j) {
-                const float p = pr[j];
-                const float4 v = *reinterpret_cast<const float4*>(sm.vs + j * D + c0);
-                o.x = fmaf(p, v.x, o.x);
-                o.y = fmaf(p, v.y, o.y);
-                o.z = fmaf(p, v.z, o.z);
-                o.w = fmaf(p, v.w, o.w);
+        // Step 3: four output columns at a time, keys in order.
+        if (live) {
+            float* og = t.out + row * D;
+            for (int c0 = 4 * sub; c0 < D; c0 += 4 * G) {
+                float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int j = 0; j < K; ++j) {
+                    const float p = pr[j];
+                    const float4 v = *reinterpret_cast<const float4*>(sm.vs + j * D + c0);
+                    o.x = fmaf(p, v.x, o.x);
+                    o.y = fmaf(p, v.y, o.y);
+                    o.z = fmaf(p, v.z, o.z);
+                    o.w = fmaf(p, v.w, o.w);
+                }
+                __stcs(reinterpret_cast<float4*>(og + c0), o);
             }
-            __stcs(reinterpret_cast<float4*>(og + c0), o);
+            if (sub == 0) {
+                if (t.t_out) t.t_out[row] = sol.T_row;
+                raise_error(t.err, sol.bits);
+            }
         }
-        if (sub == 0) {
-            if (t.t_out) t.t_out[row] = sol.T_row;
-            raise_error(t.err, sol.bits);
-        }
+        __syncthreads();
     }
 }
 
@@ -165,9 +174,11 @@ bienc_kernel(BiencTask t, int tiles) {
 
 cudaError_t launch_bienc(const BiencTask& task, int lanes_per_row,
                          int smem_bytes, cudaStream_t stream) {
-    const int rows_per_cta = kBiencThreads / lanes_per_row;
-    const int tiles = (task.Q + rows_per_cta - 1) / rows_per_cta;
-    const int64_t grid = static_cast<int64_t>(task.BH) * tiles;
+    const int rows_per_tile = kBiencThreads / lanes_per_row;
+    const int tiles = (task.Q + rows_per_tile - 1) / rows_per_tile;
+    const int tiles_per_cta = bienc_tiles_per_cta(task.Q, lanes_per_row);
+    const int64_t grid = static_cast<int64_t>(task.BH) *
+                         ((tiles + tiles_per_cta - 1) / tiles_per_cta);
     const void* kern = nullptr;
     switch (lanes_per_row) {
         case 1: kern = reinterpret_cast<const void*>(bienc_kernel<1>); break;
@@ -185,12 +196,12 @@ cudaError_t launch_bienc(const BiencTask& task, int lanes_per_row,
     if (e != cudaSuccess) return e;
     const dim3 gd(static_cast<unsigned>(grid)), bd(kBiencThreads);
     switch (lanes_per_row) {
-        case 1: bienc_kernel<1><<<gd, bd, smem_bytes, stream>>>(task, tiles); break;
-        case 2: bienc_kernel<2><<<gd, bd, smem_bytes, stream>>>(task, tiles); break;
-        case 4: bienc_kernel<4><<<gd, bd, smem_bytes, stream>>>(task, tiles); break;
-        case 8: bienc_kernel<8><<<gd, bd, smem_bytes, stream>>>(task, tiles); break;
-        case 16: bienc_kernel<16><<<gd, bd, smem_bytes, stream>>>(task, tiles); break;
-        default: bienc_kernel<32><<<gd, bd, smem_bytes, stream>>>(task, tiles); break;
+        case 1: bienc_kernel<1><<<gd, bd, smem_bytes, stream>>>(task, tiles, tiles_per_cta); break;
+        case 2: bienc_kernel<2><<<gd, bd, smem_bytes, stream>>>(task, tiles, tiles_per_cta); break;
+        case 4: bienc_kernel<4><<<gd, bd, smem_bytes, stream>>>(task, tiles, tiles_per_cta); break;
+        case 8: bienc_kernel<8><<<gd, bd, smem_bytes, stream>>>(task, tiles, tiles_per_cta); break;
+        case 16: bienc_kernel<16><<<gd, bd, smem_bytes, stream>>>(task, tiles, tiles_per_cta); break;
+        default: bienc_kernel<32><<<gd, bd, smem_bytes, stream>>>(task, tiles, tiles_per_cta); break;
     }
     return cudaGetLastError();
 }

@@ -397,7 +397,7 @@ def test_biencoder_plans():
     st, p = cs.cs_plan_biencoder_host(32, 512, 64, 64, 8, None, 232448)
     p = p.as_dict()
     assert st == 0 and p["lanes_per_row"] == 8 and p["threads_per_cta"] == 256
-    assert p["grid_ctas"] == 32 * 8 * (512 // 32)
+    assert p["grid_ctas"] == 32 * 8 * (512 // 128)
     st, p = cs.cs_plan_biencoder_host(4, 1024, 256, 64, 8, None, 232448)
     assert st == 0 and p.lanes_per_row == 32
     assert p.smem_bytes <= 232448
