@@ -830,7 +830,7 @@ cs_status cs_plan_biencoder_host(int32_t batch_size, int32_t query_len,
     }
     const int64_t smem = cs::bienc_smem_bytes(context_len, d_head, G);
     if (smem > smem_per_block_optin) return CS_ERR_OOM;
-    const int64_t rows_per_tile = cs::kBiencThreads / G;
+    const int64_t rows_per_tile = cs::bienc_threads(G) / G;
     const int64_t tiles = ceil_div(query_len, rows_per_tile);
     const int64_t per = cs::bienc_tiles_per_cta(query_len, G);
     const int64_t grid = static_cast<int64_t>(batch_size) * num_heads *
@@ -840,7 +840,7 @@ cs_status cs_plan_biencoder_host(int32_t batch_size, int32_t query_len,
     plan->variant = CS_VARIANT_ROWGROUP;
     plan->lanes_per_row = G;
     plan->elems_per_lane = 8;
-    plan->threads_per_cta = cs::kBiencThreads;
+    plan->threads_per_cta = cs::bienc_threads(G);
     plan->smem_bytes = static_cast<int32_t>(smem);
     plan->grid_ctas = grid;
     plan->staged_tensors = 3;

@@ -10,8 +10,8 @@
 // live in registers and shared memory); optionally the weights and the
 // temperatures are written out too.
 //
-// One CTA per bh and run of query tiles (R = 256 / G rows a tile, about
-// 128 rows a CTA): the keys (transposed, d-major) and values of bh are
+// One CTA per bh and run of query tiles (R = threads / G rows a tile,
+// about 128 rows a CTA): the keys (transposed, d-major) and values of bh are
 // staged in shared memory once, then each tile's queries in turn.  G lanes share a query row: lane `sub` owns keys
 // j = 4 (i G + sub) + c (i < 2, c < 4), eight per lane, read as float4s of
 // the transposed keys, and output columns 4 (sub + k G) .. + 3.
@@ -34,9 +34,9 @@ struct BiencSmem {
 };
 
 template <int G>
-__global__ void __launch_bounds__(kBiencThreads)
+__global__ void __launch_bounds__(bienc_threads(G))
 bienc_kernel(BiencTask t, int tiles, int tiles_per_cta) {
-    constexpr int R = kBiencThreads / G;
+    constexpr int R = bienc_threads(G) / G;
     extern __shared__ __align__(16) float smem_f[];
     const int K = t.K, D = t.D;
     const int kp = bienc_kp(K);
@@ -174,7 +174,7 @@ bienc_kernel(BiencTask t, int tiles, int tiles_per_cta) {
 
 cudaError_t launch_bienc(const BiencTask& task, int lanes_per_row,
                          int smem_bytes, cudaStream_t stream) {
-    const int rows_per_tile = kBiencThreads / lanes_per_row;
+    const int rows_per_tile = bienc_threads(lanes_per_row) / lanes_per_row;
     const int tiles = (task.Q + rows_per_tile - 1) / rows_per_tile;
     const int tiles_per_cta = bienc_tiles_per_cta(task.Q, lanes_per_row);
     const int64_t grid = static_cast<int64_t>(task.BH) *
@@ -194,7 +194,7 @@ cudaError_t launch_bienc(const BiencTask& task, int lanes_per_row,
     for (int g = lanes_per_row; g > 1; g >>= 1) ++slot;
     cudaError_t e = ensure_smem_attribute(kern, slot, smem_bytes, false);
     if (e != cudaSuccess) return e;
-    const dim3 gd(static_cast<unsigned>(grid)), bd(kBiencThreads);
+    const dim3 gd(static_cast<unsigned>(grid)), bd(bienc_threads(lanes_per_row));
     switch (lanes_per_row) {
         case 1: bienc_kernel<1><<<gd, bd, smem_bytes, stream>>>(task, tiles, tiles_per_cta); break;
         case 2: bienc_kernel<2><<<gd, bd, smem_bytes, stream>>>(task, tiles, tiles_per_cta); break;
