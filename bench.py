@@ -1093,7 +1093,9 @@ def bienc_arm(args, w) -> int:
     for i in range(max(3, args.warmup)):
         launch(i)
     torch.cuda.synchronize()
-    st, plan = cs.cs_plan_biencoder_host(B, Q, K, D, H, None, 232448)
+    props = torch.cuda.get_device_properties(dev)
+    optin = int(getattr(props, "shared_memory_per_block_optin", 232448))
+    st, plan = cs.cs_plan_biencoder_host(B, Q, K, D, H, None, optin)
     plan = plan.as_dict()
     tm = time_launches(args, torch, launch, stream, dist, local)
     total_ms = reduce_max(dist, tm["ms"], dev)

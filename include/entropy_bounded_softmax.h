@@ -99,10 +99,12 @@ typedef struct cs_plan {
     int32_t smem_bytes;      /* dynamic shared memory per CTA               */
     int32_t ctas_per_sm;     /* CTAs resident per SM by the plan's limits   */
     int64_t grid_ctas;       /* CTAs in the launch                          */
-    int32_t staged_tensors;  /* cluster: row tensors a CTA keeps in shared
-                                memory (forward: 1, the logits; backward:
-                                2, p and grad_out, or 1, p alone, with
-                                grad_out read again); rowgroup: 0          */
+    int32_t staged_tensors;  /* tensors a CTA keeps in shared memory
+                                (cluster forward: 1, the logits; cluster
+                                backward: 2, p and grad_out, or 1, p alone,
+                                with grad_out read again; attention row-CTA:
+                                1; biencoder: 3, keys, values and a tile of
+                                queries); rowgroup: 0                      */
 } cs_plan;
 
 /*
@@ -360,8 +362,8 @@ cs_status cs_check_attention_args(const float* scores, const float* out,
  *          max_iter 20.
  * stream   a cudaStream_t (NULL = the legacy default stream).
  *
- * Any 16-byte alignment of the bases is required (float4 staging);
- * otherwise CS_ERR_INVALID_ARG.  Ownership, execution, errors: as
+ * The four bases must be 16-byte aligned (float4 staging); otherwise
+ * CS_ERR_INVALID_ARG.  Ownership, execution, errors: as
  * cs_constrained_softmax; no intermediate goes to global memory.
  */
 cs_status cs_biencoder_attention(const float* query,
