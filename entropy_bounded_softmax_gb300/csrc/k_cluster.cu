@@ -5,9 +5,11 @@
 // Method: "BURT-IMMA CUDA Kernel API Reference", section 2.1
 // `constrained_softmax`, Description steps 1-4, with the error policy of
 // sections 5.3 and 5.4.  Per row:
-//   stage   every thread loads its part of the slice with 128-bit loads
-//           (eight in flight per thread), stores it to shared memory and
-//           folds it into its own max m_t and a finiteness check;
+//   stage   every thread brings its part of the slice into shared memory
+//           (16-byte asynchronous copies, all in flight at once, in
+//           launches with several CTAs per SM; 128-bit loads eight at a
+//           time otherwise) and folds it into its own max m_t and a
+//           finiteness check;
 //   T = 1   one pass turns the thread's classes into y_i = (l_i - m_t)
 //           log2(e) in place and sums S = sum 2^y_i, V = sum y_i 2^y_i,
 //           W = sum y_i^2 2^y_i; a single reduction then forms the row's max
