@@ -44,6 +44,25 @@ from entropy_bounded_softmax_gb300 import workloads as wl  # noqa: E402
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 METRIC = "rows/s and effective HBM GB/s (% of roofline); latency at 32x50000"
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch
+# of the automatic plan, from the committed ncu captures of the current
+# kernel source (profiles/<kernel>_<workload>.md).
+NCU_DRAM_BYTES = {
+    "latency_32x50000": {
+        "bytes": 6487552,
+        "note": "ncu, profiles/cluster_kernel_latency_32x50000.md: the "
+                "6.4 MB input read once; the output was still in L2 when "
+                "the launch ended (it drains afterwards)"},
+    "long_rows_256x131072": {
+        "bytes": 134379776 + 76688896,
+        "note": "ncu, profiles/cluster_kernel_long_rows_256x131072.md: the "
+                "134.2 MB input read once, 76.7 MB of the output drained "
+                "before the launch ended"},
+    "moe_router_65536x64": {
+        "bytes": 16805120,
+        "note": "ncu, profiles/rowgroup_kernel_moe_router_65536x64.md: the "
+                "16.8 MB input read once; the output still in L2 at the end"},
+}
 # The page's figure for this workload: 0.8 ms for batch 32 x 50000 classes
 # on an RTX 3080 (another machine: context, not a target).
 PAGE_LATENCY_MS = {"latency_32x50000": 0.8}
@@ -530,8 +549,12 @@ def our_arm(args, w: wl.Workload) -> int:
                     "peak": peaks["hbm_gbs"],
                     "frac": hbm_rate / peaks["hbm_gbs"],
                     "peak_source": f"{peaks['source']} copy bandwidth"}
+        traffic = NCU_DRAM_BYTES.get(w.name) if not (
+            args.variant != "auto" or args.param or args.threads
+            or args.strict) else None
         roof.update({
-            "traffic": None,
+            "traffic": traffic["bytes"] if traffic else None,
+            "traffic_note": traffic["note"] if traffic else None,
             "kernel": "cluster_kernel" if plan["variant"] == 2 else "rowgroup_kernel",
             "algorithmic_bytes": io_bytes,
             "algorithmic_ex2": exps,
