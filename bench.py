@@ -58,10 +58,6 @@ NCU_DRAM_BYTES = {
         "note": "ncu, profiles/cluster_kernel_long_rows_256x131072.md: the "
                 "134.2 MB input read once, 76.7 MB of the output drained "
                 "before the launch ended"},
-    "moe_router_65536x64": {
-        "bytes": 16805120,
-        "note": "ncu, profiles/rowgroup_kernel_moe_router_65536x64.md: the "
-                "16.8 MB input read once; the output still in L2 at the end"},
 }
 # The page's figure for this workload: 0.8 ms for batch 32 x 50000 classes
 # on an RTX 3080 (another machine: context, not a target).
