@@ -44,21 +44,6 @@ from entropy_bounded_softmax_gb300 import workloads as wl  # noqa: E402
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 METRIC = "rows/s and effective HBM GB/s (% of roofline); latency at 32x50000"
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch
-# of the automatic plan, from the committed ncu captures of the current
-# kernel source (profiles/<kernel>_<workload>.md).
-NCU_DRAM_BYTES = {
-    "latency_32x50000": {
-        "bytes": 6487552,
-        "note": "ncu, profiles/cluster_kernel_latency_32x50000.md: the "
-                "6.4 MB input read once; the output was still in L2 when "
-                "the launch ended (it drains afterwards)"},
-    "long_rows_256x131072": {
-        "bytes": 134379776 + 76688896,
-        "note": "ncu, profiles/cluster_kernel_long_rows_256x131072.md: the "
-                "134.2 MB input read once, 76.7 MB of the output drained "
-                "before the launch ended"},
-}
 # The page's figure for this workload: 0.8 ms for batch 32 x 50000 classes
 # on an RTX 3080 (another machine: context, not a target).
 PAGE_LATENCY_MS = {"latency_32x50000": 0.8}
@@ -92,6 +77,9 @@ def parse_args(argv=None):
                     help="untimed load before the timed region, for the "
                          "clock samples")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-configuration timings that follow "
+                         "the headline")
     ap.add_argument("--no-graph", action="store_true",
                     help="time plain stream launches instead of one CUDA "
                          "graph of the K launches")
@@ -257,25 +245,73 @@ def probe_ex2_peak(torch, cs, stream_ptr) -> float:
 
 
 # --------------------------------------------------------- algorithmic work
-def searched_rows(w: wl.Workload, x: np.ndarray) -> int:
-    """Rows whose entropy at T = 1 exceeds the bound (they run the full
-    bisection); a workload property computed in fp64 with scipy."""
+def entropy_at_one(x: np.ndarray) -> np.ndarray:
+    """H(1) of every row in fp64 (scipy), the workload property that decides
+    which rows run the bisection."""
     import scipy.special
-    n = 0
+    out = np.empty(x.shape[0])
     step = 256
     for r0 in range(0, x.shape[0], step):
         blk = x[r0:r0 + step].astype(np.float64)
         p = scipy.special.softmax(blk, axis=1)
-        H = scipy.special.entr(p).sum(axis=1)
-        n += int(np.sum(H > np.float32(w.entropy_bound)))
-    return n
+        out[r0:r0 + step] = scipy.special.entr(p).sum(axis=1)
+    return out
+
+
+def searched_rows(w: wl.Workload, x: np.ndarray, h1=None) -> int:
+    """Rows whose entropy at T = 1 exceeds the bound (they run the full
+    bisection)."""
+    h1 = entropy_at_one(x) if h1 is None else h1
+    return int(np.sum(h1 > np.float32(w.entropy_bound)))
+
+
+def formula_ex2(w: wl.Workload, n_search: int) -> int:
+    """The roofline's exponentials: (1 + max_iter) per class of a searched
+    row, 1 per class of the others (the T = 1 pass; the output pass is not
+    counted)."""
+    return (w.batch + n_search * w.max_iter) * w.num_classes
+
+
+def ex2_roofline(ex2_formula: int, ex2_executed: int | None, io_bytes: int,
+                 t_kernel: float, ex2_peak: float, hbm_gbs: float) -> dict:
+    """The kernel against the slower of HBM (io_bytes at the measured copy
+    bandwidth) and the ex2 unit (the formula's exponentials at the probe's
+    rate); frac_executed counts instead the exponentials the kernel issued
+    (every temperature each row was evaluated at, from the kernel's own
+    per-row counts, output pass included)."""
+    ex2_rate = ex2_formula / t_kernel
+    hbm_rate = io_bytes / t_kernel / 1e9
+    t_hbm = io_bytes / (hbm_gbs * 1e9)
+    t_ex2 = ex2_formula / ex2_peak
+    if t_ex2 >= t_hbm:
+        roof = {"bound": "alu", "unit": "Gex2/s", "achieved": ex2_rate / 1e9,
+                "peak": ex2_peak / 1e9, "frac": ex2_rate / ex2_peak,
+                "peak_source": "measured ex2 probe (burst)"}
+    else:
+        roof = {"bound": "hbm", "unit": "GB/s", "achieved": hbm_rate,
+                "peak": hbm_gbs, "frac": hbm_rate / hbm_gbs,
+                "peak_source": "measured copy bandwidth"}
+    roof.update({
+        "algorithmic_bytes": io_bytes,
+        "algorithmic_ex2": ex2_formula,
+        "executed_ex2": ex2_executed,
+        "frac_executed": (ex2_executed / t_kernel / ex2_peak
+                          if ex2_executed is not None else None),
+        "hbm_gbs": hbm_rate,
+        "hbm_frac": hbm_rate / hbm_gbs,
+        "hbm_peak": hbm_gbs,
+        "roofline_us": max(t_hbm, t_ex2) * 1e6,
+        "frac_of_roofline": max(t_hbm, t_ex2) / t_kernel,
+    })
+    return roof
 
 
 # ------------------------------------------------------------ reference arm
 def run_oracle_sample(w: wl.Workload, x: np.ndarray, seconds: float,
                       threads: int) -> dict:
     """The CPU oracle, as it stands, on whole rows of the workload until
-    `seconds` have passed (at least one batch of `threads` rows)."""
+    `seconds` have passed (at least one batch of `threads` rows; threads =
+    1 gives the single-core figure)."""
     import oracle
     oracle.load()
     done = 0
@@ -524,52 +560,50 @@ def our_arm(args, w: wl.Workload) -> int:
     e2e = {k: reduce_max(dist, v, dev) for k, v in e2e.items()}
     e2e_value = aggregate_rows_per_s(B, world, e2e["pipelined"] * 1e-3)
 
+    # The exponentials the kernel issues: one untimed launch with the
+    # per-row evaluation counts (the search is deterministic, so every timed
+    # launch issues the same).
+    evals = torch.zeros(B, dtype=torch.int32, device=dev)
+    cs.constrained_softmax(ins[0], w.entropy_bound, w.t_min, w.t_max,
+                           w.max_iter, out=outs[0], variant=args.variant,
+                           param=args.param, threads=args.threads,
+                           strict=args.strict, evals_out=evals)
+    ex2_executed = int(evals.sum().item()) * C
+
     line = None
     if rank == 0:
         peaks = measured_peaks()
         ex2_peak = probe_ex2_peak(torch, cs, sptr)
         n_search = searched_rows(w, x)
-        exps = (B + n_search * w.max_iter) * C
+        exps = formula_ex2(w, n_search)
         t_kernel = ms_per_step * 1e-3
-        ex2_rate = exps / t_kernel
         hbm_rate = io_bytes / t_kernel / 1e9
-        t_hbm = io_bytes / (peaks["hbm_gbs"] * 1e9)
-        t_ex2 = exps / ex2_peak
-        if t_ex2 >= t_hbm:
-            roof = {"bound": "alu", "unit": "Gex2/s",
-                    "achieved": ex2_rate / 1e9, "peak": ex2_peak / 1e9,
-                    "frac": ex2_rate / ex2_peak,
-                    "peak_source": "measured ex2 probe (burst)"}
-        else:
-            roof = {"bound": "hbm", "unit": "GB/s", "achieved": hbm_rate,
-                    "peak": peaks["hbm_gbs"],
-                    "frac": hbm_rate / peaks["hbm_gbs"],
-                    "peak_source": f"{peaks['source']} copy bandwidth"}
-        traffic = NCU_DRAM_BYTES.get(w.name) if not (
-            args.variant != "auto" or args.param or args.threads
-            or args.strict) else None
+        roof = ex2_roofline(exps, ex2_executed, io_bytes, t_kernel, ex2_peak,
+                            peaks["hbm_gbs"])
         roof.update({
-            "traffic": traffic["bytes"] if traffic else None,
-            "traffic_note": traffic["note"] if traffic else None,
+            "traffic": None,
+            "traffic_note": "DRAM bytes need an ncu capture of this build; "
+                            "not measured in this run",
             "kernel": "cluster_kernel" if plan["variant"] == 2 else "rowgroup_kernel",
-            "algorithmic_bytes": io_bytes,
-            "algorithmic_ex2": exps,
             "searched_rows": n_search,
-            "hbm_gbs": hbm_rate,
-            "hbm_frac": hbm_rate / peaks["hbm_gbs"],
-            "hbm_peak": peaks["hbm_gbs"],
-            "roofline_us": max(t_hbm, t_ex2) * 1e6,
-            "frac_of_roofline": max(t_hbm, t_ex2) / t_kernel,
+            "evals_per_row_mean": (
+                float(evals.float().mean().item()) if B else None),
         })
         cpu = None
         if not args.no_cpu_baseline:
             import oracle
             threads = oracle.default_threads()
             s = run_oracle_sample(w, x, args.cpu_seconds, threads)
+            s1 = run_oracle_sample(w, x, args.cpu_seconds / 2, 1)
             cpu = {"value": s["rows_per_s"], "unit": "rows/s",
                    "cores": threads, "kind": "oracle",
                    "sample": f"{s['rows']} whole rows of the workload in "
-                             f"{s['seconds']:.1f} s, one row per thread"}
+                             f"{s['seconds']:.1f} s, one row per thread",
+                   "single_core": {
+                       "value": s1["rows_per_s"], "unit": "rows/s",
+                       "cores": 1,
+                       "sample": f"{s1['rows']} whole rows in "
+                                 f"{s1['seconds']:.1f} s on one thread"}}
         clocks = sampler.summary(t_soak, t_end)
         page_ms = PAGE_LATENCY_MS.get(w.name)
         line = {
@@ -594,12 +628,129 @@ def our_arm(args, w: wl.Workload) -> int:
             "clocks": clocks,
             "device_errors": sorted(err),
         }
+        if not args.no_per_config and not args.batch:
+            line["per_config"] = per_config_runs(
+                torch, cs, dev, stream, ex2_peak, peaks["hbm_gbs"],
+                skip=w.name, cpu=not args.no_cpu_baseline)
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
     if line is not None:
         print(json.dumps(line), flush=True)
     return 0
+
+
+# ------------------------------------------------------------ per config
+def per_config_workloads() -> list[wl.Workload]:
+    """Every configuration of the benchmark besides the headline's:
+    4 x 1000, the 65536 x 64 router, 256 x 131072 long rows and the six
+    points of the 4096 x 32000 sweep."""
+    return [wl.SMALL, wl.LATENCY, wl.ROUTER, wl.LONG] + wl.sweep_workloads()
+
+
+def per_config_runs(torch, cs, dev, stream, ex2_peak: float, hbm_gbs: float,
+                    skip: str = "", cpu: bool = True,
+                    min_seconds: float = 0.4) -> dict:
+    """Each configuration timed in this process after the headline, by the
+    headline's rules: automatic plan, a CUDA graph of launches over enough
+    rotating input/output pairs to exceed L2 (or one pair larger than L2),
+    replayed for at least min_seconds between CUDA events on the launching
+    stream, with the SM clocks sampled during that region.  Each entry
+    carries the time per launch, rows/s, HBM GB/s, both ex2 fractions, the
+    plan and the clocks."""
+    sptr = stream.cuda_stream
+    sampler = ClockSampler(dev.index if "CUDA_VISIBLE_DEVICES" not in os.environ
+                           else 0)
+    sampler.start()
+    results = {}
+    cache = {}
+    for w in per_config_workloads():
+        if w.name == skip:
+            continue
+        base = w.name.split("_b")[0] if w.name.startswith(wl.SWEEP.name) else w.name
+        if base not in cache:
+            cache.clear()
+            xw = wl.generate(w)
+            cache[base] = (xw, entropy_at_one(xw))
+        x, h1 = cache[base]
+        B, C = x.shape
+        io_bytes = 8 * B * C
+        nbuf = (max(1, math.ceil(3 * L2_BYTES / io_bytes))
+                if io_bytes < 3 * L2_BYTES else 1)
+        xs = torch.from_numpy(x).to(dev)
+        ins = xs.unsqueeze(0).repeat(nbuf, 1, 1) if nbuf > 1 else xs.unsqueeze(0)
+        outs = torch.empty_like(ins)
+        touts = torch.empty((nbuf, B), dtype=torch.float32, device=dev)
+
+        def launch(i: int, sp: int = sptr) -> None:
+            k = i % nbuf
+            st = cs.cs_constrained_softmax_ex(
+                ins[k].data_ptr(), outs[k].data_ptr(), B, C, w.entropy_bound,
+                w.t_min, w.t_max, w.max_iter, touts[k].data_ptr(), None, sp)
+            if st != 0:
+                raise RuntimeError(f"{w.name}: status {st}")
+
+        for i in range(max(3, min(nbuf, 50))):
+            launch(i)
+        torch.cuda.synchronize()
+        K = max(20, nbuf)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            cap = torch.cuda.current_stream().cuda_stream
+            for j in range(K):
+                launch(j, cap)
+        graph.replay()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        graph.replay()
+        torch.cuda.synchronize()
+        one = max(time.perf_counter() - t0, 1e-6)
+        reps = max(1, math.ceil(min_seconds / one))
+        t_clk0 = time.time()
+        e_a = torch.cuda.Event(enable_timing=True)
+        e_b = torch.cuda.Event(enable_timing=True)
+        e_a.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        e_b.record(stream)
+        torch.cuda.synchronize()
+        t_clk1 = time.time()
+        ms = e_a.elapsed_time(e_b) / (K * reps)
+        evals = torch.zeros(B, dtype=torch.int32, device=dev)
+        cs.constrained_softmax(ins[0], w.entropy_bound, w.t_min, w.t_max,
+                               w.max_iter, out=outs[0], evals_out=evals)
+        n_eval = int(evals.sum().item())
+        n_search = searched_rows(w, x, h1)
+        t_kernel = ms * 1e-3
+        roof = ex2_roofline(formula_ex2(w, n_search), n_eval * C, io_bytes,
+                            t_kernel, ex2_peak, hbm_gbs)
+        entry = {
+            "batch": B, "num_classes": C, "entropy_bound": w.entropy_bound,
+            "max_iter": w.max_iter, "launches_timed": K * reps,
+            "ms_per_step": ms, "rows_per_s": B / t_kernel,
+            "hbm_gbs": roof["hbm_gbs"], "bound": roof["bound"],
+            "frac": roof["frac"], "frac_executed": roof["frac_executed"],
+            "hbm_frac": roof["hbm_frac"], "roofline_us": roof["roofline_us"],
+            "searched_rows": n_search, "evals_per_row_mean": n_eval / B,
+            "plan": cs.plan(B, C),
+            "l2": (f"rotating {nbuf} input/output pairs" if nbuf > 1
+                   else "inputs larger than L2"),
+            "clocks": sampler.summary(t_clk0, t_clk1),
+        }
+        if cpu and w.name == wl.SMALL.name:
+            import oracle
+            smp = run_oracle_sample(w, x, 1.0, 1)
+            entry["cpu_baseline_single_core"] = {
+                "value": smp["rows_per_s"], "unit": "rows/s", "cores": 1,
+                "kind": "oracle",
+                "sample": f"{smp['rows']} whole rows in "
+                          f"{smp['seconds']:.1f} s on one thread"}
+        results[w.name] = entry
+        del graph, ins, outs, touts, xs, evals
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    sampler.stop()
+    return results
 
 
 # --------------------------------------------------------------- backward

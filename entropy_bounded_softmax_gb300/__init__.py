@@ -82,7 +82,8 @@ def constrained_softmax(logits, entropy_bound: float = DEFAULT_ENTROPY_BOUND,
                         max_iter: int = DEFAULT_MAX_ITER,
                         return_t: bool = False, out=None, t_out=None,
                         variant: str = "auto", param: int = 0,
-                        threads: int = 0, strict: bool = False):
+                        threads: int = 0, strict: bool = False,
+                        evals_out=None):
     """Entropy-bounded softmax of a CUDA fp32 [batch, num_classes] tensor.
 
     Returns the probabilities (and the per-row temperature if ``return_t``).
@@ -90,7 +91,9 @@ def constrained_softmax(logits, entropy_bound: float = DEFAULT_ENTROPY_BOUND,
     is asynchronous on the current stream; per-row conditions (NaN/Inf rows,
     unsatisfiable bounds) are read with :func:`get_error`.
     ``variant``/``param``/``threads``/``strict`` are the launch options
-    of ``cs_constrained_softmax_ex`` (defaults: automatic).
+    of ``cs_constrained_softmax_ex`` (defaults: automatic); ``evals_out``, an
+    int32 [batch] tensor on the same device, receives how many temperatures
+    each row's exponentials were evaluated at.
     """
     import torch
     if not isinstance(logits, torch.Tensor):
@@ -120,11 +123,22 @@ def constrained_softmax(logits, entropy_bound: float = DEFAULT_ENTROPY_BOUND,
             raise ValueError("t_out must be a contiguous float32 [batch] "
                              "tensor on the logits' device")
         t_ptr = t_out.data_ptr()
+    e_ptr = None
+    if evals_out is not None:
+        if (not isinstance(evals_out, torch.Tensor)
+                or evals_out.shape != (batch,)
+                or evals_out.dtype != torch.int32
+                or evals_out.device != logits.device
+                or not evals_out.is_contiguous()):
+            raise ValueError("evals_out must be a contiguous int32 [batch] "
+                             "tensor on the logits' device")
+        e_ptr = evals_out.data_ptr()
     with torch.cuda.device(logits.device):
         st = cs_constrained_softmax_ex(
             logits.data_ptr(), out.data_ptr(), batch, num_classes,
             float(entropy_bound), float(t_min), float(t_max), int(max_iter),
-            t_ptr, options(VARIANTS[variant], param, threads, int(strict)),
+            t_ptr, options(VARIANTS[variant], param, threads, int(strict),
+                           e_ptr),
             _stream_handle(logits.device))
     if st != 0:
         raise CsError(st, "cs_constrained_softmax")

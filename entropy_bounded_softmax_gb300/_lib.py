@@ -25,6 +25,7 @@ class cs_options(ctypes.Structure):
         ("param", ctypes.c_int32),
         ("threads", ctypes.c_int32),
         ("strict", ctypes.c_int32),
+        ("evals_out", ctypes.c_void_p),
     ]
 
 
@@ -156,9 +157,11 @@ def cs_constrained_softmax(logits, out, batch, num_classes, entropy_bound,
                                          max_iter, t_out, stream)
 
 
-def options(variant=0, param=0, threads=0, strict=0):
-    """A cs_options struct (all zero = automatic)."""
-    return cs_options(int(variant), int(param), int(threads), int(strict))
+def options(variant=0, param=0, threads=0, strict=0, evals_out=None):
+    """A cs_options struct (all zero = automatic); evals_out: an optional
+    device pointer (integer) for the per-row evaluation counts."""
+    return cs_options(int(variant), int(param), int(threads), int(strict),
+                      evals_out)
 
 
 def _opt_ref(opt):

@@ -10,10 +10,12 @@
 
 #include "cs_internal.h"
 
-// The library's only device object: a bitmask of (1 << code) for the
+// The library's device objects: a bitmask of (1 << code) for the
 // asynchronous conditions of "BURT-IMMA CUDA Kernel API Reference",
-// section 5.1 (set with atomicOr, so no condition overwrites another).
+// section 5.1 (set with atomicOr, so no condition overwrites another), and
+// the word cs_get_error exchanges it into before copying it to the host.
 __device__ unsigned int g_cs_error_word;
+__device__ unsigned int g_cs_error_taken;
 
 namespace cs {
 int probe_chains();
@@ -32,6 +34,10 @@ constexpr int kRowgroupMaxE4 = 8;      // 32 classes per lane
 constexpr int kAutoRowgroupE4 = 4;     // 16 classes per lane
 constexpr int kAutoRowgroupMaxClasses = 512;
 constexpr int kMaxIter = 1024;
+// Largest t_min accepted: 2^64.  Every temperature a kernel evaluates or
+// writes is at most max(1, t_min), so 1/T >= 2^-64 and the floored
+// exponent (-2^100) times 1/T stays below -2^36: its term is exactly 0.
+constexpr float kMaxTMin = 18446744073709551616.0f;
 constexpr int64_t kMaxGridX = 2147483647;
 constexpr int64_t kMinWideSlice = 2048;
 
@@ -44,6 +50,8 @@ struct DeviceInfo {
     int cc_minor = 0;
     int max_cluster = 1;
     unsigned int* err = nullptr;
+    unsigned int* err_taken = nullptr;
+    std::mutex take_mu;  // one cs_get_error at a time uses err_taken
 };
 
 DeviceInfo g_dev[kMaxDevices];
@@ -74,7 +82,9 @@ cs_status device_info(DeviceInfo** out) {
                 }
             }
             void* p = nullptr;
-            if (cudaGetSymbolAddress(&p, g_cs_error_word) != cudaSuccess) {
+            void* q = nullptr;
+            if (cudaGetSymbolAddress(&p, g_cs_error_word) != cudaSuccess ||
+                cudaGetSymbolAddress(&q, g_cs_error_taken) != cudaSuccess) {
                 cudaGetLastError();
                 return CS_ERR_CUDA;
             }
@@ -85,6 +95,7 @@ cs_status device_info(DeviceInfo** out) {
             d.cc_minor = v[4];
             d.max_cluster = v[3] >= 9 ? cs::kMaxCluster : 1;
             d.err = static_cast<unsigned int*>(p);
+            d.err_taken = static_cast<unsigned int*>(q);
             d.ready.store(true, std::memory_order_release);
         }
     }
@@ -331,7 +342,7 @@ cs_status plan_attention(int32_t batch, int32_t heads, int32_t S,
                          int32_t aligned, const cs_options& o, int sm_count,
                          int smem_optin, int smem_per_sm, cs_plan* p) {
     (void)sm_count;
-    if (o.strict != 0) return CS_ERR_INVALID_ARG;
+    if (o.strict != 0 || o.evals_out) return CS_ERR_INVALID_ARG;
     const int64_t rows = static_cast<int64_t>(batch) * heads * S;
     // Float4s a row spans: exact for aligned rows, else at the worst
     // alignment of a row start.
@@ -414,7 +425,7 @@ cs_status cs_check_args(const float* logits, const float* out, int64_t batch,
     if (num_classes > CS_MAX_NUM_CLASSES) return CS_ERR_OOM;
     if (batch > INT64_MAX / 4 / num_classes) return CS_ERR_DIM_MISMATCH;
     if (isnan(entropy_bound)) return CS_ERR_INVALID_ARG;
-    if (!(t_min >= FLT_MIN) || isinf(t_min)) return CS_ERR_INVALID_ARG;
+    if (!(t_min >= FLT_MIN) || !(t_min <= kMaxTMin)) return CS_ERR_INVALID_ARG;
     if (isnan(t_max) || t_max < t_min) return CS_ERR_INVALID_ARG;
     if (max_iter < 0 || max_iter > kMaxIter) return CS_ERR_INVALID_ARG;
     if (batch == 0) return CS_OK;
@@ -475,6 +486,14 @@ cs_status cs_constrained_softmax_ex(const float* logits, float* out,
                                  entropy_bound, t_min, t_max, max_iter, t_out);
     if (st != CS_OK) return st;
     if (batch == 0) return CS_OK;
+    if (options && options->evals_out) {
+        const int64_t bytes = batch * num_classes * 4;
+        const void* e = options->evals_out;
+        if (ranges_overlap(e, batch * 4, logits, bytes) ||
+            ranges_overlap(e, batch * 4, out, bytes) ||
+            (t_out && ranges_overlap(e, batch * 4, t_out, batch * 4)))
+            return CS_ERR_INVALID_ARG;
+    }
     DeviceInfo* d = nullptr;
     st = device_info(&d);
     if (st != CS_OK) return st;
@@ -499,6 +518,7 @@ cs_status cs_constrained_softmax_ex(const float* logits, float* out,
     // threshold as the per-thread work rule of the thread count).
     task.async_stage = p.grid_ctas * 4 > static_cast<int64_t>(d->sm_count) * 5;
     task.wait_limit_cycles = cs::kWaitLimitCycles;
+    task.evals_out = options ? options->evals_out : nullptr;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
@@ -531,9 +551,12 @@ cs_status cs_get_error(int32_t* code_mask, void* stream) {
     if (st != CS_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     unsigned int h = 0;
-    if (cudaMemcpyAsync(&h, d->err, sizeof(h), cudaMemcpyDeviceToHost, s) !=
-            cudaSuccess ||
-        cudaMemsetAsync(d->err, 0, sizeof(h), s) != cudaSuccess ||
+    // Read and clear in one atomic exchange on the device, so that a bit a
+    // launch on another stream sets at the same time is never dropped.
+    std::lock_guard<std::mutex> lock(d->take_mu);
+    if (cs::launch_take_error(d->err, d->err_taken, s) != cudaSuccess ||
+        cudaMemcpyAsync(&h, d->err_taken, sizeof(h), cudaMemcpyDeviceToHost,
+                        s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess) {
         cudaGetLastError();
         return CS_ERR_CUDA;
@@ -572,7 +595,7 @@ cs_status cs_plan_backward_host(int64_t batch, int32_t num_classes,
         return CS_ERR_INVALID_ARG;
     if (max_cluster > cs::kMaxCluster) max_cluster = cs::kMaxCluster;
     cs_options o = options ? *options : cs_options{};
-    if (o.strict != 0) return CS_ERR_INVALID_ARG;
+    if (o.strict != 0 || o.evals_out) return CS_ERR_INVALID_ARG;
     if (o.variant == CS_VARIANT_AUTO) {
         if (o.param != 0 || o.threads != 0) return CS_ERR_INVALID_ARG;
         o.variant = num_classes <= kAutoRowgroupMaxClasses ? CS_VARIANT_ROWGROUP
@@ -814,7 +837,7 @@ cs_status cs_plan_biencoder_host(int32_t batch_size, int32_t query_len,
         return CS_ERR_OOM;
     if (d_head % 4 != 0) return CS_ERR_INVALID_ARG;
     const cs_options o = options ? *options : cs_options{};
-    if (o.threads != 0 || o.strict != 0) return CS_ERR_INVALID_ARG;
+    if (o.threads != 0 || o.strict != 0 || o.evals_out) return CS_ERR_INVALID_ARG;
     int G = 0;
     if (o.variant == CS_VARIANT_AUTO) {
         if (o.param != 0) return CS_ERR_INVALID_ARG;

@@ -13,9 +13,11 @@ namespace csd {
 
 constexpr float kLog2e = 1.44269504088896341f;
 constexpr float kLn2 = 0.693147180559945309f;
-// Floor for y = (l - max) * log2(e).  Any y below it contributes exactly 0
-// to every sum at the temperatures searched (T <= 1), and the floor keeps
-// 0 * y finite when l - max overflows to -inf.
+// Floor for y = (l - max) * log2(e).  The floor keeps 0 * y finite when
+// l - max overflows to -inf.  A floored y contributes exactly 0 to every sum
+// and output at every temperature the kernels use: those are at most
+// max(1, t_min), the argument check caps t_min at 2^64, so beta >= 2^-64
+// and beta * y <= -2^36, whose ex2 is +0 (and so is the exact term).
 constexpr float kYFloor = -1.2676506002282294e30f;  // -2^100
 
 // ---------------------------------------------------------------- math units

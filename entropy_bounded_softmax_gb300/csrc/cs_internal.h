@@ -37,6 +37,7 @@ struct RowTask {
     int32_t strict;        // 1: evaluate every bisection midpoint
     int32_t async_stage;   // cluster kernel: stage with asynchronous copies
     uint64_t wait_limit_cycles;
+    int32_t* evals_out;    // may be null: temperatures evaluated per row
 };
 
 // Cluster kernel geometry.
@@ -223,6 +224,8 @@ cudaError_t launch_probe_ex2(float* sink, int iters, int blocks, int threads,
                              cudaStream_t stream);
 cudaError_t launch_wait_timeout(unsigned int* err, uint64_t limit_cycles,
                                 cudaStream_t stream);
+cudaError_t launch_take_error(unsigned int* err, unsigned int* taken,
+                              cudaStream_t stream);
 
 // cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per device and
 // kernel, raised only when a launch needs more than was set before.

@@ -93,6 +93,7 @@ struct RowSolution {
     float beta_out;   // 1/T of the output
     float inv_s;      // 1/S at that temperature
     unsigned int bits;
+    int evals;        // temperatures evaluated (T = 1 and the search)
     bool zero;        // NaN/Inf row: output zeros
 };
 
@@ -123,6 +124,7 @@ __device__ __forceinline__ RowSolution solve_row(float4 (&y)[E4], float m,
     const int row_code = static_cast<int>(mc.y);
 
     unsigned int bits = 0;
+    int evals = 0;
     float T_row = NAN;
     float beta_out = 0.0f, inv_s = 0.0f;
     if (row_code != 0) {
@@ -136,6 +138,7 @@ __device__ __forceinline__ RowSolution solve_row(float4 (&y)[E4], float m,
             y[i].w = fmaxf((y[i].w - m) * kLog2e, kYFloor);
         }
         const float3 r1 = group_sum3<G>(reg_pass3<E4>(y, 1.0f), gmask);
+        evals = 1;
         float2 sv = make_float2(r1.x, r1.y);
         if (!entropy_above(sv, 1.0f, bound_bits)) {
             T_row = 1.0f;
@@ -143,11 +146,13 @@ __device__ __forceinline__ RowSolution solve_row(float4 (&y)[E4], float m,
             inv_s = 1.0f / sv.x;
         } else {
             bool over = false;
+            int n_search = 0;
             narrow_search(
                 cfg, r1.x, r1.y, r1.z, strict,
                 [&](float b) { return group_sum3<G>(reg_pass3<E4>(y, b), gmask); },
                 [&](float b) { return group_sum2<G>(reg_pass<E4>(y, b), gmask); },
-                T_row, beta_out, inv_s, over);
+                T_row, beta_out, inv_s, over, n_search);
+            evals += n_search;
             if (over) bits |= kBitOverflow;
         }
     }
@@ -156,6 +161,7 @@ __device__ __forceinline__ RowSolution solve_row(float4 (&y)[E4], float m,
     r.beta_out = beta_out;
     r.inv_s = inv_s;
     r.bits = bits;
+    r.evals = evals;
     r.zero = row_code != 0;
     return r;
 }

@@ -390,15 +390,17 @@ constexpr int kNarrowNewtonRounds = 5;
 // at or below (t_min when the step comes within 4 t_min of it), then, only
 // while the bracket is open, points stepping from the end moved last with
 // doubling strides.  One lg2 and one reciprocal of S serve both the
-// decision and the next step.  Returns T, 1/T, 1/S(T) and the section 5.4
-// flag.
+// decision and the next step.  Returns T, 1/T, 1/S(T), the section 5.4
+// flag and the number of evaluations made.
 template <class Eval3, class Eval2>
 __device__ __forceinline__ void narrow_search(const SearchCfg& cfg, float S1,
                                               float V1, float W1, bool strict,
                                               Eval3 eval3, Eval2 eval2,
                                               float& T_out, float& beta_out,
-                                              float& inv_s, bool& overflow) {
+                                              float& inv_s, bool& overflow,
+                                              int& evals) {
     const Grid& g = cfg.g;
+    evals = 0;
     int jl = 0, jh = g.top;
     bool jl_eval = false;   // G(jl) evaluated feasible
     bool tmin_inf = false;  // t_min evaluated infeasible
@@ -408,6 +410,7 @@ __device__ __forceinline__ void narrow_search(const SearchCfg& cfg, float S1,
             const int jm = jl + ((jh - jl) >> 1);
             const float b = rcp_approx(g.at(jm));
             const float2 sv = eval2(b);
+            ++evals;
             if (entropy_above(sv, b, cfg.bound_bits)) {
                 jh = jm;
             } else {
@@ -441,6 +444,7 @@ __device__ __forceinline__ void narrow_search(const SearchCfg& cfg, float S1,
             jn = probe ? 0 : min(max(jn, jl + 1), jh - 1);
             b = rcp_approx(probe ? cfg.t_min : g.at(jn));
             const float3 r = eval3(b);
+            ++evals;
             S = r.x;
             V = r.y;
             W = r.z;
@@ -473,6 +477,7 @@ __device__ __forceinline__ void narrow_search(const SearchCfg& cfg, float S1,
             jlast = jm;
             const float bm = rcp_approx(g.at(jm));
             const float2 sv = eval2(bm);
+            ++evals;
             if (entropy_above(sv, bm, cfg.bound_bits)) {
                 jh = jm;
             } else {
@@ -488,6 +493,7 @@ __device__ __forceinline__ void narrow_search(const SearchCfg& cfg, float S1,
     if (!tmin_inf && !jl_eval) {
         // lo is still t_min: evaluate it (section 5.4 check).
         const float2 sv = eval2(b_lo);
+        ++evals;
         s_lo = sv.x;
         overflow = entropy_above(sv, b_lo, cfg.bound_bits);
     }

@@ -1,7 +1,7 @@
 // Auxiliary kernels: the ex2 throughput probe that sets the roofline of the
-// constrained softmax (its hot loop is one ex2 per class per bisection step)
-// and the bounded-wait timeout exercise; plus the per-device cache of kernel
-// shared-memory attributes.
+// constrained softmax (its hot loop is one ex2 per class per bisection step),
+// the atomic read-and-clear of the error word and the bounded-wait timeout
+// exercise; plus the per-device cache of kernel shared-memory attributes.
 #include <atomic>
 #include <mutex>
 
@@ -44,9 +44,22 @@ __global__ void wait_timeout_kernel(unsigned int* err, uint64_t limit_cycles) {
     if (!ok && threadIdx.x == 0) raise_error(err, kBitTimeout);
 }
 
+// Reads and clears the error word in one atomic step, into the word the
+// host then copies back: a bit set by a launch on another stream lands
+// either in this read or in the word after it, never between the two.
+__global__ void take_error_kernel(unsigned int* err, unsigned int* taken) {
+    *taken = atomicExch(err, 0u);
+}
+
 }  // namespace
 
 int probe_chains() { return kProbeChains; }
+
+cudaError_t launch_take_error(unsigned int* err, unsigned int* taken,
+                              cudaStream_t stream) {
+    take_error_kernel<<<1, 1, 0, stream>>>(err, taken);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_probe_ex2(float* sink, int iters, int blocks, int threads,
                              cudaStream_t stream) {

@@ -680,6 +680,7 @@ cluster_kernel(RowTask t, int n, int slice_len) {
 
         float* dst = t.out + r * C + s0;
         unsigned int bits = 0;
+        int evals = 1;  // the T = 1 pass
         float T_row = NAN;
         float beta_out = 0.0f, inv_s = 0.0f;
         if (row_code == 0) {
@@ -696,11 +697,13 @@ cluster_kernel(RowTask t, int n, int slice_len) {
                     const float T1[kMaxPoints] = {cfg.t_min, 0.f, 0.f};
                     const int J1[kMaxPoints] = {0, 0, 0};
                     search_round<CLUSTER, 1, false>(st, cfg, T1, J1, row4, s.q4, d, sm, x);
+                    ++evals;
                 }
                 while (!st.done) {
                     float T[kMaxPoints];
                     int J[kMaxPoints];
                     const int np = search_plan(st, cfg, T, J);
+                    evals += np;
                     const bool w0 = newton_next(st);
                     if (np == 1 && w0)
                         search_round<CLUSTER, 1, true>(st, cfg, T, J, row4, s.q4, d, sm, x);
@@ -724,6 +727,7 @@ cluster_kernel(RowTask t, int n, int slice_len) {
         write_out(row4, s, dst, beta_out, d, inv_s, row_code != 0);
         if (rank == 0 && threadIdx.x == 0) {
             if (t.t_out) t.t_out[r] = T_row;
+            if (t.evals_out) t.evals_out[r] = evals + (row_code != 0 ? 0 : 1);
             raise_error(t.err, bits);
         }
         if (x.dead && !reported) {

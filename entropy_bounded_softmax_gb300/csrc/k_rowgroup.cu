@@ -123,6 +123,7 @@ rowgroup_kernel(RowTask t, int vec) {
         }
         if (sub == 0) {
             if (t.t_out) t.t_out[row] = T_row;
+            if (t.evals_out) t.evals_out[row] = sol.evals + (zero ? 0 : 1);
             raise_error(t.err, bits);
         }
     }

@@ -32,7 +32,8 @@
  * grid points are indexed by integers and evaluated in fp32.
  *
  * All functions are thread-safe.  No function allocates device memory per
- * call; the library's only device object is one 32-bit error word per GPU.
+ * call; the library's only device objects are two 32-bit words per GPU (the
+ * error word and the word cs_get_error reads it through).
  */
 #ifndef ENTROPY_BOUNDED_SOFTMAX_H
 #define ENTROPY_BOUNDED_SOFTMAX_H
@@ -85,6 +86,16 @@ typedef struct cs_options {
                           monotone H, fewer passes: up to 3 points per
                           round in the cluster kernel, one in the
                           row-group kernel)                                 */
+    int32_t* evals_out; /* cs_constrained_softmax_ex only; optional device
+                          pointer, [batch] int32: how many temperatures each
+                          row's exponentials were evaluated at, i.e. the ex2
+                          per class the row cost (the T = 1 pass, every
+                          point of every search round, and the output pass;
+                          0 for a NaN/Inf row in the row-group kernel, 1 in
+                          the cluster kernel, whose T = 1 pass runs before
+                          the row's code is known).  NULL: not recorded.
+                          Must not overlap logits, out or t_out.  The other
+                          operations reject a non-NULL value.            */
 } cs_options;
 
 /* What a launch of the given shape uses.  Filled by cs_plan_launch /
@@ -121,7 +132,10 @@ typedef struct cs_plan {
  * entropy_bound  bound on H in nats (page default 0.20).  Any non-NaN value;
  *          a negative bound is unsatisfiable, +inf disables the search.
  * t_min, t_max  search interval (page defaults 0.01 and 10.0).  t_min must
- *          be a finite normal float > 0 and t_max >= t_min (t_max may be +inf).
+ *          be a normal float in (0, 2^64] and t_max >= t_min (t_max may be
+ *          +inf).  (The cap keeps every temperature used at or below 2^64,
+ *          where logits that lie more than about 8.8e29 below the row's
+ *          maximum contribute exactly 0, as they do in exact arithmetic.)
  * max_iter bisection steps, 0..1024 (page default 20).
  * t_out    optional device pointer, [batch] fp32: the temperature each row
  *          used (1 when no search was needed, lo after a search, t_min when
@@ -159,14 +173,17 @@ cs_status cs_constrained_softmax_ex(const float* logits, float* out,
                                     void* stream);
 
 /*
- * Reads and clears the calling thread's current device's error word after
- * synchronising `stream`.  *code_mask receives a bitmask of (1 << code) for
+ * Reads and clears the calling thread's current device's error word, then
+ * synchronises `stream`.  *code_mask receives a bitmask of (1 << code) for
  * every asynchronous condition since the last call: CS_ERR_NAN_INPUT,
- * CS_ERR_INF_INPUT, CS_ERR_ENTROPY_OVERFLOW, CS_ERR_TIMEOUT.  The word is
- * shared by every launch on the device, so launches on other streams that
- * run concurrently may be counted or cleared by this call.  This is the only
- * function that synchronises.  Returns CS_ERR_INVALID_ARG for a NULL
- * code_mask, CS_ERR_CUDA when a CUDA call fails.
+ * CS_ERR_INF_INPUT, CS_ERR_ENTROPY_OVERFLOW, CS_ERR_TIMEOUT.  The read and
+ * the clear are one atomic exchange, made by a one-thread kernel on `stream`
+ * after the work enqueued on it before this call.  The word is shared by
+ * every launch on the device: a launch on another stream that runs
+ * concurrently reports its bits either to this call or to the next one,
+ * never to neither.  Calls from several host threads are serialised.  This is
+ * the only function that synchronises.  Returns CS_ERR_INVALID_ARG for a
+ * NULL code_mask, CS_ERR_CUDA when a CUDA call fails.
  */
 cs_status cs_get_error(int32_t* code_mask, void* stream);
 

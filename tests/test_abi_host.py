@@ -78,6 +78,8 @@ A, B = 1 << 20, 1 << 30   # two far-apart fake device addresses
     ((A, B, 4, 10, 0.2, 0.0, 10.0, 20, None), 8),
     ((A, B, 4, 10, 0.2, 1e-45, 10.0, 20, None), 8),         # subnormal
     ((A, B, 4, 10, 0.2, float("inf"), float("inf"), 20, None), 8),
+    ((A, B, 4, 10, 0.2, 2.0**64, float("inf"), 20, None), 0),  # the cap
+    ((A, B, 4, 10, 0.2, 2.0**65, float("inf"), 20, None), 8),  # above it
     ((A, B, 4, 10, 0.2, 0.01, 0.001, 20, None), 8),
     ((A, B, 4, 10, 0.2, 0.01, float("nan"), 20, None), 8),
     ((A, B, 4, 10, 0.2, 0.01, float("inf"), 20, None), 0),
@@ -418,4 +420,18 @@ def test_biencoder_plans():
     st, _ = cs.cs_plan_biencoder_host(1, 10, 40, 16, 1,
                                       cs.options(C["CS_VARIANT_CLUSTER"], 1),
                                       232448)
+    assert st == C["CS_ERR_INVALID_ARG"]
+
+
+def test_evaluation_counts_only_for_the_forward():
+    """cs_options.evals_out is an output of cs_constrained_softmax_ex; the
+    planners of the other operations reject it."""
+    opt = cs.options(0, 0, 0, 0, A)
+    st, _ = cs.cs_plan_host(4, 1000, opt, *GB300.values())
+    assert st == 0
+    st, _ = cs.cs_plan_backward_host(4, 1000, opt, *GB300.values())
+    assert st == C["CS_ERR_INVALID_ARG"]
+    st, _ = cs.cs_plan_attention_host(1, 1, 64, 1, opt, 152, 232448, 233472)
+    assert st == C["CS_ERR_INVALID_ARG"]
+    st, _ = cs.cs_plan_biencoder_host(1, 8, 64, 64, 1, opt, 232448)
     assert st == C["CS_ERR_INVALID_ARG"]
