@@ -43,14 +43,14 @@ struct RowTask {
 // Cluster kernel geometry.
 constexpr int kMaxCluster = 16;
 constexpr int kClusterMaxThreads = 512;
-constexpr int kSlotVals = 12;         // floats per exchange slot
+constexpr int kSlotVals = 8;          // floats per exchange slot
 
 // Byte offsets of the cluster kernel's dynamic shared memory for `warps`
-// warps and cluster size n: cluster slots [2][n][kSlotVals] floats, per-warp
-// slots [2][warps][kSlotVals], a broadcast slot, the two cluster mbarriers
-// and the load mbarriers; then (128-byte aligned) the slice.
+// warps and cluster size n: the exchange slots [2][n * warps][kSlotVals]
+// floats (one per warp of the cluster, double-buffered), the two exchange
+// mbarriers, then (128-byte aligned) the slice.
 struct ClusterSmemLayout {
-    int cslot, wslot, bcast, cbar, row;
+    int cslot, cbar, row;
 };
 
 __host__ __device__ inline ClusterSmemLayout cluster_smem_layout(int warps,
@@ -58,11 +58,7 @@ __host__ __device__ inline ClusterSmemLayout cluster_smem_layout(int warps,
     ClusterSmemLayout L;
     int p = 0;
     L.cslot = p;
-    p += 2 * n * kSlotVals * 4;
-    L.wslot = p;
-    p += 2 * warps * kSlotVals * 4;
-    L.bcast = p;
-    p += kSlotVals * 4;
+    p += 2 * n * warps * kSlotVals * 4;
     p = ((p + 7) / 8) * 8;
     L.cbar = p;
     p += 2 * 8;

@@ -105,27 +105,28 @@ struct SearchCfg {
     Grid g;
 };
 
-// Per-row search state; identical in every thread that plans for the row.
+// Per-row state of the bracket search (the cluster kernel); identical in
+// every thread that plans for the row.  Kept small: every thread of the
+// cluster holds it in registers through the whole search.
 struct Search {
     int jl, jh;         // bracket of grid indices
-    bool jl_eval;       // G(jl) was evaluated feasible (else jl = 0, unseen)
-    bool tmin_inf;      // t_min was evaluated infeasible (section 5.4)
-    bool final_round;   // this round evaluates t_min for the result
-    bool done;
-    bool strict;        // halve the bracket one evaluation per round
-    bool endgame;       // Newton has converged: quarter the bracket
-    bool single;        // one point per round
-    int jlast;          // single: the index evaluated last
-    int stride;         // the next galloping step
     int jl_prev, jh_prev;  // the bracket when the last round was planned
-    float SA;           // S at G(jl) when jl_eval
-    float S_tmin;       // S at t_min when tmin_inf
-    float b_jl, b_jh;   // beta of the bracket's ends (t_min while !jl_eval)
-    float bc, Hc, dHc;  // Newton anchor: beta, H (nats), dH/dbeta
+    int stride;         // the next galloping step
     int rounds;
-    float T_out, S_out;
-    bool overflow;      // section 5.4: even t_min violates the bound
+    uint32_t f;         // kJlEval | kTminInf | ... below
+    float SA;           // S at G(jl) when jl was evaluated; S at t_min when
+                        // t_min was found infeasible or in the final round
+    float b_jl, b_jh;   // beta of the bracket's ends (t_min while unevaluated)
+    float bc, Hc, dHc;  // Newton anchor: beta, H (nats), dH/dbeta
 };
+
+constexpr uint32_t kJlEval = 1u;     // G(jl) was evaluated feasible
+constexpr uint32_t kTminInf = 2u;    // t_min was evaluated infeasible (5.4)
+constexpr uint32_t kFinal = 4u;      // this round evaluates t_min for the result
+constexpr uint32_t kDone = 8u;
+constexpr uint32_t kStrict = 16u;    // halve the bracket one point per round
+constexpr uint32_t kEndgame = 32u;   // Newton has converged
+constexpr uint32_t kOverflow = 64u;  // section 5.4: even t_min violates the bound
 
 // H (nats) and dH/dbeta at beta from the sums, given ls = log2 S and
 // is = 1 / S.
@@ -144,89 +145,66 @@ __device__ __forceinline__ float entropy_slope(float is, float V, float W,
 // H(1) > bound.
 __device__ __forceinline__ Search search_begin(const SearchCfg& c, float S1,
                                                float V1, float W1,
-                                               bool strict, bool single) {
+                                               bool strict) {
     Search s;
     s.jl = 0;
     s.jh = c.g.top;
-    s.jl_eval = false;
-    s.tmin_inf = false;
-    s.final_round = false;
-    s.done = false;
-    s.strict = strict;
-    s.endgame = false;
-    s.single = single;
-    s.jlast = -1;
-    s.stride = 1;
     s.jl_prev = s.jl;
     s.jh_prev = s.jh;
+    s.stride = 1;
+    s.rounds = 0;
+    s.f = strict ? kStrict : 0u;
     s.SA = 0.0f;
-    s.S_tmin = 0.0f;
     s.b_jl = rcp_approx(c.t_min);
     s.b_jh = rcp_approx(c.hi0);
     const float is = rcp_approx(S1);
     s.bc = 1.0f;
     s.Hc = entropy_nats(lg2_approx(S1), is, V1, 1.0f);
     s.dHc = entropy_slope(is, V1, W1, 1.0f);
-    s.rounds = 0;
-    s.T_out = 0.0f;
-    s.S_out = 0.0f;
-    s.overflow = false;
     return s;
 }
 
-// Chooses the grid points of the next round (indices J, temperatures T);
-// returns how many (0: done, with T_out, S_out and overflow set).
+// Appends grid index v to the round's points (constant register indices,
+// no local memory).
+__device__ __forceinline__ void put_point(int (&J)[kMaxPoints], int& np,
+                                          int v) {
+    if (np == 0) J[0] = v;
+    else if (np == 1) J[1] = v;
+    else J[2] = v;
+    ++np;
+}
+
+// Chooses the grid points of the next round (indices J); returns how many
+// (0: done; the result is then search_result()).
 __device__ __forceinline__ int search_plan(Search& s, const SearchCfg& c,
-                                           float (&T)[kMaxPoints],
                                            int (&J)[kMaxPoints]) {
     const Grid& g = c.g;
-    if (s.tmin_inf) {
+    if (s.f & kTminInf) {
         // Every grid point is infeasible: lo never moves (section 5.4).
-        s.T_out = g.lo0;
-        s.S_out = s.S_tmin;
-        s.overflow = true;
-        s.done = true;
+        s.f |= kOverflow | kDone;
         return 0;
     }
     if (s.jh - s.jl <= 1) {
-        s.T_out = g.at(s.jl);
-        if (s.jl_eval) {
-            s.S_out = s.SA;
-            s.done = true;
+        if (s.f & kJlEval) {
+            s.f |= kDone;
             return 0;
         }
         // lo stayed at t_min without an evaluation there: one more for its
         // S and the section 5.4 check.
-        s.final_round = true;
+        s.f |= kFinal;
         J[0] = 0;
-        T[0] = g.lo0;
         return 1;
     }
-    if (s.strict || s.rounds >= kMaxNewtonRounds) {
+    if ((s.f & kStrict) || s.rounds >= kMaxNewtonRounds) {
         J[0] = s.jl + ((s.jh - s.jl) >> 1);
-        T[0] = g.at(J[0]);
         return 1;
     }
-    if (s.endgame && s.single) {
-        // Step from the end the last evaluation moved towards the other,
-        // doubling the step, capped at half the bracket.
-        const int d = s.jh - s.jl;
-        const int step = max(min(s.stride, d >> 1), 1);
-        if (s.jl == s.jlast)
-            J[0] = s.jl + step;
-        else if (s.jh == s.jlast)
-            J[0] = s.jh - step;
-        else
-            J[0] = s.jl + (d >> 1);
-        s.stride *= 2;
-        s.jlast = J[0];
-        T[0] = g.at(J[0]);
-        return 1;
-    }
-    if (s.endgame) {
+    int np = 0;
+    if (s.f & kEndgame) {
         const bool lo_moved = s.jl != s.jl_prev, hi_moved = s.jh != s.jh_prev;
         s.jl_prev = s.jl;
         s.jh_prev = s.jh;
+        const int d = s.jh - s.jl;
         if (g.fine && lo_moved != hi_moved) {
             // Fine grid (every fp32 value a point, so a converged Newton
             // point is still many points off) and only one end moved last
@@ -236,35 +214,22 @@ __device__ __forceinline__ int search_plan(Search& s, const SearchCfg& c,
             // shorter than a stride, quarter it instead).  On the coarser
             // exact grid the converged round almost always closes the
             // bracket, and quartering measured as fast.
-            const int d = s.jh - s.jl;
             s.stride = max(s.stride, 2);
-            int np = 0;
 #pragma unroll
             for (int k = 0; k < kMaxPoints; ++k) {
                 const int off = s.stride << k;
-                if (off >= d) break;
-                J[np++] = lo_moved ? s.jl + off : s.jh - off;
+                if (off < d) put_point(J, np, lo_moved ? s.jl + off : s.jh - off);
             }
             if (s.stride < (1 << 26)) s.stride <<= 3;
-            if (np > 0) {
-#pragma unroll
-                for (int i = 0; i < kMaxPoints; ++i)
-                    if (i < np) T[i] = g.at(J[i]);
-                return np;
-            }
+            if (np > 0) return np;
         }
         // The bracket's midpoint and quarter points: two halvings per round.
-        const int d = s.jh - s.jl;
         const int m = s.jl + (d >> 1);
-        int np = 0;
-        J[np++] = m;
+        put_point(J, np, m);
         const int a = s.jl + (d >> 2);
         const int b = m + ((s.jh - m) >> 1);
-        if (a > s.jl && a < m) J[np++] = a;
-        if (b > m && b < s.jh) J[np++] = b;
-#pragma unroll
-        for (int i = 0; i < kMaxPoints; ++i)
-            if (i < np) T[i] = g.at(J[i]);
+        if (a > s.jl && a < m) put_point(J, np, a);
+        if (b > m && b < s.jh) put_point(J, np, b);
         return np;
     }
     // Safeguarded Newton for log H = log bound in beta (plain Newton on H
@@ -285,45 +250,33 @@ __device__ __forceinline__ int search_plan(Search& s, const SearchCfg& c,
     // The grid point at or just below Tn, strictly inside the bracket.
     int jn = Tn > g.lo0 ? g.near(Tn) : 0;
     jn = min(max(jn, s.jl + 1), s.jh - 1);
-    int np = 0;
     s.jl_prev = s.jl;
     s.jh_prev = s.jh;
-    const bool probe = !s.jl_eval && Tn <= 4.0f * g.lo0;  // t_min probe
-    if (s.single) {
-        J[0] = probe ? 0 : jn;
-        T[0] = g.at(J[0]);
-        s.jlast = J[0];
-        if (!probe && fabsf(bn - s.bc) <= 1e-3f * s.bc) s.endgame = true;
-        return 1;
-    }
-    J[np++] = jn;
-    if (probe) J[np++] = 0;
-    if (np == 1 && fabsf(bn - s.bc) <= 1e-3f * s.bc) {
+    const bool probe = !(s.f & kJlEval) && Tn <= 4.0f * g.lo0;  // t_min probe
+    put_point(J, np, jn);
+    if (probe) put_point(J, np, 0);
+    if (!probe && fabsf(bn - s.bc) <= 1e-3f * s.bc) {
         // Newton has converged: also evaluate the neighbours, which close
         // the bracket when the crossing lies next to jn.
-        if (jn + 1 < s.jh) J[np++] = jn + 1;
-        if (jn - 1 > s.jl) J[np++] = jn - 1;
-        s.endgame = true;
+        if (jn + 1 < s.jh) put_point(J, np, jn + 1);
+        if (jn - 1 > s.jl) put_point(J, np, jn - 1);
+        s.f |= kEndgame;
     }
-#pragma unroll
-    for (int i = 0; i < kMaxPoints; ++i)
-        if (i < np) T[i] = g.at(J[i]);
     return np;
 }
 
 // Whether the round just planned is followed by a Newton step, which needs
 // the slope (hence W) at the round's first point.
 __device__ __forceinline__ bool newton_next(const Search& s) {
-    return !s.final_round && !s.strict && !s.endgame &&
+    return !(s.f & (kFinal | kStrict | kEndgame)) &&
            s.rounds + 1 < kMaxNewtonRounds;
 }
 
-// Records the round's evaluations: grid point J[i] (temperature T[i], at
-// beta[i] = rcp_approx(T[i])) gave the row sums S[i], V[i], and, when
-// has_w, W[0].  Feasible points raise jl, then infeasible ones lower jh;
-// a point the bracket no longer contains is already decided and skipped,
-// so fp32 evaluations that disagree with monotonicity at the crossing
-// cannot invert the bracket.
+// Records the round's evaluations: grid point J[i] (at inverse temperature
+// beta[i]) gave the row sums S[i], V[i], and, when has_w, W[0].  Feasible
+// points raise jl, then infeasible ones lower jh; a point the bracket no
+// longer contains is already decided and skipped, so fp32 evaluations that
+// disagree with monotonicity at the crossing cannot invert the bracket.
 __device__ __forceinline__ void search_update(Search& s, const SearchCfg& c,
                                               int np,
                                               const int (&J)[kMaxPoints],
@@ -337,19 +290,18 @@ __device__ __forceinline__ void search_update(Search& s, const SearchCfg& c,
     for (int i = 0; i < kMaxPoints; ++i)
         inf[i] = i < np && entropy_above(make_float2(S[i], V[i]), beta[i],
                                          c.bound_bits);
-    if (s.final_round) {
-        s.S_out = S[0];
-        s.overflow = inf[0];
-        s.done = true;
+    if (s.f & kFinal) {
+        s.SA = S[0];
+        s.f |= kDone | (inf[0] ? kOverflow : 0u);
         return;
     }
 #pragma unroll
     for (int i = 0; i < kMaxPoints; ++i) {
         if (i >= np || inf[i]) continue;
-        const bool inside = J[i] > s.jl || (J[i] == 0 && !s.jl_eval);
+        const bool inside = J[i] > s.jl || (J[i] == 0 && !(s.f & kJlEval));
         if (inside && J[i] < s.jh) {
             s.jl = J[i];
-            s.jl_eval = true;
+            s.f |= kJlEval;
             s.SA = S[i];
             s.b_jl = beta[i];
         }
@@ -357,9 +309,9 @@ __device__ __forceinline__ void search_update(Search& s, const SearchCfg& c,
 #pragma unroll
     for (int i = 0; i < kMaxPoints; ++i) {
         if (i >= np || !inf[i]) continue;
-        if (J[i] == 0 && !s.jl_eval) {
-            s.tmin_inf = true;
-            s.S_tmin = S[i];
+        if (J[i] == 0 && !(s.f & kJlEval)) {
+            s.f |= kTminInf;
+            s.SA = S[i];
         } else if (J[i] > s.jl && J[i] < s.jh) {
             s.jh = J[i];
             s.b_jh = beta[i];
@@ -374,6 +326,13 @@ __device__ __forceinline__ void search_update(Search& s, const SearchCfg& c,
         s.dHc = entropy_slope(is, V[0], W[0], beta[0]);
     }
     ++s.rounds;
+}
+
+// The search's result once search_plan returned 0: the temperature, S there
+// and the section 5.4 flag.
+__device__ __forceinline__ float search_result_T(const Search& s,
+                                                 const SearchCfg& c) {
+    return (s.f & (kTminInf | kFinal)) ? c.g.lo0 : c.g.at(s.jl);
 }
 
 // Newton rounds every searching narrow row takes before the fallback.

@@ -25,20 +25,23 @@
 //   output  p_i = 2^(beta_lo y_i) / S(lo), written with 128-bit streaming
 //           stores.
 //
-// Reduction.  Every warp reduces its partial sums with a shuffle tree and
-// writes them to a slot; after a __syncthreads warp 0 reduces the per-warp
-// slots with a second shuffle tree.  In a cluster, warp 0 then pushes the
-// CTA's sums into every CTA (st.async, counted on an mbarrier), waits for
-// the cluster's pushes and adds them in rank order.  Warp 0 broadcasts the
-// result through shared memory after a second __syncthreads.  All threads of
-// the cluster thus see bit-identical sums and take the same decisions.
-// Slots are double-buffered, which is safe because no thread can reach
-// exchange k+2 before every thread has left exchange k.
+// Reduction.  Every warp reduces its partial sums with a shuffle tree, then
+// pushes them into its own slot of every CTA of the cluster (st.async,
+// counted on that CTA's mbarrier; in a launch without clusters, a plain
+// store and an arrival).  Every warp waits for the mbarrier and reduces all
+// n x warps slots in one fixed order (each lane folds slots lane, lane + 32,
+// ..., then a butterfly), so every thread of the cluster holds bit-identical
+// sums and takes the same decisions, with no CTA-wide barrier in the
+// search.  Slots and mbarriers are double-buffered, which is safe because
+// no warp can push for exchange k+2 before every warp of the cluster has
+// pushed for exchange k+1, which each does only after reading exchange k.
 //
 // Every wait is bounded (cs::kWaitLimitCycles by default).  A thread whose
-// wait times out records CS_ERR_TIMEOUT and from then on neither waits,
-// pushes nor issues copies, but keeps the kernel's control flow so that all
-// threads still meet at every __syncthreads and cluster barrier.
+// wait times out records CS_ERR_TIMEOUT and from then on neither waits nor
+// pushes; the search then ends within its round limit on whatever the slots
+// hold, and before the kernel's final cluster barrier such a CTA sleeps for
+// a bounded while, so that pushes peers had already issued into it land
+// before it exits.
 #include <math.h>
 
 #include "cs_search.cuh"
@@ -85,10 +88,8 @@ __device__ __forceinline__ Slice make_slice(const float* src, int len) {
 
 // Shared-memory objects of one CTA (cs::cluster_smem_layout places them).
 struct Smem {
-    float* cslot;     // [2][n][kSlotVals] cluster slots (double-buffered)
-    float* wslot;     // [2][warps][kSlotVals] per-warp slots (double-buffered)
-    float* bcast;     // [kSlotVals] broadcast of reduced sums
-    uint64_t* cbar;   // [2] cluster-exchange mbarriers
+    float* cslot;     // [2][n * warps][kSlotVals] exchange slots
+    uint64_t* cbar;   // [2] exchange mbarriers
     float4* row4;     // the slice
 };
 
@@ -97,8 +98,7 @@ struct Exch {
     int warps;
     int n;
     uint32_t rank;
-    uint32_t lk;      // exchanges so far (per-warp slot buffer)
-    uint32_t xk;      // cluster exchanges so far (cluster slot buffer, phase)
+    uint32_t xk;      // exchanges so far (slot buffer, mbarrier phase)
     uint64_t limit;
     bool dead;
 };
@@ -170,93 +170,60 @@ __device__ __forceinline__ void warp_reduce(float (&a)[NV]) {
     }
 }
 
-// Cluster leg: warp 0 pushes the CTA's sums a[0..NV) into slot `rank` of
-// every CTA; the waiting threads wait for the cluster's pushes and replace
-// a with the combination over ranks, in rank order.  Every thread of the
-// CTA calls it (keeping the exchange count); only waiters wait and combine.
-template <class Op, int NV>
-__device__ __forceinline__ void cluster_leg(float (&a)[NV], const Smem& sm,
-                                            Exch& x, bool waiter) {
-    constexpr int NE = NV + (NV & 1);   // pushed as pairs
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const uint32_t buf = x.xk & 1u;
-    const uint32_t parity = (x.xk >> 1) & 1u;
-    ++x.xk;
-    float* cs = sm.cslot + buf * x.n * kSlotVals;
-    if (!x.dead) {
-        if (threadIdx.x == 0) mbar_arrive_expect_tx(&sm.cbar[buf], x.n * NE * 4);
-        if (warp == 0 && lane < x.n) {
-            const uint32_t bar = map_to_rank(smem_addr(&sm.cbar[buf]), lane);
-#pragma unroll
-            for (int i = 0; i < NE; i += 2) {
-                const uint32_t dst = map_to_rank(
-                    smem_addr(&cs[x.rank * kSlotVals + i]), lane);
-                const float hi_half = (i + 1 < NV) ? a[(i + 1 < NV) ? i + 1 : 0] : 0.0f;
-                push_pair(dst, a[i], hi_half, bar);
-            }
-        }
-        if (waiter && !mbar_wait<true>(&sm.cbar[buf], parity, x.limit))
-            x.dead = true;
-    }
-    if (waiter) {
-#pragma unroll
-        for (int i = 0; i < NV; ++i) a[i] = cs[i];
-        for (int r = 1; r < x.n; ++r) {
-            float b[NV];
-#pragma unroll
-            for (int i = 0; i < NV; ++i) b[i] = cs[r * kSlotVals + i];
-            Op::combine(a, b);
-        }
-    }
-}
-
 // Reduction (Op) over every thread of the CTA and the cluster of each
 // thread's a[0..NV); returns the same bits in every thread of the cluster.
 template <bool CLUSTER, class Op, int NV>
 __device__ __forceinline__ void exchange(float (&a)[NV], const Smem& sm,
                                          Exch& x) {
     static_assert(NV <= kSlotVals, "payload");
+    constexpr int NE = NV + (NV & 1);   // pushed as pairs
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     warp_reduce<Op, NV>(a);
-    float* ws = sm.wslot + (x.lk & 1u) * x.warps * kSlotVals;
-    ++x.lk;
-    if (lane == 0) {
+    const uint32_t buf = x.xk & 1u;
+    const uint32_t parity = (x.xk >> 1) & 1u;
+    ++x.xk;
+    const int nslot = x.n * x.warps;
+    float* cs = sm.cslot + buf * nslot * kSlotVals;
+    const int mine = static_cast<int>(x.rank) * x.warps + warp;
+    if (!x.dead) {
+        if (CLUSTER) {
+            if (threadIdx.x == 0)
+                mbar_arrive_expect_tx(&sm.cbar[buf], nslot * NE * 4);
+            if (lane < x.n) {
+                const uint32_t bar = map_to_rank(smem_addr(&sm.cbar[buf]), lane);
+                const uint32_t dst = map_to_rank(smem_addr(&cs[mine * kSlotVals]), lane);
 #pragma unroll
-        for (int i = 0; i < NV; ++i) ws[warp * kSlotVals + i] = a[i];
-    }
-    __syncthreads();
-    // Warp 0 reduces the per-warp slots (and exchanges across the cluster),
-    // then broadcasts.  (Letting every warp reduce the slots and wait on the
-    // cluster barrier saves one CTA barrier but measured slower: the extra
-    // reductions and waiters cost more than the barrier.)
-    if (warp == 0) {
-        // Lane groups of w2 >= warps lanes (a power of two) each hold every
-        // warp's slot and reduce it with a log2(w2)-level shuffle tree.
-        const int w2 = x.warps <= 4 ? 4 : (x.warps <= 8 ? 8 : 16);
-        const int sl = lane & (w2 - 1);
-        if (sl < x.warps) {
+                for (int i = 0; i < NE; i += 2) {
+                    const float hi_half = (i + 1 < NV) ? a[(i + 1 < NV) ? i + 1 : 0] : 0.0f;
+                    push_pair(dst + 4 * i, a[i], hi_half, bar);
+                }
+            }
+        } else if (lane == 0) {
 #pragma unroll
-            for (int i = 0; i < NV; ++i) a[i] = ws[sl * kSlotVals + i];
-        } else {
-            Op::identity(a);
+            for (int i = 0; i < NV; ++i) cs[mine * kSlotVals + i] = a[i];
+            mbar_arrive(&sm.cbar[buf]);
         }
-        for (int o = w2 >> 1; o > 0; o >>= 1) {
-            float b[NV];
-#pragma unroll
-            for (int i = 0; i < NV; ++i) b[i] = __shfl_xor_sync(0xffffffffu, a[i], o);
-            Op::combine(a, b);
+        if (!mbar_wait<CLUSTER>(&sm.cbar[buf], parity, x.limit)) x.dead = true;
+    }
+    Op::identity(a);
+    for (int k = lane; k < nslot; k += 32) {
+        // A slot is kSlotVals = 8 floats, 32-byte aligned: two 128-bit loads
+        // at most.
+        float v[8];
+        const float4* s4 = reinterpret_cast<const float4*>(&cs[k * kSlotVals]);
+        const float4 v0 = s4[0];
+        v[0] = v0.x; v[1] = v0.y; v[2] = v0.z; v[3] = v0.w;
+        if (NV > 4) {
+            const float4 v1 = s4[1];
+            v[4] = v1.x; v[5] = v1.y; v[6] = v1.z; v[7] = v1.w;
         }
-    }
-    if (CLUSTER) cluster_leg<Op, NV>(a, sm, x, warp == 0);
-    if (warp == 0 && lane == 0) {
+        float b[NV];
 #pragma unroll
-        for (int i = 0; i < NV; ++i) sm.bcast[i] = a[i];
+        for (int i = 0; i < NV; ++i) b[i] = v[i];
+        Op::combine(a, b);
     }
-    __syncthreads();
-#pragma unroll
-    for (int i = 0; i < NV; ++i) a[i] = sm.bcast[i];
+    warp_reduce<Op, NV>(a);
 }
 
 // Accumulators of S, V and (optionally) W at one inverse temperature: lanes
@@ -435,18 +402,18 @@ __device__ __forceinline__ void eval_pass(const float4* row4, int q4,
     }
 }
 
-// One search round with P temperatures: pass, exchange, update.  W0: the
+// One search round with P grid points J: pass, exchange, update.  W0: the
 // next round takes a Newton step from point 0, which needs its W.  d: this
 // thread's offset (its max's y relative to the row's).
 template <bool CLUSTER, int P, bool W0>
 __device__ __forceinline__ void search_round(Search& st, const SearchCfg& cfg,
-                                             const float (&T)[kMaxPoints],
                                              const int (&J)[kMaxPoints],
                                              const float4* row4, int q4,
                                              float d, const Smem& sm, Exch& x) {
     float beta[kMaxPoints];
 #pragma unroll
-    for (int p = 0; p < kMaxPoints; ++p) beta[p] = p < P ? rcp_approx(T[p]) : 1.0f;
+    for (int p = 0; p < kMaxPoints; ++p)
+        beta[p] = p < P ? rcp_approx(cfg.g.at(J[p])) : 1.0f;
     constexpr int NV = PassOut<P, W0>::kN;
     float a[NV];
     eval_pass<P, W0>(row4, q4, beta, d, a);
@@ -548,16 +515,18 @@ cluster_kernel(RowTask t, int n, int slice_len) {
     {
         const ClusterSmemLayout L = cluster_smem_layout(warps, n);
         sm.cslot = reinterpret_cast<float*>(smem + L.cslot);
-        sm.wslot = reinterpret_cast<float*>(smem + L.wslot);
-        sm.bcast = reinterpret_cast<float*>(smem + L.bcast);
         sm.cbar = reinterpret_cast<uint64_t*>(smem + L.cbar);
         sm.row4 = reinterpret_cast<float4*>(smem + L.row);
     }
     float4* row4 = sm.row4;
 
     if (threadIdx.x == 0) {
-        mbar_init(&sm.cbar[0], 1u);
-        mbar_init(&sm.cbar[1], 1u);
+        // In a cluster each phase completes on one arrival (with the
+        // expected bytes of the cluster's pushes); without one, on one
+        // arrival per warp.
+        const uint32_t count = CLUSTER ? 1u : static_cast<uint32_t>(warps);
+        mbar_init(&sm.cbar[0], count);
+        mbar_init(&sm.cbar[1], count);
         fence_mbar_init();
     }
     __syncthreads();
@@ -571,7 +540,7 @@ cluster_kernel(RowTask t, int n, int slice_len) {
                         t.entropy_bound * kLog2e,
                         t.entropy_bound > 0.0f ? lg2_approx(t.entropy_bound) : 0.0f,
                         make_grid(t.t_min, fmaxf(t.hi0, t.t_min), t.max_iter)};
-    Exch x{warps, n, rank, 0u, 0u, t.wait_limit_cycles, false};
+    Exch x{warps, n, rank, 0u, t.wait_limit_cycles, false};
     bool reported = false;
 
     for (int64_t r = cid; r < t.batch; r += ncl) {
@@ -689,37 +658,34 @@ cluster_kernel(RowTask t, int n, int slice_len) {
                 beta_out = 1.0f;
                 inv_s = 1.0f / s1[1];
             } else {
-                Search st = search_begin(cfg, s1[1], s1[2], s1[3], t.strict != 0, false);
+                Search st = search_begin(cfg, s1[1], s1[2], s1[3], t.strict != 0);
                 if (!(cfg.t_min < cfg.hi0)) {
                     // No interval to halve: T = t_min (section 5.4 check).
-                    st.final_round = true;
-                    st.T_out = cfg.t_min;
-                    const float T1[kMaxPoints] = {cfg.t_min, 0.f, 0.f};
+                    st.f |= kFinal;
                     const int J1[kMaxPoints] = {0, 0, 0};
-                    search_round<CLUSTER, 1, false>(st, cfg, T1, J1, row4, s.q4, d, sm, x);
+                    search_round<CLUSTER, 1, false>(st, cfg, J1, row4, s.q4, d, sm, x);
                     ++evals;
                 }
-                while (!st.done) {
-                    float T[kMaxPoints];
-                    int J[kMaxPoints];
-                    const int np = search_plan(st, cfg, T, J);
+                while (!(st.f & kDone)) {
+                    int J[kMaxPoints] = {0, 0, 0};
+                    const int np = search_plan(st, cfg, J);
                     evals += np;
                     const bool w0 = newton_next(st);
                     if (np == 1 && w0)
-                        search_round<CLUSTER, 1, true>(st, cfg, T, J, row4, s.q4, d, sm, x);
+                        search_round<CLUSTER, 1, true>(st, cfg, J, row4, s.q4, d, sm, x);
                     else if (np == 1)
-                        search_round<CLUSTER, 1, false>(st, cfg, T, J, row4, s.q4, d, sm, x);
+                        search_round<CLUSTER, 1, false>(st, cfg, J, row4, s.q4, d, sm, x);
                     else if (np == 2 && w0)
-                        search_round<CLUSTER, 2, true>(st, cfg, T, J, row4, s.q4, d, sm, x);
+                        search_round<CLUSTER, 2, true>(st, cfg, J, row4, s.q4, d, sm, x);
                     else if (np == 2)
-                        search_round<CLUSTER, 2, false>(st, cfg, T, J, row4, s.q4, d, sm, x);
+                        search_round<CLUSTER, 2, false>(st, cfg, J, row4, s.q4, d, sm, x);
                     else if (np == 3)
-                        search_round<CLUSTER, 3, false>(st, cfg, T, J, row4, s.q4, d, sm, x);
+                        search_round<CLUSTER, 3, false>(st, cfg, J, row4, s.q4, d, sm, x);
                 }
-                if (st.overflow) bits |= kBitOverflow;
-                T_row = st.T_out;
-                beta_out = rcp_approx(st.T_out);
-                inv_s = 1.0f / st.S_out;
+                if (st.f & kOverflow) bits |= kBitOverflow;
+                T_row = search_result_T(st, cfg);
+                beta_out = rcp_approx(T_row);
+                inv_s = 1.0f / st.SA;
             }
         } else {
             bits = row_code == 2 ? kBitNan : kBitInf;
@@ -737,7 +703,15 @@ cluster_kernel(RowTask t, int n, int slice_len) {
         // The slice buffer is rewritten by the next row's loads.
         __syncthreads();
     }
-    if (CLUSTER) cluster_sync();
+    if (CLUSTER) {
+        // After a timeout, give pushes that peers had already issued into
+        // this CTA's slots time to land before the CTA can exit (a bounded
+        // sleep: st.async completes within microseconds).
+        if (__syncthreads_or(x.dead)) {
+            for (int i = 0; i < 1000; ++i) __nanosleep(1000);
+        }
+        cluster_sync();
+    }
 }
 
 template <bool CLUSTER, int MAXT, int MINB, bool ASYNC>
