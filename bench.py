@@ -641,11 +641,17 @@ def our_arm(args, w: wl.Workload) -> int:
 
 
 # ------------------------------------------------------------ per config
-def per_config_workloads() -> list[wl.Workload]:
-    """Every configuration of the benchmark besides the headline's:
-    4 x 1000, the 65536 x 64 router, 256 x 131072 long rows and the six
-    points of the 4096 x 32000 sweep."""
-    return [wl.SMALL, wl.LATENCY, wl.ROUTER, wl.LONG] + wl.sweep_workloads()
+def per_config_workloads() -> list[tuple[wl.Workload, str]]:
+    """Every configuration of the benchmark besides the headline's, with
+    its logit type: 4 x 1000, the 65536 x 64 router, 256 x 131072 long rows
+    and the six points of the 4096 x 32000 sweep in fp32; then the long
+    rows, the 32 x 50000 rows and one sweep point with bf16 logits (the
+    work-reducing input form: 6 bytes per class instead of 8)."""
+    out = [(w, "f32") for w in [wl.SMALL, wl.LATENCY, wl.ROUTER, wl.LONG]
+           + wl.sweep_workloads()]
+    sweep02 = next(w for w in wl.sweep_workloads() if w.name.endswith("b0.2_it20"))
+    out += [(wl.LATENCY, "bf16"), (wl.LONG, "bf16"), (sweep02, "bf16")]
+    return out
 
 
 def per_config_runs(torch, cs, dev, stream, ex2_peak: float, hbm_gbs: float,
@@ -664,27 +670,37 @@ def per_config_runs(torch, cs, dev, stream, ex2_peak: float, hbm_gbs: float,
     sampler.start()
     results = {}
     cache = {}
-    for w in per_config_workloads():
-        if w.name == skip:
+    for w, dt in per_config_workloads():
+        if w.name == skip and dt == "f32":
             continue
         base = w.name.split("_b")[0] if w.name.startswith(wl.SWEEP.name) else w.name
-        if base not in cache:
+        key = (base, dt)
+        if key not in cache:
             cache.clear()
             xw = wl.generate(w)
-            cache[base] = (xw, entropy_at_one(xw))
-        x, h1 = cache[base]
+            if dt == "bf16":
+                bits = wl.to_bf16_bits(xw)
+                xw = wl.bf16_to_f32(bits)
+                dev_x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+            else:
+                dev_x = torch.from_numpy(xw)
+            cache[key] = (xw, entropy_at_one(xw), dev_x)
+        x, h1, dev_x = cache[key]
         B, C = x.shape
-        io_bytes = 8 * B * C
+        in_bytes = 2 if dt == "bf16" else 4
+        io_bytes = (in_bytes + 4) * B * C
         nbuf = (max(1, math.ceil(3 * L2_BYTES / io_bytes))
                 if io_bytes < 3 * L2_BYTES else 1)
-        xs = torch.from_numpy(x).to(dev)
+        xs = dev_x.to(dev)
         ins = xs.unsqueeze(0).repeat(nbuf, 1, 1) if nbuf > 1 else xs.unsqueeze(0)
-        outs = torch.empty_like(ins)
+        outs = torch.empty((nbuf, B, C), dtype=torch.float32, device=dev)
         touts = torch.empty((nbuf, B), dtype=torch.float32, device=dev)
+        entry_fn = (cs.cs_constrained_softmax_bf16_ex if dt == "bf16"
+                    else cs.cs_constrained_softmax_ex)
 
         def launch(i: int, sp: int = sptr) -> None:
             k = i % nbuf
-            st = cs.cs_constrained_softmax_ex(
+            st = entry_fn(
                 ins[k].data_ptr(), outs[k].data_ptr(), B, C, w.entropy_bound,
                 w.t_min, w.t_max, w.max_iter, touts[k].data_ptr(), None, sp)
             if st != 0:
@@ -726,7 +742,8 @@ def per_config_runs(torch, cs, dev, stream, ex2_peak: float, hbm_gbs: float,
                             t_kernel, ex2_peak, hbm_gbs)
         entry = {
             "batch": B, "num_classes": C, "entropy_bound": w.entropy_bound,
-            "max_iter": w.max_iter, "launches_timed": K * reps,
+            "max_iter": w.max_iter, "logits": dt, "bytes_per_class": in_bytes + 4,
+            "launches_timed": K * reps,
             "ms_per_step": ms, "rows_per_s": B / t_kernel,
             "hbm_gbs": roof["hbm_gbs"], "bound": roof["bound"],
             "frac": roof["frac"], "frac_executed": roof["frac_executed"],
@@ -745,7 +762,7 @@ def per_config_runs(torch, cs, dev, stream, ex2_peak: float, hbm_gbs: float,
                 "kind": "oracle",
                 "sample": f"{smp['rows']} whole rows in "
                           f"{smp['seconds']:.1f} s on one thread"}
-        results[w.name] = entry
+        results[w.name if dt == "f32" else f"{w.name}_bf16"] = entry
         del graph, ins, outs, touts, xs, evals
         torch.cuda.synchronize()
         torch.cuda.empty_cache()

@@ -26,6 +26,8 @@ from ._lib import (CONSTANTS, cs_attention_softmax, cs_attention_softmax_ex,
                    cs_constrained_softmax_backward,
                    cs_constrained_softmax_backward_ex,
                    cs_constrained_softmax_ex, cs_get_error,
+                   cs_constrained_softmax_bf16, cs_constrained_softmax_bf16_ex,
+                   cs_check_args_bf16,
                    cs_plan_attention_host, cs_plan_attention_launch,
                    cs_plan_backward_host, cs_plan_backward_launch,
                    cs_plan_host, cs_plan_launch, cs_probe_ex2,
@@ -37,6 +39,8 @@ __all__ = [
     "ConstrainedSoftmaxFunction", "get_error", "plan", "plan_backward",
     "version", "CsError", "ERROR_BITS", "VARIANTS", "options",
     "cs_constrained_softmax", "cs_constrained_softmax_ex",
+    "cs_constrained_softmax_bf16", "cs_constrained_softmax_bf16_ex",
+    "cs_check_args_bf16",
     "cs_constrained_softmax_backward", "cs_constrained_softmax_backward_ex",
     "cs_get_error", "cs_plan_launch", "cs_plan_host",
     "cs_plan_backward_launch", "cs_plan_backward_host", "cs_check_args",
@@ -84,7 +88,9 @@ def constrained_softmax(logits, entropy_bound: float = DEFAULT_ENTROPY_BOUND,
                         variant: str = "auto", param: int = 0,
                         threads: int = 0, strict: bool = False,
                         evals_out=None):
-    """Entropy-bounded softmax of a CUDA fp32 [batch, num_classes] tensor.
+    """Entropy-bounded softmax of a CUDA [batch, num_classes] tensor of fp32
+    logits, or of bf16 logits (``cs_constrained_softmax_bf16``: promoted
+    exactly to fp32 on load; the probabilities are fp32 either way).
 
     Returns the probabilities (and the per-row temperature if ``return_t``).
     ``out``/``t_out`` may be given to write into existing tensors.  The call
@@ -100,15 +106,16 @@ def constrained_softmax(logits, entropy_bound: float = DEFAULT_ENTROPY_BOUND,
         raise TypeError("logits must be a torch.Tensor")
     if logits.device.type != "cuda":
         raise ValueError("logits must be on a CUDA device")
-    if logits.dtype != torch.float32:
-        raise TypeError("logits must be float32")
+    if logits.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("logits must be float32 or bfloat16")
     if logits.dim() != 2:
         raise ValueError("logits must be 2-D [batch, num_classes]")
     if not logits.is_contiguous():
         raise ValueError("logits must be contiguous")
     batch, num_classes = logits.shape
     if out is None:
-        out = torch.empty_like(logits)
+        out = torch.empty(logits.shape, dtype=torch.float32,
+                          device=logits.device)
     elif (out.shape != logits.shape or out.dtype != torch.float32
           or out.device != logits.device or not out.is_contiguous()):
         raise ValueError("out must be a contiguous float32 tensor shaped like "
@@ -133,8 +140,10 @@ def constrained_softmax(logits, entropy_bound: float = DEFAULT_ENTROPY_BOUND,
             raise ValueError("evals_out must be a contiguous int32 [batch] "
                              "tensor on the logits' device")
         e_ptr = evals_out.data_ptr()
+    entry = (cs_constrained_softmax_bf16_ex
+             if logits.dtype == torch.bfloat16 else cs_constrained_softmax_ex)
     with torch.cuda.device(logits.device):
-        st = cs_constrained_softmax_ex(
+        st = entry(
             logits.data_ptr(), out.data_ptr(), batch, num_classes,
             float(entropy_bound), float(t_min), float(t_max), int(max_iter),
             t_ptr, options(VARIANTS[variant], param, threads, int(strict),

@@ -72,6 +72,14 @@ _SIGNATURES = {
     "cs_constrained_softmax_ex": (_I32, [_VP, _VP, _I64, _I32, _F32, _F32,
                                          _F32, _I32, _VP,
                                          ctypes.POINTER(cs_options), _VP]),
+    "cs_constrained_softmax_bf16": (_I32, [_VP, _VP, _I64, _I32, _F32, _F32,
+                                           _F32, _I32, _VP, _VP]),
+    "cs_constrained_softmax_bf16_ex": (_I32, [_VP, _VP, _I64, _I32, _F32,
+                                              _F32, _F32, _I32, _VP,
+                                              ctypes.POINTER(cs_options),
+                                              _VP]),
+    "cs_check_args_bf16": (_I32, [_VP, _VP, _I64, _I32, _F32, _F32, _F32,
+                                  _I32, _VP]),
     "cs_get_error": (_I32, [ctypes.POINTER(_I32), _VP]),
     "cs_plan_launch": (_I32, [_I64, _I32, ctypes.POINTER(cs_options),
                               ctypes.POINTER(cs_plan)]),
@@ -174,6 +182,29 @@ def cs_constrained_softmax_ex(logits, out, batch, num_classes, entropy_bound,
     return load().cs_constrained_softmax_ex(
         logits, out, batch, num_classes, entropy_bound, t_min, t_max,
         max_iter, t_out, _opt_ref(opt), stream)
+
+
+def cs_constrained_softmax_bf16(logits, out, batch, num_classes,
+                                entropy_bound, t_min, t_max, max_iter, t_out,
+                                stream) -> int:
+    return load().cs_constrained_softmax_bf16(logits, out, batch, num_classes,
+                                              entropy_bound, t_min, t_max,
+                                              max_iter, t_out, stream)
+
+
+def cs_constrained_softmax_bf16_ex(logits, out, batch, num_classes,
+                                   entropy_bound, t_min, t_max, max_iter,
+                                   t_out, opt, stream) -> int:
+    return load().cs_constrained_softmax_bf16_ex(
+        logits, out, batch, num_classes, entropy_bound, t_min, t_max,
+        max_iter, t_out, _opt_ref(opt), stream)
+
+
+def cs_check_args_bf16(logits, out, batch, num_classes, entropy_bound, t_min,
+                       t_max, max_iter, t_out) -> int:
+    return load().cs_check_args_bf16(logits, out, batch, num_classes,
+                                     entropy_bound, t_min, t_max, max_iter,
+                                     t_out)
 
 
 def cs_get_error(stream) -> tuple[int, int]:

@@ -416,11 +416,15 @@ cs_status plan_attention(int32_t batch, int32_t heads, int32_t S,
 
 }  // namespace
 
-extern "C" {
+namespace {
 
-cs_status cs_check_args(const float* logits, const float* out, int64_t batch,
-                        int32_t num_classes, float entropy_bound, float t_min,
-                        float t_max, int32_t max_iter, const float* t_out) {
+// Argument check of the forward for logits of in_bytes (4: fp32, 2: bf16)
+// per element.
+cs_status check_forward_args(const void* logits, const float* out,
+                             int64_t batch, int32_t num_classes,
+                             float entropy_bound, float t_min, float t_max,
+                             int32_t max_iter, const float* t_out,
+                             int in_bytes) {
     if (batch < 0 || num_classes < 1) return CS_ERR_DIM_MISMATCH;
     if (num_classes > CS_MAX_NUM_CLASSES) return CS_ERR_OOM;
     if (batch > INT64_MAX / 4 / num_classes) return CS_ERR_DIM_MISMATCH;
@@ -430,12 +434,94 @@ cs_status cs_check_args(const float* logits, const float* out, int64_t batch,
     if (max_iter < 0 || max_iter > kMaxIter) return CS_ERR_INVALID_ARG;
     if (batch == 0) return CS_OK;
     if (!logits || !out) return CS_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(logits) % in_bytes) return CS_ERR_INVALID_ARG;
+    const int64_t in_size = batch * num_classes * in_bytes;
     const int64_t bytes = batch * num_classes * 4;
-    if (ranges_overlap(logits, bytes, out, bytes)) return CS_ERR_INVALID_ARG;
-    if (t_out && (ranges_overlap(t_out, batch * 4, logits, bytes) ||
+    if (ranges_overlap(logits, in_size, out, bytes)) return CS_ERR_INVALID_ARG;
+    if (t_out && (ranges_overlap(t_out, batch * 4, logits, in_size) ||
                   ranges_overlap(t_out, batch * 4, out, bytes)))
         return CS_ERR_INVALID_ARG;
     return CS_OK;
+}
+
+// The forward for fp32 (in_bf16 = false) or bf16 logits.
+cs_status forward(const void* logits, bool in_bf16, float* out, int64_t batch,
+                  int32_t num_classes, float entropy_bound, float t_min,
+                  float t_max, int32_t max_iter, float* t_out,
+                  const cs_options* options, void* stream) {
+    const int in_bytes = in_bf16 ? 2 : 4;
+    cs_status st = check_forward_args(logits, out, batch, num_classes,
+                                      entropy_bound, t_min, t_max, max_iter,
+                                      t_out, in_bytes);
+    if (st != CS_OK) return st;
+    if (batch == 0) return CS_OK;
+    if (options && options->evals_out) {
+        const int64_t bytes = batch * num_classes * 4;
+        const void* e = options->evals_out;
+        if (ranges_overlap(e, batch * 4, logits, batch * num_classes * in_bytes) ||
+            ranges_overlap(e, batch * 4, out, bytes) ||
+            (t_out && ranges_overlap(e, batch * 4, t_out, batch * 4)))
+            return CS_ERR_INVALID_ARG;
+    }
+    DeviceInfo* d = nullptr;
+    st = device_info(&d);
+    if (st != CS_OK) return st;
+    cs_plan p;
+    st = cs_plan_host(batch, num_classes, options, d->sm_count, d->smem_optin,
+                      d->smem_per_sm, d->max_cluster, &p);
+    if (st != CS_OK) return st;
+
+    cs::RowTask task;
+    task.logits = logits;
+    task.out = out;
+    task.t_out = t_out;
+    task.err = d->err;
+    task.batch = batch;
+    task.num_classes = num_classes;
+    task.max_iter = max_iter;
+    task.entropy_bound = entropy_bound;
+    task.t_min = t_min;
+    task.hi0 = t_max < 1.0f ? t_max : 1.0f;
+    task.strict = options ? options->strict : 0;
+    // Asynchronous staging pays when several CTAs share an SM (the same
+    // threshold as the per-thread work rule of the thread count).
+    task.async_stage = p.grid_ctas * 4 > static_cast<int64_t>(d->sm_count) * 5;
+    task.wait_limit_cycles = cs::kWaitLimitCycles;
+    task.evals_out = options ? options->evals_out : nullptr;
+    task.in_bf16 = in_bf16 ? 1 : 0;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (p.variant == CS_VARIANT_ROWGROUP) {
+        e = cs::launch_rowgroup(task, p.lanes_per_row, p.elems_per_lane, s);
+    } else {
+        e = cs::launch_cluster(task, p.cluster_size, p.slice_len,
+                               p.threads_per_cta, p.smem_bytes, p.grid_ctas, s);
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return CS_ERR_CUDA;
+    }
+    return CS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+cs_status cs_check_args(const float* logits, const float* out, int64_t batch,
+                        int32_t num_classes, float entropy_bound, float t_min,
+                        float t_max, int32_t max_iter, const float* t_out) {
+    return check_forward_args(logits, out, batch, num_classes, entropy_bound,
+                              t_min, t_max, max_iter, t_out, 4);
+}
+
+cs_status cs_check_args_bf16(const uint16_t* logits, const float* out,
+                             int64_t batch, int32_t num_classes,
+                             float entropy_bound, float t_min, float t_max,
+                             int32_t max_iter, const float* t_out) {
+    return check_forward_args(logits, out, batch, num_classes, entropy_bound,
+                              t_min, t_max, max_iter, t_out, 2);
 }
 
 cs_status cs_plan_host(int64_t batch, int32_t num_classes,
@@ -482,66 +568,36 @@ cs_status cs_constrained_softmax_ex(const float* logits, float* out,
                                     float t_max, int32_t max_iter,
                                     float* t_out, const cs_options* options,
                                     void* stream) {
-    cs_status st = cs_check_args(logits, out, batch, num_classes,
-                                 entropy_bound, t_min, t_max, max_iter, t_out);
-    if (st != CS_OK) return st;
-    if (batch == 0) return CS_OK;
-    if (options && options->evals_out) {
-        const int64_t bytes = batch * num_classes * 4;
-        const void* e = options->evals_out;
-        if (ranges_overlap(e, batch * 4, logits, bytes) ||
-            ranges_overlap(e, batch * 4, out, bytes) ||
-            (t_out && ranges_overlap(e, batch * 4, t_out, batch * 4)))
-            return CS_ERR_INVALID_ARG;
-    }
-    DeviceInfo* d = nullptr;
-    st = device_info(&d);
-    if (st != CS_OK) return st;
-    cs_plan p;
-    st = cs_plan_host(batch, num_classes, options, d->sm_count, d->smem_optin,
-                      d->smem_per_sm, d->max_cluster, &p);
-    if (st != CS_OK) return st;
-
-    cs::RowTask task;
-    task.logits = logits;
-    task.out = out;
-    task.t_out = t_out;
-    task.err = d->err;
-    task.batch = batch;
-    task.num_classes = num_classes;
-    task.max_iter = max_iter;
-    task.entropy_bound = entropy_bound;
-    task.t_min = t_min;
-    task.hi0 = t_max < 1.0f ? t_max : 1.0f;
-    task.strict = options ? options->strict : 0;
-    // Asynchronous staging pays when several CTAs share an SM (the same
-    // threshold as the per-thread work rule of the thread count).
-    task.async_stage = p.grid_ctas * 4 > static_cast<int64_t>(d->sm_count) * 5;
-    task.wait_limit_cycles = cs::kWaitLimitCycles;
-    task.evals_out = options ? options->evals_out : nullptr;
-
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e;
-    if (p.variant == CS_VARIANT_ROWGROUP) {
-        e = cs::launch_rowgroup(task, p.lanes_per_row, p.elems_per_lane, s);
-    } else {
-        e = cs::launch_cluster(task, p.cluster_size, p.slice_len,
-                               p.threads_per_cta, p.smem_bytes, p.grid_ctas, s);
-    }
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return CS_ERR_CUDA;
-    }
-    return CS_OK;
+    return forward(logits, false, out, batch, num_classes, entropy_bound,
+                   t_min, t_max, max_iter, t_out, options, stream);
 }
 
 cs_status cs_constrained_softmax(const float* logits, float* out,
                                  int64_t batch, int32_t num_classes,
                                  float entropy_bound, float t_min, float t_max,
                                  int32_t max_iter, float* t_out, void* stream) {
-    return cs_constrained_softmax_ex(logits, out, batch, num_classes,
-                                     entropy_bound, t_min, t_max, max_iter,
-                                     t_out, nullptr, stream);
+    return forward(logits, false, out, batch, num_classes, entropy_bound,
+                   t_min, t_max, max_iter, t_out, nullptr, stream);
+}
+
+cs_status cs_constrained_softmax_bf16_ex(const uint16_t* logits, float* out,
+                                         int64_t batch, int32_t num_classes,
+                                         float entropy_bound, float t_min,
+                                         float t_max, int32_t max_iter,
+                                         float* t_out,
+                                         const cs_options* options,
+                                         void* stream) {
+    return forward(logits, true, out, batch, num_classes, entropy_bound,
+                   t_min, t_max, max_iter, t_out, options, stream);
+}
+
+cs_status cs_constrained_softmax_bf16(const uint16_t* logits, float* out,
+                                      int64_t batch, int32_t num_classes,
+                                      float entropy_bound, float t_min,
+                                      float t_max, int32_t max_iter,
+                                      float* t_out, void* stream) {
+    return forward(logits, true, out, batch, num_classes, entropy_bound,
+                   t_min, t_max, max_iter, t_out, nullptr, stream);
 }
 
 cs_status cs_get_error(int32_t* code_mask, void* stream) {

@@ -121,9 +121,67 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
                  :: "r"(smem_addr(dst)), "l"(src) : "memory");
 }
 
+// 8-byte asynchronous copy global -> shared (through L1); both addresses
+// 8-byte aligned.
+__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;"
+                 :: "r"(smem_addr(dst)), "l"(src) : "memory");
+}
+
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
+
+// ------------------------------------------------------------------- inputs
+// Logit element types.  fp32 logits are read as they are; bf16 logits (their
+// 16-bit patterns) are promoted to fp32 on load, which is exact (a bf16 is
+// the top half of the fp32 with the same value), so everything after the
+// load is the fp32 operation on the promoted logits.  Loads are streaming
+// (read once).  get4 reads 4 consecutive elements from an address aligned
+// to 4 elements (16 bytes for fp32, 8 for bf16).
+struct InF32 {
+    using T = float;
+    static constexpr int kBytes = 4;
+    static __device__ __forceinline__ float get(const T* p) { return *p; }
+    static __device__ __forceinline__ float get_cs(const T* p) { return __ldcs(p); }
+    static __device__ __forceinline__ float4 get4(const T* p) {
+        return __ldcs(reinterpret_cast<const float4*>(p));
+    }
+    // Asynchronous copy of 4 elements into a 16-byte shared slot, and the
+    // slot's fp32 values once it landed.
+    static __device__ __forceinline__ void copy4_async(float4* dst, const T* p) {
+        cp_async16(dst, p);
+    }
+    static __device__ __forceinline__ float4 widen(float4 slot) { return slot; }
+};
+
+struct InBF16 {
+    using T = unsigned short;
+    static constexpr int kBytes = 2;
+    static __device__ __forceinline__ float lo(uint32_t u) { return __uint_as_float(u << 16); }
+    static __device__ __forceinline__ float hi(uint32_t u) {
+        return __uint_as_float(u & 0xffff0000u);
+    }
+    static __device__ __forceinline__ float get(const T* p) {
+        return lo(static_cast<uint32_t>(*p));
+    }
+    static __device__ __forceinline__ float get_cs(const T* p) {
+        return lo(static_cast<uint32_t>(__ldcs(p)));
+    }
+    static __device__ __forceinline__ float4 get4(const T* p) {
+        const uint2 v = __ldcs(reinterpret_cast<const uint2*>(p));
+        return make_float4(lo(v.x), hi(v.x), lo(v.y), hi(v.y));
+    }
+    // The 8 bytes of 4 bf16 go to the first half of the slot; widen()
+    // expands them to the slot's four fp32 values.
+    static __device__ __forceinline__ void copy4_async(float4* dst, const T* p) {
+        cp_async8(dst, p);
+    }
+    static __device__ __forceinline__ float4 widen(float4 slot) {
+        const uint32_t a = __float_as_uint(slot.x), b = __float_as_uint(slot.y);
+        return make_float4(lo(a), hi(a), lo(b), hi(b));
+    }
+};
 
 __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;

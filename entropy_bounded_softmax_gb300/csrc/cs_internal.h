@@ -24,7 +24,7 @@ constexpr uint64_t kWaitLimitCycles = 1ull << 31;
 // parameters (the arguments of section 2.1's signature plus t_out and the
 // error word).
 struct RowTask {
-    const float* logits;
+    const void* logits;    // fp32, or bf16 bit patterns when in_bf16
     float* out;
     float* t_out;          // may be null
     unsigned int* err;     // device error word
@@ -38,6 +38,7 @@ struct RowTask {
     int32_t async_stage;   // cluster kernel: stage with asynchronous copies
     uint64_t wait_limit_cycles;
     int32_t* evals_out;    // may be null: temperatures evaluated per row
+    int32_t in_bf16;       // 1: logits are bf16 (promoted exactly to fp32)
 };
 
 // Cluster kernel geometry.

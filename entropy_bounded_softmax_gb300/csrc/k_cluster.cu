@@ -52,10 +52,10 @@ namespace {
 using namespace csd;
 
 // Geometry of one CTA's slice in shared memory.  Element j of the slice
-// lives at row[pad + j], so 16-byte aligned global addresses land on
-// 16-byte aligned shared addresses.  Float4 q in [qb0, qb1) comes in by
-// 128-bit loads; the head (q = 0 when pad > 0) and tail float4s element by
-// element.
+// lives at row[pad + j], so groups of four elements that are aligned in
+// global memory (16 bytes of fp32, 8 of bf16) land on 16-byte aligned
+// shared addresses.  Float4 q in [qb0, qb1) comes in by vector loads; the
+// head (q = 0 when pad > 0) and tail float4s element by element.
 struct Slice {
     int pad;
     int len;
@@ -65,9 +65,10 @@ struct Slice {
     int tail_q;   // -1 if none
 };
 
-__device__ __forceinline__ Slice make_slice(const float* src, int len) {
+template <class In>
+__device__ __forceinline__ Slice make_slice(const typename In::T* src, int len) {
     Slice s;
-    s.pad = static_cast<int>((reinterpret_cast<uintptr_t>(src) >> 2) & 3);
+    s.pad = static_cast<int>((reinterpret_cast<uintptr_t>(src) / In::kBytes) & 3);
     s.len = len;
     if (len <= 0) {
         s.len = 0;
@@ -501,7 +502,7 @@ __device__ __forceinline__ void write_out(const float4* row4, const Slice& s,
 // throughput plans, 512 x 1 for the latency plans); ASYNC: stage with
 // asynchronous copies (a compile-time choice: a run-time branch between
 // the two staging loops cost the other path 1.4% at 32 x 50000).
-template <bool CLUSTER, int MAXT, int MINB, bool ASYNC>
+template <bool CLUSTER, int MAXT, int MINB, bool ASYNC, class In>
 __global__ void __launch_bounds__(MAXT, MINB)
 cluster_kernel(RowTask t, int n, int slice_len) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -544,8 +545,9 @@ cluster_kernel(RowTask t, int n, int slice_len) {
     bool reported = false;
 
     for (int64_t r = cid; r < t.batch; r += ncl) {
-        const float* src = t.logits + r * C + s0;
-        const Slice s = make_slice(src, len);
+        const typename In::T* src =
+            static_cast<const typename In::T*>(t.logits) + r * C + s0;
+        const Slice s = make_slice<In>(src, len);
 
         // Stage: thread t copies float4s q = t, t + nt, ... of the slice
         // (the float4s it owns in every later pass) into shared memory and
@@ -569,7 +571,7 @@ cluster_kernel(RowTask t, int n, int slice_len) {
                 const int j = 4 * q + i - s.pad;
                 e[i] = -INFINITY;
                 if (j >= 0 && j < s.len) {
-                    e[i] = src[j];
+                    e[i] = In::get(src + j);
                     m_t = fmaxf(m_t, e[i]);
                     bad = fmaf(e[i], 0.0f, bad);
                     nan_seen = nan_seen || isnan(e[i]);
@@ -585,31 +587,39 @@ cluster_kernel(RowTask t, int n, int slice_len) {
             bad = fmaf(v.w, 0.0f, bad);
         };
         {
-            const float* gb = src - s.pad;  // float4 q of the body is at gb + 4q
+            const typename In::T* gb = src - s.pad;  // float4 q of the body is at gb + 4q
             int q = threadIdx.x;
             if (q < s.qb0) {
                 load_ragged(q);
                 q += nt;
             }
             if (ASYNC) {
+                // Each thread copies its own float4 slots, so after its own
+                // wait it may widen (bf16) and fold them without a barrier.
                 const int qb = q;
-                for (; q < s.qb1; q += nt) cp_async16(&row4[q], gb + 4 * q);
+                for (; q < s.qb1; q += nt) In::copy4_async(&row4[q], gb + 4 * q);
                 if (q < s.q4) load_ragged(q);
                 cp_async_wait_all();
                 for (q = qb; q + 3 * nt < s.qb1; q += 4 * nt) {
                     float4 v[4];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) v[i] = row4[q + i * nt];
+                    for (int i = 0; i < 4; ++i) v[i] = In::widen(row4[q + i * nt]);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) fold(v[i]);
+                    for (int i = 0; i < 4; ++i) {
+                        if (In::kBytes != 4) row4[q + i * nt] = v[i];
+                        fold(v[i]);
+                    }
                 }
-                for (; q < s.qb1; q += nt) fold(row4[q]);
+                for (; q < s.qb1; q += nt) {
+                    const float4 v = In::widen(row4[q]);
+                    if (In::kBytes != 4) row4[q] = v;
+                    fold(v);
+                }
             } else {
                 for (; q + 7 * nt < s.qb1; q += 8 * nt) {
                     float4 v[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        v[i] = __ldcs(reinterpret_cast<const float4*>(gb + 4 * (q + i * nt)));
+                    for (int i = 0; i < 8; ++i) v[i] = In::get4(gb + 4 * (q + i * nt));
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         row4[q + i * nt] = v[i];
@@ -617,7 +627,7 @@ cluster_kernel(RowTask t, int n, int slice_len) {
                     }
                 }
                 for (; q < s.qb1; q += nt) {
-                    const float4 v = __ldcs(reinterpret_cast<const float4*>(gb + 4 * q));
+                    const float4 v = In::get4(gb + 4 * q);
                     row4[q] = v;
                     fold(v);
                 }
@@ -714,11 +724,11 @@ cluster_kernel(RowTask t, int n, int slice_len) {
     }
 }
 
-template <bool CLUSTER, int MAXT, int MINB, bool ASYNC>
+template <bool CLUSTER, int MAXT, int MINB, bool ASYNC, class In>
 cudaError_t launch_one(const RowTask& task, int cluster_size, int slice_len,
                        int threads, int smem_bytes, int64_t grid_ctas,
                        cudaStream_t stream, int attr_slot) {
-    auto kern = cluster_kernel<CLUSTER, MAXT, MINB, ASYNC>;
+    auto kern = cluster_kernel<CLUSTER, MAXT, MINB, ASYNC, In>;
     cudaError_t e = ensure_smem_attribute(reinterpret_cast<const void*>(kern),
                                           attr_slot, smem_bytes, CLUSTER);
     if (e != cudaSuccess) return e;
@@ -742,23 +752,26 @@ cudaError_t launch_one(const RowTask& task, int cluster_size, int slice_len,
     return cudaLaunchKernelEx(&cfg, kern, task, cluster_size, slice_len);
 }
 
-template <bool ASYNC>
+template <bool ASYNC, class In>
 cudaError_t launch_cluster_as(const RowTask& task, int cluster_size,
                               int slice_len, int threads, int smem_bytes,
                               int64_t grid_ctas, cudaStream_t stream) {
     const bool narrow = threads <= 256;
-    const int slot = (ASYNC ? 4 : 0) + (cluster_size > 1 ? 1 : 0) + (narrow ? 0 : 2);
+    // Attribute slots: fp32 0-7, bf16 19-26 (8-18 belong to the other
+    // operations' kernels).
+    const int slot = (In::kBytes == 2 ? 19 : 0) + (ASYNC ? 4 : 0) +
+                     (cluster_size > 1 ? 1 : 0) + (narrow ? 0 : 2);
     if (cluster_size > 1)
-        return narrow ? launch_one<true, 256, 3, ASYNC>(task, cluster_size, slice_len,
-                                                        threads, smem_bytes, grid_ctas,
-                                                        stream, slot)
-                      : launch_one<true, 512, 1, ASYNC>(task, cluster_size, slice_len,
-                                                        threads, smem_bytes, grid_ctas,
-                                                        stream, slot);
-    return narrow ? launch_one<false, 256, 3, ASYNC>(task, 1, slice_len, threads,
-                                                     smem_bytes, grid_ctas, stream, slot)
-                  : launch_one<false, 512, 1, ASYNC>(task, 1, slice_len, threads,
-                                                     smem_bytes, grid_ctas, stream, slot);
+        return narrow ? launch_one<true, 256, 3, ASYNC, In>(task, cluster_size, slice_len,
+                                                            threads, smem_bytes, grid_ctas,
+                                                            stream, slot)
+                      : launch_one<true, 512, 1, ASYNC, In>(task, cluster_size, slice_len,
+                                                            threads, smem_bytes, grid_ctas,
+                                                            stream, slot);
+    return narrow ? launch_one<false, 256, 3, ASYNC, In>(task, 1, slice_len, threads,
+                                                         smem_bytes, grid_ctas, stream, slot)
+                  : launch_one<false, 512, 1, ASYNC, In>(task, 1, slice_len, threads,
+                                                         smem_bytes, grid_ctas, stream, slot);
 }
 
 }  // namespace
@@ -766,11 +779,19 @@ cudaError_t launch_cluster_as(const RowTask& task, int cluster_size,
 cudaError_t launch_cluster(const RowTask& task, int cluster_size,
                            int slice_len, int threads, int smem_bytes,
                            int64_t grid_ctas, cudaStream_t stream) {
+    if (task.in_bf16)
+        return task.async_stage
+            ? launch_cluster_as<true, InBF16>(task, cluster_size, slice_len,
+                                              threads, smem_bytes, grid_ctas,
+                                              stream)
+            : launch_cluster_as<false, InBF16>(task, cluster_size, slice_len,
+                                               threads, smem_bytes, grid_ctas,
+                                               stream);
     return task.async_stage
-        ? launch_cluster_as<true>(task, cluster_size, slice_len, threads,
-                                  smem_bytes, grid_ctas, stream)
-        : launch_cluster_as<false>(task, cluster_size, slice_len, threads,
-                                   smem_bytes, grid_ctas, stream);
+        ? launch_cluster_as<true, InF32>(task, cluster_size, slice_len, threads,
+                                         smem_bytes, grid_ctas, stream)
+        : launch_cluster_as<false, InF32>(task, cluster_size, slice_len, threads,
+                                          smem_bytes, grid_ctas, stream);
 }
 
 }  // namespace cs

@@ -24,7 +24,7 @@ using namespace csd;
 // At most 64 registers a thread (32 warps per SM, which the latency of each
 // row's dependent reduce-and-decide chain needs), or 80 when a lane holds
 // 32 classes.
-template <int G, int E4>
+template <int G, int E4, class In>
 __global__ void __launch_bounds__(64, E4 >= 8 ? 12 : 16)
 rowgroup_kernel(RowTask t, int vec) {
     const int lane = threadIdx.x & 31;
@@ -43,18 +43,17 @@ rowgroup_kernel(RowTask t, int vec) {
     for (int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x +
                         threadIdx.x) / G;
          row < t.batch; row += groups_per_grid) {
-        const float* src = t.logits + row * C;
+        const typename In::T* src = static_cast<const typename In::T*>(t.logits) + row * C;
         float* dst = t.out + row * C;
         float4 y[E4];
         float m = -INFINITY;
         float bad = 0.0f;
         if (vec) {
-            const float4* s4 = reinterpret_cast<const float4*>(src);
 #pragma unroll
             for (int i = 0; i < E4; ++i) {
                 const int q = i * G + sub;
                 if (q < Q) {
-                    y[i] = __ldcs(s4 + q);
+                    y[i] = In::get4(src + 4 * q);
                     m = fmaxf(m, fmaxf(fmaxf(y[i].x, y[i].y),
                                        fmaxf(y[i].z, y[i].w)));
                     bad = fmaf(y[i].x, 0.f, bad);
@@ -75,7 +74,7 @@ rowgroup_kernel(RowTask t, int vec) {
                     const int j = j0 + k;
                     e[k] = -INFINITY;
                     if (j < C) {
-                        e[k] = __ldcs(src + j);
+                        e[k] = In::get_cs(src + j);
                         m = fmaxf(m, e[k]);
                         bad = fmaf(e[k], 0.f, bad);
                     }
@@ -129,17 +128,31 @@ rowgroup_kernel(RowTask t, int vec) {
     }
 }
 
-template <int G>
+template <int G, class In>
 cudaError_t launch_g(const RowTask& t, int e4, int vec, dim3 grid, dim3 block,
                      cudaStream_t s) {
     switch (e4) {
-        case 1: rowgroup_kernel<G, 1><<<grid, block, 0, s>>>(t, vec); break;
-        case 2: rowgroup_kernel<G, 2><<<grid, block, 0, s>>>(t, vec); break;
-        case 4: rowgroup_kernel<G, 4><<<grid, block, 0, s>>>(t, vec); break;
-        case 8: rowgroup_kernel<G, 8><<<grid, block, 0, s>>>(t, vec); break;
+        case 1: rowgroup_kernel<G, 1, In><<<grid, block, 0, s>>>(t, vec); break;
+        case 2: rowgroup_kernel<G, 2, In><<<grid, block, 0, s>>>(t, vec); break;
+        case 4: rowgroup_kernel<G, 4, In><<<grid, block, 0, s>>>(t, vec); break;
+        case 8: rowgroup_kernel<G, 8, In><<<grid, block, 0, s>>>(t, vec); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
+}
+
+template <class In>
+cudaError_t launch_in(const RowTask& t, int lanes_per_row, int e4, int vec,
+                      dim3 grid, dim3 block, cudaStream_t stream) {
+    switch (lanes_per_row) {
+        case 1: return launch_g<1, In>(t, e4, vec, grid, block, stream);
+        case 2: return launch_g<2, In>(t, e4, vec, grid, block, stream);
+        case 4: return launch_g<4, In>(t, e4, vec, grid, block, stream);
+        case 8: return launch_g<8, In>(t, e4, vec, grid, block, stream);
+        case 16: return launch_g<16, In>(t, e4, vec, grid, block, stream);
+        case 32: return launch_g<32, In>(t, e4, vec, grid, block, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace
@@ -151,8 +164,11 @@ cudaError_t launch_rowgroup(const RowTask& t, int lanes_per_row,
                             int elems_per_lane, cudaStream_t stream) {
     const int e4 = elems_per_lane / 4;
     const int C = t.num_classes;
+    // Whole float4s of output, and of input (four elements: 16 bytes of
+    // fp32, 8 of bf16), when every row starts aligned.
+    const uintptr_t in_align = t.in_bf16 ? 8 : 16;
     const bool aligned =
-        (C % 4 == 0) && (reinterpret_cast<uintptr_t>(t.logits) % 16 == 0) &&
+        (C % 4 == 0) && (reinterpret_cast<uintptr_t>(t.logits) % in_align == 0) &&
         (reinterpret_cast<uintptr_t>(t.out) % 16 == 0);
     const int64_t rows_per_block = kRowgroupThreads / lanes_per_row;
     int64_t blocks = (t.batch + rows_per_block - 1) / rows_per_block;
@@ -160,15 +176,9 @@ cudaError_t launch_rowgroup(const RowTask& t, int lanes_per_row,
     const dim3 grid(static_cast<unsigned>(blocks));
     const dim3 block(kRowgroupThreads);
     const int vec = aligned ? 1 : 0;
-    switch (lanes_per_row) {
-        case 1: return launch_g<1>(t, e4, vec, grid, block, stream);
-        case 2: return launch_g<2>(t, e4, vec, grid, block, stream);
-        case 4: return launch_g<4>(t, e4, vec, grid, block, stream);
-        case 8: return launch_g<8>(t, e4, vec, grid, block, stream);
-        case 16: return launch_g<16>(t, e4, vec, grid, block, stream);
-        case 32: return launch_g<32>(t, e4, vec, grid, block, stream);
-        default: return cudaErrorInvalidValue;
-    }
+    return t.in_bf16
+        ? launch_in<InBF16>(t, lanes_per_row, e4, vec, grid, block, stream)
+        : launch_in<InF32>(t, lanes_per_row, e4, vec, grid, block, stream);
 }
 
 }  // namespace cs

@@ -147,6 +147,25 @@ def generate(w: Workload, rows=None) -> np.ndarray:
     return out
 
 
+# bf16 inputs.  The bf16 workloads are the fp32 workloads' logits rounded
+# to the nearest bf16 (ties to even), stored as 16-bit patterns; both sides
+# then see the same values: the CUDA path reads the patterns, the oracle the
+# fp32 numbers they stand for (a bf16 pattern is the top half of that fp32).
+def to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """fp32 array -> uint16 bf16 patterns, rounded to nearest even (NaN
+    stays a quiet NaN, infinities stay infinite)."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+    nan = np.isnan(np.asarray(x, dtype=np.float32))
+    r[nan] = ((u[nan] >> 16) | 0x40).astype(np.uint16)
+    return r
+
+
+def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
+    """uint16 bf16 patterns -> the fp32 values they stand for."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
 def sample_rows(w: Workload, n: int, seed: int = 7) -> np.ndarray:
     """A seeded, sorted sample of n distinct row indices (always includes
     the first and last row)."""

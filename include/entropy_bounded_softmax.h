@@ -173,6 +173,44 @@ cs_status cs_constrained_softmax_ex(const float* logits, float* out,
                                     void* stream);
 
 /*
+ * cs_constrained_softmax_bf16 -- the same operation on bf16 logits: a
+ * work-reducing input form of section 2.1's kernel (the survey's NEXT-2
+ * (iii)) that halves the bytes read per class (2 instead of 4; the output
+ * stays fp32).  Each logit is promoted to fp32 on load, which is exact (a
+ * bf16 value is an fp32 value whose low 16 bits are zero), and from there
+ * the computation is the fp32 one: the result equals, bit for bit,
+ * cs_constrained_softmax on the promoted logits.
+ *
+ * logits   device pointer, [batch, num_classes] bf16 bit patterns
+ *          (uint16_t), row-major, contiguous, 2-byte aligned.  Rows whose
+ *          groups of four classes are 8-byte aligned (num_classes % 4 == 0
+ *          and an 8-byte aligned base) take the vector load path.
+ * Every other argument, the ownership, execution and error behaviour are
+ * those of cs_constrained_softmax (out is fp32 and must not overlap the
+ * logits' 2 * batch * num_classes bytes).
+ */
+cs_status cs_constrained_softmax_bf16(const uint16_t* logits, float* out,
+                                      int64_t batch, int32_t num_classes,
+                                      float entropy_bound, float t_min,
+                                      float t_max, int32_t max_iter,
+                                      float* t_out, void* stream);
+
+/* The same with launch options (as cs_constrained_softmax_ex). */
+cs_status cs_constrained_softmax_bf16_ex(const uint16_t* logits, float* out,
+                                         int64_t batch, int32_t num_classes,
+                                         float entropy_bound, float t_min,
+                                         float t_max, int32_t max_iter,
+                                         float* t_out,
+                                         const cs_options* options,
+                                         void* stream);
+
+/* Host-only argument check of cs_constrained_softmax_bf16 (no CUDA call). */
+cs_status cs_check_args_bf16(const uint16_t* logits, const float* out,
+                             int64_t batch, int32_t num_classes,
+                             float entropy_bound, float t_min, float t_max,
+                             int32_t max_iter, const float* t_out);
+
+/*
  * Reads and clears the calling thread's current device's error word, then
  * synchronises `stream`.  *code_mask receives a bitmask of (1 << code) for
  * every asynchronous condition since the last call: CS_ERR_NAN_INPUT,

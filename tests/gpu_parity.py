@@ -74,6 +74,38 @@ def run_gpu(x: np.ndarray, entropy_bound=0.2, t_min=0.01, t_max=10.0,
     return out.cpu().numpy(), t_out.cpu().numpy(), mask
 
 
+def run_gpu_bf16(bits: np.ndarray, entropy_bound=0.2, t_min=0.01,
+                 t_max=10.0, max_iter=20, variant="auto", param=0,
+                 in_offset=0, out_offset=0, threads=0, strict=False):
+    """run_gpu for bf16 logits given as uint16 patterns (in_offset in bf16
+    elements); returns (p, T, error_mask)."""
+    import torch
+    import entropy_bounded_softmax_gb300 as cs
+    B, C = bits.shape
+    n = B * C
+    dev = torch.device("cuda", 0)
+    buf_in = torch.empty(n + in_offset + 8, dtype=torch.bfloat16, device=dev)
+    xin = buf_in[in_offset:in_offset + n].view(B, C)
+    xin.copy_(torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+              .view(torch.bfloat16))
+    buf_out = torch.full((n + out_offset + 4,), -7.0, dtype=torch.float32,
+                         device=dev)
+    out = buf_out[out_offset:out_offset + n].view(B, C)
+    t_out = torch.full((B,), -3.0, dtype=torch.float32, device=dev)
+    cs.get_error()  # clear
+    cs.constrained_softmax(xin, entropy_bound, t_min, t_max, max_iter,
+                           out=out, t_out=t_out, variant=variant,
+                           param=param, threads=threads, strict=strict)
+    bits_err = cs.get_error()
+    mask = 0
+    for name, bit in cs.ERROR_BITS.items():
+        if name in bits_err:
+            mask |= bit
+    assert torch.all(buf_out[:out_offset] == -7.0)
+    assert torch.all(buf_out[out_offset + n:] == -7.0)
+    return out.cpu().numpy(), t_out.cpu().numpy(), mask
+
+
 def entropy64(p: np.ndarray) -> np.ndarray:
     return scipy.special.entr(p.astype(np.float64)).sum(axis=-1)
 
