@@ -470,12 +470,67 @@ def time_e2e(torch, make_slot, step, stream, e_steps: int) -> dict:
     return {"pipelined": run(e_steps, True), "serial": run(e_steps, False)}
 
 
-def e2e_entry(value: float, ms: dict, h2d: int, d2h: int) -> dict:
-    return {"value": value, "unit": "rows/s", "ms_per_step": ms["pipelined"],
-            "ms_per_step_serial": ms["serial"],
-            "pipeline": f"{E2E_SLOTS} streams, one buffer set each; "
-                        "every step copies its inputs in and its result out",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+def pinned_copy_gbs(torch, dev, nbytes: int = 1 << 28) -> dict:
+    """Bandwidth of one large cudaMemcpyAsync between pinned host memory and
+    the device, each direction alone and both at once on two streams (best
+    of 3, CUDA events): the ceiling of the e2e steps' copies."""
+    h = torch.empty(nbytes // 4, dtype=torch.float32).pin_memory()
+    h2 = torch.empty(nbytes // 4, dtype=torch.float32).pin_memory()
+    d = torch.empty(nbytes // 4, dtype=torch.float32, device=dev)
+    d2 = torch.empty(nbytes // 4, dtype=torch.float32, device=dev)
+    s1, s2 = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def best(fn) -> float:
+        t = []
+        for _ in range(3):
+            torch.cuda.synchronize()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            s1.wait_event(a)
+            s2.wait_event(a)
+            fn()
+            torch.cuda.current_stream().wait_stream(s1)
+            torch.cuda.current_stream().wait_stream(s2)
+            b.record()
+            b.synchronize()
+            t.append(a.elapsed_time(b) * 1e-3)
+        return min(t)
+
+    def h2d():
+        with torch.cuda.stream(s1):
+            d.copy_(h, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s2):
+            h2.copy_(d2, non_blocking=True)
+
+    def both():
+        h2d()
+        d2h()
+
+    out = {"h2d_gbs": nbytes / best(h2d) / 1e9,
+           "d2h_gbs": nbytes / best(d2h) / 1e9,
+           "both_gbs": 2 * nbytes / best(both) / 1e9,
+           "bytes": nbytes}
+    del h, h2, d, d2
+    return out
+
+
+def e2e_entry(value: float, ms: dict, h2d: int, d2h: int,
+              copy_bw: dict | None = None) -> dict:
+    out = {"value": value, "unit": "rows/s", "ms_per_step": ms["pipelined"],
+           "ms_per_step_serial": ms["serial"],
+           "pipeline": f"{E2E_SLOTS} streams, one buffer set each; "
+                       "every step copies its inputs in and its result out",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    if copy_bw:
+        out["pinned_copy"] = copy_bw
+        # The step's copies alone at the measured pinned-copy bandwidth.
+        out["copy_bound_ms"] = 1e3 * max(
+            h2d / (copy_bw["h2d_gbs"] * 1e9), d2h / (copy_bw["d2h_gbs"] * 1e9),
+            (h2d + d2h) / (copy_bw["both_gbs"] * 1e9))
+    return out
 
 
 # ---------------------------------------------------------------- our arm
@@ -559,6 +614,7 @@ def our_arm(args, w: wl.Workload) -> int:
     e2e = time_e2e(torch, make_slot, e2e_step, stream, max(1, args.e2e_steps))
     e2e = {k: reduce_max(dist, v, dev) for k, v in e2e.items()}
     e2e_value = aggregate_rows_per_s(B, world, e2e["pipelined"] * 1e-3)
+    copy_bw = pinned_copy_gbs(torch, dev)
 
     # The exponentials the kernel issues: one untimed launch with the
     # per-row evaluation counts (the search is deterministic, so every timed
@@ -623,7 +679,8 @@ def our_arm(args, w: wl.Workload) -> int:
                            variant=args.variant, strict=args.strict,
                            plan=plan),
             "roofline": roof, "cpu_baseline": cpu,
-            "e2e": e2e_entry(e2e_value, e2e, 4 * elems, 4 * elems + 4 * B),
+            "e2e": e2e_entry(e2e_value, e2e, 4 * elems, 4 * elems + 4 * B,
+                             copy_bw),
             "gpu_launches": args.steps,
             "clocks": clocks,
             "device_errors": sorted(err),

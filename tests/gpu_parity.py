@@ -117,10 +117,13 @@ def t_tolerance(T: float, t_min: float, t_max: float, max_iter: int) -> float:
 
 def compare(x: np.ndarray, p_gpu: np.ndarray, T_gpu: np.ndarray, mask: int,
             ref: oracle.Result, entropy_bound=0.2, t_min=0.01, t_max=10.0,
-            max_iter=20, check_mask=True) -> dict:
+            max_iter=20, check_mask=True, p_slack=None) -> dict:
     """Asserts parity row by row; returns summary statistics (the
     T_zone count, rows accepted by the third temperature case, is always
-    0 for max_iter <= FINE_GRID_ITERS)."""
+    0 for max_iter <= FINE_GRID_ITERS).  p_slack (per row, optional) widens
+    the probability tolerance to P_TOL + p_slack[b] * p element by element,
+    for callers whose GPU logits differ from the oracle's by a known
+    rounding."""
     B = x.shape[0]
     bound32 = float(np.float32(entropy_bound))
     tmin32 = float(np.float32(t_min))
@@ -165,8 +168,14 @@ def compare(x: np.ndarray, p_gpu: np.ndarray, T_gpu: np.ndarray, mask: int,
                     f"H(T_gpu+w)-bound={H_up - bound32:.3g}")
                 stats["T_zone"] += 1
             p_ref = oracle.softmax(x[b], Tg)
-        dp = float(np.max(np.abs(p_gpu[b].astype(np.float64) - p_ref)))
-        assert dp <= P_TOL, f"row {b}: max |dp| = {dp:.3g}"
+        err = np.abs(p_gpu[b].astype(np.float64) - p_ref)
+        dp = float(np.max(err))
+        if p_slack is None:
+            assert dp <= P_TOL, f"row {b}: max |dp| = {dp:.3g}"
+        else:
+            lim = P_TOL + float(p_slack[b]) * p_ref
+            assert np.all(err <= lim), (
+                f"row {b}: |dp| {dp:.3g} above {P_TOL} + {float(p_slack[b]):.3g} p")
         Hg = float(entropy64(p_gpu[b]))
         Hr = float(entropy64(p_ref))
         dH = abs(Hg - Hr)
