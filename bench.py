@@ -432,7 +432,7 @@ def time_launches(args, torch, launch, stream, dist, local) -> dict:
 
 
 # -------------------------------------------------------------------- e2e
-E2E_SLOTS = 2
+E2E_SLOTS = 3
 
 
 def time_e2e(torch, make_slot, step, stream, e_steps: int) -> dict:
