@@ -53,6 +53,22 @@ bienc_kernel(BiencTask t, int tiles, int tiles_per_cta) {
     const float* kg = t.k + bh * K * D;
     const float* vg = t.v + bh * K * D;
 
+    // A tile's queries go into qs by 16-byte asynchronous copies (D is a
+    // multiple of 4 and the bases are 16-byte aligned), issued as soon as
+    // the previous tile's queries have been read, so that they land while
+    // that tile searches and accumulates its outputs.
+    const int D4 = D >> 2;
+    auto stage_queries = [&](int tile) {
+        const int i0 = tile * R;
+        const int nrows = min(R, t.Q - i0);
+        const float* qg = t.q + (bh * t.Q + i0) * D;
+        for (int e = threadIdx.x; e < nrows * D4; e += blockDim.x) {
+            const int r = e / D4, c4 = e - r * D4;
+            cp_async16(sm.qs + r * (D + 4) + 4 * c4, qg + r * D + 4 * c4);
+        }
+    };
+    if (tile0 < tile1) stage_queries(tile0);
+
     // Stage the keys (transposed, zero past K) and values of bh once.
     for (int e = threadIdx.x; e < K * D; e += blockDim.x)
         sm.kt[(e % D) * kp + e / D] = __ldg(kg + e);
@@ -63,11 +79,9 @@ bienc_kernel(BiencTask t, int tiles, int tiles_per_cta) {
     for (int tile = tile0; tile < tile1; ++tile) {
         const int i0 = tile * R;
         const int nrows = min(R, t.Q - i0);
-        const float* qg = t.q + (bh * t.Q + i0) * D;
-        // The tile's queries (the previous tile's readers are done: the
-        // __syncthreads at the end of the loop).
-        for (int e = threadIdx.x; e < nrows * D; e += blockDim.x)
-            sm.qs[(e / D) * (D + 4) + e % D] = __ldcs(qg + e);
+        // This thread's copies of the tile's queries have landed; after the
+        // barrier every thread's have (and the keys and values are staged).
+        cp_async_wait_all();
         __syncthreads();
 
         const int lane = threadIdx.x & 31;
@@ -119,13 +133,17 @@ bienc_kernel(BiencTask t, int tiles, int tiles_per_cta) {
             }
             y[i] = make_float4(s[0], s[1], s[2], s[3]);
         }
+        // Every thread has read its query row: the next tile's queries may
+        // overwrite qs while this tile goes on.
+        __syncthreads();
+        if (tile + 1 < tile1) stage_queries(tile + 1);
 
         // Step 2: the row's constrained softmax.
         const SearchCfg cfg{t.t_min, t.hi0, t.entropy_bound,
                             t.entropy_bound * kLog2e,
                             t.entropy_bound > 0.0f ? lg2_approx(t.entropy_bound) : 0.0f,
                             make_grid(t.t_min, fmaxf(t.hi0, t.t_min), t.max_iter)};
-        RowSolution sol{NAN, 0.0f, 0.0f, 0u, true};
+        RowSolution sol{NAN, 0.0f, 0.0f, 0u, 0, true};
         if (live)   // uniform over the lane group
             sol = solve_row<G, kBiencE4>(y, m, bad, cfg, t.entropy_bound * kLog2e,
                                          false, gmask);
@@ -166,7 +184,9 @@ bienc_kernel(BiencTask t, int tiles, int tiles_per_cta) {
                 raise_error(t.err, sol.bits);
             }
         }
-        __syncthreads();
+        // The weights row (ps) is read only by its own lane group (after its
+        // __syncwarp), and the next tile's qs is guarded by the barrier at
+        // the top of the loop: no barrier here.
     }
 }
 
