@@ -69,12 +69,23 @@ bienc_kernel(BiencTask t, int tiles, int tiles_per_cta) {
     };
     if (tile0 < tile1) stage_queries(tile0);
 
-    // Stage the keys (transposed, zero past K) and values of bh once.
-    for (int e = threadIdx.x; e < K * D; e += blockDim.x)
-        sm.kt[(e % D) * kp + e / D] = __ldg(kg + e);
+    // Stage the keys (transposed, zero past K) and values of bh once.  A
+    // thread reads four consecutive d of one key (16 bytes) and writes them
+    // to four rows of the transposed buffer; consecutive threads take
+    // consecutive keys, so each of those shared stores hits 32 different
+    // banks.  The values are copied as they are, 16 bytes at a time.
+    for (int e = threadIdx.x; e < K * D4; e += blockDim.x) {
+        const int j = e % K, c4 = e / K;
+        const float4 kv = __ldg(reinterpret_cast<const float4*>(kg + j * D) + c4);
+        sm.kt[(4 * c4 + 0) * kp + j] = kv.x;
+        sm.kt[(4 * c4 + 1) * kp + j] = kv.y;
+        sm.kt[(4 * c4 + 2) * kp + j] = kv.z;
+        sm.kt[(4 * c4 + 3) * kp + j] = kv.w;
+    }
     for (int e = threadIdx.x; e < D * (kp - K); e += blockDim.x)
         sm.kt[(e / (kp - K)) * kp + K + e % (kp - K)] = 0.0f;
-    for (int e = threadIdx.x; e < K * D; e += blockDim.x) sm.vs[e] = __ldg(vg + e);
+    for (int e = threadIdx.x; e < K * D4; e += blockDim.x)
+        cp_async16(sm.vs + 4 * e, vg + 4 * e);
 
     for (int tile = tile0; tile < tile1; ++tile) {
         const int i0 = tile * R;
