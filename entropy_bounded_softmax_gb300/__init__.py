@@ -253,10 +253,12 @@ def biencoder_attention(query, keys, values, scale=None,
                         t_max: float = DEFAULT_T_MAX,
                         max_iter: int = DEFAULT_MAX_ITER, out=None,
                         return_attn: bool = False, return_t: bool = False,
-                        lanes: int = 0):
-    """Section 2.5 biencoder_attention, fused: scores = query @ keys^T *
-    scale (default 1/sqrt(d_head)), the constrained softmax of every score
-    row, then attn @ values.  query [B, H, Q, D], keys and values
+                        lanes: int = 0, fused: bool = False):
+    """Section 2.5 biencoder_attention: scores = query @ keys^T * scale
+    (default 1/sqrt(d_head)), the constrained softmax of every score row,
+    then attn @ values (on the tensor cores for d_head <= 64 and
+    context_len <= d_head unless ``fused``, which runs all three steps in
+    one kernel on the FMA pipes).  query [B, H, Q, D], keys and values
     [B, H, K, D], CUDA fp32 contiguous.  Returns the output [B, H, Q, D]
     (and the weights [B, H, Q, K] and temperatures [B, H, Q] when asked).
     Asynchronous on the current stream."""
@@ -282,7 +284,9 @@ def biencoder_attention(query, keys, values, scale=None,
                            device=query.device)
     if return_t:
         t = torch.empty((B, H, Q), dtype=torch.float32, device=query.device)
-    opt = options(VARIANTS["rowgroup"] if lanes else 0, lanes, 0, 0)
+    variant = (CONSTANTS["CS_VARIANT_FUSED"] if fused
+               else VARIANTS["rowgroup"] if lanes else 0)
+    opt = options(variant, lanes, 0, 0)
     with torch.cuda.device(query.device):
         st = cs_biencoder_attention_ex(
             query.data_ptr(), keys.data_ptr(), values.data_ptr(),

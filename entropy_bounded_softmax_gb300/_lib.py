@@ -41,6 +41,7 @@ class cs_plan(ctypes.Structure):
         ("ctas_per_sm", ctypes.c_int32),
         ("grid_ctas", ctypes.c_int64),
         ("staged_tensors", ctypes.c_int32),
+        ("tensor_cores", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

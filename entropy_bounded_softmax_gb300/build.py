@@ -20,7 +20,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIBRARY = os.path.join(PKG, "libcsoftmax.so")
 
 SOURCES = ["cs_api.cu", "k_cluster.cu", "k_rowgroup.cu", "k_backward.cu",
-           "k_attention.cu", "k_bienc.cu", "k_aux.cu"]
+           "k_attention.cu", "k_bienc.cu", "k_bienc_pv.cu", "k_aux.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-I", INCLUDE, "-I", CSRC]

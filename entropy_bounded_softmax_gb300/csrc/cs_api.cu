@@ -902,15 +902,27 @@ cs_status cs_plan_biencoder_host(int32_t batch_size, int32_t query_len,
         if (o.param != 0) return CS_ERR_INVALID_ARG;
         G = 1;
         while (8 * G < context_len) G <<= 1;
-    } else if (o.variant == CS_VARIANT_ROWGROUP) {
+    } else if (o.variant == CS_VARIANT_ROWGROUP || o.variant == CS_VARIANT_FUSED) {
         G = o.param;
+        if (o.variant == CS_VARIANT_FUSED && G == 0) {
+            G = 1;
+            while (8 * G < context_len) G <<= 1;
+        }
         if (G < 1 || G > kRowgroupMaxLanes || (G & (G - 1)))
             return CS_ERR_INVALID_ARG;
         if (8 * G < context_len) return CS_ERR_OOM;
     } else {
         return CS_ERR_INVALID_ARG;
     }
-    const int64_t smem = cs::bienc_smem_bytes(context_len, d_head, G);
+    // Step 3 on the tensor cores (a second kernel) unless forced fused:
+    // for head sizes up to kPvMaxD and contexts no longer than the head, so
+    // that the weights fit in the output's own rows when attn_out is not
+    // requested.
+    const bool tc = o.variant != CS_VARIANT_FUSED && d_head <= cs::kPvMaxD &&
+                    context_len <= d_head &&
+                    cs::pv_smem_bytes(cs::pv_np(d_head)) <= smem_per_block_optin;
+    const int64_t smem = tc ? cs::bienc_search_smem_bytes(context_len, d_head, G)
+                            : cs::bienc_smem_bytes(context_len, d_head, G);
     if (smem > smem_per_block_optin) return CS_ERR_OOM;
     const int64_t rows_per_tile = cs::bienc_threads(G) / G;
     const int64_t tiles = ceil_div(query_len, rows_per_tile);
@@ -925,7 +937,8 @@ cs_status cs_plan_biencoder_host(int32_t batch_size, int32_t query_len,
     plan->threads_per_cta = cs::bienc_threads(G);
     plan->smem_bytes = static_cast<int32_t>(smem);
     plan->grid_ctas = grid;
-    plan->staged_tensors = 3;
+    plan->staged_tensors = tc ? 2 : 3;
+    plan->tensor_cores = tc ? 1 : 0;
     return CS_OK;
 }
 
@@ -971,8 +984,34 @@ cs_status cs_biencoder_attention_ex(const float* query,
     task.t_min = t_min;
     task.hi0 = t_max < 1.0f ? t_max : 1.0f;
     task.max_iter = max_iter;
-    const cudaError_t e = cs::launch_bienc(task, p.lanes_per_row, p.smem_bytes,
-                                           static_cast<cudaStream_t>(stream));
+    task.p_out = nullptr;
+    task.p_stride = 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (p.tensor_cores) {
+        // Steps 1-2 write the weights (to attn_out, or to the first
+        // context_len floats of each output row), then the tensor-core
+        // kernel turns them into the output on the same stream.
+        task.p_out = attn_out ? attn_out : output;
+        task.p_stride = attn_out ? context_len : d_head;
+        e = cs::launch_bienc(task, p.lanes_per_row, p.smem_bytes, s);
+        if (e == cudaSuccess) {
+            cs::PvTask pv;
+            pv.p = task.p_out;
+            pv.p_stride = task.p_stride;
+            pv.v = context_values;
+            pv.out = output;
+            pv.err = d->err;
+            pv.BH = task.BH;
+            pv.Q = query_len;
+            pv.K = context_len;
+            pv.D = d_head;
+            pv.wait_limit_cycles = cs::kWaitLimitCycles;
+            e = cs::launch_bienc_pv(pv, s);
+        }
+    } else {
+        e = cs::launch_bienc(task, p.lanes_per_row, p.smem_bytes, s);
+    }
     if (e != cudaSuccess) {
         cudaGetLastError();
         return CS_ERR_CUDA;

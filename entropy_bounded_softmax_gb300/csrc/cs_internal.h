@@ -175,6 +175,8 @@ struct BiencTask {
     float t_min;
     float hi0;             // min(1, t_max)
     int32_t max_iter;
+    float* p_out;          // non-null: steps 1-2 only, weights written here
+    int64_t p_stride;      // floats between weight rows in p_out
 };
 
 // biencoder_attention geometry: G lanes per query row holding eight
@@ -199,6 +201,14 @@ inline int64_t bienc_smem_bytes(int K, int D, int G) {
                 R * (kp + 4));
 }
 
+// Shared memory of the scores-and-search kernel when step 3 runs on the
+// tensor cores: the transposed keys and a tile of queries only.
+inline int64_t bienc_search_smem_bytes(int K, int D, int G) {
+    const int64_t R = bienc_threads(G) / G;
+    const int64_t kp = bienc_kp(K);
+    return 4 * (D * kp + R * (D + 4));
+}
+
 // Query tiles one CTA works through with its staged keys and values:
 // about 128 query rows, at most the pair's whole query range.
 inline int bienc_tiles_per_cta(int Q, int G) {
@@ -211,6 +221,55 @@ inline int bienc_tiles_per_cta(int Q, int G) {
 
 cudaError_t launch_bienc(const BiencTask& task, int lanes_per_row,
                          int smem_bytes, cudaStream_t stream);
+
+// biencoder_attention's step 3 on the tensor cores (k_bienc_pv.cu): out =
+// P . V for every bh, P written before by the scores-and-search kernel
+// (into attn_out, or into the first K floats of each output row).
+struct PvTask {
+    const float* p;        // P rows: p + (bh Q + i) p_stride
+    int64_t p_stride;      // floats between P rows (K or D)
+    const float* v;        // [BH, K, D]
+    float* out;            // [BH, Q, D]
+    unsigned int* err;     // device error word
+    int32_t BH;
+    int32_t Q;
+    int32_t K;
+    int32_t D;
+    uint64_t wait_limit_cycles;
+};
+
+constexpr int kPvM = 128;               // query rows per CTA (the MMA's M)
+constexpr int kPvKc = 32;               // context items per shared-memory chunk
+                                        // (48 KB at N = 64: four CTAs per SM)
+constexpr uint32_t kPvTmemCols = 64;    // tensor-memory columns per CTA (N <= 64)
+constexpr int kPvMaxD = 64;             // head sizes the tensor-core step takes
+constexpr int kPvSmemPad = 0;           // slack after the operands
+
+// N of the MMA: d_head rounded up to 16.
+__host__ __device__ inline int pv_np(int D) { return (D + 15) & ~15; }
+
+// Byte offsets of the step-3 kernel's shared memory: the TF32 halves of P
+// (128 x 64) and of V^T (N x 64), the completion mbarrier and the word that
+// receives the tensor-memory address.
+struct PvSmemLayout {
+    int a_hi, a_lo, b_hi, b_lo, bar, tslot, end;
+};
+
+__host__ __device__ inline PvSmemLayout pv_smem_layout(int Np) {
+    PvSmemLayout L;
+    L.a_hi = 0;
+    L.a_lo = kPvM * kPvKc * 4;
+    L.b_hi = 2 * kPvM * kPvKc * 4;
+    L.b_lo = L.b_hi + Np * kPvKc * 4;
+    L.bar = L.b_lo + Np * kPvKc * 4;
+    L.tslot = L.bar + 8;
+    L.end = L.tslot + 8 + kPvSmemPad;
+    return L;
+}
+
+inline int64_t pv_smem_bytes(int Np) { return pv_smem_layout(Np).end; }
+
+cudaError_t launch_bienc_pv(const PvTask& task, cudaStream_t stream);
 
 cudaError_t launch_rowgroup(const RowTask& task, int lanes_per_row,
                             int elems_per_lane, cudaStream_t stream);

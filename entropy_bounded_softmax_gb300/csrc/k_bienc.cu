@@ -28,12 +28,16 @@ constexpr int kBiencE4 = 2;   // float4s of keys per lane: 8 keys
 
 struct BiencSmem {
     float* kt;   // [D][kp] keys, transposed
-    float* vs;   // [K][D] values
+    float* vs;   // [K][D] values (STEP3)
     float* qs;   // [R][D + 4] query rows
-    float* ps;   // [R][kp + 4] attention weights
+    float* ps;   // [R][kp + 4] attention weights (STEP3)
 };
 
-template <int G>
+// STEP3: all three steps (the fp32 FMA contraction of step 3 included);
+// otherwise steps 1 and 2 only, the weights written to t.p_out (row
+// stride t.p_stride) for the tensor-core step 3 of k_bienc_pv.cu, and
+// neither the values nor the weights staged in shared memory.
+template <int G, bool STEP3>
 __global__ void __launch_bounds__(bienc_threads(G))
 bienc_kernel(BiencTask t, int tiles, int tiles_per_cta) {
     constexpr int R = bienc_threads(G) / G;
@@ -43,7 +47,7 @@ bienc_kernel(BiencTask t, int tiles, int tiles_per_cta) {
     BiencSmem sm;
     sm.kt = smem_f;
     sm.vs = sm.kt + D * kp;
-    sm.qs = sm.vs + K * D;
+    sm.qs = sm.vs + (STEP3 ? K * D : 0);
     sm.ps = sm.qs + R * (D + 4);
 
     const int ctas_per_bh = (tiles + tiles_per_cta - 1) / tiles_per_cta;
@@ -84,8 +88,9 @@ bienc_kernel(BiencTask t, int tiles, int tiles_per_cta) {
     }
     for (int e = threadIdx.x; e < D * (kp - K); e += blockDim.x)
         sm.kt[(e / (kp - K)) * kp + K + e % (kp - K)] = 0.0f;
-    for (int e = threadIdx.x; e < K * D4; e += blockDim.x)
-        cp_async16(sm.vs + 4 * e, vg + 4 * e);
+    if (STEP3)
+        for (int e = threadIdx.x; e < K * D4; e += blockDim.x)
+            cp_async16(sm.vs + 4 * e, vg + 4 * e);
 
     for (int tile = tile0; tile < tile1; ++tile) {
         const int i0 = tile * R;
@@ -168,10 +173,22 @@ bienc_kernel(BiencTask t, int tiles, int tiles_per_cta) {
                 const int j = 4 * (i * G + sub) + c;
                 if (live && j < K) {
                     const float p = sol.zero ? 0.0f : ex2(yy[c] * sol.beta_out) * sol.inv_s;
-                    pr[j] = p;
-                    if (t.attn_out) __stcs(t.attn_out + row * K + j, p);
+                    if (STEP3) {
+                        pr[j] = p;
+                        if (t.attn_out) __stcs(t.attn_out + row * K + j, p);
+                    } else {
+                        // Read back by the step-3 kernel moments later (L2).
+                        t.p_out[row * t.p_stride + j] = p;
+                    }
                 }
             }
+        }
+        if (!STEP3) {
+            if (live && sub == 0) {
+                if (t.t_out) t.t_out[row] = sol.T_row;
+                raise_error(t.err, sol.bits);
+            }
+            continue;
         }
         __syncwarp(gmask);
 
@@ -201,10 +218,9 @@ bienc_kernel(BiencTask t, int tiles, int tiles_per_cta) {
     }
 }
 
-}  // namespace
-
-cudaError_t launch_bienc(const BiencTask& task, int lanes_per_row,
-                         int smem_bytes, cudaStream_t stream) {
+template <bool STEP3>
+cudaError_t launch_bienc_as(const BiencTask& task, int lanes_per_row,
+                            int smem_bytes, cudaStream_t stream) {
     const int rows_per_tile = bienc_threads(lanes_per_row) / lanes_per_row;
     const int tiles = (task.Q + rows_per_tile - 1) / rows_per_tile;
     const int tiles_per_cta = bienc_tiles_per_cta(task.Q, lanes_per_row);
@@ -212,29 +228,39 @@ cudaError_t launch_bienc(const BiencTask& task, int lanes_per_row,
                          ((tiles + tiles_per_cta - 1) / tiles_per_cta);
     const void* kern = nullptr;
     switch (lanes_per_row) {
-        case 1: kern = reinterpret_cast<const void*>(bienc_kernel<1>); break;
-        case 2: kern = reinterpret_cast<const void*>(bienc_kernel<2>); break;
-        case 4: kern = reinterpret_cast<const void*>(bienc_kernel<4>); break;
-        case 8: kern = reinterpret_cast<const void*>(bienc_kernel<8>); break;
-        case 16: kern = reinterpret_cast<const void*>(bienc_kernel<16>); break;
-        case 32: kern = reinterpret_cast<const void*>(bienc_kernel<32>); break;
+        case 1: kern = reinterpret_cast<const void*>(bienc_kernel<1, STEP3>); break;
+        case 2: kern = reinterpret_cast<const void*>(bienc_kernel<2, STEP3>); break;
+        case 4: kern = reinterpret_cast<const void*>(bienc_kernel<4, STEP3>); break;
+        case 8: kern = reinterpret_cast<const void*>(bienc_kernel<8, STEP3>); break;
+        case 16: kern = reinterpret_cast<const void*>(bienc_kernel<16, STEP3>); break;
+        case 32: kern = reinterpret_cast<const void*>(bienc_kernel<32, STEP3>); break;
         default: return cudaErrorInvalidValue;
     }
-    // One attribute slot per lane count (13..18).
-    int slot = 13;
+    // One attribute slot per lane count: 13..18 (all three steps), 28..33
+    // (steps 1 and 2).
+    int slot = STEP3 ? 13 : 28;
     for (int g = lanes_per_row; g > 1; g >>= 1) ++slot;
     cudaError_t e = ensure_smem_attribute(kern, slot, smem_bytes, false);
     if (e != cudaSuccess) return e;
     const dim3 gd(static_cast<unsigned>(grid)), bd(bienc_threads(lanes_per_row));
     switch (lanes_per_row) {
-        case 1: bienc_kernel<1><<<gd, bd, smem_bytes, stream>>>(task, tiles, tiles_per_cta); break;
-        case 2: bienc_kernel<2><<<gd, bd, smem_bytes, stream>>>(task, tiles, tiles_per_cta); break;
-        case 4: bienc_kernel<4><<<gd, bd, smem_bytes, stream>>>(task, tiles, tiles_per_cta); break;
-        case 8: bienc_kernel<8><<<gd, bd, smem_bytes, stream>>>(task, tiles, tiles_per_cta); break;
-        case 16: bienc_kernel<16><<<gd, bd, smem_bytes, stream>>>(task, tiles, tiles_per_cta); break;
-        default: bienc_kernel<32><<<gd, bd, smem_bytes, stream>>>(task, tiles, tiles_per_cta); break;
+        case 1: bienc_kernel<1, STEP3><<<gd, bd, smem_bytes, stream>>>(task, tiles, tiles_per_cta); break;
+        case 2: bienc_kernel<2, STEP3><<<gd, bd, smem_bytes, stream>>>(task, tiles, tiles_per_cta); break;
+        case 4: bienc_kernel<4, STEP3><<<gd, bd, smem_bytes, stream>>>(task, tiles, tiles_per_cta); break;
+        case 8: bienc_kernel<8, STEP3><<<gd, bd, smem_bytes, stream>>>(task, tiles, tiles_per_cta); break;
+        case 16: bienc_kernel<16, STEP3><<<gd, bd, smem_bytes, stream>>>(task, tiles, tiles_per_cta); break;
+        default: bienc_kernel<32, STEP3><<<gd, bd, smem_bytes, stream>>>(task, tiles, tiles_per_cta); break;
     }
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bienc(const BiencTask& task, int lanes_per_row,
+                         int smem_bytes, cudaStream_t stream) {
+    return task.p_out
+        ? launch_bienc_as<false>(task, lanes_per_row, smem_bytes, stream)
+        : launch_bienc_as<true>(task, lanes_per_row, smem_bytes, stream);
 }
 
 }  // namespace cs

@@ -64,6 +64,9 @@ typedef int32_t cs_status;
 #define CS_VARIANT_CLUSTER 2  /* 1-16 CTAs per row, row in shared memory,
                                  partial sums exchanged over DSMEM; one CTA
                                  per row when the cluster size is 1        */
+#define CS_VARIANT_FUSED 3    /* biencoder_attention: all three steps in
+                                 one kernel, step 3 on the fp32 FMA pipes
+                                 (param = lanes per query row, 0 = auto)  */
 
 /* Largest num_classes the library accepts: a 16-CTA cluster holding the row
  * in shared memory. */
@@ -115,7 +118,10 @@ typedef struct cs_plan {
                                 backward: 2, p and grad_out, or 1, p alone,
                                 with grad_out read again; attention row-CTA:
                                 1; biencoder: 3, keys, values and a tile of
-                                queries); rowgroup: 0                      */
+                                queries, or 2, keys and queries, when step 3
+                                runs on the tensor cores); rowgroup: 0     */
+    int32_t tensor_cores;    /* biencoder: 1 when attn . V runs as a second
+                                kernel on the tensor cores (tcgen05.mma)  */
 } cs_plan;
 
 /*
@@ -419,7 +425,18 @@ cs_status cs_check_attention_args(const float* scores, const float* out,
  *
  * The four bases must be 16-byte aligned (float4 staging); otherwise
  * CS_ERR_INVALID_ARG.  Ownership, execution, errors: as
- * cs_constrained_softmax; no intermediate goes to global memory.
+ * cs_constrained_softmax.
+ *
+ * Kernels.  For d_head <= 64 and context_len <= d_head (the page's shape),
+ * steps 1 and 2 run in one kernel that writes the weights, and step 3
+ * (attn @ context_values) runs in a second kernel on the tensor cores
+ * (tcgen05.mma, TF32 operands, three TF32 products per fp32 product for
+ * fp32 accuracy, fp32 accumulation in tensor memory).  The weights pass
+ * through attn_out when it is given, otherwise through the output buffer
+ * itself (the first context_len floats of each output row, overwritten by
+ * the result): no scratch memory is used.  Other shapes, and
+ * CS_VARIANT_FUSED, run all three steps in one kernel on the fp32 FMA
+ * pipes, with nothing between the steps in global memory.
  */
 cs_status cs_biencoder_attention(const float* query,
                                  const float* context_keys,
@@ -433,9 +450,10 @@ cs_status cs_biencoder_attention(const float* query,
  * The same with the search parameters of cs_constrained_softmax and two
  * optional outputs: attn_out [batch, num_heads, query_len, context_len]
  * (the weights of step 2) and t_out [batch, num_heads, query_len] (each
- * row's temperature), either may be NULL.  options: CS_VARIANT_AUTO or
+ * row's temperature), either may be NULL.  options: CS_VARIANT_AUTO,
  * CS_VARIANT_ROWGROUP with param = lanes per query row (a power of two,
- * 8 x lanes >= context_len); threads and strict must be 0.
+ * 8 x lanes >= context_len), or CS_VARIANT_FUSED (one kernel; param as
+ * for ROWGROUP, 0 = automatic); threads and strict must be 0.
  */
 cs_status cs_biencoder_attention_ex(const float* query,
                                     const float* context_keys,

@@ -22,24 +22,31 @@ from gpu_parity import compare
 
 
 def run_biencoder(q, k, v, scale, entropy_bound=0.2, t_min=0.01, t_max=10.0,
-                  max_iter=20, lanes=0):
-    """The CUDA path through the C ABI; returns (out, attn, T, error mask)."""
+                  max_iter=20, lanes=0, fused=False, return_attn=True):
+    """The CUDA path through the C ABI; returns (out, attn, T, error mask)
+    (attn None when not requested: then the weights pass through the
+    output buffer on the tensor-core path)."""
     import torch
     import entropy_bounded_softmax_gb300 as cs
     dev = torch.device("cuda", 0)
     qd, kd, vd = (torch.from_numpy(np.ascontiguousarray(a)).to(dev)
                   for a in (q, k, v))
     cs.get_error()
-    out, attn, T = cs.biencoder_attention(qd, kd, vd, scale, entropy_bound,
-                                          t_min, t_max, max_iter,
-                                          return_attn=True, return_t=True,
-                                          lanes=lanes)
+    res = cs.biencoder_attention(qd, kd, vd, scale, entropy_bound,
+                                 t_min, t_max, max_iter,
+                                 return_attn=return_attn, return_t=True,
+                                 lanes=lanes, fused=fused)
+    if return_attn:
+        out, attn, T = res
+    else:
+        (out, T), attn = res, None
     bits = cs.get_error()
     mask = 0
     for name, bit in cs.ERROR_BITS.items():
         if name in bits:
             mask |= bit
-    return out.cpu().numpy(), attn.cpu().numpy(), T.cpu().numpy(), mask
+    return (out.cpu().numpy(), None if attn is None else attn.cpu().numpy(),
+            T.cpu().numpy(), mask)
 
 
 def compare_biencoder(q, k, v, scale, out, attn, T, mask, entropy_bound=0.2,

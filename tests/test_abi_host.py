@@ -435,3 +435,21 @@ def test_evaluation_counts_only_for_the_forward():
     assert st == C["CS_ERR_INVALID_ARG"]
     st, _ = cs.cs_plan_biencoder_host(1, 8, 64, 64, 1, opt, 232448)
     assert st == C["CS_ERR_INVALID_ARG"]
+
+
+def test_biencoder_plans_step3_on_the_tensor_cores():
+    """The page's shape (64 context items, d_head 64) runs step 3 as a
+    tensor-core kernel; a longer context, a larger head or the fused
+    variant run one kernel."""
+    def bplan(K, D, opt=None):
+        st, p = cs.cs_plan_biencoder_host(32, 512, K, D, 8, opt, 232448)
+        assert st == 0
+        return p.as_dict()
+    p = bplan(64, 64)
+    assert p["tensor_cores"] == 1 and p["staged_tensors"] == 2
+    assert bplan(12, 12)["tensor_cores"] == 1
+    assert bplan(256, 64)["tensor_cores"] == 0      # context longer than the head
+    assert bplan(64, 128)["tensor_cores"] == 0      # head above 64
+    fused = bplan(64, 64, cs.options(C["CS_VARIANT_FUSED"], 0))
+    assert fused["tensor_cores"] == 0 and fused["staged_tensors"] == 3
+    assert fused["lanes_per_row"] == p["lanes_per_row"] == 8

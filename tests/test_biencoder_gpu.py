@@ -124,3 +124,31 @@ def test_argument_errors_and_empty():
     with pytest.raises(cs.CsError) as e:          # output overlaps query
         cs.biencoder_attention(q, k, k, out=q)
     assert e.value.status == 8
+
+
+@pytest.mark.parametrize("K,D", [(64, 64), (1, 4), (5, 12), (12, 12),
+                                 (33, 48), (16, 64)])
+@pytest.mark.parametrize("Q", [1, 127, 128, 300])
+def test_tensor_core_step3_matches_fused(K, D, Q):
+    """Step 3 on the tensor cores (three TF32 products, fp32 accumulation)
+    against the oracle, with and without attn_out (the weights then pass
+    through the output buffer), and against the fused fp32 kernel: same
+    weights and temperatures bit for bit (steps 1-2 are the same code), the
+    outputs within the fp32 accumulation's bound."""
+    import entropy_bounded_softmax_gb300 as cs
+    st, plan = cs.cs_plan_biencoder_host(2, Q, K, D, 3, None, 232448)
+    assert st == 0 and plan.tensor_cores == 1
+    q, k, v = _rand(2, 3, Q, K, D, 97 * K + D + Q, sigma=1.5)
+    scale = 1.0 / np.sqrt(D)
+    out_tc, attn_tc, T_tc, m_tc = run_biencoder(q, k, v, scale)
+    compare_biencoder(q, k, v, scale, out_tc, attn_tc, T_tc, m_tc)
+    out_nb, _, T_nb, m_nb = run_biencoder(q, k, v, scale, return_attn=False)
+    compare_biencoder(q, k, v, scale, out_nb, attn_tc, T_nb, m_nb)
+    out_f, attn_f, T_f, m_f = run_biencoder(q, k, v, scale, fused=True)
+    assert np.array_equal(attn_f, attn_tc) and np.array_equal(T_f, T_tc)
+    assert m_f == m_tc == m_nb
+    assert np.array_equal(T_nb, T_tc)
+    v64 = np.abs(v.astype(np.float64))
+    bound = 1e-5 * np.einsum("bhqk,bhkd->bhqd", attn_f.astype(np.float64), v64) + 1e-30
+    assert np.all(np.abs(out_tc.astype(np.float64) - out_f) <= 2 * bound)
+    assert np.array_equal(out_nb, out_tc)

@@ -81,5 +81,10 @@ def test_biencoder_smem(K, D):
     assert 8 * G >= K and (G == 1 or 4 * G < K)
     R = p["threads_per_cta"] // G
     kp = (K + 3) // 4 * 4
-    need = 4 * (D * kp + K * D + R * (D + 4) + R * (kp + 4))
+    if p["tensor_cores"]:
+        # steps 1-2 only (keys and a query tile); step 3 on the tensor cores
+        assert K <= D <= 64 and p["staged_tensors"] == 2
+        need = 4 * (D * kp + R * (D + 4))
+    else:
+        need = 4 * (D * kp + K * D + R * (D + 4) + R * (kp + 4))
     assert need == p["smem_bytes"] <= 232448
