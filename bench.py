@@ -220,6 +220,16 @@ def measured_peaks() -> dict:
         return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
 
 
+def measured_bf16_tflops() -> float:
+    """The measured dense bf16 GEMM rate (TFLOP/s) of this machine, else
+    the recorded fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except (OSError, KeyError, ValueError):
+        return 1900.0
+
+
 def probe_ex2_peak(torch, cs, stream_ptr) -> float:
     """ex2/s of the whole GPU from the probe kernel (best of 5)."""
     n = cs.cs_probe_ex2_sink_floats()
@@ -1384,10 +1394,18 @@ def bienc_arm(args, w) -> int:
         Hs = scipy.special.entr(pr).sum(axis=1)
         searched = float(np.mean(Hs > np.float32(w.entropy_bound))) * rows
         exps = (rows + searched * 20) * K
-        flops = 4.0 * rows * K * D
+        tc = bool(plan.get("tensor_cores"))
+        # Step 1 (and, on the fused path, step 3) on the fp32 FMA pipes;
+        # with the tensor-core step 3, its three TF32 products per fp32
+        # product at the TF32 rate (half the measured bf16 rate, the
+        # nominal ratio of the two).
+        flops = (2.0 if tc else 4.0) * rows * K * D
+        tc_flops = 3 * 2.0 * rows * K * D if tc else 0.0
+        tf32_peak = 0.5 * measured_bf16_tflops() * 1e12
         t_hbm = io_bytes / (peaks["hbm_gbs"] * 1e9)
         t_ex2 = exps / ex2_peak
         t_fma = flops / (FP32_SIMT_TFLOPS * 1e12)
+        t_tc = tc_flops / tf32_peak if tc else 0.0
         bound = max(("hbm", t_hbm), ("ex2", t_ex2), ("fma", t_fma),
                     key=lambda kv: kv[1])
         roof = {"bound": "hbm" if bound[0] == "hbm" else "alu",
@@ -1402,9 +1420,11 @@ def bienc_arm(args, w) -> int:
                 "kernel": "bienc_kernel", "algorithmic_bytes": io_bytes,
                 "algorithmic_ex2": exps, "algorithmic_flops": flops,
                 "roofline_us": {"hbm": t_hbm * 1e6, "ex2": t_ex2 * 1e6,
-                                "fma": t_fma * 1e6},
+                                "fma": t_fma * 1e6, "tensor_tf32": t_tc * 1e6},
+                "tensor_core_step3": tc, "tensor_flops": tc_flops,
                 "peak_source": "hbm: measured copy bandwidth; ex2: probe; "
-                               "fma: 152 SMs x 128 lanes x 2 flops x 2.07 GHz"}
+                               "fma: 152 SMs x 128 lanes x 2 flops x 2.07 GHz; "
+                               "tf32: half the measured bf16 GEMM rate"}
         cpu = None
         if not args.no_cpu_baseline:
             t0 = time.perf_counter()
@@ -1438,7 +1458,7 @@ def bienc_arm(args, w) -> int:
             "e2e": e2e_entry(e2e_value, e2e,
                              4 * (B * H * Q * D + 2 * B * H * K * D),
                              4 * B * H * Q * D),
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * (2 if plan.get("tensor_cores") else 1),
             "clocks": tm["sampler"].summary(tm["t0"], tm["t1"]),
             "device_errors": sorted(err),
         }
