@@ -256,6 +256,17 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
     return r;
 }
 
+// The two halves of cluster_sync(), for work in between: after
+// cluster_arrive() and cluster_wait(), every thread of the cluster has
+// passed its cluster_arrive() (release / acquire at cluster scope).
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n"
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");

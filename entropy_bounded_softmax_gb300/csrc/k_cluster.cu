@@ -39,9 +39,8 @@
 // Every wait is bounded (cs::kWaitLimitCycles by default).  A thread whose
 // wait times out records CS_ERR_TIMEOUT and from then on neither waits nor
 // pushes; the search then ends within its round limit on whatever the slots
-// hold, and before the kernel's final cluster barrier such a CTA sleeps for
-// a bounded while, so that pushes peers had already issued into it land
-// before it exits.
+// hold, and before exiting such a CTA sleeps for a bounded while, so that
+// pushes peers had already issued into it land first.
 #include <math.h>
 
 #include "cs_search.cuh"
@@ -531,7 +530,11 @@ cluster_kernel(RowTask t, int n, int slice_len) {
         fence_mbar_init();
     }
     __syncthreads();
-    if (CLUSTER) cluster_sync();
+    // Peers push into this CTA's slots only after every CTA's mbarriers are
+    // initialised: arrive now, wait just before the first exchange, so that
+    // the cluster barrier's latency overlaps the first row's staging.
+    if (CLUSTER) cluster_arrive();
+    bool waited = false;
 
     const int64_t C = t.num_classes;
     const int64_t s0 = static_cast<int64_t>(rank) * slice_len;
@@ -651,6 +654,10 @@ cluster_kernel(RowTask t, int n, int slice_len) {
         // and its NaN/Inf code: no separate exchange of the max.
         float s1[5];
         transform_pass(row4, s.q4, m_t, code, s1);
+        if (CLUSTER && !waited) {
+            cluster_wait();
+            waited = true;
+        }
         exchange<CLUSTER, OpSoftmax, 5>(s1, sm, x);
         const float m = s1[0];
         const int row_code = static_cast<int>(s1[4]);
@@ -714,13 +721,16 @@ cluster_kernel(RowTask t, int n, int slice_len) {
         __syncthreads();
     }
     if (CLUSTER) {
-        // After a timeout, give pushes that peers had already issued into
-        // this CTA's slots time to land before the CTA can exit (a bounded
-        // sleep: st.async completes within microseconds).
+        if (!waited) cluster_wait();
+        // No cluster barrier at the end: every CTA of the cluster runs the
+        // same exchanges, and once this CTA's last exchange has completed,
+        // every push into its slots has landed and no peer will touch them
+        // again.  After a timeout that no longer holds: give pushes that
+        // peers had already issued time to land before the CTA exits (a
+        // bounded sleep; st.async completes within microseconds).
         if (__syncthreads_or(x.dead)) {
             for (int i = 0; i < 1000; ++i) __nanosleep(1000);
         }
-        cluster_sync();
     }
 }
 
