@@ -897,23 +897,26 @@ cs_status cs_plan_biencoder_host(int32_t batch_size, int32_t query_len,
     if (d_head % 4 != 0) return CS_ERR_INVALID_ARG;
     const cs_options o = options ? *options : cs_options{};
     if (o.threads != 0 || o.strict != 0 || o.evals_out) return CS_ERR_INVALID_ARG;
+    // G lanes a query row, each holding `keys` context items: by default
+    // sixteen (the fewest lanes, so the fewest copies of each row's search
+    // bookkeeping); a forced G holds eight when that covers the context.
     int G = 0;
-    if (o.variant == CS_VARIANT_AUTO) {
+    if (o.variant == CS_VARIANT_AUTO ||
+        (o.variant == CS_VARIANT_FUSED && o.param == 0)) {
         if (o.param != 0) return CS_ERR_INVALID_ARG;
         G = 1;
-        while (8 * G < context_len) G <<= 1;
+        while (16 * G < context_len) G <<= 1;
     } else if (o.variant == CS_VARIANT_ROWGROUP || o.variant == CS_VARIANT_FUSED) {
         G = o.param;
-        if (o.variant == CS_VARIANT_FUSED && G == 0) {
-            G = 1;
-            while (8 * G < context_len) G <<= 1;
-        }
         if (G < 1 || G > kRowgroupMaxLanes || (G & (G - 1)))
             return CS_ERR_INVALID_ARG;
-        if (8 * G < context_len) return CS_ERR_OOM;
+        if (16 * G < context_len) return CS_ERR_OOM;
     } else {
         return CS_ERR_INVALID_ARG;
     }
+    const int keys = (o.variant == CS_VARIANT_AUTO ||
+                      (o.variant == CS_VARIANT_FUSED && o.param == 0) ||
+                      8 * G < context_len) ? 16 : 8;
     // Step 3 on the tensor cores (a second kernel) unless forced fused:
     // for head sizes up to kPvMaxD and contexts no longer than the head, so
     // that the weights fit in the output's own rows when attn_out is not
@@ -933,7 +936,7 @@ cs_status cs_plan_biencoder_host(int32_t batch_size, int32_t query_len,
     *plan = cs_plan{};
     plan->variant = CS_VARIANT_ROWGROUP;
     plan->lanes_per_row = G;
-    plan->elems_per_lane = 8;
+    plan->elems_per_lane = keys;
     plan->threads_per_cta = cs::bienc_threads(G);
     plan->smem_bytes = static_cast<int32_t>(smem);
     plan->grid_ctas = grid;
@@ -994,7 +997,7 @@ cs_status cs_biencoder_attention_ex(const float* query,
         // kernel turns them into the output on the same stream.
         task.p_out = attn_out ? attn_out : output;
         task.p_stride = attn_out ? context_len : d_head;
-        e = cs::launch_bienc(task, p.lanes_per_row, p.smem_bytes, s);
+        e = cs::launch_bienc(task, p.lanes_per_row, p.elems_per_lane, p.smem_bytes, s);
         if (e == cudaSuccess) {
             cs::PvTask pv;
             pv.p = task.p_out;
@@ -1010,7 +1013,7 @@ cs_status cs_biencoder_attention_ex(const float* query,
             e = cs::launch_bienc_pv(pv, s);
         }
     } else {
-        e = cs::launch_bienc(task, p.lanes_per_row, p.smem_bytes, s);
+        e = cs::launch_bienc(task, p.lanes_per_row, p.elems_per_lane, p.smem_bytes, s);
     }
     if (e != cudaSuccess) {
         cudaGetLastError();

@@ -179,12 +179,12 @@ struct BiencTask {
     int64_t p_stride;      // floats between weight rows in p_out
 };
 
-// biencoder_attention geometry: G lanes per query row holding eight
-// context items each (K <= 8 G <= 256), in CTAs of 256 threads, or 512 for
-// G >= 16 (a 256-item context: 16-row tiles instead of 8 made
-// 4 x 8 x 1024 x 256 x 64 24% faster; at G = 8 the larger CTAs were 3%
-// slower); keys transposed in shared memory with rows of kp (K rounded up
-// to 4) floats.
+// biencoder_attention geometry: G lanes per query row holding eight or
+// sixteen context items each (K <= 8 G or 16 G, G <= 32), in CTAs of 256
+// threads, or 512 for G >= 16 (a 256-item context: 16-row tiles instead of
+// 8 made 4 x 8 x 1024 x 256 x 64 24% faster; at G = 8 the larger CTAs were
+// 3% slower); keys transposed in shared memory with rows of kp (K rounded
+// up to 4) floats.
 constexpr int kBiencMaxThreads = 512;
 __host__ __device__ constexpr int bienc_threads(int G) {
     return G >= 16 ? 512 : 256;
@@ -194,19 +194,30 @@ constexpr int kBiencMaxDHead = 256;
 
 __host__ __device__ inline int bienc_kp(int K) { return (K + 3) & ~3; }
 
+// Row stride in floats of a tile's scores (then weights): at least kp, and
+// for G < 8 congruent to 4 G modulo 32, so that the 16-byte reads of the
+// rows a quarter-warp's lanes search fall in different banks.
+__host__ __device__ inline int bienc_ss_stride(int K, int G) {
+    const int kp = bienc_kp(K);
+    if (G >= 8) return kp + 4;
+    return kp + (((4 * G - kp) % 32) + 32) % 32;
+}
+
+// Shared memory of the one-kernel path: transposed keys, values, a tile
+// of queries and a tile of scores (which become the weights).
 inline int64_t bienc_smem_bytes(int K, int D, int G) {
     const int64_t R = bienc_threads(G) / G;
     const int64_t kp = bienc_kp(K);
     return 4 * (D * kp + static_cast<int64_t>(K) * D + R * (D + 4) +
-                R * (kp + 4));
+                R * bienc_ss_stride(K, G));
 }
 
 // Shared memory of the scores-and-search kernel when step 3 runs on the
-// tensor cores: the transposed keys and a tile of queries only.
+// tensor cores: the transposed keys, a tile of queries and its scores.
 inline int64_t bienc_search_smem_bytes(int K, int D, int G) {
     const int64_t R = bienc_threads(G) / G;
     const int64_t kp = bienc_kp(K);
-    return 4 * (D * kp + R * (D + 4));
+    return 4 * (D * kp + R * (D + 4) + R * bienc_ss_stride(K, G));
 }
 
 // Query tiles one CTA works through with its staged keys and values:
@@ -220,7 +231,8 @@ inline int bienc_tiles_per_cta(int Q, int G) {
 }
 
 cudaError_t launch_bienc(const BiencTask& task, int lanes_per_row,
-                         int smem_bytes, cudaStream_t stream);
+                         int keys_per_lane, int smem_bytes,
+                         cudaStream_t stream);
 
 // biencoder_attention's step 3 on the tensor cores (k_bienc_pv.cu): out =
 // P . V for every bh, P written before by the scores-and-search kernel

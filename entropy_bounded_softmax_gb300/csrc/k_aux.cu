@@ -75,7 +75,7 @@ cudaError_t launch_wait_timeout(unsigned int* err, uint64_t limit_cycles,
 
 namespace {
 constexpr int kMaxDevices = 64;
-constexpr int kSlots = 40;
+constexpr int kSlots = 56;
 // Largest MaxDynamicSharedMemorySize set so far, per device and kernel.
 std::atomic<int> g_smem_set[kMaxDevices][kSlots];
 std::mutex g_smem_mu;

@@ -398,25 +398,32 @@ def test_check_biencoder_args(args, status):
 def test_biencoder_plans():
     st, p = cs.cs_plan_biencoder_host(32, 512, 64, 64, 8, None, 232448)
     p = p.as_dict()
-    assert st == 0 and p["lanes_per_row"] == 8 and p["threads_per_cta"] == 256
+    assert st == 0 and p["lanes_per_row"] == 4 and p["threads_per_cta"] == 256
+    assert p["elems_per_lane"] == 16
     assert p["grid_ctas"] == 32 * 8 * (512 // 128)
     st, p = cs.cs_plan_biencoder_host(4, 1024, 256, 64, 8, None, 232448)
-    assert st == 0 and p.lanes_per_row == 32
+    assert st == 0 and p.lanes_per_row == 16 and p.elems_per_lane == 16
     assert p.smem_bytes <= 232448
     st, _ = cs.cs_plan_biencoder_host(4, 1024, 256, 128, 8, None, 232448)
     assert st == C["CS_ERR_OOM"]            # keys and values exceed smem
-    for K in (1, 8, 9, 64, 65, 256):
+    for K in (1, 8, 9, 16, 17, 64, 65, 256):
+        # by default sixteen items a lane, on the fewest lanes that hold K
         st, p = cs.cs_plan_biencoder_host(1, 10, K, 16, 1, None, 232448)
-        assert st == 0 and 8 * p.lanes_per_row >= K
-        assert p.lanes_per_row == 1 or 4 * p.lanes_per_row < K
+        assert st == 0 and 16 * p.lanes_per_row >= K
+        assert p.lanes_per_row == 1 or 8 * p.lanes_per_row < K
+        assert p.elems_per_lane == 16
     st, _ = cs.cs_plan_biencoder_host(1, 10, 40, 16, 1,
+                                      cs.options(C["CS_VARIANT_ROWGROUP"], 2),
+                                      232448)
+    assert st == C["CS_ERR_OOM"]            # two lanes hold at most 32 items
+    st, p = cs.cs_plan_biencoder_host(1, 10, 40, 16, 1,
                                       cs.options(C["CS_VARIANT_ROWGROUP"], 4),
                                       232448)
-    assert st == C["CS_ERR_OOM"]
+    assert st == 0 and (p.lanes_per_row, p.elems_per_lane) == (4, 16)
     st, p = cs.cs_plan_biencoder_host(1, 10, 40, 16, 1,
                                       cs.options(C["CS_VARIANT_ROWGROUP"], 8),
                                       232448)
-    assert st == 0 and p.lanes_per_row == 8
+    assert st == 0 and (p.lanes_per_row, p.elems_per_lane) == (8, 8)
     st, _ = cs.cs_plan_biencoder_host(1, 10, 40, 16, 1,
                                       cs.options(C["CS_VARIANT_CLUSTER"], 1),
                                       232448)
@@ -452,4 +459,4 @@ def test_biencoder_plans_step3_on_the_tensor_cores():
     assert bplan(64, 128)["tensor_cores"] == 0      # head above 64
     fused = bplan(64, 64, cs.options(C["CS_VARIANT_FUSED"], 0))
     assert fused["tensor_cores"] == 0 and fused["staged_tensors"] == 3
-    assert fused["lanes_per_row"] == p["lanes_per_row"] == 8
+    assert fused["lanes_per_row"] == p["lanes_per_row"] == 4

@@ -64,10 +64,15 @@ def test_query_tiles(Q):
     compare_biencoder(q, k, v, 0.125, out, attn, T, mask)
 
 
-@pytest.mark.parametrize("lanes", [2, 4, 8, 16, 32])
-def test_lane_counts(lanes):
-    K = min(8 * lanes, 40)
-    q, k, v = _rand(2, 2, 50, K, 16, lanes)
+@pytest.mark.parametrize("lanes", [1, 2, 4, 8, 16, 32])
+@pytest.mark.parametrize("per_lane", [8, 16])
+def test_lane_counts(lanes, per_lane):
+    """A forced lane count holds eight items a lane when that covers the
+    context, else sixteen."""
+    K = min(per_lane * lanes, 40)
+    if per_lane == 16 and K <= 8 * lanes:
+        pytest.skip("eight items a lane already hold this context")
+    q, k, v = _rand(2, 2, 50, K, 16, lanes + per_lane)
     out, attn, T, mask = run_biencoder(q, k, v, 0.25, lanes=lanes)
     compare_biencoder(q, k, v, 0.25, out, attn, T, mask)
 
@@ -118,7 +123,7 @@ def test_argument_errors_and_empty():
         cs.biencoder_attention(q, k, k)
     assert e.value.status == 7
     k = torch.randn(1, 1, 40, 8, device=dev)
-    with pytest.raises(cs.CsError) as e:          # 2 lanes hold 16 items
+    with pytest.raises(cs.CsError) as e:          # 2 lanes hold 32 items
         cs.biencoder_attention(q, k, k, lanes=2)
     assert e.value.status == 7
     with pytest.raises(cs.CsError) as e:          # output overlaps query

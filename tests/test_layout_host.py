@@ -78,13 +78,20 @@ def test_biencoder_smem(K, D):
     assert st == 0
     p = p.as_dict()
     G = p["lanes_per_row"]
-    assert 8 * G >= K and (G == 1 or 4 * G < K)
+    assert 16 * G >= K and (G == 1 or 8 * G < K) and p["elems_per_lane"] == 16
     R = p["threads_per_cta"] // G
     kp = (K + 3) // 4 * 4
+    # every 4 x 4 block of a tile's scores has a thread
+    assert (R // 4) * (kp // 4) <= p["threads_per_cta"]
+    # scores rows: for G < 8 the stride is 4 G mod 32 (the rows of a
+    # quarter-warp's 16-byte reads in different banks)
+    ssw = kp + 4 if G >= 8 else kp + (4 * G - kp) % 32
+    assert ssw >= kp and (G >= 8 or ssw % 32 == 4 * G % 32)
     if p["tensor_cores"]:
-        # steps 1-2 only (keys and a query tile); step 3 on the tensor cores
+        # steps 1-2 only (keys, a query tile and its scores); step 3 on the
+        # tensor cores
         assert K <= D <= 64 and p["staged_tensors"] == 2
-        need = 4 * (D * kp + R * (D + 4))
+        need = 4 * (D * kp + R * (D + 4) + R * ssw)
     else:
-        need = 4 * (D * kp + K * D + R * (D + 4) + R * (kp + 4))
+        need = 4 * (D * kp + K * D + R * (D + 4) + R * ssw)
     assert need == p["smem_bytes"] <= 232448
