@@ -923,7 +923,7 @@ cs_status cs_plan_biencoder_host(int32_t batch_size, int32_t query_len,
     // requested.
     const bool tc = o.variant != CS_VARIANT_FUSED && d_head <= cs::kPvMaxD &&
                     context_len <= d_head &&
-                    cs::pv_smem_bytes(cs::pv_np(d_head)) <= smem_per_block_optin;
+                    cs::pv_smem_bytes(context_len, d_head) <= smem_per_block_optin;
     const int64_t smem = tc ? cs::bienc_search_smem_bytes(context_len, d_head, G)
                             : cs::bienc_smem_bytes(context_len, d_head, G);
     if (smem > smem_per_block_optin) return CS_ERR_OOM;

@@ -121,6 +121,15 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
                  :: "r"(smem_addr(dst)), "l"(src) : "memory");
 }
 
+// As cp_async16, but only the first src_bytes (0..16) bytes are read and
+// the rest of the 16 destination bytes are zero-filled (src_bytes = 0
+// reads nothing).
+__device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src,
+                                                 uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
+                 :: "r"(smem_addr(dst)), "l"(src), "r"(src_bytes) : "memory");
+}
+
 // 8-byte asynchronous copy global -> shared (through L1); both addresses
 // 8-byte aligned.
 __device__ __forceinline__ void cp_async8(void* dst, const void* src) {

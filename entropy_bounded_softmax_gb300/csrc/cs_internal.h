@@ -251,35 +251,40 @@ struct PvTask {
 };
 
 constexpr int kPvM = 128;               // query rows per CTA (the MMA's M)
-constexpr int kPvKc = 32;               // context items per shared-memory chunk
-                                        // (48 KB at N = 64: four CTAs per SM)
 constexpr uint32_t kPvTmemCols = 64;    // tensor-memory columns per CTA (N <= 64)
 constexpr int kPvMaxD = 64;             // head sizes the tensor-core step takes
-constexpr int kPvSmemPad = 0;           // slack after the operands
 
-// N of the MMA: d_head rounded up to 16.
+// N of the MMA: d_head rounded up to 16; its K: the context rounded up to 8
+// (the context is at most d_head, so one shared-memory chunk holds it).
 __host__ __device__ inline int pv_np(int D) { return (D + 15) & ~15; }
+__host__ __device__ inline int pv_kp(int K) { return (K + 7) & ~7; }
 
 // Byte offsets of the step-3 kernel's shared memory: the TF32 halves of P
-// (128 x 64) and of V^T (N x 64), the completion mbarrier and the word that
-// receives the tensor-memory address.
+// (128 x Kp) and of V^T (Np x Kp); after the MMAs the output tile (128
+// rows of D fp32, D + 4 apart) reuses the space from offset 0; then the
+// completion mbarrier and the word that receives the tensor-memory address.
 struct PvSmemLayout {
-    int a_hi, a_lo, b_hi, b_lo, bar, tslot, end;
+    int a_hi, a_lo, b_hi, b_lo, stage, bar, tslot, end;
 };
 
-__host__ __device__ inline PvSmemLayout pv_smem_layout(int Np) {
+__host__ __device__ inline PvSmemLayout pv_smem_layout(int Kp, int Np, int D) {
     PvSmemLayout L;
     L.a_hi = 0;
-    L.a_lo = kPvM * kPvKc * 4;
-    L.b_hi = 2 * kPvM * kPvKc * 4;
-    L.b_lo = L.b_hi + Np * kPvKc * 4;
-    L.bar = L.b_lo + Np * kPvKc * 4;
+    L.a_lo = kPvM * Kp * 4;
+    L.b_hi = 2 * kPvM * Kp * 4;
+    L.b_lo = L.b_hi + Np * Kp * 4;
+    L.stage = 0;
+    const int ops = L.b_lo + Np * Kp * 4;
+    const int stage = kPvM * (D + 4) * 4;
+    L.bar = ((ops > stage ? ops : stage) + 15) & ~15;
     L.tslot = L.bar + 8;
-    L.end = L.tslot + 8 + kPvSmemPad;
+    L.end = L.tslot + 8;
     return L;
 }
 
-inline int64_t pv_smem_bytes(int Np) { return pv_smem_layout(Np).end; }
+inline int64_t pv_smem_bytes(int K, int D) {
+    return pv_smem_layout(pv_kp(K), pv_np(D), D).end;
+}
 
 cudaError_t launch_bienc_pv(const PvTask& task, cudaStream_t stream);
 
