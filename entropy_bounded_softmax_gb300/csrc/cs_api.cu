@@ -1010,7 +1010,7 @@ cs_status cs_biencoder_attention_ex(const float* query,
             pv.K = context_len;
             pv.D = d_head;
             pv.wait_limit_cycles = cs::kWaitLimitCycles;
-            e = cs::launch_bienc_pv(pv, s);
+            e = cs::launch_bienc_pv(pv, d->sm_count, s);
         }
     } else {
         e = cs::launch_bienc(task, p.lanes_per_row, p.elems_per_lane, p.smem_bytes, s);

@@ -141,6 +141,24 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+// Barrier among the `count` threads (whole warps) that use barrier `id`
+// (1..15; 0 is __syncthreads).
+__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(count) : "memory");
+}
+
+// The same barrier, returning in every participating thread whether v was
+// true in all of them.
+__device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t count,
+                                                  bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
+        " bar.red.and.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}"
+        : "=r"(r) : "r"(v ? 1u : 0u), "r"(id), "r"(count) : "memory");
+    return r != 0;
+}
+
 // ------------------------------------------------------------------- inputs
 // Logit element types.  fp32 logits are read as they are; bf16 logits (their
 // 16-bit patterns) are promoted to fp32 on load, which is exact (a bf16 is

@@ -250,43 +250,52 @@ struct PvTask {
     uint64_t wait_limit_cycles;
 };
 
-constexpr int kPvM = 128;               // query rows per CTA (the MMA's M)
-constexpr uint32_t kPvTmemCols = 64;    // tensor-memory columns per CTA (N <= 64)
+constexpr int kPvM = 128;               // query rows per tile (the MMA's M)
+constexpr uint32_t kPvTmemCols = 128;   // two fp32 accumulators of N <= 64
 constexpr int kPvMaxD = 64;             // head sizes the tensor-core step takes
 
 // N of the MMA: d_head rounded up to 16; its K: the context rounded up to 8
-// (the context is at most d_head, so one shared-memory chunk holds it).
+// (the context is at most d_head, so one shared-memory stage holds it).
 __host__ __device__ inline int pv_np(int D) { return (D + 15) & ~15; }
 __host__ __device__ inline int pv_kp(int K) { return (K + 7) & ~7; }
 
-// Byte offsets of the step-3 kernel's shared memory: the TF32 halves of P
-// (128 x Kp) and of V^T (Np x Kp); after the MMAs the output tile (128
-// rows of D fp32, D + 4 apart) reuses the space from offset 0; then the
-// completion mbarrier and the word that receives the tensor-memory address.
+// Byte offsets of the step-3 kernel's shared memory: two stages of the
+// TF32 halves of a tile's P (stage s: hi at 2 s a_half, lo a_half later),
+// each half 128 rows x pv_chunks(K) chunks of 32 items in the MMA's 128-byte
+// swizzled K-major layout (a chunk is 128 rows of 128 bytes, 16 KB); the
+// halves of V^T (Np x Kp, no swizzle); the output tile (128 rows of D + 4
+// floats); ten mbarriers (full, empty, acc_full, acc_empty, landed, two of
+// each), the abort flag and the word that receives the tensor-memory
+// address.
+__host__ __device__ inline int pv_chunks(int K) { return (K + 31) / 32; }
+
 struct PvSmemLayout {
-    int a_hi, a_lo, b_hi, b_lo, stage, bar, tslot, end;
+    int a_half, b_hi, b_lo, stage, bar, flag, tslot, end;
 };
 
-__host__ __device__ inline PvSmemLayout pv_smem_layout(int Kp, int Np, int D) {
+__host__ __device__ inline PvSmemLayout pv_smem_layout(int K, int Np, int D) {
     PvSmemLayout L;
-    L.a_hi = 0;
-    L.a_lo = kPvM * Kp * 4;
-    L.b_hi = 2 * kPvM * Kp * 4;
+    const int Kp = pv_kp(K);
+    L.a_half = pv_chunks(K) * kPvM * 128;
+    L.b_hi = 4 * L.a_half;
     L.b_lo = L.b_hi + Np * Kp * 4;
-    L.stage = 0;
-    const int ops = L.b_lo + Np * Kp * 4;
-    const int stage = kPvM * (D + 4) * 4;
-    L.bar = ((ops > stage ? ops : stage) + 15) & ~15;
-    L.tslot = L.bar + 8;
-    L.end = L.tslot + 8;
+    L.stage = L.b_lo + Np * Kp * 4;
+    L.bar = L.stage + kPvM * (D + 4) * 4;
+    L.flag = L.bar + 10 * 8;
+    L.tslot = L.flag + 4;
+    L.end = L.tslot + 4;
     return L;
 }
 
+// Bytes to allocate: the layout plus slack to align it to 1024 bytes.
 inline int64_t pv_smem_bytes(int K, int D) {
-    return pv_smem_layout(pv_kp(K), pv_np(D), D).end;
+    return pv_smem_layout(K, pv_np(D), D).end + 1024;
 }
 
-cudaError_t launch_bienc_pv(const PvTask& task, cudaStream_t stream);
+// Persistent CTAs, one per SM at most, each taking a contiguous run of
+// tiles.
+cudaError_t launch_bienc_pv(const PvTask& task, int sm_count,
+                            cudaStream_t stream);
 
 cudaError_t launch_rowgroup(const RowTask& task, int lanes_per_row,
                             int elems_per_lane, cudaStream_t stream);

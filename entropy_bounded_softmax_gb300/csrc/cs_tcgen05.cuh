@@ -1,8 +1,9 @@
 // Inline-PTX wrappers for the 5th-generation tensor cores of sm_103a
 // (tcgen05): tensor-memory allocation, the MMA with operands in shared
 // memory and the accumulator in tensor memory, its completion on an
-// mbarrier, and loads of the accumulator into registers.  Used by the
-// attn . V step of biencoder_attention (k_bienc_pv.cu).
+// mbarrier, loads of the accumulator into registers, and tensor copies
+// from global into shared memory.  Used by the attn . V step of
+// biencoder_attention (k_bienc_pv.cu).
 #pragma once
 
 #include <stdint.h>
@@ -105,6 +106,31 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
         : "r"(taddr) : "memory");
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 2-D tiled copy by the tensor-memory-access unit: the box of the tensor
+// map at element coordinates (x, y) into shared memory at sdst (laid out
+// and swizzled as the map says), counted in bytes on the mbarrier at bar.
+__device__ __forceinline__ void tma_load_2d(void* sdst, const void* tmap, int x,
+                                            int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];"
+        :: "r"(smem_addr(sdst)), "l"(tmap), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand in the 128-byte
+// swizzled layout: 8-row groups of 128-byte rows (1024-byte atoms, each
+// row's 16-byte units permuted by the row index mod 8), atoms stacked
+// along M or N every sbo bytes; the start address may step through an
+// atom's row in 32-byte (one K = 8 tf32) increments.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t sbo) {
+    return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) |
+           (static_cast<uint64_t>(1u) << 16) |
+           (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) |
+           (1ull << 46) |
+           (2ull << 61);
 }
 
 }  // namespace csd
