@@ -342,7 +342,7 @@ bienc_pv_kernel(PvTask t, const __grid_constant__ CUtensorMap tmap, int use_tma)
     if (*abort_flag && threadIdx.x == 0) raise_error(t.err, kBitTimeout);
 }
 
-// cuTensorMapEncodeTiled, from the driver through the runtime (no link
+// cuTensorMapEncodeTiled, from the CUDA driver through the runtime (no link
 // against the driver library); null if unavailable.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
