@@ -82,3 +82,28 @@ def test_biencoder_random(seed):
     bound = float(rng.choice([0.05, 0.2, 1.0]))
     out, attn, T, mask = run_biencoder(q, k, v, scale, bound)
     compare_biencoder(q, k, v, scale, out, attn, T, mask, bound)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_biencoder_tensor_core_random(seed):
+    """Shapes that take the tensor-core attn . V kernel (context_len <=
+    d_head <= 64): many (batch, head) pairs per persistent CTA, ragged
+    query tiles, contexts that are not a multiple of 4 or 32.  Against the
+    oracle with the weights returned (attn_out; element loads when its rows
+    are not 16-byte aligned), and the same output bit for bit with the
+    weights passing through the output buffer (tensor copies)."""
+    rng = _case_rng("biencoder_tc", seed)
+    D = 4 * int(rng.integers(1, 17))
+    K = int(rng.integers(1, D + 1))
+    B, H, Q = (int(rng.integers(1, 4)), int(rng.integers(1, 9)),
+               int(rng.integers(1, 600)))
+    q = rng.normal(0.0, 1.0, (B, H, Q, D)).astype(np.float32)
+    k = rng.normal(0.0, 1.0, (B, H, K, D)).astype(np.float32)
+    v = rng.normal(0.0, 1.0, (B, H, K, D)).astype(np.float32)
+    scale = float(rng.uniform(0.05, 1.0))
+    bound = float(rng.choice([0.05, 0.2, 1.0]))
+    out, attn, T, mask = run_biencoder(q, k, v, scale, bound)
+    compare_biencoder(q, k, v, scale, out, attn, T, mask, bound)
+    out2, _, T2, mask2 = run_biencoder(q, k, v, scale, bound, return_attn=False)
+    assert np.array_equal(T2, T) and mask2 == mask
+    assert np.array_equal(out2, out)
