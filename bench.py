@@ -465,10 +465,14 @@ def time_e2e(torch, make_slot, step, stream, e_steps: int) -> dict:
         e0.record(stream)
         for st in streams:
             st.wait_event(e0)
+        # The current stream is switched with set_stream (a fraction of the
+        # host time of the stream context manager, on the step's path).
+        prev = torch.cuda.current_stream(stream.device)
         for i in range(n):
             k = i % E2E_SLOTS if pipelined else 0
-            with torch.cuda.stream(streams[k]):
-                step(slots[k])
+            torch.cuda.set_stream(streams[k])
+            step(slots[k])
+        torch.cuda.set_stream(prev)
         for st in streams:
             stream.wait_stream(st)
         e1.record(stream)

@@ -76,8 +76,23 @@ class CsError(RuntimeError):
 
 
 def _stream_handle(device) -> int:
+    """The raw cudaStream_t of the current stream of a CUDA device."""
     import torch
+    idx = device.index if device.index is not None else torch.cuda.current_device()
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None:
+        return raw(idx)
     return torch.cuda.current_stream(device).cuda_stream
+
+
+def _on_device(device):
+    """A context that makes `device` current: none when it already is (the
+    common case, and the cheapest: the call is on every step's path)."""
+    import contextlib
+    import torch
+    if device.index is None or device.index == torch.cuda.current_device():
+        return contextlib.nullcontext()
+    return torch.cuda.device(device)
 
 
 def constrained_softmax(logits, entropy_bound: float = DEFAULT_ENTROPY_BOUND,
@@ -142,7 +157,7 @@ def constrained_softmax(logits, entropy_bound: float = DEFAULT_ENTROPY_BOUND,
         e_ptr = evals_out.data_ptr()
     entry = (cs_constrained_softmax_bf16_ex
              if logits.dtype == torch.bfloat16 else cs_constrained_softmax_ex)
-    with torch.cuda.device(logits.device):
+    with _on_device(logits.device):
         st = entry(
             logits.data_ptr(), out.data_ptr(), batch, num_classes,
             float(entropy_bound), float(t_min), float(t_max), int(max_iter),
@@ -192,7 +207,7 @@ def constrained_softmax_backward(probs, grad_output, t, out=None,
         out = torch.empty_like(probs)
     else:
         _check_like("out", out, probs)
-    with torch.cuda.device(probs.device):
+    with _on_device(probs.device):
         st = cs_constrained_softmax_backward_ex(
             probs.data_ptr(), grad_output.data_ptr(), t.data_ptr(),
             out.data_ptr(), batch, num_classes,
@@ -237,7 +252,7 @@ def attention_softmax(scores, mask=None, causal: bool = False, out=None,
           or out.device != scores.device or not out.is_contiguous()):
         raise ValueError("out must be a contiguous float32 tensor shaped like "
                          "scores on the same device")
-    with torch.cuda.device(scores.device):
+    with _on_device(scores.device):
         st = cs_attention_softmax_ex(
             scores.data_ptr(), out.data_ptr(), m_ptr, B, H, S,
             int(bool(causal)), options(VARIANTS[variant], param, threads, 0),
@@ -287,7 +302,7 @@ def biencoder_attention(query, keys, values, scale=None,
     variant = (CONSTANTS["CS_VARIANT_FUSED"] if fused
                else VARIANTS["rowgroup"] if lanes else 0)
     opt = options(variant, lanes, 0, 0)
-    with torch.cuda.device(query.device):
+    with _on_device(query.device):
         st = cs_biencoder_attention_ex(
             query.data_ptr(), keys.data_ptr(), values.data_ptr(),
             out.data_ptr(), B, Q, K, D, H, float(scale), float(entropy_bound),
@@ -358,7 +373,7 @@ def get_error(device=None) -> set[str]:
     import torch
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None \
         else torch.device(device)
-    with torch.cuda.device(dev):
+    with _on_device(dev):
         st, mask = cs_get_error(_stream_handle(dev))
     if st != 0:
         raise CsError(st, "cs_get_error")

@@ -135,6 +135,8 @@ _SIGNATURES = {
 def load(path: str | None = None) -> ctypes.CDLL:
     """Load libcsoftmax.so (built by ``build.py``); raise if it is absent."""
     global _lib
+    if _lib is not None and path is None:   # the common case: no lock
+        return _lib
     with _lock:
         if _lib is not None and path is None:
             return _lib
