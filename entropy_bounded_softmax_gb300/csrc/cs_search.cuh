@@ -335,8 +335,20 @@ __device__ __forceinline__ float search_result_T(const Search& s,
     return (s.f & (kTminInf | kFinal)) ? c.g.lo0 : c.g.at(s.jl);
 }
 
-// Newton rounds every searching narrow row takes before the fallback.
-constexpr int kNarrowNewtonRounds = 5;
+// Newton rounds a searching narrow row may take before the fallback.
+constexpr int kNarrowNewtonRounds = 7;
+// The narrow search probes t_min instead of the Newton point when no
+// feasible point is known and the Newton point lies within this factor of
+// t_min: generously after the first step (from T = 1, whose Newton point
+// can be off by a factor of three either way), tightly later (a probe
+// costs a round whenever the root lies above t_min).
+constexpr float kNarrowProbeFirst = 4.0f;
+constexpr float kNarrowProbeLater = 1.5f;
+// A Newton point within this fraction of the bracket's far end (in beta,
+// measured from the end it steps from) is replaced by the bracket's
+// geometric midpoint: log H is far from linear over such a step, and a row
+// can otherwise oscillate between the two ends.
+constexpr float kNarrowFarEnd = 0.1f;
 
 // The search for narrow rows, one grid point per round (the row-group
 // kernel, whose rows are a few registers per lane; a multi-point pass there
@@ -345,12 +357,16 @@ constexpr int kNarrowNewtonRounds = 5;
 // row's (S, V, W) at beta and eval2(beta) its (S, V).  Strict: the
 // bisection, one evaluation per halving.  Otherwise up to
 // kNarrowNewtonRounds Newton steps on log H(beta) from the last point
-// evaluated, kept inside the bracket in beta and placed on the grid point
-// at or below (t_min when the step comes within 4 t_min of it), then, only
-// while the bracket is open, points stepping from the end moved last with
-// doubling strides.  One lg2 and one reciprocal of S serve both the
-// decision and the next step.  Returns T, 1/T, 1/S(T), the section 5.4
-// flag and the number of evaluations made.
+// evaluated, kept inside the bracket in beta (its geometric midpoint when
+// the step leaves it across the far end or lands next to that end; the
+// inner neighbour of the near end when it points back past that end) and
+// placed on the grid point at or below (t_min when the step comes near t_min and no feasible
+// point is known; when t_min then proves feasible, the next step is taken
+// from whichever of t_min and the point before it has H nearer the bound
+// in log terms), then, only while the bracket is open, points stepping
+// from the end moved last with doubling strides.  One lg2 and one
+// reciprocal of S serve both the decision and the next step.  Returns T,
+// 1/T, 1/S(T), the section 5.4 flag and the number of evaluations made.
 template <class Eval3, class Eval2>
 __device__ __forceinline__ void narrow_search(const SearchCfg& cfg, float S1,
                                               float V1, float W1, bool strict,
@@ -380,11 +396,37 @@ __device__ __forceinline__ void narrow_search(const SearchCfg& cfg, float S1,
         }
     } else if (cfg.t_min < cfg.hi0) {
         float b = 1.0f, S = S1, V = V1, W = W1;
+        // The point evaluated before a t_min probe (its beta and sums).
+        float pb = 1.0f, pS = S1, pV = V1, pW = W1;
+        bool after_probe = false;  // the last round probed t_min, feasible
+        bool last_feas = false;    // the side of the last point evaluated
         float b_inf = rcp_approx(cfg.hi0);
         float b_feas = rcp_approx(cfg.t_min);
         const bool log_newton = cfg.bound > 0.0f;
         int jlast = -1;
         for (int k = 0; k < kNarrowNewtonRounds && jh - jl > 1 && !tmin_inf; ++k) {
+            // The point stepped from is the bracket end evaluated last (from
+            // the second round on), feasible or not.
+            const bool at_end = k > 0;
+            bool anchor_feas = last_feas;
+            bool far_guard = at_end;
+            if (after_probe) {
+                const float h_t = kLn2 * (lg2_approx(S) - b * V * rcp_approx(S));
+                const float h_p = kLn2 * (lg2_approx(pS) - pb * pV * rcp_approx(pS));
+                const float lb = log_newton ? cfg.lg2_bound : 0.0f;
+                if (!(h_t > 0.0f) ||
+                    fabsf(lg2_approx(h_p) - lb) < fabsf(lg2_approx(h_t) - lb)) {
+                    // The point before the probe: infeasible, since no
+                    // feasible point was known when the probe was chosen.
+                    b = pb;
+                    S = pS;
+                    V = pV;
+                    W = pW;
+                    anchor_feas = false;
+                    far_guard = false;
+                }
+                after_probe = false;
+            }
             const float is = rcp_approx(S);
             const float ey = V * is;
             const float H = kLn2 * (lg2_approx(S) - b * ey);
@@ -396,11 +438,33 @@ __device__ __forceinline__ void narrow_search(const SearchCfg& cfg, float S1,
             } else {
                 bn = b - (H - cfg.bound) * rcp_approx(dH);
             }
-            if (!(bn > b_inf && bn < b_feas)) bn = sqrtf(b_inf * b_feas);
+            // A step that points back past the end it starts from (H there
+            // equal to the bound in fp32, or on the wrong side of it by a
+            // rounding) is kept: the clamp below then takes that end's
+            // inner neighbour, which closes the bracket when the crossing
+            // is next to it.
+            const bool back =
+                at_end && bn == bn && (anchor_feas ? !(bn < b_feas) : !(bn > b_inf));
+            if (!back) {
+                if (!(bn > b_inf && bn < b_feas)) {
+                    bn = sqrtf(b_inf * b_feas);
+                } else if (far_guard) {
+                    const float far = anchor_feas ? b_inf : b_feas;
+                    if (fabsf(far - bn) < kNarrowFarEnd * fabsf(far - b))
+                        bn = sqrtf(b_inf * b_feas);
+                }
+            }
             const float Tn = rcp_approx(bn);
-            const bool probe = !jl_eval && Tn <= 4.0f * cfg.t_min;
+            const float pf = k == 0 ? kNarrowProbeFirst : kNarrowProbeLater;
+            const bool probe = !jl_eval && Tn <= pf * cfg.t_min;
             int jn = Tn > cfg.t_min ? g.near(Tn) : 0;
             jn = probe ? 0 : min(max(jn, jl + 1), jh - 1);
+            if (probe) {
+                pb = b;
+                pS = S;
+                pV = V;
+                pW = W;
+            }
             b = rcp_approx(probe ? cfg.t_min : g.at(jn));
             const float3 r = eval3(b);
             ++evals;
@@ -409,6 +473,7 @@ __device__ __forceinline__ void narrow_search(const SearchCfg& cfg, float S1,
             W = r.z;
             const bool inf = entropy_above(make_float2(S, V), b, cfg.bound_bits);
             jlast = jn;
+            last_feas = !inf;
             if (probe) {
                 s_lo = S;
                 if (inf) {
@@ -416,6 +481,7 @@ __device__ __forceinline__ void narrow_search(const SearchCfg& cfg, float S1,
                 } else {
                     jl_eval = true;
                     b_feas = b;
+                    after_probe = true;
                 }
             } else if (inf) {
                 jh = jn;
