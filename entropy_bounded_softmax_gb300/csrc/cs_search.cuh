@@ -24,9 +24,9 @@
 // root approaches it, then, once Newton has converged, the grid points on
 // both sides of the Newton point; if the bracket is still open
 // (evaluations of H in fp32 are within rounding of the bound there) it
-// splits the bracket into quarters, two halvings per round, or, on the
-// fine grid when the last round moved only one end, gallops away from that
-// end with strides growing eightfold.  With one
+// gallops away from the end the last round moved, when only one moved,
+// with strides growing eightfold, else splits the bracket into quarters,
+// two halvings per round.  With one
 // point per round (narrow rows, where a pass costs little next to
 // divergent bookkeeping) the Newton point is evaluated alone and the
 // neighbours follow one by one, with doubling strides.  The strict mode
@@ -205,16 +205,19 @@ __device__ __forceinline__ int search_plan(Search& s, const SearchCfg& c,
         s.jl_prev = s.jl;
         s.jh_prev = s.jh;
         const int d = s.jh - s.jl;
-        if (g.fine && lo_moved != hi_moved) {
-            // Fine grid (every fp32 value a point, so a converged Newton
-            // point is still many points off) and only one end moved last
-            // round: the crossing is most likely just past that end.  Gallop
-            // from it towards the other end, 1, 2 and 4 strides out, the
-            // stride growing eightfold per round (when the bracket is
-            // shorter than a stride, quarter it instead).  On the coarser
-            // exact grid the converged round almost always closes the
-            // bracket, and quartering measured as fast.
-            s.stride = max(s.stride, 2);
+        if (lo_moved != hi_moved) {
+            // Only one end moved last round: the crossing is most likely
+            // just past that end (fp32 evaluations of H next to the bound
+            // can put a converged Newton point a few points off, and on the
+            // fine grid, where every fp32 value is a point, a converged
+            // Newton point is still many points off).  Gallop from it
+            // towards the other end, 1, 2 and 4 strides out (the stride
+            // starting at 1 on the exact grid, 2 on the fine one) and
+            // growing eightfold per round; when the bracket is shorter than
+            // a stride, quarter it instead.  Quartering the whole bracket
+            // instead cost rows whose crossing sat next to the moved end
+            // up to eight extra rounds.
+            s.stride = max(s.stride, g.fine ? 2 : 1);
 #pragma unroll
             for (int k = 0; k < kMaxPoints; ++k) {
                 const int off = s.stride << k;
@@ -245,7 +248,16 @@ __device__ __forceinline__ int search_plan(Search& s, const SearchCfg& c,
     } else {
         bn = s.dHc < 0.0f ? s.bc - (s.Hc - c.bound) * rcp_approx(s.dHc) : NAN;
     }
-    if (!(bn > b_inf && bn < b_feas)) bn = sqrtf(b_inf * b_feas);
+    // A step that leaves the bracket is replaced by the bracket's geometric
+    // midpoint, unless it points back past the bracket end the anchor is
+    // (H there equal to the bound in fp32, or on the wrong side of it by a
+    // rounding): that step is kept, and the clamp below takes that end's
+    // inner neighbour.
+    if (!(bn > b_inf && bn < b_feas)) {
+        const bool back = s.rounds > 0 &&
+                          (bn >= b_feas ? s.bc >= b_feas : (bn <= b_inf && s.bc <= b_inf));
+        if (!back) bn = sqrtf(b_inf * b_feas);
+    }
     const float Tn = rcp_approx(bn);
     // The grid point at or just below Tn, strictly inside the bracket.
     int jn = Tn > g.lo0 ? g.near(Tn) : 0;
