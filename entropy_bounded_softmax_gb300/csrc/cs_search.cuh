@@ -408,6 +408,7 @@ __device__ __forceinline__ void narrow_search(const SearchCfg& cfg, float S1,
         }
     } else if (cfg.t_min < cfg.hi0) {
         float b = 1.0f, S = S1, V = V1, W = W1;
+        float ls = lg2_approx(S);  // log2 S, shared by the decision and the step
         // The point evaluated before a t_min probe (its beta and sums).
         float pb = 1.0f, pS = S1, pV = V1, pW = W1;
         bool after_probe = false;  // the last round probed t_min, feasible
@@ -423,7 +424,7 @@ __device__ __forceinline__ void narrow_search(const SearchCfg& cfg, float S1,
             bool anchor_feas = last_feas;
             bool far_guard = at_end;
             if (after_probe) {
-                const float h_t = kLn2 * (lg2_approx(S) - b * V * rcp_approx(S));
+                const float h_t = kLn2 * (ls - b * V * rcp_approx(S));
                 const float h_p = kLn2 * (lg2_approx(pS) - pb * pV * rcp_approx(pS));
                 const float lb = log_newton ? cfg.lg2_bound : 0.0f;
                 if (!(h_t > 0.0f) ||
@@ -434,6 +435,7 @@ __device__ __forceinline__ void narrow_search(const SearchCfg& cfg, float S1,
                     S = pS;
                     V = pV;
                     W = pW;
+                    ls = lg2_approx(pS);
                     anchor_feas = false;
                     far_guard = false;
                 }
@@ -441,7 +443,7 @@ __device__ __forceinline__ void narrow_search(const SearchCfg& cfg, float S1,
             }
             const float is = rcp_approx(S);
             const float ey = V * is;
-            const float H = kLn2 * (lg2_approx(S) - b * ey);
+            const float H = kLn2 * (ls - b * ey);
             const float dH = -b * (kLn2 * kLn2) * fmaxf(fmaf(W, is, -ey * ey), 0.0f);
             float bn;
             if (log_newton && H > 0.0f) {
@@ -483,7 +485,9 @@ __device__ __forceinline__ void narrow_search(const SearchCfg& cfg, float S1,
             S = r.x;
             V = r.y;
             W = r.z;
-            const bool inf = entropy_above(make_float2(S, V), b, cfg.bound_bits);
+            // entropy_above's test, with log2 S kept for the next step.
+            ls = lg2_approx(S);
+            const bool inf = fmaf(S, ls - cfg.bound_bits, -b * V) > 0.0f;
             jlast = jn;
             last_feas = !inf;
             if (probe) {
