@@ -61,8 +61,8 @@ __device__ __forceinline__ float3 group_sum3(float3 v, unsigned mask) {
 // (S, V, W) of this lane's classes at inverse temperature beta, with
 // W = sum y^2 2^(beta y) for the Newton slope.  S and V take exactly the
 // arithmetic of reg_pass, so a grid point gets the same decision whichever
-// pass evaluates it.
-template <int E4>
+// pass evaluates it.  UNIT: beta = 1, whose product y * 1 = y is skipped.
+template <int E4, bool UNIT = false>
 __device__ __forceinline__ float3 reg_pass3(const float4 (&y)[E4], float beta) {
     SV4 acc;
     acc.zero();
@@ -72,8 +72,8 @@ __device__ __forceinline__ float3 reg_pass3(const float4 (&y)[E4], float beta) {
     for (int i = 0; i < E4; ++i) {
         const float2 y01 = make_float2(y[i].x, y[i].y);
         const float2 y23 = make_float2(y[i].z, y[i].w);
-        const float2 x01 = mul2(y01, b2);
-        const float2 x23 = mul2(y23, b2);
+        const float2 x01 = UNIT ? y01 : mul2(y01, b2);
+        const float2 x23 = UNIT ? y23 : mul2(y23, b2);
         const float2 e01 = make_float2(ex2(x01.x), ex2(x01.y));
         const float2 e23 = make_float2(ex2(x23.x), ex2(x23.y));
         acc.s01 = add2(acc.s01, e01);
@@ -130,14 +130,18 @@ __device__ __forceinline__ RowSolution solve_row(float4 (&y)[E4], float m,
     if (row_code != 0) {
         bits = row_code == 2 ? kBitNan : kBitInf;
     } else {
+        // (l - m) log2 e, floored, two lanes per packed operation (the
+        // same roundings as the scalar subtract and multiply).
+        const float2 neg_m = make_float2(-m, -m);
+        const float2 l2e = make_float2(kLog2e, kLog2e);
 #pragma unroll
         for (int i = 0; i < E4; ++i) {
-            y[i].x = fmaxf((y[i].x - m) * kLog2e, kYFloor);
-            y[i].y = fmaxf((y[i].y - m) * kLog2e, kYFloor);
-            y[i].z = fmaxf((y[i].z - m) * kLog2e, kYFloor);
-            y[i].w = fmaxf((y[i].w - m) * kLog2e, kYFloor);
+            const float2 a = mul2(add2(make_float2(y[i].x, y[i].y), neg_m), l2e);
+            const float2 b = mul2(add2(make_float2(y[i].z, y[i].w), neg_m), l2e);
+            y[i] = make_float4(fmaxf(a.x, kYFloor), fmaxf(a.y, kYFloor),
+                               fmaxf(b.x, kYFloor), fmaxf(b.y, kYFloor));
         }
-        const float3 r1 = group_sum3<G>(reg_pass3<E4>(y, 1.0f), gmask);
+        const float3 r1 = group_sum3<G>(reg_pass3<E4, true>(y, 1.0f), gmask);
         evals = 1;
         float2 sv = make_float2(r1.x, r1.y);
         if (!entropy_above(sv, 1.0f, bound_bits)) {

@@ -457,16 +457,13 @@ __device__ __forceinline__ void narrow_search(const SearchCfg& cfg, float S1,
             // rounding) is kept: the clamp below then takes that end's
             // inner neighbour, which closes the bracket when the crossing
             // is next to it.
-            const bool back =
-                at_end && bn == bn && (anchor_feas ? !(bn < b_feas) : !(bn > b_inf));
-            if (!back) {
-                if (!(bn > b_inf && bn < b_feas)) {
+            if (!(bn > b_inf && bn < b_feas)) {
+                const bool back = at_end && (anchor_feas ? bn >= b_feas : bn <= b_inf);
+                if (!back) bn = sqrtf(b_inf * b_feas);
+            } else if (far_guard) {
+                const float far = anchor_feas ? b_inf : b_feas;
+                if (fabsf(far - bn) < kNarrowFarEnd * fabsf(far - b))
                     bn = sqrtf(b_inf * b_feas);
-                } else if (far_guard) {
-                    const float far = anchor_feas ? b_inf : b_feas;
-                    if (fabsf(far - bn) < kNarrowFarEnd * fabsf(far - b))
-                        bn = sqrtf(b_inf * b_feas);
-                }
             }
             const float Tn = rcp_approx(bn);
             const float pf = k == 0 ? kNarrowProbeFirst : kNarrowProbeLater;

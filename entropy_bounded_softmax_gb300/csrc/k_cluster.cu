@@ -242,12 +242,14 @@ struct Acc {
     // beta}, with x = beta (y + d) computed as fma(y, beta, bd2), bd2 =
     // {beta d, beta d}: y is stored relative to this thread's max, d is
     // that max's offset from the row's (V and W are kept relative to the
-    // thread's max; thread_to_row() moves them).
+    // thread's max; thread_to_row() moves them).  UNIT: beta = 1 and
+    // d = 0 (the T = 1 pass), where x = y exactly and the fma is skipped.
+    template <bool UNIT = false>
     __device__ __forceinline__ void add(float4 y, float2 b2, float2 bd2) {
         const float2 y01 = make_float2(y.x, y.y);
         const float2 y23 = make_float2(y.z, y.w);
-        const float2 x01 = fma2(y01, b2, bd2);
-        const float2 x23 = fma2(y23, b2, bd2);
+        const float2 x01 = UNIT ? y01 : fma2(y01, b2, bd2);
+        const float2 x23 = UNIT ? y23 : fma2(y23, b2, bd2);
         const float2 e01 = make_float2(ex2(x01.x), ex2(x01.y));
         const float2 e23 = make_float2(ex2(x23.x), ex2(x23.y));
         s = add2(s, add2(e01, e23));
@@ -281,11 +283,15 @@ __device__ __forceinline__ void transform_pass(float4* row4, int q4, float m_t,
     acc.zero();
     const float2 one = make_float2(1.0f, 1.0f);
     const float2 zero = make_float2(0.0f, 0.0f);
-    auto to_y = [m_t](float4 l) {
-        return make_float4(fmaxf((l.x - m_t) * kLog2e, kYFloor),
-                           fmaxf((l.y - m_t) * kLog2e, kYFloor),
-                           fmaxf((l.z - m_t) * kLog2e, kYFloor),
-                           fmaxf((l.w - m_t) * kLog2e, kYFloor));
+    // (l - m_t) log2 e, floored, two lanes per packed operation (the same
+    // roundings as the scalar subtract and multiply).
+    const float2 neg_m = make_float2(-m_t, -m_t);
+    const float2 l2e = make_float2(kLog2e, kLog2e);
+    auto to_y = [neg_m, l2e](float4 l) {
+        const float2 a = mul2(add2(make_float2(l.x, l.y), neg_m), l2e);
+        const float2 b = mul2(add2(make_float2(l.z, l.w), neg_m), l2e);
+        return make_float4(fmaxf(a.x, kYFloor), fmaxf(a.y, kYFloor),
+                           fmaxf(b.x, kYFloor), fmaxf(b.y, kYFloor));
     };
     // Four float4s per trip (independent chains), then the rest one by one.
     const int nt = blockDim.x;
@@ -297,7 +303,7 @@ __device__ __forceinline__ void transform_pass(float4* row4, int q4, float m_t,
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             row4[q + i * nt] = y[i];
-            acc.add(y[i], one, zero);
+            acc.add<true>(y[i], one, zero);
         }
     }
     // At most three left: a pair, then a single.
@@ -306,14 +312,14 @@ __device__ __forceinline__ void transform_pass(float4* row4, int q4, float m_t,
         const float4 yb = to_y(row4[q + nt]);
         row4[q] = ya;
         row4[q + nt] = yb;
-        acc.add(ya, one, zero);
-        acc.add(yb, one, zero);
+        acc.add<true>(ya, one, zero);
+        acc.add<true>(yb, one, zero);
         q += 2 * nt;
     }
     if (q < q4) {
         const float4 y = to_y(row4[q]);
         row4[q] = y;
-        acc.add(y, one, zero);
+        acc.add<true>(y, one, zero);
     }
     out[0] = m_t;
     out[1] = acc.s.x + acc.s.y;

@@ -49,6 +49,9 @@ rowgroup_kernel(RowTask t, int vec) {
         float m = -INFINITY;
         float bad = 0.0f;
         if (vec) {
+            // bad becomes NaN if any element is NaN or infinite (x * 0).
+            float2 bad2 = make_float2(0.f, 0.f);
+            const float2 zero2 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int i = 0; i < E4; ++i) {
                 const int q = i * G + sub;
@@ -56,14 +59,13 @@ rowgroup_kernel(RowTask t, int vec) {
                     y[i] = In::get4(src + 4 * q);
                     m = fmaxf(m, fmaxf(fmaxf(y[i].x, y[i].y),
                                        fmaxf(y[i].z, y[i].w)));
-                    bad = fmaf(y[i].x, 0.f, bad);
-                    bad = fmaf(y[i].y, 0.f, bad);
-                    bad = fmaf(y[i].z, 0.f, bad);
-                    bad = fmaf(y[i].w, 0.f, bad);
+                    bad2 = fma2(make_float2(y[i].x, y[i].y), zero2, bad2);
+                    bad2 = fma2(make_float2(y[i].z, y[i].w), zero2, bad2);
                 } else {
                     y[i] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
                 }
             }
+            bad = bad2.x + bad2.y;
         } else {
 #pragma unroll
             for (int i = 0; i < E4; ++i) {
