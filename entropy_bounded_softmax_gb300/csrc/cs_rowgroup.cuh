@@ -102,7 +102,10 @@ struct RowSolution {
 // bad the lane's finiteness check (NaN when a logit is NaN or infinite).
 // On return y holds (l - max) log2 e (floored), ready for the output pass
 // 2^(beta_out y) inv_s.  Every lane of the group returns the same values.
-template <int G, int E4>
+// SPLIT_GRID: two copies of the search, one per grid kind (fewer
+// instructions a round; more registers, which the kernels that hold more
+// than the row in registers cannot spare).
+template <int G, int E4, bool SPLIT_GRID = true>
 __device__ __forceinline__ RowSolution solve_row(float4 (&y)[E4], float m,
                                                  float bad,
                                                  const SearchCfg& cfg,
@@ -151,11 +154,23 @@ __device__ __forceinline__ RowSolution solve_row(float4 (&y)[E4], float m,
         } else {
             bool over = false;
             int n_search = 0;
-            narrow_search(
-                cfg, r1.x, r1.y, r1.z, strict,
-                [&](float b) { return group_sum3<G>(reg_pass3<E4>(y, b), gmask); },
-                [&](float b) { return group_sum2<G>(reg_pass<E4>(y, b), gmask); },
-                T_row, beta_out, inv_s, over, n_search);
+            auto eval3 = [&](float b) { return group_sum3<G>(reg_pass3<E4>(y, b), gmask); };
+            auto eval2 = [&](float b) { return group_sum2<G>(reg_pass<E4>(y, b), gmask); };
+            if (SPLIT_GRID) {
+                // One search instance per grid kind (max_iter above 24 or
+                // not), so that its loops carry no branch on the kind.
+                if (cfg.g.fine)
+                    narrow_search<kGridFine>(cfg, r1.x, r1.y, r1.z, strict, eval3,
+                                             eval2, T_row, beta_out, inv_s, over,
+                                             n_search);
+                else
+                    narrow_search<kGridExact>(cfg, r1.x, r1.y, r1.z, strict, eval3,
+                                              eval2, T_row, beta_out, inv_s, over,
+                                              n_search);
+            } else {
+                narrow_search<kGridAny>(cfg, r1.x, r1.y, r1.z, strict, eval3, eval2,
+                                        T_row, beta_out, inv_s, over, n_search);
+            }
             evals += n_search;
             if (over) bits |= kBitOverflow;
         }

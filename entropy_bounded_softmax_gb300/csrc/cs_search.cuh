@@ -49,6 +49,10 @@ namespace csd {
 constexpr int kMaxPoints = 3;         // temperatures evaluated per round
 constexpr int kMaxNewtonRounds = 40;  // then halve the bracket round by round
 constexpr int kMaxExactLevels = 24;   // grid indices exact in fp32 up to 2^24
+// Grid kinds for code that fixes the kind at compile time (Grid::at_t).
+constexpr int kGridAny = 0;    // branch on Grid::fine
+constexpr int kGridExact = 1;  // fine == false
+constexpr int kGridFine = 2;   // fine == true
 
 // The bisection's grid (see the file comment).
 struct Grid {
@@ -69,6 +73,22 @@ struct Grid {
     // An index whose point is within about one step of T (lo0 < T).
     __device__ __forceinline__ int near(float T) const {
         if (fine) return __float_as_int(T) - lo_bits;
+        return __float2int_rd(fminf((T - lo0) * inv_step, 2.0e9f));
+    }
+    // The same for a grid kind chosen at compile time: K = kGridExact or
+    // kGridFine (which must equal fine) spares a search loop the branch on
+    // every call; kGridAny branches on fine.
+    template <int K>
+    __device__ __forceinline__ float at_t(int j) const {
+        if (K == kGridAny) return at(j);
+        if (K == kGridFine) return __int_as_float(lo_bits + j);
+        const float fj = static_cast<float>(j);
+        return fmaf(fj, step_hi, fmaf(fj, step_lo, lo0));
+    }
+    template <int K>
+    __device__ __forceinline__ int near_t(float T) const {
+        if (K == kGridAny) return near(T);
+        if (K == kGridFine) return __float_as_int(T) - lo_bits;
         return __float2int_rd(fminf((T - lo0) * inv_step, 2.0e9f));
     }
 };
@@ -379,7 +399,7 @@ constexpr float kNarrowFarEnd = 0.1f;
 // from the end moved last with doubling strides.  One lg2 and one
 // reciprocal of S serve both the decision and the next step.  Returns T,
 // 1/T, 1/S(T), the section 5.4 flag and the number of evaluations made.
-template <class Eval3, class Eval2>
+template <int K, class Eval3, class Eval2>
 __device__ __forceinline__ void narrow_search(const SearchCfg& cfg, float S1,
                                               float V1, float W1, bool strict,
                                               Eval3 eval3, Eval2 eval2,
@@ -395,7 +415,7 @@ __device__ __forceinline__ void narrow_search(const SearchCfg& cfg, float S1,
     if (cfg.t_min < cfg.hi0 && strict) {
         while (jh - jl > 1) {
             const int jm = jl + ((jh - jl) >> 1);
-            const float b = rcp_approx(g.at(jm));
+            const float b = rcp_approx(g.template at_t<K>(jm));
             const float2 sv = eval2(b);
             ++evals;
             if (entropy_above(sv, b, cfg.bound_bits)) {
@@ -468,7 +488,7 @@ __device__ __forceinline__ void narrow_search(const SearchCfg& cfg, float S1,
             const float Tn = rcp_approx(bn);
             const float pf = k == 0 ? kNarrowProbeFirst : kNarrowProbeLater;
             const bool probe = !jl_eval && Tn <= pf * cfg.t_min;
-            int jn = Tn > cfg.t_min ? g.near(Tn) : 0;
+            int jn = Tn > cfg.t_min ? g.template near_t<K>(Tn) : 0;
             jn = probe ? 0 : min(max(jn, jl + 1), jh - 1);
             if (probe) {
                 pb = b;
@@ -476,7 +496,7 @@ __device__ __forceinline__ void narrow_search(const SearchCfg& cfg, float S1,
                 pV = V;
                 pW = W;
             }
-            b = rcp_approx(probe ? cfg.t_min : g.at(jn));
+            b = rcp_approx(probe ? cfg.t_min : g.template at_t<K>(jn));
             const float3 r = eval3(b);
             ++evals;
             S = r.x;
@@ -513,7 +533,7 @@ __device__ __forceinline__ void narrow_search(const SearchCfg& cfg, float S1,
             const int jm = jl == jlast ? jl + step : jh == jlast ? jh - step : jl + (d >> 1);
             stride *= 2;
             jlast = jm;
-            const float bm = rcp_approx(g.at(jm));
+            const float bm = rcp_approx(g.template at_t<K>(jm));
             const float2 sv = eval2(bm);
             ++evals;
             if (entropy_above(sv, bm, cfg.bound_bits)) {
@@ -525,7 +545,7 @@ __device__ __forceinline__ void narrow_search(const SearchCfg& cfg, float S1,
             }
         }
     }
-    const float lo = jl_eval ? g.at(jl) : cfg.t_min;
+    const float lo = jl_eval ? g.template at_t<K>(jl) : cfg.t_min;
     const float b_lo = rcp_approx(lo);
     overflow = tmin_inf;
     if (!tmin_inf && !jl_eval) {

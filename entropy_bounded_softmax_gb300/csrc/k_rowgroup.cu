@@ -84,8 +84,8 @@ rowgroup_kernel(RowTask t, int vec) {
                 y[i] = make_float4(e[0], e[1], e[2], e[3]);
             }
         }
-        const RowSolution sol = solve_row<G, E4>(y, m, bad, cfg, bound_bits,
-                                                 t.strict != 0, gmask);
+        const RowSolution sol = solve_row<G, E4, (E4 < 8)>(y, m, bad, cfg, bound_bits,
+                                                          t.strict != 0, gmask);
         const unsigned int bits = sol.bits;
         const float T_row = sol.T_row;
         const float beta_out = sol.beta_out, inv_s = sol.inv_s;
