@@ -431,19 +431,76 @@ __device__ __forceinline__ void narrow_search(const SearchCfg& cfg, float S1,
         float ls = lg2_approx(S);  // log2 S, shared by the decision and the step
         // The point evaluated before a t_min probe (its beta and sums).
         float pb = 1.0f, pS = S1, pV = V1, pW = W1;
-        bool after_probe = false;  // the last round probed t_min, feasible
-        bool last_feas = false;    // the side of the last point evaluated
+        // The side of the point the next step starts from, and whether the
+        // far-end guard applies to that step (not right after stepping
+        // back to the point before a probe).
+        bool anchor_feas = false;
+        bool far_guard = false;
         float b_inf = rcp_approx(cfg.hi0);
         float b_feas = rcp_approx(cfg.t_min);
         const bool log_newton = cfg.bound > 0.0f;
         int jlast = -1;
+        // The round's bookkeeping is written as selects rather than
+        // branches: the lane groups of a warp take different sides at
+        // every round, and each branch would be run for both.
         for (int k = 0; k < kNarrowNewtonRounds && jh - jl > 1 && !tmin_inf; ++k) {
-            // The point stepped from is the bracket end evaluated last (from
-            // the second round on), feasible or not.
-            const bool at_end = k > 0;
-            bool anchor_feas = last_feas;
-            bool far_guard = at_end;
-            if (after_probe) {
+            const bool at_end = k > 0;  // the step starts from a bracket end
+            const float is = rcp_approx(S);
+            const float ey = V * is;
+            const float H = kLn2 * (ls - b * ey);
+            const float dH = -b * (kLn2 * kLn2) * fmaxf(fmaf(W, is, -ey * ey), 0.0f);
+            // Newton on log H (log2 H - log2 bound over its slope) when the
+            // bound is positive, else on H itself.
+            const bool on_log = log_newton && H > 0.0f;
+            const float num = on_log ? (lg2_approx(H) - cfg.lg2_bound) * H : H - cfg.bound;
+            const float den = on_log ? dH * kLog2e : dH;
+            float bn = b - num * rcp_approx(den);
+            // A step that points back past the end it starts from (H there
+            // equal to the bound in fp32, or on the wrong side of it by a
+            // rounding) is kept: the clamp below then takes that end's
+            // inner neighbour, which closes the bracket when the crossing
+            // is next to it.  A step that leaves the bracket otherwise, or
+            // lands next to its far end, takes the geometric midpoint.
+            const bool outside = !(bn > b_inf && bn < b_feas);
+            const bool back = at_end && (anchor_feas ? bn >= b_feas : bn <= b_inf);
+            const float far = anchor_feas ? b_inf : b_feas;
+            const bool by_far = far_guard && fabsf(far - bn) < kNarrowFarEnd * fabsf(far - b);
+            if (outside ? !back : by_far) bn = sqrtf(b_inf * b_feas);
+            const float Tn = rcp_approx(bn);
+            const float pf = k == 0 ? kNarrowProbeFirst : kNarrowProbeLater;
+            const bool probe = !jl_eval && Tn <= pf * cfg.t_min;
+            int jn = Tn > cfg.t_min ? g.template near_t<K>(Tn) : 0;
+            jn = probe ? 0 : min(max(jn, jl + 1), jh - 1);
+            pb = probe ? b : pb;
+            pS = probe ? S : pS;
+            pV = probe ? V : pV;
+            pW = probe ? W : pW;
+            b = rcp_approx(probe ? cfg.t_min : g.template at_t<K>(jn));
+            const float3 r = eval3(b);
+            ++evals;
+            S = r.x;
+            V = r.y;
+            W = r.z;
+            // entropy_above's test, with log2 S kept for the next step.
+            ls = lg2_approx(S);
+            const bool inf = fmaf(S, ls - cfg.bound_bits, -b * V) > 0.0f;
+            const bool feas = !inf;
+            jlast = jn;
+            s_lo = (probe || feas) ? S : s_lo;
+            tmin_inf = tmin_inf || (probe && inf);
+            jl_eval = jl_eval || feas;
+            b_feas = feas ? b : b_feas;
+            const bool move_hi = !probe && inf;
+            const bool move_lo = !probe && feas;
+            jh = move_hi ? jn : jh;
+            b_inf = move_hi ? b : b_inf;
+            jl = move_lo ? jn : jl;
+            anchor_feas = feas;
+            far_guard = true;
+            if (probe && feas) {
+                // t_min is feasible: the next step starts from whichever of
+                // t_min and the point before the probe has H nearer the
+                // bound (in log terms).
                 const float h_t = kLn2 * (ls - b * V * rcp_approx(S));
                 const float h_p = kLn2 * (lg2_approx(pS) - pb * pV * rcp_approx(pS));
                 const float lb = log_newton ? cfg.lg2_bound : 0.0f;
@@ -459,71 +516,6 @@ __device__ __forceinline__ void narrow_search(const SearchCfg& cfg, float S1,
                     anchor_feas = false;
                     far_guard = false;
                 }
-                after_probe = false;
-            }
-            const float is = rcp_approx(S);
-            const float ey = V * is;
-            const float H = kLn2 * (ls - b * ey);
-            const float dH = -b * (kLn2 * kLn2) * fmaxf(fmaf(W, is, -ey * ey), 0.0f);
-            float bn;
-            if (log_newton && H > 0.0f) {
-                const float gl = lg2_approx(H) - cfg.lg2_bound;
-                bn = b - gl * H * rcp_approx(dH * kLog2e);
-            } else {
-                bn = b - (H - cfg.bound) * rcp_approx(dH);
-            }
-            // A step that points back past the end it starts from (H there
-            // equal to the bound in fp32, or on the wrong side of it by a
-            // rounding) is kept: the clamp below then takes that end's
-            // inner neighbour, which closes the bracket when the crossing
-            // is next to it.
-            if (!(bn > b_inf && bn < b_feas)) {
-                const bool back = at_end && (anchor_feas ? bn >= b_feas : bn <= b_inf);
-                if (!back) bn = sqrtf(b_inf * b_feas);
-            } else if (far_guard) {
-                const float far = anchor_feas ? b_inf : b_feas;
-                if (fabsf(far - bn) < kNarrowFarEnd * fabsf(far - b))
-                    bn = sqrtf(b_inf * b_feas);
-            }
-            const float Tn = rcp_approx(bn);
-            const float pf = k == 0 ? kNarrowProbeFirst : kNarrowProbeLater;
-            const bool probe = !jl_eval && Tn <= pf * cfg.t_min;
-            int jn = Tn > cfg.t_min ? g.template near_t<K>(Tn) : 0;
-            jn = probe ? 0 : min(max(jn, jl + 1), jh - 1);
-            if (probe) {
-                pb = b;
-                pS = S;
-                pV = V;
-                pW = W;
-            }
-            b = rcp_approx(probe ? cfg.t_min : g.template at_t<K>(jn));
-            const float3 r = eval3(b);
-            ++evals;
-            S = r.x;
-            V = r.y;
-            W = r.z;
-            // entropy_above's test, with log2 S kept for the next step.
-            ls = lg2_approx(S);
-            const bool inf = fmaf(S, ls - cfg.bound_bits, -b * V) > 0.0f;
-            jlast = jn;
-            last_feas = !inf;
-            if (probe) {
-                s_lo = S;
-                if (inf) {
-                    tmin_inf = true;
-                } else {
-                    jl_eval = true;
-                    b_feas = b;
-                    after_probe = true;
-                }
-            } else if (inf) {
-                jh = jn;
-                b_inf = b;
-            } else {
-                jl = jn;
-                jl_eval = true;
-                s_lo = S;
-                b_feas = b;
             }
         }
         int stride = 1;
