@@ -42,6 +42,7 @@ class cs_plan(ctypes.Structure):
         ("grid_ctas", ctypes.c_int64),
         ("staged_tensors", ctypes.c_int32),
         ("tensor_cores", ctypes.c_int32),
+        ("fan_points", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

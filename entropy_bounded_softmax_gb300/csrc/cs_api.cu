@@ -221,6 +221,41 @@ cs_status plan_cluster(int64_t batch, int32_t C, const cs_options& o,
     const int64_t max_rows = kMaxGridX / n;
     if (rows > max_rows) rows = max_rows;
     p->grid_ctas = rows * n;
+    // Launches of at most one wave are bound by the slowest row's chain of
+    // rounds: there the fan, a few more exponentials per class in the T = 1
+    // pass, saves rounds.  Wider launches are bound by throughput, where the
+    // extra exponentials cost more than the rounds they save.  The fan runs
+    // in clusters of CTAs of at most 256 threads, built with registers for
+    // 512 threads an SM (cs::kFanThreadsPerSm).
+    const int64_t fan_ctas_per_sm = cs::kFanThreadsPerSm / p->threads_per_cta;
+    const int64_t resident =
+        fan_ctas_per_sm < p->ctas_per_sm ? fan_ctas_per_sm : p->ctas_per_sm;
+    const bool one_wave = p->grid_ctas <= static_cast<int64_t>(sm_count) * resident;
+    p->fan_points = (o.strict == 0 && n > 1 && p->threads_per_cta <= 256 && one_wave)
+        ? cs::kFanPoints : 0;
+    if (p->fan_points > 0 && o.param == 0 && o.threads == 0 &&
+        p->grid_ctas > 2 * static_cast<int64_t>(sm_count)) {
+        // With the fan the T = 1 pass is about twice as long, and a CTA
+        // that shares its SM with two others holds up its whole cluster's
+        // first exchange: when the widening above rounded up past two CTAs
+        // an SM, take instead the largest power-of-two cluster that keeps
+        // at most two on every SM (32 x 50000: clusters of 8 x 128, 14.5 us,
+        // against 15.3 us in the clusters of 10).
+        int nf = 1;
+        while (nf * 2 <= max_cluster && nf * 2 <= C / kMinWideSlice &&
+               rows * nf * 2 <= 2 * static_cast<int64_t>(sm_count))
+            nf *= 2;
+        cs_plan q = *p;
+        if (nf > 1 && nf != n && ceil_div(C, nf) <= cs::kTargetSlice &&
+            cluster_geometry(batch, C, nf, 0, sm_count, smem_optin, &q) &&
+            q.threads_per_cta <= 256) {
+            const int bs = static_cast<int>(smem_per_sm / (q.smem_bytes + 1024));
+            const int bt = 2048 / q.threads_per_cta;
+            q.ctas_per_sm = bs < bt ? bs : bt;
+            q.grid_ctas = rows * nf;
+            *p = q;
+        }
+    }
     return CS_OK;
 }
 
@@ -492,6 +527,14 @@ cs_status forward(const void* logits, bool in_bf16, float* out, int64_t batch,
     task.wait_limit_cycles = cs::kWaitLimitCycles;
     task.evals_out = options ? options->evals_out : nullptr;
     task.in_bf16 = in_bf16 ? 1 : 0;
+    // The fan's inverse temperatures sqrt(1 / (hi0 t_min)) times 1/4, 1 and
+    // 4: the middle of the search's range in log beta and a factor 4 on
+    // either side; only when that range spans a factor 64 or more.
+    task.fan_beta0 = 0.0f;
+    if (p.variant == CS_VARIANT_CLUSTER && p.fan_points > 0 &&
+        entropy_bound > 0.0f && 64.0 * t_min <= task.hi0)
+        task.fan_beta0 = static_cast<float>(
+            0.25 / sqrt(static_cast<double>(task.hi0) * t_min));
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;

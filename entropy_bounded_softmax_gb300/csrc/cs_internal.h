@@ -39,12 +39,21 @@ struct RowTask {
     uint64_t wait_limit_cycles;
     int32_t* evals_out;    // may be null: temperatures evaluated per row
     int32_t in_bf16;       // 1: logits are bf16 (promoted exactly to fp32)
+    float fan_beta0;       // cluster kernel: the fan's first inverse
+                           // temperature (the others 4 and 16 times it),
+                           // evaluated with T = 1; 0: no fan
 };
 
 // Cluster kernel geometry.
 constexpr int kMaxCluster = 16;
+// Temperatures the cluster kernel evaluates with T = 1 in few-row launches
+// (the fan: beta0, 4 beta0, 16 beta0, so that one exponential and two
+// squarings give all three), and the threads an SM the fan instantiations
+// keep registers for (__launch_bounds__(256, 2)).
+constexpr int kFanPoints = 3;
+constexpr int kFanThreadsPerSm = 512;
 constexpr int kClusterMaxThreads = 512;
-constexpr int kSlotVals = 8;          // floats per exchange slot
+constexpr int kSlotVals = 12;         // floats per exchange slot (48 bytes)
 
 // Byte offsets of the cluster kernel's dynamic shared memory for `warps`
 // warps and cluster size n: the exchange slots [2][n * warps][kSlotVals]

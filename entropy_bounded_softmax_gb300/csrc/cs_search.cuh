@@ -137,7 +137,8 @@ struct Search {
     float SA;           // S at G(jl) when jl was evaluated; S at t_min when
                         // t_min was found infeasible or in the final round
     float b_jl, b_jh;   // beta of the bracket's ends (t_min while unevaluated)
-    float bc, Hc, dHc;  // Newton anchor: beta, H (nats), dH/dbeta
+    float bc, Hc, dHc;  // Newton anchor: beta, H (nats), dH/dbeta; with
+                        // kFirst, bc is the next round's point instead
 };
 
 constexpr uint32_t kJlEval = 1u;     // G(jl) was evaluated feasible
@@ -147,6 +148,7 @@ constexpr uint32_t kDone = 8u;
 constexpr uint32_t kStrict = 16u;    // halve the bracket one point per round
 constexpr uint32_t kEndgame = 32u;   // Newton has converged
 constexpr uint32_t kOverflow = 64u;  // section 5.4: even t_min violates the bound
+constexpr uint32_t kFirst = 128u;    // the next round evaluates 1/bc (after a fan)
 
 // H (nats) and dH/dbeta at beta from the sums, given ls = log2 S and
 // is = 1 / S.
@@ -220,6 +222,19 @@ __device__ __forceinline__ int search_plan(Search& s, const SearchCfg& c,
         return 1;
     }
     int np = 0;
+    if (s.f & kFirst) {
+        // The point the fan placed (search_fan), t_min with it when it
+        // comes within 4 t_min and no feasible point is known.
+        s.f &= ~kFirst;
+        const float Tn = rcp_approx(s.bc);
+        int jn = Tn > g.lo0 ? g.near(Tn) : 0;
+        jn = min(max(jn, s.jl + 1), s.jh - 1);
+        s.jl_prev = s.jl;
+        s.jh_prev = s.jh;
+        put_point(J, np, jn);
+        if (!(s.f & kJlEval) && Tn <= 4.0f * g.lo0) put_point(J, np, 0);
+        return np;
+    }
     if (s.f & kEndgame) {
         const bool lo_moved = s.jl != s.jl_prev, hi_moved = s.jh != s.jh_prev;
         s.jl_prev = s.jl;
@@ -304,6 +319,89 @@ __device__ __forceinline__ bool newton_next(const Search& s) {
            s.rounds + 1 < kMaxNewtonRounds;
 }
 
+// Moves the bracket's ends with the decisions inf[i] at grid points J[i]
+// (inverse temperatures beta[i], sums S[i]), i < np: feasible points raise
+// jl, then infeasible ones lower jh; a point the bracket no longer contains
+// is already decided and skipped.
+__device__ __forceinline__ void bracket_update(Search& s, int np,
+                                               const int (&J)[kMaxPoints],
+                                               const float (&beta)[kMaxPoints],
+                                               const float (&S)[kMaxPoints],
+                                               const bool (&inf)[kMaxPoints]) {
+#pragma unroll
+    for (int i = 0; i < kMaxPoints; ++i) {
+        if (i >= np || inf[i]) continue;
+        const bool inside = J[i] > s.jl || (J[i] == 0 && !(s.f & kJlEval));
+        if (inside && J[i] < s.jh) {
+            s.jl = J[i];
+            s.f |= kJlEval;
+            s.SA = S[i];
+            s.b_jl = beta[i];
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < kMaxPoints; ++i) {
+        if (i >= np || !inf[i]) continue;
+        if (J[i] == 0 && !(s.f & kJlEval)) {
+            s.f |= kTminInf;
+            s.SA = S[i];
+        } else if (J[i] > s.jl && J[i] < s.jh) {
+            s.jh = J[i];
+            s.b_jh = beta[i];
+        }
+    }
+}
+
+// Temperatures evaluated alongside T = 1 by the few-row launches of the
+// cluster kernel (the "fan"): they place the search's first point.
+constexpr int kFanPoints = cs::kFanPoints;
+
+// Takes in the fan evaluated with the T = 1 pass: (S[k], V[k]) at inverse
+// temperatures beta[k] (increasing; not grid points, and their decisions
+// do not move the bracket), with H(1) > bound from (S1, V1).  The next
+// round evaluates the point where log H, interpolated linearly in log beta
+// between the two of {1, beta[0..]} that straddle the bound, meets it (the
+// line through the last two when the whole fan lies above the bound), and
+// the Newton steps start from there (its round accumulates W).
+__device__ __forceinline__ void search_fan(Search& s, const SearchCfg& c,
+                                           const float (&beta)[kFanPoints],
+                                           const float (&S)[kFanPoints],
+                                           const float (&V)[kFanPoints],
+                                           float S1, float V1) {
+    // (log2 beta, log2 H in bits) of T = 1 and the fan.
+    float x[kFanPoints + 1], y[kFanPoints + 1];
+    x[0] = 0.0f;
+    y[0] = lg2_approx(lg2_approx(S1) - V1 * rcp_approx(S1));
+#pragma unroll
+    for (int i = 0; i < kFanPoints; ++i) {
+        x[i + 1] = lg2_approx(beta[i]);
+        y[i + 1] = lg2_approx(lg2_approx(S[i]) - beta[i] * V[i] * rcp_approx(S[i]));
+    }
+    const float ly = c.lg2_bound - lg2_approx(kLn2);  // log2 of the bound in bits
+    // The first point at or below the bound, and the one before it.
+    int i1 = kFanPoints;
+#pragma unroll
+    for (int i = kFanPoints; i >= 1; --i)
+        if (y[i] <= ly) i1 = i;
+    float xa = x[0], ya = y[0], xb = x[1], yb = y[1];
+#pragma unroll
+    for (int i = 1; i <= kFanPoints; ++i) {
+        if (i == i1) {
+            xa = x[i - 1];
+            ya = y[i - 1];
+            xb = x[i];
+            yb = y[i];
+        }
+    }
+    // A point beyond an end of the bracket (an extended line overshoots
+    // where H falls steeply) is moved to that end: the clamp to the
+    // bracket's inner points follows in search_plan.
+    float b0 = ex2(xa + (ly - ya) * (xb - xa) * rcp_approx(yb - ya));
+    b0 = b0 == b0 ? fminf(fmaxf(b0, s.b_jh), s.b_jl) : sqrtf(s.b_jh * s.b_jl);
+    s.bc = b0;
+    s.f |= kFirst;
+}
+
 // Records the round's evaluations: grid point J[i] (at inverse temperature
 // beta[i]) gave the row sums S[i], V[i], and, when has_w, W[0].  Feasible
 // points raise jl, then infeasible ones lower jh; a point the bracket no
@@ -327,28 +425,7 @@ __device__ __forceinline__ void search_update(Search& s, const SearchCfg& c,
         s.f |= kDone | (inf[0] ? kOverflow : 0u);
         return;
     }
-#pragma unroll
-    for (int i = 0; i < kMaxPoints; ++i) {
-        if (i >= np || inf[i]) continue;
-        const bool inside = J[i] > s.jl || (J[i] == 0 && !(s.f & kJlEval));
-        if (inside && J[i] < s.jh) {
-            s.jl = J[i];
-            s.f |= kJlEval;
-            s.SA = S[i];
-            s.b_jl = beta[i];
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < kMaxPoints; ++i) {
-        if (i >= np || !inf[i]) continue;
-        if (J[i] == 0 && !(s.f & kJlEval)) {
-            s.f |= kTminInf;
-            s.SA = S[i];
-        } else if (J[i] > s.jl && J[i] < s.jh) {
-            s.jh = J[i];
-            s.b_jh = beta[i];
-        }
-    }
+    bracket_update(s, np, J, beta, S, inf);
     // The Newton anchor moves to the round's first point (only used when
     // a Newton step follows, which is when W was accumulated).
     if (has_w) {

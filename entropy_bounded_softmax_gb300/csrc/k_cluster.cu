@@ -122,20 +122,28 @@ struct OpSum {
 
 // Partial softmax statistics of a set of classes: {m, S, V, W, code} with
 // m the set's max, y = (l - m) log2 e, S = sum 2^y, V = sum y 2^y,
-// W = sum y^2 2^y, and code the set's NaN/Inf code.  Combining rescales
-// both sides to the larger max: with d = (m_i - m) log2 e <= 0, a side
-// contributes 2^d S_i, 2^d (V_i + d S_i) and 2^d (W_i + 2 d V_i + d^2 S_i).
-// An empty side (S = 0) contributes nothing.  Explicit roundings keep the
-// compiler from contracting the two sides differently.
-struct OpSoftmax {
-    static __device__ __forceinline__ void identity(float (&a)[5]) {
+// W = sum y^2 2^y, and code the set's NaN/Inf code, then, for each of NF
+// fan points at inverse temperature b_k = fb0 4^k, S_k = sum 2^(b_k y) and
+// V_k = sum y 2^(b_k y).  Combining rescales both sides to the larger max:
+// with d = (m_i - m) log2 e <= 0, a side contributes 2^d S_i,
+// 2^d (V_i + d S_i) and 2^d (W_i + 2 d V_i + d^2 S_i), and at fan point k
+// f_k S_k,i and f_k (V_k,i + d S_k,i) with f_k = 2^(b_k d) (f_0 from the
+// ex2 unit, each next one the previous squared twice).  An empty side
+// (S = 0) contributes nothing.  Explicit roundings keep the compiler from
+// contracting the two sides differently.
+template <int NF>
+struct OpSoftmaxT {
+    static constexpr int kN = 5 + 2 * NF;
+    float fb0;  // the fan's first inverse temperature
+
+    __device__ __forceinline__ void identity(float (&a)[kN]) const {
         a[0] = -INFINITY;
-        a[1] = a[2] = a[3] = a[4] = 0.0f;
+#pragma unroll
+        for (int i = 1; i < kN; ++i) a[i] = 0.0f;
     }
-    static __device__ __forceinline__ void side(const float (&a)[5], float m,
+    static __device__ __forceinline__ void side(const float (&a)[kN], float d,
                                                 float& tS, float& tV,
                                                 float& tW) {
-        const float d = __fmul_rn(__fsub_rn(a[0], m), kLog2e);
         const float f = ex2(d);
         const bool live = a[1] > 0.0f;
         tS = live ? __fmul_rn(f, a[1]) : 0.0f;
@@ -143,12 +151,35 @@ struct OpSoftmax {
         tW = live ? __fmul_rn(f, __fmaf_rn(d, __fmaf_rn(d, a[1], __fmul_rn(2.0f, a[2])), a[3]))
                   : 0.0f;
     }
-    static __device__ __forceinline__ void combine(float (&a)[5],
-                                                   const float (&b)[5]) {
+    __device__ __forceinline__ void combine(float (&a)[kN],
+                                            const float (&b)[kN]) const {
         const float m = fmaxf(a[0], b[0]);
+        const float da = __fmul_rn(__fsub_rn(a[0], m), kLog2e);
+        const float db = __fmul_rn(__fsub_rn(b[0], m), kLog2e);
         float aS, aV, aW, bS, bV, bW;
-        side(a, m, aS, aV, aW);
-        side(b, m, bS, bV, bW);
+        side(a, da, aS, aV, aW);
+        side(b, db, bS, bV, bW);
+        if (NF > 0) {
+            float fa = ex2(__fmul_rn(fb0, da));
+            float fb = ex2(__fmul_rn(fb0, db));
+#pragma unroll
+            for (int k = 0; k < NF; ++k) {
+                if (k > 0) {
+                    fa = __fmul_rn(fa, fa);
+                    fa = __fmul_rn(fa, fa);
+                    fb = __fmul_rn(fb, fb);
+                    fb = __fmul_rn(fb, fb);
+                }
+                const int iS = 5 + 2 * k, iV = 6 + 2 * k;
+                const bool la = a[iS] > 0.0f, lb = b[iS] > 0.0f;
+                const float sa = la ? __fmul_rn(fa, a[iS]) : 0.0f;
+                const float va = la ? __fmul_rn(fa, __fmaf_rn(da, a[iS], a[iV])) : 0.0f;
+                const float sb = lb ? __fmul_rn(fb, b[iS]) : 0.0f;
+                const float vb = lb ? __fmul_rn(fb, __fmaf_rn(db, b[iS], b[iV])) : 0.0f;
+                a[iS] = __fadd_rn(sa, sb);
+                a[iV] = __fadd_rn(va, vb);
+            }
+        }
         a[0] = m;
         a[1] = __fadd_rn(aS, bS);
         a[2] = __fadd_rn(aV, bV);
@@ -156,17 +187,18 @@ struct OpSoftmax {
         a[4] = fmaxf(a[4], b[4]);
     }
 };
+using OpSoftmax = OpSoftmaxT<0>;
 
 // Shuffle-tree all-reduce over the warp; every lane ends with the same
 // (bit-identical) values.
 template <class Op, int NV>
-__device__ __forceinline__ void warp_reduce(float (&a)[NV]) {
+__device__ __forceinline__ void warp_reduce(float (&a)[NV], const Op& op) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         float b[NV];
 #pragma unroll
         for (int i = 0; i < NV; ++i) b[i] = __shfl_xor_sync(0xffffffffu, a[i], o);
-        Op::combine(a, b);
+        op.combine(a, b);
     }
 }
 
@@ -174,12 +206,12 @@ __device__ __forceinline__ void warp_reduce(float (&a)[NV]) {
 // thread's a[0..NV); returns the same bits in every thread of the cluster.
 template <bool CLUSTER, class Op, int NV>
 __device__ __forceinline__ void exchange(float (&a)[NV], const Smem& sm,
-                                         Exch& x) {
+                                         Exch& x, const Op& op) {
     static_assert(NV <= kSlotVals, "payload");
     constexpr int NE = NV + (NV & 1);   // pushed as pairs
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    warp_reduce<Op, NV>(a);
+    warp_reduce<Op, NV>(a, op);
     const uint32_t buf = x.xk & 1u;
     const uint32_t parity = (x.xk >> 1) & 1u;
     ++x.xk;
@@ -206,24 +238,27 @@ __device__ __forceinline__ void exchange(float (&a)[NV], const Smem& sm,
         }
         if (!mbar_wait<CLUSTER>(&sm.cbar[buf], parity, x.limit)) x.dead = true;
     }
-    Op::identity(a);
+    op.identity(a);
     for (int k = lane; k < nslot; k += 32) {
-        // A slot is kSlotVals = 8 floats, 32-byte aligned: two 128-bit loads
-        // at most.
-        float v[8];
+        // A slot is kSlotVals floats, 16-byte aligned: NV values in
+        // (NV + 3) / 4 128-bit loads.
+        constexpr int NQ = (NV + 3) / 4;
+        float v[4 * NQ];
         const float4* s4 = reinterpret_cast<const float4*>(&cs[k * kSlotVals]);
-        const float4 v0 = s4[0];
-        v[0] = v0.x; v[1] = v0.y; v[2] = v0.z; v[3] = v0.w;
-        if (NV > 4) {
-            const float4 v1 = s4[1];
-            v[4] = v1.x; v[5] = v1.y; v[6] = v1.z; v[7] = v1.w;
+#pragma unroll
+        for (int c = 0; c < NQ; ++c) {
+            const float4 q = s4[c];
+            v[4 * c] = q.x;
+            v[4 * c + 1] = q.y;
+            v[4 * c + 2] = q.z;
+            v[4 * c + 3] = q.w;
         }
         float b[NV];
 #pragma unroll
         for (int i = 0; i < NV; ++i) b[i] = v[i];
-        Op::combine(a, b);
+        op.combine(a, b);
     }
-    warp_reduce<Op, NV>(a);
+    warp_reduce<Op, NV>(a, op);
 }
 
 // Accumulators of S, V and (optionally) W at one inverse temperature: lanes
@@ -276,13 +311,21 @@ __device__ __forceinline__ void thread_to_row(float S, float& V, float* W,
 // T = 1 pass over this thread's float4s of the slice (q = t, t + nt, ...,
 // the float4s it staged): rewrites them as y = max((l - m_t) log2 e, floor)
 // with m_t this thread's max, and returns {m_t, S, V, W, code} relative to
-// m_t for the softmax reduction.
+// m_t for the softmax reduction, followed by (S_k, V_k) at the NF fan
+// points b_k = fb0 4^k, also relative to m_t: 2^(b_0 y) from the ex2 unit,
+// each next power the previous squared twice.
+template <int NF>
 __device__ __forceinline__ void transform_pass(float4* row4, int q4, float m_t,
-                                               float code, float (&out)[5]) {
+                                               float code, float fb0,
+                                               float (&out)[5 + 2 * NF]) {
     Acc<true> acc;
     acc.zero();
+    float2 fs[NF > 0 ? NF : 1], fv[NF > 0 ? NF : 1];
+#pragma unroll
+    for (int k = 0; k < NF; ++k) fs[k] = fv[k] = make_float2(0.f, 0.f);
     const float2 one = make_float2(1.0f, 1.0f);
     const float2 zero = make_float2(0.0f, 0.0f);
+    const float2 fb2 = make_float2(fb0, fb0);
     // (l - m_t) log2 e, floored, two lanes per packed operation (the same
     // roundings as the scalar subtract and multiply).
     const float2 neg_m = make_float2(-m_t, -m_t);
@@ -292,6 +335,29 @@ __device__ __forceinline__ void transform_pass(float4* row4, int q4, float m_t,
         const float2 b = mul2(add2(make_float2(l.z, l.w), neg_m), l2e);
         return make_float4(fmaxf(a.x, kYFloor), fmaxf(a.y, kYFloor),
                            fmaxf(b.x, kYFloor), fmaxf(b.y, kYFloor));
+    };
+    auto add_all = [&](float4 y) {
+        acc.add<true>(y, one, zero);
+        if (NF > 0) {
+            const float2 y01 = make_float2(y.x, y.y);
+            const float2 y23 = make_float2(y.z, y.w);
+            const float2 x01 = mul2(y01, fb2);
+            const float2 x23 = mul2(y23, fb2);
+            float2 e01 = make_float2(ex2(x01.x), ex2(x01.y));
+            float2 e23 = make_float2(ex2(x23.x), ex2(x23.y));
+#pragma unroll
+            for (int k = 0; k < NF; ++k) {
+                if (k > 0) {
+                    e01 = mul2(e01, e01);
+                    e01 = mul2(e01, e01);
+                    e23 = mul2(e23, e23);
+                    e23 = mul2(e23, e23);
+                }
+                fs[k] = add2(fs[k], add2(e01, e23));
+                fv[k] = fma2(e01, y01, fv[k]);
+                fv[k] = fma2(e23, y23, fv[k]);
+            }
+        }
     };
     // Four float4s per trip (independent chains), then the rest one by one.
     const int nt = blockDim.x;
@@ -303,7 +369,7 @@ __device__ __forceinline__ void transform_pass(float4* row4, int q4, float m_t,
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             row4[q + i * nt] = y[i];
-            acc.add<true>(y[i], one, zero);
+            add_all(y[i]);
         }
     }
     // At most three left: a pair, then a single.
@@ -312,20 +378,25 @@ __device__ __forceinline__ void transform_pass(float4* row4, int q4, float m_t,
         const float4 yb = to_y(row4[q + nt]);
         row4[q] = ya;
         row4[q + nt] = yb;
-        acc.add<true>(ya, one, zero);
-        acc.add<true>(yb, one, zero);
+        add_all(ya);
+        add_all(yb);
         q += 2 * nt;
     }
     if (q < q4) {
         const float4 y = to_y(row4[q]);
         row4[q] = y;
-        acc.add<true>(y, one, zero);
+        add_all(y);
     }
     out[0] = m_t;
     out[1] = acc.s.x + acc.s.y;
     out[2] = acc.v.x + acc.v.y;
     out[3] = acc.w.x + acc.w.y;
     out[4] = code;
+#pragma unroll
+    for (int k = 0; k < NF; ++k) {
+        out[5 + 2 * k] = fs[k].x + fs[k].y;
+        out[6 + 2 * k] = fv[k].x + fv[k].y;
+    }
 }
 
 // Number of partial sums a pass at P temperatures produces: S and V per
@@ -423,7 +494,7 @@ __device__ __forceinline__ void search_round(Search& st, const SearchCfg& cfg,
     constexpr int NV = PassOut<P, W0>::kN;
     float a[NV];
     eval_pass<P, W0>(row4, q4, beta, d, a);
-    exchange<CLUSTER, OpSum, NV>(a, sm, x);
+    exchange<CLUSTER, OpSum, NV>(a, sm, x, OpSum{});
     float S[kMaxPoints], V[kMaxPoints], W[kMaxPoints];
 #pragma unroll
     for (int p = 0; p < kMaxPoints; ++p) {
@@ -507,7 +578,7 @@ __device__ __forceinline__ void write_out(const float4* row4, const Slice& s,
 // throughput plans, 512 x 1 for the latency plans); ASYNC: stage with
 // asynchronous copies (a compile-time choice: a run-time branch between
 // the two staging loops cost the other path 1.4% at 32 x 50000).
-template <bool CLUSTER, int MAXT, int MINB, bool ASYNC, class In>
+template <bool CLUSTER, int MAXT, int MINB, bool ASYNC, class In, bool FAN>
 __global__ void __launch_bounds__(MAXT, MINB)
 cluster_kernel(RowTask t, int n, int slice_len) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -552,6 +623,10 @@ cluster_kernel(RowTask t, int n, int slice_len) {
                         make_grid(t.t_min, fmaxf(t.hi0, t.t_min), t.max_iter)};
     Exch x{warps, n, rank, 0u, t.wait_limit_cycles, false};
     bool reported = false;
+    // The fan (FAN instantiations, few-row launches): kFanPoints
+    // temperatures evaluated with the T = 1 pass, which place the search's
+    // first point.
+    const int nfan = (FAN && t.fan_beta0 > 0.0f && !t.strict) ? kFanPoints : 0;
 
     for (int64_t r = cid; r < t.batch; r += ncl) {
         const typename In::T* src =
@@ -655,16 +730,31 @@ cluster_kernel(RowTask t, int n, int slice_len) {
             }
             code = nan_seen ? 2.0f : 1.0f;
         }
-        // T = 1 pass relative to this thread's max, then one reduction that
-        // forms the row's max, its S, V, W at T = 1 (rescaled to that max)
-        // and its NaN/Inf code: no separate exchange of the max.
-        float s1[5];
-        transform_pass(row4, s.q4, m_t, code, s1);
-        if (CLUSTER && !waited) {
-            cluster_wait();
-            waited = true;
+        // T = 1 pass relative to this thread's max (with the fan's points
+        // when there is one), then one reduction that forms the row's max,
+        // its S, V, W at T = 1 and the fan's sums (rescaled to that max) and
+        // its NaN/Inf code: no separate exchange of the max.
+        constexpr int NVF = OpSoftmaxT<kFanPoints>::kN;
+        float s1[NVF];
+        if (FAN && nfan > 0) {
+            transform_pass<kFanPoints>(row4, s.q4, m_t, code, t.fan_beta0, s1);
+            if (CLUSTER && !waited) {
+                cluster_wait();
+                waited = true;
+            }
+            exchange<CLUSTER, OpSoftmaxT<kFanPoints>, NVF>(
+                s1, sm, x, OpSoftmaxT<kFanPoints>{t.fan_beta0});
+        } else {
+            float s5[5];
+            transform_pass<0>(row4, s.q4, m_t, code, 0.0f, s5);
+            if (CLUSTER && !waited) {
+                cluster_wait();
+                waited = true;
+            }
+            exchange<CLUSTER, OpSoftmax, 5>(s5, sm, x, OpSoftmax{0.0f});
+#pragma unroll
+            for (int i = 0; i < NVF; ++i) s1[i] = i < 5 ? s5[i < 5 ? i : 0] : 0.0f;
         }
-        exchange<CLUSTER, OpSoftmax, 5>(s1, sm, x);
         const float m = s1[0];
         const int row_code = static_cast<int>(s1[4]);
         // This thread's y offset: y (row) = y (stored) + d.
@@ -672,7 +762,7 @@ cluster_kernel(RowTask t, int n, int slice_len) {
 
         float* dst = t.out + r * C + s0;
         unsigned int bits = 0;
-        int evals = 1;  // the T = 1 pass
+        int evals = 1 + (row_code == 0 ? nfan : 0);  // the T = 1 pass and the fan
         float T_row = NAN;
         float beta_out = 0.0f, inv_s = 0.0f;
         if (row_code == 0) {
@@ -688,6 +778,12 @@ cluster_kernel(RowTask t, int n, int slice_len) {
                     const int J1[kMaxPoints] = {0, 0, 0};
                     search_round<CLUSTER, 1, false>(st, cfg, J1, row4, s.q4, d, sm, x);
                     ++evals;
+                } else if (FAN && nfan > 0) {
+                    const float b0 = t.fan_beta0;
+                    const float fbeta[kFanPoints] = {b0, 4.0f * b0, 16.0f * b0};
+                    const float Sf[kFanPoints] = {s1[5], s1[7], s1[9]};
+                    const float Vf[kFanPoints] = {s1[6], s1[8], s1[10]};
+                    search_fan(st, cfg, fbeta, Sf, Vf, s1[1], s1[2]);
                 }
                 while (!(st.f & kDone)) {
                     int J[kMaxPoints] = {0, 0, 0};
@@ -740,11 +836,11 @@ cluster_kernel(RowTask t, int n, int slice_len) {
     }
 }
 
-template <bool CLUSTER, int MAXT, int MINB, bool ASYNC, class In>
+template <bool CLUSTER, int MAXT, int MINB, bool ASYNC, class In, bool FAN = false>
 cudaError_t launch_one(const RowTask& task, int cluster_size, int slice_len,
                        int threads, int smem_bytes, int64_t grid_ctas,
                        cudaStream_t stream, int attr_slot) {
-    auto kern = cluster_kernel<CLUSTER, MAXT, MINB, ASYNC, In>;
+    auto kern = cluster_kernel<CLUSTER, MAXT, MINB, ASYNC, In, FAN>;
     cudaError_t e = ensure_smem_attribute(reinterpret_cast<const void*>(kern),
                                           attr_slot, smem_bytes, CLUSTER);
     if (e != cudaSuccess) return e;
@@ -774,7 +870,15 @@ cudaError_t launch_cluster_as(const RowTask& task, int cluster_size,
                               int64_t grid_ctas, cudaStream_t stream) {
     const bool narrow = threads <= 256;
     // Attribute slots: fp32 0-7, bf16 19-26 (8-18 belong to the other
-    // operations' kernels).
+    // operations' kernels); the fan instantiations (clusters of CTAs of at
+    // most 256 threads, registers for two such CTAs an SM: the fan's one-wave
+    // launches need no more) 52-55.
+    if (task.fan_beta0 > 0.0f && narrow && cluster_size > 1) {
+        const int fslot = 52 + (In::kBytes == 2 ? 2 : 0) + (ASYNC ? 1 : 0);
+        return launch_one<true, 256, 2, ASYNC, In, true>(task, cluster_size, slice_len,
+                                                         threads, smem_bytes, grid_ctas,
+                                                         stream, fslot);
+    }
     const int slot = (In::kBytes == 2 ? 19 : 0) + (ASYNC ? 4 : 0) +
                      (cluster_size > 1 ? 1 : 0) + (narrow ? 0 : 2);
     if (cluster_size > 1)

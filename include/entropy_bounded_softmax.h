@@ -122,6 +122,12 @@ typedef struct cs_plan {
                                 runs on the tensor cores); rowgroup: 0     */
     int32_t tensor_cores;    /* biencoder: 1 when attn . V runs as a second
                                 kernel on the tensor cores (tcgen05.mma)  */
+    int32_t fan_points;      /* cluster forward: temperatures evaluated in
+                                the T = 1 pass to bracket the search before
+                                its first round (launches of at most one
+                                wave, bound > 0, not strict; the kernel
+                                drops them when the grid has no room);
+                                0 otherwise                                */
 } cs_plan;
 
 /*

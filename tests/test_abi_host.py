@@ -115,6 +115,29 @@ def test_auto_plans_for_the_workloads():
     assert p["grid_ctas"] == 256 * p["cluster_size"]
 
 
+def test_fan_only_for_one_wave_cluster_plans():
+    # Few rows: the fan (temperatures evaluated with T = 1) and clusters of
+    # a power of two that keep at most two CTAs on an SM.
+    st, p = plan(32, 50000)
+    assert st == 0 and p["fan_points"] == 3
+    assert p["cluster_size"] == 8 and p["threads_per_cta"] == 128
+    assert p["grid_ctas"] <= 2 * GB300["sm_count"]
+    # strict bisects from the whole interval: no fan, the widened plan.
+    st, p = plan(32, 50000, strict=1)
+    assert st == 0 and p["fan_points"] == 0 and p["cluster_size"] == 10
+    # Throughput launches (more than one wave) and one-CTA rows: none.
+    for batch, classes in ((4096, 32000), (256, 131072), (65536, 64),
+                           (4, 1000)):
+        st, p = plan(batch, classes)
+        assert st == 0 and p["fan_points"] == 0, (batch, classes)
+    # Forced plans keep their shape; the fan follows the same rule.
+    st, p = plan(32, 50000, variant=C["CS_VARIANT_CLUSTER"], param=10)
+    assert st == 0 and p["cluster_size"] == 10 and p["fan_points"] == 3
+    st, p = plan(32, 50000, variant=C["CS_VARIANT_CLUSTER"], param=4,
+                 threads=512)
+    assert st == 0 and p["fan_points"] == 0
+
+
 @pytest.mark.parametrize("classes", [1, 3, 17, 64, 511, 512, 513, 1000,
                                      4099, 32000, 50001, 131072, 600000,
                                      850000])

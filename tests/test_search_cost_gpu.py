@@ -34,9 +34,11 @@ def _sweep(name):
 
 
 # (workload, rows (None: all), mean bound, slowest-row bound); measured
-# means 7.9, 6.5, 7.1, 7.6, 9.7 and slowest rows 11, 10, 10, 12, 25.
+# means 10.2, 6.5, 7.1, 7.6, 9.7 and slowest rows 14, 10, 10, 12, 25.  The
+# 32 x 50000 launch evaluates a fan of three temperatures with T = 1 in
+# every row (counted), which saves it search rounds.
 CASES = [
-    (wl.LATENCY, None, 8.5, 13),
+    (wl.LATENCY, None, 11.0, 15),
     (wl.ROUTER, None, 7.0, 12),
     (wl.LONG, None, 7.6, 13),
     (_sweep("sweep_4096x32000_b0.05_it20"), 1024, 8.1, 16),
