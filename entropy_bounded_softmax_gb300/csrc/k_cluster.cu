@@ -133,7 +133,12 @@ struct OpSum {
 // contracting the two sides differently.
 template <int NF>
 struct OpSoftmaxT {
-    static constexpr int kN = 5 + 2 * NF;
+    // Value layout: {m, S, V, W, code} without a fan; with one W (not
+    // needed: the first Newton step starts from the fan's point) is left
+    // out, {m, S, V, code, S_0, V_0, ...}.
+    static constexpr int kCode = NF == 0 ? 4 : 3;
+    static constexpr int kFan = kCode + 1;
+    static constexpr int kN = kFan + 2 * NF;
     float fb0;  // the fan's first inverse temperature
 
     __device__ __forceinline__ void identity(float (&a)[kN]) const {
@@ -141,41 +146,41 @@ struct OpSoftmaxT {
 #pragma unroll
         for (int i = 1; i < kN; ++i) a[i] = 0.0f;
     }
-    static __device__ __forceinline__ void side(const float (&a)[kN], float d,
-                                                float& tS, float& tV,
-                                                float& tW) {
-        const float f = ex2(d);
-        const bool live = a[1] > 0.0f;
-        tS = live ? __fmul_rn(f, a[1]) : 0.0f;
-        tV = live ? __fmul_rn(f, __fmaf_rn(d, a[1], a[2])) : 0.0f;
-        tW = live ? __fmul_rn(f, __fmaf_rn(d, __fmaf_rn(d, a[1], __fmul_rn(2.0f, a[2])), a[3]))
-                  : 0.0f;
-    }
     __device__ __forceinline__ void combine(float (&a)[kN],
                                             const float (&b)[kN]) const {
         const float m = fmaxf(a[0], b[0]);
         const float da = __fmul_rn(__fsub_rn(a[0], m), kLog2e);
         const float db = __fmul_rn(__fsub_rn(b[0], m), kLog2e);
-        float aS, aV, aW, bS, bV, bW;
-        side(a, da, aS, aV, aW);
-        side(b, db, bS, bV, bW);
-        if (NF > 0) {
-            float fa = ex2(__fmul_rn(fb0, da));
-            float fb = ex2(__fmul_rn(fb0, db));
+        const float fa = ex2(da), fb = ex2(db);
+        const bool la = a[1] > 0.0f, lb = b[1] > 0.0f;
+        const float aS = la ? __fmul_rn(fa, a[1]) : 0.0f;
+        const float bS = lb ? __fmul_rn(fb, b[1]) : 0.0f;
+        const float aV = la ? __fmul_rn(fa, __fmaf_rn(da, a[1], a[2])) : 0.0f;
+        const float bV = lb ? __fmul_rn(fb, __fmaf_rn(db, b[1], b[2])) : 0.0f;
+        if (NF == 0) {
+            const int iW = NF == 0 ? 3 : 0;
+            const float aW = la ? __fmul_rn(fa, __fmaf_rn(da, __fmaf_rn(da, a[1], __fmul_rn(2.0f, a[2])), a[iW]))
+                                : 0.0f;
+            const float bW = lb ? __fmul_rn(fb, __fmaf_rn(db, __fmaf_rn(db, b[1], __fmul_rn(2.0f, b[2])), b[iW]))
+                                : 0.0f;
+            a[iW] = __fadd_rn(aW, bW);
+        } else {
+            float ga = ex2(__fmul_rn(fb0, da));
+            float gb = ex2(__fmul_rn(fb0, db));
 #pragma unroll
             for (int k = 0; k < NF; ++k) {
                 if (k > 0) {
-                    fa = __fmul_rn(fa, fa);
-                    fa = __fmul_rn(fa, fa);
-                    fb = __fmul_rn(fb, fb);
-                    fb = __fmul_rn(fb, fb);
+                    ga = __fmul_rn(ga, ga);
+                    ga = __fmul_rn(ga, ga);
+                    gb = __fmul_rn(gb, gb);
+                    gb = __fmul_rn(gb, gb);
                 }
-                const int iS = 5 + 2 * k, iV = 6 + 2 * k;
-                const bool la = a[iS] > 0.0f, lb = b[iS] > 0.0f;
-                const float sa = la ? __fmul_rn(fa, a[iS]) : 0.0f;
-                const float va = la ? __fmul_rn(fa, __fmaf_rn(da, a[iS], a[iV])) : 0.0f;
-                const float sb = lb ? __fmul_rn(fb, b[iS]) : 0.0f;
-                const float vb = lb ? __fmul_rn(fb, __fmaf_rn(db, b[iS], b[iV])) : 0.0f;
+                const int iS = kFan + 2 * k, iV = kFan + 1 + 2 * k;
+                const bool lka = a[iS] > 0.0f, lkb = b[iS] > 0.0f;
+                const float sa = lka ? __fmul_rn(ga, a[iS]) : 0.0f;
+                const float va = lka ? __fmul_rn(ga, __fmaf_rn(da, a[iS], a[iV])) : 0.0f;
+                const float sb = lkb ? __fmul_rn(gb, b[iS]) : 0.0f;
+                const float vb = lkb ? __fmul_rn(gb, __fmaf_rn(db, b[iS], b[iV])) : 0.0f;
                 a[iS] = __fadd_rn(sa, sb);
                 a[iV] = __fadd_rn(va, vb);
             }
@@ -183,8 +188,7 @@ struct OpSoftmaxT {
         a[0] = m;
         a[1] = __fadd_rn(aS, bS);
         a[2] = __fadd_rn(aV, bV);
-        a[3] = __fadd_rn(aW, bW);
-        a[4] = fmaxf(a[4], b[4]);
+        a[kCode] = fmaxf(a[kCode], b[kCode]);
     }
 };
 using OpSoftmax = OpSoftmaxT<0>;
@@ -311,14 +315,15 @@ __device__ __forceinline__ void thread_to_row(float S, float& V, float* W,
 // T = 1 pass over this thread's float4s of the slice (q = t, t + nt, ...,
 // the float4s it staged): rewrites them as y = max((l - m_t) log2 e, floor)
 // with m_t this thread's max, and returns {m_t, S, V, W, code} relative to
-// m_t for the softmax reduction, followed by (S_k, V_k) at the NF fan
+// m_t for the softmax reduction (no W with a fan; the layout of
+// OpSoftmaxT<NF>), followed by (S_k, V_k) at the NF fan
 // points b_k = fb0 4^k, also relative to m_t: 2^(b_0 y) from the ex2 unit,
 // each next power the previous squared twice.
 template <int NF>
 __device__ __forceinline__ void transform_pass(float4* row4, int q4, float m_t,
                                                float code, float fb0,
-                                               float (&out)[5 + 2 * NF]) {
-    Acc<true> acc;
+                                               float (&out)[OpSoftmaxT<NF>::kN]) {
+    Acc<NF == 0> acc;  // W at T = 1 only without a fan (out[3] = 0 with one)
     acc.zero();
     float2 fs[NF > 0 ? NF : 1], fv[NF > 0 ? NF : 1];
 #pragma unroll
@@ -387,15 +392,16 @@ __device__ __forceinline__ void transform_pass(float4* row4, int q4, float m_t,
         row4[q] = y;
         add_all(y);
     }
+    constexpr int kCode = OpSoftmaxT<NF>::kCode, kFan = OpSoftmaxT<NF>::kFan;
     out[0] = m_t;
     out[1] = acc.s.x + acc.s.y;
     out[2] = acc.v.x + acc.v.y;
-    out[3] = acc.w.x + acc.w.y;
-    out[4] = code;
+    if (NF == 0) out[3] = acc.w.x + acc.w.y;
+    out[kCode] = code;
 #pragma unroll
     for (int k = 0; k < NF; ++k) {
-        out[5 + 2 * k] = fs[k].x + fs[k].y;
-        out[6 + 2 * k] = fv[k].x + fv[k].y;
+        out[kFan + 2 * k] = fs[k].x + fs[k].y;
+        out[kFan + 1 + 2 * k] = fv[k].x + fv[k].y;
     }
 }
 
@@ -734,26 +740,36 @@ cluster_kernel(RowTask t, int n, int slice_len) {
         // when there is one), then one reduction that forms the row's max,
         // its S, V, W at T = 1 and the fan's sums (rescaled to that max) and
         // its NaN/Inf code: no separate exchange of the max.
-        constexpr int NVF = OpSoftmaxT<kFanPoints>::kN;
-        float s1[NVF];
+        // The reduced sums: {m, S, V, W, code} at T = 1 and (Sf, Vf) at the
+        // fan's points.
+        float s1[5];
+        float Sf[kFanPoints] = {0.0f, 0.0f, 0.0f}, Vf[kFanPoints] = {0.0f, 0.0f, 0.0f};
         if (FAN && nfan > 0) {
-            transform_pass<kFanPoints>(row4, s.q4, m_t, code, t.fan_beta0, s1);
+            using OpF = OpSoftmaxT<kFanPoints>;
+            float sf[OpF::kN];
+            transform_pass<kFanPoints>(row4, s.q4, m_t, code, t.fan_beta0, sf);
             if (CLUSTER && !waited) {
                 cluster_wait();
                 waited = true;
             }
-            exchange<CLUSTER, OpSoftmaxT<kFanPoints>, NVF>(
-                s1, sm, x, OpSoftmaxT<kFanPoints>{t.fan_beta0});
-        } else {
-            float s5[5];
-            transform_pass<0>(row4, s.q4, m_t, code, 0.0f, s5);
-            if (CLUSTER && !waited) {
-                cluster_wait();
-                waited = true;
-            }
-            exchange<CLUSTER, OpSoftmax, 5>(s5, sm, x, OpSoftmax{0.0f});
+            exchange<CLUSTER, OpF, OpF::kN>(sf, sm, x, OpF{t.fan_beta0});
+            s1[0] = sf[0];
+            s1[1] = sf[1];
+            s1[2] = sf[2];
+            s1[3] = 0.0f;
+            s1[4] = sf[OpF::kCode];
 #pragma unroll
-            for (int i = 0; i < NVF; ++i) s1[i] = i < 5 ? s5[i < 5 ? i : 0] : 0.0f;
+            for (int k = 0; k < kFanPoints; ++k) {
+                Sf[k] = sf[OpF::kFan + 2 * k];
+                Vf[k] = sf[OpF::kFan + 1 + 2 * k];
+            }
+        } else {
+            transform_pass<0>(row4, s.q4, m_t, code, 0.0f, s1);
+            if (CLUSTER && !waited) {
+                cluster_wait();
+                waited = true;
+            }
+            exchange<CLUSTER, OpSoftmax, 5>(s1, sm, x, OpSoftmax{0.0f});
         }
         const float m = s1[0];
         const int row_code = static_cast<int>(s1[4]);
@@ -781,8 +797,6 @@ cluster_kernel(RowTask t, int n, int slice_len) {
                 } else if (FAN && nfan > 0) {
                     const float b0 = t.fan_beta0;
                     const float fbeta[kFanPoints] = {b0, 4.0f * b0, 16.0f * b0};
-                    const float Sf[kFanPoints] = {s1[5], s1[7], s1[9]};
-                    const float Vf[kFanPoints] = {s1[6], s1[8], s1[10]};
                     search_fan(st, cfg, fbeta, Sf, Vf, s1[1], s1[2]);
                 }
                 while (!(st.f & kDone)) {
