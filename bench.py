@@ -282,6 +282,21 @@ def formula_ex2(w: wl.Workload, n_search: int) -> int:
     return (w.batch + n_search * w.max_iter) * w.num_classes
 
 
+def ex2_issued(evals, C: int, plan: dict) -> int:
+    """Exponentials the kernel issued, from its per-row evaluation counts
+    (T = 1, every point of the search, the output): each counted temperature
+    costs one exponential per class, except the fan's (plans with
+    fan_points), whose three temperatures share one exponential and two
+    squarings."""
+    e = evals.long()
+    total = int(e.sum().item())
+    nf = int(plan.get("fan_points", 0) or 0)
+    if nf > 1:
+        fan_rows = int((e >= nf + 2).sum().item())
+        total -= (nf - 1) * fan_rows
+    return total * C
+
+
 def ex2_roofline(ex2_formula: int, ex2_executed: int | None, io_bytes: int,
                  t_kernel: float, ex2_peak: float, hbm_gbs: float) -> dict:
     """The kernel against the slower of HBM (io_bytes at the measured copy
@@ -638,7 +653,7 @@ def our_arm(args, w: wl.Workload) -> int:
                            w.max_iter, out=outs[0], variant=args.variant,
                            param=args.param, threads=args.threads,
                            strict=args.strict, evals_out=evals)
-    ex2_executed = int(evals.sum().item()) * C
+    ex2_executed = ex2_issued(evals, C, plan)
 
     line = None
     if rank == 0:
@@ -809,7 +824,8 @@ def per_config_runs(torch, cs, dev, stream, ex2_peak: float, hbm_gbs: float,
         n_eval = int(evals.sum().item())
         n_search = searched_rows(w, x, h1)
         t_kernel = ms * 1e-3
-        roof = ex2_roofline(formula_ex2(w, n_search), n_eval * C, io_bytes,
+        roof = ex2_roofline(formula_ex2(w, n_search),
+                            ex2_issued(evals, C, cs.plan(B, C)), io_bytes,
                             t_kernel, ex2_peak, hbm_gbs)
         entry = {
             "batch": B, "num_classes": C, "entropy_bound": w.entropy_bound,
