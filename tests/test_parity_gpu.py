@@ -46,6 +46,21 @@ def test_latency_32x50000(variant, param, threads, strict):
     assert stats["T_zone"] == 0
 
 
+@pytest.mark.parametrize("seed", [7, 8, 9])
+@pytest.mark.parametrize("bound", [0.05, 0.2, 1.0])
+def test_few_row_launches_with_the_fan(seed, bound):
+    # The 32 x 50000 shape takes the fan (temperatures evaluated with T = 1
+    # that place the search's first point); other rows and bounds than the
+    # workload's, element by element against the oracle.
+    import entropy_bounded_softmax_gb300 as cs
+    w = wl.LATENCY.with_(seed=seed, entropy_bound=bound)
+    assert cs.plan(w.batch, w.num_classes)["fan_points"] == 3
+    x = wl.generate(w)
+    p, T, mask = run_gpu(x, **_params(w))
+    stats = compare(x, p, T, mask, _oracle(x, w), **_params(w))
+    assert stats["T_zone"] == 0
+
+
 def test_moe_router_full():
     w = wl.ROUTER
     x = wl.generate(w)
