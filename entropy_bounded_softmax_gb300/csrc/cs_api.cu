@@ -167,7 +167,7 @@ bool cluster_geometry(int64_t batch, int32_t C, int n, int threads_req,
                       int sm_count, int smem_optin, cs_plan* p) {
     const int64_t L = ceil_div(ceil_div(C, n), 4) * 4;
     const int threads = threads_req
-        ? threads_req : cs::cluster_threads_for(L, batch * n, sm_count);
+        ? threads_req : cs::cluster_threads_for(L, batch * n, sm_count, n);
     const int64_t smem = cs::cluster_smem_bytes(L, threads, n);
     if (smem > smem_optin) return false;
     p->cluster_size = n;

@@ -46,6 +46,24 @@ def test_latency_32x50000(variant, param, threads, strict):
     assert stats["T_zone"] == 0
 
 
+@pytest.mark.parametrize("C", [700, 1000, 1024, 1500, 2001, 4000])
+def test_many_rows_of_middle_width(C):
+    # Rows of up to 1024 classes run one warp each (row-group kernel, 32
+    # classes a lane); wider ones in one-CTA clusters of 64 threads when
+    # there are many rows.  Element by element against the oracle.
+    import entropy_bounded_softmax_gb300 as cs
+    w = wl.SMALL.with_(batch=1024, num_classes=C, sigma=2.0, seed=4000 + C)
+    plan = cs.plan(w.batch, C)
+    if C <= 1024:
+        assert plan["variant"] == 1 and plan["lanes_per_row"] == 32
+    elif C <= 4600:
+        assert plan["cluster_size"] == 1 and plan["threads_per_cta"] == 64
+    x = wl.generate(w)
+    p, T, mask = run_gpu(x, **_params(w))
+    stats = compare(x, p, T, mask, _oracle(x, w), **_params(w))
+    assert stats["T_zone"] == 0
+
+
 @pytest.mark.parametrize("seed", [7, 8, 9])
 @pytest.mark.parametrize("bound", [0.05, 0.2, 1.0])
 def test_few_row_launches_with_the_fan(seed, bound):
