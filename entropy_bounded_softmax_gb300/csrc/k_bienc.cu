@@ -196,7 +196,7 @@ bienc_kernel(BiencTask t, int tiles, int tiles_per_cta) {
                             make_grid(t.t_min, fmaxf(t.hi0, t.t_min), t.max_iter)};
         RowSolution sol{NAN, 0.0f, 0.0f, 0u, 0, true};
         if (live)   // uniform over the lane group
-            sol = solve_row<G, E4, false>(y, m, bad, cfg, t.entropy_bound * kLog2e,
+            sol = solve_row<G, E4, true>(y, m, bad, cfg, t.entropy_bound * kLog2e,
                                    false, gmask);
         const int64_t row = bh * t.Q + i0 + rr;
 #pragma unroll
