@@ -26,7 +26,9 @@
 // (evaluations of H in fp32 are within rounding of the bound there) it
 // gallops away from the end the last round moved, when only one moved,
 // with strides growing eightfold, else splits the bracket into quarters,
-// two halvings per round.  With one
+// two halvings per round.  The cluster kernel's few-row launches take the
+// first point instead from a fan of temperatures evaluated with T = 1
+// (search_fan).  With one
 // point per round (narrow rows, where a pass costs little next to
 // divergent bookkeeping) the Newton point is evaluated alone and the
 // neighbours follow one by one, with doubling strides.  The strict mode
