@@ -115,6 +115,26 @@ def test_auto_plans_for_the_workloads():
     assert p["grid_ctas"] == 256 * p["cluster_size"]
 
 
+def test_middle_width_plans():
+    # Up to 1024 classes: one warp a row, 32 classes a lane.
+    for classes in (513, 1000, 1024):
+        st, p = plan(4, classes)
+        assert st == 0 and p["variant"] == C["CS_VARIANT_ROWGROUP"]
+        assert p["lanes_per_row"] == 32 and p["elems_per_lane"] == 32
+    st, p = plan(4, 1025)
+    assert st == 0 and p["variant"] == C["CS_VARIANT_CLUSTER"]
+    # Many one-CTA rows: 64-thread CTAs; few rows: at least 128.
+    st, p = plan(4096, 2000)
+    assert st == 0 and p["cluster_size"] == 1 and p["threads_per_cta"] == 64
+    st, p = plan(4096, 8000)
+    assert st == 0 and p["threads_per_cta"] == 128
+    st, p = plan(4, 2000)
+    assert st == 0 and p["threads_per_cta"] >= 128
+    # The backward keeps its row-group kernel to 512 classes.
+    st, p = cs.cs_plan_backward_host(4, 1000, None, *GB300.values())
+    assert st == 0 and p.as_dict()["variant"] == C["CS_VARIANT_CLUSTER"]
+
+
 def test_fan_only_for_one_wave_cluster_plans():
     # Few rows: the fan (temperatures evaluated with T = 1) and clusters of
     # a power of two that keep at most two CTAs on an SM.
