@@ -186,9 +186,8 @@ cs_status cs_constrained_softmax_ex(const float* logits, float* out,
 
 /*
  * cs_constrained_softmax_bf16 -- the same operation on bf16 logits: a
- * work-reducing input form of section 2.1's kernel (the survey's NEXT-2
- * (iii)) that halves the bytes read per class (2 instead of 4; the output
- * stays fp32).  Each logit is promoted to fp32 on load, which is exact (a
+ * work-reducing input form of section 2.1's kernel that halves the bytes
+ * read per class (2 instead of 4; the output stays fp32).  Each logit is promoted to fp32 on load, which is exact (a
  * bf16 value is an fp32 value whose low 16 bits are zero), and from there
  * the computation is the fp32 one: the result equals, bit for bit,
  * cs_constrained_softmax on the promoted logits.
