@@ -91,15 +91,18 @@ constexpr int64_t kTargetSlice = 16384;
 // Automatic threads per CTA: about 40 classes per thread for a launch with
 // about one CTA per SM (up to a quarter more CTAs than SMs; all of a CTA's
 // time goes to one row), about 72 for larger launches (several CTAs share
-// an SM; measured: 16000-class slices run 4-5% faster on 224 threads than
-// on 256, 16384-class slices 2% slower); 128-256 threads either way (64-256
-// for many one-CTA rows), where the per-round reductions stay short.
+// an SM), rounded up to whole pairs of warps; 128-256 threads either way
+// (64-256 for many one-CTA rows), where the per-round reductions stay
+// short.
 inline int cluster_threads_for(int64_t slice_len, int64_t ctas,
                                int64_t sm_count, int n) {
     const bool many = ctas * 4 > sm_count * 5;
     const int64_t per = many ? 72 : 40;
     int64_t t = (slice_len + per - 1) / per;
-    t = ((t + 31) / 32) * 32;
+    // An even number of warps: the sweep's 16000-class slices ran 2.5-3%
+    // faster on 192 or 256 threads than on 224 (six sweep points), and 160
+    // was between.
+    t = ((t + 63) / 64) * 64;
     // At least 128 threads, or 64 for many one-CTA rows: 4096 rows of
     // 1500-4000 classes ran 20-28% faster in 64-thread CTAs than in
     // 128-thread ones (fewer warps wait at every exchange of a short row).
