@@ -32,9 +32,12 @@
 // n x warps slots in one fixed order (each lane folds slots lane, lane + 32,
 // ..., then a butterfly), so every thread of the cluster holds bit-identical
 // sums and takes the same decisions, with no CTA-wide barrier in the
-// search.  Slots and mbarriers are double-buffered, which is safe because
-// no warp can push for exchange k+2 before every warp of the cluster has
-// pushed for exchange k+1, which each does only after reading exchange k.
+// search.  The T = 1 statistics, whose partials are relative to different
+// maxima, take the max first at the warp and at the cluster stage and move
+// every partial to it once before summing.  Slots and mbarriers are
+// double-buffered, which is safe because no warp can push for exchange k+2
+// before every warp of the cluster has pushed for exchange k+1, which each
+// does only after reading exchange k.
 //
 // Every wait is bounded (cs::kWaitLimitCycles by default).  A thread whose
 // wait times out records CS_ERR_TIMEOUT and from then on neither waits nor
@@ -190,6 +193,36 @@ struct OpSoftmaxT {
         a[2] = __fadd_rn(aV, bV);
         a[kCode] = fmaxf(a[kCode], b[kCode]);
     }
+    // Moves a's sums from its own max a[0] to m >= a[0]: one side of
+    // combine, the same scalings.  An empty a (S = 0) becomes zeros.
+    __device__ __forceinline__ void rescale(float (&a)[kN], float m) const {
+        const float da = __fmul_rn(__fsub_rn(a[0], m), kLog2e);
+        const float fa = ex2(da);
+        const bool la = a[1] > 0.0f;
+        const float S = a[1], V = a[2];
+        a[0] = m;
+        a[1] = la ? __fmul_rn(fa, S) : 0.0f;
+        a[2] = la ? __fmul_rn(fa, __fmaf_rn(da, S, V)) : 0.0f;
+        if (NF == 0) {
+            const int iW = NF == 0 ? 3 : 0;
+            a[iW] = la ? __fmul_rn(fa, __fmaf_rn(da, __fmaf_rn(da, S, __fmul_rn(2.0f, V)), a[iW]))
+                       : 0.0f;
+        } else {
+            float ga = ex2(__fmul_rn(fb0, da));
+#pragma unroll
+            for (int k = 0; k < NF; ++k) {
+                if (k > 0) {
+                    ga = __fmul_rn(ga, ga);
+                    ga = __fmul_rn(ga, ga);
+                }
+                const int iS = kFan + 2 * k, iV = kFan + 1 + 2 * k;
+                const bool lka = a[iS] > 0.0f;
+                const float Sk = a[iS];
+                a[iS] = lka ? __fmul_rn(ga, Sk) : 0.0f;
+                a[iV] = lka ? __fmul_rn(ga, __fmaf_rn(da, Sk, a[iV])) : 0.0f;
+            }
+        }
+    }
 };
 using OpSoftmax = OpSoftmaxT<0>;
 
@@ -206,16 +239,18 @@ __device__ __forceinline__ void warp_reduce(float (&a)[NV], const Op& op) {
     }
 }
 
-// Reduction (Op) over every thread of the CTA and the cluster of each
-// thread's a[0..NV); returns the same bits in every thread of the cluster.
+// The cluster step of a reduction: pushes this warp's a[0..NV) (the same
+// in every lane) into slot (rank, warp) of every CTA of the cluster, waits
+// until all the cluster's slots of this exchange have landed, and leaves in
+// each lane the Op fold of slots lane, lane + 32, ... (Op's identity in a
+// lane without one).
 template <bool CLUSTER, class Op, int NV>
-__device__ __forceinline__ void exchange(float (&a)[NV], const Smem& sm,
-                                         Exch& x, const Op& op) {
+__device__ __forceinline__ void push_fold(float (&a)[NV], const Smem& sm,
+                                          Exch& x, const Op& op) {
     static_assert(NV <= kSlotVals, "payload");
     constexpr int NE = NV + (NV & 1);   // pushed as pairs
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    warp_reduce<Op, NV>(a, op);
     const uint32_t buf = x.xk & 1u;
     const uint32_t parity = (x.xk >> 1) & 1u;
     ++x.xk;
@@ -242,10 +277,9 @@ __device__ __forceinline__ void exchange(float (&a)[NV], const Smem& sm,
         }
         if (!mbar_wait<CLUSTER>(&sm.cbar[buf], parity, x.limit)) x.dead = true;
     }
-    op.identity(a);
-    for (int k = lane; k < nslot; k += 32) {
-        // A slot is kSlotVals floats, 16-byte aligned: NV values in
-        // (NV + 3) / 4 128-bit loads.
+    // A slot is kSlotVals floats, 16-byte aligned: NV values in
+    // (NV + 3) / 4 128-bit loads.
+    auto load_slot = [&](int k, float (&b)[NV]) {
         constexpr int NQ = (NV + 3) / 4;
         float v[4 * NQ];
         const float4* s4 = reinterpret_cast<const float4*>(&cs[k * kSlotVals]);
@@ -257,12 +291,69 @@ __device__ __forceinline__ void exchange(float (&a)[NV], const Smem& sm,
             v[4 * c + 2] = q.z;
             v[4 * c + 3] = q.w;
         }
-        float b[NV];
 #pragma unroll
         for (int i = 0; i < NV; ++i) b[i] = v[i];
+    };
+    // The lane's first slot is taken as it is (combining it with the
+    // identity would give the same values).
+    int k = lane;
+    if (k < nslot) {
+        load_slot(k, a);
+        k += 32;
+    } else {
+        op.identity(a);
+    }
+    for (; k < nslot; k += 32) {
+        float b[NV];
+        load_slot(k, b);
         op.combine(a, b);
     }
+}
+
+// Reduction (Op) over every thread of the CTA and the cluster of each
+// thread's a[0..NV); returns the same bits in every thread of the cluster.
+template <bool CLUSTER, class Op, int NV>
+__device__ __forceinline__ void exchange(float (&a)[NV], const Smem& sm,
+                                         Exch& x, const Op& op) {
     warp_reduce<Op, NV>(a, op);
+    push_fold<CLUSTER, Op, NV>(a, sm, x, op);
+    warp_reduce<Op, NV>(a, op);
+}
+
+// The softmax statistics (OpSoftmaxT) reduced over the warp: the max first
+// (a butterfly of one value), then every lane's partial moved to it once
+// (rescale) and the sums added (the code by max).  The same bits in every
+// lane, and one rescaling per partial where a combine tree rescales at
+// every level.
+template <int NF>
+__device__ __forceinline__ void softmax_warp_reduce(float (&a)[OpSoftmaxT<NF>::kN],
+                                                    const OpSoftmaxT<NF>& op) {
+    using Op = OpSoftmaxT<NF>;
+    float m = a[0];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    op.rescale(a, m);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        float b[Op::kN];
+#pragma unroll
+        for (int i = 1; i < Op::kN; ++i) b[i] = __shfl_xor_sync(0xffffffffu, a[i], o);
+#pragma unroll
+        for (int i = 1; i < Op::kN; ++i)
+            a[i] = i == Op::kCode ? fmaxf(a[i], b[i]) : __fadd_rn(a[i], b[i]);
+    }
+}
+
+// exchange() for the softmax statistics: the warp and the cluster stages
+// each take the max first (softmax_warp_reduce); a lane folding more than
+// one slot combines them with op.
+template <bool CLUSTER, int NF>
+__device__ __forceinline__ void softmax_exchange(float (&a)[OpSoftmaxT<NF>::kN],
+                                                 const Smem& sm, Exch& x,
+                                                 const OpSoftmaxT<NF>& op) {
+    softmax_warp_reduce<NF>(a, op);
+    push_fold<CLUSTER, OpSoftmaxT<NF>, OpSoftmaxT<NF>::kN>(a, sm, x, op);
+    softmax_warp_reduce<NF>(a, op);
 }
 
 // Accumulators of S, V and (optionally) W at one inverse temperature: lanes
@@ -752,7 +843,7 @@ cluster_kernel(RowTask t, int n, int slice_len) {
                 cluster_wait();
                 waited = true;
             }
-            exchange<CLUSTER, OpF, OpF::kN>(sf, sm, x, OpF{t.fan_beta0});
+            softmax_exchange<CLUSTER, kFanPoints>(sf, sm, x, OpF{t.fan_beta0});
             s1[0] = sf[0];
             s1[1] = sf[1];
             s1[2] = sf[2];
@@ -769,7 +860,7 @@ cluster_kernel(RowTask t, int n, int slice_len) {
                 cluster_wait();
                 waited = true;
             }
-            exchange<CLUSTER, OpSoftmax, 5>(s1, sm, x, OpSoftmax{0.0f});
+            softmax_exchange<CLUSTER, 0>(s1, sm, x, OpSoftmax{0.0f});
         }
         const float m = s1[0];
         const int row_code = static_cast<int>(s1[4]);
