@@ -433,7 +433,7 @@ __device__ __forceinline__ void transform_pass(float4* row4, int q4, float m_t,
                            fmaxf(b.x, kYFloor), fmaxf(b.y, kYFloor));
     };
     auto add_all = [&](float4 y) {
-        acc.add<true>(y, one, zero);
+        acc.template add<true>(y, one, zero);
         if (NF > 0) {
             const float2 y01 = make_float2(y.x, y.y);
             const float2 y23 = make_float2(y.z, y.w);
@@ -872,47 +872,50 @@ cluster_kernel(RowTask t, int n, int slice_len) {
         int evals = 1 + (row_code == 0 ? nfan : 0);  // the T = 1 pass and the fan
         float T_row = NAN;
         float beta_out = 0.0f, inv_s = 0.0f;
-        if (row_code == 0) {
-            if (!entropy_above(make_float2(s1[1], s1[2]), 1.0f, cfg.bound_bits)) {
-                T_row = 1.0f;
-                beta_out = 1.0f;
-                inv_s = 1.0f / s1[1];
-            } else {
-                Search st = search_begin(cfg, s1[1], s1[2], s1[3], t.strict != 0);
-                if (!(cfg.t_min < cfg.hi0)) {
-                    // No interval to halve: T = t_min (section 5.4 check).
-                    st.f |= kFinal;
-                    const int J1[kMaxPoints] = {0, 0, 0};
-                    search_round<CLUSTER, 1, false>(st, cfg, J1, row4, s.q4, d, sm, x);
-                    ++evals;
-                } else if (FAN && nfan > 0) {
-                    const float b0 = t.fan_beta0;
-                    const float fbeta[kFanPoints] = {b0, 4.0f * b0, 16.0f * b0};
-                    search_fan(st, cfg, fbeta, Sf, Vf, s1[1], s1[2]);
-                }
-                while (!(st.f & kDone)) {
-                    int J[kMaxPoints] = {0, 0, 0};
-                    const int np = search_plan(st, cfg, J);
-                    evals += np;
-                    const bool w0 = newton_next(st);
-                    if (np == 1 && w0)
-                        search_round<CLUSTER, 1, true>(st, cfg, J, row4, s.q4, d, sm, x);
-                    else if (np == 1)
-                        search_round<CLUSTER, 1, false>(st, cfg, J, row4, s.q4, d, sm, x);
-                    else if (np == 2 && w0)
-                        search_round<CLUSTER, 2, true>(st, cfg, J, row4, s.q4, d, sm, x);
-                    else if (np == 2)
-                        search_round<CLUSTER, 2, false>(st, cfg, J, row4, s.q4, d, sm, x);
-                    else if (np == 3)
-                        search_round<CLUSTER, 3, false>(st, cfg, J, row4, s.q4, d, sm, x);
-                }
-                if (st.f & kOverflow) bits |= kBitOverflow;
-                T_row = search_result_T(st, cfg);
-                beta_out = rcp_approx(T_row);
-                inv_s = 1.0f / st.SA;
-            }
-        } else {
+        const bool searching =
+            row_code == 0 && entropy_above(make_float2(s1[1], s1[2]), 1.0f, cfg.bound_bits);
+        if (row_code != 0) {
             bits = row_code == 2 ? kBitNan : kBitInf;
+        } else if (!searching) {
+            T_row = 1.0f;
+            beta_out = 1.0f;
+            inv_s = 1.0f / s1[1];
+        } else {
+            Search st = search_begin(cfg, s1[1], s1[2], s1[3], t.strict != 0);
+            if (!(cfg.t_min < cfg.hi0)) {
+                // No interval to halve: T = t_min (section 5.4 check).
+                st.f |= kFinal;
+                const int J1[kMaxPoints] = {0, 0, 0};
+                search_round<CLUSTER, 1, false>(st, cfg, J1, row4, s.q4, d, sm, x);
+                ++evals;
+            } else if (FAN && nfan > 0) {
+                const float b0 = t.fan_beta0;
+                const float fbeta[kFanPoints] = {b0, 4.0f * b0, 16.0f * b0};
+                search_fan(st, cfg, fbeta, Sf, Vf, s1[1], s1[2]);
+            }
+            // One round per trip: plan (0 points: the search is over), then
+            // the round's shape, one of five instantiations.
+            while (true) {
+                int J[kMaxPoints] = {0, 0, 0};
+                const int np = (st.f & kDone) ? 0 : search_plan(st, cfg, J);
+                const bool w0 = newton_next(st);
+                if (np == 0) break;
+                evals += np;
+                if (np == 1 && w0)
+                    search_round<CLUSTER, 1, true>(st, cfg, J, row4, s.q4, d, sm, x);
+                else if (np == 1)
+                    search_round<CLUSTER, 1, false>(st, cfg, J, row4, s.q4, d, sm, x);
+                else if (np == 2 && w0)
+                    search_round<CLUSTER, 2, true>(st, cfg, J, row4, s.q4, d, sm, x);
+                else if (np == 2)
+                    search_round<CLUSTER, 2, false>(st, cfg, J, row4, s.q4, d, sm, x);
+                else
+                    search_round<CLUSTER, 3, false>(st, cfg, J, row4, s.q4, d, sm, x);
+            }
+            if (st.f & kOverflow) bits |= kBitOverflow;
+            T_row = search_result_T(st, cfg);
+            beta_out = rcp_approx(T_row);
+            inv_s = 1.0f / st.SA;
         }
         write_out(row4, s, dst, beta_out, d, inv_s, row_code != 0);
         if (rank == 0 && threadIdx.x == 0) {
